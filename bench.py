@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark: one Skiparse attention training step (forward + backward) per GPU.
+
+Workload: group skip, B=2, heads=24, D=128, latent grid 24x22x40 (N=21120
+tokens), sparse_k=4, bf16 q, k, v, dO ~ N(0,1) from fixed seeds (synthetic; no
+dataset). A step is the whole hot path: skiparse_attn_fwd (RoPE, scope gather,
+attention, reverse store) then skiparse_attn_bwd (preprocess, main, post).
+
+Printed JSON line (rank 0):
+  value        TFLOP/s of the whole job, inputs resident in HBM, counted as
+               3.5 * 4*B*heads*N^2*D/k per step per GPU (forward 1x, backward 2.5x);
+  e2e          the same metric with host (pinned) inputs copied in and all
+               outputs copied out inside the timed region;
+  roofline     the dominant kernel (by device time): algorithmic FLOPs per launch
+               over its mean launch time from CUDA events, against the measured
+               bf16 peak;
+  cpu_baseline the float64 CPU oracle on a bounded sample (whole scopes) of the
+               same workload, timed on this host's cores (rank 0, one GPU only);
+  speedup_vs_k1  the same step at sparse_k=1 (dense attention) over this one.
+
+--impl reference times the oracle alone (the reference arm of this method).
+Multi-GPU: one process per GPU (torchrun); every rank runs its own batch
+(weak scaling), the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Skiparse attn fwd/fwd+bwd TFLOP/s and % of GB300 bf16 peak; speedup vs k=1 dense"
+WORKLOADS = {
+    # the timed workload: a training step on the 21,120-token group-skip grid
+    "train": dict(name="skiparse_train_step_group_24x22x40_k4", B=2, heads=24, D=128, T=24, H=22, W=40, k=4, mode=1),
+    # a smaller case of the same kernels for ncu captures (inputs still larger than L2)
+    "ncu_small": dict(name="skiparse_train_step_group_24x22x40_k4_b1h8", B=1, heads=8, D=128, T=24, H=22, W=40, k=4,
+                      mode=1),
+}
+WORKLOAD = WORKLOADS["train"]
+KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0}   # x forward FLOPs, per launch
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def fwd_flops(w, k=None):
+    N = w["T"] * w["H"] * w["W"]
+    return 4.0 * w["B"] * w["heads"] * N * N * w["D"] / (k or w["k"])
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and parts[0].replace("GPU-", "") != self.uuid.replace("GPU-", ""):
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(seconds: float, max_scopes: int = 64):
+    """Oracle forward+backward on whole scopes of the workload until `seconds`
+    pass. Returns (TFLOP/s, scopes done, elapsed)."""
+    import numpy as np
+    from oracle import skiparse_oracle as O
+    from sparse_spatiotemporal_attention_gb300 import synthetic
+    w = WORKLOAD
+    N = w["T"] * w["H"] * w["W"]
+    L = N // w["k"]
+    ins = synthetic.attention_inputs(w["B"], N, w["heads"], w["D"], with_grad=True)
+    done, flops = 0, 0.0
+    t0 = time.perf_counter()
+    order = [(b, h, s) for h in range(w["heads"]) for b in range(w["B"]) for s in range(w["k"])]
+    for b, h, s in order[:max_scopes]:
+        sub = {n: synthetic.bf16_bits_to_f64(ins[n][b:b + 1, :, h:h + 1]) for n in ins}
+        O.skiparse_scope(sub["q"], sub["k"], sub["v"], sub["do"], w["T"], w["H"], w["W"], w["k"], w["mode"], 0, 0, s)
+        done += 1
+        flops += 3.5 * 4.0 * L * L * w["D"]
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return flops / el / 1e12, done, el
+
+
+def run_cpu_baseline(seconds: float):
+    """Runs the oracle sample in a fresh process with every host core given to BLAS."""
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-worker", str(seconds)],
+                       stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d.update({"unit": "TFLOP/s", "cores": cores, "kind": "oracle"})
+    return d
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def traffic_record(kernel_name):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel's
+    source is unchanged since it was taken; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(kernel_name)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "sparse_spatiotemporal_attention_gb300", "csrc", rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_spatiotemporal_attention_gb300 as skp
+    from sparse_spatiotemporal_attention_gb300 import synthetic
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    w = WORKLOAD
+    B, heads, D, T, H, W, k, mode = w["B"], w["heads"], w["D"], w["T"], w["H"], w["W"], w["k"], w["mode"]
+    N = T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True, seeds={"q": 1 + 10 * rank, "k": 2 + 10 * rank,
+                                                                               "v": 3 + 10 * rank, "do": 4 + 10 * rank})
+    pin = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for n, a in ins.items()}
+    d = {n: t.to(dev) for n, t in pin.items()}
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((B, heads, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(d["q"]) for _ in range(3))
+    ws = torch.empty(skp.skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, k, mode), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(kk=k):
+        skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, mode, stream=stream)
+        skp.skiparse_attn_bwd(d["q"], d["k"], d["v"], out, lse, d["do"], dq, dk, dv, ws, T, H, W, kk, mode,
+                              stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, detail = skp.skiparse_device_error()
+    if st != 0:
+        raise RuntimeError(f"device wait gave up during warm-up: code {detail:#x}")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+
+    # ---- timed region: device-resident inputs
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    skp.skiparse_trace_begin()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    kms, kcnt = skp.skiparse_trace_end(4)
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms_step = ms / args.steps
+    flops_step = 3.5 * fwd_flops(w)
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # ---- e2e: host inputs in, all outputs out, every step
+    h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in
+             (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    bi = sum(t.numel() * t.element_size() for t in pin.values())
+    bo = sum(t.numel() * t.element_size() for t in h_out.values())
+    e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        for n in pin:
+            d[n].copy_(pin[n], non_blocking=True)
+        step()
+        for n, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            h_out[n].copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+    e2e = {"value": world * flops_step / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
+           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps}
+
+    # ---- the same step at k=1 (dense attention) for the speedup
+    k1 = None
+    if not args.no_k1:
+        k1_steps = max(2, min(args.steps // 10, 10))
+        step(1)
+        torch.cuda.synchronize()
+        barrier()
+        e0.record(stream)
+        for _ in range(k1_steps):
+            step(1)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms1 = max_over_ranks(e0.elapsed_time(e1)) / k1_steps
+        k1 = {"ms_per_step": ms1, "tflops": world * 3.5 * fwd_flops(w, 1) / (ms1 * 1e-3) / 1e12, "steps": k1_steps,
+              "speedup": ms1 / ms_step}
+    st, detail = skp.skiparse_device_error()
+    if st != 0:
+        raise RuntimeError(f"device wait gave up: code {detail:#x}")
+
+    peaks, src = load_peaks()
+    kernels = {}
+    tot = sum(kms) or 1.0
+    for i in range(4):
+        if kcnt[i]:
+            kernels[skp.KERNEL_NAMES[i]] = {"launches": kcnt[i], "ms_per_launch": kms[i] / kcnt[i],
+                                            "share": kms[i] / tot}
+    dom = max(range(4), key=lambda i: kms[i])
+    dom_ms = kms[dom] / max(1, kcnt[dom])
+    dom_flops = KERNEL_FLOP_FACTOR[dom] * fwd_flops(w)
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    fwd_ms = kms[0] / max(1, kcnt[0])
+    roofline = {"bound": "tensor", "kernel": skp.KERNEL_NAMES[dom], "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic_record(skp.KERNEL_NAMES[dom]),
+                "peak_source": f"{src} bf16 sustained (kernel timed inside a long step loop)",
+                "flops_per_launch": dom_flops}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) bf16 q, k, v, dO (splitmix64 + Box-Muller), no dataset",
+        "config": {"workload": w["name"], "pass": "fwd+bwd", "B": B, "heads": heads, "D": D, "grid": f"{T}x{H}x{W}",
+                   "N": N, "sparse_k": k, "mode": "group", "rope_theta": 10000.0,
+                   "flops_per_step_per_gpu": flops_step,
+                   "l2": "inputs larger than L2 (q, k, v, dO 260 MB each); no flush",
+                   "parallelism": f"replicas x{world}, each rank its own batch"},
+        "pct_of_peak": {"burst": value / world / float(peaks.get("bf16_tflops", 1900.0)),
+                        "sustained": value / world / peak, "source": src},
+        "fwd": {"ms_per_launch": fwd_ms, "tflops": fwd_flops(w) / (fwd_ms * 1e-3) / 1e12},
+        "speedup_vs_k1": (k1 or {}).get("speedup"), "k1": k1,
+        "clocks": clocks, "e2e": e2e, "gpu_launches": int(sum(kcnt)), "kernels": kernels, "roofline": roofline,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = run_cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline"] = cb
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def reference_arm(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOAD
+    N = w["T"] * w["H"] * w["W"]
+    cores = os.cpu_count() or 1
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    times, flops = [], []
+    t_start = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-worker", str(per_step)],
+                           stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env, timeout=900)
+        if r.returncode != 0:
+            print(json.dumps({"impl": "reference", "unavailable": "oracle run failed: " +
+                              (r.stderr.strip().splitlines() or ["?"])[-1]}))
+            return
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        if i >= args.warmup:
+            times.append(d["elapsed_s"])
+            flops.append(d["value"] * 1e12 * d["elapsed_s"])
+    el = sum(times)
+    value = sum(flops) / el / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+            "data": "synthetic: seeded N(0,1) bf16-valued q, k, v, dO, computed in float64",
+            "config": {"workload": w["name"], "pass": "fwd+bwd", "B": w["B"], "heads": w["heads"], "D": w["D"],
+                       "grid": f"{w['T']}x{w['H']}x{w['W']}", "N": N, "sparse_k": w["k"], "mode": "group"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"whole scopes (L={N // w['k']}) forward+backward, about {per_step:.0f} s "
+                                       "of oracle work per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t_start}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-k1", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", default="train", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    global WORKLOAD
+    WORKLOAD = WORKLOADS[args.workload]
+    if args.cpu_oracle_worker is not None:
+        v, n, el = cpu_oracle_sample(args.cpu_oracle_worker)
+        N = WORKLOAD["T"] * WORKLOAD["H"] * WORKLOAD["W"]
+        print(json.dumps({"value": v, "elapsed_s": el, "scopes": n,
+                          "sample": f"{n} whole scopes (L={N // WORKLOAD['k']}, fwd+bwd) of the workload"}))
+        return
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,139 @@
+/*
+ * skiparse.h -- C ABI of a GB300 (sm_103a) library for Skiparse attention.
+ *
+ * Skiparse attention is defined on the "Open-Sora Plan" docs page, section
+ * "Skiparse Attention" (Single Skip and Group Skip implementation listings):
+ * q and k are rotated by 3D RoPE at each token's original (t, h, w) position,
+ * the tokens are rearranged into sparse_k scopes, softmax attention runs inside
+ * every scope, and the result is rearranged back.
+ *   single skip: token i belongs to scope i mod k, at position i div k;
+ *   group skip:  token i belongs to scope (i div k) mod k, at position
+ *                (i div k^2) * k + (i mod k).
+ * No permuted copy is ever made: the rearrange is folded into TMA tensor-map
+ * strides on load and into the output addresses on store.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer owned by the caller, except where a
+ *     comment says otherwise. The library allocates no device memory.
+ *   - Tensors q, k, v, out, dout, dq, dk, dv are bf16, layout (B, N, heads, D),
+ *     contiguous. lse is fp32, layout (B, heads, N), original token order.
+ *   - Tokens are flattened t-major: i = (t * H + h) * W + w, N = T * H * W.
+ *   - 3D RoPE: the D channels of a head are split in order into D/4 channels
+ *     for t, 3D/8 for h and 3D/8 for w; within a chunk of d channels the pair
+ *     (2j, 2j+1) is rotated by angle pos * rope_theta^(-2j/d).
+ *   - Softmax scale is 1/sqrt(D); lse = max + ln(sum exp(scaled scores - max)).
+ *   - All calls are asynchronous on `stream` and return a skiparse_status_t.
+ *     Validation happens on the host before anything is launched; a call that
+ *     fails validation writes nothing. Inputs may alias one another; outputs
+ *     must not overlap any input or each other.
+ *   - B, heads or N equal to 0 is a valid empty call: nothing is launched and
+ *     the pointers may be NULL.
+ *   - Kernel-side waits are bounded; a wait that runs out records a code in a
+ *     device error word that skiparse_device_error() returns.
+ */
+#ifndef SKIPARSE_H_
+#define SKIPARSE_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SKIPARSE_SINGLE = 0, SKIPARSE_GROUP = 1 } skiparse_mode_t;
+
+typedef enum {
+  SKIPARSE_OK = 0,
+  SKIPARSE_ERR_INVALID_ARG = -1,    /* NULL pointer, negative size, bad mode or theta */
+  SKIPARSE_ERR_SHAPE = -2,          /* N != T*H*W, N % k (single) or N % k^2 (group) */
+  SKIPARSE_ERR_UNSUPPORTED = -3,    /* D not 64/128, group k not dividing 128, RoPE table too large */
+  SKIPARSE_ERR_ALIGNMENT = -4,      /* a pointer not 16-byte aligned */
+  SKIPARSE_ERR_DEVICE = -5,         /* no device, or the current device is not sm_103 */
+  SKIPARSE_ERR_WORKSPACE = -6,      /* workspace NULL or smaller than the query says */
+  SKIPARSE_ERR_LAUNCH = -7,         /* tensor-map encode or kernel launch failed */
+  SKIPARSE_ERR_DEVICE_TIMEOUT = -8, /* a kernel gave up on a bounded wait */
+  SKIPARSE_ERR_ALIAS = -9           /* an output overlaps an input or another output */
+} skiparse_status_t;
+
+/*
+ * Forward pass. Page: "Open-Sora Plan" docs, "Skiparse Attention", both
+ * implementation listings (RoPE, rearrange, scaled_dot_product_attention,
+ * reverse rearrange), fused into one persistent kernel.
+ *   q, k, v   in : bf16 (B, N, heads, D), the PRE-RoPE projections.
+ *   out       out: bf16 (B, N, heads, D), fully overwritten.
+ *   lse       out: fp32 (B, heads, N), natural-log LSE of each query row.
+ *   D in {64, 128}; sparse_k >= 1; mode is a skiparse_mode_t; rope_theta > 0.
+ *   Group mode needs sparse_k to divide 128.
+ */
+int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      int B, int heads, int N, int D, int T, int H, int W,
+                      int sparse_k, int mode, float rope_theta, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace skiparse_attn_bwd needs for these sizes: an fp32
+ * dQ accumulator, rotated bf16 copies of q and k, per-scope fp32 LSE and
+ * delta rows, and the RoPE cos/sin table. Returns 0 for empty or invalid sizes.
+ */
+size_t skiparse_attn_bwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
+                                         int sparse_k, int mode);
+
+/*
+ * Backward pass: gradients of <dout, out> w.r.t. the pre-RoPE q, k and v.
+ * Implied by the section's purpose (the method accelerates training); the
+ * pages print no backward code. P is recomputed from lse.
+ *   q, k, v, out, dout in : bf16 (B, N, heads, D); out is the forward output.
+ *   lse                in : fp32 (B, heads, N), as written by skiparse_attn_fwd.
+ *   dq, dk, dv         out: bf16 (B, N, heads, D), fully overwritten.
+ *   workspace          scratch: device memory of at least
+ *                      skiparse_attn_bwd_workspace_bytes(...) bytes, 256-byte
+ *                      aligned, owned by the caller, contents ignored on entry
+ *                      and undefined on return. Must not overlap any tensor.
+ */
+int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv,
+                      void* workspace, size_t workspace_bytes,
+                      int B, int heads, int N, int D, int T, int H, int W,
+                      int sparse_k, int mode, float rope_theta, cudaStream_t stream);
+
+/*
+ * Test hook: the token -> (scope, position) map exactly as the kernels address
+ * it (the listings' rearrange patterns). Writes int32 scope_of_token[N] and
+ * pos_of_token[N].
+ */
+int skiparse_debug_index_map(int* scope_of_token, int* pos_of_token, int N, int sparse_k, int mode,
+                             cudaStream_t stream);
+
+/*
+ * Test hook: 3D RoPE of x (bf16, (B, N, heads, D)) computed by the same device
+ * table and rotation the kernels use, written unrounded as fp32 to x_rot.
+ */
+int skiparse_debug_rope(const void* x, float* x_rot, int B, int heads, int N, int D,
+                        int T, int H, int W, float rope_theta, cudaStream_t stream);
+
+/* Static, human-readable text for a status code. */
+const char* skiparse_status_string(int status);
+
+/*
+ * Reads and clears the device error word of the current device (synchronises
+ * the device). Returns SKIPARSE_OK when no kernel gave up a wait, else
+ * SKIPARSE_ERR_DEVICE_TIMEOUT with the kernel's code in *detail (may be NULL).
+ */
+int skiparse_device_error(int* detail);
+
+/*
+ * Tracing. Between skiparse_trace_begin() and skiparse_trace_end() every kernel
+ * launch is bracketed by CUDA events on its stream. skiparse_trace_end()
+ * synchronises on them and writes, per kernel id, the summed device time in ms
+ * and the launch count (arrays of n entries, host memory). Kernel ids:
+ * 0 forward, 1 backward preprocess, 2 backward main, 3 backward post.
+ */
+int skiparse_trace_begin(void);
+int skiparse_trace_end(float* ms_per_kernel, int* launches_per_kernel, int n);
+const char* skiparse_kernel_name(int id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKIPARSE_H_ */

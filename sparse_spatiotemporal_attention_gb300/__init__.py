@@ -1,0 +1,163 @@
+"""GB300-native Skiparse attention (Open-Sora Plan), Python binding.
+
+The library is `_lib/libskiparse.so`, a C ABI declared in include/skiparse.h
+and built for sm_103a by `_build.build()`. This module only marshals arguments
+(torch tensors -> device pointers, sizes, the current stream) and turns status
+codes into exceptions: every step of the attention runs in the library's CUDA
+kernels. If the library is missing, every call raises; there is no fallback.
+
+Tensor layouts: q, k, v, out, dout, dq, dk, dv are bf16 (B, N, heads, D)
+contiguous on the GPU; lse is fp32 (B, heads, N).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+SINGLE = 0
+GROUP = 1
+KERNEL_NAMES = ("skiparse_fwd_kernel", "skiparse_bwd_pre_kernel", "skiparse_bwd_main_kernel",
+                "skiparse_bwd_post_kernel")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libskiparse.so")
+
+EXPORTS = (
+    "skiparse_attn_fwd", "skiparse_attn_bwd_workspace_bytes", "skiparse_attn_bwd",
+    "skiparse_debug_index_map", "skiparse_debug_rope", "skiparse_status_string",
+    "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
+)
+
+
+class SkiparseError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+_lib = None
+
+_c_int, _c_size, _c_float, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libskiparse.so once. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libskiparse.so not found at {path}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "skiparse_attn_fwd": (_c_int, [_vp] * 5 + [_c_int] * 9 + [_c_float, _vp]),
+        "skiparse_attn_bwd_workspace_bytes": (_c_size, [_c_int] * 9),
+        "skiparse_attn_bwd": (_c_int, [_vp] * 10 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
+        "skiparse_debug_index_map": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp]),
+        "skiparse_debug_rope": (_c_int, [_vp, _vp] + [_c_int] * 7 + [_c_float, _vp]),
+        "skiparse_status_string": (ctypes.c_char_p, [_c_int]),
+        "skiparse_device_error": (_c_int, [ctypes.POINTER(_c_int)]),
+        "skiparse_trace_begin": (_c_int, []),
+        "skiparse_trace_end": (_c_int, [ctypes.POINTER(_c_float), ctypes.POINTER(_c_int), _c_int]),
+        "skiparse_kernel_name": (ctypes.c_char_p, [_c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().skiparse_status_string(int(status)).decode()
+
+
+skiparse_status_string = status_string
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise SkiparseError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _shape(q):
+    B, N, heads, D = q.shape
+    return int(B), int(heads), int(N), int(D)
+
+
+def skiparse_attn_fwd(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=10000.0, stream=None):
+    """Forward pass into caller-allocated out (bf16, like q) and lse (fp32 (B, heads, N))."""
+    B, heads, N, D = _shape(q)
+    st = load_library().skiparse_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                          B, heads, N, D, T, H, W, sparse_k, mode,
+                                          float(rope_theta), _stream(stream))
+    _check(st, "skiparse_attn_fwd")
+
+
+def skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode) -> int:
+    return int(load_library().skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode))
+
+
+def skiparse_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace, T, H, W, sparse_k, mode,
+                      rope_theta=10000.0, stream=None, workspace_bytes=None):
+    """Backward pass into caller-allocated dq, dk, dv; `workspace` is a device
+    buffer of at least skiparse_attn_bwd_workspace_bytes(...) bytes."""
+    B, heads, N, D = _shape(q)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = load_library().skiparse_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                          _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes),
+                                          B, heads, N, D, T, H, W, sparse_k, mode,
+                                          float(rope_theta), _stream(stream))
+    _check(st, "skiparse_attn_bwd")
+
+
+def skiparse_debug_index_map(scope_of_token, pos_of_token, N, sparse_k, mode, stream=None):
+    st = load_library().skiparse_debug_index_map(_ptr(scope_of_token), _ptr(pos_of_token), N, sparse_k, mode,
+                                                 _stream(stream))
+    _check(st, "skiparse_debug_index_map")
+
+
+def skiparse_debug_rope(x, x_rot, T, H, W, rope_theta=10000.0, stream=None):
+    B, heads, N, D = _shape(x)
+    st = load_library().skiparse_debug_rope(_ptr(x), _ptr(x_rot), B, heads, N, D, T, H, W,
+                                            float(rope_theta), _stream(stream))
+    _check(st, "skiparse_debug_rope")
+
+
+def skiparse_device_error():
+    """(status, detail): reads and clears the device error word (synchronises)."""
+    d = _c_int(0)
+    st = load_library().skiparse_device_error(ctypes.byref(d))
+    return int(st), int(d.value)
+
+
+def skiparse_trace_begin():
+    _check(load_library().skiparse_trace_begin(), "skiparse_trace_begin")
+
+
+def skiparse_trace_end(n: int = 4):
+    """Returns ([ms per kernel id], [launches per kernel id])."""
+    ms = (_c_float * n)()
+    cnt = (_c_int * n)()
+    _check(load_library().skiparse_trace_end(ms, cnt, n), "skiparse_trace_end")
+    return [float(x) for x in ms], [int(x) for x in cnt]

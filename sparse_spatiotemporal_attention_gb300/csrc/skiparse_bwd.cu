@@ -1,0 +1,496 @@
+// Skiparse attention backward: preprocess, main and post kernels.
+//
+// The pages print no backward; it is implied by the method's purpose (it
+// accelerates training, "Open-Sora Plan" docs, "Skiparse Attention"). The
+// gradient is that of softmax attention inside every scope, followed by the
+// transpose of the RoPE rotation for q and k (RoPE came first in the forward).
+//
+//  preprocess  per token row: delta = rowsum(dO * O) and lse * log2(e) in
+//              scope order, rotated bf16 copies of q and k (so the main loop
+//              reloads no RoPE), dQ accumulator zeroed, cos/sin table written.
+//  main        one work unit = (b, head, scope, 128-row K/V tile); loops over
+//              the scope's Q tiles with five tcgen05 MMAs per tile pair:
+//                S^T  = K~ Q~^T          dP^T = V dO^T
+//                dV  += P^T dO           dK~ += dS^T Q~          dQ~_part = dS K~
+//              P^T = exp(S^T * scale - lse), dS^T = P^T * (dP^T - delta).
+//              dQ~_part is added into the fp32 accumulator with vector atomics.
+//              Epilogue: dv, and dk = scale * R^T dK~, stored at original rows.
+//  post        dq = R^T (scale * dQ~_acc) -> bf16.
+// Warp roles of the main kernel:
+//   warps 0-3  one key row per thread: P^T, dS^T, and the dK / dV epilogue;
+//   warps 4-7  one query row per thread: dQ~ partial -> fp32 atomics;
+//   warp  8    TMA producer (K~, V per unit; Q~, dO, lse, delta per Q tile);
+//   warp  9    MMA issuer.
+// TMEM columns: S^T (P^T as bf16) 0..127, dP^T / dQ~ partial 128..255,
+// dV 256..383, dK~ 384..511.
+#include "skiparse_internal.h"
+
+namespace skp {
+
+// ===========================================================================
+// preprocess and post: one warp per (b, token, head) row
+// ===========================================================================
+
+constexpr int kRowThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ float2 tab[];
+  const Geom& g = p.g;
+  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < p.rope.entries; e += blockDim.x) p.rope_tab[e] = tab[e];
+  constexpr int PPL = D / 64;               // channel pairs per lane
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  PairSel sel[PPL];
+#pragma unroll
+  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
+  const long long rows = (long long)g.B * g.N * g.heads;
+  for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb) {
+    const int head = (int)(row % g.heads);
+    const long long bi = row / g.heads;
+    const int i = (int)(bi % g.N);
+    const int b = (int)(bi / g.N);
+    int t, hh, w;
+    token_coords(p.rope, i, t, hh, w);
+    const size_t base = (size_t)row * D + lane * 2 * PPL;
+    float dsum = 0.f;
+    uint32_t qv[PPL], kv[PPL], ov[PPL], dv[PPL];
+    if (PPL == 2) {
+      const uint2 a = *reinterpret_cast<const uint2*>(p.q + base);
+      const uint2 bb = *reinterpret_cast<const uint2*>(p.k + base);
+      const uint2 c = *reinterpret_cast<const uint2*>(p.out + base);
+      const uint2 d = *reinterpret_cast<const uint2*>(p.dout + base);
+      qv[0] = a.x; qv[PPL - 1] = a.y; kv[0] = bb.x; kv[PPL - 1] = bb.y;
+      ov[0] = c.x; ov[PPL - 1] = c.y; dv[0] = d.x; dv[PPL - 1] = d.y;
+    } else {
+      qv[0] = *reinterpret_cast<const uint32_t*>(p.q + base);
+      kv[0] = *reinterpret_cast<const uint32_t*>(p.k + base);
+      ov[0] = *reinterpret_cast<const uint32_t*>(p.out + base);
+      dv[0] = *reinterpret_cast<const uint32_t*>(p.dout + base);
+    }
+    uint32_t qo[PPL], ko[PPL];
+#pragma unroll
+    for (int e = 0; e < PPL; ++e) {
+      dsum = fmaf(bf16lo(ov[e]), bf16lo(dv[e]), dsum);
+      dsum = fmaf(bf16hi(ov[e]), bf16hi(dv[e]), dsum);
+      const float2 cs = tab[pair_index(sel[e], t, hh, w)];
+      const float2 a = rope_rotate(bf16lo(qv[e]), bf16hi(qv[e]), cs);
+      const float2 c = rope_rotate(bf16lo(kv[e]), bf16hi(kv[e]), cs);
+      qo[e] = pack_bf16(a.x, a.y);
+      ko[e] = pack_bf16(c.x, c.y);
+    }
+    if (PPL == 2) {
+      *reinterpret_cast<uint2*>(p.qr + base) = make_uint2(qo[0], qo[PPL - 1]);
+      *reinterpret_cast<uint2*>(p.kr + base) = make_uint2(ko[0], ko[PPL - 1]);
+      *reinterpret_cast<float4*>(p.dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      *reinterpret_cast<uint32_t*>(p.qr + base) = qo[0];
+      *reinterpret_cast<uint32_t*>(p.kr + base) = ko[0];
+      *reinterpret_cast<float2*>(p.dq_acc + base) = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+    if (lane == 0) {
+      int s, pp;
+      scope_pos_of(g, i, s, pp);
+      const size_t idx = (((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp;
+      p.delta_s[idx] = dsum;
+      p.lse2s[idx] = p.lse[((size_t)b * g.heads + head) * g.N + i] * 1.4426950408889634f;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __grid_constant__ BwdParams p) {
+  const Geom& g = p.g;
+  constexpr int PPL = D / 64;
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  PairSel sel[PPL];
+#pragma unroll
+  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
+  const long long rows = (long long)g.B * g.N * g.heads;
+  for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb) {
+    const int i = (int)((row / g.heads) % g.N);
+    int t, hh, w;
+    token_coords(p.rope, i, t, hh, w);
+    const size_t base = (size_t)row * D + lane * 2 * PPL;
+    float x[2 * PPL];
+    if (PPL == 2) {
+      const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + base);
+      x[0] = a.x; x[1] = a.y; x[2 * PPL - 2] = a.z; x[2 * PPL - 1] = a.w;
+    } else {
+      const float2 a = *reinterpret_cast<const float2*>(p.dq_acc + base);
+      x[0] = a.x; x[1] = a.y;
+    }
+    uint32_t o[PPL];
+#pragma unroll
+    for (int e = 0; e < PPL; ++e) {
+      const float2 cs = __ldg(&p.rope_tab[pair_index(sel[e], t, hh, w)]);
+      const float2 r = rope_rotate_t(x[2 * e] * p.scale, x[2 * e + 1] * p.scale, cs);
+      o[e] = pack_bf16(r.x, r.y);
+    }
+    if (PPL == 2) *reinterpret_cast<uint2*>(p.dq + base) = make_uint2(o[0], o[PPL - 1]);
+    else *reinterpret_cast<uint32_t*>(p.dq + base) = o[0];
+  }
+}
+
+// ===========================================================================
+// main kernel
+// ===========================================================================
+
+template <int D>
+struct BwdLayout {
+  static constexpr int HALVES = D / 64;
+  static constexpr int TILE = 128 * D * 2;
+  static constexpr int DS_BYTES = 128 * 128 * 2;
+  static constexpr int STATS_OFF = 1024;                 // [2 stages][lse2 | delta][128] fp32
+  static constexpr int K_OFF = 3072;
+  static constexpr int V_OFF = K_OFF + TILE;
+  static constexpr int Q_OFF = V_OFF + TILE;            // 2 stages
+  static constexpr int DO_OFF = Q_OFF + 2 * TILE;       // 2 stages
+  static constexpr int DS_OFF = DO_OFF + 2 * TILE;
+  static constexpr int BYTES = DS_OFF + DS_BYTES;
+};
+
+enum BwdBar {
+  B_KVFULL, B_KVEMPTY, B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1, B_SFULL, B_DSREADY, B_DSFREE,
+  B_DQFULL, B_DQFREE, B_DKVDONE, B_DKVFREE, B_FINAL, B_NBARS
+};
+
+constexpr int kBwdThreads = 320;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+
+__device__ __forceinline__ void decode_unit_bwd(const Geom& g, int u, int& b, int& head, int& s, int& tile) {
+  tile = u % g.n_tiles;
+  int r = u / g.n_tiles;
+  s = r % g.k;
+  r /= g.k;
+  head = r % g.heads;
+  b = r / g.heads;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const __grid_constant__ BwdParams p) {
+  using Ly = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
+  int* abort_flag = reinterpret_cast<int*>(smem + 520);
+  float* stats = reinterpret_cast<float*>(smem + Ly::STATS_OFF);
+  const uint32_t sK = smem_u32(smem + Ly::K_OFF);
+  const uint32_t sV = smem_u32(smem + Ly::V_OFF);
+  const uint32_t sQ = smem_u32(smem + Ly::Q_OFF);
+  const uint32_t sDO = smem_u32(smem + Ly::DO_OFF);
+  const uint32_t sDS = smem_u32(smem + Ly::DS_OFF);
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  const Ctl ctl{abort_flag, p.err};
+  const Geom& g = p.g;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    const uint32_t counts[B_NBARS] = {1, 1, 1, 1, 1, 1, 1, 4, 1, 1, 4, 1, 4, 1};
+    for (int i = 0; i < B_NBARS; ++i) mbar_init(bar(i), counts[i]);
+    mbar_fence_init();
+  }
+  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&p.tm_q);
+      tma_prefetch_map(&p.tm_k);
+      tma_prefetch_map(&p.tm_v);
+      tma_prefetch_map(&p.tm_do);
+      uint32_t kv_issued = 0, q_issued[2] = {0, 0};
+      uint32_t g0 = 0;
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+        int b, head, s, kt;
+        decode_unit_bwd(g, u, b, head, s, kt);
+        if (it > 0 && !mbar_wait(bar(B_KVEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_BWD + B_KVEMPTY)) break;
+        mbar_expect_tx(bar(B_KVFULL), 2 * Ly::TILE);
+        const int krow = b * g.Nn + (kt * kTile) / g.G;
+#pragma unroll
+        for (int h = 0; h < Ly::HALVES; ++h) {
+          tma_load_5d(sK + h * kHalfBytes, &p.tm_k, bar(B_KVFULL), h * 64, head, 0, s, krow);
+          tma_load_5d(sV + h * kHalfBytes, &p.tm_v, bar(B_KVFULL), h * 64, head, 0, s, krow);
+        }
+        ++kv_issued;
+        const size_t srow = (((size_t)b * g.heads + head) * g.k + s) * p.Lp;
+        for (int i = 0; i < g.n_tiles; ++i) {
+          const uint32_t gg = g0 + i;
+          const int st = gg & 1;
+          const uint32_t n = gg >> 1;
+          if (n > 0 && !mbar_wait(bar(B_QEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_BWD + B_QEMPTY0 + st)) { ok = false; break; }
+          mbar_expect_tx(bar(B_QFULL0 + st), 2 * Ly::TILE + 1024);
+          const int qrow = b * g.Nn + (i * kTile) / g.G;
+#pragma unroll
+          for (int h = 0; h < Ly::HALVES; ++h) {
+            tma_load_5d(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(B_QFULL0 + st), h * 64, head, 0, s, qrow);
+            tma_load_5d(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(B_QFULL0 + st), h * 64, head, 0, s, qrow);
+          }
+          const uint32_t dst = smem_u32(stats + st * 256);
+          bulk_load(dst, p.lse2s + srow + i * kTile, 512, bar(B_QFULL0 + st));
+          bulk_load(dst + 512, p.delta_s + srow + i * kTile, 512, bar(B_QFULL0 + st));
+          ++q_issued[st];
+        }
+        g0 += g.n_tiles;
+      }
+      if (kv_issued) mbar_drain(bar(B_KVFULL), (kv_issued - 1) & 1);
+      for (int st = 0; st < 2; ++st)
+        if (q_issued[st]) mbar_drain(bar(B_QFULL0 + st), (q_issued[st] - 1) & 1);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO (MN-major)
+      constexpr uint32_t kIdDK = idesc_bf16(128, D, false, true);     // dS^T (K-major) x Q~ (MN-major)
+      constexpr uint32_t kIdDQ = idesc_bf16(128, D, true, true);      // dS (MN-major) x K~ (MN-major)
+      uint32_t g0 = 0;
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+        if (!mbar_wait(bar(B_KVFULL), it & 1, ctl, ERR_KERNEL_BWD + B_KVFULL)) break;
+        if (it > 0 && !mbar_wait(bar(B_DKVFREE), (it - 1) & 1, ctl, ERR_KERNEL_BWD + B_DKVFREE)) break;
+        tc_fence_after();
+        for (int i = 0; i < g.n_tiles; ++i) {
+          const uint32_t gg = g0 + i;
+          const int st = gg & 1;
+          const uint32_t n = gg >> 1;
+          if (!mbar_wait(bar(B_QFULL0 + st), n & 1, ctl, ERR_KERNEL_BWD + B_QFULL0 + st)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qt = sQ + st * Ly::TILE;
+          const uint32_t dot = sDO + st * Ly::TILE;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tmem + kColS, desc_kmajor(sK, ks), desc_kmajor(qt, ks), kIdS, ks > 0 ? 1u : 0u);
+          if (gg > 0 && !mbar_wait(bar(B_DQFREE), (gg - 1) & 1, ctl, ERR_KERNEL_BWD + B_DQFREE)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tmem + kColDP, desc_kmajor(sV, ks), desc_kmajor(dot, ks), kIdS, ks > 0 ? 1u : 0u);
+          tc_commit(bar(B_SFULL));
+          if (!mbar_wait(bar(B_DSREADY), gg & 1, ctl, ERR_KERNEL_BWD + B_DSREADY)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + kColDV, tmem + kColS + ks * 8, desc_mnmajor(dot, ks), kIdDV, (i > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss(tmem + kColDK, desc_kmajor(sDS, ks), desc_mnmajor(qt, ks), kIdDK, (i > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss(tmem + kColDP, desc_mnmajor(sDS, ks), desc_mnmajor(sK, ks), kIdDQ, ks > 0 ? 1u : 0u);
+          tc_commit(bar(B_DQFULL));
+          tc_commit(bar(B_QEMPTY0 + st));
+          tc_commit(bar(B_DSFREE));
+        }
+        if (!ok) break;
+        tc_commit(bar(B_DKVDONE));
+        tc_commit(bar(B_KVEMPTY));
+        g0 += g.n_tiles;
+      }
+      tc_commit(bar(B_FINAL));
+      mbar_drain(bar(B_FINAL), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ dQ warps
+    const int qi = tid - 128;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    uint32_t g0 = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      int b, head, s, kt;
+      decode_unit_bwd(g, u, b, head, s, kt);
+      for (int i = 0; i < g.n_tiles; ++i) {
+        const uint32_t gg = g0 + i;
+        if (!mbar_wait(bar(B_DQFULL), gg & 1, ctl, ERR_KERNEL_BWD + B_DQFULL)) { ok = false; break; }
+        tc_fence_after();
+        const int prow = i * kTile + qi;
+        const bool row_ok = prow < g.L;
+        const int tok = row_ok ? token_of(g, s, prow) : 0;
+        float* dst = p.dq_acc + (((size_t)b * g.N + tok) * g.heads + head) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float x[32];
+          tmem_ld32(tmem + lane_base + kColDP + c * 32, x);
+          if (row_ok) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + q4 * 4),
+                        make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DQFREE));
+      }
+      g0 += g.n_tiles;
+    }
+  } else {
+    // ------------------------------------------------------------ P^T / dS^T warps
+    const int j = tid;                                       // key row of the K/V tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint8_t* ds_row = smem + Ly::DS_OFF + j * 128;
+    uint32_t g0 = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      int b, head, s, kt;
+      decode_unit_bwd(g, u, b, head, s, kt);
+      const bool key_ok = kt * kTile + j < g.L;
+      for (int i = 0; i < g.n_tiles; ++i) {
+        const uint32_t gg = g0 + i;
+        const int st = gg & 1;
+        if (!mbar_wait(bar(B_SFULL), gg & 1, ctl, ERR_KERNEL_BWD + B_SFULL)) { ok = false; break; }
+        if (gg > 0 && !mbar_wait(bar(B_DSFREE), (gg - 1) & 1, ctl, ERR_KERNEL_BWD + B_DSFREE)) { ok = false; break; }
+        tc_fence_after();
+        const float* lse2 = stats + st * 256;
+        const float* delta = lse2 + 128;
+        const int qvalid = key_ok ? min(kTile, g.L - i * kTile) : 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float sv[32], dp[32];
+          tmem_ld32(tmem + lane_base + kColS + c * 32, sv);
+          tmem_ld32(tmem + lane_base + kColDP + c * 32, dp);
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int q0 = c * 32 + 2 * e;
+            const float p0 = q0 < qvalid ? ex2(fmaf(sv[2 * e], sl2, -lse2[q0])) : 0.f;
+            const float p1 = q0 + 1 < qvalid ? ex2(fmaf(sv[2 * e + 1], sl2, -lse2[q0 + 1])) : 0.f;
+            const float d0 = q0 < qvalid ? p0 * (dp[2 * e] - delta[q0]) : 0.f;
+            const float d1 = q0 + 1 < qvalid ? p1 * (dp[2 * e + 1] - delta[q0 + 1]) : 0.f;
+            pk[e] = pack_bf16(p0, p1);
+            dk[e] = pack_bf16(d0, d1);
+          }
+          tmem_st16(tmem + lane_base + kColS + c * 16, pk);
+          // dS^T row j, query columns 32c .. 32c+31: box c/2, 16-byte chunks (c%2)*4 ..
+          uint8_t* rowp = ds_row + (c >> 1) * kHalfBytes;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int chunk = ((c & 1) * 4 + q4) ^ (j & 7);
+            *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2], dk[4 * q4 + 3]);
+          }
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DSREADY));
+      }
+      if (!ok) break;
+      // ---- epilogue: dv and dk = scale * R^T dK~ at the key's original row
+      if (!mbar_wait(bar(B_DKVDONE), it & 1, ctl, ERR_KERNEL_BWD + B_DKVDONE)) break;
+      tc_fence_after();
+      const int prow = kt * kTile + j;
+      const int tok = key_ok ? token_of(g, s, prow) : 0;
+      int t = 0, hh = 0, w = 0;
+      if (key_ok) token_coords(p.rope, tok, t, hh, w);
+      const size_t rbase = (((size_t)b * g.N + tok) * g.heads + head) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float x[32];
+        tmem_ld32(tmem + lane_base + kColDV + c * 32, x);
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_uint4(pack_bf16(x[8 * q4], x[8 * q4 + 1]), pack_bf16(x[8 * q4 + 2], x[8 * q4 + 3]),
+                                 pack_bf16(x[8 * q4 + 4], x[8 * q4 + 5]), pack_bf16(x[8 * q4 + 6], x[8 * q4 + 7]));
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float x[32];
+        tmem_ld32(tmem + lane_base + kColDK + c * 32, x);
+        if (key_ok) {
+          uint32_t o[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const PairSel sl = pair_select(p.rope, c * 16 + e);
+            const float2 cs = __ldg(&p.rope_tab[pair_index(sl, t, hh, w)]);
+            const float2 r = rope_rotate_t(x[2 * e] * p.scale, x[2 * e + 1] * p.scale, cs);
+            o[e] = pack_bf16(r.x, r.y);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DKVFREE));
+      g0 += g.n_tiles;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+size_t bwd_main_smem_bytes(int D) {
+  return D == 128 ? (size_t)BwdLayout<128>::BYTES : (size_t)BwdLayout<64>::BYTES;
+}
+
+cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = (size_t)p.rope.entries * sizeof(float2);
+  cudaError_t e;
+  if (p.g.D == 128) {
+    e = cudaFuncSetAttribute(skiparse_bwd_pre_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_bwd_pre_kernel<128><<<grid, kRowThreads, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(skiparse_bwd_pre_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_bwd_pre_kernel<64><<<grid, kRowThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = bwd_main_smem_bytes(p.g.D);
+  cudaError_t e;
+  if (p.g.D == 128) {
+    e = cudaFuncSetAttribute(skiparse_bwd_main_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_bwd_main_kernel<128><<<grid, kBwdThreads, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(skiparse_bwd_main_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_bwd_main_kernel<64><<<grid, kBwdThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const BwdParams& p, int grid, cudaStream_t stream) {
+  if (p.g.D == 128) skiparse_bwd_post_kernel<128><<<grid, kRowThreads, 0, stream>>>(p);
+  else skiparse_bwd_post_kernel<64><<<grid, kRowThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace skp

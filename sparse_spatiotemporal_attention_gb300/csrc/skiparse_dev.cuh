@@ -1,0 +1,369 @@
+// Device building blocks for the Skiparse attention kernels (sm_103a).
+//
+//  * scope geometry: the token <-> (scope, position) maps of the "Open-Sora
+//    Plan" docs page, section "Skiparse Attention" (single and group skip
+//    rearrange patterns), written with a group size G: G = 1 for single skip,
+//    G = k for group skip. A scope position p holds token
+//        i = (p div G) * k * G + s * G + (p mod G),
+//    which is i = p*k + s for single skip and i = (p div k)*k^2 + s*k + p mod k
+//    for group skip.
+//  * 3D RoPE cos/sin table and pair rotation;
+//  * thin inline-PTX wrappers: mbarrier, TMA (cp.async.bulk), tcgen05
+//    (alloc, mma, commit, ld, st, fences) and the shared-memory / instruction
+//    descriptors of tcgen05.mma kind::f16.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+namespace skp {
+
+constexpr int kTile = 128;                  // rows of every Q / K / V tile
+constexpr int kHalfBytes = 128 * 128;       // one 128-row x 64-channel bf16 box (128B swizzle)
+constexpr int kMaxRopeEntries = 8192;       // cos/sin pairs of the RoPE table
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s per bounded wait
+
+// ---------------------------------------------------------------------------
+// Geometry and RoPE parameters (plain structs, passed inside kernel params)
+// ---------------------------------------------------------------------------
+
+struct Geom {
+  int B, heads, N, D;
+  int k;        // sparse_k: number of scopes
+  int G;        // group size: 1 (single skip) or k (group skip)
+  int L;        // scope length N / k
+  int Nn;       // L / G: rows of the merged (n, b) tensor-map dimension per batch
+  int n_tiles;  // ceil(L / 128)
+};
+
+struct RopeParams {
+  double om_t[16];    // rope_theta^(-2j/dt) for the t chunk (dt = D/4 channels, D/8 pairs)
+  double om_hw[24];   // rope_theta^(-2j/dh) for the h and w chunks (3D/8 channels each)
+  int T, H, W;
+  int dt2, dh2;       // pairs per chunk: D/8 and 3D/16
+  int entries;        // T*dt2 + H*dh2 + W*dh2
+};
+
+__device__ __forceinline__ int token_of(const Geom& g, int s, int p) {
+  return (p / g.G) * (g.k * g.G) + s * g.G + (p % g.G);
+}
+
+__device__ __forceinline__ void scope_pos_of(const Geom& g, int i, int& s, int& p) {
+  s = (i / g.G) % g.k;
+  p = (i / (g.k * g.G)) * g.G + (i % g.G);
+}
+
+__device__ __forceinline__ void token_coords(const RopeParams& r, int i, int& t, int& h, int& w) {
+  const int hw = r.H * r.W;
+  t = i / hw;
+  const int rem = i - t * hw;
+  h = rem / r.W;
+  w = rem - h * r.W;
+}
+
+// Table entry e holds (cos, sin) of pos * omega for one axis, position and pair.
+// Angles are reduced modulo 2*pi in double before the float sincos, so large
+// positions lose no accuracy.
+__device__ __forceinline__ void rope_build_table(float2* tab, const RopeParams& r, int tid, int nthreads) {
+  const int nt = r.T * r.dt2, nh = r.H * r.dh2;
+  for (int e = tid; e < r.entries; e += nthreads) {
+    int pos, j;
+    double om;
+    if (e < nt) {
+      pos = e / r.dt2; j = e - pos * r.dt2; om = r.om_t[j];
+    } else if (e < nt + nh) {
+      const int e2 = e - nt; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j];
+    } else {
+      const int e2 = e - nt - nh; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j];
+    }
+    const double a = (double)pos * om;
+    const double n = rint(a * 0.15915494309189535);          // a / (2 pi)
+    double red = fma(-n, 6.283185307179586, a);               // 2 pi, high part
+    red = fma(-n, 2.4492935982947064e-16, red);               // 2 pi, low part
+    float sn, cs;
+    sincosf((float)red, &sn, &cs);
+    tab[e] = make_float2(cs, sn);
+  }
+}
+
+// Which table slice a channel pair pp (0 .. D/2-1) reads from.
+struct PairSel { int base, stride, local, axis; };
+
+__device__ __forceinline__ PairSel pair_select(const RopeParams& r, int pp) {
+  PairSel s;
+  if (pp < r.dt2) { s.base = 0; s.stride = r.dt2; s.local = pp; s.axis = 0; }
+  else if (pp < r.dt2 + r.dh2) { s.base = r.T * r.dt2; s.stride = r.dh2; s.local = pp - r.dt2; s.axis = 1; }
+  else { s.base = r.T * r.dt2 + r.H * r.dh2; s.stride = r.dh2; s.local = pp - r.dt2 - r.dh2; s.axis = 2; }
+  return s;
+}
+
+__device__ __forceinline__ int pair_index(const PairSel& s, int t, int h, int w) {
+  const int pos = s.axis == 0 ? t : (s.axis == 1 ? h : w);
+  return s.base + pos * s.stride + s.local;
+}
+
+// (x, y) -> (x cos - y sin, x sin + y cos)
+__device__ __forceinline__ float2 rope_rotate(float x, float y, float2 cs) {
+  return make_float2(fmaf(x, cs.x, -(y * cs.y)), fmaf(x, cs.y, y * cs.x));
+}
+
+// transpose rotation, used for gradients: (x, y) -> (x cos + y sin, -x sin + y cos)
+__device__ __forceinline__ float2 rope_rotate_t(float x, float y, float2 cs) {
+  return make_float2(fmaf(x, cs.x, y * cs.y), fmaf(y, cs.x, -(x * cs.y)));
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of the 4-byte word `w` (0..31) of row `r` inside a 128-row box
+// written by TMA with 128-byte swizzle: 16-byte chunk c of row r sits at chunk
+// c ^ (r mod 8).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int w) {
+  return (uint32_t)(r * 128 + ((((w >> 2) ^ (r & 7))) << 4) + ((w & 3) << 2));
+}
+
+// ---------------------------------------------------------------------------
+// Shared memory / barriers / bounded waits
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Control block every role of a CTA shares: a CTA-wide abort flag in shared
+// memory and the device error word.
+struct Ctl {
+  volatile int* abort;
+  int* err;
+};
+
+// Slow path of a bounded wait: give up after kWaitLimitNs, or at once when
+// another role already gave up. Records `code` in the error word.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, Ctl c, int code) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (*c.abort) return false;
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *c.abort = 1;
+      atomicCAS(c.err, 0, code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl c, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, c, code);
+}
+
+// Bounded wait that ignores the abort flag: used only to drain copies and MMAs
+// still in flight before a CTA releases its shared memory and TMEM.
+static __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMA
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"((uint64_t)m) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+      :: "r"(dst), "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
+// Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"((uint64_t)src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(dst_smem), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(bar) : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
+//  bits 4-5 D type (1 = f32), 7-9 A type (1 = bf16), 10-12 B type (1 = bf16),
+//  15 A MN-major, 16 B MN-major, 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor with 128-byte swizzle.
+//  bits 0-13 start >> 4, 16-29 leading byte offset >> 4, 32-45 stride byte
+//  offset >> 4, 46-48 = 0b001 (tcgen05 descriptor version), 61-63 = 2 (128B swizzle).
+// K-major operands: rows of 64 bf16 (128 B), 8-row groups SBO = 1024 B apart.
+// MN-major operands: 64 MN-elements per 128-B row, one row per K index; the
+// next 8 K rows are SBO = 1024 B on, the next 64 MN-elements LBO bytes on.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// K-major operand made of 128-row x 64-channel boxes (one per 64 channels):
+// k-step ks of 16 channels starts in box ks/4, 32 B into each row.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int ks) {
+  return sdesc_sw128(tile + (uint32_t)((ks >> 2) * kHalfBytes + (ks & 3) * 32), 16, 1024);
+}
+
+// MN-major operand stored as [K rows][MN columns] in the same boxes: k-step
+// ks of 16 rows starts 16 * 128 B further; MN columns 64.. are in the next box.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int ks) {
+  return sdesc_sw128(tile + (uint32_t)(ks * 2048), kHalfBytes, 1024);
+}
+
+// tcgen05.ld, 32 lanes x 32 bit, 32 consecutive columns; waits for completion.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr) : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tcgen05.st, 32 lanes x 32 bit, 16 consecutive columns (no wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// tcgen05.st, 32 lanes x 32 bit, 32 consecutive columns (no wait).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+      :: "r"(taddr),
+         "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+         "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+         "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+         "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+         "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
+         "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace skp

@@ -1,0 +1,380 @@
+// Skiparse attention forward: one persistent kernel per call.
+//
+// What it computes ("Open-Sora Plan" docs, "Skiparse Attention", single and
+// group skip listings): for every (batch b, head, scope s) the softmax
+// attention of the scope's L = N/k tokens among themselves, with q and k
+// rotated by 3D RoPE at their original positions, written back to the tokens'
+// original rows. The rearrange never happens in memory: the TMA tensor maps
+// address the scope's rows directly (see skiparse_host.cu), and the epilogue
+// stores each output row at its original token index.
+//
+// One work unit = (b, head, s, 128-row Q tile). Warp roles of a CTA:
+//   warps 0-3  softmax: one query row per thread (TMEM lane), online softmax
+//              with lazy O rescaling, P written back to TMEM as bf16, final
+//              O / l and LSE stores;
+//   warps 4-7  RoPE: rotate each Q and K tile in shared memory after TMA lands it;
+//   warp  8    TMA producer: Q tile, then a 2-stage K / V ring;
+//   warp  9    MMA issuer: S = Q K^T (smem x smem) and O += P V (TMEM x smem),
+//              tcgen05.mma kind::f16, fp32 accumulators in TMEM.
+// TMEM columns: S/P buffer 0 at 0, S/P buffer 1 at 128, O at 256.
+#include "skiparse_internal.h"
+
+namespace skp {
+
+template <int D>
+struct FwdLayout {
+  static constexpr int HALVES = D / 64;
+  static constexpr int TILE = 128 * D * 2;
+  static constexpr int HDR = 1024;
+  static constexpr int Q_OFF = HDR;
+  static constexpr int K_OFF = Q_OFF + TILE;
+  static constexpr int V_OFF = K_OFF + 2 * TILE;
+  static constexpr int ROPE_OFF = V_OFF + 2 * TILE;
+};
+
+enum FwdBar {
+  F_QFULL, F_QROT, F_QEMPTY,
+  F_KFULL0, F_KFULL1, F_KROT0, F_KROT1, F_KEMPTY0, F_KEMPTY1,
+  F_VFULL0, F_VFULL1, F_VEMPTY0, F_VEMPTY1,
+  F_SFULL0, F_SFULL1, F_PFULL0, F_PFULL1, F_ODONE, F_OEMPTY, F_FINAL, F_NBARS
+};
+
+constexpr int kFwdThreads = 320;
+constexpr uint32_t kColO = 256;
+
+__device__ __forceinline__ void decode_unit(const Geom& g, int u, int& b, int& head, int& s, int& tile) {
+  tile = u % g.n_tiles;
+  int r = u / g.n_tiles;
+  s = r % g.k;
+  r /= g.k;
+  head = r % g.heads;
+  b = r / g.heads;
+}
+
+// Rotate the rows of one 128-row tile in shared memory, in place. The tile
+// holds positions p0 .. p0+127 of scope s; rows at or past L are left alone.
+// Warp `wid` (0..3) owns rows 32*wid .. 32*wid+31; lane = channel pair within
+// a 64-channel box, so a warp touches one 128-byte row per step.
+template <int D>
+__device__ __forceinline__ void rope_tile(uint8_t* tile, int p0, int s, const Geom& g, const RopeParams& rp,
+                                          const float2* tab, int wid, int lane) {
+  constexpr int HALVES = D / 64;
+  const int r_mine = wid * 32 + lane;
+  const int p_mine = p0 + r_mine;
+  int t = 0, hh = 0, w = 0;
+  const bool valid = p_mine < g.L;
+  if (valid) token_coords(rp, token_of(g, s, p_mine), t, hh, w);
+  PairSel sel[HALVES];
+#pragma unroll
+  for (int hb = 0; hb < HALVES; ++hb) sel[hb] = pair_select(rp, hb * 32 + lane);
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+  for (int i = 0; i < 32; ++i) {
+    const int ti = __shfl_sync(0xffffffffu, t, i);
+    const int hi = __shfl_sync(0xffffffffu, hh, i);
+    const int wi = __shfl_sync(0xffffffffu, w, i);
+    if (!((vmask >> i) & 1u)) continue;
+    const int r = wid * 32 + i;
+#pragma unroll
+    for (int hb = 0; hb < HALVES; ++hb) {
+      const float2 cs = tab[pair_index(sel[hb], ti, hi, wi)];
+      uint32_t* word = reinterpret_cast<uint32_t*>(tile + hb * kHalfBytes + sw128_offset(r, lane));
+      const uint32_t u = *word;
+      const float2 o = rope_rotate(bf16lo(u), bf16hi(u), cs);
+      *word = pack_bf16(o.x, o.y);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using Ly = FwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
+  int* abort_flag = reinterpret_cast<int*>(smem + 520);
+  float2* tab = reinterpret_cast<float2*>(smem + Ly::ROPE_OFF);
+  const uint32_t sQ = smem_u32(smem + Ly::Q_OFF);
+  const uint32_t sK = smem_u32(smem + Ly::K_OFF);
+  const uint32_t sV = smem_u32(smem + Ly::V_OFF);
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  const Ctl ctl{abort_flag, p.err};
+  const Geom& g = p.g;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    const uint32_t counts[F_NBARS] = {1, 4, 1, 1, 1, 4, 4, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 4, 1};
+    for (int i = 0; i < F_NBARS; ++i) mbar_init(bar(i), counts[i]);
+    mbar_fence_init();
+  }
+  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
+  rope_build_table(tab, p.rope, tid, kFwdThreads);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&p.tm_q);
+      tma_prefetch_map(&p.tm_k);
+      tma_prefetch_map(&p.tm_v);
+      uint32_t q_issued = 0, k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
+      uint32_t gk = 0;
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+        int b, head, s, tile;
+        decode_unit(g, u, b, head, s, tile);
+        if (it > 0 && !mbar_wait(bar(F_QEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_QEMPTY)) break;
+        mbar_expect_tx(bar(F_QFULL), Ly::TILE);
+        const int qrow = b * g.Nn + (tile * kTile) / g.G;
+#pragma unroll
+        for (int h = 0; h < Ly::HALVES; ++h)
+          tma_load_5d(sQ + h * kHalfBytes, &p.tm_q, bar(F_QFULL), h * 64, head, 0, s, qrow);
+        ++q_issued;
+        for (int j = 0; j < g.n_tiles; ++j) {
+          const uint32_t gg = gk + j;
+          const int st = gg & 1;
+          const uint32_t n = gg >> 1;
+          const int krow = b * g.Nn + (j * kTile) / g.G;
+          if (n > 0 && !mbar_wait(bar(F_KEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_FWD + F_KEMPTY0 + st)) { ok = false; break; }
+          mbar_expect_tx(bar(F_KFULL0 + st), Ly::TILE);
+#pragma unroll
+          for (int h = 0; h < Ly::HALVES; ++h)
+            tma_load_5d(sK + st * Ly::TILE + h * kHalfBytes, &p.tm_k, bar(F_KFULL0 + st), h * 64, head, 0, s, krow);
+          ++k_issued[st];
+          if (n > 0 && !mbar_wait(bar(F_VEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_FWD + F_VEMPTY0 + st)) { ok = false; break; }
+          mbar_expect_tx(bar(F_VFULL0 + st), Ly::TILE);
+#pragma unroll
+          for (int h = 0; h < Ly::HALVES; ++h)
+            tma_load_5d(sV + st * Ly::TILE + h * kHalfBytes, &p.tm_v, bar(F_VFULL0 + st), h * 64, head, 0, s, krow);
+          ++v_issued[st];
+        }
+        gk += g.n_tiles;
+      }
+      // Copies still in flight (only after an abort) must land before exit.
+      if (q_issued) mbar_drain(bar(F_QFULL), (q_issued - 1) & 1);
+      for (int st = 0; st < 2; ++st) {
+        if (k_issued[st]) mbar_drain(bar(F_KFULL0 + st), (k_issued[st] - 1) & 1);
+        if (v_issued[st]) mbar_drain(bar(F_VFULL0 + st), (v_issued[st] - 1) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+      uint32_t g0 = 0;
+      int it = 0;
+      bool ok = true;
+      // O += P_j V_j for global tile index gg (local index j of unit number it).
+      auto issue_pv = [&](uint32_t gg, int j) -> bool {
+        const int st = gg & 1;
+        const uint32_t n = gg >> 1;
+        if (j == 0 && it > 0 && !mbar_wait(bar(F_OEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_OEMPTY)) return false;
+        if (!mbar_wait(bar(F_PFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_PFULL0 + st)) return false;
+        if (!mbar_wait(bar(F_VFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_VFULL0 + st)) return false;
+        tc_fence_after();
+        const uint32_t vt = sV + st * Ly::TILE;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tmem + kColO, tmem + st * 128 + ks * 8, desc_mnmajor(vt, ks), kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(bar(F_ODONE));
+        tc_commit(bar(F_VEMPTY0 + st));
+        return true;
+      };
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+        if (!mbar_wait(bar(F_QROT), it & 1, ctl, ERR_KERNEL_FWD + F_QROT)) break;
+        tc_fence_after();
+        for (int j = 0; j < g.n_tiles; ++j) {
+          const uint32_t gg = g0 + j;
+          const int st = gg & 1;
+          const uint32_t n = gg >> 1;
+          if (!mbar_wait(bar(F_KROT0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_KROT0 + st)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kt = sK + st * Ly::TILE;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tmem + st * 128, desc_kmajor(sQ, ks), desc_kmajor(kt, ks), kIdS, ks > 0 ? 1u : 0u);
+          tc_commit(bar(F_SFULL0 + st));
+          tc_commit(bar(F_KEMPTY0 + st));
+          if (j == g.n_tiles - 1) tc_commit(bar(F_QEMPTY));
+          if (j >= 1 && !issue_pv(gg - 1, j - 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!issue_pv(g0 + g.n_tiles - 1, g.n_tiles - 1)) break;
+        g0 += g.n_tiles;
+      }
+      tc_commit(bar(F_FINAL));
+      mbar_drain(bar(F_FINAL), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ RoPE warps
+    const int wid = warp - 4;
+    uint32_t gk = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      int b, head, s, tile;
+      decode_unit(g, u, b, head, s, tile);
+      if (!mbar_wait(bar(F_QFULL), it & 1, ctl, ERR_KERNEL_FWD + F_QFULL)) break;
+      rope_tile<D>(smem + Ly::Q_OFF, tile * kTile, s, g, p.rope, tab, wid, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(F_QROT));
+      for (int j = 0; j < g.n_tiles; ++j) {
+        const uint32_t gg = gk + j;
+        const int st = gg & 1;
+        const uint32_t n = gg >> 1;
+        if (!mbar_wait(bar(F_KFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_KFULL0 + st)) { ok = false; break; }
+        rope_tile<D>(smem + Ly::K_OFF + st * Ly::TILE, j * kTile, s, g, p.rope, tab, wid, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(F_KROT0 + st));
+      }
+      gk += g.n_tiles;
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int r = tid;                                  // query row of the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    uint32_t g0 = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      int b, head, s, tile;
+      decode_unit(g, u, b, head, s, tile);
+      float m = 0.f, l = 0.f;
+      for (int j = 0; j < g.n_tiles; ++j) {
+        const uint32_t gg = g0 + j;
+        const int st = gg & 1;
+        const uint32_t n = gg >> 1;
+        if (!mbar_wait(bar(F_SFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_SFULL0 + st)) { ok = false; break; }
+        tc_fence_after();
+        float sv[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tmem + lane_base + st * 128 + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+        const int valid = min(kTile, g.L - j * kTile);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 128; ++e) {
+          if (e >= valid) sv[e] = -INFINITY;
+          mx = fmaxf(mx, sv[e]);
+        }
+        mx *= sl2;
+        if (j == 0) {
+          m = mx;
+        } else {
+          const bool need = mx > m + 8.0f;
+          if (__any_sync(0xffffffffu, need)) {
+            // O holds sum over earlier tiles against the old reference max:
+            // wait until the last P V landed, then rescale O in TMEM.
+            if (!mbar_wait(bar(F_ODONE), (gg - 1) & 1, ctl, ERR_KERNEL_FWD + F_ODONE)) { ok = false; break; }
+            tc_fence_after();
+            const float m_new = need ? mx : m;
+            const float f = ex2(m - m_new);
+            m = m_new;
+            l *= f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              float o[32];
+              tmem_ld32(tmem + lane_base + kColO + c * 32, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= f;
+              tmem_st32(tmem + lane_base + kColO + c * 32, o);
+            }
+            tmem_st_wait();
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = ex2(fmaf(sv[c * 32 + 2 * e], sl2, -m));
+            const float bb = ex2(fmaf(sv[c * 32 + 2 * e + 1], sl2, -m));
+            l += a + bb;
+            pk[e] = pack_bf16(a, bb);
+          }
+          tmem_st16(tmem + lane_base + st * 128 + c * 16, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(F_PFULL0 + st));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l to the token's original row, LSE in natural log
+      const uint32_t glast = g0 + g.n_tiles - 1;
+      if (!mbar_wait(bar(F_ODONE), glast & 1, ctl, ERR_KERNEL_FWD + F_ODONE)) break;
+      tc_fence_after();
+      const int prow = tile * kTile + r;
+      const bool row_ok = prow < g.L;
+      const int tok = row_ok ? token_of(g, s, prow) : 0;
+      const float inv_l = 1.0f / l;
+      uint16_t* orow = p.out + (((size_t)b * g.N + tok) * g.heads + head) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + kColO + c * 32, o);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16(o[8 * q4 + 0] * inv_l, o[8 * q4 + 1] * inv_l);
+            w.y = pack_bf16(o[8 * q4 + 2] * inv_l, o[8 * q4 + 3] * inv_l);
+            w.z = pack_bf16(o[8 * q4 + 4] * inv_l, o[8 * q4 + 5] * inv_l);
+            w.w = pack_bf16(o[8 * q4 + 6] * inv_l, o[8 * q4 + 7] * inv_l);
+            dst[q4] = w;
+          }
+        }
+      }
+      if (row_ok) p.lse[((size_t)b * g.heads + head) * g.N + tok] = (m + log2f(l)) * 0.6931471805599453f;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(F_OEMPTY));
+      g0 += g.n_tiles;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+size_t fwd_smem_bytes(int D, int rope_entries) {
+  const size_t base = (D == 128) ? FwdLayout<128>::ROPE_OFF : FwdLayout<64>::ROPE_OFF;
+  return base + (size_t)rope_entries * sizeof(float2);
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = fwd_smem_bytes(p.g.D, p.rope.entries);
+  cudaError_t e;
+  if (p.g.D == 128) {
+    e = cudaFuncSetAttribute(skiparse_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_fwd_kernel<128><<<grid, kFwdThreads, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(skiparse_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_fwd_kernel<64><<<grid, kFwdThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace skp

@@ -1,0 +1,481 @@
+// C-ABI host layer: argument validation, TMA tensor maps that fold the
+// Skiparse rearrange into strides, kernel launches, device error word, tracing.
+//
+// The scope gather ("Open-Sora Plan" docs, "Skiparse Attention", single and
+// group skip rearrange patterns) becomes a 5-D tensor map over the caller's
+// (B, N, heads, D) buffer. With G = 1 (single) or G = k (group), token
+// i = n*k*G + s*G + kk, so the token axis splits into (n, s, kk); n and b merge
+// because b's stride is exactly N/(k*G) times n's:
+//   dim 0  channel d         extent D            stride 2 B
+//   dim 1  head              extent heads        stride D*2
+//   dim 2  kk (in-group)     extent G            stride heads*D*2
+//   dim 3  s (scope)         extent k            stride G*heads*D*2
+//   dim 4  (b, n) merged     extent B*N/(k*G)    stride k*G*heads*D*2
+// A box of (64, 1, G, 1, 128/G) elements is 128 consecutive positions of one
+// scope (position p = n*G + kk), landing as 128 rows of 128 B with 128-byte
+// swizzle. Rows past the end of a scope read the next batch's rows or zero
+// fill; the kernels mask them.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/skiparse.h"
+#include "skiparse_internal.h"
+
+using namespace skp;
+
+__device__ int g_skiparse_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int smem_optin = 0;
+  int cc = 0;
+  int* err_word = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Current device's facts; SKIPARSE_ERR_DEVICE if there is none or it is not sm_103.
+int device_info(DeviceInfo& out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SKIPARSE_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return SKIPARSE_ERR_DEVICE;
+    }
+    d.cc = major * 10 + minor;
+    void* addr = nullptr;
+    if (d.cc == 103) {
+      if (cudaGetSymbolAddress(&addr, g_skiparse_error_word) != cudaSuccess) {
+        cudaGetLastError();
+        return SKIPARSE_ERR_DEVICE;
+      }
+    }
+    d.err_word = static_cast<int*>(addr);
+    d.ready = true;
+  }
+  if (d.cc != 103) return SKIPARSE_ERR_DEVICE;
+  out = d;
+  return SKIPARSE_OK;
+}
+
+// ---------------------------------------------------------------- tracing
+
+struct TraceRec {
+  int id;
+  cudaEvent_t a, b;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+
+template <class F>
+cudaError_t traced_launch(int id, cudaStream_t stream, F&& launch) {
+  bool on;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    on = g_trace_on;
+  }
+  if (!on) return launch();
+  TraceRec r{id, nullptr, nullptr};
+  if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return cudaGetLastError();
+  cudaEventRecord(r.a, stream);
+  const cudaError_t e = launch();
+  cudaEventRecord(r.b, stream);
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace.push_back(r);
+  return e;
+}
+
+// ---------------------------------------------------------------- validation
+
+struct Shape {
+  int B, heads, N, D, T, H, W, k, mode;
+  bool empty;
+  long long elems;     // B*N*heads*D
+  int rope_entries;
+};
+
+int check_shape(int B, int heads, int N, int D, int T, int H, int W, int k, int mode, float theta, Shape& s) {
+  if (mode != SKIPARSE_SINGLE && mode != SKIPARSE_GROUP) return SKIPARSE_ERR_INVALID_ARG;
+  if (B < 0 || heads < 0 || N < 0 || T < 0 || H < 0 || W < 0 || k < 1 || D < 0) return SKIPARSE_ERR_INVALID_ARG;
+  if (!(theta > 0.0f) || !std::isfinite(theta)) return SKIPARSE_ERR_INVALID_ARG;
+  if ((long long)T * H * W != (long long)N) return SKIPARSE_ERR_SHAPE;
+  s = Shape{B, heads, N, D, T, H, W, k, mode, false, 0, 0};
+  if (B == 0 || heads == 0 || N == 0) {
+    s.empty = true;
+    return SKIPARSE_OK;
+  }
+  if (D != 64 && D != 128) return SKIPARSE_ERR_UNSUPPORTED;
+  if (mode == SKIPARSE_SINGLE && N % k != 0) return SKIPARSE_ERR_SHAPE;
+  if (mode == SKIPARSE_GROUP) {
+    if ((long long)k * k > N || N % (k * k) != 0) return SKIPARSE_ERR_SHAPE;
+    if (128 % k != 0) return SKIPARSE_ERR_UNSUPPORTED;
+  }
+  const long long entries = (long long)T * (D / 8) + (long long)H * (3 * D / 16) + (long long)W * (3 * D / 16);
+  if (entries > kMaxRopeEntries) return SKIPARSE_ERR_UNSUPPORTED;
+  s.rope_entries = (int)entries;
+  s.elems = (long long)B * N * heads * D;
+  const long long L = N / k;
+  const long long units = (long long)B * heads * k * ((L + kTile - 1) / kTile);
+  if (s.elems > (1ll << 46) || units >= (1ll << 31) || (long long)B * N >= (1ll << 31)) return SKIPARSE_ERR_UNSUPPORTED;
+  return SKIPARSE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  const void* p;
+  size_t bytes;
+};
+
+bool overlaps(const Range& a, const Range& b) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a.bytes && b.bytes && a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// outputs must not overlap inputs or each other
+bool any_alias(const std::vector<Range>& outs, const std::vector<Range>& ins) {
+  for (size_t i = 0; i < outs.size(); ++i) {
+    for (const Range& r : ins)
+      if (overlaps(outs[i], r)) return true;
+    for (size_t j = i + 1; j < outs.size(); ++j)
+      if (overlaps(outs[i], outs[j])) return true;
+  }
+  return false;
+}
+
+Geom make_geom(const Shape& s) {
+  Geom g;
+  g.B = s.B;
+  g.heads = s.heads;
+  g.N = s.N;
+  g.D = s.D;
+  g.k = s.k;
+  g.G = s.mode == SKIPARSE_SINGLE ? 1 : s.k;
+  g.L = s.N / s.k;
+  g.Nn = g.L / g.G;
+  g.n_tiles = (g.L + kTile - 1) / kTile;
+  return g;
+}
+
+RopeParams make_rope(const Shape& s, float theta) {
+  RopeParams r;
+  std::memset(&r, 0, sizeof(r));
+  const int dt = s.D / 4, dh = 3 * s.D / 8;
+  r.T = s.T;
+  r.H = s.H;
+  r.W = s.W;
+  r.dt2 = dt / 2;
+  r.dh2 = dh / 2;
+  r.entries = s.rope_entries;
+  for (int j = 0; j < r.dt2; ++j) r.om_t[j] = std::pow((double)theta, -2.0 * j / dt);
+  for (int j = 0; j < r.dh2; ++j) r.om_hw[j] = std::pow((double)theta, -2.0 * j / dh);
+  return r;
+}
+
+bool encode_scope_map(CUtensorMap* m, const void* base, const Geom& g) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t row = (cuuint64_t)g.heads * g.D * 2;
+  const cuuint64_t dims[5] = {(cuuint64_t)g.D, (cuuint64_t)g.heads, (cuuint64_t)g.G, (cuuint64_t)g.k,
+                              (cuuint64_t)g.B * g.Nn};
+  const cuuint64_t strides[4] = {(cuuint64_t)g.D * 2, row, row * g.G, row * g.G * g.k};
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)g.G, 1, (cuuint32_t)(kTile / g.G)};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WsLayout {
+  size_t dq_acc, qr, kr, lse2s, delta_s, tab, total;
+  int Lp;
+};
+
+WsLayout ws_layout(const Shape& s) {
+  WsLayout w;
+  const size_t e = (size_t)s.elems;
+  const int L = s.N / s.k;
+  w.Lp = ((L + kTile - 1) / kTile) * kTile;
+  const size_t stats = (size_t)s.B * s.heads * s.k * w.Lp;
+  size_t off = 0;
+  w.dq_acc = off; off += align256(e * 4);
+  w.qr = off;     off += align256(e * 2);
+  w.kr = off;     off += align256(e * 2);
+  w.lse2s = off;  off += align256(stats * 4);
+  w.delta_s = off; off += align256(stats * 4);
+  w.tab = off;    off += align256((size_t)s.rope_entries * sizeof(float2));
+  w.total = off;
+  return w;
+}
+
+int launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return SKIPARSE_OK;
+  cudaGetLastError();
+  return SKIPARSE_ERR_LAUNCH;
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+
+extern "C" {
+
+const char* skiparse_status_string(int status) {
+  switch (status) {
+    case SKIPARSE_OK: return "ok";
+    case SKIPARSE_ERR_INVALID_ARG: return "invalid argument (NULL pointer, negative size, bad mode or rope_theta)";
+    case SKIPARSE_ERR_SHAPE: return "shape mismatch (N != T*H*W, or N not divisible by k (single) / k*k (group))";
+    case SKIPARSE_ERR_UNSUPPORTED: return "unsupported configuration (D must be 64 or 128; group k must divide 128; RoPE table too large)";
+    case SKIPARSE_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case SKIPARSE_ERR_DEVICE: return "no CUDA device, or the current device is not sm_103 (GB300)";
+    case SKIPARSE_ERR_WORKSPACE: return "workspace missing or too small";
+    case SKIPARSE_ERR_LAUNCH: return "tensor-map encode or kernel launch failed";
+    case SKIPARSE_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (see detail code)";
+    case SKIPARSE_ERR_ALIAS: return "an output overlaps an input or another output";
+    default: return "unknown status";
+  }
+}
+
+const char* skiparse_kernel_name(int id) {
+  switch (id) {
+    case 0: return "skiparse_fwd_kernel";
+    case 1: return "skiparse_bwd_pre_kernel";
+    case 2: return "skiparse_bwd_main_kernel";
+    case 3: return "skiparse_bwd_post_kernel";
+    default: return "unknown";
+  }
+}
+
+int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      int B, int heads, int N, int D, int T, int H, int W,
+                      int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+  Shape s;
+  int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
+  if (st != SKIPARSE_OK || s.empty) return st;
+  if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
+  const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
+  if (any_alias({{out, tb}, {lse, lb}}, {{q, tb}, {k, tb}, {v, tb}})) return SKIPARSE_ERR_ALIAS;
+  DeviceInfo dev;
+  if ((st = device_info(dev)) != SKIPARSE_OK) return st;
+  if ((size_t)dev.smem_optin < fwd_smem_bytes(D, s.rope_entries)) return SKIPARSE_ERR_UNSUPPORTED;
+
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = make_geom(s);
+  p.rope = make_rope(s, rope_theta);
+  if (!encode_scope_map(&p.tm_q, q, p.g) || !encode_scope_map(&p.tm_k, k, p.g) || !encode_scope_map(&p.tm_v, v, p.g))
+    return SKIPARSE_ERR_LAUNCH;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.err = dev.err_word;
+  p.n_units = B * heads * sparse_k * p.g.n_tiles;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
+  return launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));
+}
+
+size_t skiparse_attn_bwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode) {
+  Shape s;
+  if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty) return 0;
+  return ws_layout(s).total;
+}
+
+int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                      int B, int heads, int N, int D, int T, int H, int W,
+                      int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+  Shape s;
+  int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
+  if (st != SKIPARSE_OK || s.empty) return st;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return SKIPARSE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return SKIPARSE_ERR_ALIGNMENT;
+  const WsLayout w = ws_layout(s);
+  if (!workspace || workspace_bytes < w.total) return SKIPARSE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
+  const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
+  if (any_alias({{dq, tb}, {dk, tb}, {dv, tb}, {workspace, w.total}},
+                {{q, tb}, {k, tb}, {v, tb}, {out, tb}, {lse, lb}, {dout, tb}}))
+    return SKIPARSE_ERR_ALIAS;
+  DeviceInfo dev;
+  if ((st = device_info(dev)) != SKIPARSE_OK) return st;
+  if ((size_t)dev.smem_optin < bwd_main_smem_bytes(D)) return SKIPARSE_ERR_UNSUPPORTED;
+
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = make_geom(s);
+  p.rope = make_rope(s, rope_theta);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.out = static_cast<const uint16_t*>(out);
+  p.dout = static_cast<const uint16_t*>(dout);
+  p.lse = lse;
+  p.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+  p.qr = reinterpret_cast<uint16_t*>(ws + w.qr);
+  p.kr = reinterpret_cast<uint16_t*>(ws + w.kr);
+  p.lse2s = reinterpret_cast<float*>(ws + w.lse2s);
+  p.delta_s = reinterpret_cast<float*>(ws + w.delta_s);
+  p.rope_tab = reinterpret_cast<float2*>(ws + w.tab);
+  p.dq = static_cast<uint16_t*>(dq);
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  p.err = dev.err_word;
+  p.Lp = w.Lp;
+  p.n_units = B * heads * sparse_k * p.g.n_tiles;
+  p.scale = (float)(1.0 / std::sqrt((double)D));
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  if (!encode_scope_map(&p.tm_q, p.qr, p.g) || !encode_scope_map(&p.tm_k, p.kr, p.g) ||
+      !encode_scope_map(&p.tm_v, v, p.g) || !encode_scope_map(&p.tm_do, dout, p.g))
+    return SKIPARSE_ERR_LAUNCH;
+
+  const long long rows = (long long)B * N * heads;
+  long long rgrid = (rows + 7) / 8;
+  if (rgrid > 4ll * dev.sms) rgrid = 4ll * dev.sms;
+  const int mgrid = p.n_units < dev.sms ? p.n_units : dev.sms;
+  st = launch_status(traced_launch(1, stream, [&] { return launch_bwd_pre(p, (int)rgrid, stream); }));
+  if (st != SKIPARSE_OK) return st;
+  st = launch_status(traced_launch(2, stream, [&] { return launch_bwd_main(p, mgrid, stream); }));
+  if (st != SKIPARSE_OK) return st;
+  return launch_status(traced_launch(3, stream, [&] { return launch_bwd_post(p, (int)rgrid, stream); }));
+}
+
+int skiparse_debug_index_map(int* scope_of_token, int* pos_of_token, int N, int sparse_k, int mode,
+                             cudaStream_t stream) {
+  if (mode != SKIPARSE_SINGLE && mode != SKIPARSE_GROUP) return SKIPARSE_ERR_INVALID_ARG;
+  if (N < 0 || sparse_k < 1) return SKIPARSE_ERR_INVALID_ARG;
+  if (N == 0) return SKIPARSE_OK;
+  if (!scope_of_token || !pos_of_token) return SKIPARSE_ERR_INVALID_ARG;
+  if (N % sparse_k != 0) return SKIPARSE_ERR_SHAPE;
+  if (mode == SKIPARSE_GROUP && ((long long)sparse_k * sparse_k > N || N % (sparse_k * sparse_k) != 0))
+    return SKIPARSE_ERR_SHAPE;
+  if (any_alias({{scope_of_token, (size_t)N * 4}, {pos_of_token, (size_t)N * 4}}, {})) return SKIPARSE_ERR_ALIAS;
+  DeviceInfo dev;
+  int st = device_info(dev);
+  if (st != SKIPARSE_OK) return st;
+  DebugParams p;
+  std::memset(&p, 0, sizeof(p));
+  Shape s{1, 1, N, 64, 1, 1, N, sparse_k, mode, false, 0, 0};
+  p.g = make_geom(s);
+  p.scope_of_token = scope_of_token;
+  p.pos_of_token = pos_of_token;
+  return launch_status(launch_debug_index_map(p, stream));
+}
+
+int skiparse_debug_rope(const void* x, float* x_rot, int B, int heads, int N, int D, int T, int H, int W,
+                        float rope_theta, cudaStream_t stream) {
+  Shape s;
+  int st = check_shape(B, heads, N, D, T, H, W, 1, SKIPARSE_SINGLE, rope_theta, s);
+  if (st != SKIPARSE_OK || s.empty) return st;
+  if (!x || !x_rot) return SKIPARSE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_rot)) return SKIPARSE_ERR_ALIGNMENT;
+  if (any_alias({{x_rot, (size_t)s.elems * 4}}, {{x, (size_t)s.elems * 2}})) return SKIPARSE_ERR_ALIAS;
+  DeviceInfo dev;
+  if ((st = device_info(dev)) != SKIPARSE_OK) return st;
+  DebugParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = make_geom(s);
+  p.rope = make_rope(s, rope_theta);
+  p.x = static_cast<const uint16_t*>(x);
+  p.x_rot = x_rot;
+  return launch_status(launch_debug_rope(p, stream));
+}
+
+int skiparse_device_error(int* detail) {
+  DeviceInfo dev;
+  int st = device_info(dev);
+  if (st != SKIPARSE_OK) return st;
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return SKIPARSE_ERR_LAUNCH;
+  }
+  if (cudaMemcpyFromSymbol(&v, g_skiparse_error_word, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return SKIPARSE_ERR_LAUNCH;
+  }
+  const int zero = 0;
+  cudaMemcpyToSymbol(g_skiparse_error_word, &zero, sizeof(int));
+  if (detail) *detail = v;
+  return v == 0 ? SKIPARSE_OK : SKIPARSE_ERR_DEVICE_TIMEOUT;
+}
+
+int skiparse_trace_begin(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = true;
+  return SKIPARSE_OK;
+}
+
+int skiparse_trace_end(float* ms_per_kernel, int* launches_per_kernel, int n) {
+  std::vector<TraceRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace_on = false;
+    recs.swap(g_trace);
+  }
+  for (int i = 0; i < n; ++i) {
+    if (ms_per_kernel) ms_per_kernel[i] = 0.f;
+    if (launches_per_kernel) launches_per_kernel[i] = 0;
+  }
+  int st = SKIPARSE_OK;
+  for (const TraceRec& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      cudaGetLastError();
+      st = SKIPARSE_ERR_LAUNCH;
+    }
+    if (r.id >= 0 && r.id < n) {
+      if (ms_per_kernel) ms_per_kernel[r.id] += ms;
+      if (launches_per_kernel) launches_per_kernel[r.id] += 1;
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Internal interface between the C-ABI host layer and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "skiparse_dev.cuh"
+
+namespace skp {
+
+// Codes written to the device error word when a bounded wait runs out:
+// 0x100 * kernel + barrier index (+ 0x80 for the drain path).
+enum : int {
+  ERR_KERNEL_FWD = 0x1000,
+  ERR_KERNEL_BWD = 0x2000,
+  ERR_SMEM_ALIGN = 0x7001,
+};
+
+struct FwdParams {
+  CUtensorMap tm_q, tm_k, tm_v;   // scope-gather maps over the caller's q, k, v
+  Geom g;
+  RopeParams rope;
+  uint16_t* out;                  // bf16 (B, N, heads, D)
+  float* lse;                     // (B, heads, N)
+  int* err;                       // device error word
+  int n_units;                    // B * heads * k * n_tiles
+  float scale_log2;               // log2(e) / sqrt(D)
+};
+
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // maps over rotated q, rotated k, v, dout
+  Geom g;
+  RopeParams rope;
+  const uint16_t* q;       // pre-RoPE inputs
+  const uint16_t* k;
+  const uint16_t* out;
+  const uint16_t* dout;
+  const float* lse;
+  uint16_t* qr;            // workspace: rotated q, bf16 (B, N, heads, D)
+  uint16_t* kr;            // workspace: rotated k
+  float* dq_acc;           // workspace: fp32 (B, N, heads, D)
+  float* lse2s;            // workspace: lse * log2(e), scope order (B, heads, k, Lp)
+  float* delta_s;          // workspace: rowsum(dO * O), scope order (B, heads, k, Lp)
+  float2* rope_tab;        // workspace: cos/sin table
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  int* err;
+  int n_units;             // B * heads * k * n_tiles (one K/V tile each)
+  int Lp;                  // L rounded up to a multiple of 128
+  float scale;             // 1 / sqrt(D)
+  float scale_log2;        // log2(e) / sqrt(D)
+};
+
+struct DebugParams {
+  Geom g;
+  RopeParams rope;
+  const uint16_t* x;
+  float* x_rot;
+  int* scope_of_token;
+  int* pos_of_token;
+};
+
+// Shared-memory bytes and launch helpers (defined next to each kernel).
+size_t fwd_smem_bytes(int D, int rope_entries);
+cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
+
+size_t bwd_main_smem_bytes(int D);
+cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_post(const BwdParams& p, int grid, cudaStream_t stream);
+
+cudaError_t launch_debug_index_map(const DebugParams& p, cudaStream_t stream);
+cudaError_t launch_debug_rope(const DebugParams& p, cudaStream_t stream);
+
+}  // namespace skp

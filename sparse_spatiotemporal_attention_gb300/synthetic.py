@@ -17,6 +17,8 @@ Default seeds: q=1, k=2, v=3, dO=4.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
@@ -29,31 +31,54 @@ SEEDS = {"q": 1, "k": 2, "v": 3, "do": 4}
 def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
     """Draws start .. start+count-1 of the splitmix64 stream of `seed` (uint64)."""
     with np.errstate(over="ignore"):
-        n = np.arange(start + 1, start + count + 1, dtype=np.uint64)
-        z = np.uint64(seed) + n * _GOLDEN
-        z = (z ^ (z >> np.uint64(30))) * _M1
-        z = (z ^ (z >> np.uint64(27))) * _M2
-        z = z ^ (z >> np.uint64(31))
+        z = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+        z *= _GOLDEN
+        z += np.uint64(seed)
+        t = z >> np.uint64(30)
+        z ^= t
+        z *= _M1
+        np.right_shift(z, np.uint64(27), out=t)
+        z ^= t
+        z *= _M2
+        np.right_shift(z, np.uint64(31), out=t)
+        z ^= t
     return z
 
 
-def normal_f64(seed: int, count: int, chunk: int = 1 << 22) -> np.ndarray:
-    """`count` N(0,1) float64 values of stream `seed` (Box-Muller on draw pairs)."""
+def _normal_pairs(seed: int, p0: int, p1: int) -> np.ndarray:
+    """Box-Muller values 2*p0 .. 2*p1-1 of stream `seed`."""
+    z = splitmix64(seed, 2 * p0, 2 * (p1 - p0))
+    u = ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+    u1, u2 = u[0::2], u[1::2]
+    r = np.sqrt(-2.0 * np.log(u1))
+    ang = 2.0 * np.pi * u2
+    blk = np.empty(2 * (p1 - p0), dtype=np.float64)
+    blk[0::2] = r * np.cos(ang)
+    blk[1::2] = r * np.sin(ang)
+    return blk
+
+
+def normal_f64(seed: int, count: int, chunk: int = 1 << 21) -> np.ndarray:
+    """`count` N(0,1) float64 values of stream `seed` (Box-Muller on draw pairs).
+    Chunks are independent (counter-based stream), so they run on a thread pool;
+    the result does not depend on the chunking."""
     out = np.empty(count, dtype=np.float64)
     npairs = (count + 1) // 2
-    for p0 in range(0, npairs, chunk):
+
+    def work(p0):
         p1 = min(npairs, p0 + chunk)
-        z = splitmix64(seed, 2 * p0, 2 * (p1 - p0))
-        u = ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
-        u1, u2 = u[0::2], u[1::2]
-        r = np.sqrt(-2.0 * np.log(u1))
-        ang = 2.0 * np.pi * u2
-        blk = np.empty(2 * (p1 - p0), dtype=np.float64)
-        blk[0::2] = r * np.cos(ang)
-        blk[1::2] = r * np.sin(ang)
-        o0 = 2 * p0
-        o1 = min(count, 2 * p1)
+        blk = _normal_pairs(seed, p0, p1)
+        o0, o1 = 2 * p0, min(count, 2 * p1)
         out[o0:o1] = blk[: o1 - o0]
+
+    starts = range(0, npairs, chunk)
+    if npairs > chunk:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(work, starts))
+    else:
+        for p0 in starts:
+            work(p0)
     return out
 
 
@@ -71,13 +96,46 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
-def normal_bf16_bits(seed: int, shape, scale: float = 1.0) -> np.ndarray:
-    """N(0, scale^2) values rounded to bfloat16, as a uint16 array of `shape`."""
+def normal_bf16_bits_numpy(seed: int, shape, scale: float = 1.0) -> np.ndarray:
+    """N(0, scale^2) values rounded to bfloat16, as a uint16 array of `shape`
+    (the definition of the recipe, in numpy)."""
     count = int(np.prod(shape))
     x = normal_f64(seed, count)
     if scale != 1.0:
         x = x * scale
     return f32_to_bf16_bits(x.astype(np.float32)).reshape(shape)
+
+
+_CLIB = None
+
+
+def _c_generator():
+    """The same recipe in C (csrc/synthetic_gen.c), built on demand with gcc."""
+    global _CLIB
+    if _CLIB is None:
+        import ctypes
+        from . import _build
+        path = _build.build_synthetic()
+        lib = ctypes.CDLL(path)
+        lib.synth_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double,
+                                          ctypes.c_void_p, ctypes.c_int]
+        lib.synth_normal_bf16.restype = None
+        _CLIB = lib
+    return _CLIB
+
+
+def normal_bf16_bits(seed: int, shape, scale: float = 1.0) -> np.ndarray:
+    """N(0, scale^2) values rounded to bfloat16, as a uint16 array of `shape`.
+    Uses the threaded C implementation of the recipe; falls back to numpy when
+    no C compiler is available."""
+    count = int(np.prod(shape))
+    try:
+        lib = _c_generator()
+    except Exception:
+        return normal_bf16_bits_numpy(seed, shape, scale)
+    out = np.empty(count, dtype=np.uint16)
+    lib.synth_normal_bf16(seed, count, float(scale), out.ctypes.data, os.cpu_count() or 1)
+    return out.reshape(shape)
 
 
 def attention_inputs(B: int, N: int, heads: int, D: int, with_grad: bool = False,

@@ -1,0 +1,121 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/skiparse.h declares, and rejects bad arguments on the host before
+touching the device (a valid call on a machine without a GPU reports
+SKIPARSE_ERR_DEVICE)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_spatiotemporal_attention_gb300 as skp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "skiparse.h")
+
+OK, INVALID, SHAPE, UNSUP, ALIGN, DEVICE, WORKSPACE, LAUNCH, TIMEOUT, ALIAS = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_spatiotemporal_attention_gb300 import _build
+    _build.build()
+    return skp.load_library()
+
+
+def _header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(skiparse_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_exports_match(lib):
+    names = _header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(skp.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code in (OK, INVALID, SHAPE, UNSUP, ALIGN, DEVICE, WORKSPACE, LAUNCH, TIMEOUT, ALIAS):
+        s = skp.status_string(code)
+        assert s and s != "unknown status"
+    assert skp.status_string(12345) == "unknown status"
+    for i in range(4):
+        assert lib.skiparse_kernel_name(i).decode() == skp.KERNEL_NAMES[i]
+
+
+A = 1 << 20  # fake, 16-byte-aligned device addresses: validation fails before any use
+
+
+def fwd(lib, q=A, k=2 * A, v=3 * A, out=4 * A, lse=5 * A, B=1, heads=2, N=256, D=64, T=4, H=8, W=8,
+        sk=2, mode=0, theta=10000.0):
+    return lib.skiparse_attn_fwd(q, k, v, out, lse, B, heads, N, D, T, H, W, sk, mode, theta, None)
+
+
+def test_fwd_validation(lib):
+    assert fwd(lib, mode=2) == INVALID
+    assert fwd(lib, B=-1) == INVALID
+    assert fwd(lib, sk=0) == INVALID
+    assert fwd(lib, theta=0.0) == INVALID
+    assert fwd(lib, theta=float("inf")) == INVALID
+    assert fwd(lib, N=255) == SHAPE                      # N != T*H*W
+    assert fwd(lib, D=96) == UNSUP
+    assert fwd(lib, T=3, N=192, sk=5) == SHAPE           # 192 % 5
+    assert fwd(lib, N=256, sk=32, mode=1) == SHAPE       # 256 % 1024
+    assert fwd(lib, T=9, H=6, W=6, N=324, sk=3, mode=1) == UNSUP   # group k must divide 128
+    assert fwd(lib, T=2000, H=20, W=20, N=800000) == UNSUP         # RoPE table too large
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, lse=5 * A + 4) == ALIGN
+    assert fwd(lib, out=A + 64) == ALIAS                 # out overlaps q
+    assert fwd(lib, lse=4 * A + 128) == ALIAS            # lse overlaps out
+    # empty calls are valid no-ops, pointers may be NULL
+    assert fwd(lib, B=0, q=None, k=None, v=None, out=None, lse=None) == OK
+    assert fwd(lib, T=0, N=0) == OK
+    # a valid call with no GPU present reaches the device check
+    assert fwd(lib) in (DEVICE,)
+
+
+def test_bwd_validation_and_workspace(lib):
+    ws = lib.skiparse_attn_bwd_workspace_bytes(1, 2, 256, 64, 4, 8, 8, 2, 0)
+    elems = 256 * 2 * 64
+    assert ws >= elems * 4 + 2 * elems * 2
+    assert lib.skiparse_attn_bwd_workspace_bytes(0, 2, 256, 64, 4, 8, 8, 2, 0) == 0
+    assert lib.skiparse_attn_bwd_workspace_bytes(1, 2, 256, 96, 4, 8, 8, 2, 0) == 0
+    big = lib.skiparse_attn_bwd_workspace_bytes(2, 24, 21120, 128, 24, 22, 40, 4, 1)
+    assert big >= 2 * 24 * 21120 * 128 * 8
+
+    def bwd(ws_ptr=10 * A, ws_bytes=ws, dq=7 * A, mode=0):
+        return lib.skiparse_attn_bwd(A, 2 * A, 3 * A, 4 * A, 5 * A, 6 * A, dq, 8 * A, 9 * A, ws_ptr, ws_bytes,
+                                     1, 2, 256, 64, 4, 8, 8, 2, mode, 10000.0, None)
+    assert bwd(ws_ptr=None) == WORKSPACE
+    assert bwd(ws_bytes=ws - 1) == WORKSPACE
+    assert bwd(ws_ptr=10 * A + 16) == ALIGN
+    assert bwd(dq=6 * A) == ALIAS
+    assert bwd(ws_ptr=9 * A) == ALIAS
+    assert bwd() == DEVICE
+
+
+def test_debug_hook_validation(lib):
+    assert lib.skiparse_debug_index_map(A, 2 * A, 16, 3, 0, None) == SHAPE
+    assert lib.skiparse_debug_index_map(A, 2 * A, 16, 2, 2, None) == INVALID
+    assert lib.skiparse_debug_index_map(A, A, 16, 2, 0, None) == ALIAS
+    assert lib.skiparse_debug_index_map(None, None, 0, 2, 0, None) == OK
+    assert lib.skiparse_debug_rope(A, 2 * A, 1, 1, 256, 64, 4, 8, 8, 10000.0, None) == DEVICE
+    assert lib.skiparse_debug_rope(A, A + 16, 1, 1, 256, 64, 4, 8, 8, 10000.0, None) == ALIAS
+
+
+def test_trace_without_gpu(lib):
+    skp.skiparse_trace_begin()
+    ms, cnt = skp.skiparse_trace_end(4)
+    assert ms == [0.0] * 4 and cnt == [0] * 4
+
+
+def test_package_has_no_fallback():
+    """The binding must not import the oracle or any CPU path."""
+    src = open(os.path.join(ROOT, "sparse_spatiotemporal_attention_gb300", "__init__.py")).read()
+    assert "oracle" not in src.replace("fallback", "")
+    for f in os.listdir(os.path.join(ROOT, "sparse_spatiotemporal_attention_gb300")):
+        if f.endswith(".py"):
+            assert "import oracle" not in open(os.path.join(ROOT, "sparse_spatiotemporal_attention_gb300", f)).read()

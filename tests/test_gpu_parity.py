@@ -1,0 +1,174 @@
+"""GPU parity through the C ABI against the float64 oracle (small and medium
+shapes the oracle finishes in seconds). Each case spans one or more 128-row
+tiles; several have a ragged last tile (L not a multiple of 128) or a scope
+shorter than one tile.
+
+Bars: index maps bit-exact; RoPE fp32 max-abs 1e-5; out, dq, dk, dv (bf16)
+max-abs 2e-2, mean-abs 2e-3 and relative RMS 1e-2; LSE max-abs 1e-2.
+"""
+import numpy as np
+import pytest
+
+from oracle import skiparse_oracle as O
+from sparse_spatiotemporal_attention_gb300 import synthetic
+import skiparse_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_spatiotemporal_attention_gb300 as skp
+    assert torch.cuda.is_available()
+    return skp, torch.device("cuda:0")
+
+
+# (B, heads, D, T, H, W, k, mode)
+CASES = [
+    (1, 2, 64, 4, 8, 8, 2, O.SINGLE),        # the tiny correctness config, single skip
+    (1, 2, 64, 4, 8, 8, 2, O.GROUP),         # the tiny correctness config, group skip
+    (1, 2, 128, 3, 10, 10, 2, O.SINGLE),     # L = 150: two tiles, ragged tail of 22
+    (1, 2, 128, 3, 10, 10, 2, O.GROUP),
+    (2, 3, 64, 2, 8, 12, 2, O.SINGLE),       # B > 1, L = 96 < one tile
+    (2, 2, 128, 2, 12, 20, 4, O.GROUP),      # B > 1, L = 120, merged batch rows in the tail
+    (1, 2, 128, 1, 16, 24, 4, O.GROUP),      # T = 1 (an image), L = 96
+    (1, 2, 128, 2, 8, 16, 1, O.SINGLE),      # k = 1: dense attention, L = 256
+    (1, 1, 128, 2, 8, 16, 1, O.GROUP),
+    (1, 2, 128, 4, 16, 16, 2, O.GROUP),      # L = 512: four full tiles
+    (1, 1, 128, 2, 16, 32, 8, O.GROUP),      # k = 8
+    (1, 2, 64, 3, 6, 8, 3, O.SINGLE),        # k = 3 (single skip takes any k), L = 48
+    (1, 2, 128, 5, 9, 14, 5, O.SINGLE),      # k = 5, L = 126
+    (2, 2, 128, 3, 20, 24, 4, O.SINGLE),     # L = 360: 3 tiles, tail 104, B = 2
+    (1, 1, 128, 8, 32, 32, 4, O.SINGLE),     # the 8x32x32 grid with one head, L = 2048
+]
+
+
+def _ids(c):
+    B, h, D, T, H, W, k, m = c
+    return f"B{B}h{h}D{D}_{T}x{H}x{W}_k{k}_{'single' if m == O.SINGLE else 'group'}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_forward_parity(env, case):
+    skp, dev = env
+    B, heads, D, T, H, W, k, mode = case
+    N = T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D)
+    fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode)
+    f = tl.f64_inputs(ins)
+    rout, rlse = O.skiparse_fwd(f["q"], f["k"], f["v"], T, H, W, k, mode)
+    tl.compare("out", tl.host(fw["out"]), rout)
+    tl.compare("lse", tl.host(fw["lse"]), rlse, tol_max=tl.TOL_LSE, tol_mean=tl.TOL_LSE, tol_rel=1e-3)
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
+
+
+BWD_CASES = [c for c in CASES if c[3] * c[4] * c[5] <= 4096]
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=_ids)
+def test_backward_parity(env, case):
+    skp, dev = env
+    B, heads, D, T, H, W, k, mode = case
+    N = T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True)
+    fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode)
+    bw = tl.run_bwd(skp, dev, ins, fw, B, heads, N, D, T, H, W, k, mode)
+    f = tl.f64_inputs(ins)
+    rdq, rdk, rdv, rout, rlse = O.skiparse_bwd(f["q"], f["k"], f["v"], f["do"], T, H, W, k, mode)
+    tl.compare("out", tl.host(fw["out"]), rout)
+    tl.compare("dv", tl.host(bw["dv"]), rdv)
+    tl.compare("dk", tl.host(bw["dk"]), rdk)
+    tl.compare("dq", tl.host(bw["dq"]), rdq)
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
+
+
+def test_peaky_softmax_rescale(env):
+    """q scaled by 4 makes row maxima jump between key tiles, exercising the
+    online-softmax rescale of O. Not a contract workload: with |q| four times
+    larger, the bf16 rounding of the rotated q and k (the MMA operands) moves
+    each logit by up to ~2^-9 * |q~||k~| / sqrt(D), about 0.05 here, and the
+    bf16 P and output roundings add 2^-9 * max|v| each. The bound is therefore
+    stated relative to the data: relative RMS 1e-2, max-abs 2^-4 * max|ref|."""
+    skp, dev = env
+    B, heads, D, T, H, W, k, mode = 1, 2, 128, 4, 16, 16, 2, O.SINGLE
+    N = T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True, q_scale=4.0)
+    fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode)
+    bw = tl.run_bwd(skp, dev, ins, fw, B, heads, N, D, T, H, W, k, mode)
+    f = tl.f64_inputs(ins)
+    rdq, rdk, rdv, rout, rlse = O.skiparse_bwd(f["q"], f["k"], f["v"], f["do"], T, H, W, k, mode)
+    tl.compare("lse", tl.host(fw["lse"]), rlse, tol_max=tl.TOL_LSE * 4, tol_mean=tl.TOL_LSE, tol_rel=1e-3)
+    for name, got, ref in (("out", fw["out"], rout), ("dv", bw["dv"], rdv), ("dk", bw["dk"], rdk),
+                           ("dq", bw["dq"], rdq)):
+        m = np.abs(ref).max()
+        tl.compare(name, tl.host(got), ref, tol_max=m / 16, tol_mean=m / 256, tol_rel=1e-2)
+
+
+@pytest.mark.parametrize("mode", [O.SINGLE, O.GROUP])
+@pytest.mark.parametrize("N,k", [(256, 2), (4096, 4), (21120, 4), (57600, 4), (1024, 8), (300, 3), (512, 1)])
+def test_index_map_bit_exact(env, mode, N, k):
+    import torch
+    skp, dev = env
+    if mode == O.GROUP and (N % (k * k) or 128 % k):
+        pytest.skip("not a group-skip shape")
+    if N % k:
+        pytest.skip("not a single-skip shape")
+    scope = torch.empty(N, dtype=torch.int32, device=dev)
+    pos = torch.empty(N, dtype=torch.int32, device=dev)
+    skp.skiparse_debug_index_map(scope, pos, N, k, mode)
+    torch.cuda.synchronize()
+    rs, rp = O.index_maps(N, k, mode)
+    assert np.array_equal(scope.cpu().numpy(), rs)
+    assert np.array_equal(pos.cpu().numpy(), rp)
+
+
+@pytest.mark.parametrize("D,grid", [(64, (4, 8, 8)), (128, (24, 22, 40)), (128, (16, 45, 80)), (128, (1, 3, 5))])
+def test_rope_fp32(env, D, grid):
+    import torch
+    skp, dev = env
+    T, H, W = grid
+    N = T * H * W
+    heads = 2
+    x = synthetic.normal_bf16_bits(7, (1, N, heads, D))
+    xd = tl.to_device(x, dev)
+    out = torch.empty((1, N, heads, D), dtype=torch.float32, device=dev)
+    skp.skiparse_debug_rope(xd, out, T, H, W, 10000.0)
+    torch.cuda.synchronize()
+    ref = O.apply_rope(synthetic.bf16_bits_to_f64(x), T, H, W, 10000.0)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref).max()
+    assert err <= tl.TOL_ROPE, err
+
+
+def test_trace_counts_launches(env):
+    skp, dev = env
+    B, heads, D, T, H, W, k, mode = 1, 2, 64, 4, 8, 8, 2, O.GROUP
+    N = T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True)
+    skp.skiparse_trace_begin()
+    fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode, guard=False)
+    tl.run_bwd(skp, dev, ins, fw, B, heads, N, D, T, H, W, k, mode, guard=False)
+    ms, cnt = skp.skiparse_trace_end(4)
+    assert cnt == [1, 1, 1, 1]
+    assert all(m > 0 for m in ms)
+
+
+def test_empty_and_invalid_calls_on_device(env):
+    import torch
+    skp, dev = env
+    q = torch.zeros((1, 256, 2, 64), dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros((1, 2, 256), dtype=torch.float32, device=dev)
+    out = torch.zeros_like(q)
+    with pytest.raises(skp.SkiparseError) as e:
+        skp.skiparse_attn_fwd(q, q, q, out, lse, 4, 8, 7, 2, 0)      # N != T*H*W
+    assert e.value.status == -2
+    with pytest.raises(skp.SkiparseError) as e:
+        skp.skiparse_attn_fwd(q, q, q, q, lse, 4, 8, 8, 2, 0)        # out aliases q
+    assert e.value.status == -9
+    empty = torch.zeros((0, 256, 2, 64), dtype=torch.bfloat16, device=dev)
+    skp.skiparse_attn_fwd(empty, empty, empty, empty, lse, 4, 8, 8, 2, 0)
+    assert out.abs().sum().item() == 0
