@@ -164,20 +164,29 @@ def run_cpu_baseline(seconds: float):
 # ---------------------------------------------------------------------------- GPU arm
 
 def traffic_record(kernel_name):
-    """Per-launch DRAM bytes from the committed ncu summary, if the kernel's
-    source is unchanged since it was taken; else None."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    """Per-launch DRAM bytes of `kernel_name` from the committed ncu summaries
+    (a `traffic_record:` line in profiles/*.md), if the kernel's sources are
+    unchanged since the capture; else None."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
         return None
-    with open(p) as f:
-        d = json.load(f)
-    rec = d.get(kernel_name)
-    if not rec:
-        return None
-    src = os.path.join(ROOT, "sparse_spatiotemporal_attention_gb300", "csrc", rec["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
-        return None
-    return rec["dram_bytes_per_launch"]
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith(".md"):
+            continue
+        for line in open(os.path.join(pdir, fn)):
+            if not line.startswith("traffic_record:"):
+                continue
+            rec = json.loads(line.split(":", 1)[1])
+            if rec.get("kernel") != kernel_name:
+                continue
+            h = hashlib.sha256()
+            for src in rec["sources"]:
+                path = os.path.join(ROOT, "sparse_spatiotemporal_attention_gb300", "csrc", src)
+                if not os.path.exists(path):
+                    return None
+                h.update(open(path, "rb").read())
+            return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
+    return None
 
 
 def gpu_arm(args):

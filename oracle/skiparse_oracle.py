@@ -23,7 +23,7 @@ listings, step by step in the order given there:
 Everything is float64 from the bf16-valued inputs; no rounding is modelled.
 The backward pass is the exact analytic gradient of that float64 forward pass.
 
-Readings taken where the page is silent (each also listed in the design doc):
+Readings taken where the page is silent:
   * tokens are flattened t-major, then h, then w: i = (t*H + h)*W + w;
   * multi-head: the rearrange acts on the token axis only, identically per head,
     and the softmax scale is 1/sqrt(D) with D the head dimension;
