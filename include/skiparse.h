@@ -97,6 +97,32 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
+ * Allocation-free backward. The pages have no counterpart to this entry point:
+ * it exists for callers that cannot allocate device memory when they run the
+ * backward (a host whose allocator must not be re-entered, a plugin or
+ * embedded runtime that owns all device memory, or a fixed memory plan).
+ * Arguments and results are those of skiparse_attn_bwd without the workspace:
+ * the scratch is one device array of SKIPARSE_NOALLOC_SCRATCH_BYTES (64 MiB)
+ * built into the library, which every GPU that loads the library holds until
+ * the process exits.
+ *   - Returns SKIPARSE_ERR_WORKSPACE, launching nothing, when
+ *     skiparse_attn_bwd_workspace_bytes(...) for these sizes is larger than
+ *     SKIPARSE_NOALLOC_SCRATCH_BYTES (about 8M elements of B*N*heads*D).
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     contents; each call rewrites all it reads and zeroes its dQ accumulator.
+ *     Calls that overlap on the GPU (e.g. on two streams) race on the array:
+ *     serialise them.
+ */
+#define SKIPARSE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int skiparse_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv,
+                              int B, int heads, int N, int D, int T, int H, int W,
+                              int sparse_k, int mode, float rope_theta, cudaStream_t stream);
+
+/*
  * Test hook: the token -> (scope, position) map exactly as the kernels address
  * it (the listings' rearrange patterns). Writes int32 scope_of_token[N] and
  * pos_of_token[N].

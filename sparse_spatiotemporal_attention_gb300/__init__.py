@@ -26,6 +26,7 @@ EXPORTS = (
     "skiparse_attn_fwd", "skiparse_attn_bwd_workspace_bytes", "skiparse_attn_bwd",
     "skiparse_debug_index_map", "skiparse_debug_rope", "skiparse_status_string",
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
+    "skiparse_attn_bwd_noalloc",
 )
 
 
@@ -61,6 +62,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_trace_begin": (_c_int, []),
         "skiparse_trace_end": (_c_int, [ctypes.POINTER(_c_float), ctypes.POINTER(_c_int), _c_int]),
         "skiparse_kernel_name": (ctypes.c_char_p, [_c_int]),
+        "skiparse_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 9 + [_c_float, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -129,6 +131,22 @@ def skiparse_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace, T, H, W, s
                                           B, heads, N, D, T, H, W, sparse_k, mode,
                                           float(rope_theta), _stream(stream))
     _check(st, "skiparse_attn_bwd")
+
+
+def skiparse_attn_bwd_noalloc(q, k, v, out, lse, dout, dq, dk, dv, T, H, W, sparse_k, mode,
+                              rope_theta=10000.0, stream=None):
+    """Backward pass for callers that cannot allocate device memory: the scratch
+    is a fixed array inside the library (SKIPARSE_NOALLOC_SCRATCH_BYTES, 64 MiB),
+    shared by all calls, so calls must not overlap on the GPU. Larger sizes are
+    rejected with status -6 (SKIPARSE_ERR_WORKSPACE)."""
+    B, heads, N, D = _shape(q)
+    st = load_library().skiparse_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                                  _ptr(dq), _ptr(dk), _ptr(dv), B, heads, N, D, T, H, W,
+                                                  sparse_k, mode, float(rope_theta), _stream(stream))
+    _check(st, "skiparse_attn_bwd_noalloc")
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def skiparse_debug_index_map(scope_of_token, pos_of_token, N, sparse_k, mode, stream=None):
