@@ -12,7 +12,8 @@
 //   warps 0-3  softmax: one query row per thread (TMEM lane), online softmax
 //              with lazy O rescaling, P written back to TMEM as bf16, final
 //              O / l and LSE stores;
-//   warps 4-7  RoPE: rotate each Q and K tile in shared memory after TMA lands it;
+//   warps 4-7  RoPE: rotate each Q and K tile in shared memory after TMA lands it
+//              (16-byte chunks, per-row table offsets staged in shared memory);
 //   warp  8    TMA producer: Q tile, then a 2-stage K / V ring;
 //   warp  9    MMA issuer: S = Q K^T (smem x smem) and O += P V (TMEM x smem),
 //              tcgen05.mma kind::f16, fp32 accumulators in TMEM.
@@ -29,7 +30,8 @@ struct FwdLayout {
   static constexpr int Q_OFF = HDR;
   static constexpr int K_OFF = Q_OFF + TILE;
   static constexpr int V_OFF = K_OFF + 2 * TILE;
-  static constexpr int ROPE_OFF = V_OFF + 2 * TILE;
+  static constexpr int ROWOFF_OFF = V_OFF + 2 * TILE;   // [2][128] int4 per-row RoPE table offsets
+  static constexpr int ROPE_OFF = ROWOFF_OFF + 2 * 128 * 16;
 };
 
 enum FwdBar {
@@ -51,38 +53,70 @@ __device__ __forceinline__ void decode_unit(const Geom& g, int u, int& b, int& h
   b = r / g.heads;
 }
 
+// Named barrier over the 4 RoPE warps that also ANDs a predicate across them,
+// so that every RoPE warp takes the same branch after a bounded wait.
+__device__ __forceinline__ bool rope_bar_and(bool v) {
+  uint32_t out;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(out) : "r"(v ? 1u : 0u) : "memory");
+  return out != 0;
+}
+
 // Rotate the rows of one 128-row tile in shared memory, in place. The tile
 // holds positions p0 .. p0+127 of scope s; rows at or past L are left alone.
-// Warp `wid` (0..3) owns rows 32*wid .. 32*wid+31; lane = channel pair within
-// a 64-channel box, so a warp touches one 128-byte row per step.
+// Step 1: RoPE thread r (0..127) stores row r's table offsets in `rowoff`
+// (entry of pair 0 of the t, h and w chunks at the row's position, and a
+// valid flag). Step 2, after the barrier (which also ANDs `ok`): a lane owns
+// one 16-byte chunk (4 channel pairs, always inside one axis chunk) of one of
+// 4 rows, so a warp touches 4 whole 128-byte rows per step. Returns false if
+// any RoPE thread passed in ok = false (then nothing is rotated).
 template <int D>
-__device__ __forceinline__ void rope_tile(uint8_t* tile, int p0, int s, const Geom& g, const RopeParams& rp,
-                                          const float2* tab, int wid, int lane) {
+__device__ __forceinline__ bool rope_tile(uint8_t* tile, int4* rowoff, int p0, int s, const Geom& g,
+                                          const RopeParams& rp, const float2* tab, int rtid, int lane, bool ok) {
   constexpr int HALVES = D / 64;
-  const int r_mine = wid * 32 + lane;
-  const int p_mine = p0 + r_mine;
-  int t = 0, hh = 0, w = 0;
-  const bool valid = p_mine < g.L;
-  if (valid) token_coords(rp, token_of(g, s, p_mine), t, hh, w);
-  PairSel sel[HALVES];
+  {
+    const int p = p0 + rtid;
+    int4 ro = make_int4(0, 0, 0, 0);
+    if (ok && p < g.L) {
+      int t, hh, w;
+      token_coords(rp, token_of(g, s, p), t, hh, w);
+      const int bt = rp.T * rp.dt2;
+      ro = make_int4(t * rp.dt2, bt + hh * rp.dh2, bt + rp.H * rp.dh2 + w * rp.dh2, 1);
+    }
+    rowoff[rtid] = ro;
+  }
+  if (!rope_bar_and(ok)) return false;
+  const int wid = rtid >> 5;
+  const int rsub = lane >> 3;
+  const int c = lane & 7;
+  int axis[HALVES], local[HALVES];
 #pragma unroll
-  for (int hb = 0; hb < HALVES; ++hb) sel[hb] = pair_select(rp, hb * 32 + lane);
-  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-  for (int i = 0; i < 32; ++i) {
-    const int ti = __shfl_sync(0xffffffffu, t, i);
-    const int hi = __shfl_sync(0xffffffffu, hh, i);
-    const int wi = __shfl_sync(0xffffffffu, w, i);
-    if (!((vmask >> i) & 1u)) continue;
-    const int r = wid * 32 + i;
+  for (int hb = 0; hb < HALVES; ++hb) {
+    const PairSel sel = pair_select(rp, (hb * 8 + c) * 4);
+    axis[hb] = sel.axis;
+    local[hb] = sel.local;
+  }
+#pragma unroll 2
+  for (int it = 0; it < 8; ++it) {
+    const int r = wid * 32 + it * 4 + rsub;
+    const int4 ro = rowoff[r];
+    if (!ro.w) continue;
 #pragma unroll
     for (int hb = 0; hb < HALVES; ++hb) {
-      const float2 cs = tab[pair_index(sel[hb], ti, hi, wi)];
-      uint32_t* word = reinterpret_cast<uint32_t*>(tile + hb * kHalfBytes + sw128_offset(r, lane));
-      const uint32_t u = *word;
-      const float2 o = rope_rotate(bf16lo(u), bf16hi(u), cs);
-      *word = pack_bf16(o.x, o.y);
+      const int e = (axis[hb] == 0 ? ro.x : (axis[hb] == 1 ? ro.y : ro.z)) + local[hb];
+      const float4 cs01 = *reinterpret_cast<const float4*>(tab + e);
+      const float4 cs23 = *reinterpret_cast<const float4*>(tab + e + 2);
+      uint4* ptr = reinterpret_cast<uint4*>(tile + hb * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4));
+      const uint4 v = *ptr;
+      const float2 a0 = rope_rotate(bf16lo(v.x), bf16hi(v.x), make_float2(cs01.x, cs01.y));
+      const float2 a1 = rope_rotate(bf16lo(v.y), bf16hi(v.y), make_float2(cs01.z, cs01.w));
+      const float2 a2 = rope_rotate(bf16lo(v.z), bf16hi(v.z), make_float2(cs23.x, cs23.y));
+      const float2 a3 = rope_rotate(bf16lo(v.w), bf16hi(v.w), make_float2(cs23.z, cs23.w));
+      *ptr = make_uint4(pack_bf16(a0.x, a0.y), pack_bf16(a1.x, a1.y), pack_bf16(a2.x, a2.y), pack_bf16(a3.x, a3.y));
     }
   }
+  return true;
 }
 
 template <int D>
@@ -100,6 +134,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
   int* abort_flag = reinterpret_cast<int*>(smem + 520);
   float2* tab = reinterpret_cast<float2*>(smem + Ly::ROPE_OFF);
+  int4* rowoff = reinterpret_cast<int4*>(smem + Ly::ROWOFF_OFF);
   const uint32_t sQ = smem_u32(smem + Ly::Q_OFF);
   const uint32_t sK = smem_u32(smem + Ly::K_OFF);
   const uint32_t sV = smem_u32(smem + Ly::V_OFF);
@@ -219,15 +254,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ RoPE warps
-    const int wid = warp - 4;
-    uint32_t gk = 0;
+    const int rtid = tid - 128;
+    uint32_t gk = 0, ntile = 0;
     int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
       int b, head, s, tile;
       decode_unit(g, u, b, head, s, tile);
-      if (!mbar_wait(bar(F_QFULL), it & 1, ctl, ERR_KERNEL_FWD + F_QFULL)) break;
-      rope_tile<D>(smem + Ly::Q_OFF, tile * kTile, s, g, p.rope, tab, wid, lane);
+      ok = mbar_wait(bar(F_QFULL), it & 1, ctl, ERR_KERNEL_FWD + F_QFULL);
+      ok = rope_tile<D>(smem + Ly::Q_OFF, rowoff + (ntile++ & 1) * 128, tile * kTile, s, g, p.rope, tab, rtid, lane, ok);
+      if (!ok) break;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(F_QROT));
@@ -235,8 +271,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
         const uint32_t gg = gk + j;
         const int st = gg & 1;
         const uint32_t n = gg >> 1;
-        if (!mbar_wait(bar(F_KFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_KFULL0 + st)) { ok = false; break; }
-        rope_tile<D>(smem + Ly::K_OFF + st * Ly::TILE, j * kTile, s, g, p.rope, tab, wid, lane);
+        ok = mbar_wait(bar(F_KFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_KFULL0 + st);
+        ok = rope_tile<D>(smem + Ly::K_OFF + st * Ly::TILE, rowoff + (ntile++ & 1) * 128, j * kTile, s, g, p.rope,
+                          tab, rtid, lane, ok);
+        if (!ok) break;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(F_KROT0 + st));
