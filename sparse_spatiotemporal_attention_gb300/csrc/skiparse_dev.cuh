@@ -234,6 +234,37 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       :: "r"(dst), "l"((uint64_t)src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// Bulk reduce-add of `bytes` fp32 values from shared to global memory (the
+// TMA unit adds them element-wise, atomically per element), tracked as a bulk
+// group of the issuing thread.
+__device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+               :: "l"((uint64_t)gdst), "r"(ssrc), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed bulk groups still read their shared source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
+}
+// Wait until every committed bulk group has fully completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Named barrier over `nthreads` threads that ANDs a predicate across them, so a
+// group of warps takes the same branch after bounded waits.
+template <int ID, int NTHREADS>
+__device__ __forceinline__ bool bar_and(bool v) {
+  uint32_t out;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(out) : "r"(v ? 1u : 0u), "n"(ID), "n"(NTHREADS) : "memory");
+  return out != 0;
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
 // ---------------------------------------------------------------------------
@@ -299,16 +330,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// K-major operand made of 128-row x 64-channel boxes (one per 64 channels):
-// k-step ks of 16 channels starts in box ks/4, 32 B into each row.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int ks) {
-  return sdesc_sw128(tile + (uint32_t)((ks >> 2) * kHalfBytes + (ks & 3) * 32), 16, 1024);
+// K-major operand made of row x 64-channel boxes (one per 64 channels, `box`
+// bytes apart; 128-row boxes by default): k-step ks of 16 channels starts in
+// box ks/4, 32 B into each row.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int ks, uint32_t box = kHalfBytes) {
+  return sdesc_sw128(tile + (uint32_t)((ks >> 2) * box + (ks & 3) * 32), 16, 1024);
 }
 
 // MN-major operand stored as [K rows][MN columns] in the same boxes: k-step
 // ks of 16 rows starts 16 * 128 B further; MN columns 64.. are in the next box.
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int ks) {
-  return sdesc_sw128(tile + (uint32_t)(ks * 2048), kHalfBytes, 1024);
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int ks, uint32_t box = kHalfBytes) {
+  return sdesc_sw128(tile + (uint32_t)(ks * 2048), box, 1024);
 }
 
 // tcgen05.ld, 32 lanes x 32 bit, 32 consecutive columns; waits for completion.

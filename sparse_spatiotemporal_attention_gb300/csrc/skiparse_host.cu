@@ -209,14 +209,15 @@ RopeParams make_rope(const Shape& s, float theta) {
   return r;
 }
 
-bool encode_scope_map(CUtensorMap* m, const void* base, const Geom& g) {
+bool encode_scope_map(CUtensorMap* m, const void* base, const Geom& g, int box_rows = kTile) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t row = (cuuint64_t)g.heads * g.D * 2;
   const cuuint64_t dims[5] = {(cuuint64_t)g.D, (cuuint64_t)g.heads, (cuuint64_t)g.G, (cuuint64_t)g.k,
                               (cuuint64_t)g.B * g.Nn};
   const cuuint64_t strides[4] = {(cuuint64_t)g.D * 2, row, row * g.G, row * g.G * g.k};
-  const cuuint32_t box[5] = {64, 1, (cuuint32_t)g.G, 1, (cuuint32_t)(kTile / g.G)};
+  if (box_rows % g.G != 0) return false;
+  const cuuint32_t box[5] = {64, 1, (cuuint32_t)g.G, 1, (cuuint32_t)(box_rows / g.G)};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -238,7 +239,7 @@ WsLayout ws_layout(const Shape& s) {
   w.Lp = ((L + kTile - 1) / kTile) * kTile;
   const size_t stats = (size_t)s.B * s.heads * s.k * w.Lp;
   size_t off = 0;
-  w.dq_acc = off; off += align256(e * 4);
+  w.dq_acc = off; off += align256(stats * (size_t)s.D * 4);   // scope order (B, heads, k, Lp, D)
   w.qr = off;     off += align256(e * 2);
   w.kr = off;     off += align256(e * 2);
   w.lse2s = off;  off += align256(stats * 4);
@@ -343,7 +344,8 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
     return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
-  if ((size_t)dev.smem_optin < bwd_main_smem_bytes(D)) return SKIPARSE_ERR_UNSUPPORTED;
+  const int G = mode == SKIPARSE_SINGLE ? 1 : sparse_k;
+  if ((size_t)dev.smem_optin < bwd_main_smem_bytes(D, G)) return SKIPARSE_ERR_UNSUPPORTED;
 
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -371,6 +373,9 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   if (!encode_scope_map(&p.tm_q, p.qr, p.g) || !encode_scope_map(&p.tm_k, p.kr, p.g) ||
       !encode_scope_map(&p.tm_v, v, p.g) || !encode_scope_map(&p.tm_do, dout, p.g))
+    return SKIPARSE_ERR_LAUNCH;
+  if (bwd_uses_half_tiles(p.g.D, p.g.G) &&
+      (!encode_scope_map(&p.tm_q64, p.qr, p.g, 64) || !encode_scope_map(&p.tm_do64, dout, p.g, 64)))
     return SKIPARSE_ERR_LAUNCH;
 
   const long long rows = (long long)B * N * heads;

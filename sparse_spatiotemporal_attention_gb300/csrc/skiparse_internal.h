@@ -30,7 +30,8 @@ struct FwdParams {
 };
 
 struct BwdParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // maps over rotated q, rotated k, v, dout
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // maps over rotated q, rotated k, v, dout (128-row boxes)
+  CUtensorMap tm_q64, tm_do64;           // rotated q and dout with 64-row boxes (query halves)
   Geom g;
   RopeParams rope;
   const uint16_t* q;       // pre-RoPE inputs
@@ -40,7 +41,7 @@ struct BwdParams {
   const float* lse;
   uint16_t* qr;            // workspace: rotated q, bf16 (B, N, heads, D)
   uint16_t* kr;            // workspace: rotated k
-  float* dq_acc;           // workspace: fp32 (B, N, heads, D)
+  float* dq_acc;           // workspace: fp32 (B, heads, k, Lp, D), scope order
   float* lse2s;            // workspace: lse * log2(e), scope order (B, heads, k, Lp)
   float* delta_s;          // workspace: rowsum(dO * O), scope order (B, heads, k, Lp)
   float2* rope_tab;        // workspace: cos/sin table
@@ -67,7 +68,8 @@ struct DebugParams {
 size_t fwd_smem_bytes(int D, int rope_entries);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
 
-size_t bwd_main_smem_bytes(int D);
+size_t bwd_main_smem_bytes(int D, int G);
+bool bwd_uses_half_tiles(int D, int G);
 cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdParams& p, int grid, cudaStream_t stream);
