@@ -25,16 +25,44 @@ constexpr int kMaxRopeEntries = 8192;       // cos/sin pairs of the RoPE table
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s per bounded wait
 
 // ---------------------------------------------------------------------------
+// Division by a runtime constant d >= 1 for 0 <= n < 2^31, by multiply-high:
+// n / d = (n * m) >> (32 + s) with s = ceil(log2 d) and m = floor(2^(32+s) / d) + 1
+// (m <= 2^33, so for n < 2^31 the product n * m fits in 64 bits).
+// ---------------------------------------------------------------------------
+struct FastDiv {
+  unsigned long long m;
+  int s;
+  int d;
+};
+
+inline FastDiv make_fastdiv(int d) {
+  FastDiv f;
+  f.d = d;
+  int s = 0;
+  while ((1ll << s) < d) ++s;
+  f.s = s;
+  f.m = (unsigned long long)((((unsigned __int128)1) << (32 + s)) / (unsigned)d) + 1ull;
+  return f;
+}
+
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  return (int)(((unsigned long long)(unsigned)n * f.m) >> (32 + f.s));
+}
+
+// ---------------------------------------------------------------------------
 // Geometry and RoPE parameters (plain structs, passed inside kernel params)
 // ---------------------------------------------------------------------------
 
 struct Geom {
   int B, heads, N, D;
   int k;        // sparse_k: number of scopes
-  int G;        // group size: 1 (single skip) or k (group skip)
+  int G;        // group size: 1 (single skip) or k (group skip); always a power of two
+  int lgG;      // log2(G)
   int L;        // scope length N / k
   int Nn;       // L / G: rows of the merged (n, b) tensor-map dimension per batch
   int n_tiles;  // ceil(L / 128)
+  FastDiv fk;   // division by k
+  FastDiv fkG;  // division by k * G
 };
 
 struct RopeParams {
@@ -43,22 +71,24 @@ struct RopeParams {
   int T, H, W;
   int dt2, dh2;       // pairs per chunk: D/8 and 3D/16
   int entries;        // T*dt2 + H*dh2 + W*dh2
+  FastDiv fHW;        // division by H*W
+  FastDiv fW;         // division by W
 };
 
 __device__ __forceinline__ int token_of(const Geom& g, int s, int p) {
-  return (p / g.G) * (g.k * g.G) + s * g.G + (p % g.G);
+  return ((p >> g.lgG) * g.k << g.lgG) + (s << g.lgG) + (p & (g.G - 1));
 }
 
 __device__ __forceinline__ void scope_pos_of(const Geom& g, int i, int& s, int& p) {
-  s = (i / g.G) % g.k;
-  p = (i / (g.k * g.G)) * g.G + (i % g.G);
+  const int ig = i >> g.lgG;                     // i / G
+  s = ig - fdiv(ig, g.fk) * g.k;                 // (i / G) mod k
+  p = (fdiv(i, g.fkG) << g.lgG) + (i & (g.G - 1));
 }
 
 __device__ __forceinline__ void token_coords(const RopeParams& r, int i, int& t, int& h, int& w) {
-  const int hw = r.H * r.W;
-  t = i / hw;
-  const int rem = i - t * hw;
-  h = rem / r.W;
+  t = fdiv(i, r.fHW);
+  const int rem = i - t * r.fHW.d;
+  h = fdiv(rem, r.fW);
   w = rem - h * r.W;
 }
 
@@ -369,6 +399,29 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+
+// tcgen05.ld, 32 lanes x 32 bit, 16 consecutive columns; waits for completion.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr) : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tcgen05.st, 32 lanes x 32 bit, 16 consecutive columns of floats (no wait).
+__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float (&v)[16]) {
+  uint32_t r[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i]);
+  tmem_st16(taddr, r);
+}
+
 
 // tcgen05.st, 32 lanes x 32 bit, 32 consecutive columns (no wait).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {

@@ -304,13 +304,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
         for (int c = 0; c < 4; ++c)
           tmem_ld32(tmem + lane_base + st * 128 + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
         const int valid = min(kTile, g.L - j * kTile);
-        float mx = -INFINITY;
+        if (valid < kTile) {
 #pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          if (e >= valid) sv[e] = -INFINITY;
-          mx = fmaxf(mx, sv[e]);
+          for (int e = 0; e < 128; ++e)
+            if (e >= valid) sv[e] = -INFINITY;
         }
-        mx *= sl2;
+        // row max as a 4-way tree (short dependency chains)
+        float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+        for (int e = 4; e < 128; e += 4) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) m4[q] = fmaxf(m4[q], sv[e + q]);
+        }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
         if (j == 0) {
           m = mx;
         } else {
@@ -324,17 +330,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
             const float f = ex2(m - m_new);
             m = m_new;
             l *= f;
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              float o[16];
+              tmem_ld16(tmem + lane_base + kColO + c * 16, o);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              float o[32];
-              tmem_ld32(tmem + lane_base + kColO + c * 32, o);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= f;
-              tmem_st32(tmem + lane_base + kColO + c * 32, o);
+              for (int e = 0; e < 16; ++e) o[e] *= f;
+              tmem_st16f(tmem + lane_base + kColO + c * 16, o);
             }
             tmem_st_wait();
           }
         }
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -342,11 +349,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
           for (int e = 0; e < 16; ++e) {
             const float a = ex2(fmaf(sv[c * 32 + 2 * e], sl2, -m));
             const float bb = ex2(fmaf(sv[c * 32 + 2 * e + 1], sl2, -m));
-            l += a + bb;
+            l4[(2 * e) & 3] += a;
+            l4[(2 * e + 1) & 3] += bb;
             pk[e] = pack_bf16(a, bb);
           }
           tmem_st16(tmem + lane_base + st * 128 + c * 16, pk);
         }
+        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -354,7 +363,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       }
       if (!ok) break;
       // ---- epilogue: O / l to the token's original row, LSE in natural log
+      // A parity wait is only unambiguous one phase ahead: S_glast being done
+      // proves P V up to glast-2 has completed, so wait for glast-1, then glast.
       const uint32_t glast = g0 + g.n_tiles - 1;
+      if (g.n_tiles >= 2 && !mbar_wait(bar(F_ODONE), (glast - 1) & 1, ctl, ERR_KERNEL_FWD + F_ODONE)) break;
       if (!mbar_wait(bar(F_ODONE), glast & 1, ctl, ERR_KERNEL_FWD + F_ODONE)) break;
       tc_fence_after();
       const int prow = tile * kTile + r;

@@ -188,6 +188,10 @@ Geom make_geom(const Shape& s) {
   g.D = s.D;
   g.k = s.k;
   g.G = s.mode == SKIPARSE_SINGLE ? 1 : s.k;
+  g.lgG = 0;
+  while ((1 << g.lgG) < g.G) ++g.lgG;
+  g.fk = make_fastdiv(s.k);
+  g.fkG = make_fastdiv(s.k * g.G);
   g.L = s.N / s.k;
   g.Nn = g.L / g.G;
   g.n_tiles = (g.L + kTile - 1) / kTile;
@@ -204,6 +208,8 @@ RopeParams make_rope(const Shape& s, float theta) {
   r.dt2 = dt / 2;
   r.dh2 = dh / 2;
   r.entries = s.rope_entries;
+  r.fHW = make_fastdiv(s.H * s.W > 0 ? s.H * s.W : 1);
+  r.fW = make_fastdiv(s.W > 0 ? s.W : 1);
   for (int j = 0; j < r.dt2; ++j) r.om_t[j] = std::pow((double)theta, -2.0 * j / dt);
   for (int j = 0; j < r.dh2; ++j) r.om_hw[j] = std::pow((double)theta, -2.0 * j / dh);
   return r;
@@ -398,6 +404,7 @@ int skiparse_debug_index_map(int* scope_of_token, int* pos_of_token, int N, int 
   if (N % sparse_k != 0) return SKIPARSE_ERR_SHAPE;
   if (mode == SKIPARSE_GROUP && ((long long)sparse_k * sparse_k > N || N % (sparse_k * sparse_k) != 0))
     return SKIPARSE_ERR_SHAPE;
+  if (mode == SKIPARSE_GROUP && 128 % sparse_k != 0) return SKIPARSE_ERR_UNSUPPORTED;
   if (any_alias({{scope_of_token, (size_t)N * 4}, {pos_of_token, (size_t)N * 4}}, {})) return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   int st = device_info(dev);
