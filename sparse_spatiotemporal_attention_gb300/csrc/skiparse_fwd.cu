@@ -8,16 +8,23 @@
 // address the scope's rows directly (see skiparse_host.cu), and the epilogue
 // stores each output row at its original token index.
 //
-// One work unit = (b, head, s, 128-row Q tile). Warp roles of a CTA:
-//   warps 0-3  softmax: one query row per thread (TMEM lane), online softmax
-//              with lazy O rescaling, P written back to TMEM as bf16, final
-//              O / l and LSE stores;
-//   warps 4-7  RoPE: rotate each Q and K tile in shared memory after TMA lands it
-//              (16-byte chunks, per-row table offsets staged in shared memory);
-//   warp  8    TMA producer: Q tile, then a 2-stage K / V ring;
-//   warp  9    MMA issuer: S = Q K^T (smem x smem) and O += P V (TMEM x smem),
-//              tcgen05.mma kind::f16, fp32 accumulators in TMEM.
-// TMEM columns: S/P buffer 0 at 0, S/P buffer 1 at 128, O at 256.
+// One work unit = (b, head, s, a pair of 128-row Q tiles A and B), so every
+// K / V tile is loaded and rotated once for 256 query rows. Warp roles:
+//   warps 0-3   softmax for Q tile A, one query row per thread (TMEM lane);
+//   warps 4-7   softmax for Q tile B;
+//   warps 8-11  RoPE: rotate the Q tiles and each K tile in shared memory
+//               (16-byte chunks, per-row table offsets staged in shared memory);
+//   warp  12    TMA producer: Q pair, then a 2-stage K / V ring;
+//   warp  13    MMA issuer (tcgen05.mma kind::f16, fp32 accumulators in TMEM).
+// TMEM columns: S_A / P_A 0..127, S_B / P_B 128..255, O_A 256.., O_B 384...
+// MMA issue order: S_A(g), S_B(g), PV_A(g), S_A(g+1), PV_B(g), S_B(g+1), ...
+// so each softmax warpgroup's critical loop is softmax + two MMA groups while
+// the tensor core alternates between the two Q tiles. Because S_X(g) is issued
+// after PV_X(g-1), the S-full barrier of tile g proves PV_X(g-1) complete, which
+// keeps every parity wait on the O-done barriers one phase ahead at most.
+// The softmax reads S twice from TMEM (max pass, then exp pass) so that all 14
+// warps fit in 128 registers; online softmax with lazy O rescaling (threshold
+// 2^8), P written back over S as bf16.
 #include "skiparse_internal.h"
 
 namespace skp {
@@ -27,8 +34,9 @@ struct FwdLayout {
   static constexpr int HALVES = D / 64;
   static constexpr int TILE = 128 * D * 2;
   static constexpr int HDR = 1024;
-  static constexpr int Q_OFF = HDR;
-  static constexpr int K_OFF = Q_OFF + TILE;
+  static constexpr int QA_OFF = HDR;
+  static constexpr int QB_OFF = QA_OFF + TILE;
+  static constexpr int K_OFF = QB_OFF + TILE;
   static constexpr int V_OFF = K_OFF + 2 * TILE;
   static constexpr int ROWOFF_OFF = V_OFF + 2 * TILE;   // [2][128] int4 per-row RoPE table offsets
   static constexpr int ROPE_OFF = ROWOFF_OFF + 2 * 128 * 16;
@@ -38,15 +46,14 @@ enum FwdBar {
   F_QFULL, F_QROT, F_QEMPTY,
   F_KFULL0, F_KFULL1, F_KROT0, F_KROT1, F_KEMPTY0, F_KEMPTY1,
   F_VFULL0, F_VFULL1, F_VEMPTY0, F_VEMPTY1,
-  F_SFULL0, F_SFULL1, F_PFULL0, F_PFULL1, F_ODONE, F_OEMPTY, F_FINAL, F_NBARS
+  F_SFULL_A, F_SFULL_B, F_PFULL_A, F_PFULL_B, F_ODONE_A, F_ODONE_B, F_OEMPTY_A, F_OEMPTY_B, F_FINAL, F_NBARS
 };
 
-constexpr int kFwdThreads = 320;
-constexpr uint32_t kColO = 256;
+constexpr int kFwdThreads = 448;
 
-__device__ __forceinline__ void decode_unit(const Geom& g, int u, int& b, int& head, int& s, int& tile) {
-  tile = u % g.n_tiles;
-  int r = u / g.n_tiles;
+__device__ __forceinline__ void decode_unit(const Geom& g, int n_pairs, int u, int& b, int& head, int& s, int& pair) {
+  pair = u % n_pairs;
+  int r = u / n_pairs;
   s = r % g.k;
   r /= g.k;
   head = r % g.heads;
@@ -120,7 +127,7 @@ __device__ __forceinline__ bool rope_tile(uint8_t* tile, int4* rowoff, int p0, i
 }
 
 template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_constant__ FwdParams p) {
   using Ly = FwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -135,28 +142,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
   int* abort_flag = reinterpret_cast<int*>(smem + 520);
   float2* tab = reinterpret_cast<float2*>(smem + Ly::ROPE_OFF);
   int4* rowoff = reinterpret_cast<int4*>(smem + Ly::ROWOFF_OFF);
-  const uint32_t sQ = smem_u32(smem + Ly::Q_OFF);
+  const uint32_t sQA = smem_u32(smem + Ly::QA_OFF);
+  const uint32_t sQB = smem_u32(smem + Ly::QB_OFF);
   const uint32_t sK = smem_u32(smem + Ly::K_OFF);
   const uint32_t sV = smem_u32(smem + Ly::V_OFF);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   const Ctl ctl{abort_flag, p.err};
   const Geom& g = p.g;
+  const int n_pairs = (g.n_tiles + 1) >> 1;
 
   if (tid == 0) {
     *abort_flag = 0;
-    const uint32_t counts[F_NBARS] = {1, 4, 1, 1, 1, 4, 4, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 4, 1};
+    const uint32_t counts[F_NBARS] = {1, 4, 1, 1, 1, 4, 4, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 4, 4, 1};
     for (int i = 0; i < F_NBARS; ++i) mbar_init(bar(i), counts[i]);
     mbar_fence_init();
   }
-  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == 13) tmem_alloc(smem_u32(tmem_slot), 512);
   rope_build_table(tab, p.rope, tid, kFwdThreads);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_map(&p.tm_q);
@@ -167,14 +176,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-        int b, head, s, tile;
-        decode_unit(g, u, b, head, s, tile);
+        int b, head, s, pair;
+        decode_unit(g, n_pairs, u, b, head, s, pair);
         if (it > 0 && !mbar_wait(bar(F_QEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_QEMPTY)) break;
-        mbar_expect_tx(bar(F_QFULL), Ly::TILE);
-        const int qrow = b * g.Nn + (tile * kTile) / g.G;
+        mbar_expect_tx(bar(F_QFULL), 2 * Ly::TILE);
+        const int qrow = b * g.Nn + (2 * pair * kTile) / g.G;
 #pragma unroll
-        for (int h = 0; h < Ly::HALVES; ++h)
-          tma_load_5d(sQ + h * kHalfBytes, &p.tm_q, bar(F_QFULL), h * 64, head, 0, s, qrow);
+        for (int h = 0; h < Ly::HALVES; ++h) {
+          tma_load_5d(sQA + h * kHalfBytes, &p.tm_q, bar(F_QFULL), h * 64, head, 0, s, qrow);
+          tma_load_5d(sQB + h * kHalfBytes, &p.tm_q, bar(F_QFULL), h * 64, head, 0, s, qrow + kTile / g.G);
+        }
         ++q_issued;
         for (int j = 0; j < g.n_tiles; ++j) {
           const uint32_t gg = gk + j;
@@ -203,7 +214,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
         if (v_issued[st]) mbar_drain(bar(F_VFULL0 + st), (v_issued[st] - 1) & 1);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
@@ -211,58 +222,86 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       uint32_t g0 = 0;
       int it = 0;
       bool ok = true;
-      // O += P_j V_j for global tile index gg (local index j of unit number it).
-      auto issue_pv = [&](uint32_t gg, int j) -> bool {
-        const int st = gg & 1;
-        const uint32_t n = gg >> 1;
-        if (j == 0 && it > 0 && !mbar_wait(bar(F_OEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_OEMPTY)) return false;
-        if (!mbar_wait(bar(F_PFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_PFULL0 + st)) return false;
-        if (!mbar_wait(bar(F_VFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_VFULL0 + st)) return false;
-        tc_fence_after();
+      // S_X = Q_X K_g^T into TMEM columns colS (X = A: 0, B: 128)
+      auto issue_s = [&](uint32_t qt, uint32_t colS, int st) {
+        const uint32_t kt = sK + st * Ly::TILE;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + colS, desc_kmajor(qt, ks), desc_kmajor(kt, ks), kIdS, ks > 0 ? 1u : 0u);
+      };
+      // O_X += P_X V_g, P_X in TMEM over S_X
+      auto issue_pv = [&](uint32_t colS, uint32_t colO, int st, bool first) {
         const uint32_t vt = sV + st * Ly::TILE;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tmem + kColO, tmem + st * 128 + ks * 8, desc_mnmajor(vt, ks), kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(bar(F_ODONE));
-        tc_commit(bar(F_VEMPTY0 + st));
-        return true;
+          mma_ts(tmem + colO, tmem + colS + ks * 8, desc_mnmajor(vt, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
       };
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+        const int n = g.n_tiles;
         if (!mbar_wait(bar(F_QROT), it & 1, ctl, ERR_KERNEL_FWD + F_QROT)) break;
+        if (!mbar_wait(bar(F_KROT0 + (g0 & 1)), (g0 >> 1) & 1, ctl, ERR_KERNEL_FWD + F_KROT0)) break;
         tc_fence_after();
-        for (int j = 0; j < g.n_tiles; ++j) {
+        issue_s(sQA, 0, g0 & 1);
+        tc_commit(bar(F_SFULL_A));
+        issue_s(sQB, 128, g0 & 1);
+        tc_commit(bar(F_SFULL_B));
+        tc_commit(bar(F_KEMPTY0 + (g0 & 1)));
+        if (n == 1) tc_commit(bar(F_QEMPTY));
+        for (int j = 0; j < n; ++j) {
           const uint32_t gg = g0 + j;
           const int st = gg & 1;
-          const uint32_t n = gg >> 1;
-          if (!mbar_wait(bar(F_KROT0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_KROT0 + st)) { ok = false; break; }
+          const uint32_t nn = gg >> 1;
+          // PV_A(g)
+          if (j == 0 && it > 0 && !mbar_wait(bar(F_OEMPTY_A), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_OEMPTY_A)) { ok = false; break; }
+          if (!mbar_wait(bar(F_PFULL_A), gg & 1, ctl, ERR_KERNEL_FWD + F_PFULL_A)) { ok = false; break; }
+          if (!mbar_wait(bar(F_VFULL0 + st), nn & 1, ctl, ERR_KERNEL_FWD + F_VFULL0 + st)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kt = sK + st * Ly::TILE;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tmem + st * 128, desc_kmajor(sQ, ks), desc_kmajor(kt, ks), kIdS, ks > 0 ? 1u : 0u);
-          tc_commit(bar(F_SFULL0 + st));
-          tc_commit(bar(F_KEMPTY0 + st));
-          if (j == g.n_tiles - 1) tc_commit(bar(F_QEMPTY));
-          if (j >= 1 && !issue_pv(gg - 1, j - 1)) { ok = false; break; }
+          issue_pv(0, 256, st, j == 0);
+          tc_commit(bar(F_ODONE_A));
+          // S_A(g+1)
+          const bool more = j + 1 < n;
+          if (more) {
+            const int st1 = (gg + 1) & 1;
+            if (!mbar_wait(bar(F_KROT0 + st1), ((gg + 1) >> 1) & 1, ctl, ERR_KERNEL_FWD + F_KROT0 + st1)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(sQA, 0, st1);
+            tc_commit(bar(F_SFULL_A));
+          }
+          // PV_B(g)
+          if (j == 0 && it > 0 && !mbar_wait(bar(F_OEMPTY_B), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_OEMPTY_B)) { ok = false; break; }
+          if (!mbar_wait(bar(F_PFULL_B), gg & 1, ctl, ERR_KERNEL_FWD + F_PFULL_B)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(128, 256 + D, st, j == 0);
+          tc_commit(bar(F_ODONE_B));
+          tc_commit(bar(F_VEMPTY0 + st));
+          // S_B(g+1)
+          if (more) {
+            const int st1 = (gg + 1) & 1;
+            issue_s(sQB, 128, st1);
+            tc_commit(bar(F_SFULL_B));
+            tc_commit(bar(F_KEMPTY0 + st1));
+            if (j + 2 == n) tc_commit(bar(F_QEMPTY));
+          }
         }
-        if (!ok) break;
-        if (!issue_pv(g0 + g.n_tiles - 1, g.n_tiles - 1)) break;
-        g0 += g.n_tiles;
+        g0 += n;
       }
       tc_commit(bar(F_FINAL));
       mbar_drain(bar(F_FINAL), 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 8) {
     // ------------------------------------------------------------ RoPE warps
-    const int rtid = tid - 128;
+    const int rtid = tid - 256;
     uint32_t gk = 0, ntile = 0;
     int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-      int b, head, s, tile;
-      decode_unit(g, u, b, head, s, tile);
+      int b, head, s, pair;
+      decode_unit(g, n_pairs, u, b, head, s, pair);
       ok = mbar_wait(bar(F_QFULL), it & 1, ctl, ERR_KERNEL_FWD + F_QFULL);
-      ok = rope_tile<D>(smem + Ly::Q_OFF, rowoff + (ntile++ & 1) * 128, tile * kTile, s, g, p.rope, tab, rtid, lane, ok);
+      ok = rope_tile<D>(smem + Ly::QA_OFF, rowoff + (ntile++ & 1) * 128, 2 * pair * kTile, s, g, p.rope, tab, rtid, lane, ok);
+      if (!ok) break;
+      ok = rope_tile<D>(smem + Ly::QB_OFF, rowoff + (ntile++ & 1) * 128, (2 * pair + 1) * kTile, s, g, p.rope, tab, rtid,
+                        lane, ok);
       if (!ok) break;
       fence_proxy_async_smem();
       __syncwarp();
@@ -282,39 +321,41 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       gk += g.n_tiles;
     }
   } else {
-    // ------------------------------------------------------------ softmax warps
-    const int r = tid;                                  // query row of the tile = TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax warps (A: 0-3, B: 4-7)
+    const int wg = warp >> 2;                              // 0 = Q tile A, 1 = Q tile B
+    const int r = tid & 127;                               // query row of the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t colS = wg ? 128u : 0u;
+    const uint32_t colO = 256u + (wg ? (uint32_t)D : 0u);
+    const int barS = wg ? F_SFULL_B : F_SFULL_A;
+    const int barP = wg ? F_PFULL_B : F_PFULL_A;
+    const int barO = wg ? F_ODONE_B : F_ODONE_A;
+    const int barOE = wg ? F_OEMPTY_B : F_OEMPTY_A;
     const float sl2 = p.scale_log2;
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-      int b, head, s, tile;
-      decode_unit(g, u, b, head, s, tile);
+      int b, head, s, pair;
+      decode_unit(g, n_pairs, u, b, head, s, pair);
+      const int tile = 2 * pair + wg;
       float m = 0.f, l = 0.f;
       for (int j = 0; j < g.n_tiles; ++j) {
         const uint32_t gg = g0 + j;
-        const int st = gg & 1;
-        const uint32_t n = gg >> 1;
-        if (!mbar_wait(bar(F_SFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_SFULL0 + st)) { ok = false; break; }
+        if (!mbar_wait(bar(barS), gg & 1, ctl, ERR_KERNEL_FWD + barS)) { ok = false; break; }
         tc_fence_after();
-        float sv[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tmem + lane_base + st * 128 + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
         const int valid = min(kTile, g.L - j * kTile);
-        if (valid < kTile) {
+        // pass 1: row max
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int e = 0; e < 128; ++e)
-            if (e >= valid) sv[e] = -INFINITY;
-        }
-        // row max as a 4-way tree (short dependency chains)
-        float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tmem_ld32(tmem + lane_base + colS + c * 32, x);
 #pragma unroll
-        for (int e = 4; e < 128; e += 4) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) m4[q] = fmaxf(m4[q], sv[e + q]);
+          for (int e = 0; e < 32; ++e) {
+            const float v = (c * 32 + e < valid) ? x[e] : -INFINITY;
+            m4[e & 3] = fmaxf(m4[e & 3], v);
+          }
         }
         const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
         if (j == 0) {
@@ -322,9 +363,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
         } else {
           const bool need = mx > m + 8.0f;
           if (__any_sync(0xffffffffu, need)) {
-            // O holds sum over earlier tiles against the old reference max:
-            // wait until the last P V landed, then rescale O in TMEM.
-            if (!mbar_wait(bar(F_ODONE), (gg - 1) & 1, ctl, ERR_KERNEL_FWD + F_ODONE)) { ok = false; break; }
+            // S_X(g) was issued after PV_X(g-1), so that P V is already complete;
+            // the wait only orders this thread after it.
+            if (!mbar_wait(bar(barO), (gg - 1) & 1, ctl, ERR_KERNEL_FWD + barO)) { ok = false; break; }
             tc_fence_after();
             const float m_new = need ? mx : m;
             const float f = ex2(m - m_new);
@@ -333,41 +374,42 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
 #pragma unroll 1
             for (int c = 0; c < D / 16; ++c) {
               float o[16];
-              tmem_ld16(tmem + lane_base + kColO + c * 16, o);
+              tmem_ld16(tmem + lane_base + colO + c * 16, o);
 #pragma unroll
               for (int e = 0; e < 16; ++e) o[e] *= f;
-              tmem_st16f(tmem + lane_base + kColO + c * 16, o);
+              tmem_st16f(tmem + lane_base + colO + c * 16, o);
             }
             tmem_st_wait();
           }
         }
+        // pass 2: P = 2^(S * scale * log2 e - m) as bf16 over the S columns already read
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tmem_ld32(tmem + lane_base + colS + c * 32, x);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float a = ex2(fmaf(sv[c * 32 + 2 * e], sl2, -m));
-            const float bb = ex2(fmaf(sv[c * 32 + 2 * e + 1], sl2, -m));
+            const float a = (c * 32 + 2 * e < valid) ? ex2(fmaf(x[2 * e], sl2, -m)) : 0.f;
+            const float bb = (c * 32 + 2 * e + 1 < valid) ? ex2(fmaf(x[2 * e + 1], sl2, -m)) : 0.f;
             l4[(2 * e) & 3] += a;
             l4[(2 * e + 1) & 3] += bb;
             pk[e] = pack_bf16(a, bb);
           }
-          tmem_st16(tmem + lane_base + st * 128 + c * 16, pk);
+          tmem_st16(tmem + lane_base + colS + c * 16, pk);
         }
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(F_PFULL0 + st));
+        if (lane == 0) mbar_arrive(bar(barP));
       }
       if (!ok) break;
-      // ---- epilogue: O / l to the token's original row, LSE in natural log
-      // A parity wait is only unambiguous one phase ahead: S_glast being done
-      // proves P V up to glast-2 has completed, so wait for glast-1, then glast.
+      // ---- epilogue: O / l to the token's original row, LSE in natural log.
+      // S_X(glast) proved PV_X(glast-1) complete, so one parity wait suffices.
       const uint32_t glast = g0 + g.n_tiles - 1;
-      if (g.n_tiles >= 2 && !mbar_wait(bar(F_ODONE), (glast - 1) & 1, ctl, ERR_KERNEL_FWD + F_ODONE)) break;
-      if (!mbar_wait(bar(F_ODONE), glast & 1, ctl, ERR_KERNEL_FWD + F_ODONE)) break;
+      if (!mbar_wait(bar(barO), glast & 1, ctl, ERR_KERNEL_FWD + barO)) break;
       tc_fence_after();
       const int prow = tile * kTile + r;
       const bool row_ok = prow < g.L;
@@ -377,7 +419,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
-        tmem_ld32(tmem + lane_base + kColO + c * 32, o);
+        tmem_ld32(tmem + lane_base + colO + c * 32, o);
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -394,14 +436,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       if (row_ok) p.lse[((size_t)b * g.heads + head) * g.N + tok] = (m + log2f(l)) * 0.6931471805599453f;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(F_OEMPTY));
+      if (lane == 0) mbar_arrive(bar(barOE));
       g0 += g.n_tiles;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -411,6 +453,8 @@ size_t fwd_smem_bytes(int D, int rope_entries) {
   const size_t base = (D == 128) ? FwdLayout<128>::ROPE_OFF : FwdLayout<64>::ROPE_OFF;
   return base + (size_t)rope_entries * sizeof(float2);
 }
+
+int fwd_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 2); }
 
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
   const size_t smem = fwd_smem_bytes(p.g.D, p.rope.entries);

@@ -318,7 +318,7 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.err = dev.err_word;
-  p.n_units = B * heads * sparse_k * p.g.n_tiles;
+  p.n_units = fwd_units(p.g);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
   return launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));

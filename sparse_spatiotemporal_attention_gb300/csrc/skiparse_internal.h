@@ -25,7 +25,7 @@ struct FwdParams {
   uint16_t* out;                  // bf16 (B, N, heads, D)
   float* lse;                     // (B, heads, N)
   int* err;                       // device error word
-  int n_units;                    // B * heads * k * n_tiles
+  int n_units;                    // B * heads * k * ceil(n_tiles / 2): pairs of Q tiles
   float scale_log2;               // log2(e) / sqrt(D)
 };
 
@@ -66,6 +66,7 @@ struct DebugParams {
 
 // Shared-memory bytes and launch helpers (defined next to each kernel).
 size_t fwd_smem_bytes(int D, int rope_entries);
+int fwd_units(const Geom& g);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
 
 size_t bwd_main_smem_bytes(int D, int G);
