@@ -345,16 +345,23 @@ __global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_const
         if (!mbar_wait(bar(barS), gg & 1, ctl, ERR_KERNEL_FWD + barS)) { ok = false; break; }
         tc_fence_after();
         const int valid = min(kTile, g.L - j * kTile);
-        // pass 1: row max
+        // pass 1: row max (keys at or past `valid` only exist in the scope's last tile)
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (valid == kTile) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tmem_ld32(tmem + lane_base + colS + c * 32, x);
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + colS + c * 32, x);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float v = (c * 32 + e < valid) ? x[e] : -INFINITY;
-            m4[e & 3] = fmaxf(m4[e & 3], v);
+            for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], x[e]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            tmem_ld32(tmem + lane_base + colS + c * 32, x);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], (c * 32 + e < valid) ? x[e] : -INFINITY);
           }
         }
         const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
@@ -382,8 +389,11 @@ __global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_const
             tmem_st_wait();
           }
         }
-        // pass 2: P = 2^(S * scale * log2 e - m) as bf16 over the S columns already read
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        // pass 2: P = 2^(S * scale * log2 e - m) as bf16 over the S columns already
+        // read; the exponent argument and the row sum use packed two-lane fp32.
+        const unsigned long long sl2x2 = f2_pack(sl2, sl2);
+        const unsigned long long negm2 = f2_pack(-m, -m);
+        unsigned long long acc2[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float x[32];
@@ -391,15 +401,24 @@ __global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_const
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float a = (c * 32 + 2 * e < valid) ? ex2(fmaf(x[2 * e], sl2, -m)) : 0.f;
-            const float bb = (c * 32 + 2 * e + 1 < valid) ? ex2(fmaf(x[2 * e + 1], sl2, -m)) : 0.f;
-            l4[(2 * e) & 3] += a;
-            l4[(2 * e + 1) & 3] += bb;
+            float t0, t1;
+            f2_unpack(ffma2(f2_pack(x[2 * e], x[2 * e + 1]), sl2x2, negm2), t0, t1);
+            float a = ex2(t0), bb = ex2(t1);
+            if (valid < kTile) {
+              a = (c * 32 + 2 * e < valid) ? a : 0.f;
+              bb = (c * 32 + 2 * e + 1 < valid) ? bb : 0.f;
+            }
+            acc2[e & 1] = fadd2(acc2[e & 1], f2_pack(a, bb));
             pk[e] = pack_bf16(a, bb);
           }
           tmem_st16(tmem + lane_base + colS + c * 16, pk);
         }
-        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        {
+          float s0, s1, s2, s3;
+          f2_unpack(acc2[0], s0, s1);
+          f2_unpack(acc2[1], s2, s3);
+          l += (s0 + s1) + (s2 + s3);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
