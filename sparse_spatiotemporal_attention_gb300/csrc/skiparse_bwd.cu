@@ -13,14 +13,19 @@
 //                S^T  = K~ Q~^T          dP^T = V dO^T
 //                dV  += P^T dO           dK~ += dS^T Q~          dQ~_part = dS K~
 //              P^T = exp(S^T * scale - lse), dS^T = P^T * (dP^T - delta).
-//              dQ~_part is added into the fp32 accumulator with vector atomics.
+//              dQ~_part is added into the fp32 accumulator (scope order) with
+//              fire-and-forget reduction stores to L2.
 //              Epilogue: dv, and dk = scale * R^T dK~, stored at original rows.
 //  post        dq = R^T (scale * dQ~_acc) -> bf16.
-// Warp roles of the main kernel:
-//   warps 0-3  one key row per thread: P^T, dS^T, and the dK / dV epilogue;
-//   warps 4-7  one query row per thread: dQ~ partial -> fp32 atomics;
-//   warp  8    TMA producer (K~, V per unit; Q~, dO, lse, delta per Q tile);
-//   warp  9    MMA issuer.
+// Two main kernels share that plan. D = 128 (the 18-warp tile kernel):
+//   warps 0-7   P^T / dS^T in four 32-query chunks (one key row, 16 queries of
+//               a chunk per thread) and the dK / dV epilogue;
+//   warps 8-15  dQ~^T out of TMEM (one channel, 64 queries per thread) and its
+//               coalesced adds into the accumulator;
+//   warp 16     TMA producer (K~, V per unit; Q~, dO, lse, delta per Q tile);
+//   warp 17     MMA issuer; every MMA has M = N = 128.
+// D = 64 (the 10-warp kernel): warps 0-3 P^T / dS^T and the epilogue, warps
+// 4-7 one query row each for the dQ~ adds (vector atomics), warp 8 TMA, warp 9 MMA.
 // TMEM columns: S^T (P^T as bf16) 0..127, dP^T / dQ~ partial 128..255,
 // dV 256..383, dK~ 384..511.
 #include "skiparse_internal.h"
@@ -146,7 +151,7 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __
 }
 
 // ===========================================================================
-// main kernel
+// main kernel for D = 64: 128-query tiles, dQ~ added by four of its warps
 // ===========================================================================
 
 template <int D>
@@ -460,45 +465,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
 }
 
 // ===========================================================================
-// main kernel for D = 128: query half-tiles of 64 rows through two TMEM slots
+// main kernel for D = 128: full 128-query tiles, dQ drained by its own warps
 // ===========================================================================
 //
-// Work unit as above (b, head, scope, 128-key tile); the scope's queries are
-// taken 64 at a time ("halves"). Half h uses TMEM slot h mod 2 (128 columns:
-// S^T / P^T in the first 64, dP^T then dQ~^T in the second 64) and dS^T buffer
-// h mod 2, so the P^T / dS^T warps work on one half while the tensor core runs
-// the other half's MMAs. Per half:
-//   MMA1: S^T = K~ Q~_h^T, dP^T = V dO_h^T                  (M=128 keys, N=64)
-//   MMA2: dV += P^T dO_h, dK~ += dS^T Q~_h                   (N=128, K=64)
-//         dQ~_h^T = K~^T dS^T_h                              (M=128 channels, N=64)
-// Issue order: MMA1(h), MMA2(h-1), MMA1(h+1), ... The dQ warps copy dQ~_h^T
-// (one channel per thread) into a 64 x 128 fp32 staging tile in shared memory
-// and one thread adds the whole tile to the scope-order accumulator with a
-// single bulk reduce (cp.reduce.async.bulk .add.f32, 32 KB), so no thread
-// issues per-element atomics.
-struct BwdHalfLayout {
-  static constexpr int TILE = 128 * 128 * 2;        // K~ or V tile: two 16 KB boxes
-  static constexpr int HBOX = 64 * 128;             // 64-row x 64-channel box
-  static constexpr int HTILE = 2 * HBOX;            // 64 rows x 128 channels
-  static constexpr int STAGE = 2 * HTILE;           // Q~ half, then dO half
-  static constexpr int NSTAGE = 3;
-  static constexpr int STATS_OFF = 1024;            // [3][lse2 x64 | delta x64] fp32
-  static constexpr int K_OFF = 3072;
-  static constexpr int V_OFF = K_OFF + TILE;
-  static constexpr int Q_OFF = V_OFF + TILE;
-  static constexpr int DS_OFF = Q_OFF + NSTAGE * STAGE;     // 2 x 16 KB: [128 keys][64 queries] bf16
-  static constexpr int DQ_OFF = DS_OFF + 2 * 16384;         // 64 x 128 fp32 staging
-  static constexpr int BYTES = DQ_OFF + 64 * 128 * 4;
+// Every MMA has M = N = 128 (40 tcgen05.mma per key-tile x query-tile pair).
+// Per query tile i:
+//   MMA1:  S^T = K~ Q~_i^T -> TMEM 0..127, dP^T = V dO_i^T -> TMEM 128..255
+//   warps 0-7 form P^T / dS^T in four chunks of 32 queries; after chunk c
+//          the tensor core runs dV += P^T_c dO_i[c] and dK~ += dS^T_c Q~_i[c]
+//          (K = 32) while the warps form chunk c+1;
+//   MMA3:  dQ~^T = K~^T dS^T -> TMEM 128..255 (M = 128 channels, N = 128 queries)
+// Warps 8-15 copy dQ~^T out of TMEM (one channel, 64 queries per thread),
+// release it, and add it into the scope-order fp32 accumulator with
+// fire-and-forget red.global.add: one 128-byte line per warp instruction. The
+// adds of tile i overlap the MMAs and softmax of tile i+1, which is what keeps
+// the SM's stream of dQ~ partial sums (64 KB per pair) off the critical path.
+// P^T for queries 16m .. 16m+15 is packed into S^T columns 16m .. 16m+7, which
+// the writing thread has itself read; warps w and w+4 share TMEM lanes (key
+// rows) and split each chunk's 32 queries 16 / 16.
+enum BwdTileBar {
+  T_KVFULL, T_KVEMPTY, T_QFULL0, T_QFULL1, T_QEMPTY0, T_QEMPTY1, T_SFULL, T_DSC0, T_DSC1, T_DSC2, T_DSC3,
+  T_DQFULL, T_DQFREE, T_DKVDONE, T_DKVFREE, T_FINAL, T_NBARS
 };
 
-enum BwdHalfBar {
-  H_KVFULL, H_KVEMPTY, H_QFULL0, H_QFULL1, H_QFULL2, H_QEMPTY0, H_QEMPTY1, H_QEMPTY2,
-  H_SFULL0, H_SFULL1, H_DSREADY0, H_DSREADY1, H_DSFREE0, H_DSFREE1, H_DQFULL0, H_DQFULL1,
-  H_DQFREE0, H_DQFREE1, H_DKVDONE, H_DKVFREE, H_FINAL, H_NBARS
-};
+constexpr int kTileThreads = 576;   // 8 softmax warps, 8 dQ warps, TMA warp, MMA warp
+constexpr int kTileTmaWarp = 16, kTileMmaWarp = 17;
 
-__global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_half_kernel(const __grid_constant__ BwdParams p) {
-  using Ly = BwdHalfLayout;
+// Query tile visited at step i by the unit of key tile kt. The CTAs of one
+// scope start together; rotating the order by kt spreads their dQ~ adds over
+// different accumulator rows.
+__device__ __forceinline__ int stagger(int i, int kt, int n) {
+  const int r = i + kt;
+  return r >= n ? r - n : r;
+}
+
+__global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel(const __grid_constant__ BwdParams p) {
+  using Ly = BwdLayout<128>;
   constexpr int D = 128;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -515,229 +517,210 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_half_kernel(
   const uint32_t sK = smem_u32(smem + Ly::K_OFF);
   const uint32_t sV = smem_u32(smem + Ly::V_OFF);
   const uint32_t sQ = smem_u32(smem + Ly::Q_OFF);
+  const uint32_t sDO = smem_u32(smem + Ly::DO_OFF);
   const uint32_t sDS = smem_u32(smem + Ly::DS_OFF);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   const Ctl ctl{abort_flag, p.err};
   const Geom& g = p.g;
-  const int n_half = (g.L + 63) >> 6;
+  constexpr int E = ERR_KERNEL_BWD + 0x80;
 
   if (tid == 0) {
     *abort_flag = 0;
-    const uint32_t counts[H_NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 1, 1, 4, 4, 1, 4, 1};
-    for (int i = 0; i < H_NBARS; ++i) mbar_init(bar(i), counts[i]);
+    const uint32_t counts[T_NBARS] = {1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 8, 1, 8, 1, 8, 1};
+    for (int i = 0; i < T_NBARS; ++i) mbar_init(bar(i), counts[i]);
     mbar_fence_init();
   }
-  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == kTileMmaWarp) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kTileTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      tma_prefetch_map(&p.tm_q);
       tma_prefetch_map(&p.tm_k);
       tma_prefetch_map(&p.tm_v);
-      tma_prefetch_map(&p.tm_q64);
-      tma_prefetch_map(&p.tm_do64);
-      uint32_t kv_issued = 0, q_issued[3] = {0, 0, 0};
-      uint32_t gh = 0;
+      tma_prefetch_map(&p.tm_do);
+      uint32_t kv_issued = 0, q_issued[2] = {0, 0};
+      uint32_t g0 = 0;
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
         int b, head, s, kt;
         decode_unit_bwd(g, u, b, head, s, kt);
-        if (it > 0 && !mbar_wait(bar(H_KVEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_KVEMPTY)) break;
-        mbar_expect_tx(bar(H_KVFULL), 2 * Ly::TILE);
+        if (it > 0 && !mbar_wait(bar(T_KVEMPTY), (it - 1) & 1, ctl, E + T_KVEMPTY)) break;
+        mbar_expect_tx(bar(T_KVFULL), 2 * Ly::TILE);
         const int krow = b * g.Nn + (kt * kTile) / g.G;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          tma_load_5d(sK + h * kHalfBytes, &p.tm_k, bar(H_KVFULL), h * 64, head, 0, s, krow);
-          tma_load_5d(sV + h * kHalfBytes, &p.tm_v, bar(H_KVFULL), h * 64, head, 0, s, krow);
+          tma_load_5d(sK + h * kHalfBytes, &p.tm_k, bar(T_KVFULL), h * 64, head, 0, s, krow);
+          tma_load_5d(sV + h * kHalfBytes, &p.tm_v, bar(T_KVFULL), h * 64, head, 0, s, krow);
         }
         ++kv_issued;
         const size_t srow = (((size_t)b * g.heads + head) * g.k + s) * p.Lp;
-        for (int qh = 0; qh < n_half; ++qh, ++gh) {
-          const int st = gh % 3;
-          const uint32_t n = gh / 3;
-          if (n > 0 && !mbar_wait(bar(H_QEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_QEMPTY0 + st)) {
+        for (int i = 0; i < g.n_tiles; ++i) {
+          const uint32_t gg = g0 + i;
+          const int st = gg & 1;
+          const uint32_t n = gg >> 1;
+          if (n > 0 && !mbar_wait(bar(T_QEMPTY0 + st), (n - 1) & 1, ctl, E + T_QEMPTY0 + st)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(bar(H_QFULL0 + st), Ly::STAGE + 512);
-          const int qrow = b * g.Nn + (qh * 64) / g.G;
-          const uint32_t qt = sQ + st * Ly::STAGE;
+          mbar_expect_tx(bar(T_QFULL0 + st), 2 * Ly::TILE + 1024);
+          const int qi = stagger(i, kt, g.n_tiles);
+          const int qrow = b * g.Nn + (qi * kTile) / g.G;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            tma_load_5d(qt + h * Ly::HBOX, &p.tm_q64, bar(H_QFULL0 + st), h * 64, head, 0, s, qrow);
-            tma_load_5d(qt + Ly::HTILE + h * Ly::HBOX, &p.tm_do64, bar(H_QFULL0 + st), h * 64, head, 0, s, qrow);
+            tma_load_5d(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(T_QFULL0 + st), h * 64, head, 0, s, qrow);
+            tma_load_5d(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(T_QFULL0 + st), h * 64, head, 0, s, qrow);
           }
-          const uint32_t dst = smem_u32(stats + st * 128);
-          bulk_load(dst, p.lse2s + srow + qh * 64, 256, bar(H_QFULL0 + st));
-          bulk_load(dst + 256, p.delta_s + srow + qh * 64, 256, bar(H_QFULL0 + st));
+          const uint32_t dst = smem_u32(stats + st * 256);
+          bulk_load(dst, p.lse2s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
+          bulk_load(dst + 512, p.delta_s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
           ++q_issued[st];
         }
+        g0 += g.n_tiles;
       }
-      if (kv_issued) mbar_drain(bar(H_KVFULL), (kv_issued - 1) & 1);
-      for (int st = 0; st < 3; ++st)
-        if (q_issued[st]) mbar_drain(bar(H_QFULL0 + st), (q_issued[st] - 1) & 1);
+      if (kv_issued) mbar_drain(bar(T_KVFULL), (kv_issued - 1) & 1);
+      for (int st = 0; st < 2; ++st)
+        if (q_issued[st]) mbar_drain(bar(T_QFULL0 + st), (q_issued[st] - 1) & 1);
     }
-  } else if (warp == 9) {
+  } else if (warp == kTileMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);    // S^T, dP^T
-      constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO_h (MN-major)
-      constexpr uint32_t kIdDK = idesc_bf16(128, D, false, true);     // dS^T (K-major) x Q~_h (MN-major)
-      constexpr uint32_t kIdDQ = idesc_bf16(D, 64, true, true);       // K~^T (MN-major) x dS^T (MN-major)
-      auto mma1 = [&](uint32_t gh) -> bool {
-        const int st = gh % 3;
-        const uint32_t sl = gh & 1;
-        if (!mbar_wait(bar(H_QFULL0 + st), (gh / 3) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_QFULL0 + st)) return false;
-        if (gh >= 2 && !mbar_wait(bar(H_DQFREE0 + sl), ((gh - 2) >> 1) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_DQFREE0 + sl))
-          return false;
-        tc_fence_after();
-        const uint32_t qt = sQ + st * Ly::STAGE;
-        const uint32_t dot = qt + Ly::HTILE;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + sl * 128, desc_kmajor(sK, ks), desc_kmajor(qt, ks, Ly::HBOX), kIdS, ks > 0 ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + sl * 128 + 64, desc_kmajor(sV, ks), desc_kmajor(dot, ks, Ly::HBOX), kIdS, ks > 0 ? 1u : 0u);
-        tc_commit(bar(H_SFULL0 + sl));
-        return true;
-      };
-      auto mma2 = [&](uint32_t gh, bool first) -> bool {
-        const int st = gh % 3;
-        const uint32_t sl = gh & 1;
-        if (!mbar_wait(bar(H_DSREADY0 + sl), (gh >> 1) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_DSREADY0 + sl)) return false;
-        tc_fence_after();
-        const uint32_t qt = sQ + st * Ly::STAGE;
-        const uint32_t dot = qt + Ly::HTILE;
-        const uint32_t ds = sDS + sl * 16384;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ts(tmem + 256, tmem + sl * 128 + ks * 8, desc_mnmajor(dot, ks, Ly::HBOX), kIdDV, (!first || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(tmem + 384, desc_kmajor(ds, ks), desc_mnmajor(qt, ks, Ly::HBOX), kIdDK, (!first || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tmem + sl * 128 + 64, desc_mnmajor(sK, ks), desc_mnmajor(ds, ks), kIdDQ, ks > 0 ? 1u : 0u);
-        tc_commit(bar(H_DQFULL0 + sl));
-        tc_commit(bar(H_QEMPTY0 + st));
-        tc_commit(bar(H_DSFREE0 + sl));
-        return true;
-      };
-      uint32_t gh = 0;
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+      constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO (MN-major)
+      constexpr uint32_t kIdDK = idesc_bf16(128, D, false, true);     // dS^T (K-major) x Q~ (MN-major)
+      constexpr uint32_t kIdDQ = idesc_bf16(D, 128, true, true);      // K~^T (MN-major) x dS^T (MN-major)
+      uint32_t g0 = 0;
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-        if (!mbar_wait(bar(H_KVFULL), it & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_KVFULL)) break;
+        if (!mbar_wait(bar(T_KVFULL), it & 1, ctl, E + T_KVFULL)) break;
         tc_fence_after();
-        for (int qh = 0; qh <= n_half; ++qh) {
-          if (qh < n_half && !mma1(gh + qh)) { ok = false; break; }
-          if (qh >= 1) {
-            // the unit's first MMA2 overwrites dV / dK~: the previous epilogue must be done
-            if (qh == 1 && it > 0 && !mbar_wait(bar(H_DKVFREE), (it - 1) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_DKVFREE)) {
+        for (int i = 0; ok && i < g.n_tiles; ++i) {
+          const uint32_t gg = g0 + i;
+          const int st = gg & 1;
+          if (!mbar_wait(bar(T_QFULL0 + st), (gg >> 1) & 1, ctl, E + T_QFULL0 + st)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qt = sQ + st * Ly::TILE;
+          const uint32_t dot = sDO + st * Ly::TILE;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tmem, desc_kmajor(sK, ks), desc_kmajor(qt, ks), kIdS, ks > 0 ? 1u : 0u);
+          // dP^T overwrites the previous tile's dQ~^T: wait until the dQ warps hold it
+          if (gg > 0 && !mbar_wait(bar(T_DQFREE), (gg - 1) & 1, ctl, E + T_DQFREE)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tmem + 128, desc_kmajor(sV, ks), desc_kmajor(dot, ks), kIdS, ks > 0 ? 1u : 0u);
+          tc_commit(bar(T_SFULL));
+          for (int c = 0; c < 4; ++c) {
+            if (!mbar_wait(bar(T_DSC0 + c), gg & 1, ctl, E + T_DSC0 + c)) { ok = false; break; }
+            // the previous unit's dV / dK must have been written out before the first accumulate
+            if (c == 0 && i == 0 && it > 0 && !mbar_wait(bar(T_DKVFREE), (it - 1) & 1, ctl, E + T_DKVFREE)) {
               ok = false;
               break;
             }
-            if (!mma2(gh + qh - 1, qh == 1)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ks = 2 * c + e;
+              mma_ts(tmem + 256, tmem + 16 * ks, desc_mnmajor(dot, ks), kIdDV, (i > 0 || ks > 0) ? 1u : 0u);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ks = 2 * c + e;
+              mma_ss(tmem + 384, desc_kmajor(sDS, ks), desc_mnmajor(qt, ks), kIdDK, (i > 0 || ks > 0) ? 1u : 0u);
+            }
           }
+          if (!ok) break;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss(tmem + 128, desc_mnmajor(sK, ks), desc_mnmajor(sDS, ks), kIdDQ, ks > 0 ? 1u : 0u);
+          tc_commit(bar(T_DQFULL));
+          tc_commit(bar(T_QEMPTY0 + st));
         }
         if (!ok) break;
-        tc_commit(bar(H_DKVDONE));
-        tc_commit(bar(H_KVEMPTY));
-        gh += n_half;
+        tc_commit(bar(T_DKVDONE));
+        tc_commit(bar(T_KVEMPTY));
+        g0 += g.n_tiles;
       }
-      tc_commit(bar(H_FINAL));
-      mbar_drain(bar(H_FINAL), 0);
+      tc_commit(bar(T_FINAL));
+      mbar_drain(bar(T_FINAL), 0);
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ dQ warps
-    const int ch = (warp & 3) * 32 + lane;                   // channel = TMEM lane of dQ~^T
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ warps (8-15)
+    const int j = (warp & 3) * 32 + lane;                    // channel d = TMEM lane of dQ~^T
+    const int qh = (warp - 8) >> 2;                          // query half of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    float* stage = reinterpret_cast<float*>(smem + Ly::DQ_OFF);
-    const uint32_t stage_s = smem_u32(stage);
-    const bool leader = tid == 128;
-    uint32_t gh = 0;
-    int it = 0;
+    uint32_t g0 = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
       decode_unit_bwd(g, u, b, head, s, kt);
-      float* acc = p.dq_acc + (((size_t)b * g.heads + head) * g.k + s) * (size_t)p.Lp * D;
-      for (int qh = 0; qh < n_half; ++qh, ++gh) {
-        const uint32_t sl = gh & 1;
-        bool w_ok = mbar_wait(bar(H_DQFULL0 + sl), (gh >> 1) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_DQFULL0 + sl);
-        w_ok = __all_sync(0xffffffffu, w_ok);
+      float* acc = p.dq_acc + (((size_t)b * g.heads + head) * g.k + s) * (size_t)p.Lp * D + j;
+      for (int i = 0; i < g.n_tiles; ++i) {
+        const uint32_t gg = g0 + i;
+        if (!bar_and<3, 256>(mbar_wait(bar(T_DQFULL), gg & 1, ctl, E + T_DQFULL))) { ok = false; break; }
+        tc_fence_after();
         float x[64];
-        if (w_ok) {
-          tc_fence_after();
-          tmem_ld32(tmem + lane_base + sl * 128 + 64, *reinterpret_cast<float(*)[32]>(&x[0]));
-          tmem_ld32(tmem + lane_base + sl * 128 + 96, *reinterpret_cast<float(*)[32]>(&x[32]));
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(H_DQFREE0 + sl));
-        }
-        // the staging tile is free once the previous bulk reduce has read it
-        if (leader) bulk_wait_read<0>();
-        if (!bar_and<2, 128>(w_ok)) { ok = false; break; }
+        tmem_ld32(tmem + lane_base + 128 + qh * 64, *reinterpret_cast<float(*)[32]>(&x[0]));
+        tmem_ld32(tmem + lane_base + 128 + qh * 64 + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(T_DQFREE));
+        const int q0 = stagger(i, kt, g.n_tiles) * kTile + qh * 64;
+        const int nq = min(64, g.L - q0);
+        float* rowp = acc + (size_t)q0 * D;
 #pragma unroll
-        for (int q = 0; q < 64; ++q) stage[q * D + ch] = x[q];
-        fence_proxy_async_smem();
-        asm volatile("bar.sync 2, 128;" ::: "memory");
-        if (leader) {
-          bulk_reduce_add_f32(acc + (size_t)qh * 64 * D, stage_s, 64 * D * 4);
-          bulk_commit_group();
-        }
+        for (int q = 0; q < 64; ++q)
+          if (q < nq) atomicAdd(rowp + (size_t)q * D, x[q]);
       }
+      g0 += g.n_tiles;
     }
-    if (leader) bulk_wait_all();
   } else {
-    // ------------------------------------------------------------ P^T / dS^T warps
-    const int j = tid;                                       // key row of the K/V tile = TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------------------ P^T / dS^T warps (0-7)
+    const int ch = warp >> 2;                                // which 16 queries of each 32-query chunk
+    const int j = (warp & 3) * 32 + lane;                    // key row (TMEM lane)
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t gh = 0;
+    uint8_t* ds_row = smem + Ly::DS_OFF + j * 128;
+    uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
       int b, head, s, kt;
       decode_unit_bwd(g, u, b, head, s, kt);
       const bool key_ok = kt * kTile + j < g.L;
-      for (int qh = 0; qh < n_half; ++qh) {
-        const uint32_t ghh = gh + qh;
-        const uint32_t sl = ghh & 1;
-        const int st = ghh % 3;
-        if (!mbar_wait(bar(H_SFULL0 + sl), (ghh >> 1) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_SFULL0 + sl)) { ok = false; break; }
-        if (ghh >= 2 && !mbar_wait(bar(H_DSFREE0 + sl), ((ghh - 2) >> 1) & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_DSFREE0 + sl)) {
-          ok = false;
-          break;
-        }
+      for (int i = 0; i < g.n_tiles; ++i) {
+        const uint32_t gg = g0 + i;
+        const int st = gg & 1;
+        // SFULL also says the previous tile's MMAs (readers of the dS^T buffer) are done
+        if (!bar_and<2, 256>(mbar_wait(bar(T_SFULL), gg & 1, ctl, E + T_SFULL))) { ok = false; break; }
         tc_fence_after();
-        const float4* lse4 = reinterpret_cast<const float4*>(stats + st * 128);
-        const float4* del4 = lse4 + 16;
-        const int qvalid = key_ok ? min(64, g.L - qh * 64) : 0;
-        uint8_t* rowp = smem + Ly::DS_OFF + sl * 16384 + j * 128;
+        const float4* lse4 = reinterpret_cast<const float4*>(stats + st * 256);
+        const float4* del4 = lse4 + 32;
+        const int qvalid = key_ok ? min(kTile, g.L - stagger(i, kt, g.n_tiles) * kTile) : 0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float sv[32], dp[32];
-          tmem_ld32(tmem + lane_base + sl * 128 + c * 32, sv);
-          tmem_ld32(tmem + lane_base + sl * 128 + 64 + c * 32, dp);
-          uint32_t pk[16], dk[16];
+        for (int c = 0; c < 4; ++c) {
+          const int qb = c * 32 + ch * 16;                   // first query of this thread's 16 columns
+          float sv[16], dp[16];
+          tmem_ld16x2(tmem + lane_base + qb, tmem + lane_base + 128 + qb, sv, dp);
+          uint32_t pk[8], dk[8];
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 l4 = lse4[c * 8 + e4];
-            const float4 d4 = del4[c * 8 + e4];
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 l4 = lse4[(qb >> 2) + e4];
+            const float4 d4 = del4[(qb >> 2) + e4];
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
             const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
             float pv[4], dsv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int q = c * 32 + e4 * 4 + e;
+              const int q = qb + e4 * 4 + e;
               const float pe = ex2(fmaf(sv[e4 * 4 + e], sl2, -lv[e]));
               pv[e] = q < qvalid ? pe : 0.f;
               dsv[e] = q < qvalid ? pe * (dp[e4 * 4 + e] - dv4[e]) : 0.f;
@@ -747,77 +730,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_half_kernel(
             dk[e4 * 2] = pack_bf16(dsv[0], dsv[1]);
             dk[e4 * 2 + 1] = pack_bf16(dsv[2], dsv[3]);
           }
-          tmem_st16(tmem + lane_base + sl * 128 + c * 16, pk);
+          tmem_st8(tmem + lane_base + qb, pk);
+          // dS^T row j, queries qb .. qb+15: box c/2, 16-byte chunks (c%2)*4 + ch*2 + {0,1}
+          uint8_t* rowp = ds_row + (c >> 1) * kHalfBytes;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int chunk = (c * 4 + q4) ^ (j & 7);
-            *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2], dk[4 * q4 + 3]);
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int chunk = ((c & 1) * 4 + ch * 2 + q2) ^ (j & 7);
+            *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(dk[4 * q2], dk[4 * q2 + 1], dk[4 * q2 + 2], dk[4 * q2 + 3]);
           }
+          tmem_st_wait();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(T_DSC0 + c));
         }
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(H_DSREADY0 + sl));
       }
       if (!ok) break;
-      // ---- epilogue: dv and dk = scale * R^T dK~ at the key's original row
-      if (!mbar_wait(bar(H_DKVDONE), it & 1, ctl, ERR_KERNEL_BWD + 0x40 + H_DKVDONE)) break;
+      // ---- epilogue: warps 0-3 write dv, warps 4-7 write dk = scale * R^T dK~ (key row j)
+      if (!bar_and<2, 256>(mbar_wait(bar(T_DKVDONE), it & 1, ctl, E + T_DKVDONE))) break;
       tc_fence_after();
       const int prow = kt * kTile + j;
       const int tok = key_ok ? token_of(g, s, prow) : 0;
       int t = 0, hh = 0, w = 0;
       if (key_ok) token_coords(p.rope, tok, t, hh, w);
       const size_t rbase = (((size_t)b * g.N + tok) * g.heads + head) * D;
+      if (ch == 0) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float y[32];
+          tmem_ld32(tmem + lane_base + 256 + c * 32, y);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float x[32];
-        tmem_ld32(tmem + lane_base + 256 + c * 32, x);
-        if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(pack_bf16(x[8 * q4], x[8 * q4 + 1]), pack_bf16(x[8 * q4 + 2], x[8 * q4 + 3]),
-                                 pack_bf16(x[8 * q4 + 4], x[8 * q4 + 5]), pack_bf16(x[8 * q4 + 6], x[8 * q4 + 7]));
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float x[32];
-        tmem_ld32(tmem + lane_base + 384 + c * 32, x);
-        if (key_ok) {
-          uint32_t o[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const PairSel sel = pair_select(p.rope, c * 16 + e);
-            const float2 cs = __ldg(&p.rope_tab[pair_index(sel, t, hh, w)]);
-            const float2 r = rope_rotate_t(x[2 * e] * p.scale, x[2 * e + 1] * p.scale, cs);
-            o[e] = pack_bf16(r.x, r.y);
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_uint4(pack_bf16(y[8 * q4], y[8 * q4 + 1]), pack_bf16(y[8 * q4 + 2], y[8 * q4 + 3]),
+                                   pack_bf16(y[8 * q4 + 4], y[8 * q4 + 5]), pack_bf16(y[8 * q4 + 6], y[8 * q4 + 7]));
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float y[32];
+          tmem_ld32(tmem + lane_base + 384 + c * 32, y);
+          if (key_ok) {
+            uint32_t o[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+            for (int e = 0; e < 16; ++e) {
+              const PairSel sel = pair_select(p.rope, c * 16 + e);
+              const float2 cs = __ldg(&p.rope_tab[pair_index(sel, t, hh, w)]);
+              const float2 r = rope_rotate_t(y[2 * e] * p.scale, y[2 * e + 1] * p.scale, cs);
+              o[e] = pack_bf16(r.x, r.y);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(H_DKVFREE));
-      gh += n_half;
+      if (lane == 0) mbar_arrive(bar(T_DKVFREE));
+      g0 += g.n_tiles;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kTileMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-bool bwd_uses_half_tiles(int D, int G) { return D == 128 && G <= 64; }
+bool bwd_uses_tile_kernel(int D) { return D == 128; }
 
-size_t bwd_main_smem_bytes(int D, int G) {
-  if (bwd_uses_half_tiles(D, G)) return (size_t)BwdHalfLayout::BYTES;
+size_t bwd_main_smem_bytes(int D) {
   return D == 128 ? (size_t)BwdLayout<128>::BYTES : (size_t)BwdLayout<64>::BYTES;
 }
 
@@ -837,16 +824,12 @@ cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = bwd_main_smem_bytes(p.g.D, p.g.G);
+  const size_t smem = bwd_main_smem_bytes(p.g.D);
   cudaError_t e;
-  if (bwd_uses_half_tiles(p.g.D, p.g.G)) {
-    e = cudaFuncSetAttribute(skiparse_bwd_main_half_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (bwd_uses_tile_kernel(p.g.D)) {
+    e = cudaFuncSetAttribute(skiparse_bwd_main_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    skiparse_bwd_main_half_kernel<<<grid, kBwdThreads, smem, stream>>>(p);
-  } else if (p.g.D == 128) {
-    e = cudaFuncSetAttribute(skiparse_bwd_main_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_bwd_main_kernel<128><<<grid, kBwdThreads, smem, stream>>>(p);
+    skiparse_bwd_main_tile_kernel<<<grid, kTileThreads, smem, stream>>>(p);
   } else {
     e = cudaFuncSetAttribute(skiparse_bwd_main_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

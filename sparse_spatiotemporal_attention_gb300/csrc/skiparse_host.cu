@@ -215,7 +215,8 @@ RopeParams make_rope(const Shape& s, float theta) {
   return r;
 }
 
-bool encode_scope_map(CUtensorMap* m, const void* base, const Geom& g, int box_rows = kTile) {
+bool encode_scope_map(CUtensorMap* m, const void* base, const Geom& g) {
+  const int box_rows = kTile;
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t row = (cuuint64_t)g.heads * g.D * 2;
@@ -350,8 +351,7 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
     return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
-  const int G = mode == SKIPARSE_SINGLE ? 1 : sparse_k;
-  if ((size_t)dev.smem_optin < bwd_main_smem_bytes(D, G)) return SKIPARSE_ERR_UNSUPPORTED;
+  if ((size_t)dev.smem_optin < bwd_main_smem_bytes(D)) return SKIPARSE_ERR_UNSUPPORTED;
 
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -379,9 +379,6 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   if (!encode_scope_map(&p.tm_q, p.qr, p.g) || !encode_scope_map(&p.tm_k, p.kr, p.g) ||
       !encode_scope_map(&p.tm_v, v, p.g) || !encode_scope_map(&p.tm_do, dout, p.g))
-    return SKIPARSE_ERR_LAUNCH;
-  if (bwd_uses_half_tiles(p.g.D, p.g.G) &&
-      (!encode_scope_map(&p.tm_q64, p.qr, p.g, 64) || !encode_scope_map(&p.tm_do64, dout, p.g, 64)))
     return SKIPARSE_ERR_LAUNCH;
 
   const long long rows = (long long)B * N * heads;

@@ -11,7 +11,8 @@
 namespace skp {
 
 // Codes written to the device error word when a bounded wait runs out:
-// 0x100 * kernel + barrier index (+ 0x80 for the drain path).
+// kernel base + barrier index; the backward main kernels add 0x00 (128-query
+// tiles, D = 64), 0x40 (64-query halves) or 0x80 (128-query tiles, D = 128).
 enum : int {
   ERR_KERNEL_FWD = 0x1000,
   ERR_KERNEL_BWD = 0x2000,
@@ -31,7 +32,6 @@ struct FwdParams {
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;   // maps over rotated q, rotated k, v, dout (128-row boxes)
-  CUtensorMap tm_q64, tm_do64;           // rotated q and dout with 64-row boxes (query halves)
   Geom g;
   RopeParams rope;
   const uint16_t* q;       // pre-RoPE inputs
@@ -69,8 +69,8 @@ size_t fwd_smem_bytes(int D, int rope_entries);
 int fwd_units(const Geom& g);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
 
-size_t bwd_main_smem_bytes(int D, int G);
-bool bwd_uses_half_tiles(int D, int G);
+size_t bwd_main_smem_bytes(int D);
+bool bwd_uses_tile_kernel(int D);
 cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdParams& p, int grid, cudaStream_t stream);
