@@ -13,15 +13,15 @@
 //                S^T  = K~ Q~^T          dP^T = V dO^T
 //                dV  += P^T dO           dK~ += dS^T Q~          dQ~_part = dS K~
 //              P^T = exp(S^T * scale - lse), dS^T = P^T * (dP^T - delta).
-//              dQ~_part is added into the fp32 accumulator (scope order) with
-//              fire-and-forget reduction stores to L2.
+//              dQ~_part is added into the fp32 accumulator (scope order) by
+//              bulk reduce-adds (D = 128) or vector atomics (D = 64).
 //              Epilogue: dv, and dk = scale * R^T dK~, stored at original rows.
 //  post        dq = R^T (scale * dQ~_acc) -> bf16.
 // Two main kernels share that plan. D = 128 (the 18-warp tile kernel):
 //   warps 0-7   P^T / dS^T in four 32-query chunks (one key row, 16 queries of
 //               a chunk per thread) and the dK / dV epilogue;
-//   warps 8-15  dQ~^T out of TMEM (one channel, 64 queries per thread) and its
-//               coalesced adds into the accumulator;
+//   warps 8-15  dQ~^T out of TMEM (one channel, 64 queries per thread), staged
+//               in the tile's dead Q~ / dO slots and bulk-added to the accumulator;
 //   warp 16     TMA producer (K~, V per unit; Q~, dO, lse, delta per Q tile);
 //   warp 17     MMA issuer; every MMA has M = N = 128.
 // D = 64 (the 10-warp kernel): warps 0-3 P^T / dS^T and the epilogue, warps
@@ -471,21 +471,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
 // Every MMA has M = N = 128 (40 tcgen05.mma per key-tile x query-tile pair).
 // Per query tile i:
 //   MMA1:  S^T = K~ Q~_i^T -> TMEM 0..127, dP^T = V dO_i^T -> TMEM 128..255
-//   warps 0-7 form P^T / dS^T in four chunks of 32 queries; after chunk c
-//          the tensor core runs dV += P^T_c dO_i[c] and dK~ += dS^T_c Q~_i[c]
-//          (K = 32) while the warps form chunk c+1;
+//   warps 0-7 form P^T / dS^T in four chunks of 32 queries. P^T of chunks
+//          0 and 1 is published as soon as S^T lands (while dP^T is still on
+//          the tensor core), so dV += P^T_{0,1} dO_i[0:64] runs while the warps
+//          form dS^T_0; after each dS^T_c the tensor core runs dK~ += dS^T_c
+//          Q~_i[c] (and dV for chunks 2, 3) while the warps form chunk c+1;
 //   MMA3:  dQ~^T = K~^T dS^T -> TMEM 128..255 (M = 128 channels, N = 128 queries)
 // Warps 8-15 copy dQ~^T out of TMEM (one channel, 64 queries per thread),
-// release it, and add it into the scope-order fp32 accumulator with
-// fire-and-forget red.global.add: one 128-byte line per warp instruction. The
-// adds of tile i overlap the MMAs and softmax of tile i+1, which is what keeps
-// the SM's stream of dQ~ partial sums (64 KB per pair) off the critical path.
+// release it, stage it in the tile's own Q~ / dO slots (dead by then until the
+// refill two tiles later) and add it into the scope-order fp32 accumulator with
+// two bulk reduce-adds, which the TMA engine streams to L2 while the next tile
+// runs. (Reduction stores issued from registers would instead share the
+// load/store pipe with the softmax warps' shared-memory traffic and slow it.)
 // P^T for queries 16m .. 16m+15 is packed into S^T columns 16m .. 16m+7, which
 // the writing thread has itself read; warps w and w+4 share TMEM lanes (key
 // rows) and split each chunk's 32 queries 16 / 16.
 enum BwdTileBar {
-  T_KVFULL, T_KVEMPTY, T_QFULL0, T_QFULL1, T_QEMPTY0, T_QEMPTY1, T_SFULL, T_DSC0, T_DSC1, T_DSC2, T_DSC3,
-  T_DQFULL, T_DQFREE, T_DKVDONE, T_DKVFREE, T_FINAL, T_NBARS
+  T_KVFULL, T_KVEMPTY,
+  T_QFULL0, T_QFULL1,       // Q~ tile + lse / delta of stage 0 / 1 landed
+  T_OFULL0, T_OFULL1,       // dO tile of stage 0 / 1 landed
+  T_QFREE0, T_QFREE1,       // Q~ slot of stage 0 / 1 free again (its dQ~ staging has been read)
+  T_OFREE0, T_OFREE1,       // dO slot likewise
+  T_SRDY, T_DPRDY, T_PRDY, T_DSC0, T_DSC1, T_DSC2, T_DSC3, T_DQFULL, T_DQFREE, T_DKVDONE, T_DKVFREE, T_FINAL,
+  T_NBARS
 };
 
 constexpr int kTileThreads = 576;   // 8 softmax warps, 8 dQ warps, TMA warp, MMA warp
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
 
   if (tid == 0) {
     *abort_flag = 0;
-    const uint32_t counts[T_NBARS] = {1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 8, 1, 8, 1, 8, 1};
+    const uint32_t counts[T_NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 8, 8, 1, 8, 1, 8, 1};
     for (int i = 0; i < T_NBARS; ++i) mbar_init(bar(i), counts[i]);
     mbar_fence_init();
   }
@@ -537,21 +545,29 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // The TMA and MMA warps run their loops with all 32 lanes (waits are voted
+  // across the warp so every lane takes the same branch); lane 0 issues.
+  auto warp_wait = [&](int i, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ctl, E + i)) != 0;
+  };
+  const bool leader = lane == 0;
   if (warp == kTileTmaWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (leader) {
       tma_prefetch_map(&p.tm_q);
       tma_prefetch_map(&p.tm_k);
       tma_prefetch_map(&p.tm_v);
       tma_prefetch_map(&p.tm_do);
-      uint32_t kv_issued = 0, q_issued[2] = {0, 0};
-      uint32_t g0 = 0;
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-        int b, head, s, kt;
-        decode_unit_bwd(g, u, b, head, s, kt);
-        if (it > 0 && !mbar_wait(bar(T_KVEMPTY), (it - 1) & 1, ctl, E + T_KVEMPTY)) break;
+    }
+    uint32_t kv_issued = 0, q_issued[2] = {0, 0};
+    uint32_t g0 = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      int b, head, s, kt;
+      decode_unit_bwd(g, u, b, head, s, kt);
+      if (it > 0 && !warp_wait(T_KVEMPTY, (it - 1) & 1)) break;
+      if (leader) {
         mbar_expect_tx(bar(T_KVFULL), 2 * Ly::TILE);
         const int krow = b * g.Nn + (kt * kTile) / g.G;
 #pragma unroll
@@ -559,77 +575,113 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
           tma_load_5d(sK + h * kHalfBytes, &p.tm_k, bar(T_KVFULL), h * 64, head, 0, s, krow);
           tma_load_5d(sV + h * kHalfBytes, &p.tm_v, bar(T_KVFULL), h * 64, head, 0, s, krow);
         }
-        ++kv_issued;
-        const size_t srow = (((size_t)b * g.heads + head) * g.k + s) * p.Lp;
-        for (int i = 0; i < g.n_tiles; ++i) {
-          const uint32_t gg = g0 + i;
-          const int st = gg & 1;
-          const uint32_t n = gg >> 1;
-          if (n > 0 && !mbar_wait(bar(T_QEMPTY0 + st), (n - 1) & 1, ctl, E + T_QEMPTY0 + st)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(bar(T_QFULL0 + st), 2 * Ly::TILE + 1024);
-          const int qi = stagger(i, kt, g.n_tiles);
-          const int qrow = b * g.Nn + (qi * kTile) / g.G;
+      }
+      __syncwarp();
+      ++kv_issued;
+      const size_t srow = (((size_t)b * g.heads + head) * g.k + s) * p.Lp;
+      for (int i = 0; i < g.n_tiles; ++i) {
+        const uint32_t gg = g0 + i;
+        const int st = gg & 1;
+        const uint32_t n = gg >> 1;
+        const int qi = stagger(i, kt, g.n_tiles);
+        const int qrow = b * g.Nn + (qi * kTile) / g.G;
+        // a slot is refilled once the dQ~ staging of tile gg-2 placed in it has been read out
+        if (n > 0 && !warp_wait(T_QFREE0 + st, (n - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          mbar_expect_tx(bar(T_QFULL0 + st), Ly::TILE + 1024);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2; ++h)
             tma_load_5d(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(T_QFULL0 + st), h * 64, head, 0, s, qrow);
-            tma_load_5d(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(T_QFULL0 + st), h * 64, head, 0, s, qrow);
-          }
           const uint32_t dst = smem_u32(stats + st * 256);
           bulk_load(dst, p.lse2s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
           bulk_load(dst + 512, p.delta_s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
-          ++q_issued[st];
         }
-        g0 += g.n_tiles;
+        __syncwarp();
+        if (n > 0 && !warp_wait(T_OFREE0 + st, (n - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          mbar_expect_tx(bar(T_OFULL0 + st), Ly::TILE);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_5d(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(T_OFULL0 + st), h * 64, head, 0, s, qrow);
+        }
+        __syncwarp();
+        ++q_issued[st];
       }
+      g0 += g.n_tiles;
+    }
+    if (leader) {
       if (kv_issued) mbar_drain(bar(T_KVFULL), (kv_issued - 1) & 1);
       for (int st = 0; st < 2; ++st)
-        if (q_issued[st]) mbar_drain(bar(T_QFULL0 + st), (q_issued[st] - 1) & 1);
+        if (q_issued[st]) {
+          mbar_drain(bar(T_QFULL0 + st), (q_issued[st] - 1) & 1);
+          mbar_drain(bar(T_OFULL0 + st), (q_issued[st] - 1) & 1);
+        }
     }
+    __syncwarp();
   } else if (warp == kTileMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
-      constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO (MN-major)
-      constexpr uint32_t kIdDK = idesc_bf16(128, D, false, true);     // dS^T (K-major) x Q~ (MN-major)
-      constexpr uint32_t kIdDQ = idesc_bf16(D, 128, true, true);      // K~^T (MN-major) x dS^T (MN-major)
-      uint32_t g0 = 0;
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-        if (!mbar_wait(bar(T_KVFULL), it & 1, ctl, E + T_KVFULL)) break;
+    constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+    constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO (MN-major)
+    constexpr uint32_t kIdDK = idesc_bf16(128, D, false, true);     // dS^T (K-major) x Q~ (MN-major)
+    constexpr uint32_t kIdDQ = idesc_bf16(D, 128, true, true);      // K~^T (MN-major) x dS^T (MN-major)
+    uint32_t g0 = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      if (!warp_wait(T_KVFULL, it & 1)) break;
+      tc_fence_after();
+      for (int i = 0; ok && i < g.n_tiles; ++i) {
+        const uint32_t gg = g0 + i;
+        const int st = gg & 1;
+        if (!warp_wait(T_QFULL0 + st, (gg >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        for (int i = 0; ok && i < g.n_tiles; ++i) {
-          const uint32_t gg = g0 + i;
-          const int st = gg & 1;
-          if (!mbar_wait(bar(T_QFULL0 + st), (gg >> 1) & 1, ctl, E + T_QFULL0 + st)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t qt = sQ + st * Ly::TILE;
-          const uint32_t dot = sDO + st * Ly::TILE;
+        const uint32_t qt = sQ + st * Ly::TILE;
+        const uint32_t dot = sDO + st * Ly::TILE;
+        if (leader) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
             mma_ss(tmem, desc_kmajor(sK, ks), desc_kmajor(qt, ks), kIdS, ks > 0 ? 1u : 0u);
-          // dP^T overwrites the previous tile's dQ~^T: wait until the dQ warps hold it
-          if (gg > 0 && !mbar_wait(bar(T_DQFREE), (gg - 1) & 1, ctl, E + T_DQFREE)) { ok = false; break; }
-          tc_fence_after();
+          tc_commit(bar(T_SRDY));
+        }
+        __syncwarp();
+        // dP^T overwrites the previous tile's dQ~^T: wait until the dQ warps hold it
+        if (gg > 0 && !warp_wait(T_DQFREE, (gg - 1) & 1)) { ok = false; break; }
+        if (!warp_wait(T_OFULL0 + st, (gg >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
             mma_ss(tmem + 128, desc_kmajor(sV, ks), desc_kmajor(dot, ks), kIdS, ks > 0 ? 1u : 0u);
-          tc_commit(bar(T_SFULL));
-          for (int c = 0; c < 4; ++c) {
-            if (!mbar_wait(bar(T_DSC0 + c), gg & 1, ctl, E + T_DSC0 + c)) { ok = false; break; }
-            // the previous unit's dV / dK must have been written out before the first accumulate
-            if (c == 0 && i == 0 && it > 0 && !mbar_wait(bar(T_DKVFREE), (it - 1) & 1, ctl, E + T_DKVFREE)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          tc_commit(bar(T_DPRDY));
+        }
+        __syncwarp();
+        // P^T of queries 0..63 is published while dP^T is still being computed
+        if (!warp_wait(T_PRDY, gg & 1)) { ok = false; break; }
+        // the previous unit's dV / dK must have been written out before the first accumulate
+        if (i == 0 && it > 0 && !warp_wait(T_DKVFREE, (it - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int ks = 2 * c + e;
-              mma_ts(tmem + 256, tmem + 16 * ks, desc_mnmajor(dot, ks), kIdDV, (i > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts(tmem + 256, tmem + 16 * ks, desc_mnmajor(dot, ks), kIdDV, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+        for (int c = 0; c < 4; ++c) {
+          if (!warp_wait(T_DSC0 + c, gg & 1)) { ok = false; break; }
+          tc_fence_after();
+          if (leader) {
+            if (c >= 2) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int ks = 2 * c + e;
+                mma_ts(tmem + 256, tmem + 16 * ks, desc_mnmajor(dot, ks), kIdDV, 1u);
+              }
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -637,34 +689,49 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
               mma_ss(tmem + 384, desc_kmajor(sDS, ks), desc_mnmajor(qt, ks), kIdDK, (i > 0 || ks > 0) ? 1u : 0u);
             }
           }
-          if (!ok) break;
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (leader) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             mma_ss(tmem + 128, desc_mnmajor(sK, ks), desc_mnmajor(sDS, ks), kIdDQ, ks > 0 ? 1u : 0u);
           tc_commit(bar(T_DQFULL));
-          tc_commit(bar(T_QEMPTY0 + st));
         }
-        if (!ok) break;
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (leader) {
         tc_commit(bar(T_DKVDONE));
         tc_commit(bar(T_KVEMPTY));
-        g0 += g.n_tiles;
       }
+      __syncwarp();
+      g0 += g.n_tiles;
+    }
+    if (leader) {
       tc_commit(bar(T_FINAL));
       mbar_drain(bar(T_FINAL), 0);
     }
+    __syncwarp();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ warps (8-15)
+    // Tile gg's Q~ and dO slots are dead once DQFULL(gg) fired (it follows the
+    // last MMA reading them) and stay so until the tile gg+2 refill: the two
+    // query halves of dQ~ are staged there as 64 x 128 fp32 row blocks and
+    // bulk-added into the accumulator; the slot is released when read out.
     const int j = (warp & 3) * 32 + lane;                    // channel d = TMEM lane of dQ~^T
-    const int qh = (warp - 8) >> 2;                          // query half of the tile
+    const int qh = (warp - 8) >> 2;                          // query half: 0 -> Q~ slot, 1 -> dO slot
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const bool half_leader = (warp & 3) == 0 && lane == 0;
     uint32_t g0 = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
       decode_unit_bwd(g, u, b, head, s, kt);
-      float* acc = p.dq_acc + (((size_t)b * g.heads + head) * g.k + s) * (size_t)p.Lp * D + j;
+      float* acc = p.dq_acc + (((size_t)b * g.heads + head) * g.k + s) * (size_t)p.Lp * D;
       for (int i = 0; i < g.n_tiles; ++i) {
         const uint32_t gg = g0 + i;
+        const int st = gg & 1;
         if (!bar_and<3, 256>(mbar_wait(bar(T_DQFULL), gg & 1, ctl, E + T_DQFULL))) { ok = false; break; }
         tc_fence_after();
         float x[64];
@@ -673,15 +740,23 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(T_DQFREE));
-        const int q0 = stagger(i, kt, g.n_tiles) * kTile + qh * 64;
-        const int nq = min(64, g.L - q0);
-        float* rowp = acc + (size_t)q0 * D;
+        float* slot = reinterpret_cast<float*>(smem + (qh ? Ly::DO_OFF : Ly::Q_OFF) + st * Ly::TILE);
 #pragma unroll
-        for (int q = 0; q < 64; ++q)
-          if (q < nq) atomicAdd(rowp + (size_t)q * D, x[q]);
+        for (int q = 0; q < 64; ++q) slot[q * D + j] = x[q];
+        fence_proxy_async_smem();
+        asm volatile("bar.sync %0, 128;" ::"r"(4 + qh) : "memory");
+        if (half_leader) {
+          const int q0 = stagger(i, kt, g.n_tiles) * kTile + qh * 64;   // rows < Lp: padded rows get zeros
+          bulk_reduce_add_f32(acc + (size_t)q0 * D, smem_u32(slot), 64 * D * 4);
+          bulk_commit_group();
+          bulk_wait_read<0>();
+          mbar_arrive(bar((qh ? T_OFREE0 : T_QFREE0) + st));
+        }
+        __syncwarp();
       }
       g0 += g.n_tiles;
     }
+    if (half_leader) bulk_wait_all();
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps (0-7)
     const int ch = warp >> 2;                                // which 16 queries of each 32-query chunk
@@ -699,45 +774,89 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
       for (int i = 0; i < g.n_tiles; ++i) {
         const uint32_t gg = g0 + i;
         const int st = gg & 1;
-        // SFULL also says the previous tile's MMAs (readers of the dS^T buffer) are done
-        if (!bar_and<2, 256>(mbar_wait(bar(T_SFULL), gg & 1, ctl, E + T_SFULL))) { ok = false; break; }
+        if (!bar_and<2, 256>(mbar_wait(bar(T_SRDY), gg & 1, ctl, E + T_SRDY))) { ok = false; break; }
         tc_fence_after();
         const float4* lse4 = reinterpret_cast<const float4*>(stats + st * 256);
         const float4* del4 = lse4 + 32;
         const int qvalid = key_ok ? min(kTile, g.L - stagger(i, kt, g.n_tiles) * kTile) : 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int qb = c * 32 + ch * 16;                   // first query of this thread's 16 columns
-          float sv[16], dp[16];
-          tmem_ld16x2(tmem + lane_base + qb, tmem + lane_base + 128 + qb, sv, dp);
-          uint32_t pk[8], dk[8];
+        // P = exp2(S * scale * log2(e) - lse * log2(e)) for this thread's 16 queries at qb (zero past the scope)
+        auto exp_p = [&](const float (&sv)[16], int qb, float (&pv)[16]) {
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
             const float4 l4 = lse4[(qb >> 2) + e4];
-            const float4 d4 = del4[(qb >> 2) + e4];
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dsv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int q = qb + e4 * 4 + e;
               const float pe = ex2(fmaf(sv[e4 * 4 + e], sl2, -lv[e]));
-              pv[e] = q < qvalid ? pe : 0.f;
-              dsv[e] = q < qvalid ? pe * (dp[e4 * 4 + e] - dv4[e]) : 0.f;
+              pv[e4 * 4 + e] = qb + e4 * 4 + e < qvalid ? pe : 0.f;
             }
-            pk[e4 * 2] = pack_bf16(pv[0], pv[1]);
-            pk[e4 * 2 + 1] = pack_bf16(pv[2], pv[3]);
+          }
+        };
+        auto store_pt = [&](const float (&pv)[16], int qb) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(pv[2 * e], pv[2 * e + 1]);
+          // P^T over this thread's own S^T columns qb .. qb+7 (already read by this thread)
+          tmem_st8(tmem + lane_base + qb, pk);
+        };
+        // dS^T = P^T * (dP^T - delta) -> row j of the dS^T buffer, queries qb .. qb+15
+        // (explicit zero past the scope: the padded delta entries are never written)
+        auto store_ds = [&](const float (&pv)[16], const float (&dp)[16], int c, int qb) {
+          uint32_t dk[8];
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 d4 = del4[(qb >> 2) + e4];
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dsv[e] = qb + e4 * 4 + e < qvalid ? pv[e4 * 4 + e] * (dp[e4 * 4 + e] - dv4[e]) : 0.f;
             dk[e4 * 2] = pack_bf16(dsv[0], dsv[1]);
             dk[e4 * 2 + 1] = pack_bf16(dsv[2], dsv[3]);
           }
-          tmem_st8(tmem + lane_base + qb, pk);
-          // dS^T row j, queries qb .. qb+15: box c/2, 16-byte chunks (c%2)*4 + ch*2 + {0,1}
+          // box c/2, 16-byte chunks (c%2)*4 + ch*2 + {0,1}
           uint8_t* rowp = ds_row + (c >> 1) * kHalfBytes;
 #pragma unroll
           for (int q2 = 0; q2 < 2; ++q2) {
             const int chunk = ((c & 1) * 4 + ch * 2 + q2) ^ (j & 7);
             *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(dk[4 * q2], dk[4 * q2 + 1], dk[4 * q2 + 2], dk[4 * q2 + 3]);
           }
+        };
+        // chunks 0 and 1: P^T first (the tensor core computes dP^T meanwhile), P kept in fp32
+        float p01[2][16];
+        {
+          float s0[16], s1[16];
+          tmem_ld16x2(tmem + lane_base + ch * 16, tmem + lane_base + 32 + ch * 16, s0, s1);
+          exp_p(s0, ch * 16, p01[0]);
+          exp_p(s1, 32 + ch * 16, p01[1]);
+          store_pt(p01[0], ch * 16);
+          store_pt(p01[1], 32 + ch * 16);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(T_PRDY));
+        }
+        // DPRDY also says the previous tile's MMAs (readers of the dS^T buffer) are done
+        if (!bar_and<2, 256>(mbar_wait(bar(T_DPRDY), gg & 1, ctl, E + T_DPRDY))) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float dp[16];
+          tmem_ld16(tmem + lane_base + 128 + c * 32 + ch * 16, dp);
+          store_ds(p01[c], dp, c, c * 32 + ch * 16);
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(T_DSC0 + c));
+        }
+#pragma unroll
+        for (int c = 2; c < 4; ++c) {
+          const int qb = c * 32 + ch * 16;
+          float sv[16], dp[16], pv[16];
+          tmem_ld16x2(tmem + lane_base + qb, tmem + lane_base + 128 + qb, sv, dp);
+          exp_p(sv, qb, pv);
+          store_pt(pv, qb);
+          store_ds(pv, dp, c, qb);
           tmem_st_wait();
           fence_proxy_async_smem();
           tc_fence_before();

@@ -289,6 +289,7 @@ __device__ __forceinline__ void bulk_wait_all() {
 template <int ID, int NTHREADS>
 __device__ __forceinline__ bool bar_and(bool v) {
   uint32_t out;
+  __syncwarp();   // bar.red is the aligned form: the warp must arrive converged
   asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
                "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
                : "=r"(out) : "r"(v ? 1u : 0u), "n"(ID), "n"(NTHREADS) : "memory");
