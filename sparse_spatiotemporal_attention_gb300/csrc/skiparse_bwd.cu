@@ -28,6 +28,8 @@
 // 4-7 one query row each for the dQ~ adds (vector atomics), warp 8 TMA, warp 9 MMA.
 // TMEM columns: S^T (P^T as bf16) 0..127, dP^T / dQ~ partial 128..255,
 // dV 256..383, dK~ 384..511.
+#include <type_traits>
+
 #include "skiparse_internal.h"
 
 namespace skp {
@@ -722,7 +724,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     const int j = (warp & 3) * 32 + lane;                    // channel d = TMEM lane of dQ~^T
     const int qh = (warp - 8) >> 2;                          // query half: 0 -> Q~ slot, 1 -> dO slot
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const bool half_leader = (warp & 3) == 0 && lane == 0;
+    const bool leader = tid == 256;
     uint32_t g0 = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
@@ -744,19 +746,24 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
 #pragma unroll
         for (int q = 0; q < 64; ++q) slot[q * D + j] = x[q];
         fence_proxy_async_smem();
-        asm volatile("bar.sync %0, 128;" ::"r"(4 + qh) : "memory");
-        if (half_leader) {
-          const int q0 = stagger(i, kt, g.n_tiles) * kTile + qh * 64;   // rows < Lp: padded rows get zeros
-          bulk_reduce_add_f32(acc + (size_t)q0 * D, smem_u32(slot), 64 * D * 4);
+        asm volatile("bar.sync 4, 256;" ::: "memory");
+        if (leader) {
+          // the Q~ slot's half first: Q~ of tile gg+2 is needed before its dO
+          const int q0 = stagger(i, kt, g.n_tiles) * kTile;   // rows < Lp: padded rows get zeros
+          bulk_reduce_add_f32(acc + (size_t)q0 * D, smem_u32(smem + Ly::Q_OFF + st * Ly::TILE), 64 * D * 4);
           bulk_commit_group();
+          bulk_reduce_add_f32(acc + (size_t)(q0 + 64) * D, smem_u32(smem + Ly::DO_OFF + st * Ly::TILE), 64 * D * 4);
+          bulk_commit_group();
+          bulk_wait_read<1>();
+          mbar_arrive(bar(T_QFREE0 + st));
           bulk_wait_read<0>();
-          mbar_arrive(bar((qh ? T_OFREE0 : T_QFREE0) + st));
+          mbar_arrive(bar(T_OFREE0 + st));
         }
         __syncwarp();
       }
       g0 += g.n_tiles;
     }
-    if (half_leader) bulk_wait_all();
+    if (leader) bulk_wait_all();
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps (0-7)
     const int ch = warp >> 2;                                // which 16 queries of each 32-query chunk
@@ -779,16 +786,25 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         const float4* lse4 = reinterpret_cast<const float4*>(stats + st * 256);
         const float4* del4 = lse4 + 32;
         const int qvalid = key_ok ? min(kTile, g.L - stagger(i, kt, g.n_tiles) * kTile) : 0;
-        // P = exp2(S * scale * log2(e) - lse * log2(e)) for this thread's 16 queries at qb (zero past the scope)
-        auto exp_p = [&](const float (&sv)[16], int qb, float (&pv)[16]) {
+        // Full tiles (every key row of the warp and every query of the tile inside
+        // the scope: all but the last query or key tile) take a select-free path;
+        // rows and columns past the scope are zeroed otherwise. Warp-uniform, so
+        // both paths keep their warp-level synchronisation.
+        const bool full = __all_sync(0xffffffffu, qvalid == kTile) != 0;
+        const unsigned long long sl2x2 = f2_pack(sl2, sl2);
+        // P = exp2(S * scale * log2(e) - lse * log2(e)) for this thread's 16 queries at qb
+        auto exp_p = [&](auto F, const float (&sv)[16], int qb, float (&pv)[16]) {
+          constexpr bool FULL = decltype(F)::value;
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
             const float4 l4 = lse4[(qb >> 2) + e4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float a[4];
+            f2_unpack(ffma2(f2_pack(sv[e4 * 4], sv[e4 * 4 + 1]), sl2x2, f2_pack(-l4.x, -l4.y)), a[0], a[1]);
+            f2_unpack(ffma2(f2_pack(sv[e4 * 4 + 2], sv[e4 * 4 + 3]), sl2x2, f2_pack(-l4.z, -l4.w)), a[2], a[3]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float pe = ex2(fmaf(sv[e4 * 4 + e], sl2, -lv[e]));
-              pv[e4 * 4 + e] = qb + e4 * 4 + e < qvalid ? pe : 0.f;
+              const float pe = ex2(a[e]);
+              pv[e4 * 4 + e] = (FULL || qb + e4 * 4 + e < qvalid) ? pe : 0.f;
             }
           }
         };
@@ -801,16 +817,22 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         };
         // dS^T = P^T * (dP^T - delta) -> row j of the dS^T buffer, queries qb .. qb+15
         // (explicit zero past the scope: the padded delta entries are never written)
-        auto store_ds = [&](const float (&pv)[16], const float (&dp)[16], int c, int qb) {
+        auto store_ds = [&](auto F, const float (&pv)[16], const float (&dp)[16], int c, int qb) {
+          constexpr bool FULL = decltype(F)::value;
           uint32_t dk[8];
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
             const float4 d4 = del4[(qb >> 2) + e4];
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
             float dsv[4];
+            f2_unpack(fmul2(f2_pack(pv[e4 * 4], pv[e4 * 4 + 1]),
+                            fsub2(f2_pack(dp[e4 * 4], dp[e4 * 4 + 1]), f2_pack(d4.x, d4.y))), dsv[0], dsv[1]);
+            f2_unpack(fmul2(f2_pack(pv[e4 * 4 + 2], pv[e4 * 4 + 3]),
+                            fsub2(f2_pack(dp[e4 * 4 + 2], dp[e4 * 4 + 3]), f2_pack(d4.z, d4.w))), dsv[2], dsv[3]);
+            if (!FULL) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dsv[e] = qb + e4 * 4 + e < qvalid ? pv[e4 * 4 + e] * (dp[e4 * 4 + e] - dv4[e]) : 0.f;
+              for (int e = 0; e < 4; ++e)
+                if (qb + e4 * 4 + e >= qvalid) dsv[e] = 0.f;
+            }
             dk[e4 * 2] = pack_bf16(dsv[0], dsv[1]);
             dk[e4 * 2 + 1] = pack_bf16(dsv[2], dsv[3]);
           }
@@ -824,45 +846,51 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         };
         // chunks 0 and 1: P^T first (the tensor core computes dP^T meanwhile), P kept in fp32
         float p01[2][16];
-        {
+        auto p_phase = [&](auto F) {
           float s0[16], s1[16];
           tmem_ld16x2(tmem + lane_base + ch * 16, tmem + lane_base + 32 + ch * 16, s0, s1);
-          exp_p(s0, ch * 16, p01[0]);
-          exp_p(s1, 32 + ch * 16, p01[1]);
+          exp_p(F, s0, ch * 16, p01[0]);
+          exp_p(F, s1, 32 + ch * 16, p01[1]);
           store_pt(p01[0], ch * 16);
           store_pt(p01[1], 32 + ch * 16);
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(T_PRDY));
-        }
+        };
+        if (full) p_phase(std::true_type{});
+        else p_phase(std::false_type{});
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(T_PRDY));
         // DPRDY also says the previous tile's MMAs (readers of the dS^T buffer) are done
         if (!bar_and<2, 256>(mbar_wait(bar(T_DPRDY), gg & 1, ctl, E + T_DPRDY))) { ok = false; break; }
         tc_fence_after();
+        auto ds_phase = [&](auto F) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float dp[16];
-          tmem_ld16(tmem + lane_base + 128 + c * 32 + ch * 16, dp);
-          store_ds(p01[c], dp, c, c * 32 + ch * 16);
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(T_DSC0 + c));
-        }
+          for (int c = 0; c < 2; ++c) {
+            float dp[16];
+            tmem_ld16(tmem + lane_base + 128 + c * 32 + ch * 16, dp);
+            store_ds(F, p01[c], dp, c, c * 32 + ch * 16);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(T_DSC0 + c));
+          }
 #pragma unroll
-        for (int c = 2; c < 4; ++c) {
-          const int qb = c * 32 + ch * 16;
-          float sv[16], dp[16], pv[16];
-          tmem_ld16x2(tmem + lane_base + qb, tmem + lane_base + 128 + qb, sv, dp);
-          exp_p(sv, qb, pv);
-          store_pt(pv, qb);
-          store_ds(pv, dp, c, qb);
-          tmem_st_wait();
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(T_DSC0 + c));
-        }
+          for (int c = 2; c < 4; ++c) {
+            const int qb = c * 32 + ch * 16;
+            float sv[16], dp[16], pv[16];
+            tmem_ld16x2(tmem + lane_base + qb, tmem + lane_base + 128 + qb, sv, dp);
+            exp_p(F, sv, qb, pv);
+            store_pt(pv, qb);
+            store_ds(F, pv, dp, c, qb);
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(T_DSC0 + c));
+          }
+        };
+        if (full) ds_phase(std::true_type{});
+        else ds_phase(std::false_type{});
       }
       if (!ok) break;
       // ---- epilogue: warps 0-3 write dv, warps 4-7 write dk = scale * R^T dK~ (key row j)
