@@ -47,7 +47,7 @@ WORKLOADS = {
                       mode=1),
 }
 WORKLOAD = WORKLOADS["train"]
-KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0}   # x forward FLOPs, per launch
+KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0, 4: 0.0}   # x forward FLOPs, per launch
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -229,10 +229,12 @@ def gpu_arm(args):
     dq, dk, dv = (torch.empty_like(d["q"]) for _ in range(3))
     ws = torch.empty(skp.skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, k, mode), dtype=torch.uint8,
                      device=dev)
+    fws = torch.empty(skp.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, k, mode), dtype=torch.uint8,
+                      device=dev)
     stream = torch.cuda.current_stream()
 
     def step(kk=k):
-        skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, mode, stream=stream)
+        skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, mode, stream=stream, workspace=fws)
         skp.skiparse_attn_bwd(d["q"], d["k"], d["v"], out, lse, d["do"], dq, dk, dv, ws, T, H, W, kk, mode,
                               stream=stream)
 
@@ -263,7 +265,8 @@ def gpu_arm(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    kms, kcnt = skp.skiparse_trace_end(4)
+    nk = len(skp.KERNEL_NAMES)
+    kms, kcnt = skp.skiparse_trace_end(nk)
     clocks = sampler.stop()
     ms = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms / args.steps
@@ -319,16 +322,16 @@ def gpu_arm(args):
     peaks, src = load_peaks()
     kernels = {}
     tot = sum(kms) or 1.0
-    for i in range(4):
+    for i in range(nk):
         if kcnt[i]:
             kernels[skp.KERNEL_NAMES[i]] = {"launches": kcnt[i], "ms_per_launch": kms[i] / kcnt[i],
                                             "share": kms[i] / tot}
-    dom = max(range(4), key=lambda i: kms[i])
+    dom = max(range(nk), key=lambda i: kms[i])
     dom_ms = kms[dom] / max(1, kcnt[dom])
     dom_flops = KERNEL_FLOP_FACTOR[dom] * fwd_flops(w)
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    fwd_ms = kms[0] / max(1, kcnt[0])
+    fwd_ms = (kms[0] + kms[4]) / max(1, kcnt[0])     # RoPE pass + attention kernel
     roofline = {"bound": "tensor", "kernel": skp.KERNEL_NAMES[dom], "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic_record(skp.KERNEL_NAMES[dom]),
                 "peak_source": f"{src} bf16 sustained (kernel timed inside a long step loop)",

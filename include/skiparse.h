@@ -57,16 +57,31 @@ typedef enum {
 } skiparse_status_t;
 
 /*
+ * Bytes of device workspace skiparse_attn_fwd needs for these sizes: rotated
+ * bf16 copies of q and k (2 * B*N*heads*D*2 bytes, each rounded up to 256).
+ * Returns 0 for empty or invalid sizes.
+ */
+size_t skiparse_attn_fwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
+                                         int sparse_k, int mode);
+
+/*
  * Forward pass. Page: "Open-Sora Plan" docs, "Skiparse Attention", both
  * implementation listings (RoPE, rearrange, scaled_dot_product_attention,
- * reverse rearrange), fused into one persistent kernel.
+ * reverse rearrange): a RoPE kernel that rotates q and k once into the
+ * workspace, then one persistent attention kernel over the scopes.
  *   q, k, v   in : bf16 (B, N, heads, D), the PRE-RoPE projections.
  *   out       out: bf16 (B, N, heads, D), fully overwritten.
  *   lse       out: fp32 (B, heads, N), natural-log LSE of each query row.
+ *   workspace scratch: device memory of at least
+ *             skiparse_attn_fwd_workspace_bytes(...) bytes, 256-byte aligned,
+ *             owned by the caller, contents ignored on entry; on return it
+ *             holds the rotated q and k (row layout of q). Must not overlap
+ *             any tensor. SKIPARSE_ERR_WORKSPACE when NULL or too small.
  *   D in {64, 128}; sparse_k >= 1; mode is a skiparse_mode_t; rope_theta > 0.
  *   Group mode needs sparse_k to divide 128.
  */
 int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes,
                       int B, int heads, int N, int D, int T, int H, int W,
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
@@ -152,7 +167,8 @@ int skiparse_device_error(int* detail);
  * launch is bracketed by CUDA events on its stream. skiparse_trace_end()
  * synchronises on them and writes, per kernel id, the summed device time in ms
  * and the launch count (arrays of n entries, host memory). Kernel ids:
- * 0 forward, 1 backward preprocess, 2 backward main, 3 backward post.
+ * 0 forward attention, 1 backward preprocess, 2 backward main, 3 backward
+ * post, 4 forward RoPE.
  */
 int skiparse_trace_begin(void);
 int skiparse_trace_end(float* ms_per_kernel, int* launches_per_kernel, int n);

@@ -17,13 +17,13 @@ import os
 SINGLE = 0
 GROUP = 1
 KERNEL_NAMES = ("skiparse_fwd_kernel", "skiparse_bwd_pre_kernel", "skiparse_bwd_main_kernel",
-                "skiparse_bwd_post_kernel")
+                "skiparse_bwd_post_kernel", "skiparse_fwd_rope_kernel")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libskiparse.so")
 
 EXPORTS = (
-    "skiparse_attn_fwd", "skiparse_attn_bwd_workspace_bytes", "skiparse_attn_bwd",
+    "skiparse_attn_fwd_workspace_bytes", "skiparse_attn_fwd", "skiparse_attn_bwd_workspace_bytes", "skiparse_attn_bwd",
     "skiparse_debug_index_map", "skiparse_debug_rope", "skiparse_status_string",
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
     "skiparse_attn_bwd_noalloc",
@@ -52,7 +52,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
     lib = ctypes.CDLL(path)
     sig = {
-        "skiparse_attn_fwd": (_c_int, [_vp] * 5 + [_c_int] * 9 + [_c_float, _vp]),
+        "skiparse_attn_fwd_workspace_bytes": (_c_size, [_c_int] * 9),
+        "skiparse_attn_fwd": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_bwd_workspace_bytes": (_c_size, [_c_int] * 9),
         "skiparse_attn_bwd": (_c_int, [_vp] * 10 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_debug_index_map": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _vp]),
@@ -106,10 +107,24 @@ def _shape(q):
     return int(B), int(heads), int(N), int(D)
 
 
-def skiparse_attn_fwd(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=10000.0, stream=None):
-    """Forward pass into caller-allocated out (bf16, like q) and lse (fp32 (B, heads, N))."""
+def skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode) -> int:
+    return int(load_library().skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode))
+
+
+def skiparse_attn_fwd(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=10000.0, stream=None,
+                      workspace=None, workspace_bytes=None):
+    """Forward pass into caller-allocated out (bf16, like q) and lse (fp32 (B, heads, N)).
+    `workspace` is a device buffer of at least skiparse_attn_fwd_workspace_bytes(...)
+    bytes; when None, one is taken from torch's caching allocator for this call."""
     B, heads, N, D = _shape(q)
+    if workspace is None:
+        import torch
+        nbytes = skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
     st = load_library().skiparse_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                          _ptr(workspace), int(workspace_bytes),
                                           B, heads, N, D, T, H, W, sparse_k, mode,
                                           float(rope_theta), _stream(stream))
     _check(st, "skiparse_attn_fwd")
@@ -173,7 +188,7 @@ def skiparse_trace_begin():
     _check(load_library().skiparse_trace_begin(), "skiparse_trace_begin")
 
 
-def skiparse_trace_end(n: int = 4):
+def skiparse_trace_end(n: int = 5):
     """Returns ([ms per kernel id], [launches per kernel id])."""
     ms = (_c_float * n)()
     cnt = (_c_int * n)()

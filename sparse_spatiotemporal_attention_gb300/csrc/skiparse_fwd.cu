@@ -1,4 +1,4 @@
-// Skiparse attention forward: one persistent kernel per call.
+// Skiparse attention forward: a RoPE pass and one persistent attention kernel.
 //
 // What it computes ("Open-Sora Plan" docs, "Skiparse Attention", single and
 // group skip listings): for every (batch b, head, scope s) the softmax
@@ -8,23 +8,27 @@
 // address the scope's rows directly (see skiparse_host.cu), and the epilogue
 // stores each output row at its original token index.
 //
-// One work unit = (b, head, s, a pair of 128-row Q tiles A and B), so every
-// K / V tile is loaded and rotated once for 256 query rows. Warp roles:
+// RoPE pass: one warp per (b, token, head) row rotates q and k once into the
+// caller's workspace (row layout unchanged). Every K tile is read by all the
+// query-tile pairs of its scope, so rotating it once here instead of in each
+// attention CTA removes L/256 redundant rotations per tile.
+//
+// Attention: one work unit = (b, head, s, a pair of 128-row Q tiles A and B),
+// so every K / V tile is loaded once for 256 query rows. Warp roles:
 //   warps 0-3   softmax for Q tile A, one query row per thread (TMEM lane);
 //   warps 4-7   softmax for Q tile B;
-//   warps 8-11  RoPE: rotate the Q tiles and each K tile in shared memory
-//               (16-byte chunks, per-row table offsets staged in shared memory);
-//   warp  12    TMA producer: Q pair, then a 2-stage K / V ring;
-//   warp  13    MMA issuer (tcgen05.mma kind::f16, fp32 accumulators in TMEM).
+//   warp  8     TMA producer: rotated Q pair, then a 2-stage K / V ring;
+//   warp  9     MMA issuer (tcgen05.mma kind::f16, fp32 accumulators in TMEM).
+// The TMA and MMA warps run their loops with all lanes (waits voted across the
+// warp), lane 0 issuing.
 // TMEM columns: S_A / P_A 0..127, S_B / P_B 128..255, O_A 256.., O_B 384...
 // MMA issue order: S_A(g), S_B(g), PV_A(g), S_A(g+1), PV_B(g), S_B(g+1), ...
 // so each softmax warpgroup's critical loop is softmax + two MMA groups while
 // the tensor core alternates between the two Q tiles. Because S_X(g) is issued
 // after PV_X(g-1), the S-full barrier of tile g proves PV_X(g-1) complete, which
 // keeps every parity wait on the O-done barriers one phase ahead at most.
-// The softmax reads S twice from TMEM (max pass, then exp pass) so that all 14
-// warps fit in 128 registers; online softmax with lazy O rescaling (threshold
-// 2^8), P written back over S as bf16.
+// The softmax reads S twice from TMEM (max pass, then exp pass); online softmax
+// with lazy O rescaling (threshold 2^8), P written back over S as bf16.
 #include "skiparse_internal.h"
 
 namespace skp {
@@ -38,18 +42,18 @@ struct FwdLayout {
   static constexpr int QB_OFF = QA_OFF + TILE;
   static constexpr int K_OFF = QB_OFF + TILE;
   static constexpr int V_OFF = K_OFF + 2 * TILE;
-  static constexpr int ROWOFF_OFF = V_OFF + 2 * TILE;   // [2][128] int4 per-row RoPE table offsets
-  static constexpr int ROPE_OFF = ROWOFF_OFF + 2 * 128 * 16;
+  static constexpr int BYTES = V_OFF + 2 * TILE;
 };
 
 enum FwdBar {
-  F_QFULL, F_QROT, F_QEMPTY,
-  F_KFULL0, F_KFULL1, F_KROT0, F_KROT1, F_KEMPTY0, F_KEMPTY1,
+  F_QFULL, F_QEMPTY,
+  F_KFULL0, F_KFULL1, F_KEMPTY0, F_KEMPTY1,
   F_VFULL0, F_VFULL1, F_VEMPTY0, F_VEMPTY1,
   F_SFULL_A, F_SFULL_B, F_PFULL_A, F_PFULL_B, F_ODONE_A, F_ODONE_B, F_OEMPTY_A, F_OEMPTY_B, F_FINAL, F_NBARS
 };
 
-constexpr int kFwdThreads = 448;
+constexpr int kFwdThreads = 320;
+constexpr int kRopeThreads = 256;
 
 __device__ __forceinline__ void decode_unit(const Geom& g, int n_pairs, int u, int& b, int& head, int& s, int& pair) {
   pair = u % n_pairs;
@@ -60,74 +64,74 @@ __device__ __forceinline__ void decode_unit(const Geom& g, int n_pairs, int u, i
   b = r / g.heads;
 }
 
-// Named barrier over the 4 RoPE warps that also ANDs a predicate across them,
-// so that every RoPE warp takes the same branch after a bounded wait.
-__device__ __forceinline__ bool rope_bar_and(bool v) {
-  uint32_t out;
-  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-               "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-               : "=r"(out) : "r"(v ? 1u : 0u) : "memory");
-  return out != 0;
-}
-
-// Rotate the rows of one 128-row tile in shared memory, in place. The tile
-// holds positions p0 .. p0+127 of scope s; rows at or past L are left alone.
-// Step 1: RoPE thread r (0..127) stores row r's table offsets in `rowoff`
-// (entry of pair 0 of the t, h and w chunks at the row's position, and a
-// valid flag). Step 2, after the barrier (which also ANDs `ok`): a lane owns
-// one 16-byte chunk (4 channel pairs, always inside one axis chunk) of one of
-// 4 rows, so a warp touches 4 whole 128-byte rows per step. Returns false if
-// any RoPE thread passed in ok = false (then nothing is rotated).
+// ---------------------------------------------------------------------------
+// RoPE pass: q, k (pre-RoPE) -> rotated copies in the workspace. One warp per
+// (b, token, head) row, two rows per iteration so each lane has four 8-byte
+// loads in flight; lane l owns channel pairs l*PPL .. l*PPL+PPL-1.
+// ---------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ bool rope_tile(uint8_t* tile, int4* rowoff, int p0, int s, const Geom& g,
-                                          const RopeParams& rp, const float2* tab, int rtid, int lane, bool ok) {
-  constexpr int HALVES = D / 64;
-  {
-    const int p = p0 + rtid;
-    int4 ro = make_int4(0, 0, 0, 0);
-    if (ok && p < g.L) {
-      int t, hh, w;
-      token_coords(rp, token_of(g, s, p), t, hh, w);
-      const int bt = rp.T * rp.dt2;
-      ro = make_int4(t * rp.dt2, bt + hh * rp.dh2, bt + rp.H * rp.dh2 + w * rp.dh2, 1);
+__global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_rope_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ float2 tab[];
+  const Geom& g = p.g;
+  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  __syncthreads();
+  constexpr int PPL = D / 64;
+  const int lane = threadIdx.x & 31;
+  const long long wpb = blockDim.x >> 5;
+  PairSel sel[PPL];
+#pragma unroll
+  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
+  const long long rows = (long long)g.B * g.N * g.heads;
+  const long long stride = (long long)gridDim.x * wpb;
+  for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += 2 * stride) {
+    uint32_t qv[2][PPL], kv[2][PPL];
+    int tt[2], th[2], tw[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long row = r0 + u * stride;
+      if (row >= rows) continue;
+      const int i = (int)((row / g.heads) % g.N);
+      token_coords(p.rope, i, tt[u], th[u], tw[u]);
+      const size_t base = (size_t)row * D + lane * 2 * PPL;
+      if (PPL == 2) {
+        const uint2 a = *reinterpret_cast<const uint2*>(p.q + base);
+        const uint2 c = *reinterpret_cast<const uint2*>(p.k + base);
+        qv[u][0] = a.x; qv[u][PPL - 1] = a.y; kv[u][0] = c.x; kv[u][PPL - 1] = c.y;
+      } else {
+        qv[u][0] = *reinterpret_cast<const uint32_t*>(p.q + base);
+        kv[u][0] = *reinterpret_cast<const uint32_t*>(p.k + base);
+      }
     }
-    rowoff[rtid] = ro;
-  }
-  if (!rope_bar_and(ok)) return false;
-  const int wid = rtid >> 5;
-  const int rsub = lane >> 3;
-  const int c = lane & 7;
-  int axis[HALVES], local[HALVES];
 #pragma unroll
-  for (int hb = 0; hb < HALVES; ++hb) {
-    const PairSel sel = pair_select(rp, (hb * 8 + c) * 4);
-    axis[hb] = sel.axis;
-    local[hb] = sel.local;
-  }
-#pragma unroll 2
-  for (int it = 0; it < 8; ++it) {
-    const int r = wid * 32 + it * 4 + rsub;
-    const int4 ro = rowoff[r];
-    if (!ro.w) continue;
+    for (int u = 0; u < 2; ++u) {
+      const long long row = r0 + u * stride;
+      if (row >= rows) continue;
+      uint32_t qo[PPL], ko[PPL];
 #pragma unroll
-    for (int hb = 0; hb < HALVES; ++hb) {
-      const int e = (axis[hb] == 0 ? ro.x : (axis[hb] == 1 ? ro.y : ro.z)) + local[hb];
-      const float4 cs01 = *reinterpret_cast<const float4*>(tab + e);
-      const float4 cs23 = *reinterpret_cast<const float4*>(tab + e + 2);
-      uint4* ptr = reinterpret_cast<uint4*>(tile + hb * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4));
-      const uint4 v = *ptr;
-      const float2 a0 = rope_rotate(bf16lo(v.x), bf16hi(v.x), make_float2(cs01.x, cs01.y));
-      const float2 a1 = rope_rotate(bf16lo(v.y), bf16hi(v.y), make_float2(cs01.z, cs01.w));
-      const float2 a2 = rope_rotate(bf16lo(v.z), bf16hi(v.z), make_float2(cs23.x, cs23.y));
-      const float2 a3 = rope_rotate(bf16lo(v.w), bf16hi(v.w), make_float2(cs23.z, cs23.w));
-      *ptr = make_uint4(pack_bf16(a0.x, a0.y), pack_bf16(a1.x, a1.y), pack_bf16(a2.x, a2.y), pack_bf16(a3.x, a3.y));
+      for (int e = 0; e < PPL; ++e) {
+        const float2 cs = tab[pair_index(sel[e], tt[u], th[u], tw[u])];
+        const float2 a = rope_rotate(bf16lo(qv[u][e]), bf16hi(qv[u][e]), cs);
+        const float2 c = rope_rotate(bf16lo(kv[u][e]), bf16hi(kv[u][e]), cs);
+        qo[e] = pack_bf16(a.x, a.y);
+        ko[e] = pack_bf16(c.x, c.y);
+      }
+      const size_t base = (size_t)row * D + lane * 2 * PPL;
+      if (PPL == 2) {
+        *reinterpret_cast<uint2*>(p.qr + base) = make_uint2(qo[0], qo[PPL - 1]);
+        *reinterpret_cast<uint2*>(p.kr + base) = make_uint2(ko[0], ko[PPL - 1]);
+      } else {
+        *reinterpret_cast<uint32_t*>(p.qr + base) = qo[0];
+        *reinterpret_cast<uint32_t*>(p.kr + base) = ko[0];
+      }
     }
   }
-  return true;
 }
 
+// ---------------------------------------------------------------------------
+// Attention over rotated q / k
+// ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __grid_constant__ FwdParams p) {
   using Ly = FwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -140,8 +144,6 @@ __global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
   int* abort_flag = reinterpret_cast<int*>(smem + 520);
-  float2* tab = reinterpret_cast<float2*>(smem + Ly::ROPE_OFF);
-  int4* rowoff = reinterpret_cast<int4*>(smem + Ly::ROWOFF_OFF);
   const uint32_t sQA = smem_u32(smem + Ly::QA_OFF);
   const uint32_t sQB = smem_u32(smem + Ly::QB_OFF);
   const uint32_t sK = smem_u32(smem + Ly::K_OFF);
@@ -151,34 +153,40 @@ __global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_const
   const Ctl ctl{abort_flag, p.err};
   const Geom& g = p.g;
   const int n_pairs = (g.n_tiles + 1) >> 1;
+  constexpr int E = ERR_KERNEL_FWD;
 
   if (tid == 0) {
     *abort_flag = 0;
-    const uint32_t counts[F_NBARS] = {1, 4, 1, 1, 1, 4, 4, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 4, 4, 1};
+    const uint32_t counts[F_NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 4, 4, 1};
     for (int i = 0; i < F_NBARS; ++i) mbar_init(bar(i), counts[i]);
     mbar_fence_init();
   }
-  if (warp == 13) tmem_alloc(smem_u32(tmem_slot), 512);
-  rope_build_table(tab, p.rope, tid, kFwdThreads);
+  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  auto warp_wait = [&](int i, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ctl, E + i)) != 0;
+  };
+  const bool leader = lane == 0;
 
-  if (warp == 12) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (leader) {
       tma_prefetch_map(&p.tm_q);
       tma_prefetch_map(&p.tm_k);
       tma_prefetch_map(&p.tm_v);
-      uint32_t q_issued = 0, k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
-      uint32_t gk = 0;
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-        int b, head, s, pair;
-        decode_unit(g, n_pairs, u, b, head, s, pair);
-        if (it > 0 && !mbar_wait(bar(F_QEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_QEMPTY)) break;
+    }
+    uint32_t q_issued = 0, k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
+    uint32_t gk = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      int b, head, s, pair;
+      decode_unit(g, n_pairs, u, b, head, s, pair);
+      if (it > 0 && !warp_wait(F_QEMPTY, (it - 1) & 1)) break;
+      if (leader) {
         mbar_expect_tx(bar(F_QFULL), 2 * Ly::TILE);
         const int qrow = b * g.Nn + (2 * pair * kTile) / g.G;
 #pragma unroll
@@ -186,91 +194,110 @@ __global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_const
           tma_load_5d(sQA + h * kHalfBytes, &p.tm_q, bar(F_QFULL), h * 64, head, 0, s, qrow);
           tma_load_5d(sQB + h * kHalfBytes, &p.tm_q, bar(F_QFULL), h * 64, head, 0, s, qrow + kTile / g.G);
         }
-        ++q_issued;
-        for (int j = 0; j < g.n_tiles; ++j) {
-          const uint32_t gg = gk + j;
-          const int st = gg & 1;
-          const uint32_t n = gg >> 1;
-          const int krow = b * g.Nn + (j * kTile) / g.G;
-          if (n > 0 && !mbar_wait(bar(F_KEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_FWD + F_KEMPTY0 + st)) { ok = false; break; }
+      }
+      __syncwarp();
+      ++q_issued;
+      for (int j = 0; j < g.n_tiles; ++j) {
+        const uint32_t gg = gk + j;
+        const int st = gg & 1;
+        const uint32_t n = gg >> 1;
+        const int krow = b * g.Nn + (j * kTile) / g.G;
+        if (n > 0 && !warp_wait(F_KEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
+        if (leader) {
           mbar_expect_tx(bar(F_KFULL0 + st), Ly::TILE);
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h)
             tma_load_5d(sK + st * Ly::TILE + h * kHalfBytes, &p.tm_k, bar(F_KFULL0 + st), h * 64, head, 0, s, krow);
-          ++k_issued[st];
-          if (n > 0 && !mbar_wait(bar(F_VEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_FWD + F_VEMPTY0 + st)) { ok = false; break; }
+        }
+        __syncwarp();
+        ++k_issued[st];
+        if (n > 0 && !warp_wait(F_VEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
+        if (leader) {
           mbar_expect_tx(bar(F_VFULL0 + st), Ly::TILE);
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h)
             tma_load_5d(sV + st * Ly::TILE + h * kHalfBytes, &p.tm_v, bar(F_VFULL0 + st), h * 64, head, 0, s, krow);
-          ++v_issued[st];
         }
-        gk += g.n_tiles;
+        __syncwarp();
+        ++v_issued[st];
       }
-      // Copies still in flight (only after an abort) must land before exit.
+      gk += g.n_tiles;
+    }
+    // Copies still in flight (only after an abort) must land before exit.
+    if (leader) {
       if (q_issued) mbar_drain(bar(F_QFULL), (q_issued - 1) & 1);
       for (int st = 0; st < 2; ++st) {
         if (k_issued[st]) mbar_drain(bar(F_KFULL0 + st), (k_issued[st] - 1) & 1);
         if (v_issued[st]) mbar_drain(bar(F_VFULL0 + st), (v_issued[st] - 1) & 1);
       }
     }
-  } else if (warp == 13) {
+    __syncwarp();
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
-      uint32_t g0 = 0;
-      int it = 0;
-      bool ok = true;
-      // S_X = Q_X K_g^T into TMEM columns colS (X = A: 0, B: 128)
-      auto issue_s = [&](uint32_t qt, uint32_t colS, int st) {
-        const uint32_t kt = sK + st * Ly::TILE;
+    constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+    uint32_t g0 = 0;
+    int it = 0;
+    bool ok = true;
+    // S_X = Q_X K_g^T into TMEM columns colS (X = A: 0, B: 128)
+    auto issue_s = [&](uint32_t qt, uint32_t colS, int st) {
+      const uint32_t kt = sK + st * Ly::TILE;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + colS, desc_kmajor(qt, ks), desc_kmajor(kt, ks), kIdS, ks > 0 ? 1u : 0u);
-      };
-      // O_X += P_X V_g, P_X in TMEM over S_X
-      auto issue_pv = [&](uint32_t colS, uint32_t colO, int st, bool first) {
-        const uint32_t vt = sV + st * Ly::TILE;
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_ss(tmem + colS, desc_kmajor(qt, ks), desc_kmajor(kt, ks), kIdS, ks > 0 ? 1u : 0u);
+    };
+    // O_X += P_X V_g, P_X in TMEM over S_X
+    auto issue_pv = [&](uint32_t colS, uint32_t colO, int st, bool first) {
+      const uint32_t vt = sV + st * Ly::TILE;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tmem + colO, tmem + colS + ks * 8, desc_mnmajor(vt, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
-      };
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-        const int n = g.n_tiles;
-        if (!mbar_wait(bar(F_QROT), it & 1, ctl, ERR_KERNEL_FWD + F_QROT)) break;
-        if (!mbar_wait(bar(F_KROT0 + (g0 & 1)), (g0 >> 1) & 1, ctl, ERR_KERNEL_FWD + F_KROT0)) break;
-        tc_fence_after();
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ts(tmem + colO, tmem + colS + ks * 8, desc_mnmajor(vt, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
+    };
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      const int n = g.n_tiles;
+      if (!warp_wait(F_QFULL, it & 1)) break;
+      if (!warp_wait(F_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
+      tc_fence_after();
+      if (leader) {
         issue_s(sQA, 0, g0 & 1);
         tc_commit(bar(F_SFULL_A));
         issue_s(sQB, 128, g0 & 1);
         tc_commit(bar(F_SFULL_B));
         tc_commit(bar(F_KEMPTY0 + (g0 & 1)));
         if (n == 1) tc_commit(bar(F_QEMPTY));
-        for (int j = 0; j < n; ++j) {
-          const uint32_t gg = g0 + j;
-          const int st = gg & 1;
-          const uint32_t nn = gg >> 1;
-          // PV_A(g)
-          if (j == 0 && it > 0 && !mbar_wait(bar(F_OEMPTY_A), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_OEMPTY_A)) { ok = false; break; }
-          if (!mbar_wait(bar(F_PFULL_A), gg & 1, ctl, ERR_KERNEL_FWD + F_PFULL_A)) { ok = false; break; }
-          if (!mbar_wait(bar(F_VFULL0 + st), nn & 1, ctl, ERR_KERNEL_FWD + F_VFULL0 + st)) { ok = false; break; }
-          tc_fence_after();
+      }
+      __syncwarp();
+      for (int j = 0; j < n; ++j) {
+        const uint32_t gg = g0 + j;
+        const int st = gg & 1;
+        const uint32_t nn = gg >> 1;
+        // PV_A(g)
+        if (j == 0 && it > 0 && !warp_wait(F_OEMPTY_A, (it - 1) & 1)) { ok = false; break; }
+        if (!warp_wait(F_PFULL_A, gg & 1)) { ok = false; break; }
+        if (!warp_wait(F_VFULL0 + st, nn & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
           issue_pv(0, 256, st, j == 0);
           tc_commit(bar(F_ODONE_A));
-          // S_A(g+1)
-          const bool more = j + 1 < n;
-          if (more) {
-            const int st1 = (gg + 1) & 1;
-            if (!mbar_wait(bar(F_KROT0 + st1), ((gg + 1) >> 1) & 1, ctl, ERR_KERNEL_FWD + F_KROT0 + st1)) { ok = false; break; }
-            tc_fence_after();
+        }
+        __syncwarp();
+        // S_A(g+1)
+        const bool more = j + 1 < n;
+        if (more) {
+          const int st1 = (gg + 1) & 1;
+          if (!warp_wait(F_KFULL0 + st1, ((gg + 1) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          if (leader) {
             issue_s(sQA, 0, st1);
             tc_commit(bar(F_SFULL_A));
           }
-          // PV_B(g)
-          if (j == 0 && it > 0 && !mbar_wait(bar(F_OEMPTY_B), (it - 1) & 1, ctl, ERR_KERNEL_FWD + F_OEMPTY_B)) { ok = false; break; }
-          if (!mbar_wait(bar(F_PFULL_B), gg & 1, ctl, ERR_KERNEL_FWD + F_PFULL_B)) { ok = false; break; }
-          tc_fence_after();
+          __syncwarp();
+        }
+        // PV_B(g)
+        if (j == 0 && it > 0 && !warp_wait(F_OEMPTY_B, (it - 1) & 1)) { ok = false; break; }
+        if (!warp_wait(F_PFULL_B, gg & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
           issue_pv(128, 256 + D, st, j == 0);
           tc_commit(bar(F_ODONE_B));
           tc_commit(bar(F_VEMPTY0 + st));
@@ -283,43 +310,15 @@ __global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_const
             if (j + 2 == n) tc_commit(bar(F_QEMPTY));
           }
         }
-        g0 += n;
+        __syncwarp();
       }
+      g0 += n;
+    }
+    if (leader) {
       tc_commit(bar(F_FINAL));
       mbar_drain(bar(F_FINAL), 0);
     }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ RoPE warps
-    const int rtid = tid - 256;
-    uint32_t gk = 0, ntile = 0;
-    int it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-      int b, head, s, pair;
-      decode_unit(g, n_pairs, u, b, head, s, pair);
-      ok = mbar_wait(bar(F_QFULL), it & 1, ctl, ERR_KERNEL_FWD + F_QFULL);
-      ok = rope_tile<D>(smem + Ly::QA_OFF, rowoff + (ntile++ & 1) * 128, 2 * pair * kTile, s, g, p.rope, tab, rtid, lane, ok);
-      if (!ok) break;
-      ok = rope_tile<D>(smem + Ly::QB_OFF, rowoff + (ntile++ & 1) * 128, (2 * pair + 1) * kTile, s, g, p.rope, tab, rtid,
-                        lane, ok);
-      if (!ok) break;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(F_QROT));
-      for (int j = 0; j < g.n_tiles; ++j) {
-        const uint32_t gg = gk + j;
-        const int st = gg & 1;
-        const uint32_t n = gg >> 1;
-        ok = mbar_wait(bar(F_KFULL0 + st), n & 1, ctl, ERR_KERNEL_FWD + F_KFULL0 + st);
-        ok = rope_tile<D>(smem + Ly::K_OFF + st * Ly::TILE, rowoff + (ntile++ & 1) * 128, j * kTile, s, g, p.rope,
-                          tab, rtid, lane, ok);
-        if (!ok) break;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(F_KROT0 + st));
-      }
-      gk += g.n_tiles;
-    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps (A: 0-3, B: 4-7)
     const int wg = warp >> 2;                              // 0 = Q tile A, 1 = Q tile B
@@ -462,21 +461,35 @@ __global__ void __launch_bounds__(512, 1) skiparse_fwd_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-size_t fwd_smem_bytes(int D, int rope_entries) {
-  const size_t base = (D == 128) ? FwdLayout<128>::ROPE_OFF : FwdLayout<64>::ROPE_OFF;
-  return base + (size_t)rope_entries * sizeof(float2);
-}
+size_t fwd_smem_bytes(int D) { return D == 128 ? FwdLayout<128>::BYTES : FwdLayout<64>::BYTES; }
+
+size_t fwd_rope_smem_bytes(int rope_entries) { return (size_t)rope_entries * sizeof(float2); }
 
 int fwd_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 2); }
 
+cudaError_t launch_fwd_rope(const FwdParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = fwd_rope_smem_bytes(p.rope.entries);
+  cudaError_t e;
+  if (p.g.D == 128) {
+    e = cudaFuncSetAttribute(skiparse_fwd_rope_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_fwd_rope_kernel<128><<<grid, kRopeThreads, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(skiparse_fwd_rope_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_fwd_rope_kernel<64><<<grid, kRopeThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = fwd_smem_bytes(p.g.D, p.rope.entries);
+  const size_t smem = fwd_smem_bytes(p.g.D);
   cudaError_t e;
   if (p.g.D == 128) {
     e = cudaFuncSetAttribute(skiparse_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

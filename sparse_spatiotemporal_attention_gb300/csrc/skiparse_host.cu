@@ -292,11 +292,19 @@ const char* skiparse_kernel_name(int id) {
     case 1: return "skiparse_bwd_pre_kernel";
     case 2: return "skiparse_bwd_main_kernel";
     case 3: return "skiparse_bwd_post_kernel";
+    case 4: return "skiparse_fwd_rope_kernel";
     default: return "unknown";
   }
 }
 
+size_t skiparse_attn_fwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode) {
+  Shape s;
+  if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty) return 0;
+  return 2 * align256((size_t)s.elems * 2);
+}
+
 int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes,
                       int B, int heads, int N, int D, int T, int H, int W,
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
   Shape s;
@@ -304,24 +312,39 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   if (st != SKIPARSE_OK || s.empty) return st;
   if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
+  const size_t half = align256((size_t)s.elems * 2);
+  if (!workspace || workspace_bytes < 2 * half) return SKIPARSE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
   const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
-  if (any_alias({{out, tb}, {lse, lb}}, {{q, tb}, {k, tb}, {v, tb}})) return SKIPARSE_ERR_ALIAS;
+  if (any_alias({{out, tb}, {lse, lb}, {workspace, 2 * half}}, {{q, tb}, {k, tb}, {v, tb}})) return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
-  if ((size_t)dev.smem_optin < fwd_smem_bytes(D, s.rope_entries)) return SKIPARSE_ERR_UNSUPPORTED;
+  if ((size_t)dev.smem_optin < fwd_smem_bytes(D) || (size_t)dev.smem_optin < fwd_rope_smem_bytes(s.rope_entries))
+    return SKIPARSE_ERR_UNSUPPORTED;
 
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   p.g = make_geom(s);
   p.rope = make_rope(s, rope_theta);
-  if (!encode_scope_map(&p.tm_q, q, p.g) || !encode_scope_map(&p.tm_k, k, p.g) || !encode_scope_map(&p.tm_v, v, p.g))
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.qr = reinterpret_cast<uint16_t*>(ws);
+  p.kr = reinterpret_cast<uint16_t*>(ws + half);
+  if (!encode_scope_map(&p.tm_q, p.qr, p.g) || !encode_scope_map(&p.tm_k, p.kr, p.g) ||
+      !encode_scope_map(&p.tm_v, v, p.g))
     return SKIPARSE_ERR_LAUNCH;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.err = dev.err_word;
   p.n_units = fwd_units(p.g);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  const long long rows = (long long)B * N * heads;
+  long long rgrid = (rows + 15) / 16;
+  if (rgrid > 4ll * dev.sms) rgrid = 4ll * dev.sms;
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
+  st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, stream); }));
+  if (st != SKIPARSE_OK) return st;
   return launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));
 }
 

@@ -20,7 +20,11 @@ enum : int {
 };
 
 struct FwdParams {
-  CUtensorMap tm_q, tm_k, tm_v;   // scope-gather maps over the caller's q, k, v
+  CUtensorMap tm_q, tm_k, tm_v;   // scope-gather maps over rotated q, rotated k (workspace) and v
+  const uint16_t* q;              // pre-RoPE inputs (RoPE pass)
+  const uint16_t* k;
+  uint16_t* qr;                   // workspace: rotated q, bf16 (B, N, heads, D)
+  uint16_t* kr;                   // workspace: rotated k
   Geom g;
   RopeParams rope;
   uint16_t* out;                  // bf16 (B, N, heads, D)
@@ -65,8 +69,10 @@ struct DebugParams {
 };
 
 // Shared-memory bytes and launch helpers (defined next to each kernel).
-size_t fwd_smem_bytes(int D, int rope_entries);
+size_t fwd_smem_bytes(int D);
+size_t fwd_rope_smem_bytes(int rope_entries);
 int fwd_units(const Geom& g);
+cudaError_t launch_fwd_rope(const FwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
 
 size_t bwd_main_smem_bytes(int D);

@@ -42,16 +42,20 @@ def test_status_strings(lib):
         s = skp.status_string(code)
         assert s and s != "unknown status"
     assert skp.status_string(12345) == "unknown status"
-    for i in range(4):
+    for i in range(len(skp.KERNEL_NAMES)):
         assert lib.skiparse_kernel_name(i).decode() == skp.KERNEL_NAMES[i]
+    assert lib.skiparse_kernel_name(len(skp.KERNEL_NAMES)).decode() == "unknown"
 
 
 A = 1 << 20  # fake, 16-byte-aligned device addresses: validation fails before any use
 
 
-def fwd(lib, q=A, k=2 * A, v=3 * A, out=4 * A, lse=5 * A, B=1, heads=2, N=256, D=64, T=4, H=8, W=8,
-        sk=2, mode=0, theta=10000.0):
-    return lib.skiparse_attn_fwd(q, k, v, out, lse, B, heads, N, D, T, H, W, sk, mode, theta, None)
+FWD_WS = 2 * 256 * 2 * 64 * 2   # rotated q and k for B=1, heads=2, N=256, D=64
+
+
+def fwd(lib, q=A, k=2 * A, v=3 * A, out=4 * A, lse=5 * A, ws=8 * A, ws_bytes=FWD_WS, B=1, heads=2, N=256, D=64,
+        T=4, H=8, W=8, sk=2, mode=0, theta=10000.0):
+    return lib.skiparse_attn_fwd(q, k, v, out, lse, ws, ws_bytes, B, heads, N, D, T, H, W, sk, mode, theta, None)
 
 
 def test_fwd_validation(lib):
@@ -70,11 +74,23 @@ def test_fwd_validation(lib):
     assert fwd(lib, lse=5 * A + 4) == ALIGN
     assert fwd(lib, out=A + 64) == ALIAS                 # out overlaps q
     assert fwd(lib, lse=4 * A + 128) == ALIAS            # lse overlaps out
+    assert fwd(lib, ws=None) == WORKSPACE
+    assert fwd(lib, ws_bytes=FWD_WS - 1) == WORKSPACE
+    assert fwd(lib, ws=8 * A + 16) == ALIGN              # workspace: 256-byte aligned
+    assert fwd(lib, ws=3 * A) == ALIAS                   # workspace overlaps v
     # empty calls are valid no-ops, pointers may be NULL
     assert fwd(lib, B=0, q=None, k=None, v=None, out=None, lse=None) == OK
     assert fwd(lib, T=0, N=0) == OK
     # a valid call with no GPU present reaches the device check
     assert fwd(lib) in (DEVICE,)
+
+
+def test_fwd_workspace_bytes(lib):
+    assert lib.skiparse_attn_fwd_workspace_bytes(1, 2, 256, 64, 4, 8, 8, 2, 0) == FWD_WS
+    assert lib.skiparse_attn_fwd_workspace_bytes(0, 2, 256, 64, 4, 8, 8, 2, 0) == 0
+    assert lib.skiparse_attn_fwd_workspace_bytes(1, 2, 256, 96, 4, 8, 8, 2, 0) == 0
+    # each rotated copy is rounded up to 256 bytes: 1 x 1 x 3 tokens x 64 channels
+    assert lib.skiparse_attn_fwd_workspace_bytes(1, 1, 3, 64, 1, 1, 3, 1, 0) == 2 * 512
 
 
 def test_bwd_validation_and_workspace(lib):
@@ -108,8 +124,8 @@ def test_debug_hook_validation(lib):
 
 def test_trace_without_gpu(lib):
     skp.skiparse_trace_begin()
-    ms, cnt = skp.skiparse_trace_end(4)
-    assert ms == [0.0] * 4 and cnt == [0] * 4
+    ms, cnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
+    assert ms == [0.0] * len(skp.KERNEL_NAMES) and cnt == [0] * len(skp.KERNEL_NAMES)
 
 
 def test_package_has_no_fallback():

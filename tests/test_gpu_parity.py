@@ -152,8 +152,8 @@ def test_trace_counts_launches(env):
     skp.skiparse_trace_begin()
     fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode, guard=False)
     tl.run_bwd(skp, dev, ins, fw, B, heads, N, D, T, H, W, k, mode, guard=False)
-    ms, cnt = skp.skiparse_trace_end(4)
-    assert cnt == [1, 1, 1, 1]
+    ms, cnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
+    assert cnt == [1, 1, 1, 1, 1]
     assert all(m > 0 for m in ms)
 
 
@@ -169,6 +169,10 @@ def test_empty_and_invalid_calls_on_device(env):
     with pytest.raises(skp.SkiparseError) as e:
         skp.skiparse_attn_fwd(q, q, q, q, lse, 4, 8, 8, 2, 0)        # out aliases q
     assert e.value.status == -9
+    small = torch.empty(1024, dtype=torch.uint8, device=dev)
+    with pytest.raises(skp.SkiparseError) as e:
+        skp.skiparse_attn_fwd(q, q, q, out, lse, 4, 8, 8, 2, 0, workspace=small)   # workspace too small
+    assert e.value.status == -6
     empty = torch.zeros((0, 256, 2, 64), dtype=torch.bfloat16, device=dev)
     skp.skiparse_attn_fwd(empty, empty, empty, empty, lse, 4, 8, 8, 2, 0)
     assert out.abs().sum().item() == 0
