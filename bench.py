@@ -16,7 +16,10 @@ Printed JSON line (rank 0):
                bf16 peak;
   cpu_baseline the float64 CPU oracle on a bounded sample (whole scopes) of the
                same workload, timed on this host's cores (rank 0, one GPU only);
-  speedup_vs_k1  the same step at sparse_k=1 (dense attention) over this one.
+  speedup_vs_k1  the same step at sparse_k=1 (dense attention) over this one;
+  fwd_configs  forward-only throughput (RoPE pass + attention) of the single-skip
+               8x32x32 and the long-sequence group-skip 16x45x80 (57,600-token)
+               configurations, the latter also at k=1 (rank 0; skipped with --no-k1).
 
 --impl reference times the oracle alone (the reference arm of this method).
 Multi-GPU: one process per GPU (torchrun); every rank runs its own batch
@@ -47,6 +50,11 @@ WORKLOADS = {
                       mode=1),
 }
 WORKLOAD = WORKLOADS["train"]
+# forward-only configurations reported beside the timed step (same kernels)
+FWD_CONFIGS = [
+    dict(name="skiparse_fwd_single_8x32x32_k4", B=1, heads=24, D=128, T=8, H=32, W=32, k=4, mode=0, k1=False),
+    dict(name="skiparse_fwd_group_16x45x80_k4", B=1, heads=24, D=128, T=16, H=45, W=80, k=4, mode=1, k1=True),
+]
 KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0, 4: 0.0}   # x forward FLOPs, per launch
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
@@ -189,6 +197,54 @@ def traffic_record(kernel_name):
     return None
 
 
+def fwd_config_lines(skp, dev, stream, peaks, launches=10):
+    """Forward-only throughput (RoPE pass + attention) of FWD_CONFIGS, and the
+    dense k = 1 forward on the same inputs where the configuration asks for it."""
+    import numpy as np
+    import torch
+    from sparse_spatiotemporal_attention_gb300 import synthetic
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    lines = []
+    for c in FWD_CONFIGS:
+        B, heads, D, T, H, W = c["B"], c["heads"], c["D"], c["T"], c["H"], c["W"]
+        N = T * H * W
+        ins = synthetic.attention_inputs(B, N, heads, D, with_grad=False)
+        d = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev) for n, a in ins.items()}
+        out = torch.empty_like(d["q"])
+        lse = torch.empty((B, heads, N), dtype=torch.float32, device=dev)
+        fws = torch.empty(skp.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, 1, c["mode"]),
+                          dtype=torch.uint8, device=dev)
+
+        def timed(kk):
+            for _ in range(3):
+                skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, c["mode"], stream=stream,
+                                      workspace=fws)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(launches):
+                skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, c["mode"], stream=stream,
+                                      workspace=fws)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / launches
+
+        ms = timed(c["k"])
+        tf = fwd_flops(c) / (ms * 1e-3) / 1e12
+        line = {"workload": c["name"], "pass": "fwd", "mode": "group" if c["mode"] else "single", "B": B,
+                "heads": heads, "D": D, "grid": f"{T}x{H}x{W}", "N": N, "sparse_k": c["k"], "ms_per_launch": ms,
+                "tflops": tf, "pct_of_peak": {"burst": tf / burst, "sustained": tf / sustained}}
+        if c["k1"]:
+            ms1 = timed(1)
+            line["k1"] = {"ms_per_launch": ms1, "tflops": fwd_flops(c, 1) / (ms1 * 1e-3) / 1e12,
+                          "speedup": ms1 / ms}
+        lines.append(line)
+        del d, out, lse, fws
+        torch.cuda.empty_cache()
+    return lines
+
+
 def gpu_arm(args):
     import numpy as np
     import torch
@@ -320,6 +376,9 @@ def gpu_arm(args):
         raise RuntimeError(f"device wait gave up: code {detail:#x}")
 
     peaks, src = load_peaks()
+    fwd_lines = None
+    if not args.no_k1 and rank == 0:
+        fwd_lines = fwd_config_lines(skp, dev, stream, peaks)
     kernels = {}
     tot = sum(kms) or 1.0
     for i in range(nk):
@@ -350,6 +409,7 @@ def gpu_arm(args):
                         "sustained": value / world / peak, "source": src},
         "fwd": {"ms_per_launch": fwd_ms, "tflops": fwd_flops(w) / (fwd_ms * 1e-3) / 1e12},
         "speedup_vs_k1": (k1 or {}).get("speedup"), "k1": k1,
+        "fwd_configs": fwd_lines,
         "clocks": clocks, "e2e": e2e, "gpu_launches": int(sum(kcnt)), "kernels": kernels, "roofline": roofline,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -1,4 +1,5 @@
-// Skiparse attention backward: preprocess, main and post kernels.
+// Skiparse attention backward: the main kernels (the preprocess and post row
+// kernels are in skiparse_bwd_rows.cu).
 //
 // The pages print no backward; it is implied by the method's purpose (it
 // accelerates training, "Open-Sora Plan" docs, "Skiparse Attention"). The
@@ -33,124 +34,6 @@
 #include "skiparse_internal.h"
 
 namespace skp {
-
-// ===========================================================================
-// preprocess and post: one warp per (b, token, head) row
-// ===========================================================================
-
-constexpr int kRowThreads = 256;
-
-template <int D>
-__global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
-  extern __shared__ float2 tab[];
-  const Geom& g = p.g;
-  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
-  __syncthreads();
-  if (blockIdx.x == 0)
-    for (int e = threadIdx.x; e < p.rope.entries; e += blockDim.x) p.rope_tab[e] = tab[e];
-  constexpr int PPL = D / 64;               // channel pairs per lane
-  const int lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
-  PairSel sel[PPL];
-#pragma unroll
-  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
-  const long long rows = (long long)g.B * g.N * g.heads;
-  for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb) {
-    const int head = (int)(row % g.heads);
-    const long long bi = row / g.heads;
-    const int i = (int)(bi % g.N);
-    const int b = (int)(bi / g.N);
-    int t, hh, w;
-    token_coords(p.rope, i, t, hh, w);
-    const size_t base = (size_t)row * D + lane * 2 * PPL;
-    float dsum = 0.f;
-    uint32_t qv[PPL], kv[PPL], ov[PPL], dv[PPL];
-    if (PPL == 2) {
-      const uint2 a = *reinterpret_cast<const uint2*>(p.q + base);
-      const uint2 bb = *reinterpret_cast<const uint2*>(p.k + base);
-      const uint2 c = *reinterpret_cast<const uint2*>(p.out + base);
-      const uint2 d = *reinterpret_cast<const uint2*>(p.dout + base);
-      qv[0] = a.x; qv[PPL - 1] = a.y; kv[0] = bb.x; kv[PPL - 1] = bb.y;
-      ov[0] = c.x; ov[PPL - 1] = c.y; dv[0] = d.x; dv[PPL - 1] = d.y;
-    } else {
-      qv[0] = *reinterpret_cast<const uint32_t*>(p.q + base);
-      kv[0] = *reinterpret_cast<const uint32_t*>(p.k + base);
-      ov[0] = *reinterpret_cast<const uint32_t*>(p.out + base);
-      dv[0] = *reinterpret_cast<const uint32_t*>(p.dout + base);
-    }
-    uint32_t qo[PPL], ko[PPL];
-#pragma unroll
-    for (int e = 0; e < PPL; ++e) {
-      dsum = fmaf(bf16lo(ov[e]), bf16lo(dv[e]), dsum);
-      dsum = fmaf(bf16hi(ov[e]), bf16hi(dv[e]), dsum);
-      const float2 cs = tab[pair_index(sel[e], t, hh, w)];
-      const float2 a = rope_rotate(bf16lo(qv[e]), bf16hi(qv[e]), cs);
-      const float2 c = rope_rotate(bf16lo(kv[e]), bf16hi(kv[e]), cs);
-      qo[e] = pack_bf16(a.x, a.y);
-      ko[e] = pack_bf16(c.x, c.y);
-    }
-    int s, pp;
-    scope_pos_of(g, i, s, pp);
-    const size_t idx = (((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp;   // scope-order row
-    float* acc = p.dq_acc + idx * D + lane * 2 * PPL;
-    if (PPL == 2) {
-      *reinterpret_cast<uint2*>(p.qr + base) = make_uint2(qo[0], qo[PPL - 1]);
-      *reinterpret_cast<uint2*>(p.kr + base) = make_uint2(ko[0], ko[PPL - 1]);
-      *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      *reinterpret_cast<uint32_t*>(p.qr + base) = qo[0];
-      *reinterpret_cast<uint32_t*>(p.kr + base) = ko[0];
-      *reinterpret_cast<float2*>(acc) = make_float2(0.f, 0.f);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-    if (lane == 0) {
-      p.delta_s[idx] = dsum;
-      p.lse2s[idx] = p.lse[((size_t)b * g.heads + head) * g.N + i] * 1.4426950408889634f;
-    }
-  }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __grid_constant__ BwdParams p) {
-  const Geom& g = p.g;
-  constexpr int PPL = D / 64;
-  const int lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
-  PairSel sel[PPL];
-#pragma unroll
-  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
-  const long long rows = (long long)g.B * g.N * g.heads;
-  for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb) {
-    const int head = (int)(row % g.heads);
-    const long long bi = row / g.heads;
-    const int i = (int)(bi % g.N);
-    const int b = (int)(bi / g.N);
-    int t, hh, w;
-    token_coords(p.rope, i, t, hh, w);
-    const size_t base = (size_t)row * D + lane * 2 * PPL;
-    int s, pp;
-    scope_pos_of(g, i, s, pp);
-    const float* acc = p.dq_acc + ((((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp) * D + lane * 2 * PPL;
-    float x[2 * PPL];
-    if (PPL == 2) {
-      const float4 a = *reinterpret_cast<const float4*>(acc);
-      x[0] = a.x; x[1] = a.y; x[2 * PPL - 2] = a.z; x[2 * PPL - 1] = a.w;
-    } else {
-      const float2 a = *reinterpret_cast<const float2*>(acc);
-      x[0] = a.x; x[1] = a.y;
-    }
-    uint32_t o[PPL];
-#pragma unroll
-    for (int e = 0; e < PPL; ++e) {
-      const float2 cs = __ldg(&p.rope_tab[pair_index(sel[e], t, hh, w)]);
-      const float2 r = rope_rotate_t(x[2 * e] * p.scale, x[2 * e + 1] * p.scale, cs);
-      o[e] = pack_bf16(r.x, r.y);
-    }
-    if (PPL == 2) *reinterpret_cast<uint2*>(p.dq + base) = make_uint2(o[0], o[PPL - 1]);
-    else *reinterpret_cast<uint32_t*>(p.dq + base) = o[0];
-  }
-}
 
 // ===========================================================================
 // main kernel for D = 64: 128-query tiles, dQ~ added by four of its warps
@@ -955,21 +838,6 @@ size_t bwd_main_smem_bytes(int D) {
   return D == 128 ? (size_t)BwdLayout<128>::BYTES : (size_t)BwdLayout<64>::BYTES;
 }
 
-cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = (size_t)p.rope.entries * sizeof(float2);
-  cudaError_t e;
-  if (p.g.D == 128) {
-    e = cudaFuncSetAttribute(skiparse_bwd_pre_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_bwd_pre_kernel<128><<<grid, kRowThreads, smem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(skiparse_bwd_pre_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_bwd_pre_kernel<64><<<grid, kRowThreads, smem, stream>>>(p);
-  }
-  return cudaGetLastError();
-}
-
 cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream) {
   const size_t smem = bwd_main_smem_bytes(p.g.D);
   cudaError_t e;
@@ -982,12 +850,6 @@ cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     skiparse_bwd_main_kernel<64><<<grid, kBwdThreads, smem, stream>>>(p);
   }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_post(const BwdParams& p, int grid, cudaStream_t stream) {
-  if (p.g.D == 128) skiparse_bwd_post_kernel<128><<<grid, kRowThreads, 0, stream>>>(p);
-  else skiparse_bwd_post_kernel<64><<<grid, kRowThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

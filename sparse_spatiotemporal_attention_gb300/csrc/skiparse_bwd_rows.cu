@@ -1,0 +1,190 @@
+// Skiparse attention backward, row kernels: the preprocess before and the
+// post pass after the main kernel (skiparse_bwd.cu). Both are HBM-bound, one
+// warp per (b, token, head) row of the original layout.
+//
+//  preprocess  delta = rowsum(dO * O) and lse * log2(e) at the row's
+//              scope-order slot, rotated bf16 copies of q and k (so the main
+//              loop reloads no RoPE), the row's dQ~ accumulator zeroed, and
+//              the cos/sin table written to the workspace (for the main
+//              kernel's dK epilogue and the post pass).
+//  post        dq = R^T (scale * dQ~_acc) -> bf16 at the original row.
+#include "skiparse_internal.h"
+
+namespace skp {
+
+// ===========================================================================
+// preprocess and post: one warp per (b, token, head) row
+// ===========================================================================
+
+constexpr int kRowThreads = 256;
+
+// 8-byte (PPL = 2) or 4-byte (PPL = 1) slice of a bf16 row owned by one lane.
+template <int PPL>
+__device__ __forceinline__ void ld_slice(const uint16_t* src, uint32_t (&v)[PPL]) {
+  if (PPL == 2) {
+    const uint2 a = *reinterpret_cast<const uint2*>(src);
+    v[0] = a.x;
+    v[PPL - 1] = a.y;
+  } else {
+    v[0] = *reinterpret_cast<const uint32_t*>(src);
+  }
+}
+template <int PPL>
+__device__ __forceinline__ void st_slice(uint16_t* dst, const uint32_t (&v)[PPL]) {
+  if (PPL == 2) *reinterpret_cast<uint2*>(dst) = make_uint2(v[0], v[PPL - 1]);
+  else *reinterpret_cast<uint32_t*>(dst) = v[0];
+}
+
+// Preprocess: per (b, token, head) row, delta = rowsum(dO * O) and lse * log2(e)
+// at the row's scope-order slot, rotated bf16 copies of q and k, and the row's
+// dQ accumulator zeroed. One warp per row, two rows per iteration so each lane
+// has its loads of both rows in flight before it uses either.
+template <int D>
+__global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ float2 tab[];
+  const Geom& g = p.g;
+  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < p.rope.entries; e += blockDim.x) p.rope_tab[e] = tab[e];
+  constexpr int PPL = D / 64;               // channel pairs per lane
+  const int lane = threadIdx.x & 31;
+  const long long wpb = blockDim.x >> 5;
+  PairSel sel[PPL];
+#pragma unroll
+  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
+  const long long rows = (long long)g.B * g.N * g.heads;
+  const long long stride = (long long)gridDim.x * wpb;
+  for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += 2 * stride) {
+    uint32_t qv[2][PPL], kv[2][PPL], ov[2][PPL], dv[2][PPL];
+    float lse[2] = {0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long row = r0 + u * stride;
+      if (row >= rows) continue;
+      const size_t base = (size_t)row * D + lane * 2 * PPL;
+      ld_slice<PPL>(p.q + base, qv[u]);
+      ld_slice<PPL>(p.k + base, kv[u]);
+      ld_slice<PPL>(p.out + base, ov[u]);
+      ld_slice<PPL>(p.dout + base, dv[u]);
+      if (lane == 0) {
+        const int head = (int)(row % g.heads);
+        const long long bi = row / g.heads;
+        lse[u] = p.lse[((size_t)(bi / g.N) * g.heads + head) * g.N + (bi % g.N)];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long row = r0 + u * stride;
+      if (row >= rows) continue;
+      const int head = (int)(row % g.heads);
+      const long long bi = row / g.heads;
+      const int i = (int)(bi % g.N);
+      const int b = (int)(bi / g.N);
+      int t, hh, w;
+      token_coords(p.rope, i, t, hh, w);
+      float dsum = 0.f;
+      uint32_t qo[PPL], ko[PPL];
+#pragma unroll
+      for (int e = 0; e < PPL; ++e) {
+        dsum = fmaf(bf16lo(ov[u][e]), bf16lo(dv[u][e]), dsum);
+        dsum = fmaf(bf16hi(ov[u][e]), bf16hi(dv[u][e]), dsum);
+        const float2 cs = tab[pair_index(sel[e], t, hh, w)];
+        const float2 a = rope_rotate(bf16lo(qv[u][e]), bf16hi(qv[u][e]), cs);
+        const float2 c = rope_rotate(bf16lo(kv[u][e]), bf16hi(kv[u][e]), cs);
+        qo[e] = pack_bf16(a.x, a.y);
+        ko[e] = pack_bf16(c.x, c.y);
+      }
+      int s, pp;
+      scope_pos_of(g, i, s, pp);
+      const size_t idx = (((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp;   // scope-order row
+      const size_t base = (size_t)row * D + lane * 2 * PPL;
+      st_slice<PPL>(p.qr + base, qo);
+      st_slice<PPL>(p.kr + base, ko);
+      float* acc = p.dq_acc + idx * D + lane * 2 * PPL;
+      if (PPL == 2) *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
+      else *reinterpret_cast<float2*>(acc) = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+      if (lane == 0) {
+        p.delta_s[idx] = dsum;
+        p.lse2s[idx] = lse[u] * 1.4426950408889634f;
+      }
+    }
+  }
+}
+
+// Post: dq = R^T (scale * dQ~) for each (b, token, head) row, read from the
+// row's scope-order accumulator slot; two rows per warp iteration.
+template <int D>
+__global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __grid_constant__ BwdParams p) {
+  const Geom& g = p.g;
+  constexpr int PPL = D / 64;
+  const int lane = threadIdx.x & 31;
+  const long long wpb = blockDim.x >> 5;
+  PairSel sel[PPL];
+#pragma unroll
+  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
+  const long long rows = (long long)g.B * g.N * g.heads;
+  const long long stride = (long long)gridDim.x * wpb;
+  for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += 2 * stride) {
+    float x[2][2 * PPL];
+    int tt[2], th[2], tw[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long row = r0 + u * stride;
+      if (row >= rows) continue;
+      const int head = (int)(row % g.heads);
+      const long long bi = row / g.heads;
+      const int i = (int)(bi % g.N);
+      const int b = (int)(bi / g.N);
+      token_coords(p.rope, i, tt[u], th[u], tw[u]);
+      int s, pp;
+      scope_pos_of(g, i, s, pp);
+      const float* acc = p.dq_acc + ((((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp) * D + lane * 2 * PPL;
+      if (PPL == 2) {
+        const float4 a = *reinterpret_cast<const float4*>(acc);
+        x[u][0] = a.x; x[u][1] = a.y; x[u][2 * PPL - 2] = a.z; x[u][2 * PPL - 1] = a.w;
+      } else {
+        const float2 a = *reinterpret_cast<const float2*>(acc);
+        x[u][0] = a.x; x[u][1] = a.y;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long row = r0 + u * stride;
+      if (row >= rows) continue;
+      uint32_t o[PPL];
+#pragma unroll
+      for (int e = 0; e < PPL; ++e) {
+        const float2 cs = __ldg(&p.rope_tab[pair_index(sel[e], tt[u], th[u], tw[u])]);
+        const float2 r = rope_rotate_t(x[u][2 * e] * p.scale, x[u][2 * e + 1] * p.scale, cs);
+        o[e] = pack_bf16(r.x, r.y);
+      }
+      st_slice<PPL>(p.dq + (size_t)row * D + lane * 2 * PPL, o);
+    }
+  }
+}
+
+cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = (size_t)p.rope.entries * sizeof(float2);
+  cudaError_t e;
+  if (p.g.D == 128) {
+    e = cudaFuncSetAttribute(skiparse_bwd_pre_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_bwd_pre_kernel<128><<<grid, kRowThreads, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(skiparse_bwd_pre_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_bwd_pre_kernel<64><<<grid, kRowThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const BwdParams& p, int grid, cudaStream_t stream) {
+  if (p.g.D == 128) skiparse_bwd_post_kernel<128><<<grid, kRowThreads, 0, stream>>>(p);
+  else skiparse_bwd_post_kernel<64><<<grid, kRowThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace skp

@@ -340,8 +340,8 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   p.n_units = fwd_units(p.g);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const long long rows = (long long)B * N * heads;
-  long long rgrid = (rows + 15) / 16;
-  if (rgrid > 4ll * dev.sms) rgrid = 4ll * dev.sms;
+  long long rgrid = (rows + 15) / 16;                 // 8 warps per CTA, 2 rows per warp
+  if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
   st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, stream); }));
   if (st != SKIPARSE_OK) return st;
@@ -405,8 +405,8 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
     return SKIPARSE_ERR_LAUNCH;
 
   const long long rows = (long long)B * N * heads;
-  long long rgrid = (rows + 7) / 8;
-  if (rgrid > 4ll * dev.sms) rgrid = 4ll * dev.sms;
+  long long rgrid = (rows + 15) / 16;                 // 8 warps per CTA, 2 rows per warp
+  if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
   const int mgrid = p.n_units < dev.sms ? p.n_units : dev.sms;
   st = launch_status(traced_launch(1, stream, [&] { return launch_bwd_pre(p, (int)rgrid, stream); }));
   if (st != SKIPARSE_OK) return st;
