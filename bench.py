@@ -197,6 +197,35 @@ def traffic_record(kernel_name):
     return None
 
 
+# ---------------------------------------------------------------------------- multi-rank host logic
+
+def rank_env():
+    """(world, rank, local rank) from the torchrun environment; 1 process when unset."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seeds(rank):
+    """Input seeds of one rank: every rank runs its own batch (weak scaling)."""
+    return {"q": 1 + 10 * rank, "k": 2 + 10 * rank, "v": 3 + 10 * rank, "do": 4 + 10 * rank}
+
+
+def max_over_ranks(x, world, device):
+    """The slowest rank's time: max of x over the process group (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Whole-job TFLOP/s: the work of all ranks over the slowest rank's step time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def fwd_config_lines(skp, dev, stream, peaks, launches=10):
     """Forward-only throughput (RoPE pass + attention) of FWD_CONFIGS, and the
     dense k = 1 forward on the same inputs where the configuration asks for it."""
@@ -254,9 +283,7 @@ def gpu_arm(args):
     import sparse_spatiotemporal_attention_gb300 as skp
     from sparse_spatiotemporal_attention_gb300 import synthetic
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -266,18 +293,13 @@ def gpu_arm(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def max_ranks(x):
+        return max_over_ranks(x, world, dev)
 
     w = WORKLOAD
     B, heads, D, T, H, W, k, mode = w["B"], w["heads"], w["D"], w["T"], w["H"], w["W"], w["k"], w["mode"]
     N = T * H * W
-    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True, seeds={"q": 1 + 10 * rank, "k": 2 + 10 * rank,
-                                                                               "v": 3 + 10 * rank, "do": 4 + 10 * rank})
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True, seeds=rank_seeds(rank))
     pin = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for n, a in ins.items()}
     d = {n: t.to(dev) for n, t in pin.items()}
     out = torch.empty_like(d["q"])
@@ -324,10 +346,10 @@ def gpu_arm(args):
     nk = len(skp.KERNEL_NAMES)
     kms, kcnt = skp.skiparse_trace_end(nk)
     clocks = sampler.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms = max_ranks(e0.elapsed_time(e1))
     ms_step = ms / args.steps
     flops_step = 3.5 * fwd_flops(w)
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, flops_step, ms_step)
 
     # ---- e2e: host inputs in, all outputs out, every step
     h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in
@@ -352,8 +374,8 @@ def gpu_arm(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
-    e2e = {"value": world * flops_step / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
+    ms_e2e = max_ranks(e0.elapsed_time(e1)) / e2e_steps
+    e2e = {"value": job_tflops(world, flops_step, ms_e2e), "unit": "TFLOP/s", "ms_per_step": ms_e2e,
            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps}
 
     # ---- the same step at k=1 (dense attention) for the speedup
@@ -368,7 +390,7 @@ def gpu_arm(args):
             step(1)
         e1.record(stream)
         torch.cuda.synchronize()
-        ms1 = max_over_ranks(e0.elapsed_time(e1)) / k1_steps
+        ms1 = max_ranks(e0.elapsed_time(e1)) / k1_steps
         k1 = {"ms_per_step": ms1, "tflops": world * 3.5 * fwd_flops(w, 1) / (ms1 * 1e-3) / 1e12, "steps": k1_steps,
               "speedup": ms1 / ms_step}
     st, detail = skp.skiparse_device_error()
@@ -422,8 +444,7 @@ def gpu_arm(args):
 
 
 def reference_arm(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    world, rank, _ = rank_env()
     if rank != 0:
         return
     w = WORKLOAD
