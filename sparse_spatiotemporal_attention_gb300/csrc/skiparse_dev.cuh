@@ -374,6 +374,14 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int ks, uint32_t
   return sdesc_sw128(tile + (uint32_t)(ks * 2048), box, 1024);
 }
 
+// Descriptor of k-step ks from the k-step-0 descriptor: the start address field
+// (bits 0-13, in 16-byte units) advances by the step's byte offset >> 4 (shared
+// memory addresses stay below 2^18, so the field never carries).
+__device__ __forceinline__ uint64_t kmajor_step(uint64_t d0, int ks, uint32_t box = kHalfBytes) {
+  return d0 + (uint64_t)(((ks >> 2) * box + (ks & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t mnmajor_step(uint64_t d0, int ks) { return d0 + (uint64_t)(ks * 128); }
+
 // tcgen05.ld, 32 lanes x 32 bit, 32 consecutive columns; waits for completion.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];

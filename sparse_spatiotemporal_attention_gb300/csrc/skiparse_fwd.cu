@@ -239,19 +239,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
+    // operand descriptors of k-step 0, per tile and stage (k-steps add a constant)
+    const uint64_t dQA = desc_kmajor(sQA, 0), dQB = desc_kmajor(sQB, 0);
+    const uint64_t dK0 = desc_kmajor(sK, 0), dK1 = desc_kmajor(sK + Ly::TILE, 0);
+    const uint64_t dV0 = desc_mnmajor(sV, 0), dV1 = desc_mnmajor(sV + Ly::TILE, 0);
     // S_X = Q_X K_g^T into TMEM columns colS (X = A: 0, B: 128)
-    auto issue_s = [&](uint32_t qt, uint32_t colS, int st) {
-      const uint32_t kt = sK + st * Ly::TILE;
+    auto issue_s = [&](uint64_t dq, uint32_t colS, int st) {
+      const uint64_t dk = st ? dK1 : dK0;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_ss(tmem + colS, desc_kmajor(qt, ks), desc_kmajor(kt, ks), kIdS, ks > 0 ? 1u : 0u);
+        mma_ss(tmem + colS, kmajor_step(dq, ks), kmajor_step(dk, ks), kIdS, ks > 0 ? 1u : 0u);
     };
     // O_X += P_X V_g, P_X in TMEM over S_X
     auto issue_pv = [&](uint32_t colS, uint32_t colO, int st, bool first) {
-      const uint32_t vt = sV + st * Ly::TILE;
+      const uint64_t dv = st ? dV1 : dV0;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_ts(tmem + colO, tmem + colS + ks * 8, desc_mnmajor(vt, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
+        mma_ts(tmem + colO, tmem + colS + ks * 8, mnmajor_step(dv, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
     };
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
       const int n = g.n_tiles;
@@ -259,9 +263,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       if (!warp_wait(F_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
       tc_fence_after();
       if (leader) {
-        issue_s(sQA, 0, g0 & 1);
+        issue_s(dQA, 0, g0 & 1);
         tc_commit(bar(F_SFULL_A));
-        issue_s(sQB, 128, g0 & 1);
+        issue_s(dQB, 128, g0 & 1);
         tc_commit(bar(F_SFULL_B));
         tc_commit(bar(F_KEMPTY0 + (g0 & 1)));
         if (n == 1) tc_commit(bar(F_QEMPTY));
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
           if (!warp_wait(F_KFULL0 + st1, ((gg + 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           if (leader) {
-            issue_s(sQA, 0, st1);
+            issue_s(dQA, 0, st1);
             tc_commit(bar(F_SFULL_A));
           }
           __syncwarp();
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
           // S_B(g+1)
           if (more) {
             const int st1 = (gg + 1) & 1;
-            issue_s(sQB, 128, st1);
+            issue_s(dQB, 128, st1);
             tc_commit(bar(F_SFULL_B));
             tc_commit(bar(F_KEMPTY0 + st1));
             if (j + 2 == n) tc_commit(bar(F_QEMPTY));
