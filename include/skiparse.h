@@ -152,6 +152,17 @@ int skiparse_debug_index_map(int* scope_of_token, int* pos_of_token, int N, int 
 int skiparse_debug_rope(const void* x, float* x_rot, int B, int heads, int N, int D,
                         int T, int H, int W, float rope_theta, cudaStream_t stream);
 
+/*
+ * Test hook for the bounded waits (no counterpart in the method; robustness of
+ * this library only). Launches one CTA whose two warps wait, through the same
+ * bounded mbarrier wait the attention kernels use, on barriers nothing arrives
+ * at. After about one second the first wait gives up and records `code`
+ * (must be > 0) in the device error word; the kernel then exits normally and
+ * the context stays usable. Read the result with skiparse_device_error().
+ * Returns SKIPARSE_ERR_INVALID_ARG for code <= 0.
+ */
+int skiparse_debug_wait_timeout(int code, cudaStream_t stream);
+
 /* Static, human-readable text for a status code. */
 const char* skiparse_status_string(int status);
 

@@ -26,7 +26,7 @@ EXPORTS = (
     "skiparse_attn_fwd_workspace_bytes", "skiparse_attn_fwd", "skiparse_attn_bwd_workspace_bytes", "skiparse_attn_bwd",
     "skiparse_debug_index_map", "skiparse_debug_rope", "skiparse_status_string",
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
-    "skiparse_attn_bwd_noalloc",
+    "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout",
 )
 
 
@@ -64,6 +64,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_trace_end": (_c_int, [ctypes.POINTER(_c_float), ctypes.POINTER(_c_int), _c_int]),
         "skiparse_kernel_name": (ctypes.c_char_p, [_c_int]),
         "skiparse_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 9 + [_c_float, _vp]),
+        "skiparse_debug_wait_timeout": (_c_int, [_c_int, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -175,6 +176,11 @@ def skiparse_debug_rope(x, x_rot, T, H, W, rope_theta=10000.0, stream=None):
     st = load_library().skiparse_debug_rope(_ptr(x), _ptr(x_rot), B, heads, N, D, T, H, W,
                                             float(rope_theta), _stream(stream))
     _check(st, "skiparse_debug_rope")
+
+
+def skiparse_debug_wait_timeout(code, stream=None):
+    """Launches the bounded-wait check (about one second); read it with skiparse_device_error()."""
+    _check(load_library().skiparse_debug_wait_timeout(int(code), _stream(stream)), "skiparse_debug_wait_timeout")
 
 
 def skiparse_device_error():

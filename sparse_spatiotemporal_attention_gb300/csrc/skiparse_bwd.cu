@@ -515,6 +515,9 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO (MN-major)
     constexpr uint32_t kIdDK = idesc_bf16(128, D, false, true);     // dS^T (K-major) x Q~ (MN-major)
     constexpr uint32_t kIdDQ = idesc_bf16(D, 128, true, true);      // K~^T (MN-major) x dS^T (MN-major)
+    // k-step-0 descriptors of every operand tile; k-steps add a constant
+    const uint64_t dKk = desc_kmajor(sK, 0), dKmn = desc_mnmajor(sK, 0), dVk = desc_kmajor(sV, 0);
+    const uint64_t dDSk = desc_kmajor(sDS, 0), dDSmn = desc_mnmajor(sDS, 0);
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
@@ -528,10 +531,12 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         tc_fence_after();
         const uint32_t qt = sQ + st * Ly::TILE;
         const uint32_t dot = sDO + st * Ly::TILE;
+        const uint64_t dQk = desc_kmajor(qt, 0), dQmn = desc_mnmajor(qt, 0);
+        const uint64_t dOk = desc_kmajor(dot, 0), dOmn = desc_mnmajor(dot, 0);
         if (leader) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tmem, desc_kmajor(sK, ks), desc_kmajor(qt, ks), kIdS, ks > 0 ? 1u : 0u);
+            mma_ss(tmem, kmajor_step(dKk, ks), kmajor_step(dQk, ks), kIdS, ks > 0 ? 1u : 0u);
           tc_commit(bar(T_SRDY));
         }
         __syncwarp();
@@ -542,7 +547,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         if (leader) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tmem + 128, desc_kmajor(sV, ks), desc_kmajor(dot, ks), kIdS, ks > 0 ? 1u : 0u);
+            mma_ss(tmem + 128, kmajor_step(dVk, ks), kmajor_step(dOk, ks), kIdS, ks > 0 ? 1u : 0u);
           tc_commit(bar(T_DPRDY));
         }
         __syncwarp();
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         if (leader) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_ts(tmem + 256, tmem + 16 * ks, desc_mnmajor(dot, ks), kIdDV, (i > 0 || ks > 0) ? 1u : 0u);
+            mma_ts(tmem + 256, tmem + 16 * ks, mnmajor_step(dOmn, ks), kIdDV, (i > 0 || ks > 0) ? 1u : 0u);
         }
         __syncwarp();
         for (int c = 0; c < 4; ++c) {
@@ -565,13 +570,13 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int ks = 2 * c + e;
-                mma_ts(tmem + 256, tmem + 16 * ks, desc_mnmajor(dot, ks), kIdDV, 1u);
+                mma_ts(tmem + 256, tmem + 16 * ks, mnmajor_step(dOmn, ks), kIdDV, 1u);
               }
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int ks = 2 * c + e;
-              mma_ss(tmem + 384, desc_kmajor(sDS, ks), desc_mnmajor(qt, ks), kIdDK, (i > 0 || ks > 0) ? 1u : 0u);
+              mma_ss(tmem + 384, kmajor_step(dDSk, ks), mnmajor_step(dQmn, ks), kIdDK, (i > 0 || ks > 0) ? 1u : 0u);
             }
           }
           __syncwarp();
@@ -580,7 +585,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         if (leader) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_ss(tmem + 128, desc_mnmajor(sK, ks), desc_mnmajor(sDS, ks), kIdDQ, ks > 0 ? 1u : 0u);
+            mma_ss(tmem + 128, mnmajor_step(dKmn, ks), mnmajor_step(dDSmn, ks), kIdDQ, ks > 0 ? 1u : 0u);
           tc_commit(bar(T_DQFULL));
         }
         __syncwarp();

@@ -43,6 +43,31 @@ __global__ void skiparse_debug_rope_kernel(const __grid_constant__ DebugParams p
   }
 }
 
+// Bounded-wait check: one CTA of two warps, each waiting on its own mbarrier
+// that nothing ever arrives at, through the same bounded wait the attention
+// kernels use. The first wait to run out records `code` in the error word and
+// raises the CTA's abort flag; the other returns as soon as it sees the flag.
+// Nothing is left in flight, so the CTA exits normally.
+__global__ void skiparse_debug_wait_timeout_kernel(int* err, int code) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const Ctl c{&abort_flag, err};
+  if ((threadIdx.x & 31) == 0) mbar_wait(smem_u32(&bars[threadIdx.x >> 5]), 0, c, code);
+  __syncthreads();
+}
+
+cudaError_t launch_debug_wait_timeout(int* err, int code, cudaStream_t stream) {
+  skiparse_debug_wait_timeout_kernel<<<1, 64, 0, stream>>>(err, code);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_debug_index_map(const DebugParams& p, cudaStream_t stream) {
   const int grid = (p.g.N + 255) / 256;
   skiparse_debug_index_map_kernel<<<grid > 0 ? grid : 1, 256, 0, stream>>>(p);

@@ -457,6 +457,14 @@ int skiparse_debug_rope(const void* x, float* x_rot, int B, int heads, int N, in
   return launch_status(launch_debug_rope(p, stream));
 }
 
+int skiparse_debug_wait_timeout(int code, cudaStream_t stream) {
+  if (code <= 0) return SKIPARSE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  int st = device_info(dev);
+  if (st != SKIPARSE_OK) return st;
+  return launch_status(launch_debug_wait_timeout(dev.err_word, code, stream));
+}
+
 int skiparse_device_error(int* detail) {
   DeviceInfo dev;
   int st = device_info(dev);

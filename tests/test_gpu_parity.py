@@ -176,3 +176,31 @@ def test_empty_and_invalid_calls_on_device(env):
     empty = torch.zeros((0, 256, 2, 64), dtype=torch.bfloat16, device=dev)
     skp.skiparse_attn_fwd(empty, empty, empty, empty, lse, 4, 8, 8, 2, 0)
     assert out.abs().sum().item() == 0
+
+
+def test_bounded_wait_times_out_and_context_survives(env):
+    """A wait on an mbarrier that nothing arrives at gives up after about one
+    second, records its code in the device error word and lets the kernel exit;
+    the context then still runs an attention call to parity."""
+    import time
+    import torch
+    skp, dev = env
+    assert skp.skiparse_device_error() == (0, 0)
+    with pytest.raises(skp.SkiparseError):
+        skp.skiparse_debug_wait_timeout(0)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    skp.skiparse_debug_wait_timeout(0x7e01)
+    st, detail = skp.skiparse_device_error()
+    elapsed = time.perf_counter() - t0
+    assert st == -8 and detail == 0x7e01
+    assert 0.9 < elapsed < 10.0
+    assert skp.skiparse_device_error() == (0, 0)        # reading clears the word
+    B, heads, D, T, H, W, k, mode = 1, 2, 64, 4, 8, 8, 2, O.GROUP
+    N = T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D)
+    fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode)
+    f = tl.f64_inputs(ins)
+    rout, _ = O.skiparse_fwd(f["q"], f["k"], f["v"], T, H, W, k, mode)
+    tl.compare("out", tl.host(fw["out"]), rout)
+    assert skp.skiparse_device_error() == (0, 0)
