@@ -312,10 +312,12 @@ def gpu_arm(args):
                       device=dev)
     stream = torch.cuda.current_stream()
 
+    # a training step: the backward reuses the rotated q / k the forward left in
+    # its workspace (as autograd keeps a forward's saved tensors for its backward)
     def step(kk=k):
         skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, mode, stream=stream, workspace=fws)
-        skp.skiparse_attn_bwd(d["q"], d["k"], d["v"], out, lse, d["do"], dq, dk, dv, ws, T, H, W, kk, mode,
-                              stream=stream)
+        skp.skiparse_attn_bwd_saved(fws, d["v"], out, lse, d["do"], dq, dk, dv, ws, T, H, W, kk, mode,
+                                    stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -370,8 +372,8 @@ def gpu_arm(args):
     def step_on(di, do_):
         skp.skiparse_attn_fwd(di["q"], di["k"], di["v"], do_["out"], do_["lse"], T, H, W, k, mode, stream=stream,
                               workspace=fws)
-        skp.skiparse_attn_bwd(di["q"], di["k"], di["v"], do_["out"], do_["lse"], di["do"], do_["dq"], do_["dk"],
-                              do_["dv"], ws, T, H, W, k, mode, stream=stream)
+        skp.skiparse_attn_bwd_saved(fws, di["v"], do_["out"], do_["lse"], di["do"], do_["dq"], do_["dk"], do_["dv"],
+                                    ws, T, H, W, k, mode, stream=stream)
 
     def e2e_pipeline(nsteps, e_start=None):
         ev_comp, ev_out = [], []

@@ -112,6 +112,30 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
+ * Backward pass reusing the forward pass's rotated q and k: the same outputs,
+ * bit for bit, as skiparse_attn_bwd on the q and k of that forward call, for
+ * a training step that keeps the forward workspace until its backward (no
+ * counterpart in the pages; it saves the preprocess's re-read of q and k and
+ * its rewrite of their rotated copies).
+ *   fwd_workspace      in : the workspace skiparse_attn_fwd wrote for the same
+ *                           sizes, mode and rope_theta, unchanged since;
+ *                           fwd_workspace_bytes at least
+ *                           skiparse_attn_fwd_workspace_bytes(...); read only.
+ *   v, out, lse, dout  in : as for skiparse_attn_bwd.
+ *   dq, dk, dv         out: as for skiparse_attn_bwd (gradients w.r.t. the
+ *                           pre-RoPE q, k and v of the forward call).
+ *   workspace          scratch: as for skiparse_attn_bwd; this call needs
+ *                           less (no rotated copies), so a workspace sized by
+ *                           skiparse_attn_bwd_workspace_bytes(...) suffices.
+ * Errors as for skiparse_attn_bwd; SKIPARSE_ERR_WORKSPACE also when
+ * fwd_workspace_bytes is too small. fwd_workspace must not overlap any output.
+ */
+int skiparse_attn_bwd_saved(const void* fwd_workspace, size_t fwd_workspace_bytes, const void* v, const void* out,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, int B, int heads, int N, int D, int T, int H, int W,
+                            int sparse_k, int mode, float rope_theta, cudaStream_t stream);
+
+/*
  * Allocation-free backward. The pages have no counterpart to this entry point:
  * it exists for callers that cannot allocate device memory when they run the
  * backward (a host whose allocator must not be re-entered, a plugin or

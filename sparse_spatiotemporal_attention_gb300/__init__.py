@@ -26,7 +26,7 @@ EXPORTS = (
     "skiparse_attn_fwd_workspace_bytes", "skiparse_attn_fwd", "skiparse_attn_bwd_workspace_bytes", "skiparse_attn_bwd",
     "skiparse_debug_index_map", "skiparse_debug_rope", "skiparse_status_string",
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
-    "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout",
+    "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout", "skiparse_attn_bwd_saved",
 )
 
 
@@ -65,6 +65,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_kernel_name": (ctypes.c_char_p, [_c_int]),
         "skiparse_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_debug_wait_timeout": (_c_int, [_c_int, _vp]),
+        "skiparse_attn_bwd_saved": (_c_int, [_vp, _c_size] + [_vp] * 8 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -147,6 +148,22 @@ def skiparse_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace, T, H, W, s
                                           B, heads, N, D, T, H, W, sparse_k, mode,
                                           float(rope_theta), _stream(stream))
     _check(st, "skiparse_attn_bwd")
+
+
+def skiparse_attn_bwd_saved(fwd_workspace, v, out, lse, dout, dq, dk, dv, workspace, T, H, W, sparse_k, mode,
+                            rope_theta=10000.0, stream=None, fwd_workspace_bytes=None, workspace_bytes=None):
+    """Backward pass that reuses the rotated q and k the forward call left in
+    `fwd_workspace` (same sizes, mode and rope_theta; unchanged since)."""
+    B, heads, N, D = _shape(v)
+    if fwd_workspace_bytes is None:
+        fwd_workspace_bytes = fwd_workspace.numel() * fwd_workspace.element_size()
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = load_library().skiparse_attn_bwd_saved(_ptr(fwd_workspace), int(fwd_workspace_bytes), _ptr(v), _ptr(out),
+                                                _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                                int(workspace_bytes), B, heads, N, D, T, H, W, sparse_k, mode,
+                                                float(rope_theta), _stream(stream))
+    _check(st, "skiparse_attn_bwd_saved")
 
 
 def skiparse_attn_bwd_noalloc(q, k, v, out, lse, dout, dq, dk, dv, T, H, W, sparse_k, mode,

@@ -36,8 +36,8 @@ __device__ __forceinline__ void st_slice(uint16_t* dst, const uint32_t (&v)[PPL]
 }
 
 // Preprocess: per (b, token, head) row, delta = rowsum(dO * O) and lse * log2(e)
-// at the row's scope-order slot, rotated bf16 copies of q and k, and the row's
-// dQ accumulator zeroed. One warp per row, two rows per iteration so each lane
+// at the row's scope-order slot, rotated bf16 copies of q and k (unless the
+// forward pass's copies are reused), and the row's dQ accumulator zeroed. One warp per row, two rows per iteration so each lane
 // has its loads of both rows in flight before it uses either.
 template <int D>
 __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
@@ -63,8 +63,10 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
       const long long row = r0 + u * stride;
       if (row >= rows) continue;
       const size_t base = (size_t)row * D + lane * 2 * PPL;
-      ld_slice<PPL>(p.q + base, qv[u]);
-      ld_slice<PPL>(p.k + base, kv[u]);
+      if (p.rotate_qk) {
+        ld_slice<PPL>(p.q + base, qv[u]);
+        ld_slice<PPL>(p.k + base, kv[u]);
+      }
       ld_slice<PPL>(p.out + base, ov[u]);
       ld_slice<PPL>(p.dout + base, dv[u]);
       if (lane == 0) {
@@ -84,23 +86,28 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
       int t, hh, w;
       token_coords(p.rope, i, t, hh, w);
       float dsum = 0.f;
-      uint32_t qo[PPL], ko[PPL];
 #pragma unroll
       for (int e = 0; e < PPL; ++e) {
         dsum = fmaf(bf16lo(ov[u][e]), bf16lo(dv[u][e]), dsum);
         dsum = fmaf(bf16hi(ov[u][e]), bf16hi(dv[u][e]), dsum);
-        const float2 cs = tab[pair_index(sel[e], t, hh, w)];
-        const float2 a = rope_rotate(bf16lo(qv[u][e]), bf16hi(qv[u][e]), cs);
-        const float2 c = rope_rotate(bf16lo(kv[u][e]), bf16hi(kv[u][e]), cs);
-        qo[e] = pack_bf16(a.x, a.y);
-        ko[e] = pack_bf16(c.x, c.y);
+      }
+      const size_t base = (size_t)row * D + lane * 2 * PPL;
+      if (p.rotate_qk) {
+        uint32_t qo[PPL], ko[PPL];
+#pragma unroll
+        for (int e = 0; e < PPL; ++e) {
+          const float2 cs = tab[pair_index(sel[e], t, hh, w)];
+          const float2 a = rope_rotate(bf16lo(qv[u][e]), bf16hi(qv[u][e]), cs);
+          const float2 c = rope_rotate(bf16lo(kv[u][e]), bf16hi(kv[u][e]), cs);
+          qo[e] = pack_bf16(a.x, a.y);
+          ko[e] = pack_bf16(c.x, c.y);
+        }
+        st_slice<PPL>(p.qr + base, qo);
+        st_slice<PPL>(p.kr + base, ko);
       }
       int s, pp;
       scope_pos_of(g, i, s, pp);
       const size_t idx = (((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp;   // scope-order row
-      const size_t base = (size_t)row * D + lane * 2 * PPL;
-      st_slice<PPL>(p.qr + base, qo);
-      st_slice<PPL>(p.kr + base, ko);
       float* acc = p.dq_acc + idx * D + lane * 2 * PPL;
       if (PPL == 2) *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
       else *reinterpret_cast<float2*>(acc) = make_float2(0.f, 0.f);

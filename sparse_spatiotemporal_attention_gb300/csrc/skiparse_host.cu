@@ -239,7 +239,9 @@ struct WsLayout {
   int Lp;
 };
 
-WsLayout ws_layout(const Shape& s) {
+// with_qk = false: the rotated q / k come from the forward pass's workspace and
+// their regions are left out (the full layout is a superset).
+WsLayout ws_layout(const Shape& s, bool with_qk = true) {
   WsLayout w;
   const size_t e = (size_t)s.elems;
   const int L = s.N / s.k;
@@ -247,8 +249,8 @@ WsLayout ws_layout(const Shape& s) {
   const size_t stats = (size_t)s.B * s.heads * s.k * w.Lp;
   size_t off = 0;
   w.dq_acc = off; off += align256(stats * (size_t)s.D * 4);   // scope order (B, heads, k, Lp, D)
-  w.qr = off;     off += align256(e * 2);
-  w.kr = off;     off += align256(e * 2);
+  w.qr = off;     off += with_qk ? align256(e * 2) : 0;
+  w.kr = off;     off += with_qk ? align256(e * 2) : 0;
   w.lse2s = off;  off += align256(stats * 4);
   w.delta_s = off; off += align256(stats * 4);
   w.tab = off;    off += align256((size_t)s.rope_entries * sizeof(float2));
@@ -354,23 +356,34 @@ size_t skiparse_attn_bwd_workspace_bytes(int B, int heads, int N, int D, int T, 
   return ws_layout(s).total;
 }
 
-int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                      const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                      int B, int heads, int N, int D, int T, int H, int W,
-                      int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Backward: q / k given (rotated here, qr_in == kr_in == nullptr), or the
+// forward pass's rotated copies qr_in / kr_in (q == k == nullptr).
+int bwd_impl(const void* q, const void* k, const void* qr_in, const void* kr_in, size_t fwd_ws_bytes,
+             const void* v, const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+             void* workspace, size_t workspace_bytes, int B, int heads, int N, int D, int T, int H, int W,
+             int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
   Shape s;
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
-  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return SKIPARSE_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
+  const bool saved = qr_in != nullptr;
+  if (!v || !out || !lse || !dout || !dq || !dk || !dv) return SKIPARSE_ERR_INVALID_ARG;
+  if (saved ? !kr_in : (!q || !k)) return SKIPARSE_ERR_INVALID_ARG;
+  const void* qa = saved ? qr_in : q;
+  const void* ka = saved ? kr_in : k;
+  if (!aligned16(qa) || !aligned16(ka) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return SKIPARSE_ERR_ALIGNMENT;
-  const WsLayout w = ws_layout(s);
+  const WsLayout w = ws_layout(s, !saved);
   if (!workspace || workspace_bytes < w.total) return SKIPARSE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
   const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
+  if (saved && fwd_ws_bytes < 2 * align256(tb)) return SKIPARSE_ERR_WORKSPACE;
   if (any_alias({{dq, tb}, {dk, tb}, {dv, tb}, {workspace, w.total}},
-                {{q, tb}, {k, tb}, {v, tb}, {out, tb}, {lse, lb}, {dout, tb}}))
+                {{qa, tb}, {ka, tb}, {v, tb}, {out, tb}, {lse, lb}, {dout, tb}}))
     return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
@@ -387,8 +400,9 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
   p.dout = static_cast<const uint16_t*>(dout);
   p.lse = lse;
   p.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
-  p.qr = reinterpret_cast<uint16_t*>(ws + w.qr);
-  p.kr = reinterpret_cast<uint16_t*>(ws + w.kr);
+  p.rotate_qk = saved ? 0 : 1;
+  p.qr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(qr_in)) : reinterpret_cast<uint16_t*>(ws + w.qr);
+  p.kr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kr_in)) : reinterpret_cast<uint16_t*>(ws + w.kr);
   p.lse2s = reinterpret_cast<float*>(ws + w.lse2s);
   p.delta_s = reinterpret_cast<float*>(ws + w.delta_s);
   p.rope_tab = reinterpret_cast<float2*>(ws + w.tab);
@@ -413,6 +427,34 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
   st = launch_status(traced_launch(2, stream, [&] { return launch_bwd_main(p, mgrid, stream); }));
   if (st != SKIPARSE_OK) return st;
   return launch_status(traced_launch(3, stream, [&] { return launch_bwd_post(p, (int)rgrid, stream); }));
+}
+
+}  // namespace
+
+extern "C" {
+
+int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                      int B, int heads, int N, int D, int T, int H, int W,
+                      int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+  return bwd_impl(q, k, nullptr, nullptr, 0, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, heads, N,
+                  D, T, H, W, sparse_k, mode, rope_theta, stream);
+}
+
+int skiparse_attn_bwd_saved(const void* fwd_workspace, size_t fwd_workspace_bytes, const void* v, const void* out,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, int B, int heads, int N, int D, int T, int H, int W,
+                            int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+  Shape s;
+  const int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
+  if (st != SKIPARSE_OK || s.empty) return st;
+  if (!fwd_workspace) return SKIPARSE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(fwd_workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
+  // the forward workspace holds rotated q, then rotated k, each 256-byte aligned
+  const uint8_t* fw = static_cast<const uint8_t*>(fwd_workspace);
+  const size_t half = align256((size_t)s.elems * 2);
+  return bwd_impl(nullptr, nullptr, fw, fw + half, fwd_workspace_bytes, v, out, lse, dout, dq, dk, dv, workspace,
+                  workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, stream);
 }
 
 int skiparse_debug_index_map(int* scope_of_token, int* pos_of_token, int N, int sparse_k, int mode,

@@ -43,8 +43,8 @@ struct BwdParams {
   const uint16_t* out;
   const uint16_t* dout;
   const float* lse;
-  uint16_t* qr;            // workspace: rotated q, bf16 (B, N, heads, D)
-  uint16_t* kr;            // workspace: rotated k
+  uint16_t* qr;            // rotated q, bf16 (B, N, heads, D): workspace, or the forward's
+  uint16_t* kr;            // rotated k, likewise
   float* dq_acc;           // workspace: fp32 (B, heads, k, Lp, D), scope order
   float* lse2s;            // workspace: lse * log2(e), scope order (B, heads, k, Lp)
   float* delta_s;          // workspace: rowsum(dO * O), scope order (B, heads, k, Lp)
@@ -54,6 +54,7 @@ struct BwdParams {
   uint16_t* dv;
   int* err;
   int n_units;             // B * heads * k * n_tiles (one K/V tile each)
+  int rotate_qk;           // 1: the preprocess writes qr / kr from q / k; 0: qr / kr are given
   int Lp;                  // L rounded up to a multiple of 128
   float scale;             // 1 / sqrt(D)
   float scale_log2;        // log2(e) / sqrt(D)

@@ -113,6 +113,26 @@ def test_bwd_validation_and_workspace(lib):
     assert bwd() == DEVICE
 
 
+def test_bwd_saved_validation(lib):
+    """The backward that reuses the forward's rotated q / k validates on the host first."""
+    fws = lib.skiparse_attn_fwd_workspace_bytes(1, 2, 256, 64, 4, 8, 8, 2, 0)
+    ws = lib.skiparse_attn_bwd_workspace_bytes(1, 2, 256, 64, 4, 8, 8, 2, 0)
+
+    def bwd(fw_ptr=11 * A, fw_bytes=fws, ws_ptr=10 * A, ws_bytes=ws, dq=7 * A, B=1):
+        return lib.skiparse_attn_bwd_saved(fw_ptr, fw_bytes, 3 * A, 4 * A, 5 * A, 6 * A, dq, 8 * A, 9 * A, ws_ptr,
+                                           ws_bytes, B, 2, 256, 64, 4, 8, 8, 2, 0, 10000.0, None)
+    assert bwd(fw_ptr=None) == INVALID
+    assert bwd(fw_ptr=11 * A + 16) == ALIGN
+    assert bwd(fw_bytes=fws - 1) == WORKSPACE
+    assert bwd(ws_ptr=None) == WORKSPACE
+    assert bwd(dq=3 * A) == ALIAS
+    assert bwd(ws_ptr=11 * A) == ALIAS          # scratch over the forward's rotated q
+    assert bwd(B=0, fw_ptr=None) == OK           # empty call
+    assert bwd() == DEVICE
+    # it needs less scratch than the regular backward (no rotated copies)
+    assert bwd(ws_bytes=ws - 2 * 256 * 2 * 64 * 2) == DEVICE
+
+
 def test_debug_hook_validation(lib):
     assert lib.skiparse_debug_index_map(A, 2 * A, 16, 3, 0, None) == SHAPE
     assert lib.skiparse_debug_index_map(A, 2 * A, 16, 2, 2, None) == INVALID

@@ -87,6 +87,43 @@ def test_backward_parity(env, case):
     assert st == 0, hex(detail)
 
 
+SAVED_CASES = [(1, 2, 128, 3, 10, 10, 2, O.GROUP), (2, 3, 64, 2, 8, 12, 2, O.SINGLE), (2, 2, 128, 3, 20, 24, 4, O.SINGLE)]
+
+
+@pytest.mark.parametrize("case", SAVED_CASES, ids=_ids)
+def test_backward_saved_bitwise_and_parity(env, case):
+    """The backward that reuses the forward's rotated q / k gives the regular
+    backward's outputs bit for bit (the same kernels read bitwise-equal rotated
+    copies), and so matches the oracle."""
+    import torch
+    skp, dev = env
+    B, heads, D, T, H, W, k, mode = case
+    N = T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True)
+    q, kk, v, do = (tl.to_device(ins[n], dev) for n in ("q", "k", "v", "do"))
+    out = torch.empty((B, N, heads, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, heads, N), dtype=torch.float32, device=dev)
+    fws = torch.empty(skp.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, k, mode), dtype=torch.uint8,
+                      device=dev)
+    skp.skiparse_attn_fwd(q, kk, v, out, lse, T, H, W, k, mode, workspace=fws)
+    nbytes = skp.skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, k, mode)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    g1 = [torch.empty_like(q) for _ in range(3)]
+    g2 = [torch.full_like(q, float("nan")) for _ in range(3)]
+    skp.skiparse_attn_bwd(q, kk, v, out, lse, do, *g1, ws, T, H, W, k, mode)
+    skp.skiparse_attn_bwd_saved(fws, v, out, lse, do, *g2, ws, T, H, W, k, mode)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("dq", "dk", "dv"), g1, g2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
+    f = tl.f64_inputs(ins)
+    rdq, rdk, rdv, _, _ = O.skiparse_bwd(f["q"], f["k"], f["v"], f["do"], T, H, W, k, mode)
+    tl.compare("dq", tl.host(g2[0]), rdq)
+    tl.compare("dk", tl.host(g2[1]), rdk)
+    tl.compare("dv", tl.host(g2[2]), rdv)
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
+
+
 def test_peaky_softmax_rescale(env):
     """q scaled by 4 makes row maxima jump between key tiles, exercising the
     online-softmax rescale of O. Not a contract workload: with |q| four times
