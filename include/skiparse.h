@@ -47,7 +47,8 @@ typedef enum {
   SKIPARSE_OK = 0,
   SKIPARSE_ERR_INVALID_ARG = -1,    /* NULL pointer, negative size, bad mode or theta */
   SKIPARSE_ERR_SHAPE = -2,          /* N != T*H*W, N % k (single) or N % k^2 (group) */
-  SKIPARSE_ERR_UNSUPPORTED = -3,    /* D not 64/128, group k not dividing 128, RoPE table too large */
+  SKIPARSE_ERR_UNSUPPORTED = -3,    /* D not 64/128, group k not dividing 128, RoPE table too large,
+                                       B * N * heads >= 2^31 */
   SKIPARSE_ERR_ALIGNMENT = -4,      /* a pointer not 16-byte aligned */
   SKIPARSE_ERR_DEVICE = -5,         /* no device, or the current device is not sm_103 */
   SKIPARSE_ERR_WORKSPACE = -6,      /* workspace NULL or smaller than the query says */

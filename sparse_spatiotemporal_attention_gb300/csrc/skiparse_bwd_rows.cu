@@ -36,14 +36,18 @@ __device__ __forceinline__ void st_slice(uint16_t* dst, const uint32_t (&v)[PPL]
 }
 
 // Preprocess: per (b, token, head) row, delta = rowsum(dO * O) and lse * log2(e)
-// at the row's scope-order slot, rotated bf16 copies of q and k (unless the
-// forward pass's copies are reused), and the row's dQ accumulator zeroed. One warp per row, two rows per iteration so each lane
-// has its loads of both rows in flight before it uses either.
-template <int D>
+// at the row's scope-order slot and the row's dQ accumulator zeroed; with ROT,
+// also rotated bf16 copies of q and k (without it the forward pass's copies are
+// reused). One warp per row, R rows per iteration so each lane has the loads
+// of all R rows in flight before it uses any.
+template <int D, bool ROT>
 __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
+  constexpr int R = 2;
   extern __shared__ float2 tab[];
   const Geom& g = p.g;
-  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  // the table rotates q and k here; without ROT only block 0 builds it, to hand
+  // it to the post kernel
+  if (ROT || blockIdx.x == 0) rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
   __syncthreads();
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e < p.rope.entries; e += blockDim.x) p.rope_tab[e] = tab[e];
@@ -55,36 +59,33 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
   for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
   const long long rows = (long long)g.B * g.N * g.heads;
   const long long stride = (long long)gridDim.x * wpb;
-  for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += 2 * stride) {
-    uint32_t qv[2][PPL], kv[2][PPL], ov[2][PPL], dv[2][PPL];
-    float lse[2] = {0.f, 0.f};
+  for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += R * stride) {
+    uint32_t qv[R][PPL], kv[R][PPL], ov[R][PPL], dv[R][PPL];
+    float lse[R];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < R; ++u) {
+      lse[u] = 0.f;
       const long long row = r0 + u * stride;
       if (row >= rows) continue;
       const size_t base = (size_t)row * D + lane * 2 * PPL;
-      if (p.rotate_qk) {
+      if (ROT) {
         ld_slice<PPL>(p.q + base, qv[u]);
         ld_slice<PPL>(p.k + base, kv[u]);
       }
       ld_slice<PPL>(p.out + base, ov[u]);
       ld_slice<PPL>(p.dout + base, dv[u]);
       if (lane == 0) {
-        const int head = (int)(row % g.heads);
-        const long long bi = row / g.heads;
-        lse[u] = p.lse[((size_t)(bi / g.N) * g.heads + head) * g.N + (bi % g.N)];
+        int b, i, head;
+        row_coords(g, (int)row, b, i, head);
+        lse[u] = p.lse[((size_t)b * g.heads + head) * g.N + i];
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < R; ++u) {
       const long long row = r0 + u * stride;
       if (row >= rows) continue;
-      const int head = (int)(row % g.heads);
-      const long long bi = row / g.heads;
-      const int i = (int)(bi % g.N);
-      const int b = (int)(bi / g.N);
-      int t, hh, w;
-      token_coords(p.rope, i, t, hh, w);
+      int b, i, head;
+      row_coords(g, (int)row, b, i, head);
       float dsum = 0.f;
 #pragma unroll
       for (int e = 0; e < PPL; ++e) {
@@ -92,7 +93,9 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
         dsum = fmaf(bf16hi(ov[u][e]), bf16hi(dv[u][e]), dsum);
       }
       const size_t base = (size_t)row * D + lane * 2 * PPL;
-      if (p.rotate_qk) {
+      if (ROT) {
+        int t, hh, w;
+        token_coords(p.rope, i, t, hh, w);
         uint32_t qo[PPL], ko[PPL];
 #pragma unroll
         for (int e = 0; e < PPL; ++e) {
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
 }
 
 // Post: dq = R^T (scale * dQ~) for each (b, token, head) row, read from the
-// row's scope-order accumulator slot; two rows per warp iteration.
+// row's scope-order accumulator slot; four rows per warp iteration.
 template <int D>
 __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __grid_constant__ BwdParams p) {
   const Geom& g = p.g;
@@ -134,17 +137,16 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __
   for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
   const long long rows = (long long)g.B * g.N * g.heads;
   const long long stride = (long long)gridDim.x * wpb;
-  for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += 2 * stride) {
-    float x[2][2 * PPL];
-    int tt[2], th[2], tw[2];
+  constexpr int R = 4;
+  for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += R * stride) {
+    float x[R][2 * PPL];
+    int tt[R], th[R], tw[R];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < R; ++u) {
       const long long row = r0 + u * stride;
       if (row >= rows) continue;
-      const int head = (int)(row % g.heads);
-      const long long bi = row / g.heads;
-      const int i = (int)(bi % g.N);
-      const int b = (int)(bi / g.N);
+      int b, i, head;
+      row_coords(g, (int)row, b, i, head);
       token_coords(p.rope, i, tt[u], th[u], tw[u]);
       int s, pp;
       scope_pos_of(g, i, s, pp);
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < R; ++u) {
       const long long row = r0 + u * stride;
       if (row >= rows) continue;
       uint32_t o[PPL];
@@ -173,24 +175,33 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __
   }
 }
 
-cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = (size_t)p.rope.entries * sizeof(float2);
-  cudaError_t e;
-  if (p.g.D == 128) {
-    e = cudaFuncSetAttribute(skiparse_bwd_pre_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_bwd_pre_kernel<128><<<grid, kRowThreads, smem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(skiparse_bwd_pre_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_bwd_pre_kernel<64><<<grid, kRowThreads, smem, stream>>>(p);
-  }
+template <int D, bool ROT>
+static cudaError_t launch_pre_variant(const BwdParams& p, int grid, int sms, size_t smem, cudaStream_t stream) {
+  const cudaError_t e =
+      cudaFuncSetAttribute(skiparse_bwd_pre_kernel<D, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  grid = one_wave(skiparse_bwd_pre_kernel<D, ROT>, grid, kRowThreads, smem, sms);
+  skiparse_bwd_pre_kernel<D, ROT><<<grid, kRowThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_post(const BwdParams& p, int grid, cudaStream_t stream) {
-  if (p.g.D == 128) skiparse_bwd_post_kernel<128><<<grid, kRowThreads, 0, stream>>>(p);
-  else skiparse_bwd_post_kernel<64><<<grid, kRowThreads, 0, stream>>>(p);
+cudaError_t launch_bwd_pre(const BwdParams& p, int grid, int sms, cudaStream_t stream) {
+  const size_t smem = (size_t)p.rope.entries * sizeof(float2);
+  if (p.g.D == 128)
+    return p.rotate_qk ? launch_pre_variant<128, true>(p, grid, sms, smem, stream)
+                       : launch_pre_variant<128, false>(p, grid, sms, smem, stream);
+  return p.rotate_qk ? launch_pre_variant<64, true>(p, grid, sms, smem, stream)
+                     : launch_pre_variant<64, false>(p, grid, sms, smem, stream);
+}
+
+cudaError_t launch_bwd_post(const BwdParams& p, int grid, int sms, cudaStream_t stream) {
+  if (p.g.D == 128) {
+    grid = one_wave(skiparse_bwd_post_kernel<128>, grid, kRowThreads, 0, sms);
+    skiparse_bwd_post_kernel<128><<<grid, kRowThreads, 0, stream>>>(p);
+  } else {
+    grid = one_wave(skiparse_bwd_post_kernel<64>, grid, kRowThreads, 0, sms);
+    skiparse_bwd_post_kernel<64><<<grid, kRowThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

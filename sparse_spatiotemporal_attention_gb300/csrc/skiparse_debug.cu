@@ -30,7 +30,8 @@ __global__ void skiparse_debug_rope_kernel(const __grid_constant__ DebugParams p
   const int wpb = blockDim.x >> 5;
   const long long rows = (long long)g.B * g.N * g.heads;
   for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb) {
-    const int i = (int)((row / g.heads) % g.N);
+    int b, i, head;
+    row_coords(g, (int)row, b, i, head);
     int t, hh, w;
     token_coords(p.rope, i, t, hh, w);
     for (int pp = lane; pp < D / 2; pp += 32) {

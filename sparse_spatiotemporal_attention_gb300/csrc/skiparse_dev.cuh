@@ -63,7 +63,18 @@ struct Geom {
   int n_tiles;  // ceil(L / 128)
   FastDiv fk;   // division by k
   FastDiv fkG;  // division by k * G
+  FastDiv fheads;  // division by heads (row index -> (b * N + token, head))
+  FastDiv fN;      // division by N (b * N + token -> (b, token))
 };
+
+// (b, token i, head) of row index `row` = (b * N + i) * heads + head of a
+// (B, N, heads, D) tensor; rows < 2^31.
+__device__ __forceinline__ void row_coords(const Geom& g, int row, int& b, int& i, int& head) {
+  const int bi = fdiv(row, g.fheads);
+  head = row - bi * g.heads;
+  b = fdiv(bi, g.fN);
+  i = bi - b * g.N;
+}
 
 struct RopeParams {
   double om_t[16];    // rope_theta^(-2j/dt) for the t chunk (dt = D/4 channels, D/8 pairs)

@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_rope_kernel(const _
     for (int u = 0; u < 2; ++u) {
       const long long row = r0 + u * stride;
       if (row >= rows) continue;
-      const int i = (int)((row / g.heads) % g.N);
+      int b, i, head;
+      row_coords(g, (int)row, b, i, head);
       token_coords(p.rope, i, tt[u], th[u], tw[u]);
       const size_t base = (size_t)row * D + lane * 2 * PPL;
       if (PPL == 2) {
@@ -477,16 +478,18 @@ size_t fwd_rope_smem_bytes(int rope_entries) { return (size_t)rope_entries * siz
 
 int fwd_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 2); }
 
-cudaError_t launch_fwd_rope(const FwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t stream) {
   const size_t smem = fwd_rope_smem_bytes(p.rope.entries);
   cudaError_t e;
   if (p.g.D == 128) {
     e = cudaFuncSetAttribute(skiparse_fwd_rope_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    grid = one_wave(skiparse_fwd_rope_kernel<128>, grid, kRopeThreads, smem, sms);
     skiparse_fwd_rope_kernel<128><<<grid, kRopeThreads, smem, stream>>>(p);
   } else {
     e = cudaFuncSetAttribute(skiparse_fwd_rope_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    grid = one_wave(skiparse_fwd_rope_kernel<64>, grid, kRopeThreads, smem, sms);
     skiparse_fwd_rope_kernel<64><<<grid, kRopeThreads, smem, stream>>>(p);
   }
   return cudaGetLastError();

@@ -153,7 +153,8 @@ int check_shape(int B, int heads, int N, int D, int T, int H, int W, int k, int 
   s.elems = (long long)B * N * heads * D;
   const long long L = N / k;
   const long long units = (long long)B * heads * k * ((L + kTile - 1) / kTile);
-  if (s.elems > (1ll << 46) || units >= (1ll << 31) || (long long)B * N >= (1ll << 31)) return SKIPARSE_ERR_UNSUPPORTED;
+  if (s.elems > (1ll << 46) || units >= (1ll << 31) || (long long)B * N * heads >= (1ll << 31))
+    return SKIPARSE_ERR_UNSUPPORTED;
   return SKIPARSE_OK;
 }
 
@@ -192,6 +193,8 @@ Geom make_geom(const Shape& s) {
   while ((1 << g.lgG) < g.G) ++g.lgG;
   g.fk = make_fastdiv(s.k);
   g.fkG = make_fastdiv(s.k * g.G);
+  g.fheads = make_fastdiv(s.heads > 0 ? s.heads : 1);
+  g.fN = make_fastdiv(s.N > 0 ? s.N : 1);
   g.L = s.N / s.k;
   g.Nn = g.L / g.G;
   g.n_tiles = (g.L + kTile - 1) / kTile;
@@ -345,7 +348,7 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   long long rgrid = (rows + 15) / 16;                 // 8 warps per CTA, 2 rows per warp
   if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
-  st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, stream); }));
+  st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, dev.sms, stream); }));
   if (st != SKIPARSE_OK) return st;
   return launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));
 }
@@ -422,11 +425,11 @@ int bwd_impl(const void* q, const void* k, const void* qr_in, const void* kr_in,
   long long rgrid = (rows + 15) / 16;                 // 8 warps per CTA, 2 rows per warp
   if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
   const int mgrid = p.n_units < dev.sms ? p.n_units : dev.sms;
-  st = launch_status(traced_launch(1, stream, [&] { return launch_bwd_pre(p, (int)rgrid, stream); }));
+  st = launch_status(traced_launch(1, stream, [&] { return launch_bwd_pre(p, (int)rgrid, dev.sms, stream); }));
   if (st != SKIPARSE_OK) return st;
   st = launch_status(traced_launch(2, stream, [&] { return launch_bwd_main(p, mgrid, stream); }));
   if (st != SKIPARSE_OK) return st;
-  return launch_status(traced_launch(3, stream, [&] { return launch_bwd_post(p, (int)rgrid, stream); }));
+  return launch_status(traced_launch(3, stream, [&] { return launch_bwd_post(p, (int)rgrid, dev.sms, stream); }));
 }
 
 }  // namespace

@@ -69,18 +69,31 @@ struct DebugParams {
   int* pos_of_token;
 };
 
+// Grid-stride row kernels: at most one wave of resident CTAs (SMs x CTAs per SM
+// at this block size and shared memory), so no partial second wave idles SMs.
+template <typename K>
+inline int one_wave(K kernel, int grid, int threads, size_t smem, int sms) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    return grid;
+  }
+  const long long wave = (long long)per_sm * sms;
+  return grid < wave ? grid : (int)wave;
+}
+
 // Shared-memory bytes and launch helpers (defined next to each kernel).
 size_t fwd_smem_bytes(int D);
 size_t fwd_rope_smem_bytes(int rope_entries);
 int fwd_units(const Geom& g);
-cudaError_t launch_fwd_rope(const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
 
 size_t bwd_main_smem_bytes(int D);
 bool bwd_uses_tile_kernel(int D);
-cudaError_t launch_bwd_pre(const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const BwdParams& p, int grid, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_bwd_post(const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_post(const BwdParams& p, int grid, int sms, cudaStream_t stream);
 
 cudaError_t launch_debug_index_map(const DebugParams& p, cudaStream_t stream);
 cudaError_t launch_debug_rope(const DebugParams& p, cudaStream_t stream);
