@@ -1,0 +1,165 @@
+"""Plain CPU float64 oracle for the 8-bit Skiparse attention forward pass.
+
+TEST INFRASTRUCTURE ONLY: imported by tests and bench.py's CPU legs, never by
+the library. It builds on skiparse_oracle.py (RoPE, rearrange) and shares no
+code with the GPU path.
+
+The method follows the Wan 2.1 report ("Open and Advanced Large-Scale Video
+Generative Models"), section 4 "Model Design and Acceleration", 4.4.3
+"Quantization", paragraph "8-Bit FlashAttention":
+attention inputs are quantized to 8 bits for the two products S = Q K^T and
+O = P V, and the products of successive key blocks are accumulated in fp32.
+Readings taken here (the page gives the recipe for Hopper and no formulas):
+
+  * both products use FP8 E4M3 operands. The page's INT8 for S = Q K^T is not
+    a fast path on the target (its INT8 tensor rate is far below its FP8 rate);
+    E4M3 keeps the page's point of 8-bit operands with per-row scales;
+  * q and k are quantized after RoPE, per (token, head) row: scale
+    s = max|x| / 448 (448 = largest finite E4M3), codes RNE(x * 448 / max|x|)
+    (an all-zero row gets scale 1 and codes 0);
+  * v is quantized per (batch, head, channel) over all N tokens with the same
+    rule, so its scale factors out of O = P V column by column;
+  * attention runs per scope over blocks of 128 keys (scope order) with an
+    online softmax in base 2: the running row max m (of S * scale * log2 e) is
+    set by the first block and raised only when a later block's max exceeds it
+    by more than 8 (then O and l are rescaled by 2^(m_old - m_new)); this is
+    the fp32 kernel's lazy rescaling rule, needed here because P is quantized
+    against the running max, not the final one;
+  * P = 2^(S * scale * log2 e - m) is quantized as RNE_E4M3(P * 2^8) for O += P V
+    (fp32 cross-block accumulation), while the row sum l adds the unquantized P;
+  * out = O * s_v / (2^8 * l) (bf16 on the GPU), lse = (m + log2 l) * ln 2.
+
+Everything else is float64. Parity pins: tests/test_oracle_fp8.py.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import skiparse_oracle as O
+
+E4M3_MAX = 448.0
+P_SCALE = 256.0
+BLOCK = 128
+LAZY_LOG2 = 8.0
+
+
+def e4m3_values() -> np.ndarray:
+    """All finite non-negative E4M3 (fn) values, ascending, from the format's
+    definition: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent field 0
+    is subnormal (m/8 * 2^-6); the all-ones code (S.1111.111) is NaN, so the
+    largest finite value is 1.75 * 2^8 = 448."""
+    vals = []
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue                      # NaN
+            if e == 0:
+                vals.append(m / 8.0 * 2.0 ** -6)
+            else:
+                vals.append((1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return np.array(vals, dtype=np.float64)
+
+
+_GRID = e4m3_values()
+
+
+def round_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest finite E4M3 value, ties to the even code,
+    saturating at +-448 (the GPU's cvt.rn.satfinite)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    idx = np.searchsorted(_GRID, a)                      # first grid value >= a
+    idx = np.clip(idx, 1, len(_GRID) - 1)
+    lo, hi = _GRID[idx - 1], _GRID[idx]
+    take_hi = (hi - a) < (a - lo)
+    tie = (hi - a) == (a - lo)
+    # codes are consecutive integers along the grid: the even code is the even index
+    take_hi = take_hi | (tie & ((idx % 2) == 0))
+    r = np.where(take_hi, hi, lo)
+    r = np.where(a <= _GRID[0], 0.0, r)
+    return np.copysign(r, x)
+
+
+def quantize_rows(x: np.ndarray):
+    """Per-row E4M3 codes and scales over the last axis: x ~ codes * scale."""
+    amax = np.abs(x).max(axis=-1, keepdims=True)
+    safe = np.where(amax > 0, amax, E4M3_MAX)
+    codes = round_e4m3(x * (E4M3_MAX / safe))
+    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0)
+    return codes, scale[..., 0]
+
+
+def quantize_channels(v: np.ndarray):
+    """v (B, N, heads, D): per (b, head, channel) E4M3 codes and scales over N."""
+    amax = np.abs(v).max(axis=1, keepdims=True)                   # (B, 1, heads, D)
+    safe = np.where(amax > 0, amax, E4M3_MAX)
+    codes = round_e4m3(v * (E4M3_MAX / safe))
+    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0)
+    return codes, scale[:, 0]                                       # (B, heads, D)
+
+
+def blocked_attention(sq, sk, q8, k8, v8, sv, scale, quantize_p=True):
+    """One scope problem: q8 (L, D) codes with row scales sq (L,), k8 (L, D) with
+    sk (L,), v8 (L, D) with channel scales sv (D,). Online softmax over blocks of
+    128 keys with the lazy rule; returns (out (L, D), lse (L,))."""
+    L, D = q8.shape
+    log2e = 1.0 / math.log(2.0)
+    S = (sq[:, None] * sk[None, :]) * (q8 @ k8.T) * scale * log2e     # (L, L), base-2 units
+    m = np.zeros(L)
+    l = np.zeros(L)
+    acc = np.zeros((L, D))
+    for j0 in range(0, L, BLOCK):
+        Sb = S[:, j0:j0 + BLOCK]
+        mx = Sb.max(axis=1)
+        if j0 == 0:
+            m = mx.copy()
+        else:
+            up = mx > m + LAZY_LOG2
+            m_new = np.where(up, mx, m)
+            f = np.exp2(m - m_new)
+            acc *= f[:, None]
+            l *= f
+            m = m_new
+        P = np.exp2(Sb - m[:, None])
+        l += P.sum(axis=1)
+        Pq = round_e4m3(P * P_SCALE) if quantize_p else P * P_SCALE
+        acc += Pq @ v8[j0:j0 + BLOCK]
+    out = acc * sv[None, :] / (P_SCALE * l[:, None])
+    lse = (m + np.log2(l)) * math.log(2.0)
+    return out, lse
+
+
+def skiparse_fwd_fp8(q, k, v, T, H, W, sparse_k, mode, theta=10000.0, quantize=True):
+    """q, k, v: (B, N, heads, D) float64 (bf16-valued). Returns out (B, N, heads, D)
+    and lse (B, heads, N). quantize=False replaces every E4M3 rounding by the
+    identity (then the result is exact softmax attention)."""
+    B, N, nh, D = q.shape
+    scale = 1.0 / math.sqrt(D)
+    qr = O.apply_rope(q, T, H, W, theta)
+    kr = O.apply_rope(k, T, H, W, theta)
+    vv = np.asarray(v, dtype=np.float64)
+    if quantize:
+        q8, sq = quantize_rows(qr)
+        k8, sk = quantize_rows(kr)
+        v8, sv = quantize_channels(vv)
+    else:
+        q8, sq = qr, np.ones(qr.shape[:-1])
+        k8, sk = kr, np.ones(kr.shape[:-1])
+        v8, sv = vv, np.ones((B, nh, D))
+    q8r, k8r, v8r = (O.rearrange(a, sparse_k, mode) for a in (q8, k8, v8))
+    sqr = O.rearrange(sq[..., None], sparse_k, mode)[..., 0]          # (kB, L, heads)
+    skr = O.rearrange(sk[..., None], sparse_k, mode)[..., 0]
+    o_r = np.empty_like(q8r)
+    lse_r = np.empty(q8r.shape[:3])
+    for r in range(q8r.shape[0]):
+        b = r % B                                    # rearranged batch row r = s * B + b
+        for h in range(nh):
+            o, lse = blocked_attention(sqr[r, :, h], skr[r, :, h], q8r[r, :, h], k8r[r, :, h], v8r[r, :, h],
+                                       sv[b, h], scale, quantize_p=quantize)
+            o_r[r, :, h] = o
+            lse_r[r, :, h] = lse
+    out = O.reverse(o_r, sparse_k, mode)
+    lse = O.reverse(lse_r, sparse_k, mode)
+    return out, np.ascontiguousarray(np.transpose(lse, (0, 2, 1)))
