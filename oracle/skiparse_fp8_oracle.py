@@ -14,9 +14,10 @@ Readings taken here (the page gives the recipe for Hopper and no formulas):
   * both products use FP8 E4M3 operands. The page's INT8 for S = Q K^T is not
     a fast path on the target (its INT8 tensor rate is far below its FP8 rate);
     E4M3 keeps the page's point of 8-bit operands with per-row scales;
-  * q and k are quantized after RoPE, per (token, head) row: scale
-    s = max|x| / 448 (448 = largest finite E4M3), codes RNE(x * 448 / max|x|)
-    (an all-zero row gets scale 1 and codes 0);
+  * q and k are quantized after RoPE: q per (token, head) row, k per block of
+    128 consecutive keys of a scope (a per-block scale, as SageAttention's),
+    with scale s = max|x| / 448 over the row or block (448 = largest finite
+    E4M3) and codes RNE(x * 448 / max|x|) (all-zero data: scale 1, codes 0);
   * v is quantized per (batch, head, channel) over all N tokens with the same
     rule, so its scale factors out of O = P V column by column;
   * attention runs per scope over blocks of 128 keys (scope order) with an
@@ -91,6 +92,18 @@ def quantize_rows(x: np.ndarray):
     return codes, scale[..., 0]
 
 
+def quantize_blocks(x: np.ndarray, block: int = BLOCK):
+    """x (L, D) in scope order: per block of `block` rows, E4M3 codes and one
+    scale (returned per row, constant within a block)."""
+    codes = np.empty_like(x)
+    scale = np.empty(x.shape[0])
+    for j0 in range(0, x.shape[0], block):
+        c, s_ = quantize_rows(x[j0:j0 + block].reshape(1, -1))
+        codes[j0:j0 + block] = c.reshape(-1, x.shape[1])
+        scale[j0:j0 + block] = s_[0]
+    return codes, scale
+
+
 def quantize_channels(v: np.ndarray):
     """v (B, N, heads, D): per (b, head, channel) E4M3 codes and scales over N."""
     amax = np.abs(v).max(axis=1, keepdims=True)                   # (B, 1, heads, D)
@@ -142,21 +155,23 @@ def skiparse_fwd_fp8(q, k, v, T, H, W, sparse_k, mode, theta=10000.0, quantize=T
     vv = np.asarray(v, dtype=np.float64)
     if quantize:
         q8, sq = quantize_rows(qr)
-        k8, sk = quantize_rows(kr)
         v8, sv = quantize_channels(vv)
     else:
         q8, sq = qr, np.ones(qr.shape[:-1])
-        k8, sk = kr, np.ones(kr.shape[:-1])
         v8, sv = vv, np.ones((B, nh, D))
-    q8r, k8r, v8r = (O.rearrange(a, sparse_k, mode) for a in (q8, k8, v8))
+    q8r, v8r = (O.rearrange(a, sparse_k, mode) for a in (q8, v8))
+    krr = O.rearrange(kr, sparse_k, mode)                              # k blocks are scope blocks
     sqr = O.rearrange(sq[..., None], sparse_k, mode)[..., 0]          # (kB, L, heads)
-    skr = O.rearrange(sk[..., None], sparse_k, mode)[..., 0]
     o_r = np.empty_like(q8r)
     lse_r = np.empty(q8r.shape[:3])
     for r in range(q8r.shape[0]):
         b = r % B                                    # rearranged batch row r = s * B + b
         for h in range(nh):
-            o, lse = blocked_attention(sqr[r, :, h], skr[r, :, h], q8r[r, :, h], k8r[r, :, h], v8r[r, :, h],
+            if quantize:
+                k8, sk = quantize_blocks(krr[r, :, h])
+            else:
+                k8, sk = krr[r, :, h], np.ones(krr.shape[1])
+            o, lse = blocked_attention(sqr[r, :, h], sk, q8r[r, :, h], k8, v8r[r, :, h],
                                        sv[b, h], scale, quantize_p=quantize)
             o_r[r, :, h] = o
             lse_r[r, :, h] = lse

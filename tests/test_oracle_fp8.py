@@ -60,6 +60,17 @@ def test_row_quantizer_reconstructs_within_half_ulp():
     assert np.all(zc == 0) and np.all(zs == 1.0)
 
 
+def test_block_quantizer_one_scale_per_128_rows():
+    rs = np.random.RandomState(4)
+    x = rs.randn(300, 64)
+    x[130] *= 10.0                                     # an outlier row sets block 1's scale
+    codes, scale = F.quantize_blocks(x)
+    assert np.all(scale[:128] == scale[0]) and np.all(scale[128:256] == scale[128]) and np.all(scale[256:] == scale[256])
+    assert np.isclose(scale[128], np.abs(x[128:256]).max() / 448.0)
+    assert np.isclose(np.abs(codes[128:256]).max(), 448.0)
+    assert np.all(np.abs(codes * scale[:, None] - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * scale[:, None]) * (1 + 1e-12))
+
+
 def test_channel_quantizer_scales_over_tokens():
     rs = np.random.RandomState(6)
     v = rs.randn(2, 300, 3, 64)
@@ -109,13 +120,15 @@ def test_uniform_attention_closed_form():
 
 
 def test_quantized_forward_error_is_of_the_expected_size():
-    """8-bit operands change the result by roughly the E4M3 step (2^-4
-    relative) averaged over the contraction: far from exact, far from garbage."""
+    """8-bit operands change the result by about the E4M3 rounding error: its
+    relative step is 2^-3, so q, k, P and v each carry ~3 % RMS rounding error,
+    which add roughly in quadrature to ~5-6 % at the output. Bound: 8 %, far
+    from exact (quantization is on) and far from garbage (~100 %)."""
     B, heads, D, T, H, W, k = 1, 2, 128, 2, 8, 16, 2
     rs = np.random.RandomState(9)
     q, kk, v = (rs.randn(B, T * H * W, heads, D) for _ in range(3))
     out, lse = F.skiparse_fwd_fp8(q, kk, v, T, H, W, k, O.SINGLE)
     rout, rlse = O.skiparse_fwd(q, kk, v, T, H, W, k, O.SINGLE)
     rel = np.sqrt(np.sum((out - rout) ** 2) / np.sum(rout ** 2))
-    assert 1e-3 < rel < 5e-2
+    assert 1e-3 < rel < 8e-2
     assert np.max(np.abs(lse - rlse)) < 5e-2
