@@ -23,12 +23,15 @@ Readings taken here (the page gives the recipe for Hopper and no formulas):
   * attention runs per scope over blocks of 128 keys (scope order) with an
     online softmax in base 2: the running row max m (of S * scale * log2 e) is
     set by the first block and raised only when a later block's max exceeds it
-    by more than 8 (then O and l are rescaled by 2^(m_old - m_new)); this is
-    the fp32 kernel's lazy rescaling rule, needed here because P is quantized
-    against the running max, not the final one;
-  * P = 2^(S * scale * log2 e - m) is quantized as RNE_E4M3(P * 2^8) for O += P V
-    (fp32 cross-block accumulation), while the row sum l adds the unquantized P;
-  * out = O * s_v / (2^8 * l) (bf16 on the GPU), lse = (m + log2 l) * ln 2.
+    by more than 2 (then O and l are rescaled by 2^(m_old - m_new)), the lazy
+    rescaling of the fp32 kernel with a threshold of 2^2 instead of 2^8, so
+    that P = 2^(S * scale * log2 e - m) stays below 2^2;
+  * P is quantized as RNE_E4M3(P * 2^6) for O += P V (fp32 cross-block
+    accumulation): 2^2 * 2^6 = 256 < 448 keeps every code below saturation
+    (with the fp32 kernel's 2^8 threshold, P * 2^8 would saturate and the
+    error grows with the number of key blocks), while small P stay normal
+    down to 2^-12; the row sum l adds the unquantized P;
+  * out = O * s_v / (2^6 * l) (bf16 on the GPU), lse = (m + log2 l) * ln 2.
 
 Everything else is float64. Parity pins: tests/test_oracle_fp8.py.
 """
@@ -41,9 +44,9 @@ import numpy as np
 from . import skiparse_oracle as O
 
 E4M3_MAX = 448.0
-P_SCALE = 256.0
+P_SCALE = 64.0        # 2^6
 BLOCK = 128
-LAZY_LOG2 = 8.0
+LAZY_LOG2 = 2.0       # rescale when a block's row max exceeds the running max by more than 2^2
 
 
 def e4m3_values() -> np.ndarray:

@@ -99,8 +99,14 @@ def test_blocked_online_softmax_is_exact_without_quantization(mode, peaky):
     assert np.max(np.abs(lse - rlse)) < 1e-10
 
 
+def test_quantized_p_never_saturates():
+    """P is below 2^LAZY_LOG2 by the lazy rule, so its scaled codes stay below
+    E4M3's largest finite value."""
+    assert 2.0 ** F.LAZY_LOG2 * F.P_SCALE <= F.E4M3_MAX
+
+
 def test_uniform_attention_closed_form():
-    """q = 0: every score is 0, P = 1 is exact in E4M3 (P * 2^8 = 256), so each
+    """q = 0: every score is 0, P = 1 is exact in E4M3 (P * 2^6 = 64), so each
     output row is the mean over its scope of the dequantized v."""
     B, heads, D, T, H, W, k = 1, 1, 64, 2, 8, 16, 2
     N = T * H * W
