@@ -33,7 +33,12 @@ Readings taken here (the page gives the recipe for Hopper and no formulas):
     down to 2^-12; the row sum l adds the unquantized P;
   * out = O * s_v / (2^6 * l) (bf16 on the GPU), lse = (m + log2 l) * ln 2.
 
-Everything else is float64. Parity pins: tests/test_oracle_fp8.py.
+Where floating point decides a code, it is decided in the kernel's precision
+(float32): the values handed to the E4M3 rounding (q, k, v times 448 / max|x|,
+and P * 2^6 with P = 2^t, t = S * c - m + 6 formed as one float32 fused
+multiply-add and 2^t in float32) are float32 numbers; everything else
+(RoPE, the products, the sums, the rescaling, the output) is float64.
+Parity pins: tests/test_oracle_fp8.py.
 """
 from __future__ import annotations
 
@@ -86,11 +91,19 @@ def round_e4m3(x: np.ndarray) -> np.ndarray:
     return np.copysign(r, x)
 
 
+def _f32_codes(x: np.ndarray, amax: np.ndarray) -> np.ndarray:
+    """E4M3 codes of x * (448 / amax), the product formed in float32."""
+    x32 = np.asarray(x, dtype=np.float32)
+    a32 = np.asarray(amax, dtype=np.float32)
+    inv = np.where(a32 > 0, np.float32(E4M3_MAX) / np.where(a32 > 0, a32, np.float32(1)), np.float32(0))
+    return round_e4m3((x32 * inv.astype(np.float32)).astype(np.float64))
+
+
 def quantize_rows(x: np.ndarray):
     """Per-row E4M3 codes and scales over the last axis: x ~ codes * scale."""
-    amax = np.abs(x).max(axis=-1, keepdims=True)
-    safe = np.where(amax > 0, amax, E4M3_MAX)
-    codes = round_e4m3(x * (E4M3_MAX / safe))
+    x32 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    amax = np.abs(x32).max(axis=-1, keepdims=True)
+    codes = _f32_codes(x32, amax)
     scale = np.where(amax > 0, amax / E4M3_MAX, 1.0)
     return codes, scale[..., 0]
 
@@ -109,9 +122,9 @@ def quantize_blocks(x: np.ndarray, block: int = BLOCK):
 
 def quantize_channels(v: np.ndarray):
     """v (B, N, heads, D): per (b, head, channel) E4M3 codes and scales over N."""
-    amax = np.abs(v).max(axis=1, keepdims=True)                   # (B, 1, heads, D)
-    safe = np.where(amax > 0, amax, E4M3_MAX)
-    codes = round_e4m3(v * (E4M3_MAX / safe))
+    v32 = np.asarray(v, dtype=np.float32).astype(np.float64)
+    amax = np.abs(v32).max(axis=1, keepdims=True)                 # (B, 1, heads, D)
+    codes = _f32_codes(v32, amax)
     scale = np.where(amax > 0, amax / E4M3_MAX, 1.0)
     return codes, scale[:, 0]                                       # (B, heads, D)
 
@@ -122,7 +135,15 @@ def blocked_attention(sq, sk, q8, k8, v8, sv, scale, quantize_p=True):
     128 keys with the lazy rule; returns (out (L, D), lse (L,))."""
     L, D = q8.shape
     log2e = 1.0 / math.log(2.0)
-    S = (sq[:, None] * sk[None, :]) * (q8 @ k8.T) * scale * log2e     # (L, L), base-2 units
+    raw = q8 @ k8.T                                                  # exact: sums of E4M3 products
+    if quantize_p:
+        # per-row and per-block factor c = sq * sk * scale * log2 e and the scores
+        # in float32, as the kernel forms the values its codes are decided on
+        c = (np.float32(scale * log2e) * sq.astype(np.float32))[:, None] * sk.astype(np.float32)[None, :]
+        c = c.astype(np.float32).astype(np.float64)
+        S = raw.astype(np.float32).astype(np.float64) * c            # (L, L), base-2 units
+    else:
+        S = (sq[:, None] * sk[None, :]) * raw * scale * log2e
     m = np.zeros(L)
     l = np.zeros(L)
     acc = np.zeros((L, D))
@@ -138,9 +159,18 @@ def blocked_attention(sq, sk, q8, k8, v8, sv, scale, quantize_p=True):
             acc *= f[:, None]
             l *= f
             m = m_new
-        P = np.exp2(Sb - m[:, None])
-        l += P.sum(axis=1)
-        Pq = round_e4m3(P * P_SCALE) if quantize_p else P * P_SCALE
+        if quantize_p:
+            # 2^6 P = 2^t, t = S * c + (6 - m) as one float32 fused multiply-add, 2^t in float32
+            shift = (np.float32(math.log2(P_SCALE)) - m.astype(np.float32)).astype(np.float64)
+            t = (raw[:, j0:j0 + BLOCK].astype(np.float32).astype(np.float64) * c[:, j0:j0 + BLOCK]
+                 + shift[:, None]).astype(np.float32)
+            Ps = np.exp2(t).astype(np.float64)                       # 2^6 P
+            l += Ps.sum(axis=1) / P_SCALE
+            Pq = round_e4m3(Ps)
+        else:
+            P = np.exp2(Sb - m[:, None])
+            l += P.sum(axis=1)
+            Pq = P * P_SCALE
         acc += Pq @ v8[j0:j0 + BLOCK]
     out = acc * sv[None, :] / (P_SCALE * l[:, None])
     lse = (m + np.log2(l)) * math.log(2.0)

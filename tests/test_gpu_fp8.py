@@ -1,0 +1,98 @@
+"""GPU parity of the 8-bit forward pass (skiparse_attn_fwd_fp8) through the C
+ABI against the 8-bit oracle (oracle/skiparse_fp8_oracle.py), which applies the
+same quantization, deciding every E4M3 code on float32 values as the kernel
+does. The two differ by the final bf16 rounding and, rarely, by one code where
+a value lies within an ulp of a rounding midpoint, so the bf16 path's bars
+apply (out mean-abs 2e-3, relative RMS 1e-2, max-abs 2e-2 for all but one
+element in 10^4 and 0.1 for every element; LSE max-abs 1e-2). Against exact attention (the
+main oracle) the kernel's error must not exceed the 8-bit method's own (the
+oracle's) beyond bf16 rounding, and the method's error stays of the size E4M3
+operands give (relative RMS < 8 %; about 5 % on these inputs)."""
+import numpy as np
+import pytest
+
+from oracle import skiparse_fp8_oracle as F
+from oracle import skiparse_oracle as O
+from sparse_spatiotemporal_attention_gb300 import synthetic
+import skiparse_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_spatiotemporal_attention_gb300 as skp
+    assert torch.cuda.is_available()
+    return skp, torch.device("cuda:0")
+
+
+# (B, heads, T, H, W, k, mode); D = 128
+CASES = [
+    (1, 2, 3, 10, 10, 2, O.GROUP),      # L = 150: two tiles, ragged tail
+    (2, 2, 3, 20, 24, 4, O.SINGLE),     # L = 360: three tiles (odd: tile B of the last pair past the scope)
+    (1, 2, 2, 8, 16, 1, O.SINGLE),      # k = 1: dense, L = 256
+    (1, 1, 2, 16, 32, 8, O.GROUP),      # k = 8, L = 128
+    (1, 1, 8, 32, 32, 4, O.SINGLE),     # L = 2048, 16 tiles
+]
+
+
+def _ids(c):
+    B, h, T, H, W, k, m = c
+    return f"B{B}h{h}_{T}x{H}x{W}_k{k}_{'single' if m == O.SINGLE else 'group'}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_fp8_forward_parity(env, case):
+    import torch
+    skp, dev = env
+    B, heads, T, H, W, k, mode = case
+    D, N = 128, T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D)
+    q, kk, v = (tl.to_device(ins[n], dev) for n in ("q", "k", "v"))
+    obuf, out = tl.guarded_empty((B, N, heads, D), torch.bfloat16, dev)
+    lbuf, lse = tl.guarded_empty((B, heads, N), torch.float32, dev)
+    skp.skiparse_attn_fwd_fp8(q, kk, v, out, lse, T, H, W, k, mode)
+    torch.cuda.synchronize()
+    assert tl.guards_intact(obuf) and tl.guards_intact(lbuf), "8-bit forward wrote outside its outputs"
+    f = tl.f64_inputs(ins)
+    rout, rlse = F.skiparse_fwd_fp8(f["q"], f["k"], f["v"], T, H, W, k, mode)
+    got = tl.host(out)
+    # both sides decide every E4M3 code on float32 values, but sin / cos and 2^x
+    # are different float32 implementations on the two sides, so a value within
+    # an ulp of a rounding midpoint can take the neighbouring code: an isolated
+    # element may then miss the max-abs bar (one in 10^4 allowed, none past 0.1)
+    err = np.abs(got - rout)
+    assert np.all(np.isfinite(got))
+    assert err.mean() <= tl.TOL_MEAN, err.mean()
+    assert np.sqrt(np.sum(err ** 2) / np.sum(rout ** 2)) <= tl.TOL_RMS_REL
+    assert np.count_nonzero(err > tl.TOL_MAX) <= max(1, err.size // 10000), np.count_nonzero(err > tl.TOL_MAX)
+    assert err.max() <= 0.1, err.max()
+    tl.compare("lse", tl.host(lse), rlse, tol_max=tl.TOL_LSE, tol_mean=tl.TOL_LSE, tol_rel=1e-3)
+    # against exact attention the kernel adds nothing to the method's own error
+    eout, _ = O.skiparse_fwd(f["q"], f["k"], f["v"], T, H, W, k, mode)
+    rel_gpu = np.sqrt(np.sum((got - eout) ** 2) / np.sum(eout ** 2))
+    rel_method = np.sqrt(np.sum((rout - eout) ** 2) / np.sum(eout ** 2))
+    assert rel_gpu <= 1.05 * rel_method + 2e-3, (rel_gpu, rel_method)
+    assert rel_method < 0.08, rel_method
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
+
+
+def test_fp8_rejects_d64_and_small_workspace(env):
+    import torch
+    skp, dev = env
+    q = torch.zeros((1, 256, 2, 64), dtype=torch.bfloat16, device=dev)
+    out = torch.zeros_like(q)
+    lse = torch.zeros((1, 2, 256), dtype=torch.float32, device=dev)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    with pytest.raises(skp.SkiparseError) as e:
+        skp.skiparse_attn_fwd_fp8(q, q, q, out, lse, 4, 8, 8, 2, 0, workspace=ws)
+    assert e.value.status == -3
+    q = torch.zeros((1, 256, 2, 128), dtype=torch.bfloat16, device=dev)
+    out = torch.zeros_like(q)
+    with pytest.raises(skp.SkiparseError) as e:
+        skp.skiparse_attn_fwd_fp8(q, q, q, out, lse, 4, 8, 8, 2, 0, workspace=ws[:1024])
+    assert e.value.status == -6
