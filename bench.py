@@ -56,7 +56,7 @@ FWD_CONFIGS = [
     dict(name="skiparse_fwd_single_8x32x32_k4", B=1, heads=24, D=128, T=8, H=32, W=32, k=4, mode=0, k1=False),
     dict(name="skiparse_fwd_group_16x45x80_k4", B=1, heads=24, D=128, T=16, H=45, W=80, k=4, mode=1, k1=True),
 ]
-KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0, 4: 0.0}   # x forward FLOPs, per launch
+KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0, 4: 0.0, 5: 0.0, 6: 0.0, 7: 1.0}   # x forward FLOPs, per launch
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 

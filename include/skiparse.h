@@ -87,6 +87,25 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
+ * 8-bit forward pass (D = 128): the Wan 2.1 report, section 4.4.3
+ * "Quantization", paragraph "8-Bit FlashAttention", applied to this forward:
+ * E4M3 operands for S = Q K^T and O = P V with fp32 accumulation across key
+ * blocks. q is quantized after RoPE per (token, head) row, k per block of 128
+ * keys of a scope, v per (batch, head, channel); P enters O = P V as E4M3 of
+ * 2^8 P. Same arguments, layouts, outputs and errors as skiparse_attn_fwd,
+ * with its own workspace (skiparse_attn_fwd_fp8_workspace_bytes(...) bytes,
+ * 256-byte aligned, owned by the caller, contents undefined on return);
+ * SKIPARSE_ERR_UNSUPPORTED for D != 128. The outputs approximate the bf16
+ * forward to the accuracy of 8-bit operands (a few percent relative).
+ */
+size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
+                                             int sparse_k, int mode);
+int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes,
+                          int B, int heads, int N, int D, int T, int H, int W,
+                          int sparse_k, int mode, float rope_theta, cudaStream_t stream);
+
+/*
  * Bytes of device workspace skiparse_attn_bwd needs for these sizes: an fp32
  * dQ accumulator, rotated bf16 copies of q and k, per-scope fp32 LSE and
  * delta rows, and the RoPE cos/sin table. Returns 0 for empty or invalid sizes.
@@ -204,7 +223,7 @@ int skiparse_device_error(int* detail);
  * synchronises on them and writes, per kernel id, the summed device time in ms
  * and the launch count (arrays of n entries, host memory). Kernel ids:
  * 0 forward attention, 1 backward preprocess, 2 backward main, 3 backward
- * post, 4 forward RoPE.
+ * post, 4 forward RoPE, 5-7 8-bit forward (V channel max, quantization, attention).
  */
 int skiparse_trace_begin(void);
 int skiparse_trace_end(float* ms_per_kernel, int* launches_per_kernel, int n);

@@ -17,7 +17,8 @@ import os
 SINGLE = 0
 GROUP = 1
 KERNEL_NAMES = ("skiparse_fwd_kernel", "skiparse_bwd_pre_kernel", "skiparse_bwd_main_kernel",
-                "skiparse_bwd_post_kernel", "skiparse_fwd_rope_kernel")
+                "skiparse_bwd_post_kernel", "skiparse_fwd_rope_kernel", "skiparse_fwd8_vmax_kernel",
+                "skiparse_fwd8_prep_kernel", "skiparse_fwd8_kernel")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libskiparse.so")
@@ -27,6 +28,7 @@ EXPORTS = (
     "skiparse_debug_index_map", "skiparse_debug_rope", "skiparse_status_string",
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
     "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout", "skiparse_attn_bwd_saved",
+    "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8",
 )
 
 
@@ -65,6 +67,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_kernel_name": (ctypes.c_char_p, [_c_int]),
         "skiparse_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_debug_wait_timeout": (_c_int, [_c_int, _vp]),
+        "skiparse_attn_fwd_fp8_workspace_bytes": (_c_size, [_c_int] * 9),
+        "skiparse_attn_fwd_fp8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_bwd_saved": (_c_int, [_vp, _c_size] + [_vp] * 8 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
     }
     for name, (res, args) in sig.items():
@@ -130,6 +134,27 @@ def skiparse_attn_fwd(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=100
                                           B, heads, N, D, T, H, W, sparse_k, mode,
                                           float(rope_theta), _stream(stream))
     _check(st, "skiparse_attn_fwd")
+
+
+def skiparse_attn_fwd_fp8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode) -> int:
+    return int(load_library().skiparse_attn_fwd_fp8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode))
+
+
+def skiparse_attn_fwd_fp8(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=10000.0, stream=None,
+                          workspace=None, workspace_bytes=None):
+    """8-bit forward pass (D = 128) into caller-allocated out and lse; `workspace`
+    as for skiparse_attn_fwd, sized by skiparse_attn_fwd_fp8_workspace_bytes(...)."""
+    B, heads, N, D = _shape(q)
+    if workspace is None:
+        import torch
+        nbytes = skiparse_attn_fwd_fp8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = load_library().skiparse_attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
+                                              int(workspace_bytes), B, heads, N, D, T, H, W, sparse_k, mode,
+                                              float(rope_theta), _stream(stream))
+    _check(st, "skiparse_attn_fwd_fp8")
 
 
 def skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode) -> int:
@@ -211,7 +236,7 @@ def skiparse_trace_begin():
     _check(load_library().skiparse_trace_begin(), "skiparse_trace_begin")
 
 
-def skiparse_trace_end(n: int = 5):
+def skiparse_trace_end(n: int = len(KERNEL_NAMES)):
     """Returns ([ms per kernel id], [launches per kernel id])."""
     ms = (_c_float * n)()
     cnt = (_c_int * n)()

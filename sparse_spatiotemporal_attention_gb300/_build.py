@@ -20,8 +20,8 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libskiparse.so")
 SYNTH_SRC = os.path.join(CSRC, "synthetic_gen.c")
 SYNTH_LIB = os.path.join(LIBDIR, "libsynthetic.so")
-SOURCES = ["skiparse_host.cu", "skiparse_fwd.cu", "skiparse_bwd.cu", "skiparse_bwd_rows.cu", "skiparse_debug.cu",
-           "skiparse_noalloc.cu"]
+SOURCES = ["skiparse_host.cu", "skiparse_fwd.cu", "skiparse_fwd8.cu", "skiparse_bwd.cu", "skiparse_bwd_rows.cu",
+           "skiparse_debug.cu", "skiparse_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,536 @@
+// Skiparse attention forward with 8-bit operands: the Wan 2.1 report, section 4
+// "Model Design and Acceleration", 4.4.3 "Quantization", paragraph "8-Bit
+// FlashAttention" (8-bit operands for S = Q K^T and O = P V, fp32 accumulation
+// across key blocks), applied to the Skiparse forward pass of "Open-Sora Plan"
+// docs, "Skiparse Attention". D = 128.
+//
+// Quantization (readings, the page gives the recipe for Hopper):
+//   * E4M3 for both products (the page's INT8 for Q K^T is not a fast tensor
+//     path here); q after RoPE per (token, head) row, k after RoPE per block of
+//     128 consecutive keys of a scope (one scale per K tile), v per (batch,
+//     head, channel) over all tokens; scale = max|x| / 448, codes
+//     RNE(x * 448 / max|x|);
+//   * P = 2^(S * scale * log2 e - m) enters O = P V as RNE_E4M3(2^6 P); the row
+//     sum adds the unquantized P; O accumulates in fp32 TMEM across K tiles;
+//   * online softmax with lazy rescaling only when a K tile's row max exceeds
+//     the running max by more than 2^2 (2^8 in the fp32 kernel): P < 2^2 then,
+//     so 2^6 P < 256 never saturates E4M3 (448).
+//
+// Kernels:
+//   skiparse_fwd8_vmax_kernel   max |v| per (b, head, channel) (atomicMax on the
+//                               bits of non-negative floats into a zeroed array);
+//   skiparse_fwd8_prep_kernel   one CTA per (scope, 128-position tile): RoPE and
+//                               quantize q (per row) and k (per tile), quantize v
+//                               and transpose it, all in scope-tile order, so the
+//                               attention kernel reads plain 128 x 128-byte boxes
+//                               (every 8-bit operand K-major);
+//   skiparse_fwd8_kernel        the forward kernel's structure (two Q tiles per
+//                               CTA, softmax warps 0-7, TMA warp 8, MMA warp 9)
+//                               with kind::f8f6f4 MMAs: 4 per 128 x 128 product
+//                               instead of 8, P stored as E4M3 over S (32 TMEM
+//                               columns per tile).
+#include "skiparse_internal.h"
+
+namespace skp {
+
+namespace {
+
+constexpr int kD8 = 128;
+constexpr int kF8Threads = 320;
+constexpr int kPrepThreads = 256;
+constexpr float kE4M3Max = 448.0f;
+
+struct F8Layout {
+  static constexpr int TILE = 128 * 128;          // 16 KB: 128 rows x 128 bytes, one 128-byte swizzled box
+  static constexpr int HDR = 1024;
+  static constexpr int QA_OFF = HDR;
+  static constexpr int QB_OFF = QA_OFF + TILE;
+  static constexpr int K_OFF = QB_OFF + TILE;
+  static constexpr int V_OFF = K_OFF + 2 * TILE;
+  static constexpr int BYTES = V_OFF + 2 * TILE;
+};
+
+enum F8Bar {
+  E_QFULL, E_QEMPTY,
+  E_KFULL0, E_KFULL1, E_KEMPTY0, E_KEMPTY1,
+  E_VFULL0, E_VFULL1, E_VEMPTY0, E_VEMPTY1,
+  E_SFULL_A, E_SFULL_B, E_PFULL_A, E_PFULL_B, E_ODONE_A, E_ODONE_B, E_OEMPTY_A, E_OEMPTY_B, E_FINAL, E_NBARS
+};
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// max |v| per (b, head, channel): grid (token chunks of 256, B * heads)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) skiparse_fwd8_vmax_kernel(const __grid_constant__ Fwd8Params p) {
+  __shared__ float part[4][kD8];
+  const Geom& g = p.g;
+  const int bh = blockIdx.y;
+  const int b = bh / g.heads, head = bh - b * g.heads;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * 256;
+  const int t1 = min(t0 + 256, g.N);
+  float mx[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = t0 + warp; i < t1; i += 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p.v + (((size_t)b * g.N + i) * g.heads + head) * kD8 + lane * 4);
+    mx[0] = fmaxf(mx[0], fabsf(bf16lo(u.x)));
+    mx[1] = fmaxf(mx[1], fabsf(bf16hi(u.x)));
+    mx[2] = fmaxf(mx[2], fabsf(bf16lo(u.y)));
+    mx[3] = fmaxf(mx[3], fabsf(bf16hi(u.y)));
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) part[warp][lane * 4 + e] = mx[e];
+  __syncthreads();
+  const int d = threadIdx.x;
+  const float m = fmaxf(fmaxf(part[0][d], part[1][d]), fmaxf(part[2][d], part[3][d]));
+  atomicMax(p.vmax + (size_t)bh * kD8 + d, __float_as_uint(m));   // non-negative floats order as their bits
+}
+
+// ---------------------------------------------------------------------------
+// prep: one CTA per (scope index sidx = (b * heads + head) * k + s, 128-position tile)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPrepThreads) skiparse_fwd8_prep_kernel(const __grid_constant__ Fwd8Params p) {
+  extern __shared__ __align__(16) uint8_t psm[];
+  float2* tab = reinterpret_cast<float2*>(psm);                                     // RoPE table
+  float* kbuf = reinterpret_cast<float*>(psm + p.rope.entries * sizeof(float2));    // 128 x 128 rotated k
+  float* rowmax = kbuf + 128 * kD8;                                                 // 128
+  uint8_t* vt = reinterpret_cast<uint8_t*>(rowmax + 128);                           // 128 channels x 132 bytes
+  constexpr int VT_STRIDE = 132;
+  const Geom& g = p.g;
+  const int tile = blockIdx.x % g.n_tiles;
+  const int sidx = blockIdx.x / g.n_tiles;
+  const int s = sidx % g.k;
+  const int bh = sidx / g.k;
+  const int b = bh / g.heads, head = bh - b * g.heads;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  __syncthreads();
+  PairSel sel[2];
+  sel[0] = pair_select(p.rope, lane * 2);
+  sel[1] = pair_select(p.rope, lane * 2 + 1);
+  float inv_v[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float m = __uint_as_float(p.vmax[(size_t)bh * kD8 + lane * 4 + e]);
+    inv_v[e] = m > 0.f ? kE4M3Max / m : 0.f;
+  }
+  float kmax = 0.f;
+  for (int r = warp; r < 128; r += 8) {
+    const int pos = tile * kTile + r;
+    const size_t slot = (size_t)sidx * p.Lp + pos;          // scope-order row
+    uint32_t qc = 0, vc = 0;
+    float sq = 0.f;
+    float kr[4] = {0.f, 0.f, 0.f, 0.f};
+    if (pos < g.L) {
+      const int i = token_of(g, s, pos);
+      int t, hh, w;
+      token_coords(p.rope, i, t, hh, w);
+      const size_t base = (((size_t)b * g.N + i) * g.heads + head) * kD8 + lane * 4;
+      const uint2 qu = *reinterpret_cast<const uint2*>(p.q + base);
+      const uint2 ku = *reinterpret_cast<const uint2*>(p.k + base);
+      const uint2 vu = *reinterpret_cast<const uint2*>(p.v + base);
+      float qr[4];
+      const float2 c0 = tab[pair_index(sel[0], t, hh, w)];
+      const float2 c1 = tab[pair_index(sel[1], t, hh, w)];
+      float2 a = rope_rotate(bf16lo(qu.x), bf16hi(qu.x), c0);
+      float2 bq = rope_rotate(bf16lo(qu.y), bf16hi(qu.y), c1);
+      qr[0] = a.x; qr[1] = a.y; qr[2] = bq.x; qr[3] = bq.y;
+      a = rope_rotate(bf16lo(ku.x), bf16hi(ku.x), c0);
+      bq = rope_rotate(bf16lo(ku.y), bf16hi(ku.y), c1);
+      kr[0] = a.x; kr[1] = a.y; kr[2] = bq.x; kr[3] = bq.y;
+      // q: per-row scale
+      float qm = fmaxf(fmaxf(fabsf(qr[0]), fabsf(qr[1])), fmaxf(fabsf(qr[2]), fabsf(qr[3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+      const float qi = qm > 0.f ? kE4M3Max / qm : 0.f;
+      qc = e4m3x4(qr[0] * qi, qr[1] * qi, qr[2] * qi, qr[3] * qi);
+      sq = qm > 0.f ? qm / kE4M3Max : 1.f;
+      vc = e4m3x4(bf16lo(vu.x) * inv_v[0], bf16hi(vu.x) * inv_v[1], bf16lo(vu.y) * inv_v[2], bf16hi(vu.y) * inv_v[3]);
+      kmax = fmaxf(kmax, fmaxf(fmaxf(fabsf(kr[0]), fabsf(kr[1])), fmaxf(fabsf(kr[2]), fabsf(kr[3]))));
+    }
+    *reinterpret_cast<uint32_t*>(p.q8 + slot * kD8 + lane * 4) = qc;
+    if (lane == 0) p.sq[slot] = sq;
+    *reinterpret_cast<float4*>(kbuf + r * kD8 + lane * 4) = make_float4(kr[0], kr[1], kr[2], kr[3]);
+    // v transposed: channel-major rows of 128 positions (padded stride against bank conflicts)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) vt[(lane * 4 + e) * VT_STRIDE + r] = (uint8_t)(vc >> (8 * e));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  if (lane == 0) rowmax[warp] = kmax;
+  __syncthreads();
+  float tmax = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tmax = fmaxf(tmax, rowmax[w]);
+  const float ki = tmax > 0.f ? kE4M3Max / tmax : 0.f;
+  if (threadIdx.x == 0) p.sk[(size_t)sidx * g.n_tiles + tile] = tmax > 0.f ? tmax / kE4M3Max : 1.f;
+  for (int r = warp; r < 128; r += 8) {
+    const float4 x = *reinterpret_cast<const float4*>(kbuf + r * kD8 + lane * 4);
+    const size_t slot = (size_t)sidx * p.Lp + tile * kTile + r;
+    *reinterpret_cast<uint32_t*>(p.k8 + slot * kD8 + lane * 4) = e4m3x4(x.x * ki, x.y * ki, x.z * ki, x.w * ki);
+  }
+  // V^T rows: channel d of this tile's 128 positions, 4 bytes per thread per step
+  for (int idx = threadIdx.x; idx < kD8 * 32; idx += blockDim.x) {
+    const int d = idx >> 5, c = idx & 31;
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(vt + d * VT_STRIDE + c * 4);
+    *reinterpret_cast<uint32_t*>(p.vt8 + ((size_t)sidx * kD8 + d) * p.Lp + tile * kTile + c * 4) = word;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// attention over 8-bit operands
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __grid_constant__ Fwd8Params p) {
+  using Ly = F8Layout;
+  constexpr int D = kD8;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
+  int* abort_flag = reinterpret_cast<int*>(smem + 520);
+  const uint32_t sQA = smem_u32(smem + Ly::QA_OFF);
+  const uint32_t sQB = smem_u32(smem + Ly::QB_OFF);
+  const uint32_t sK = smem_u32(smem + Ly::K_OFF);
+  const uint32_t sV = smem_u32(smem + Ly::V_OFF);
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  const Ctl ctl{abort_flag, p.err};
+  const Geom& g = p.g;
+  const int n_pairs = (g.n_tiles + 1) >> 1;
+  constexpr int E = ERR_KERNEL_FWD + 0x80;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    const uint32_t counts[E_NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 4, 4, 1};
+    for (int i = 0; i < E_NBARS; ++i) mbar_init(bar(i), counts[i]);
+    mbar_fence_init();
+  }
+  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto warp_wait = [&](int i, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ctl, E + i)) != 0;
+  };
+  const bool leader = lane == 0;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (leader) {
+      tma_prefetch_map(&p.tm_q8);
+      tma_prefetch_map(&p.tm_k8);
+      tma_prefetch_map(&p.tm_vt);
+    }
+    uint32_t q_issued = 0, k_issued[2] = {0, 0}, v_issued[2] = {0, 0};
+    uint32_t gk = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      const int pair = u % n_pairs, sidx = u / n_pairs;
+      if (it > 0 && !warp_wait(E_QEMPTY, (it - 1) & 1)) break;
+      if (leader) {
+        mbar_expect_tx(bar(E_QFULL), 2 * Ly::TILE);
+        tma_load_3d(sQA, &p.tm_q8, bar(E_QFULL), 0, 2 * pair * kTile, sidx);
+        tma_load_3d(sQB, &p.tm_q8, bar(E_QFULL), 0, (2 * pair + 1) * kTile, sidx);
+      }
+      __syncwarp();
+      ++q_issued;
+      for (int j = 0; j < g.n_tiles; ++j) {
+        const uint32_t gg = gk + j;
+        const int st = gg & 1;
+        const uint32_t n = gg >> 1;
+        if (n > 0 && !warp_wait(E_KEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
+        if (leader) {
+          mbar_expect_tx(bar(E_KFULL0 + st), Ly::TILE);
+          tma_load_3d(sK + st * Ly::TILE, &p.tm_k8, bar(E_KFULL0 + st), 0, j * kTile, sidx);
+        }
+        __syncwarp();
+        ++k_issued[st];
+        if (n > 0 && !warp_wait(E_VEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
+        if (leader) {
+          mbar_expect_tx(bar(E_VFULL0 + st), Ly::TILE);
+          tma_load_3d(sV + st * Ly::TILE, &p.tm_vt, bar(E_VFULL0 + st), j * kTile, 0, sidx);
+        }
+        __syncwarp();
+        ++v_issued[st];
+      }
+      gk += g.n_tiles;
+    }
+    if (leader) {
+      if (q_issued) mbar_drain(bar(E_QFULL), (q_issued - 1) & 1);
+      for (int st = 0; st < 2; ++st) {
+        if (k_issued[st]) mbar_drain(bar(E_KFULL0 + st), (k_issued[st] - 1) & 1);
+        if (v_issued[st]) mbar_drain(bar(E_VFULL0 + st), (v_issued[st] - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kId = idesc_e4m3(128, 128);
+    const uint64_t dQA = desc_kmajor(sQA, 0), dQB = desc_kmajor(sQB, 0);
+    const uint64_t dK0 = desc_kmajor(sK, 0), dK1 = desc_kmajor(sK + Ly::TILE, 0);
+    const uint64_t dV0 = desc_kmajor(sV, 0), dV1 = desc_kmajor(sV + Ly::TILE, 0);
+    // S_X = Q_X K_g^T (4 k-steps of 32 bytes)
+    auto issue_s = [&](uint64_t dq, uint32_t colS, int st) {
+      const uint64_t dk = st ? dK1 : dK0;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) mma8_ss(tmem + colS, kmajor_step(dq, ks), kmajor_step(dk, ks), kId, ks > 0 ? 1u : 0u);
+    };
+    // O_X += P_X V_g: P_X as E4M3 in TMEM columns colS .. colS+31, V^T K-major
+    auto issue_pv = [&](uint32_t colS, uint32_t colO, int st, bool first) {
+      const uint64_t dv = st ? dV1 : dV0;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma8_ts(tmem + colO, tmem + colS + ks * 8, kmajor_step(dv, ks), kId, (!first || ks > 0) ? 1u : 0u);
+    };
+    uint32_t g0 = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      const int n = g.n_tiles;
+      if (!warp_wait(E_QFULL, it & 1)) break;
+      if (!warp_wait(E_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
+      tc_fence_after();
+      if (leader) {
+        issue_s(dQA, 0, g0 & 1);
+        tc_commit(bar(E_SFULL_A));
+        issue_s(dQB, 128, g0 & 1);
+        tc_commit(bar(E_SFULL_B));
+        tc_commit(bar(E_KEMPTY0 + (g0 & 1)));
+        if (n == 1) tc_commit(bar(E_QEMPTY));
+      }
+      __syncwarp();
+      for (int j = 0; j < n; ++j) {
+        const uint32_t gg = g0 + j;
+        const int st = gg & 1;
+        const uint32_t nn = gg >> 1;
+        if (j == 0 && it > 0 && !warp_wait(E_OEMPTY_A, (it - 1) & 1)) { ok = false; break; }
+        if (!warp_wait(E_PFULL_A, gg & 1)) { ok = false; break; }
+        if (!warp_wait(E_VFULL0 + st, nn & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
+          issue_pv(0, 256, st, j == 0);
+          tc_commit(bar(E_ODONE_A));
+        }
+        __syncwarp();
+        const bool more = j + 1 < n;
+        if (more) {
+          const int st1 = (gg + 1) & 1;
+          if (!warp_wait(E_KFULL0 + st1, ((gg + 1) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          if (leader) {
+            issue_s(dQA, 0, st1);
+            tc_commit(bar(E_SFULL_A));
+          }
+          __syncwarp();
+        }
+        if (j == 0 && it > 0 && !warp_wait(E_OEMPTY_B, (it - 1) & 1)) { ok = false; break; }
+        if (!warp_wait(E_PFULL_B, gg & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
+          issue_pv(128, 256 + D, st, j == 0);
+          tc_commit(bar(E_ODONE_B));
+          tc_commit(bar(E_VEMPTY0 + st));
+          if (more) {
+            const int st1 = (gg + 1) & 1;
+            issue_s(dQB, 128, st1);
+            tc_commit(bar(E_SFULL_B));
+            tc_commit(bar(E_KEMPTY0 + st1));
+            if (j + 2 == n) tc_commit(bar(E_QEMPTY));
+          }
+        }
+        __syncwarp();
+      }
+      g0 += n;
+    }
+    if (leader) {
+      tc_commit(bar(E_FINAL));
+      mbar_drain(bar(E_FINAL), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps (A: 0-3, B: 4-7)
+    const int wg = warp >> 2;
+    const int r = tid & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t colS = wg ? 128u : 0u;
+    const uint32_t colO = 256u + (wg ? (uint32_t)D : 0u);
+    const int barS = wg ? E_SFULL_B : E_SFULL_A;
+    const int barP = wg ? E_PFULL_B : E_PFULL_A;
+    const int barO = wg ? E_ODONE_B : E_ODONE_A;
+    const int barOE = wg ? E_OEMPTY_B : E_OEMPTY_A;
+    uint32_t g0 = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      const int pair = u % n_pairs, sidx = u / n_pairs;
+      const int tile = 2 * pair + wg;
+      const int prow = tile * kTile + r;
+      // scaled score in log2 units = S * sq_row * sk_tile * scale * log2 e
+      // (tile B of a scope with an odd tile count lies past Lp: zero rows, no scale)
+      const float crow = prow < p.Lp ? p.sq[(size_t)sidx * p.Lp + prow] * p.scale_log2 : 0.f;
+      const float* skt = p.sk + (size_t)sidx * g.n_tiles;
+      float m = 0.f, l = 0.f;          // l in units of 2^6 P
+      for (int j = 0; j < g.n_tiles; ++j) {
+        const uint32_t gg = g0 + j;
+        const float ck = crow * __ldg(skt + j);
+        if (!mbar_wait(bar(barS), gg & 1, ctl, E + barS)) { ok = false; break; }
+        tc_fence_after();
+        const int valid = min(kTile, g.L - j * kTile);
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tmem_ld32(tmem + lane_base + colS + c * 32, x);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], (c * 32 + e < valid) ? x[e] : -INFINITY);
+        }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * ck;
+        if (j == 0) {
+          m = mx;
+        } else {
+          const bool need = mx > m + 2.0f;
+          if (__any_sync(0xffffffffu, need)) {
+            if (!mbar_wait(bar(barO), (gg - 1) & 1, ctl, E + barO)) { ok = false; break; }
+            tc_fence_after();
+            const float m_new = need ? mx : m;
+            const float f = ex2(m - m_new);
+            m = m_new;
+            l *= f;
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              float o[16];
+              tmem_ld16(tmem + lane_base + colO + c * 16, o);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] *= f;
+              tmem_st16f(tmem + lane_base + colO + c * 16, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        // 2^6 P = 2^(S * ck - m + 6) as E4M3 over the S columns already read:
+        // keys 32c .. 32c+31 -> columns colS + 8c .. +7 (four codes per column)
+        const unsigned long long ck2 = f2_pack(ck, ck);
+        const unsigned long long off2 = f2_pack(6.0f - m, 6.0f - m);
+        unsigned long long acc2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          tmem_ld32(tmem + lane_base + colS + c * 32, x);
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float t0, t1, t2, t3;
+            f2_unpack(ffma2(f2_pack(x[4 * e], x[4 * e + 1]), ck2, off2), t0, t1);
+            f2_unpack(ffma2(f2_pack(x[4 * e + 2], x[4 * e + 3]), ck2, off2), t2, t3);
+            float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+            if (valid < kTile) {
+              const int k0 = c * 32 + 4 * e;
+              p0 = k0 < valid ? p0 : 0.f;
+              p1 = k0 + 1 < valid ? p1 : 0.f;
+              p2 = k0 + 2 < valid ? p2 : 0.f;
+              p3 = k0 + 3 < valid ? p3 : 0.f;
+            }
+            acc2[e & 1] = fadd2(acc2[e & 1], f2_pack(p0 + p2, p1 + p3));
+            pk[e] = e4m3x4(p0, p1, p2, p3);
+          }
+          tmem_st8(tmem + lane_base + colS + c * 8, pk);
+        }
+        {
+          float s0, s1, s2, s3;
+          f2_unpack(acc2[0], s0, s1);
+          f2_unpack(acc2[1], s2, s3);
+          l += (s0 + s1) + (s2 + s3);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(barP));
+      }
+      if (!ok) break;
+      // ---- epilogue: out = O * s_v / l (l and O both in units of 2^6 P); LSE natural log
+      const uint32_t glast = g0 + g.n_tiles - 1;
+      if (!mbar_wait(bar(barO), glast & 1, ctl, E + barO)) break;
+      tc_fence_after();
+      const int s = sidx % g.k, bh = sidx / g.k;
+      const int b = bh / g.heads, head = bh - b * g.heads;
+      const bool row_ok = prow < g.L;
+      const int tok = row_ok ? token_of(g, s, prow) : 0;
+      const float inv_l = 1.0f / (l * kE4M3Max);
+      const unsigned* vm = p.vmax + (size_t)bh * D;
+      uint16_t* orow = p.out + (((size_t)b * g.N + tok) * g.heads + head) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + colO + c * 32, o);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = o[8 * q4 + e] * (__uint_as_float(__ldg(vm + c * 32 + 8 * q4 + e)) * inv_l);
+            uint4 w;
+            w.x = pack_bf16(y[0], y[1]);
+            w.y = pack_bf16(y[2], y[3]);
+            w.z = pack_bf16(y[4], y[5]);
+            w.w = pack_bf16(y[6], y[7]);
+            dst[q4] = w;
+          }
+        }
+      }
+      if (row_ok) p.lse[((size_t)b * g.heads + head) * g.N + tok] = (m + log2f(l) - 6.0f) * 0.6931471805599453f;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(barOE));
+      g0 += g.n_tiles;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+size_t fwd8_smem_bytes() { return F8Layout::BYTES; }
+
+size_t fwd8_prep_smem_bytes(int rope_entries) {
+  return (size_t)rope_entries * sizeof(float2) + (size_t)128 * kD8 * 4 + 128 * 4 + (size_t)kD8 * 132;
+}
+
+int fwd8_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 2); }
+
+cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream) {
+  const dim3 grid((p.g.N + 255) / 256, p.g.B * p.g.heads);
+  skiparse_fwd8_vmax_kernel<<<grid, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd8_prep(const Fwd8Params& p, cudaStream_t stream) {
+  const size_t smem = fwd8_prep_smem_bytes(p.rope.entries);
+  cudaError_t e = cudaFuncSetAttribute(skiparse_fwd8_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = p.g.B * p.g.heads * p.g.k * p.g.n_tiles;
+  skiparse_fwd8_prep_kernel<<<grid, kPrepThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd8(const Fwd8Params& p, int grid, cudaStream_t stream) {
+  const size_t smem = fwd8_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(skiparse_fwd8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  skiparse_fwd8_kernel<<<grid, kF8Threads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace skp

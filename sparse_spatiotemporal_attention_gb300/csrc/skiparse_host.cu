@@ -237,6 +237,46 @@ bool encode_scope_map(CUtensorMap* m, const void* base, const Geom& g) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// 3-D byte tensor map, 128 x 128-byte boxes with 128-byte swizzle: dims
+// (d0 innermost, d1, d2), byte strides s1, s2.
+bool encode_bytes_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                     uint64_t s2) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 8-bit forward workspace: E4M3 q, k (scopes, Lp, 128) and V^T (scopes, 128, Lp),
+// q scales per scope-order row, k scales per K tile, max |v| per (b, head, channel).
+struct Ws8Layout {
+  size_t q8, k8, vt8, sq, sk, vmax, total;
+  int Lp, scopes;
+};
+
+Ws8Layout ws8_layout(const Shape& s) {
+  Ws8Layout w;
+  const int L = s.N / s.k;
+  w.Lp = ((L + kTile - 1) / kTile) * kTile;
+  w.scopes = s.B * s.heads * s.k;
+  const size_t rows = (size_t)w.scopes * w.Lp;
+  size_t off = 0;
+  w.q8 = off;   off += align256(rows * 128);
+  w.k8 = off;   off += align256(rows * 128);
+  w.vt8 = off;  off += align256(rows * 128);
+  w.sq = off;   off += align256(rows * 4);
+  w.sk = off;   off += align256((size_t)w.scopes * (w.Lp / kTile) * 4);
+  w.vmax = off; off += align256((size_t)s.B * s.heads * 128 * 4);
+  w.total = off;
+  return w;
+}
+
 struct WsLayout {
   size_t dq_acc, qr, kr, lse2s, delta_s, tab, total;
   int Lp;
@@ -298,6 +338,9 @@ const char* skiparse_kernel_name(int id) {
     case 2: return "skiparse_bwd_main_kernel";
     case 3: return "skiparse_bwd_post_kernel";
     case 4: return "skiparse_fwd_rope_kernel";
+    case 5: return "skiparse_fwd8_vmax_kernel";
+    case 6: return "skiparse_fwd8_prep_kernel";
+    case 7: return "skiparse_fwd8_kernel";
     default: return "unknown";
   }
 }
@@ -351,6 +394,67 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, dev.sms, stream); }));
   if (st != SKIPARSE_OK) return st;
   return launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));
+}
+
+size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k,
+                                             int mode) {
+  Shape s;
+  if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty || D != 128) return 0;
+  return ws8_layout(s).total;
+}
+
+int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes,
+                          int B, int heads, int N, int D, int T, int H, int W,
+                          int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+  Shape s;
+  int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
+  if (st != SKIPARSE_OK || s.empty) return st;
+  if (D != 128) return SKIPARSE_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
+  const Ws8Layout w = ws8_layout(s);
+  if (!workspace || workspace_bytes < w.total) return SKIPARSE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
+  const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
+  if (any_alias({{out, tb}, {lse, lb}, {workspace, w.total}}, {{q, tb}, {k, tb}, {v, tb}})) return SKIPARSE_ERR_ALIAS;
+  DeviceInfo dev;
+  if ((st = device_info(dev)) != SKIPARSE_OK) return st;
+  if ((size_t)dev.smem_optin < fwd8_smem_bytes() || (size_t)dev.smem_optin < fwd8_prep_smem_bytes(s.rope_entries))
+    return SKIPARSE_ERR_UNSUPPORTED;
+
+  Fwd8Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = make_geom(s);
+  p.rope = make_rope(s, rope_theta);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.q8 = ws + w.q8;
+  p.k8 = ws + w.k8;
+  p.vt8 = ws + w.vt8;
+  p.sq = reinterpret_cast<float*>(ws + w.sq);
+  p.sk = reinterpret_cast<float*>(ws + w.sk);
+  p.vmax = reinterpret_cast<unsigned*>(ws + w.vmax);
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.err = dev.err_word;
+  p.Lp = w.Lp;
+  p.n_units = fwd8_units(p.g);
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  const uint64_t Lp = (uint64_t)w.Lp, sc = (uint64_t)w.scopes;
+  if (!encode_bytes_3d(&p.tm_q8, p.q8, 128, Lp, sc, 128, 128 * Lp) ||
+      !encode_bytes_3d(&p.tm_k8, p.k8, 128, Lp, sc, 128, 128 * Lp) ||
+      !encode_bytes_3d(&p.tm_vt, p.vt8, Lp, 128, sc, Lp, 128 * Lp))
+    return SKIPARSE_ERR_LAUNCH;
+  const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
+  if (cudaMemsetAsync(p.vmax, 0, (size_t)B * heads * 128 * 4, stream) != cudaSuccess) return launch_status(cudaErrorUnknown);
+  st = launch_status(traced_launch(5, stream, [&] { return launch_fwd8_vmax(p, stream); }));
+  if (st != SKIPARSE_OK) return st;
+  st = launch_status(traced_launch(6, stream, [&] { return launch_fwd8_prep(p, stream); }));
+  if (st != SKIPARSE_OK) return st;
+  return launch_status(traced_launch(7, stream, [&] { return launch_fwd8(p, grid, stream); }));
 }
 
 size_t skiparse_attn_bwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode) {

@@ -60,6 +60,28 @@ struct BwdParams {
   float scale_log2;        // log2(e) / sqrt(D)
 };
 
+struct Fwd8Params {
+  CUtensorMap tm_q8, tm_k8;       // 8-bit q / k, scope-tile order: (128 bytes, Lp rows, scopes), 128 x 128 boxes
+  CUtensorMap tm_vt;              // 8-bit V^T per scope: (Lp keys, 128 channels, scopes), 128 x 128 boxes
+  Geom g;
+  RopeParams rope;
+  const uint16_t* q;              // bf16 (B, N, heads, D) inputs
+  const uint16_t* k;
+  const uint16_t* v;
+  uint8_t* q8;                    // workspace: E4M3 codes (scopes, Lp, 128), scope order
+  uint8_t* k8;
+  uint8_t* vt8;                   // workspace: E4M3 V^T (scopes, 128, Lp)
+  float* sq;                      // workspace: q scale per scope-order row (scopes, Lp)
+  float* sk;                      // workspace: k scale per K tile (scopes, n_tiles)
+  unsigned* vmax;                 // workspace: max |v| per (b, head, channel) as float bits
+  uint16_t* out;                  // bf16 (B, N, heads, D)
+  float* lse;                     // (B, heads, N)
+  int* err;
+  int n_units;                    // scopes * ceil(n_tiles / 2)
+  int Lp;                         // L rounded up to a multiple of 128
+  float scale_log2;               // log2(e) / sqrt(D)
+};
+
 struct DebugParams {
   Geom g;
   RopeParams rope;
@@ -88,6 +110,13 @@ size_t fwd_rope_smem_bytes(int rope_entries);
 int fwd_units(const Geom& g);
 cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
+
+size_t fwd8_smem_bytes();
+size_t fwd8_prep_smem_bytes(int rope_entries);
+int fwd8_units(const Geom& g);
+cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream);
+cudaError_t launch_fwd8_prep(const Fwd8Params& p, cudaStream_t stream);
+cudaError_t launch_fwd8(const Fwd8Params& p, int grid, cudaStream_t stream);
 
 size_t bwd_main_smem_bytes(int D);
 bool bwd_uses_tile_kernel(int D);
