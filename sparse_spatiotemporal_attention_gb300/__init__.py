@@ -28,7 +28,7 @@ EXPORTS = (
     "skiparse_debug_index_map", "skiparse_debug_rope", "skiparse_status_string",
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
     "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout", "skiparse_attn_bwd_saved",
-    "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8",
+    "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8", "skiparse_debug_exp2",
 )
 
 
@@ -67,6 +67,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_kernel_name": (ctypes.c_char_p, [_c_int]),
         "skiparse_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_debug_wait_timeout": (_c_int, [_c_int, _vp]),
+        "skiparse_debug_exp2": (_c_int, [_vp, _vp, _c_int, _c_int, _vp]),
         "skiparse_attn_fwd_fp8_workspace_bytes": (_c_size, [_c_int] * 9),
         "skiparse_attn_fwd_fp8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_bwd_saved": (_c_int, [_vp, _c_size] + [_vp] * 8 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
@@ -223,6 +224,16 @@ def skiparse_debug_rope(x, x_rot, T, H, W, rope_theta=10000.0, stream=None):
 def skiparse_debug_wait_timeout(code, stream=None):
     """Launches the bounded-wait check (about one second); read it with skiparse_device_error()."""
     _check(load_library().skiparse_debug_wait_timeout(int(code), _stream(stream)), "skiparse_debug_wait_timeout")
+
+
+def skiparse_debug_exp2(x, y, mufu=False, stream=None):
+    """y = 2^x (float32 device tensors of equal size) through the softmax's
+    FMA-pipe routine, or the MUFU ex2.approx with mufu=True."""
+    n = x.numel()
+    if y.numel() != n:
+        raise ValueError("x and y must have the same number of elements")
+    _check(load_library().skiparse_debug_exp2(_ptr(x), _ptr(y), n, int(bool(mufu)), _stream(stream)),
+           "skiparse_debug_exp2")
 
 
 def skiparse_device_error():

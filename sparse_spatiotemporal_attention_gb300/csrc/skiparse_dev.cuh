@@ -378,10 +378,13 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
 // Four fp32 values to E4M3 (round to nearest even, saturating at +-448), first
 // value in the lowest byte.
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-  return (uint32_t)lo | ((uint32_t)hi << 16);
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
@@ -519,6 +522,30 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)
 }
 
 // tcgen05.st, 32 lanes x 32 bit, 8 consecutive columns (no wait).
+// tcgen05.ld, 32 lanes x 32 bit, 64 consecutive columns, one wait for all of them.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr) : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tcgen05.ld, 32 lanes x 32 bit, 128 consecutive columns, one wait for all of them.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr) : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
@@ -565,6 +592,67 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x for two values on the FMA pipe. The softmax's exponentials run at the
+// MUFU's 16 per clock per SM, which matches the bf16 tensor rate of the S and
+// P V products and is half the E4M3 one, so a share of them is computed here.
+// Range reduction: adding 1.5 * 2^23 rounds x to the nearest integer j and
+// leaves j in the low mantissa bits of the sum; subtracting 1.5 * 2^23 back
+// gives j exactly, and f = x - j in [-1/2, 1/2] is exact too. 2^f is a
+// degree-3 polynomial with the least maximum relative error on that interval
+// (Remez exchange, fitted by exp2_poly_fit.py beside this file: 7.5e-5 with
+// float32 Horner steps), and 2^j enters as the integer j << 23 added to the
+// polynomial's bit pattern (its exponent field). x is clamped to -125 from
+// below so that field stays normal; valid for x < 128.
+__device__ __forceinline__ void exp2_fma_x2(float x0, float x1, float& y0, float& y1) {
+  constexpr float kRound = 12582912.0f;                  // 1.5 * 2^23
+  constexpr float kC0 = 0x1.fff692p-1f, kC1 = 0x1.62f31ap-1f, kC2 = 0x1.f0de1ap-3f, kC3 = 0x1.c3f76p-5f;
+  const unsigned long long xx = f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
+  const unsigned long long sh = fadd2(xx, f2_pack(kRound, kRound));
+  const unsigned long long f = fsub2(xx, fsub2(sh, f2_pack(kRound, kRound)));
+  unsigned long long p = ffma2(f, f2_pack(kC3, kC3), f2_pack(kC2, kC2));
+  p = ffma2(p, f, f2_pack(kC1, kC1));
+  p = ffma2(p, f, f2_pack(kC0, kC0));
+  float p0, p1, s0, s1;
+  f2_unpack(p, p0, p1);
+  f2_unpack(sh, s0, s1);
+  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(s0) << 23));
+  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(s1) << 23));
+}
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Largest of the 128 scores of a softmax row held in registers: four chains of
+// three-input maxima. With RAGGED, scores at or past `valid` (keys beyond the
+// scope's end in its last tile) are first set to -inf.
+template <bool RAGGED>
+__device__ __forceinline__ float row_max128(float (&x)[128], int valid) {
+  if constexpr (RAGGED) {
+#pragma unroll
+    for (int e = 0; e < 128; ++e) x[e] = e < valid ? x[e] : -INFINITY;
+  }
+  float mm[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) mm[i] = fmaxf(x[i], x[i + 4]);
+#pragma unroll
+  for (int e = 8; e < 128; e += 8) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mm[i] = fmax3(mm[i], x[e + i], x[e + 4 + i]);
+  }
+  return fmax3(mm[0], mm[1], fmaxf(mm[2], mm[3]));
+}
+
+// Of every 16 consecutive element pairs of a softmax row chunk, NF take their
+// 2^x from exp2_fma_x2 and the rest from the MUFU, spread evenly.
+template <int NF>
+__host__ __device__ constexpr bool exp2_on_fma(int pair) {
+  return ((pair % 16 + 1) * NF) / 16 > ((pair % 16) * NF) / 16;
 }
 
 }  // namespace skp

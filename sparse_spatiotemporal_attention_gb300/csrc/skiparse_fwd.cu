@@ -54,6 +54,51 @@ enum FwdBar {
 
 constexpr int kFwdThreads = 320;
 constexpr int kRopeThreads = 256;
+#ifndef SKP_FWD_FMA_PAIRS
+#define SKP_FWD_FMA_PAIRS 0
+#endif
+// element pairs out of every 16 of a softmax row whose 2^x runs on the FMA pipe
+constexpr int kFmaPairs = SKP_FWD_FMA_PAIRS;
+
+// P = 2^(S * sl2 - m) for one softmax row held in registers (x, 128 keys), as
+// bf16 into TMEM at taddr (16 columns per 32 keys, over the row's S columns);
+// returns the row sum of the unrounded P. The exponent argument and the sum use
+// packed two-lane fp32. With RAGGED, keys at or past `valid` get P = 0.
+template <bool RAGGED>
+__device__ __forceinline__ float softmax_p_bf16(const float (&x)[kTile], uint32_t taddr, float sl2, float m,
+                                                int valid) {
+  const unsigned long long sl2x2 = f2_pack(sl2, sl2);
+  const unsigned long long negm2 = f2_pack(-m, -m);
+  unsigned long long acc2[2] = {0ull, 0ull};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int k0 = c * 32 + 2 * e;
+      float t0, t1;
+      f2_unpack(ffma2(f2_pack(x[k0], x[k0 + 1]), sl2x2, negm2), t0, t1);
+      float a, bb;
+      if (exp2_on_fma<kFmaPairs>(e)) {
+        exp2_fma_x2(t0, t1, a, bb);
+      } else {
+        a = ex2(t0);
+        bb = ex2(t1);
+      }
+      if constexpr (RAGGED) {
+        a = k0 < valid ? a : 0.f;
+        bb = k0 + 1 < valid ? bb : 0.f;
+      }
+      acc2[e & 1] = fadd2(acc2[e & 1], f2_pack(a, bb));
+      pk[e] = pack_bf16(a, bb);
+    }
+    tmem_st16(taddr + c * 16, pk);
+  }
+  float s0, s1, s2, s3;
+  f2_unpack(acc2[0], s0, s1);
+  f2_unpack(acc2[1], s2, s3);
+  return (s0 + s1) + (s2 + s3);
+}
 
 __device__ __forceinline__ void decode_unit(const Geom& g, int n_pairs, int u, int& b, int& head, int& s, int& pair) {
   pair = u % n_pairs;
@@ -349,79 +394,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
         if (!mbar_wait(bar(barS), gg & 1, ctl, ERR_KERNEL_FWD + barS)) { ok = false; break; }
         tc_fence_after();
         const int valid = min(kTile, g.L - j * kTile);
-        // pass 1: row max (keys at or past `valid` only exist in the scope's last tile)
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (valid == kTile) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float x[32];
-            tmem_ld32(tmem + lane_base + colS + c * 32, x);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], x[e]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float x[32];
-            tmem_ld32(tmem + lane_base + colS + c * 32, x);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], (c * 32 + e < valid) ? x[e] : -INFINITY);
-          }
-        }
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+        // the whole S row in registers with one TMEM round trip
+        float x[kTile];
+        tmem_ld128(tmem + lane_base + colS, x);
+        const float mx = (valid == kTile ? row_max128<false>(x, valid) : row_max128<true>(x, valid)) * sl2;
+        float f = 1.f;
+        bool rescale = false;
         if (j == 0) {
           m = mx;
         } else {
           const bool need = mx > m + 8.0f;
-          if (__any_sync(0xffffffffu, need)) {
-            // S_X(g) was issued after PV_X(g-1), so that P V is already complete;
-            // the wait only orders this thread after it.
-            if (!mbar_wait(bar(barO), (gg - 1) & 1, ctl, ERR_KERNEL_FWD + barO)) { ok = false; break; }
-            tc_fence_after();
+          rescale = __any_sync(0xffffffffu, need);
+          if (rescale) {
             const float m_new = need ? mx : m;
-            const float f = ex2(m - m_new);
+            f = ex2(m - m_new);
             m = m_new;
             l *= f;
-#pragma unroll 1
-            for (int c = 0; c < D / 16; ++c) {
-              float o[16];
-              tmem_ld16(tmem + lane_base + colO + c * 16, o);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) o[e] *= f;
-              tmem_st16f(tmem + lane_base + colO + c * 16, o);
-            }
+          }
+        }
+        // P over the S columns (the full-tile path has no masking)
+        l += valid == kTile ? softmax_p_bf16<false>(x, tmem + lane_base + colS, sl2, m, valid)
+                            : softmax_p_bf16<true>(x, tmem + lane_base + colS, sl2, m, valid);
+        if (rescale) {
+          // O *= 2^(m_old - m_new) before P V adds this tile. S_X(g) was issued
+          // after PV_X(g-1), so that P V is already complete; the wait only
+          // orders this thread after it.
+          if (!mbar_wait(bar(barO), (gg - 1) & 1, ctl, ERR_KERNEL_FWD + barO)) {
             tmem_st_wait();
+            ok = false;
+            break;
           }
-        }
-        // pass 2: P = 2^(S * scale * log2 e - m) as bf16 over the S columns already
-        // read; the exponent argument and the row sum use packed two-lane fp32.
-        const unsigned long long sl2x2 = f2_pack(sl2, sl2);
-        const unsigned long long negm2 = f2_pack(-m, -m);
-        unsigned long long acc2[2] = {0ull, 0ull};
+          tc_fence_after();
+          if constexpr (D == 128) {
+            float o[128];
+            tmem_ld128(tmem + lane_base + colO, o);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tmem_ld32(tmem + lane_base + colS + c * 32, x);
-          uint32_t pk[16];
+            for (int c = 0; c < 8; ++c) {
+              float oc[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float t0, t1;
-            f2_unpack(ffma2(f2_pack(x[2 * e], x[2 * e + 1]), sl2x2, negm2), t0, t1);
-            float a = ex2(t0), bb = ex2(t1);
-            if (valid < kTile) {
-              a = (c * 32 + 2 * e < valid) ? a : 0.f;
-              bb = (c * 32 + 2 * e + 1 < valid) ? bb : 0.f;
+              for (int e = 0; e < 16; ++e) oc[e] = o[c * 16 + e] * f;
+              tmem_st16f(tmem + lane_base + colO + c * 16, oc);
             }
-            acc2[e & 1] = fadd2(acc2[e & 1], f2_pack(a, bb));
-            pk[e] = pack_bf16(a, bb);
+          } else {
+            float o[64];
+            tmem_ld64(tmem + lane_base + colO, o);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              float oc[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) oc[e] = o[c * 16 + e] * f;
+              tmem_st16f(tmem + lane_base + colO + c * 16, oc);
+            }
           }
-          tmem_st16(tmem + lane_base + colS + c * 16, pk);
-        }
-        {
-          float s0, s1, s2, s3;
-          f2_unpack(acc2[0], s0, s1);
-          f2_unpack(acc2[1], s2, s3);
-          l += (s0 + s1) + (s2 + s3);
         }
         tmem_st_wait();
         tc_fence_before();

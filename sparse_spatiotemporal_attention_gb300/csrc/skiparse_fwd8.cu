@@ -39,6 +39,61 @@ constexpr int kD8 = 128;
 constexpr int kF8Threads = 320;
 constexpr int kPrepThreads = 256;
 constexpr float kE4M3Max = 448.0f;
+#ifndef SKP_FWD8_FMA_PAIRS
+#define SKP_FWD8_FMA_PAIRS 0
+#endif
+// element pairs out of every 16 of a softmax row whose 2^x runs on the FMA pipe
+constexpr int kFmaPairs = SKP_FWD8_FMA_PAIRS;
+
+// 2^6 P = 2^(S * ck + off) for one softmax row held in registers (x, 128 keys;
+// off = 6 - m), as E4M3 codes into TMEM at taddr: keys 32c .. 32c+31 go to
+// columns 8c .. 8c+7, four codes per column. Returns the row sum of the
+// unquantized 2^6 P. With RAGGED, keys at or past `valid` get P = 0.
+template <bool RAGGED>
+__device__ __forceinline__ float softmax_p_e4m3(const float (&x)[kTile], uint32_t taddr, float ck, float off,
+                                                int valid) {
+  const unsigned long long ck2 = f2_pack(ck, ck);
+  const unsigned long long off2 = f2_pack(off, off);
+  unsigned long long acc2[2] = {0ull, 0ull};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int k0 = c * 32 + 4 * e;
+      float t0, t1, t2, t3;
+      f2_unpack(ffma2(f2_pack(x[k0], x[k0 + 1]), ck2, off2), t0, t1);
+      f2_unpack(ffma2(f2_pack(x[k0 + 2], x[k0 + 3]), ck2, off2), t2, t3);
+      float p0, p1, p2, p3;
+      if (exp2_on_fma<kFmaPairs>(2 * e)) {
+        exp2_fma_x2(t0, t1, p0, p1);
+      } else {
+        p0 = ex2(t0);
+        p1 = ex2(t1);
+      }
+      if (exp2_on_fma<kFmaPairs>(2 * e + 1)) {
+        exp2_fma_x2(t2, t3, p2, p3);
+      } else {
+        p2 = ex2(t2);
+        p3 = ex2(t3);
+      }
+      if constexpr (RAGGED) {
+        p0 = k0 < valid ? p0 : 0.f;
+        p1 = k0 + 1 < valid ? p1 : 0.f;
+        p2 = k0 + 2 < valid ? p2 : 0.f;
+        p3 = k0 + 3 < valid ? p3 : 0.f;
+      }
+      acc2[0] = fadd2(acc2[0], f2_pack(p0, p1));
+      acc2[1] = fadd2(acc2[1], f2_pack(p2, p3));
+      pk[e] = e4m3x4(p0, p1, p2, p3);
+    }
+    tmem_st8(taddr + c * 8, pk);
+  }
+  float s0, s1, s2, s3;
+  f2_unpack(acc2[0], s0, s1);
+  f2_unpack(acc2[1], s2, s3);
+  return (s0 + s1) + (s2 + s3);
+}
 
 struct F8Layout {
   static constexpr int TILE = 128 * 128;          // 16 KB: 128 rows x 128 bytes, one 128-byte swizzled box
@@ -384,70 +439,45 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
         if (!mbar_wait(bar(barS), gg & 1, ctl, E + barS)) { ok = false; break; }
         tc_fence_after();
         const int valid = min(kTile, g.L - j * kTile);
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tmem_ld32(tmem + lane_base + colS + c * 32, x);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], (c * 32 + e < valid) ? x[e] : -INFINITY);
-        }
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * ck;
+        // the whole S row in registers with one TMEM round trip
+        float x[kTile];
+        tmem_ld128(tmem + lane_base + colS, x);
+        const float mx = (valid == kTile ? row_max128<false>(x, valid) : row_max128<true>(x, valid)) * ck;
+        float f = 1.f;
+        bool rescale = false;
         if (j == 0) {
           m = mx;
         } else {
           const bool need = mx > m + 2.0f;
-          if (__any_sync(0xffffffffu, need)) {
-            if (!mbar_wait(bar(barO), (gg - 1) & 1, ctl, E + barO)) { ok = false; break; }
-            tc_fence_after();
+          rescale = __any_sync(0xffffffffu, need);
+          if (rescale) {
             const float m_new = need ? mx : m;
-            const float f = ex2(m - m_new);
+            f = ex2(m - m_new);
             m = m_new;
             l *= f;
-#pragma unroll 1
-            for (int c = 0; c < D / 16; ++c) {
-              float o[16];
-              tmem_ld16(tmem + lane_base + colO + c * 16, o);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) o[e] *= f;
-              tmem_st16f(tmem + lane_base + colO + c * 16, o);
-            }
+          }
+        }
+        // 2^6 P as E4M3 over the S columns (the full-tile path has no masking)
+        l += valid == kTile ? softmax_p_e4m3<false>(x, tmem + lane_base + colS, ck, 6.0f - m, valid)
+                            : softmax_p_e4m3<true>(x, tmem + lane_base + colS, ck, 6.0f - m, valid);
+        if (rescale) {
+          // O *= 2^(m_old - m_new) before P V adds this tile (PV_X(g-1) is
+          // complete: S_X(g) was issued after it)
+          if (!mbar_wait(bar(barO), (gg - 1) & 1, ctl, E + barO)) {
             tmem_st_wait();
+            ok = false;
+            break;
           }
-        }
-        // 2^6 P = 2^(S * ck - m + 6) as E4M3 over the S columns already read:
-        // keys 32c .. 32c+31 -> columns colS + 8c .. +7 (four codes per column)
-        const unsigned long long ck2 = f2_pack(ck, ck);
-        const unsigned long long off2 = f2_pack(6.0f - m, 6.0f - m);
-        unsigned long long acc2[2] = {0ull, 0ull};
+          tc_fence_after();
+          float o[kD8];
+          tmem_ld128(tmem + lane_base + colO, o);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float x[32];
-          tmem_ld32(tmem + lane_base + colS + c * 32, x);
-          uint32_t pk[8];
+          for (int c = 0; c < kD8 / 16; ++c) {
+            float oc[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float t0, t1, t2, t3;
-            f2_unpack(ffma2(f2_pack(x[4 * e], x[4 * e + 1]), ck2, off2), t0, t1);
-            f2_unpack(ffma2(f2_pack(x[4 * e + 2], x[4 * e + 3]), ck2, off2), t2, t3);
-            float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
-            if (valid < kTile) {
-              const int k0 = c * 32 + 4 * e;
-              p0 = k0 < valid ? p0 : 0.f;
-              p1 = k0 + 1 < valid ? p1 : 0.f;
-              p2 = k0 + 2 < valid ? p2 : 0.f;
-              p3 = k0 + 3 < valid ? p3 : 0.f;
-            }
-            acc2[e & 1] = fadd2(acc2[e & 1], f2_pack(p0 + p2, p1 + p3));
-            pk[e] = e4m3x4(p0, p1, p2, p3);
+            for (int e = 0; e < 16; ++e) oc[e] = o[c * 16 + e] * f;
+            tmem_st16f(tmem + lane_base + colO + c * 16, oc);
           }
-          tmem_st8(tmem + lane_base + colS + c * 8, pk);
-        }
-        {
-          float s0, s1, s2, s3;
-          f2_unpack(acc2[0], s0, s1);
-          f2_unpack(acc2[1], s2, s3);
-          l += (s0 + s1) + (s2 + s3);
         }
         tmem_st_wait();
         tc_fence_before();

@@ -614,6 +614,17 @@ int skiparse_debug_wait_timeout(int code, cudaStream_t stream) {
   return launch_status(launch_debug_wait_timeout(dev.err_word, code, stream));
 }
 
+int skiparse_debug_exp2(const float* x, float* y, int n, int mufu, cudaStream_t stream) {
+  if (n < 0 || (mufu != 0 && mufu != 1) || (n > 0 && (!x || !y))) return SKIPARSE_ERR_INVALID_ARG;
+  if (n == 0) return SKIPARSE_OK;
+  if (!aligned16(x) || !aligned16(y)) return SKIPARSE_ERR_ALIGNMENT;
+  if (any_alias({{y, (size_t)n * 4}}, {{x, (size_t)n * 4}})) return SKIPARSE_ERR_ALIAS;
+  DeviceInfo dev;
+  const int st = device_info(dev);
+  if (st != SKIPARSE_OK) return st;
+  return launch_status(launch_debug_exp2(x, y, n, mufu, stream));
+}
+
 int skiparse_device_error(int* detail) {
   DeviceInfo dev;
   int st = device_info(dev);

@@ -127,5 +127,6 @@ cudaError_t launch_bwd_post(const BwdParams& p, int grid, int sms, cudaStream_t 
 cudaError_t launch_debug_index_map(const DebugParams& p, cudaStream_t stream);
 cudaError_t launch_debug_rope(const DebugParams& p, cudaStream_t stream);
 cudaError_t launch_debug_wait_timeout(int* err, int code, cudaStream_t stream);
+cudaError_t launch_debug_exp2(const float* x, float* y, int n, int mufu, cudaStream_t stream);
 
 }  // namespace skp
