@@ -19,9 +19,10 @@
 // Kernels:
 //   skiparse_fwd8_vmax_kernel   max |v| per (b, head, channel) (atomicMax on the
 //                               bits of non-negative floats into a zeroed array);
-//   skiparse_fwd8_prep_kernel   one CTA per (scope, 128-position tile): RoPE and
-//                               quantize q (per row) and k (per tile), quantize v
-//                               and transpose it, all in scope-tile order, so the
+//   skiparse_fwd8_prep_kernel   persistent CTAs (one RoPE table each) over (scope,
+//                               128-position tile) items: RoPE and quantize q (per
+//                               row) and k (per tile), quantize v and transpose it
+//                               in shared memory, all in scope-tile order, so the
 //                               attention kernel reads plain 128 x 128-byte boxes
 //                               (every 8-bit operand K-major);
 //   skiparse_fwd8_kernel        the forward kernel's structure (two Q tiles per
@@ -39,6 +40,9 @@ constexpr int kD8 = 128;
 constexpr int kF8Threads = 320;
 constexpr int kPrepThreads = 256;
 constexpr float kE4M3Max = 448.0f;
+
+// RoPE table bytes in the prep kernel's shared memory, rounded up to 16
+__host__ __device__ constexpr size_t prep_table_bytes(int entries) { return ((size_t)entries * 8 + 15) & ~(size_t)15; }
 #ifndef SKP_FWD8_FMA_PAIRS
 #define SKP_FWD8_FMA_PAIRS 0
 #endif
@@ -147,88 +151,120 @@ __global__ void __launch_bounds__(128) skiparse_fwd8_vmax_kernel(const __grid_co
 __global__ void __launch_bounds__(kPrepThreads) skiparse_fwd8_prep_kernel(const __grid_constant__ Fwd8Params p) {
   extern __shared__ __align__(16) uint8_t psm[];
   float2* tab = reinterpret_cast<float2*>(psm);                                     // RoPE table
-  float* kbuf = reinterpret_cast<float*>(psm + p.rope.entries * sizeof(float2));    // 128 x 128 rotated k
-  float* rowmax = kbuf + 128 * kD8;                                                 // 128
-  uint8_t* vt = reinterpret_cast<uint8_t*>(rowmax + 128);                           // 128 channels x 132 bytes
-  constexpr int VT_STRIDE = 132;
+  uint32_t* vt = reinterpret_cast<uint32_t*>(psm + prep_table_bytes(p.rope.entries));  // 128 channels x 32 words
+  float* rowmax = reinterpret_cast<float*>(vt + kD8 * 32);                          // one per warp
   const Geom& g = p.g;
-  const int tile = blockIdx.x % g.n_tiles;
-  const int sidx = blockIdx.x / g.n_tiles;
-  const int s = sidx % g.k;
-  const int bh = sidx / g.k;
-  const int b = bh / g.heads, head = bh - b * g.heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
   __syncthreads();
-  PairSel sel[2];
-  sel[0] = pair_select(p.rope, lane * 2);
-  sel[1] = pair_select(p.rope, lane * 2 + 1);
-  float inv_v[4];
+  const PairSel sel0 = pair_select(p.rope, lane * 2);
+  const PairSel sel1 = pair_select(p.rope, lane * 2 + 1);
+  const int n_items = g.B * g.heads * g.k * g.n_tiles;
+  // persistent: one (scope, 128-position tile) item at a time; warp w owns the
+  // tile's rows 4(w + 8i) .. 4(w + 8i) + 3, i = 0..3
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int tile = item % g.n_tiles;
+    const int sidx = item / g.n_tiles;
+    const int s = sidx % g.k;
+    const int bh = sidx / g.k;
+    const int b = bh / g.heads, head = bh - b * g.heads;
+    float inv_v[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float m = __uint_as_float(p.vmax[(size_t)bh * kD8 + lane * 4 + e]);
-    inv_v[e] = m > 0.f ? kE4M3Max / m : 0.f;
-  }
-  float kmax = 0.f;
-  for (int r = warp; r < 128; r += 8) {
-    const int pos = tile * kTile + r;
-    const size_t slot = (size_t)sidx * p.Lp + pos;          // scope-order row
-    uint32_t qc = 0, vc = 0;
-    float sq = 0.f;
-    float kr[4] = {0.f, 0.f, 0.f, 0.f};
-    if (pos < g.L) {
-      const int i = token_of(g, s, pos);
-      int t, hh, w;
-      token_coords(p.rope, i, t, hh, w);
-      const size_t base = (((size_t)b * g.N + i) * g.heads + head) * kD8 + lane * 4;
-      const uint2 qu = *reinterpret_cast<const uint2*>(p.q + base);
-      const uint2 ku = *reinterpret_cast<const uint2*>(p.k + base);
-      const uint2 vu = *reinterpret_cast<const uint2*>(p.v + base);
-      float qr[4];
-      const float2 c0 = tab[pair_index(sel[0], t, hh, w)];
-      const float2 c1 = tab[pair_index(sel[1], t, hh, w)];
-      float2 a = rope_rotate(bf16lo(qu.x), bf16hi(qu.x), c0);
-      float2 bq = rope_rotate(bf16lo(qu.y), bf16hi(qu.y), c1);
-      qr[0] = a.x; qr[1] = a.y; qr[2] = bq.x; qr[3] = bq.y;
-      a = rope_rotate(bf16lo(ku.x), bf16hi(ku.x), c0);
-      bq = rope_rotate(bf16lo(ku.y), bf16hi(ku.y), c1);
-      kr[0] = a.x; kr[1] = a.y; kr[2] = bq.x; kr[3] = bq.y;
-      // q: per-row scale
-      float qm = fmaxf(fmaxf(fabsf(qr[0]), fabsf(qr[1])), fmaxf(fabsf(qr[2]), fabsf(qr[3])));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
-      const float qi = qm > 0.f ? kE4M3Max / qm : 0.f;
-      qc = e4m3x4(qr[0] * qi, qr[1] * qi, qr[2] * qi, qr[3] * qi);
-      sq = qm > 0.f ? qm / kE4M3Max : 1.f;
-      vc = e4m3x4(bf16lo(vu.x) * inv_v[0], bf16hi(vu.x) * inv_v[1], bf16lo(vu.y) * inv_v[2], bf16hi(vu.y) * inv_v[3]);
-      kmax = fmaxf(kmax, fmaxf(fmaxf(fabsf(kr[0]), fabsf(kr[1])), fmaxf(fabsf(kr[2]), fabsf(kr[3]))));
+    for (int e = 0; e < 4; ++e) {
+      const float m = __uint_as_float(p.vmax[(size_t)bh * kD8 + lane * 4 + e]);
+      inv_v[e] = m > 0.f ? kE4M3Max / m : 0.f;
     }
-    *reinterpret_cast<uint32_t*>(p.q8 + slot * kD8 + lane * 4) = qc;
-    if (lane == 0) p.sq[slot] = sq;
-    *reinterpret_cast<float4*>(kbuf + r * kD8 + lane * 4) = make_float4(kr[0], kr[1], kr[2], kr[3]);
-    // v transposed: channel-major rows of 128 positions (padded stride against bank conflicts)
+    float kr[4][4][4];                 // rotated k of the warp's 16 rows, 4 channels per lane
+    float kmax = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) vt[(lane * 4 + e) * VT_STRIDE + r] = (uint8_t)(vc >> (8 * e));
-  }
+    for (int i = 0; i < 4; ++i) {
+      const int r0 = 4 * (warp + 8 * i);
+      // the group's loads first (all in flight together), then the arithmetic
+      uint2 qu4[4], ku4[4], vu4[4];
+      int tok4[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  if (lane == 0) rowmax[warp] = kmax;
-  __syncthreads();
-  float tmax = 0.f;
+      for (int rr = 0; rr < 4; ++rr) {
+        const int pos = tile * kTile + r0 + rr;
+        tok4[rr] = pos < g.L ? token_of(g, s, pos) : -1;
+        qu4[rr] = ku4[rr] = vu4[rr] = make_uint2(0u, 0u);
+        if (tok4[rr] >= 0) {
+          const size_t base = (((size_t)b * g.N + tok4[rr]) * g.heads + head) * kD8 + lane * 4;
+          qu4[rr] = __ldg(reinterpret_cast<const uint2*>(p.q + base));
+          ku4[rr] = __ldg(reinterpret_cast<const uint2*>(p.k + base));
+          vu4[rr] = __ldg(reinterpret_cast<const uint2*>(p.v + base));
+        }
+      }
+      uint32_t vc[4];
 #pragma unroll
-  for (int w = 0; w < 8; ++w) tmax = fmaxf(tmax, rowmax[w]);
-  const float ki = tmax > 0.f ? kE4M3Max / tmax : 0.f;
-  if (threadIdx.x == 0) p.sk[(size_t)sidx * g.n_tiles + tile] = tmax > 0.f ? tmax / kE4M3Max : 1.f;
-  for (int r = warp; r < 128; r += 8) {
-    const float4 x = *reinterpret_cast<const float4*>(kbuf + r * kD8 + lane * 4);
-    const size_t slot = (size_t)sidx * p.Lp + tile * kTile + r;
-    *reinterpret_cast<uint32_t*>(p.k8 + slot * kD8 + lane * 4) = e4m3x4(x.x * ki, x.y * ki, x.z * ki, x.w * ki);
-  }
-  // V^T rows: channel d of this tile's 128 positions, 4 bytes per thread per step
-  for (int idx = threadIdx.x; idx < kD8 * 32; idx += blockDim.x) {
-    const int d = idx >> 5, c = idx & 31;
-    const uint32_t word = *reinterpret_cast<const uint32_t*>(vt + d * VT_STRIDE + c * 4);
-    *reinterpret_cast<uint32_t*>(p.vt8 + ((size_t)sidx * kD8 + d) * p.Lp + tile * kTile + c * 4) = word;
+      for (int rr = 0; rr < 4; ++rr) {
+        const int pos = tile * kTile + r0 + rr;
+        const size_t slot = (size_t)sidx * p.Lp + pos;          // scope-order row
+        uint32_t qc = 0;
+        float sq = 0.f;
+        vc[rr] = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kr[i][rr][e] = 0.f;
+        if (tok4[rr] >= 0) {
+          int t, hh, w;
+          token_coords(p.rope, tok4[rr], t, hh, w);
+          const uint2 qu = qu4[rr], ku = ku4[rr], vu = vu4[rr];
+          const float2 c0 = tab[pair_index(sel0, t, hh, w)];
+          const float2 c1 = tab[pair_index(sel1, t, hh, w)];
+          const float2 qa = rope_rotate(bf16lo(qu.x), bf16hi(qu.x), c0);
+          const float2 qb = rope_rotate(bf16lo(qu.y), bf16hi(qu.y), c1);
+          const float2 ka = rope_rotate(bf16lo(ku.x), bf16hi(ku.x), c0);
+          const float2 kb = rope_rotate(bf16lo(ku.y), bf16hi(ku.y), c1);
+          kr[i][rr][0] = ka.x; kr[i][rr][1] = ka.y; kr[i][rr][2] = kb.x; kr[i][rr][3] = kb.y;
+          // q: per-row scale
+          float qm = fmaxf(fmaxf(fabsf(qa.x), fabsf(qa.y)), fmaxf(fabsf(qb.x), fabsf(qb.y)));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+          const float qi = qm > 0.f ? kE4M3Max / qm : 0.f;
+          qc = e4m3x4(qa.x * qi, qa.y * qi, qb.x * qi, qb.y * qi);
+          sq = qm > 0.f ? qm / kE4M3Max : 1.f;
+          vc[rr] = e4m3x4(bf16lo(vu.x) * inv_v[0], bf16hi(vu.x) * inv_v[1], bf16lo(vu.y) * inv_v[2],
+                          bf16hi(vu.y) * inv_v[3]);
+          kmax = fmaxf(kmax, fmaxf(fmaxf(fabsf(ka.x), fabsf(ka.y)), fmaxf(fabsf(kb.x), fabsf(kb.y))));
+        }
+        *reinterpret_cast<uint32_t*>(p.q8 + slot * kD8 + lane * 4) = qc;
+        if (lane == 0) p.sq[slot] = sq;
+      }
+      // 4 rows x 4 channels of v codes -> channel 4 lane + e gets positions r0 .. r0+3 in one
+      // word, stored at word (r0 / 4) ^ lane of the channel's 32 (conflict-free across lanes)
+      const uint32_t lo01 = __byte_perm(vc[0], vc[1], 0x5140), hi01 = __byte_perm(vc[0], vc[1], 0x7362);
+      const uint32_t lo23 = __byte_perm(vc[2], vc[3], 0x5140), hi23 = __byte_perm(vc[2], vc[3], 0x7362);
+      const int wi = (r0 >> 2) ^ lane;
+      vt[(4 * lane + 0) * 32 + wi] = __byte_perm(lo01, lo23, 0x5410);
+      vt[(4 * lane + 1) * 32 + wi] = __byte_perm(lo01, lo23, 0x7632);
+      vt[(4 * lane + 2) * 32 + wi] = __byte_perm(hi01, hi23, 0x5410);
+      vt[(4 * lane + 3) * 32 + wi] = __byte_perm(hi01, hi23, 0x7632);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    if (lane == 0) rowmax[warp] = kmax;
+    __syncthreads();
+    float tmax = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) tmax = fmaxf(tmax, rowmax[w]);
+    const float ki = tmax > 0.f ? kE4M3Max / tmax : 0.f;
+    if (threadIdx.x == 0) p.sk[(size_t)sidx * g.n_tiles + tile] = tmax > 0.f ? tmax / kE4M3Max : 1.f;
+    // k: one scale per tile
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const size_t slot = (size_t)sidx * p.Lp + tile * kTile + 4 * (warp + 8 * i) + rr;
+        *reinterpret_cast<uint32_t*>(p.k8 + slot * kD8 + lane * 4) =
+            e4m3x4(kr[i][rr][0] * ki, kr[i][rr][1] * ki, kr[i][rr][2] * ki, kr[i][rr][3] * ki);
+      }
+    }
+    // V^T rows: channel d of this tile's 128 positions, one word per thread per step
+    for (int idx = threadIdx.x; idx < kD8 * 32; idx += blockDim.x) {
+      const int d = idx >> 5, c = idx & 31;
+      const uint32_t word = vt[d * 32 + (c ^ (d >> 2))];
+      *reinterpret_cast<uint32_t*>(p.vt8 + ((size_t)sidx * kD8 + d) * p.Lp + tile * kTile + c * 4) = word;
+    }
+    __syncthreads();                   // vt and rowmax are reused by the next item
   }
 }
 
@@ -535,7 +571,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
 size_t fwd8_smem_bytes() { return F8Layout::BYTES; }
 
 size_t fwd8_prep_smem_bytes(int rope_entries) {
-  return (size_t)rope_entries * sizeof(float2) + (size_t)128 * kD8 * 4 + 128 * 4 + (size_t)kD8 * 132;
+  return prep_table_bytes(rope_entries) + (size_t)kD8 * 32 * 4 + (kPrepThreads / 32) * 4;
 }
 
 int fwd8_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 2); }
@@ -546,11 +582,11 @@ cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd8_prep(const Fwd8Params& p, cudaStream_t stream) {
+cudaError_t launch_fwd8_prep(const Fwd8Params& p, int sms, cudaStream_t stream) {
   const size_t smem = fwd8_prep_smem_bytes(p.rope.entries);
   cudaError_t e = cudaFuncSetAttribute(skiparse_fwd8_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = p.g.B * p.g.heads * p.g.k * p.g.n_tiles;
+  const int grid = one_wave(skiparse_fwd8_prep_kernel, p.g.B * p.g.heads * p.g.k * p.g.n_tiles, kPrepThreads, smem, sms);
   skiparse_fwd8_prep_kernel<<<grid, kPrepThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }

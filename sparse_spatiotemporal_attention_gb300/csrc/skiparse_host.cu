@@ -452,7 +452,7 @@ int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out
   if (cudaMemsetAsync(p.vmax, 0, (size_t)B * heads * 128 * 4, stream) != cudaSuccess) return launch_status(cudaErrorUnknown);
   st = launch_status(traced_launch(5, stream, [&] { return launch_fwd8_vmax(p, stream); }));
   if (st != SKIPARSE_OK) return st;
-  st = launch_status(traced_launch(6, stream, [&] { return launch_fwd8_prep(p, stream); }));
+  st = launch_status(traced_launch(6, stream, [&] { return launch_fwd8_prep(p, dev.sms, stream); }));
   if (st != SKIPARSE_OK) return st;
   return launch_status(traced_launch(7, stream, [&] { return launch_fwd8(p, grid, stream); }));
 }

@@ -115,7 +115,7 @@ size_t fwd8_smem_bytes();
 size_t fwd8_prep_smem_bytes(int rope_entries);
 int fwd8_units(const Geom& g);
 cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream);
-cudaError_t launch_fwd8_prep(const Fwd8Params& p, cudaStream_t stream);
+cudaError_t launch_fwd8_prep(const Fwd8Params& p, int sms, cudaStream_t stream);
 cudaError_t launch_fwd8(const Fwd8Params& p, int grid, cudaStream_t stream);
 
 size_t bwd_main_smem_bytes(int D);
