@@ -21,7 +21,8 @@ Printed JSON line (rank 0):
   fwd_configs  forward-only throughput (RoPE pass + attention) of the single-skip
                8x32x32, the group-skip 24x22x40 (B=2) and the long-sequence
                group-skip 16x45x80 (57,600-token) configurations, the group ones
-               also at k=1 (rank 0; skipped with --no-k1); each with the 8-bit
+               also at k=1 (rank 0; skipped with --no-fwd-configs, the k=1
+               runs here and the step's k=1 run with --no-k1); each with the 8-bit
                forward (skiparse_attn_fwd_fp8) beside it, against the FP8 peak
                taken as the measured bf16 peak x the nominal FP8 / bf16 ratio.
 
@@ -49,9 +50,11 @@ METRIC = "Skiparse attn fwd/fwd+bwd TFLOP/s and % of GB300 bf16 peak; speedup vs
 WORKLOADS = {
     # the timed workload: a training step on the 21,120-token group-skip grid
     "train": dict(name="skiparse_train_step_group_24x22x40_k4", B=2, heads=24, D=128, T=24, H=22, W=40, k=4, mode=1),
-    # a smaller case of the same kernels for ncu captures (inputs still larger than L2)
+    # a smaller case of the same kernels for ncu captures (inputs still larger than L2),
+    # with one forward configuration of the same size for the forward kernels
     "ncu_small": dict(name="skiparse_train_step_group_24x22x40_k4_b1h8", B=1, heads=8, D=128, T=24, H=22, W=40, k=4,
-                      mode=1),
+                      mode=1, fwd=[dict(name="skiparse_fwd_group_24x22x40_k4_b1h8", B=1, heads=8, D=128, T=24, H=22,
+                                        W=40, k=4, mode=1, k1=False)]),
 }
 WORKLOAD = WORKLOADS["train"]
 # forward-only configurations reported beside the timed step (same kernels)
@@ -232,7 +235,7 @@ def job_tflops(world, flops_per_rank_step, ms_per_step):
     return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
-def fwd_config_lines(skp, dev, stream, peaks, launches=10):
+def fwd_config_lines(skp, dev, stream, peaks, launches=10, with_k1=True):
     """Forward-only throughput (RoPE pass + attention) of FWD_CONFIGS, and the
     dense k = 1 forward on the same inputs where the configuration asks for it."""
     import numpy as np
@@ -241,7 +244,7 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10):
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     lines = []
-    for c in FWD_CONFIGS:
+    for c in WORKLOAD.get("fwd", FWD_CONFIGS):
         B, heads, D, T, H, W = c["B"], c["heads"], c["D"], c["T"], c["H"], c["W"]
         N = T * H * W
         ins = synthetic.attention_inputs(B, N, heads, D, with_grad=False)
@@ -294,7 +297,7 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10):
                        "speedup_vs_bf16": ms / ms8,
                        "kernels": {skp.KERNEL_NAMES[i]: kms[i] / kcnt[i] for i in range(len(kcnt)) if kcnt[i]}}
         del ws8
-        if c["k1"]:
+        if c["k1"] and with_k1:
             ms1 = timed(1)
             line["k1"] = {"ms_per_launch": ms1, "tflops": fwd_flops(c, 1) / (ms1 * 1e-3) / 1e12,
                           "speedup": ms1 / ms}
@@ -302,6 +305,44 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10):
         del d, out, lse, fws
         torch.cuda.empty_cache()
     return lines
+
+
+def proj_line(skp, dev, stream, peaks, launches=10):
+    """Q/K/V projection with the RoPE epilogue (skiparse_qkv_rope) at the timed
+    workload's sizes: x (B, N, C = heads D), W (3 heads D, C), bf16, with bias."""
+    import numpy as np
+    import torch
+    from sparse_spatiotemporal_attention_gb300 import synthetic
+    w_ = WORKLOAD
+    B, heads, D, T, H, W = w_["B"], w_["heads"], w_["D"], w_["T"], w_["H"], w_["W"]
+    N, C = T * H * W, heads * D
+    hd = heads * D
+
+    def dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x = dev_bf16(synthetic.normal_bf16_bits(11, (B, N, C)))
+    wt = dev_bf16(synthetic.normal_bf16_bits(12, (3 * hd, C), 1.0 / np.sqrt(C)))
+    bias = dev_bf16(synthetic.normal_bf16_bits(13, (3 * hd,), 0.1))
+    q, k, v = (torch.empty((B, N, heads, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    for _ in range(3):
+        skp.skiparse_qkv_rope(x, wt, bias, q, k, v, T, H, W, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(launches):
+        skp.skiparse_qkv_rope(x, wt, bias, q, k, v, T, H, W, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / launches
+    flops = 2.0 * B * N * C * 3 * hd
+    tf = flops / (ms * 1e-3) / 1e12
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    del x, wt, bias, q, k, v
+    torch.cuda.empty_cache()
+    return {"workload": f"qkv_proj_rope_{T}x{H}x{W}_b{B}_c{C}_h{heads}", "M": B * N, "C": C, "N_out": 3 * hd,
+            "ms_per_launch": ms, "tflops": tf, "pct_of_peak": {"burst": tf / burst, "sustained": tf / sustained}}
 
 
 def gpu_arm(args):
@@ -467,8 +508,10 @@ def gpu_arm(args):
 
     peaks, src = load_peaks()
     fwd_lines = None
-    if not args.no_k1 and rank == 0:
-        fwd_lines = fwd_config_lines(skp, dev, stream, peaks)
+    qkv_line = None
+    if not args.no_fwd_configs and rank == 0:
+        fwd_lines = fwd_config_lines(skp, dev, stream, peaks, with_k1=not args.no_k1)
+        qkv_line = proj_line(skp, dev, stream, peaks)
     kernels = {}
     tot = sum(kms) or 1.0
     for i in range(nk):
@@ -500,6 +543,7 @@ def gpu_arm(args):
         "fwd": {"ms_per_launch": fwd_ms, "tflops": fwd_flops(w) / (fwd_ms * 1e-3) / 1e12},
         "speedup_vs_k1": (k1 or {}).get("speedup"), "k1": k1,
         "fwd_configs": fwd_lines,
+        "qkv_proj": qkv_line,
         "clocks": clocks, "e2e": e2e, "gpu_launches": int(sum(kcnt)), "kernels": kernels, "roofline": roofline,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -559,6 +603,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-k1", action="store_true")
+    ap.add_argument("--no-fwd-configs", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="train", choices=sorted(WORKLOADS))

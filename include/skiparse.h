@@ -182,6 +182,35 @@ int skiparse_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
                               int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
+ * Q/K/V projection with the RoPE epilogue: the step before the attention in
+ * the Skiparse listings (Open-Sora Plan docs, "Skiparse Attention", single-
+ * and group-skip implementations: q, k, v = Q(x), K(x), V(x), then RoPE on q
+ * and k at each token's original position, the same 3D RoPE as
+ * skiparse_attn_fwd applies).
+ *
+ *   [q | k | v] = x W^T + bias
+ *   x     bf16 (B, N, C) row-major (C contiguous)
+ *   w     bf16 (3 heads D, C): rows 0 .. heads D - 1 are Q's weight, then K's,
+ *         then V's (the three nn.Linear weights stacked, out x in)
+ *   bias  bf16 [3 heads D], or NULL for none
+ *   q, k, v  bf16 (B, N, heads, D) outputs; q and k rotated by RoPE(t, h, w)
+ *         of token n = t H W + h W + w with rope_theta; v not rotated
+ * Products accumulate in fp32 (tcgen05, TMEM); bias and RoPE are applied in
+ * fp32 and each output is rounded to bf16 once. All pointers are device
+ * pointers owned by the caller, 16-byte aligned; q, k and v must not overlap
+ * each other or an input. Asynchronous on `stream`; nothing is written when
+ * validation fails. Status: SKIPARSE_ERR_SHAPE if N != T H W;
+ * SKIPARSE_ERR_UNSUPPORTED for D not in {64, 128}, C < 8 or C % 8 != 0,
+ * heads D % 128 != 0, a RoPE table over 8192 pairs, or sizes past 2^31 rows;
+ * SKIPARSE_ERR_INVALID_ARG for negative sizes, a non-positive rope_theta or a
+ * NULL x / w / q / k / v; SKIPARSE_ERR_ALIGNMENT, SKIPARSE_ERR_ALIAS and
+ * SKIPARSE_ERR_DEVICE as elsewhere. B, N or heads of 0: nothing to do, OK.
+ */
+int skiparse_qkv_rope(const void* x, const void* w, const void* bias, void* q, void* k, void* v,
+                      int B, int N, int C, int heads, int D, int T, int H, int W,
+                      float rope_theta, cudaStream_t stream);
+
+/*
  * Test hook: the token -> (scope, position) map exactly as the kernels address
  * it (the listings' rearrange patterns). Writes int32 scope_of_token[N] and
  * pos_of_token[N].

@@ -18,7 +18,7 @@ SINGLE = 0
 GROUP = 1
 KERNEL_NAMES = ("skiparse_fwd_kernel", "skiparse_bwd_pre_kernel", "skiparse_bwd_main_kernel",
                 "skiparse_bwd_post_kernel", "skiparse_fwd_rope_kernel", "skiparse_fwd8_vmax_kernel",
-                "skiparse_fwd8_prep_kernel", "skiparse_fwd8_kernel")
+                "skiparse_fwd8_prep_kernel", "skiparse_fwd8_kernel", "skiparse_qkv_rope_kernel")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libskiparse.so")
@@ -29,6 +29,7 @@ EXPORTS = (
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
     "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout", "skiparse_attn_bwd_saved",
     "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8", "skiparse_debug_exp2",
+    "skiparse_qkv_rope",
 )
 
 
@@ -68,6 +69,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_debug_wait_timeout": (_c_int, [_c_int, _vp]),
         "skiparse_debug_exp2": (_c_int, [_vp, _vp, _c_int, _c_int, _vp]),
+        "skiparse_qkv_rope": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _vp]),
         "skiparse_attn_fwd_fp8_workspace_bytes": (_c_size, [_c_int] * 9),
         "skiparse_attn_fwd_fp8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_bwd_saved": (_c_int, [_vp, _c_size] + [_vp] * 8 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
@@ -224,6 +226,23 @@ def skiparse_debug_rope(x, x_rot, T, H, W, rope_theta=10000.0, stream=None):
 def skiparse_debug_wait_timeout(code, stream=None):
     """Launches the bounded-wait check (about one second); read it with skiparse_device_error()."""
     _check(load_library().skiparse_debug_wait_timeout(int(code), _stream(stream)), "skiparse_debug_wait_timeout")
+
+
+def skiparse_qkv_rope(x, w, bias, q, k, v, T, H, W, rope_theta=10000.0, stream=None):
+    """[q | k | v] = x w^T (+ bias), RoPE on q and k (the Skiparse listings'
+    projections before the attention). x (B, N, C), w (3 heads D, C), bias
+    [3 heads D] or None, all bf16; q, k, v (B, N, heads, D) bf16 outputs."""
+    B, N, C = x.shape
+    Bq, Nq, heads, D = q.shape
+    if (Bq, Nq) != (B, N) or tuple(k.shape) != tuple(q.shape) or tuple(v.shape) != tuple(q.shape):
+        raise ValueError("q, k, v must be (B, N, heads, D) with x's B and N")
+    if tuple(w.shape) != (3 * heads * D, C):
+        raise ValueError("w must be (3 heads D, C)")
+    if bias is not None and bias.numel() != 3 * heads * D:
+        raise ValueError("bias must have 3 heads D elements")
+    st = load_library().skiparse_qkv_rope(_ptr(x), _ptr(w), _ptr(bias), _ptr(q), _ptr(k), _ptr(v), B, N, C, heads,
+                                          D, T, H, W, float(rope_theta), _stream(stream))
+    _check(st, "skiparse_qkv_rope")
 
 
 def skiparse_debug_exp2(x, y, mufu=False, stream=None):

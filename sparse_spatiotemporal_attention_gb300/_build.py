@@ -21,7 +21,7 @@ LIB = os.path.join(LIBDIR, "libskiparse.so")
 SYNTH_SRC = os.path.join(CSRC, "synthetic_gen.c")
 SYNTH_LIB = os.path.join(LIBDIR, "libsynthetic.so")
 SOURCES = ["skiparse_host.cu", "skiparse_fwd.cu", "skiparse_fwd8.cu", "skiparse_bwd.cu", "skiparse_bwd_rows.cu",
-           "skiparse_debug.cu", "skiparse_noalloc.cu"]
+           "skiparse_debug.cu", "skiparse_noalloc.cu", "skiparse_proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

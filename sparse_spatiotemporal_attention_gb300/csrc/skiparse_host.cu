@@ -237,6 +237,21 @@ bool encode_scope_map(CUtensorMap* m, const void* base, const Geom& g) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// 2-D bf16 tensor map over a row-major (rows, cols) matrix: boxes of 64 columns
+// (128 bytes, 128-byte swizzle) x box_rows rows; reads past either edge fill zeros.
+bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D byte tensor map, 128 x 128-byte boxes with 128-byte swizzle: dims
 // (d0 innermost, d1, d2), byte strides s1, s2.
 bool encode_bytes_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
@@ -341,6 +356,7 @@ const char* skiparse_kernel_name(int id) {
     case 5: return "skiparse_fwd8_vmax_kernel";
     case 6: return "skiparse_fwd8_prep_kernel";
     case 7: return "skiparse_fwd8_kernel";
+    case 8: return "skiparse_qkv_rope_kernel";
     default: return "unknown";
   }
 }
@@ -623,6 +639,64 @@ int skiparse_debug_exp2(const float* x, float* y, int n, int mufu, cudaStream_t 
   const int st = device_info(dev);
   if (st != SKIPARSE_OK) return st;
   return launch_status(launch_debug_exp2(x, y, n, mufu, stream));
+}
+
+int skiparse_qkv_rope(const void* x, const void* w, const void* bias, void* q, void* k, void* v, int B, int N,
+                      int C, int heads, int D, int T, int H, int W, float rope_theta, cudaStream_t stream) {
+  if (B < 0 || N < 0 || C < 0 || heads < 0 || D < 0 || T < 0 || H < 0 || W < 0) return SKIPARSE_ERR_INVALID_ARG;
+  if (!(rope_theta > 0.0f) || !std::isfinite(rope_theta)) return SKIPARSE_ERR_INVALID_ARG;
+  if ((long long)T * H * W != (long long)N) return SKIPARSE_ERR_SHAPE;
+  if (B == 0 || N == 0 || heads == 0) return SKIPARSE_OK;
+  if (D != 64 && D != 128) return SKIPARSE_ERR_UNSUPPORTED;
+  const long long hd = (long long)heads * D;
+  if (C < 8 || C % 8 != 0 || hd % 128 != 0) return SKIPARSE_ERR_UNSUPPORTED;
+  const long long entries = (long long)T * (D / 8) + (long long)H * (3 * D / 16) + (long long)W * (3 * D / 16);
+  if (entries > kMaxRopeEntries) return SKIPARSE_ERR_UNSUPPORTED;
+  const long long M = (long long)B * N;
+  if (M >= (1ll << 31) || 3 * hd >= (1ll << 31) || M * hd > (1ll << 46) || M * C > (1ll << 46))
+    return SKIPARSE_ERR_UNSUPPORTED;
+  if (!x || !w || !q || !k || !v) return SKIPARSE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      (bias && !aligned16(bias)))
+    return SKIPARSE_ERR_ALIGNMENT;
+  const size_t out_bytes = (size_t)(M * hd) * 2;
+  if (any_alias({{q, out_bytes}, {k, out_bytes}, {v, out_bytes}},
+                {{x, (size_t)(M * C) * 2}, {w, (size_t)(3 * hd * C) * 2}, {bias, bias ? (size_t)(3 * hd) * 2 : 0}}))
+    return SKIPARSE_ERR_ALIAS;
+  DeviceInfo dev;
+  int st = device_info(dev);
+  if (st != SKIPARSE_OK) return st;
+  const int bn = proj_bn((int)hd);
+  const size_t header = proj_header_bytes((int)entries);
+  const size_t per_stage = proj_stage_bytes(bn);
+  long long stages = ((long long)dev.smem_optin - (long long)header) / (long long)per_stage;
+  if (stages > 4) stages = 4;
+  if (stages < 2) return SKIPARSE_ERR_UNSUPPORTED;
+  Shape s{B, heads, N, D, T, H, W, 1, SKIPARSE_SINGLE, false, M * hd, (int)entries};
+  ProjParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.rope = make_rope(s, rope_theta);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.q = static_cast<uint16_t*>(q);
+  p.k = static_cast<uint16_t*>(k);
+  p.v = static_cast<uint16_t*>(v);
+  p.err = dev.err_word;
+  p.fN = make_fastdiv(N);
+  p.M = (int)M;
+  p.C = C;
+  p.hd = (int)hd;
+  p.D = D;
+  p.m_tiles = (int)((M + 127) / 128);
+  p.n_tiles = (int)(3 * hd / bn);
+  p.k_steps = (C + 63) / 64;
+  p.stages = (int)stages;
+  p.stage_off = (int)header;
+  if (!encode_bf16_2d(&p.tm_x, x, (uint64_t)C, (uint64_t)M, 128) ||
+      !encode_bf16_2d(&p.tm_w, w, (uint64_t)C, (uint64_t)(3 * hd), (uint32_t)bn))
+    return SKIPARSE_ERR_LAUNCH;
+  const long long tiles = (long long)p.m_tiles * p.n_tiles;
+  const int grid = (int)(tiles < dev.sms ? tiles : dev.sms);
+  return launch_status(traced_launch(8, stream, [&] { return launch_proj(p, bn, grid, stream); }));
 }
 
 int skiparse_device_error(int* detail) {

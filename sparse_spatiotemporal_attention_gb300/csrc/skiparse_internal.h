@@ -16,6 +16,7 @@ namespace skp {
 enum : int {
   ERR_KERNEL_FWD = 0x1000,
   ERR_KERNEL_BWD = 0x2000,
+  ERR_KERNEL_PROJ = 0x3000,
   ERR_SMEM_ALIGN = 0x7001,
 };
 
@@ -82,6 +83,24 @@ struct Fwd8Params {
   float scale_log2;               // log2(e) / sqrt(D)
 };
 
+// Q/K/V projection with the RoPE epilogue: [q | k | v] = x W^T (+ bias), RoPE on q and k.
+struct ProjParams {
+  CUtensorMap tm_x;               // x bf16 (M rows, C channels): boxes of 64 channels x 128 rows
+  CUtensorMap tm_w;               // W bf16 (3 heads D rows, C channels): boxes of 64 channels x BN rows
+  RopeParams rope;
+  const uint16_t* bias;           // bf16 [3 heads D] or nullptr
+  uint16_t* q;                    // bf16 (B, N, heads, D) outputs
+  uint16_t* k;
+  uint16_t* v;
+  int* err;
+  FastDiv fN;                     // row -> token
+  int M, C, hd, D;                // rows B N, channels, heads D, head dim
+  int m_tiles, n_tiles;           // 128-row tiles, BN-column tiles
+  int k_steps;                    // ceil(C / 64)
+  int stages;                     // pipeline depth (2 .. 4)
+  int stage_off;                  // byte offset of stage 0 in shared memory (1024-aligned)
+};
+
 struct DebugParams {
   Geom g;
   RopeParams rope;
@@ -117,6 +136,11 @@ int fwd8_units(const Geom& g);
 cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream);
 cudaError_t launch_fwd8_prep(const Fwd8Params& p, int sms, cudaStream_t stream);
 cudaError_t launch_fwd8(const Fwd8Params& p, int grid, cudaStream_t stream);
+
+int proj_bn(int hd);
+size_t proj_stage_bytes(int bn);
+size_t proj_header_bytes(int rope_entries);
+cudaError_t launch_proj(const ProjParams& p, int bn, int grid, cudaStream_t stream);
 
 size_t bwd_main_smem_bytes(int D);
 bool bwd_uses_tile_kernel(int D);

@@ -1,0 +1,244 @@
+// Q/K/V projection with the RoPE epilogue: the step before the attention in
+// Open-Sora Plan's Skiparse listings ("Open-Sora Plan" docs, "Skiparse
+// Attention", single- and group-skip implementations: q, k, v = Q(x), K(x),
+// V(x), then RoPE on q and k at each token's original position).
+//
+//   [q | k | v] = x W^T (+ bias)       x (B N, C) bf16, W (3 heads D, C) bf16
+//   q, k <- RoPE(t, h, w) in fp32 on the accumulator, one bf16 rounding
+//
+// skiparse_qkv_rope_kernel<BN>: persistent, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: 64-channel stages of a 128-row x tile and a
+//               BN-row W tile (128-byte swizzle), up to 4 stages in flight;
+//   warp 1      MMA issuer (converged, lane 0 issues): 4 tcgen05 MMAs
+//               M=128 N=BN K=16 per stage into one of two TMEM accumulators;
+//   warps 2-5   epilogue: each thread one output row (its TMEM lane); bias,
+//               RoPE from the shared-memory cos/sin table for the q and k
+//               column ranges, bf16, stores into (B, N, heads, D).
+// Two accumulators of BN columns let a tile's epilogue overlap the next
+// tile's main loop. Tiles run n-block fastest, so the CTAs of one wave share a
+// few 128-row x blocks (read from HBM once) while W stays in L2.
+#include "skiparse_internal.h"
+
+namespace skp {
+
+namespace {
+
+constexpr int kProjThreads = 192;
+constexpr int kPBM = 128;                 // output rows per tile
+constexpr int kPBK = 64;                  // channels per stage (one 128-byte row of bf16)
+constexpr int kABytes = kPBM * kPBK * 2;  // 16 KB
+constexpr int kMaxStages = 4;
+
+// barrier indices
+enum : int {
+  P_FULL0 = 0,                       // .. +3: stage landed (TMA -> MMA)
+  P_EMPTY0 = 4,                      // .. +3: stage consumed (MMA commit -> TMA)
+  P_ACCF0 = 8,                       // .. +1: accumulator ready (MMA commit -> epilogue)
+  P_ACCE0 = 10,                      // .. +1: accumulator drained (4 epilogue warps -> MMA)
+  P_FINAL = 12,                      // every MMA done (teardown)
+  P_NBARS = 13,
+};
+
+}  // namespace
+
+template <int BN>
+__global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(const __grid_constant__ ProjParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int kBBytes = BN * kPBK * 2;
+  constexpr int kStage = kABytes + kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
+  int* abort_flag = reinterpret_cast<int*>(smem + 264);
+  float2* tab = reinterpret_cast<float2*>(smem + 1024);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  const uint32_t st0 = smem_u32(smem) + (uint32_t)p.stage_off;
+  if ((st0 & 1023u) != 0 || p.stages < 2 || p.stages > kMaxStages) {   // swizzled stages: 1024-byte alignment
+    if (tid == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
+    return;
+  }
+  const Ctl ctl{abort_flag, p.err};
+  constexpr int E = ERR_KERNEL_PROJ;
+  const int stages = p.stages;
+  const int n_total = p.m_tiles * p.n_tiles;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < P_NBARS; ++i) mbar_init(bar(i), (i == P_ACCE0 || i == P_ACCE0 + 1) ? 4u : 1u);
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+  rope_build_table(tab, p.rope, tid, kProjThreads);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto warp_wait = [&](int i, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ctl, E + i)) != 0;
+  };
+  const bool leader = lane == 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (leader) {
+      tma_prefetch_map(&p.tm_x);
+      tma_prefetch_map(&p.tm_w);
+    }
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < n_total; t += gridDim.x) {
+      const int nb = t % p.n_tiles, mb = t / p.n_tiles;
+      for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
+        const int s = (int)(it % (uint32_t)stages);
+        const uint32_t use = it / (uint32_t)stages;
+        if (use > 0 && !warp_wait(P_EMPTY0 + s, (use - 1) & 1)) { ok = false; break; }
+        if (leader) {
+          const uint32_t a = st0 + (uint32_t)(s * kStage);
+          mbar_expect_tx(bar(P_FULL0 + s), kStage);
+          tma_load_2d(a, &p.tm_x, bar(P_FULL0 + s), ks * kPBK, mb * kPBM);
+          tma_load_2d(a + kABytes, &p.tm_w, bar(P_FULL0 + s), ks * kPBK, nb * BN);
+        }
+        __syncwarp();
+      }
+    }
+    // copies still in flight land before the CTA releases its shared memory
+    if (leader) {
+      for (int s = 0; s < stages; ++s) {
+        const uint32_t issued = it > (uint32_t)s ? (it - 1 - (uint32_t)s) / (uint32_t)stages + 1 : 0;
+        if (issued) mbar_drain(bar(P_FULL0 + s), (issued - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kId = idesc_bf16(kPBM, BN, false, false);
+    uint32_t it = 0;
+    int tl = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < n_total; t += gridDim.x, ++tl) {
+      const int a = tl & 1;
+      const uint32_t use = (uint32_t)tl >> 1;
+      if (use > 0 && !warp_wait(P_ACCE0 + a, (use - 1) & 1)) break;
+      tc_fence_after();
+      const uint32_t dacc = tmem + (uint32_t)(a * BN);
+      for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
+        const int s = (int)(it % (uint32_t)stages);
+        if (!warp_wait(P_FULL0 + s, (it / (uint32_t)stages) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
+          const uint32_t sa = st0 + (uint32_t)(s * kStage);
+          const uint64_t da = desc_kmajor(sa, 0), db = desc_kmajor(sa + kABytes, 0);
+#pragma unroll
+          for (int kk = 0; kk < kPBK / 16; ++kk)
+            mma_ss(dacc, kmajor_step(da, kk), kmajor_step(db, kk), kId, (ks > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(P_EMPTY0 + s));
+          if (ks + 1 == p.k_steps) tc_commit(bar(P_ACCF0 + a));
+        }
+        __syncwarp();
+      }
+    }
+    if (leader) {
+      tc_commit(bar(P_FINAL));
+      mbar_drain(bar(P_FINAL), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2-5
+    const int quarter = warp & 3;                          // TMEM lanes 32 quarter .. +31
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    int tl = 0;
+    for (int t = blockIdx.x; t < n_total; t += gridDim.x, ++tl) {
+      const int a = tl & 1;
+      if (!mbar_wait(bar(P_ACCF0 + a), ((uint32_t)tl >> 1) & 1, ctl, E + P_ACCF0 + a)) break;
+      tc_fence_after();
+      const int nb = t % p.n_tiles, mb = t / p.n_tiles;
+      const int row = mb * kPBM + quarter * 32 + lane;     // b N + token
+      const bool row_ok = row < p.M;
+      const int n0 = nb * BN;                              // column in [q | k | v]
+      const int region = n0 / p.hd;                        // 0 q, 1 k, 2 v (BN divides heads D)
+      const int col0 = n0 - region * p.hd;                 // column in (heads, D)
+      uint16_t* dst = region == 0 ? p.q : (region == 1 ? p.k : p.v);
+      int tt = 0, hh = 0, ww = 0;
+      if (row_ok && region < 2) {
+        const int tok = row - fdiv(row, p.fN) * p.fN.d;
+        token_coords(p.rope, tok, tt, hh, ww);
+      }
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float x[32];
+        tmem_ld32(tmem + lane_base + (uint32_t)(a * BN + c * 32), x);
+        if (p.bias) {
+          const uint4* bp = reinterpret_cast<const uint4*>(p.bias + n0 + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 u = __ldg(bp + q4);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              x[8 * q4 + 2 * e] += bf16lo(w4[e]);
+              x[8 * q4 + 2 * e + 1] += bf16hi(w4[e]);
+            }
+          }
+        }
+        if (region < 2) {
+          const int d0 = (col0 + c * 32) % p.D;            // channel of x[0] within its head
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const PairSel sel = pair_select(p.rope, d0 / 2 + e);
+            const float2 cs = tab[pair_index(sel, tt, hh, ww)];
+            const float2 r = rope_rotate(x[2 * e], x[2 * e + 1], cs);
+            x[2 * e] = r.x;
+            x[2 * e + 1] = r.y;
+          }
+        }
+        if (row_ok) {
+          uint4* o = reinterpret_cast<uint4*>(dst + (size_t)row * p.hd + col0 + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16(x[8 * q4 + 0], x[8 * q4 + 1]);
+            w.y = pack_bf16(x[8 * q4 + 2], x[8 * q4 + 3]);
+            w.z = pack_bf16(x[8 * q4 + 4], x[8 * q4 + 5]);
+            w.w = pack_bf16(x[8 * q4 + 6], x[8 * q4 + 7]);
+            o[q4] = w;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (leader) mbar_arrive(bar(P_ACCE0 + a));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * BN);
+  }
+}
+
+int proj_bn(int hd) { return hd % 256 == 0 ? 256 : 128; }
+
+size_t proj_stage_bytes(int bn) { return (size_t)kABytes + (size_t)bn * kPBK * 2; }
+
+// barriers and flags (1 KB), then the RoPE table, rounded up to 1 KB
+size_t proj_header_bytes(int rope_entries) { return 1024 + (((size_t)rope_entries * 8 + 1023) & ~(size_t)1023); }
+
+cudaError_t launch_proj(const ProjParams& p, int bn, int grid, cudaStream_t stream) {
+  const size_t smem = (size_t)p.stage_off + (size_t)p.stages * proj_stage_bytes(bn);
+  cudaError_t e;
+  if (bn == 256) {
+    e = cudaFuncSetAttribute(skiparse_qkv_rope_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_qkv_rope_kernel<256><<<grid, kProjThreads, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(skiparse_qkv_rope_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    skiparse_qkv_rope_kernel<128><<<grid, kProjThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace skp
