@@ -21,6 +21,10 @@
  *   - 3D RoPE: the D channels of a head are split in order into D/4 channels
  *     for t, 3D/8 for h and 3D/8 for w; within a chunk of d channels the pair
  *     (2j, 2j+1) is rotated by angle pos * rope_theta^(-2j/d).
+ *     rope_theta = 0 means no rotation: q and k arrive already rotated (for
+ *     instance by skiparse_qkv_rope, which applies the same RoPE in its
+ *     epilogue), and dq, dk are the gradients w.r.t. those rotated inputs.
+ *     Negative or non-finite rope_theta: SKIPARSE_ERR_INVALID_ARG.
  *   - Softmax scale is 1/sqrt(D); lse = max + ln(sum exp(scaled scores - max)).
  *   - All calls are asynchronous on `stream` and return a skiparse_status_t.
  *     Validation happens on the host before anything is launched; a call that
@@ -76,9 +80,11 @@ size_t skiparse_attn_fwd_workspace_bytes(int B, int heads, int N, int D, int T, 
  *   workspace scratch: device memory of at least
  *             skiparse_attn_fwd_workspace_bytes(...) bytes, 256-byte aligned,
  *             owned by the caller, contents ignored on entry; on return it
- *             holds the rotated q and k (row layout of q). Must not overlap
+ *             holds the rotated q and k (row layout of q); with rope_theta = 0
+ *             it is not written (the kernel gathers q and k directly and the
+ *             RoPE pass is skipped). Must not overlap
  *             any tensor. SKIPARSE_ERR_WORKSPACE when NULL or too small.
- *   D in {64, 128}; sparse_k >= 1; mode is a skiparse_mode_t; rope_theta > 0.
+ *   D in {64, 128}; sparse_k >= 1; mode is a skiparse_mode_t; rope_theta >= 0.
  *   Group mode needs sparse_k to divide 128.
  */
 int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -138,7 +144,9 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
  * counterpart in the pages; it saves the preprocess's re-read of q and k and
  * its rewrite of their rotated copies).
  *   fwd_workspace      in : the workspace skiparse_attn_fwd wrote for the same
- *                           sizes, mode and rope_theta, unchanged since;
+ *                           sizes, mode and rope_theta (> 0: with 0 the
+ *                           forward writes no rotated copies and this call
+ *                           returns SKIPARSE_ERR_INVALID_ARG), unchanged since;
  *                           fwd_workspace_bytes at least
  *                           skiparse_attn_fwd_workspace_bytes(...); read only.
  *   v, out, lse, dout  in : as for skiparse_attn_bwd.
@@ -202,7 +210,8 @@ int skiparse_attn_bwd_noalloc(const void* q, const void* k, const void* v, const
  * validation fails. Status: SKIPARSE_ERR_SHAPE if N != T H W;
  * SKIPARSE_ERR_UNSUPPORTED for D not in {64, 128}, C < 8 or C % 8 != 0,
  * heads D % 128 != 0, a RoPE table over 8192 pairs, or sizes past 2^31 rows;
- * SKIPARSE_ERR_INVALID_ARG for negative sizes, a non-positive rope_theta or a
+ * SKIPARSE_ERR_INVALID_ARG for negative sizes, a negative rope_theta (0: no
+ * rotation, q and k come out as plain projections) or a
  * NULL x / w / q / k / v; SKIPARSE_ERR_ALIGNMENT, SKIPARSE_ERR_ALIAS and
  * SKIPARSE_ERR_DEVICE as elsewhere. B, N or heads of 0: nothing to do, OK.
  */

@@ -160,7 +160,11 @@ def rope_chunks(D: int):
 
 def apply_rope(x: np.ndarray, T: int, H: int, W: int, theta: float, inverse: bool = False) -> np.ndarray:
     """Rotate x (B, N, heads, D) float64 by each token's (t, h, w); inverse=True
-    applies the transpose rotation (used for the gradient, R^T g)."""
+    applies the transpose rotation (used for the gradient, R^T g). theta = 0
+    means no rotation: q and k arrive already rotated (the listings rotate the
+    projections' outputs, so a projection with a RoPE epilogue has done it)."""
+    if theta == 0:
+        return np.array(x, dtype=np.float64, copy=True)
     B, N, nh, D = x.shape
     coords = token_coords(N, T, H, W)
     out = np.array(x, dtype=np.float64, copy=True)
@@ -326,6 +330,8 @@ def skiparse_scope(q, k, v, do, T, H, W, sparse_k, mode, b, head, s, theta=10000
 
 def _rope_rows(x, t, h, w, theta, inverse=False):
     """apply_rope for a list of rows x (n, D) whose coordinates are given."""
+    if theta == 0:
+        return np.array(x, dtype=np.float64, copy=True)
     D = x.shape[1]
     out = np.array(x, dtype=np.float64, copy=True)
     sign = -1.0 if inverse else 1.0

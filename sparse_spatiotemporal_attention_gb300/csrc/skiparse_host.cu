@@ -134,7 +134,7 @@ struct Shape {
 int check_shape(int B, int heads, int N, int D, int T, int H, int W, int k, int mode, float theta, Shape& s) {
   if (mode != SKIPARSE_SINGLE && mode != SKIPARSE_GROUP) return SKIPARSE_ERR_INVALID_ARG;
   if (B < 0 || heads < 0 || N < 0 || T < 0 || H < 0 || W < 0 || k < 1 || D < 0) return SKIPARSE_ERR_INVALID_ARG;
-  if (!(theta > 0.0f) || !std::isfinite(theta)) return SKIPARSE_ERR_INVALID_ARG;
+  if (!(theta >= 0.0f) || !std::isfinite(theta)) return SKIPARSE_ERR_INVALID_ARG;   // 0: no rotation
   if ((long long)T * H * W != (long long)N) return SKIPARSE_ERR_SHAPE;
   s = Shape{B, heads, N, D, T, H, W, k, mode, false, 0, 0};
   if (B == 0 || heads == 0 || N == 0) {
@@ -213,8 +213,10 @@ RopeParams make_rope(const Shape& s, float theta) {
   r.entries = s.rope_entries;
   r.fHW = make_fastdiv(s.H * s.W > 0 ? s.H * s.W : 1);
   r.fW = make_fastdiv(s.W > 0 ? s.W : 1);
-  for (int j = 0; j < r.dt2; ++j) r.om_t[j] = std::pow((double)theta, -2.0 * j / dt);
-  for (int j = 0; j < r.dh2; ++j) r.om_hw[j] = std::pow((double)theta, -2.0 * j / dh);
+  // rope_theta == 0 means q and k arrive rotated: every angle is 0 (cos 1, sin 0),
+  // which makes each rotation an exact identity
+  for (int j = 0; j < r.dt2; ++j) r.om_t[j] = theta == 0.0f ? 0.0 : std::pow((double)theta, -2.0 * j / dt);
+  for (int j = 0; j < r.dh2; ++j) r.om_hw[j] = theta == 0.0f ? 0.0 : std::pow((double)theta, -2.0 * j / dh);
   return r;
 }
 
@@ -395,7 +397,8 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   p.k = static_cast<const uint16_t*>(k);
   p.qr = reinterpret_cast<uint16_t*>(ws);
   p.kr = reinterpret_cast<uint16_t*>(ws + half);
-  if (!encode_scope_map(&p.tm_q, p.qr, p.g) || !encode_scope_map(&p.tm_k, p.kr, p.g) ||
+  const bool rotate = rope_theta != 0.0f;            // 0: q and k are already rotated
+  if (!encode_scope_map(&p.tm_q, rotate ? p.qr : q, p.g) || !encode_scope_map(&p.tm_k, rotate ? p.kr : k, p.g) ||
       !encode_scope_map(&p.tm_v, v, p.g))
     return SKIPARSE_ERR_LAUNCH;
   p.out = static_cast<uint16_t*>(out);
@@ -407,8 +410,10 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   long long rgrid = (rows + 15) / 16;                 // 8 warps per CTA, 2 rows per warp
   if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
-  st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, dev.sms, stream); }));
-  if (st != SKIPARSE_OK) return st;
+  if (rotate) {
+    st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, dev.sms, stream); }));
+    if (st != SKIPARSE_OK) return st;
+  }
   return launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));
 }
 
@@ -493,6 +498,8 @@ int bwd_impl(const void* q, const void* k, const void* qr_in, const void* kr_in,
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
   const bool saved = qr_in != nullptr;
+  const bool rotate = rope_theta != 0.0f;            // 0: q and k are already rotated
+  if (saved && !rotate) return SKIPARSE_ERR_INVALID_ARG;   // the forward wrote no rotated copies
   if (!v || !out || !lse || !dout || !dq || !dk || !dv) return SKIPARSE_ERR_INVALID_ARG;
   if (saved ? !kr_in : (!q || !k)) return SKIPARSE_ERR_INVALID_ARG;
   const void* qa = saved ? qr_in : q;
@@ -500,7 +507,7 @@ int bwd_impl(const void* q, const void* k, const void* qr_in, const void* kr_in,
   if (!aligned16(qa) || !aligned16(ka) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return SKIPARSE_ERR_ALIGNMENT;
-  const WsLayout w = ws_layout(s, !saved);
+  const WsLayout w = ws_layout(s, !saved && rotate);
   if (!workspace || workspace_bytes < w.total) return SKIPARSE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
   const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
@@ -523,9 +530,11 @@ int bwd_impl(const void* q, const void* k, const void* qr_in, const void* kr_in,
   p.dout = static_cast<const uint16_t*>(dout);
   p.lse = lse;
   p.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
-  p.rotate_qk = saved ? 0 : 1;
-  p.qr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(qr_in)) : reinterpret_cast<uint16_t*>(ws + w.qr);
-  p.kr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kr_in)) : reinterpret_cast<uint16_t*>(ws + w.kr);
+  p.rotate_qk = (!saved && rotate) ? 1 : 0;
+  p.qr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(qr_in))
+               : rotate ? reinterpret_cast<uint16_t*>(ws + w.qr) : const_cast<uint16_t*>(static_cast<const uint16_t*>(q));
+  p.kr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kr_in))
+               : rotate ? reinterpret_cast<uint16_t*>(ws + w.kr) : const_cast<uint16_t*>(static_cast<const uint16_t*>(k));
   p.lse2s = reinterpret_cast<float*>(ws + w.lse2s);
   p.delta_s = reinterpret_cast<float*>(ws + w.delta_s);
   p.rope_tab = reinterpret_cast<float2*>(ws + w.tab);
@@ -644,7 +653,7 @@ int skiparse_debug_exp2(const float* x, float* y, int n, int mufu, cudaStream_t 
 int skiparse_qkv_rope(const void* x, const void* w, const void* bias, void* q, void* k, void* v, int B, int N,
                       int C, int heads, int D, int T, int H, int W, float rope_theta, cudaStream_t stream) {
   if (B < 0 || N < 0 || C < 0 || heads < 0 || D < 0 || T < 0 || H < 0 || W < 0) return SKIPARSE_ERR_INVALID_ARG;
-  if (!(rope_theta > 0.0f) || !std::isfinite(rope_theta)) return SKIPARSE_ERR_INVALID_ARG;
+  if (!(rope_theta >= 0.0f) || !std::isfinite(rope_theta)) return SKIPARSE_ERR_INVALID_ARG;   // 0: no rotation
   if ((long long)T * H * W != (long long)N) return SKIPARSE_ERR_SHAPE;
   if (B == 0 || N == 0 || heads == 0) return SKIPARSE_OK;
   if (D != 64 && D != 128) return SKIPARSE_ERR_UNSUPPORTED;

@@ -62,7 +62,8 @@ def test_fwd_validation(lib):
     assert fwd(lib, mode=2) == INVALID
     assert fwd(lib, B=-1) == INVALID
     assert fwd(lib, sk=0) == INVALID
-    assert fwd(lib, theta=0.0) == INVALID
+    assert fwd(lib, theta=-1.0) == INVALID
+    assert fwd(lib, theta=0.0) == DEVICE                 # 0: q, k already rotated; valid, no GPU here
     assert fwd(lib, theta=float("inf")) == INVALID
     assert fwd(lib, N=255) == SHAPE                      # N != T*H*W
     assert fwd(lib, D=96) == UNSUP

@@ -121,3 +121,50 @@ def test_qkv_rope_rejects(env):
     with pytest.raises(skp.SkiparseError) as e:                 # heads D = 64 is not a multiple of 128
         skp.skiparse_qkv_rope(x, w1, None, q1, k1, v1, 4, 4, 4)
     assert e.value.status == -3
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["single", "group"])
+def test_projection_then_attention_without_rotation(env, mode):
+    """The listings' order with RoPE fused into the projection: x -> q~, k~, v
+    (skiparse_qkv_rope) -> attention with rope_theta = 0 (no second rotation),
+    forward and backward, against the oracle on the same bf16 q~, k~, v; and the
+    composition against the oracle run from x."""
+    import torch
+    from oracle import skiparse_oracle as O
+    skp, dev = env
+    B, T, H, W, C, heads, D, k = 1, 3, 8, 16, 128, 2, 128, 2
+    N = T * H * W
+    x, w, b = _inputs(B, N, C, heads, D, True)
+    xd, wd, bd = tl.to_device(x, dev), tl.to_device(w, dev), tl.to_device(b, dev)
+    q, kk, v = (torch.empty((B, N, heads, D), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    skp.skiparse_qkv_rope(xd, wd, bd, q, kk, v, T, H, W)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, heads, N), dtype=torch.float32, device=dev)
+    skp.skiparse_attn_fwd(q, kk, v, out, lse, T, H, W, k, mode, rope_theta=0.0)
+    do = tl.to_device(synthetic.normal_bf16_bits(4, (B, N, heads, D)), dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(skp.skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, k, mode), dtype=torch.uint8,
+                     device=dev)
+    skp.skiparse_attn_bwd(q, kk, v, out, lse, do, dq, dk, dv, ws, T, H, W, k, mode, rope_theta=0.0)
+    torch.cuda.synchronize()
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
+    qf, kf, vf, dof = (tl.host(t) for t in (q, kk, v, do))
+    rout, rlse = O.skiparse_fwd(qf, kf, vf, T, H, W, k, mode, theta=0.0)
+    tl.compare("out", tl.host(out), rout)
+    tl.compare("lse", tl.host(lse), rlse, tol_max=tl.TOL_LSE, tol_mean=tl.TOL_LSE, tol_rel=1e-3)
+    rdq, rdk, rdv = O.skiparse_bwd(qf, kf, vf, dof, T, H, W, k, mode, theta=0.0)[:3]
+    tl.compare("dq", tl.host(dq), rdq)
+    tl.compare("dk", tl.host(dk), rdk)
+    tl.compare("dv", tl.host(dv), rdv)
+    # the whole chain from x: the oracle projection (float64) then attention
+    f = [synthetic.bf16_bits_to_f64(a) for a in (x, w, b)]
+    pq, pk, pv = P.qkv_rope(f[0], f[1], f[2], heads, D, T, H, W)
+    cout, _ = O.skiparse_fwd(pq, pk, pv, T, H, W, k, mode, theta=0.0)
+    tl.compare("out (from x)", tl.host(out), cout)
+    # the saved backward has no rotated copies to read when nothing was rotated
+    fws = torch.empty(skp.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, k, mode), dtype=torch.uint8,
+                      device=dev)
+    with pytest.raises(skp.SkiparseError) as e:
+        skp.skiparse_attn_bwd_saved(fws, v, out, lse, do, dq, dk, dv, ws, T, H, W, k, mode, rope_theta=0.0)
+    assert e.value.status == -1

@@ -85,3 +85,24 @@ def test_row_sampler_matches_full():
         assert np.allclose(qs[i], q[bi, n], atol=1e-12)
         assert np.allclose(ks[i], k[bi, n], atol=1e-12)
         assert np.allclose(vs[i], v[bi, n], atol=1e-12)
+
+
+def test_prerotated_attention_equals_attention_with_rope():
+    """theta = 0 takes q and k as already rotated: attention on RoPE'd inputs
+    without rotation equals attention with rotation on the raw inputs, and the
+    gradients relate by R^T (dq = R^T dq_rot), as the chain rule demands."""
+    rs = np.random.RandomState(8)
+    B, heads, D, T, H, W, k = 1, 2, 16, 2, 4, 4, 2
+    N = T * H * W
+    q, kk, v, do = (rs.randn(B, N, heads, D) for _ in range(4))
+    assert np.array_equal(O.apply_rope(q, T, H, W, 0.0), q)
+    qr, kr = O.apply_rope(q, T, H, W, 10000.0), O.apply_rope(kk, T, H, W, 10000.0)
+    for mode in (O.SINGLE, O.GROUP):
+        o1, l1 = O.skiparse_fwd(q, kk, v, T, H, W, k, mode)
+        o0, l0 = O.skiparse_fwd(qr, kr, v, T, H, W, k, mode, theta=0.0)
+        assert np.allclose(o0, o1, atol=1e-12) and np.allclose(l0, l1, atol=1e-12)
+        dq1, dk1, dv1 = O.skiparse_bwd(q, kk, v, do, T, H, W, k, mode)[:3]
+        dq0, dk0, dv0 = O.skiparse_bwd(qr, kr, v, do, T, H, W, k, mode, theta=0.0)[:3]
+        assert np.allclose(O.apply_rope(dq0, T, H, W, 10000.0, inverse=True), dq1, atol=1e-12)
+        assert np.allclose(O.apply_rope(dk0, T, H, W, 10000.0, inverse=True), dk1, atol=1e-12)
+        assert np.allclose(dv0, dv1, atol=1e-12)
