@@ -106,6 +106,16 @@ __device__ __forceinline__ void token_coords(const RopeParams& r, int i, int& t,
 // Table entry e holds (cos, sin) of pos * omega for one axis, position and pair.
 // Angles are reduced modulo 2*pi in double before the float sincos, so large
 // positions lose no accuracy.
+__device__ __forceinline__ float2 rope_cos_sin(int pos, double om) {
+  const double a = (double)pos * om;
+  const double n = rint(a * 0.15915494309189535);          // a / (2 pi)
+  double red = fma(-n, 6.283185307179586, a);               // 2 pi, high part
+  red = fma(-n, 2.4492935982947064e-16, red);               // 2 pi, low part
+  float sn, cs;
+  sincosf((float)red, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
 __device__ __forceinline__ void rope_build_table(float2* tab, const RopeParams& r, int tid, int nthreads) {
   const int nt = r.T * r.dt2, nh = r.H * r.dh2;
   for (int e = tid; e < r.entries; e += nthreads) {
@@ -118,13 +128,7 @@ __device__ __forceinline__ void rope_build_table(float2* tab, const RopeParams& 
     } else {
       const int e2 = e - nt - nh; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j];
     }
-    const double a = (double)pos * om;
-    const double n = rint(a * 0.15915494309189535);          // a / (2 pi)
-    double red = fma(-n, 6.283185307179586, a);               // 2 pi, high part
-    red = fma(-n, 2.4492935982947064e-16, red);               // 2 pi, low part
-    float sn, cs;
-    sincosf((float)red, &sn, &cs);
-    tab[e] = make_float2(cs, sn);
+    tab[e] = rope_cos_sin(pos, om);
   }
 }
 

@@ -39,6 +39,35 @@ enum : int {
   P_NBARS = 13,
 };
 
+// The RoPE table with positions innermost: entry (axis, pair j, pos) at
+// base(axis) + j * npos(axis) + pos, so the 32 rows of an epilogue warp (32
+// consecutive tokens, usually consecutive w) read consecutive words. Same
+// values as rope_build_table (rope_cos_sin).
+__device__ __forceinline__ void proj_build_table(float2* tab, const RopeParams& r, int tid, int nthreads) {
+  const int nt = r.T * r.dt2, nh = r.H * r.dh2;
+  for (int e = tid; e < r.entries; e += nthreads) {
+    int pos, j, dst;
+    double om;
+    if (e < nt) {
+      pos = e / r.dt2; j = e - pos * r.dt2; om = r.om_t[j]; dst = j * r.T + pos;
+    } else if (e < nt + nh) {
+      const int e2 = e - nt; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j]; dst = nt + j * r.H + pos;
+    } else {
+      const int e2 = e - nt - nh; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j];
+      dst = nt + nh + j * r.W + pos;
+    }
+    tab[dst] = rope_cos_sin(pos, om);
+  }
+}
+
+// (cos, sin) of channel pair pp (0 .. D/2-1) at (t, h, w) in the table above
+__device__ __forceinline__ float2 proj_cs(const float2* tab, const RopeParams& r, int pp, int t, int h, int w) {
+  const int nt = r.T * r.dt2, nh = r.H * r.dh2;
+  if (pp < r.dt2) return tab[pp * r.T + t];
+  if (pp < r.dt2 + r.dh2) return tab[nt + (pp - r.dt2) * r.H + h];
+  return tab[nt + nh + (pp - r.dt2 - r.dh2) * r.W + w];
+}
+
 }  // namespace
 
 template <int BN>
@@ -69,7 +98,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(cons
     mbar_fence_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * BN);
-  rope_build_table(tab, p.rope, tid, kProjThreads);
+  proj_build_table(tab, p.rope, tid, kProjThreads);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -185,8 +214,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(cons
           const int d0 = (col0 + c * 32) % p.D;            // channel of x[0] within its head
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const PairSel sel = pair_select(p.rope, d0 / 2 + e);
-            const float2 cs = tab[pair_index(sel, tt, hh, ww)];
+            const float2 cs = proj_cs(tab, p.rope, d0 / 2 + e, tt, hh, ww);
             const float2 r = rope_rotate(x[2 * e], x[2 * e + 1], cs);
             x[2 * e] = r.x;
             x[2 * e + 1] = r.y;
