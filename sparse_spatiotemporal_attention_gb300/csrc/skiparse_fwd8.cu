@@ -37,7 +37,7 @@ namespace skp {
 namespace {
 
 constexpr int kD8 = 128;
-constexpr int kF8Threads = 320;
+constexpr int kF8Threads = 352;   // softmax 0-7, TMA 8, MMA issuers 9 (Q tile A) and 10 (Q tile B)
 constexpr int kPrepThreads = 256;
 constexpr float kE4M3Max = 448.0f;
 
@@ -50,18 +50,17 @@ __host__ __device__ constexpr size_t prep_table_bytes(int entries) { return ((si
 constexpr int kFmaPairs = SKP_FWD8_FMA_PAIRS;
 
 // 2^6 P = 2^(S * ck + off) for one softmax row held in registers (x, 128 keys;
-// off = 6 - m), as E4M3 codes into TMEM at taddr: keys 32c .. 32c+31 go to
-// columns 8c .. 8c+7, four codes per column. Returns the row sum of the
-// unquantized 2^6 P. With RAGGED, keys at or past `valid` get P = 0.
+// off = 6 - m), as E4M3 codes: word w of pk holds keys 4w .. 4w+3, the first
+// in the lowest byte. Returns the row sum of the unquantized 2^6 P. With
+// RAGGED, keys at or past `valid` get P = 0.
 template <bool RAGGED>
-__device__ __forceinline__ float softmax_p_e4m3(const float (&x)[kTile], uint32_t taddr, float ck, float off,
-                                                int valid) {
+__device__ __forceinline__ float softmax_p_e4m3(const float (&x)[kTile], uint32_t (&pk)[kTile / 4], float ck,
+                                                float off, int valid) {
   const unsigned long long ck2 = f2_pack(ck, ck);
   const unsigned long long off2 = f2_pack(off, off);
   unsigned long long acc2[2] = {0ull, 0ull};
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    uint32_t pk[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int k0 = c * 32 + 4 * e;
@@ -89,9 +88,8 @@ __device__ __forceinline__ float softmax_p_e4m3(const float (&x)[kTile], uint32_
       }
       acc2[0] = fadd2(acc2[0], f2_pack(p0, p1));
       acc2[1] = fadd2(acc2[1], f2_pack(p2, p3));
-      pk[e] = e4m3x4(p0, p1, p2, p3);
+      pk[c * 8 + e] = e4m3x4(p0, p1, p2, p3);
     }
-    tmem_st8(taddr + c * 8, pk);
   }
   float s0, s1, s2, s3;
   f2_unpack(acc2[0], s0, s1);
@@ -106,14 +104,18 @@ struct F8Layout {
   static constexpr int QB_OFF = QA_OFF + TILE;
   static constexpr int K_OFF = QB_OFF + TILE;
   static constexpr int V_OFF = K_OFF + 2 * TILE;
-  static constexpr int BYTES = V_OFF + 2 * TILE;
+  static constexpr int PA_OFF = V_OFF + 2 * TILE;   // P of Q tile A as E4M3 codes (A operand of P V)
+  static constexpr int PB_OFF = PA_OFF + TILE;
+  static constexpr int BYTES = PB_OFF + TILE;
 };
 
 enum F8Bar {
   E_QFULL, E_QEMPTY,
   E_KFULL0, E_KFULL1, E_KEMPTY0, E_KEMPTY1,
   E_VFULL0, E_VFULL1, E_VEMPTY0, E_VEMPTY1,
-  E_SFULL_A, E_SFULL_B, E_PFULL_A, E_PFULL_B, E_ODONE_A, E_ODONE_B, E_OEMPTY_A, E_OEMPTY_B, E_FINAL, E_NBARS
+  E_SFULL_A, E_SFULL_B, E_PFULL_A, E_PFULL_B, E_ODONE_A, E_ODONE_B, E_OEMPTY_A, E_OEMPTY_B,
+  E_SFREE_A, E_SFREE_B,   // the softmax warps hold S in registers: the next S may be written
+  E_FINAL, E_NBARS
 };
 
 }  // namespace
@@ -289,6 +291,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
   const uint32_t sQB = smem_u32(smem + Ly::QB_OFF);
   const uint32_t sK = smem_u32(smem + Ly::K_OFF);
   const uint32_t sV = smem_u32(smem + Ly::V_OFF);
+  const uint32_t sPA = smem_u32(smem + Ly::PA_OFF);
+  const uint32_t sPB = smem_u32(smem + Ly::PB_OFF);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   const Ctl ctl{abort_flag, p.err};
@@ -298,7 +302,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
 
   if (tid == 0) {
     *abort_flag = 0;
-    const uint32_t counts[E_NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 1, 4, 4, 1};
+    // stages shared by both Q tiles are released by a commit from each MMA issuer
+    const uint32_t counts[E_NBARS] = {1, 2, 1, 1, 2, 2, 1, 1, 2, 2, 1, 1, 4, 4, 1, 1, 4, 4, 4, 4, 2};
     for (int i = 0; i < E_NBARS; ++i) mbar_init(bar(i), counts[i]);
     mbar_fence_init();
   }
@@ -362,25 +367,40 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // One warp per Q tile X (9: A, 10: B), each issuing its own S_X and P_X V
+    // (two issuing threads keep the tensor core fed; one alone spends more
+    // cycles per MMA issuing than the MMA runs).
+    const int xb = warp - 9;
     constexpr uint32_t kId = idesc_e4m3(128, 128);
-    const uint64_t dQA = desc_kmajor(sQA, 0), dQB = desc_kmajor(sQB, 0);
+    const uint64_t dQ = desc_kmajor(xb ? sQB : sQA, 0);
     const uint64_t dK0 = desc_kmajor(sK, 0), dK1 = desc_kmajor(sK + Ly::TILE, 0);
     const uint64_t dV0 = desc_kmajor(sV, 0), dV1 = desc_kmajor(sV + Ly::TILE, 0);
+    const uint64_t dP = desc_kmajor(xb ? sPB : sPA, 0);
+    const uint32_t colS = xb ? 128u : 0u;
+    const uint32_t colO = 256u + (xb ? (uint32_t)D : 0u);
+    const int barSF = xb ? E_SFREE_B : E_SFREE_A;
+    const int barS = xb ? E_SFULL_B : E_SFULL_A;
+    const int barP = xb ? E_PFULL_B : E_PFULL_A;
+    const int barO = xb ? E_ODONE_B : E_ODONE_A;
+    const int barOE = xb ? E_OEMPTY_B : E_OEMPTY_A;
     // S_X = Q_X K_g^T (4 k-steps of 32 bytes)
-    auto issue_s = [&](uint64_t dq, uint32_t colS, int st) {
+    auto issue_s = [&](int st) {
       const uint64_t dk = st ? dK1 : dK0;
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) mma8_ss(tmem + colS, kmajor_step(dq, ks), kmajor_step(dk, ks), kId, ks > 0 ? 1u : 0u);
+      for (int ks = 0; ks < 4; ++ks) mma8_ss(tmem + colS, kmajor_step(dQ, ks), kmajor_step(dk, ks), kId, ks > 0 ? 1u : 0u);
     };
-    // O_X += P_X V_g: P_X as E4M3 in TMEM columns colS .. colS+31, V^T K-major
-    auto issue_pv = [&](uint32_t colS, uint32_t colO, int st, bool first) {
+    // O_X += P_X V_g: P_X as E4M3 codes in shared memory (K-major), V^T K-major
+    auto issue_pv = [&](int st, bool first) {
       const uint64_t dv = st ? dV1 : dV0;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma8_ts(tmem + colO, tmem + colS + ks * 8, kmajor_step(dv, ks), kId, (!first || ks > 0) ? 1u : 0u);
+        mma8_ss(tmem + colO, kmajor_step(dP, ks), kmajor_step(dv, ks), kId, (!first || ks > 0) ? 1u : 0u);
     };
+    // Per K step g of a unit: S_X(g+1) as soon as the softmax warps hold S_X(g)
+    // in registers, then P_X(g) V once P is in shared memory; the next S is
+    // computed while the softmax works on this one.
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
@@ -388,12 +408,11 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
       const int n = g.n_tiles;
       if (!warp_wait(E_QFULL, it & 1)) break;
       if (!warp_wait(E_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
+      if (g0 > 0 && !warp_wait(barSF, (g0 - 1) & 1)) break;
       tc_fence_after();
       if (leader) {
-        issue_s(dQA, 0, g0 & 1);
-        tc_commit(bar(E_SFULL_A));
-        issue_s(dQB, 128, g0 & 1);
-        tc_commit(bar(E_SFULL_B));
+        issue_s(g0 & 1);
+        tc_commit(bar(barS));
         tc_commit(bar(E_KEMPTY0 + (g0 & 1)));
         if (n == 1) tc_commit(bar(E_QEMPTY));
       }
@@ -402,40 +421,27 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
         const uint32_t gg = g0 + j;
         const int st = gg & 1;
         const uint32_t nn = gg >> 1;
-        if (j == 0 && it > 0 && !warp_wait(E_OEMPTY_A, (it - 1) & 1)) { ok = false; break; }
-        if (!warp_wait(E_PFULL_A, gg & 1)) { ok = false; break; }
-        if (!warp_wait(E_VFULL0 + st, nn & 1)) { ok = false; break; }
-        tc_fence_after();
-        if (leader) {
-          issue_pv(0, 256, st, j == 0);
-          tc_commit(bar(E_ODONE_A));
-        }
-        __syncwarp();
-        const bool more = j + 1 < n;
-        if (more) {
+        if (j + 1 < n) {
           const int st1 = (gg + 1) & 1;
+          if (!warp_wait(barSF, gg & 1)) { ok = false; break; }
           if (!warp_wait(E_KFULL0 + st1, ((gg + 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           if (leader) {
-            issue_s(dQA, 0, st1);
-            tc_commit(bar(E_SFULL_A));
-          }
-          __syncwarp();
-        }
-        if (j == 0 && it > 0 && !warp_wait(E_OEMPTY_B, (it - 1) & 1)) { ok = false; break; }
-        if (!warp_wait(E_PFULL_B, gg & 1)) { ok = false; break; }
-        tc_fence_after();
-        if (leader) {
-          issue_pv(128, 256 + D, st, j == 0);
-          tc_commit(bar(E_ODONE_B));
-          tc_commit(bar(E_VEMPTY0 + st));
-          if (more) {
-            const int st1 = (gg + 1) & 1;
-            issue_s(dQB, 128, st1);
-            tc_commit(bar(E_SFULL_B));
+            issue_s(st1);
+            tc_commit(bar(barS));
             tc_commit(bar(E_KEMPTY0 + st1));
             if (j + 2 == n) tc_commit(bar(E_QEMPTY));
           }
+          __syncwarp();
+        }
+        if (j == 0 && it > 0 && !warp_wait(barOE, (it - 1) & 1)) { ok = false; break; }
+        if (!warp_wait(barP, gg & 1)) { ok = false; break; }
+        if (!warp_wait(E_VFULL0 + st, nn & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (leader) {
+          issue_pv(st, j == 0);
+          tc_commit(bar(barO));
+          tc_commit(bar(E_VEMPTY0 + st));
         }
         __syncwarp();
       }
@@ -457,6 +463,9 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
     const int barP = wg ? E_PFULL_B : E_PFULL_A;
     const int barO = wg ? E_ODONE_B : E_ODONE_A;
     const int barOE = wg ? E_OEMPTY_B : E_OEMPTY_A;
+    const int barSF = wg ? E_SFREE_B : E_SFREE_A;
+    // this thread's row of P (128 codes, 128-byte swizzled rows as TMA writes them)
+    uint8_t* prow_smem = smem + (wg ? Ly::PB_OFF : Ly::PA_OFF) + r * 128;
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
@@ -478,6 +487,10 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
         // the whole S row in registers with one TMEM round trip
         float x[kTile];
         tmem_ld128(tmem + lane_base + colS, x);
+        // S is in registers: the MMA warp may write the next S over it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(barSF));
         const float mx = (valid == kTile ? row_max128<false>(x, valid) : row_max128<true>(x, valid)) * ck;
         float f = 1.f;
         bool rescale = false;
@@ -493,29 +506,40 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
             l *= f;
           }
         }
-        // 2^6 P as E4M3 over the S columns (the full-tile path has no masking)
-        l += valid == kTile ? softmax_p_e4m3<false>(x, tmem + lane_base + colS, ck, 6.0f - m, valid)
-                            : softmax_p_e4m3<true>(x, tmem + lane_base + colS, ck, 6.0f - m, valid);
-        if (rescale) {
-          // O *= 2^(m_old - m_new) before P V adds this tile (PV_X(g-1) is
-          // complete: S_X(g) was issued after it)
-          if (!mbar_wait(bar(barO), (gg - 1) & 1, ctl, E + barO)) {
-            tmem_st_wait();
-            ok = false;
-            break;
-          }
+        // 2^6 P as E4M3 codes in registers (the full-tile path has no masking)
+        uint32_t pk[kTile / 4];
+        l += valid == kTile ? softmax_p_e4m3<false>(x, pk, ck, 6.0f - m, valid)
+                            : softmax_p_e4m3<true>(x, pk, ck, 6.0f - m, valid);
+        // P_X(g-1) V has read the P buffer and added into O: the first PV of a
+        // unit follows the previous unit's epilogue, which waited for it
+        if (j > 0) {
+          if (!mbar_wait(bar(barO), (gg - 1) & 1, ctl, E + barO)) { ok = false; break; }
           tc_fence_after();
-          float o[kD8];
-          tmem_ld128(tmem + lane_base + colO, o);
-#pragma unroll
-          for (int c = 0; c < kD8 / 16; ++c) {
-            float oc[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) oc[e] = o[c * 16 + e] * f;
-            tmem_st16f(tmem + lane_base + colO + c * 16, oc);
-          }
         }
-        tmem_st_wait();
+        if (rescale) {
+          // O *= 2^(m_old - m_new) before P V adds this tile
+#pragma unroll 1
+          for (int c = 0; c < kD8 / 32; ++c) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + colO + c * 32, o);
+            float oc[16], od[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              oc[e] = o[e] * f;
+              od[e] = o[16 + e] * f;
+            }
+            tmem_st16f(tmem + lane_base + colO + c * 32, oc);
+            tmem_st16f(tmem + lane_base + colO + c * 32 + 16, od);
+          }
+          tmem_st_wait();
+        }
+        // codes of keys 16c .. 16c+15 are the row's 16-byte chunk c, stored at
+        // chunk c ^ (row mod 8) (128-byte swizzle)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow_smem + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(barP));
