@@ -701,10 +701,12 @@ int skiparse_qkv_rope(const void* x, const void* w, const void* bias, void* q, v
   p.stages = (int)stages;
   p.stage_off = (int)header;
   if (!encode_bf16_2d(&p.tm_x, x, (uint64_t)C, (uint64_t)M, 128) ||
-      !encode_bf16_2d(&p.tm_w, w, (uint64_t)C, (uint64_t)(3 * hd), (uint32_t)bn))
+      !encode_bf16_2d(&p.tm_w, w, (uint64_t)C, (uint64_t)(3 * hd), (uint32_t)bn / 2))
     return SKIPARSE_ERR_LAUNCH;
-  const long long tiles = (long long)p.m_tiles * p.n_tiles;
-  const int grid = (int)(tiles < dev.sms ? tiles : dev.sms);
+  // clusters of two CTAs, one per vertically adjacent pair of tiles
+  const long long pairs = (long long)((p.m_tiles + 1) / 2) * p.n_tiles;
+  const long long clusters = pairs < dev.sms / 2 ? pairs : dev.sms / 2;
+  const int grid = (int)(2 * clusters);
   return launch_status(traced_launch(8, stream, [&] { return launch_proj(p, bn, grid, stream); }));
 }
 

@@ -15,8 +15,12 @@
 //               RoPE from the shared-memory cos/sin table for the q and k
 //               column ranges, bf16, stores into (B, N, heads, D).
 // Two accumulators of BN columns let a tile's epilogue overlap the next
-// tile's main loop. Tiles run n-block fastest, so the CTAs of one wave share a
-// few 128-row x blocks (read from HBM once) while W stays in L2.
+// tile's main loop. CTAs run in clusters of two on vertically adjacent tiles
+// (the same BN columns of W): each loads its own x tile and one half of the W
+// tile, multicast into both, so a stage costs each SM 32 KB of L2 reads
+// instead of 48; a stage is refilled once both CTAs' MMAs have read it. Tile
+// pairs run n-block fastest, so a wave shares a few x row blocks (read from
+// HBM once) while W stays in L2.
 #include "skiparse_internal.h"
 
 namespace skp {
@@ -32,7 +36,7 @@ constexpr int kMaxStages = 4;
 // barrier indices
 enum : int {
   P_FULL0 = 0,                       // .. +3: stage landed (TMA -> MMA)
-  P_EMPTY0 = 4,                      // .. +3: stage consumed (MMA commit -> TMA)
+  P_EMPTY0 = 4,                      // .. +3: stage consumed by both CTAs (MMA commits -> TMA)
   P_ACCF0 = 8,                       // .. +1: accumulator ready (MMA commit -> epilogue)
   P_ACCE0 = 10,                      // .. +1: accumulator drained (4 epilogue warps -> MMA)
   P_FINAL = 12,                      // every MMA done (teardown)
@@ -71,7 +75,8 @@ __device__ __forceinline__ float2 proj_cs(const float2* tab, const RopeParams& r
 }  // namespace
 
 template <int BN>
-__global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(const __grid_constant__ ProjParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
+    skiparse_qkv_rope_kernel(const __grid_constant__ ProjParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr int kBBytes = BN * kPBK * 2;
   constexpr int kStage = kABytes + kBBytes;
@@ -90,17 +95,27 @@ __global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(cons
   const Ctl ctl{abort_flag, p.err};
   constexpr int E = ERR_KERNEL_PROJ;
   const int stages = p.stages;
-  const int n_total = p.m_tiles * p.n_tiles;
+  const int rank = (int)cluster_ctarank();
+  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int n_total = ((p.m_tiles + 1) >> 1) * p.n_tiles;     // tile pairs
+  constexpr int kBHalf = BN / 2 * kPBK * 2;                    // this CTA's share of a W tile
+  constexpr uint16_t kBoth = 3;
 
   if (tid == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < P_NBARS; ++i) mbar_init(bar(i), (i == P_ACCE0 || i == P_ACCE0 + 1) ? 4u : 1u);
+    for (int i = 0; i < P_NBARS; ++i) {
+      uint32_t cnt = 1;
+      if (i == P_ACCE0 || i == P_ACCE0 + 1) cnt = 4;
+      if (i >= P_EMPTY0 && i < P_EMPTY0 + 4) cnt = 2;
+      mbar_init(bar(i), cnt);
+    }
     mbar_fence_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * BN);
   proj_build_table(tab, p.rope, tid, kProjThreads);
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();        // both CTAs' barriers exist before any multicast targets them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto warp_wait = [&](int i, uint32_t parity) -> bool {
@@ -116,26 +131,31 @@ __global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(cons
     }
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < n_total; t += gridDim.x) {
-      const int nb = t % p.n_tiles, mb = t / p.n_tiles;
+    for (int t = cid; ok && t < n_total; t += n_clusters) {
+      const int nb = t % p.n_tiles, mb = 2 * (t / p.n_tiles) + rank;   // mb may be past the rows: zero fill
       for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
         const int s = (int)(it % (uint32_t)stages);
         const uint32_t use = it / (uint32_t)stages;
         if (use > 0 && !warp_wait(P_EMPTY0 + s, (use - 1) & 1)) { ok = false; break; }
         if (leader) {
           const uint32_t a = st0 + (uint32_t)(s * kStage);
-          mbar_expect_tx(bar(P_FULL0 + s), kStage);
+          mbar_expect_tx(bar(P_FULL0 + s), kStage);      // own x tile, both W halves
           tma_load_2d(a, &p.tm_x, bar(P_FULL0 + s), ks * kPBK, mb * kPBM);
-          tma_load_2d(a + kABytes, &p.tm_w, bar(P_FULL0 + s), ks * kPBK, nb * BN);
+          tma_load_2d_mc(a + kABytes + (uint32_t)(rank * kBHalf), &p.tm_w, bar(P_FULL0 + s), ks * kPBK,
+                         nb * BN + rank * (BN / 2), kBoth);
         }
         __syncwarp();
       }
     }
-    // copies still in flight land before the CTA releases its shared memory
+    // copies into this CTA land, and both CTAs' MMA commits for every stage
+    // arrive, before the cluster may release its shared memory
     if (leader) {
       for (int s = 0; s < stages; ++s) {
         const uint32_t issued = it > (uint32_t)s ? (it - 1 - (uint32_t)s) / (uint32_t)stages + 1 : 0;
-        if (issued) mbar_drain(bar(P_FULL0 + s), (issued - 1) & 1);
+        if (issued) {
+          mbar_drain(bar(P_FULL0 + s), (issued - 1) & 1);
+          mbar_drain(bar(P_EMPTY0 + s), (issued - 1) & 1);
+        }
       }
     }
     __syncwarp();
@@ -145,7 +165,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(cons
     uint32_t it = 0;
     int tl = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < n_total; t += gridDim.x, ++tl) {
+    for (int t = cid; ok && t < n_total; t += n_clusters, ++tl) {
       const int a = tl & 1;
       const uint32_t use = (uint32_t)tl >> 1;
       if (use > 0 && !warp_wait(P_ACCE0 + a, (use - 1) & 1)) break;
@@ -161,7 +181,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(cons
 #pragma unroll
           for (int kk = 0; kk < kPBK / 16; ++kk)
             mma_ss(dacc, kmajor_step(da, kk), kmajor_step(db, kk), kId, (ks > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(P_EMPTY0 + s));
+          tc_commit_mc(bar(P_EMPTY0 + s), kBoth);       // the stage is free in both CTAs' view
           if (ks + 1 == p.k_steps) tc_commit(bar(P_ACCF0 + a));
         }
         __syncwarp();
@@ -177,11 +197,11 @@ __global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(cons
     const int quarter = warp & 3;                          // TMEM lanes 32 quarter .. +31
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     int tl = 0;
-    for (int t = blockIdx.x; t < n_total; t += gridDim.x, ++tl) {
+    for (int t = cid; t < n_total; t += n_clusters, ++tl) {
       const int a = tl & 1;
       if (!mbar_wait(bar(P_ACCF0 + a), ((uint32_t)tl >> 1) & 1, ctl, E + P_ACCF0 + a)) break;
       tc_fence_after();
-      const int nb = t % p.n_tiles, mb = t / p.n_tiles;
+      const int nb = t % p.n_tiles, mb = 2 * (t / p.n_tiles) + rank;
       const int row = mb * kPBM + quarter * 32 + lane;     // b N + token
       const bool row_ok = row < p.M;
       const int n0 = nb * BN;                              // column in [q | k | v]
@@ -241,6 +261,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) skiparse_qkv_rope_kernel(cons
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();        // neither CTA leaves while the other may still write into it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 2 * BN);
@@ -254,19 +275,33 @@ size_t proj_stage_bytes(int bn) { return (size_t)kABytes + (size_t)bn * kPBK * 2
 // barriers and flags (1 KB), then the RoPE table, rounded up to 1 KB
 size_t proj_header_bytes(int rope_entries) { return 1024 + (((size_t)rope_entries * 8 + 1023) & ~(size_t)1023); }
 
+namespace {
+
+// Launch with at most as many CTA pairs as can be resident at once (an SM
+// left over in a GPC cannot host half a pair).
+template <class K>
+cudaError_t launch_pairs(K kernel, const ProjParams& p, int grid, size_t smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kProjThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters > 0 && 2 * clusters < grid)
+    grid = 2 * clusters;
+  cudaGetLastError();
+  kernel<<<grid, kProjThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_proj(const ProjParams& p, int bn, int grid, cudaStream_t stream) {
   const size_t smem = (size_t)p.stage_off + (size_t)p.stages * proj_stage_bytes(bn);
-  cudaError_t e;
-  if (bn == 256) {
-    e = cudaFuncSetAttribute(skiparse_qkv_rope_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_qkv_rope_kernel<256><<<grid, kProjThreads, smem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(skiparse_qkv_rope_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_qkv_rope_kernel<128><<<grid, kProjThreads, smem, stream>>>(p);
-  }
-  return cudaGetLastError();
+  if (bn == 256) return launch_pairs(skiparse_qkv_rope_kernel<256>, p, grid, smem, stream);
+  return launch_pairs(skiparse_qkv_rope_kernel<128>, p, grid, smem, stream);
 }
 
 }  // namespace skp
