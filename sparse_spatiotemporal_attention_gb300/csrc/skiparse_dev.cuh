@@ -242,6 +242,51 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl c, 
   return mbar_wait_slow(bar, parity, c, code);
 }
 
+// The same waits for barriers that also receive arrivals from the other CTA of
+// a cluster (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+static __device__ __noinline__ bool mbar_wait_cl_slow(uint32_t bar, uint32_t parity, Ctl c, int code) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (*c.abort) return false;
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait_cl(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *c.abort = 1;
+      atomicCAS(c.err, 0, code);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, Ctl c, int code) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  return mbar_wait_cl_slow(bar, parity, c, code);
+}
+static __device__ __noinline__ void mbar_drain_cl(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cl(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// Shared-memory address `addr` of this CTA as seen in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+// Arrive on a barrier of another CTA of the cluster (address from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+
 // Bounded wait that ignores the abort flag: used only to drain copies and MMAs
 // still in flight before a CTA releases its shared memory and TMEM.
 static __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
@@ -266,6 +311,16 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* m) {
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];"
+      :: "r"(dst), "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Load into this CTA's shared memory, completing on a barrier that may be in
+// the other CTA of the pair (`bar` a shared::cluster address from mapa_shared).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];"
       :: "r"(dst), "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
@@ -374,6 +429,29 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                :: "r"(bar) : "memory");
+}
+
+// CTA-pair (cta_group::2) forms: one M = 256 MMA over the two CTAs' shared
+// memory (each CTA holds its 128 rows of A and its half of B's rows, at the
+// same offsets) into each CTA's own TMEM, issued by the pair's first CTA.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_pair_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// Arrive on the barrier at the same offset in every CTA in `mask` once the
+// pair MMAs this thread issued are done.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               :: "r"(bar), "h"(mask) : "memory");
 }
 
 // As tc_commit, arriving on the barrier at the same offset in every CTA of the

@@ -679,7 +679,7 @@ int skiparse_qkv_rope(const void* x, const void* w, const void* bias, void* q, v
   const size_t header = proj_header_bytes((int)entries);
   const size_t per_stage = proj_stage_bytes(bn);
   long long stages = ((long long)dev.smem_optin - (long long)header) / (long long)per_stage;
-  if (stages > 4) stages = 4;
+  if (stages > 6) stages = 6;
   if (stages < 2) return SKIPARSE_ERR_UNSUPPORTED;
   Shape s{B, heads, N, D, T, H, W, 1, SKIPARSE_SINGLE, false, M * hd, (int)entries};
   ProjParams p;

@@ -6,19 +6,22 @@
 //   [q | k | v] = x W^T (+ bias)       x (B N, C) bf16, W (3 heads D, C) bf16
 //   q, k <- RoPE(t, h, w) in fp32 on the accumulator, one bf16 rounding
 //
-// skiparse_qkv_rope_kernel<BN>: persistent, one CTA per SM, 6 warps:
-//   warp 0      TMA producer: 64-channel stages of a 128-row x tile and a
-//               BN-row W tile (128-byte swizzle), up to 4 stages in flight;
-//   warp 1      MMA issuer (converged, lane 0 issues): 4 tcgen05 MMAs
-//               M=128 N=BN K=16 per stage into one of two TMEM accumulators;
+// skiparse_qkv_rope_kernel<BN>: persistent CTA pairs (clusters of two, one
+// CTA per SM); a pair computes a 256-row x BN-column output tile with 2-SM
+// MMAs (cta_group::2, M = 256: each CTA's 128 rows land in its own TMEM).
+// Per CTA, 6 warps:
+//   warp 0      TMA producer: 64-channel stages of the CTA's 128-row x tile
+//               and its half (BN/2 rows) of the W tile, 128-byte swizzle, up
+//               to 6 stages of 32 KB in flight;
+//   warp 1      CTA 0: MMA issuer (converged, lane 0 issues 4 pair MMAs
+//               M=256 N=BN K=16 per stage into one of two accumulators);
+//               both CTAs' copies of a stage complete on CTA 0's barrier;
 //   warps 2-5   epilogue: each thread one output row (its TMEM lane); bias,
 //               RoPE from the shared-memory cos/sin table for the q and k
 //               column ranges, bf16, stores into (B, N, heads, D).
 // Two accumulators of BN columns let a tile's epilogue overlap the next
-// tile's main loop. CTAs run in clusters of two on vertically adjacent tiles
-// (the same BN columns of W): each loads its own x tile and one half of the W
-// tile, multicast into both, so a stage costs each SM 32 KB of L2 reads
-// instead of 48; a stage is refilled once both CTAs' MMAs have read it. Tile
+// tile's main loop. A stage costs each SM 32 KB of L2 reads per 512 tensor
+// cycles (half of W per CTA), and one thread issues the MMAs of two SMs. Tile
 // pairs run n-block fastest, so a wave shares a few x row blocks (read from
 // HBM once) while W stays in L2.
 #include "skiparse_internal.h"
@@ -31,16 +34,16 @@ constexpr int kProjThreads = 192;
 constexpr int kPBM = 128;                 // output rows per tile
 constexpr int kPBK = 64;                  // channels per stage (one 128-byte row of bf16)
 constexpr int kABytes = kPBM * kPBK * 2;  // 16 KB
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 
 // barrier indices
 enum : int {
-  P_FULL0 = 0,                       // .. +3: stage landed (TMA -> MMA)
-  P_EMPTY0 = 4,                      // .. +3: stage consumed by both CTAs (MMA commits -> TMA)
-  P_ACCF0 = 8,                       // .. +1: accumulator ready (MMA commit -> epilogue)
-  P_ACCE0 = 10,                      // .. +1: accumulator drained (4 epilogue warps -> MMA)
-  P_FINAL = 12,                      // every MMA done (teardown)
-  P_NBARS = 13,
+  P_FULL0 = 0,                       // .. +5: stage landed in both CTAs (CTA 0's barrier)
+  P_EMPTY0 = 6,                      // .. +5: stage consumed (pair MMA commit, both CTAs)
+  P_ACCF0 = 12,                      // .. +1: accumulator ready (pair MMA commit, both CTAs)
+  P_ACCE0 = 14,                      // .. +1: accumulator drained (CTA 0: 4 epilogue warps of each CTA)
+  P_FINAL = 16,                      // every MMA done (teardown, CTA 0)
+  P_NBARS = 17,
 };
 
 // The RoPE table with positions innermost: entry (axis, pair j, pos) at
@@ -78,7 +81,7 @@ template <int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     skiparse_qkv_rope_kernel(const __grid_constant__ ProjParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  constexpr int kBBytes = BN * kPBK * 2;
+  constexpr int kBBytes = BN / 2 * kPBK * 2;               // this CTA's half of the W tile
   constexpr int kStage = kABytes + kBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
@@ -97,21 +100,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
   const int stages = p.stages;
   const int rank = (int)cluster_ctarank();
   const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
-  const int n_total = ((p.m_tiles + 1) >> 1) * p.n_tiles;     // tile pairs
-  constexpr int kBHalf = BN / 2 * kPBK * 2;                    // this CTA's share of a W tile
+  const int n_total = ((p.m_tiles + 1) >> 1) * p.n_tiles;     // 256-row tile pairs
   constexpr uint16_t kBoth = 3;
 
   if (tid == 0) {
     *abort_flag = 0;
     for (int i = 0; i < P_NBARS; ++i) {
       uint32_t cnt = 1;
-      if (i == P_ACCE0 || i == P_ACCE0 + 1) cnt = 4;
-      if (i >= P_EMPTY0 && i < P_EMPTY0 + 4) cnt = 2;
+      if (i == P_ACCE0 || i == P_ACCE0 + 1) cnt = 8;                        // epilogue warps of both CTAs
       mbar_init(bar(i), cnt);
     }
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * BN);
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), 2 * BN);   // the same columns in both SMs
   proj_build_table(tab, p.rope, tid, kProjThreads);
   tc_fence_before();
   __syncthreads();
@@ -120,6 +121,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
   const uint32_t tmem = *tmem_slot;
   auto warp_wait = [&](int i, uint32_t parity) -> bool {
     return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ctl, E + i)) != 0;
+  };
+  // for barriers that also receive arrivals from the other CTA
+  auto warp_wait_cl = [&](int i, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait_cl(bar(i), parity, ctl, E + i)) != 0;
   };
   const bool leader = lane == 0;
 
@@ -136,70 +141,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
       for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
         const int s = (int)(it % (uint32_t)stages);
         const uint32_t use = it / (uint32_t)stages;
-        if (use > 0 && !warp_wait(P_EMPTY0 + s, (use - 1) & 1)) { ok = false; break; }
+        if (use > 0 && !warp_wait_cl(P_EMPTY0 + s, (use - 1) & 1)) { ok = false; break; }
         if (leader) {
+          // own x tile and own half of the W tile, both completing on CTA 0's barrier
           const uint32_t a = st0 + (uint32_t)(s * kStage);
-          mbar_expect_tx(bar(P_FULL0 + s), kStage);      // own x tile, both W halves
-          tma_load_2d(a, &p.tm_x, bar(P_FULL0 + s), ks * kPBK, mb * kPBM);
-          tma_load_2d_mc(a + kABytes + (uint32_t)(rank * kBHalf), &p.tm_w, bar(P_FULL0 + s), ks * kPBK,
-                         nb * BN + rank * (BN / 2), kBoth);
+          const uint32_t full = mapa_shared(bar(P_FULL0 + s), 0);
+          if (rank == 0) mbar_expect_tx(bar(P_FULL0 + s), 2 * kStage);
+          tma_load_2d_pair(a, &p.tm_x, full, ks * kPBK, mb * kPBM);
+          tma_load_2d_pair(a + kABytes, &p.tm_w, full, ks * kPBK, nb * BN + rank * (BN / 2));
         }
         __syncwarp();
       }
     }
-    // copies into this CTA land, and both CTAs' MMA commits for every stage
-    // arrive, before the cluster may release its shared memory
+    // copies into this CTA land, and the pair MMAs' commits for every stage
+    // arrive, before the pair may release its shared memory
     if (leader) {
       for (int s = 0; s < stages; ++s) {
         const uint32_t issued = it > (uint32_t)s ? (it - 1 - (uint32_t)s) / (uint32_t)stages + 1 : 0;
         if (issued) {
-          mbar_drain(bar(P_FULL0 + s), (issued - 1) & 1);
-          mbar_drain(bar(P_EMPTY0 + s), (issued - 1) & 1);
+          if (rank == 0) mbar_drain_cl(bar(P_FULL0 + s), (issued - 1) & 1);   // both CTAs' copies
+          mbar_drain_cl(bar(P_EMPTY0 + s), (issued - 1) & 1);
         }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kId = idesc_bf16(kPBM, BN, false, false);
+  } else if (warp == 1 && rank == 0) {
+    // ------------------------------------------------------------ CTA 0: MMA issuer for the pair
+    constexpr uint32_t kId = idesc_bf16(2 * kPBM, BN, false, false);
     uint32_t it = 0;
     int tl = 0;
     bool ok = true;
     for (int t = cid; ok && t < n_total; t += n_clusters, ++tl) {
       const int a = tl & 1;
       const uint32_t use = (uint32_t)tl >> 1;
-      if (use > 0 && !warp_wait(P_ACCE0 + a, (use - 1) & 1)) break;
+      if (use > 0 && !warp_wait_cl(P_ACCE0 + a, (use - 1) & 1)) break;
       tc_fence_after();
       const uint32_t dacc = tmem + (uint32_t)(a * BN);
       for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
         const int s = (int)(it % (uint32_t)stages);
-        if (!warp_wait(P_FULL0 + s, (it / (uint32_t)stages) & 1)) { ok = false; break; }
+        if (!warp_wait_cl(P_FULL0 + s, (it / (uint32_t)stages) & 1)) { ok = false; break; }
         tc_fence_after();
         if (leader) {
           const uint32_t sa = st0 + (uint32_t)(s * kStage);
           const uint64_t da = desc_kmajor(sa, 0), db = desc_kmajor(sa + kABytes, 0);
 #pragma unroll
           for (int kk = 0; kk < kPBK / 16; ++kk)
-            mma_ss(dacc, kmajor_step(da, kk), kmajor_step(db, kk), kId, (ks > 0 || kk > 0) ? 1u : 0u);
-          tc_commit_mc(bar(P_EMPTY0 + s), kBoth);       // the stage is free in both CTAs' view
-          if (ks + 1 == p.k_steps) tc_commit(bar(P_ACCF0 + a));
+            mma_pair_ss(dacc, kmajor_step(da, kk), kmajor_step(db, kk), kId, (ks > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_pair_mc(bar(P_EMPTY0 + s), kBoth);        // the stage is free in both CTAs
+          if (ks + 1 == p.k_steps) tc_commit_pair_mc(bar(P_ACCF0 + a), kBoth);
         }
         __syncwarp();
       }
     }
     if (leader) {
-      tc_commit(bar(P_FINAL));
-      mbar_drain(bar(P_FINAL), 0);
+      tc_commit_pair_mc(bar(P_FINAL), 1);
+      mbar_drain_cl(bar(P_FINAL), 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue warps 2-5
     const int quarter = warp & 3;                          // TMEM lanes 32 quarter .. +31
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     int tl = 0;
     for (int t = cid; t < n_total; t += n_clusters, ++tl) {
       const int a = tl & 1;
-      if (!mbar_wait(bar(P_ACCF0 + a), ((uint32_t)tl >> 1) & 1, ctl, E + P_ACCF0 + a)) break;
+      if (!mbar_wait_cl(bar(P_ACCF0 + a), ((uint32_t)tl >> 1) & 1, ctl, E + P_ACCF0 + a)) break;
       tc_fence_after();
       const int nb = t % p.n_tiles, mb = 2 * (t / p.n_tiles) + rank;
       const int row = mb * kPBM + quarter * 32 + lane;     // b N + token
@@ -255,22 +261,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (leader) mbar_arrive(bar(P_ACCE0 + a));
+      if (leader) {
+        if (rank == 0) mbar_arrive(bar(P_ACCE0 + a));
+        else mbar_arrive_remote(mapa_shared(bar(P_ACCE0 + a), 0));
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();        // neither CTA leaves while the other may still write into it
+  cluster_sync_all();        // neither CTA leaves, or frees the pair's TMEM, while the other may use it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * BN);
+    tmem_dealloc_pair(tmem, 2 * BN);
   }
 }
 
 int proj_bn(int hd) { return hd % 256 == 0 ? 256 : 128; }
 
-size_t proj_stage_bytes(int bn) { return (size_t)kABytes + (size_t)bn * kPBK * 2; }
+size_t proj_stage_bytes(int bn) { return (size_t)kABytes + (size_t)(bn / 2) * kPBK * 2; }
 
 // barriers and flags (1 KB), then the RoPE table, rounded up to 1 KB
 size_t proj_header_bytes(int rope_entries) { return 1024 + (((size_t)rope_entries * 8 + 1023) & ~(size_t)1023); }
