@@ -697,7 +697,7 @@ int skiparse_qkv_rope(const void* x, const void* w, const void* bias, void* q, v
   p.D = D;
   p.m_tiles = (int)((M + 127) / 128);
   p.n_tiles = (int)(3 * hd / bn);
-  p.k_steps = (C + 63) / 64;
+  p.k_steps = (C + proj_stage_channels() - 1) / proj_stage_channels();
   p.stages = (int)stages;
   p.stage_off = (int)header;
   if (!encode_bf16_2d(&p.tm_x, x, (uint64_t)C, (uint64_t)M, 128) ||

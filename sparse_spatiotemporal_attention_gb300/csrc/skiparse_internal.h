@@ -96,7 +96,7 @@ struct ProjParams {
   FastDiv fN;                     // row -> token
   int M, C, hd, D;                // rows B N, channels, heads D, head dim
   int m_tiles, n_tiles;           // 128-row tiles, BN-column tiles
-  int k_steps;                    // ceil(C / 64)
+  int k_steps;                    // ceil(C / channels per stage)
   int stages;                     // pipeline depth (2 .. 4)
   int stage_off;                  // byte offset of stage 0 in shared memory (1024-aligned)
 };
@@ -139,6 +139,7 @@ cudaError_t launch_fwd8(const Fwd8Params& p, int grid, cudaStream_t stream);
 
 int proj_bn(int hd);
 size_t proj_stage_bytes(int bn);
+int proj_stage_channels();
 size_t proj_header_bytes(int rope_entries);
 cudaError_t launch_proj(const ProjParams& p, int bn, int grid, cudaStream_t stream);
 

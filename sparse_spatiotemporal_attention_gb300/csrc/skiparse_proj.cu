@@ -11,8 +11,8 @@
 // MMAs (cta_group::2, M = 256: each CTA's 128 rows land in its own TMEM).
 // Per CTA, 6 warps:
 //   warp 0      TMA producer: 64-channel stages of the CTA's 128-row x tile
-//               and its half (BN/2 rows) of the W tile, 128-byte swizzle, up
-//               to 6 stages of 32 KB in flight;
+//               and its half (BN/2 rows) of the W tile, 128 channels per
+//               stage as two 128-byte swizzled boxes, 3 stages of 64 KB;
 //   warp 1      CTA 0: MMA issuer (converged, lane 0 issues 4 pair MMAs
 //               M=256 N=BN K=16 per stage into one of two accumulators);
 //               both CTAs' copies of a stage complete on CTA 0's barrier;
@@ -32,8 +32,10 @@ namespace {
 
 constexpr int kProjThreads = 192;
 constexpr int kPBM = 128;                 // output rows per tile
-constexpr int kPBK = 64;                  // channels per stage (one 128-byte row of bf16)
-constexpr int kABytes = kPBM * kPBK * 2;  // 16 KB
+constexpr int kPBK = 64;                  // channels per box (one 128-byte row of bf16)
+constexpr int kBoxes = 2;                 // boxes per stage: 128 channels, 8 MMA k-steps per wait
+constexpr int kABox = kPBM * kPBK * 2;    // 16 KB
+constexpr int kABytes = kBoxes * kABox;   // 32 KB
 constexpr int kMaxStages = 6;
 
 // barrier indices
@@ -81,7 +83,8 @@ template <int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
     skiparse_qkv_rope_kernel(const __grid_constant__ ProjParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  constexpr int kBBytes = BN / 2 * kPBK * 2;               // this CTA's half of the W tile
+  constexpr int kBBox = BN / 2 * kPBK * 2;                 // this CTA's half of the W tile, one box
+  constexpr int kBBytes = kBoxes * kBBox;
   constexpr int kStage = kABytes + kBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
@@ -147,8 +150,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
           const uint32_t a = st0 + (uint32_t)(s * kStage);
           const uint32_t full = mapa_shared(bar(P_FULL0 + s), 0);
           if (rank == 0) mbar_expect_tx(bar(P_FULL0 + s), 2 * kStage);
-          tma_load_2d_pair(a, &p.tm_x, full, ks * kPBK, mb * kPBM);
-          tma_load_2d_pair(a + kABytes, &p.tm_w, full, ks * kPBK, nb * BN + rank * (BN / 2));
+#pragma unroll
+          for (int h = 0; h < kBoxes; ++h) {
+            const int c0 = (ks * kBoxes + h) * kPBK;        // past C: the box fills with zeros
+            tma_load_2d_pair(a + h * kABox, &p.tm_x, full, c0, mb * kPBM);
+            tma_load_2d_pair(a + kABytes + h * kBBox, &p.tm_w, full, c0, nb * BN + rank * (BN / 2));
+          }
         }
         __syncwarp();
       }
@@ -185,8 +192,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
           const uint32_t sa = st0 + (uint32_t)(s * kStage);
           const uint64_t da = desc_kmajor(sa, 0), db = desc_kmajor(sa + kABytes, 0);
 #pragma unroll
-          for (int kk = 0; kk < kPBK / 16; ++kk)
-            mma_pair_ss(dacc, kmajor_step(da, kk), kmajor_step(db, kk), kId, (ks > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBoxes * kPBK / 16; ++kk)
+            mma_pair_ss(dacc, kmajor_step(da, kk, kABox), kmajor_step(db, kk, kBBox), kId, (ks > 0 || kk > 0) ? 1u : 0u);
           tc_commit_pair_mc(bar(P_EMPTY0 + s), kBoth);        // the stage is free in both CTAs
           if (ks + 1 == p.k_steps) tc_commit_pair_mc(bar(P_ACCF0 + a), kBoth);
         }
@@ -279,7 +286,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProjThreads, 1)
 
 int proj_bn(int hd) { return hd % 256 == 0 ? 256 : 128; }
 
-size_t proj_stage_bytes(int bn) { return (size_t)kABytes + (size_t)(bn / 2) * kPBK * 2; }
+size_t proj_stage_bytes(int bn) { return (size_t)kABytes + (size_t)kBoxes * (bn / 2) * kPBK * 2; }
+
+int proj_stage_channels() { return kBoxes * kPBK; }
 
 // barriers and flags (1 KB), then the RoPE table, rounded up to 1 KB
 size_t proj_header_bytes(int rope_entries) { return 1024 + (((size_t)rope_entries * 8 + 1023) & ~(size_t)1023); }
