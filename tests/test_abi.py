@@ -156,3 +156,42 @@ def test_package_has_no_fallback():
     for f in os.listdir(os.path.join(ROOT, "sparse_spatiotemporal_attention_gb300")):
         if f.endswith(".py"):
             assert "import oracle" not in open(os.path.join(ROOT, "sparse_spatiotemporal_attention_gb300", f)).read()
+
+
+def test_fwd_fp8_validation(lib):
+    """The 8-bit forward validates on the host first (D = 128 only)."""
+    ws = lib.skiparse_attn_fwd_fp8_workspace_bytes(1, 2, 256, 128, 4, 8, 8, 2, 0)
+    assert ws > 0
+    assert lib.skiparse_attn_fwd_fp8_workspace_bytes(1, 2, 256, 64, 4, 8, 8, 2, 0) == 0
+
+    def fwd(ws_ptr=10 * A, ws_bytes=ws, D=128, out=4 * A, theta=10000.0, N=256):
+        return lib.skiparse_attn_fwd_fp8(A, 2 * A, 3 * A, out, 5 * A, ws_ptr, ws_bytes, 1, 2, N, D, 4, 8, 8, 2, 0,
+                                         theta, None)
+    assert fwd(D=64) == UNSUP
+    assert fwd(N=255) == SHAPE
+    assert fwd(theta=-1.0) == INVALID
+    assert fwd(ws_ptr=None) == WORKSPACE
+    assert fwd(ws_bytes=ws - 1) == WORKSPACE
+    assert fwd(out=A) == ALIAS
+    assert fwd() == DEVICE
+    assert fwd(theta=0.0) == DEVICE          # 0: q, k already rotated
+
+
+def test_qkv_rope_validation(lib):
+    """The projection validates on the host first: shapes, sizes, alignment, overlaps."""
+    def proj(x=A, w=2 * A, bias=3 * A, q=4 * A, k=5 * A, v=6 * A, B=1, N=256, C=128, heads=2, D=64,
+             T=4, H=8, W=8, theta=10000.0):
+        return lib.skiparse_qkv_rope(x, w, bias, q, k, v, B, N, C, heads, D, T, H, W, theta, None)
+    assert proj(N=255) == SHAPE
+    assert proj(D=96) == UNSUP
+    assert proj(C=100) == UNSUP                 # C % 8
+    assert proj(heads=1) == UNSUP               # heads D = 64 not a multiple of 128
+    assert proj(theta=-1.0) == INVALID
+    assert proj(x=None) == INVALID
+    assert proj(q=4 * A + 8) == ALIGN
+    assert proj(k=4 * A) == ALIAS               # q and k overlap
+    assert proj(q=A) == ALIAS                   # q over x
+    assert proj(B=0, x=None) == OK              # empty call
+    assert proj(bias=None) == DEVICE            # bias is optional
+    assert proj() == DEVICE
+    assert proj(theta=0.0) == DEVICE            # 0: no rotation

@@ -96,3 +96,27 @@ def test_fp8_rejects_d64_and_small_workspace(env):
     with pytest.raises(skp.SkiparseError) as e:
         skp.skiparse_attn_fwd_fp8(q, q, q, out, lse, 4, 8, 8, 2, 0, workspace=ws[:1024])
     assert e.value.status == -6
+
+
+def test_fp8_forward_prerotated_inputs(env):
+    """rope_theta = 0: q and k are taken as already rotated (no rotation in the
+    prep kernel), against the 8-bit oracle with the same convention."""
+    import torch
+    skp, dev = env
+    B, heads, T, H, W, k, mode = 1, 2, 3, 10, 10, 2, O.GROUP
+    D, N = 128, T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D)
+    q, kk, v = (tl.to_device(ins[n], dev) for n in ("q", "k", "v"))
+    obuf, out = tl.guarded_empty((B, N, heads, D), torch.bfloat16, dev)
+    lse = torch.empty((B, heads, N), dtype=torch.float32, device=dev)
+    skp.skiparse_attn_fwd_fp8(q, kk, v, out, lse, T, H, W, k, mode, rope_theta=0.0)
+    torch.cuda.synchronize()
+    assert tl.guards_intact(obuf)
+    f = tl.f64_inputs(ins)
+    rout, rlse = F.skiparse_fwd_fp8(f["q"], f["k"], f["v"], T, H, W, k, mode, theta=0.0)
+    err = np.abs(tl.host(out) - rout)
+    assert err.mean() <= tl.TOL_MEAN and err.max() <= 0.1
+    assert np.sqrt(np.sum(err ** 2) / np.sum(rout ** 2)) <= tl.TOL_RMS_REL
+    tl.compare("lse", tl.host(lse), rlse, tol_max=tl.TOL_LSE, tol_mean=tl.TOL_LSE, tol_rel=1e-3)
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
