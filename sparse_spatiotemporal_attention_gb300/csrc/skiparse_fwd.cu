@@ -280,91 +280,83 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
-    uint32_t g0 = 0;
-    int it = 0;
-    bool ok = true;
-    // operand descriptors of k-step 0, per tile and stage (k-steps add a constant)
-    const uint64_t dQA = desc_kmajor(sQA, 0), dQB = desc_kmajor(sQB, 0);
-    const uint64_t dK0 = desc_kmajor(sK, 0), dK1 = desc_kmajor(sK + Ly::TILE, 0);
-    const uint64_t dV0 = desc_mnmajor(sV, 0), dV1 = desc_mnmajor(sV + Ly::TILE, 0);
-    // S_X = Q_X K_g^T into TMEM columns colS (X = A: 0, B: 128)
-    auto issue_s = [&](uint64_t dq, uint32_t colS, int st) {
-      const uint64_t dk = st ? dK1 : dK0;
+    // Lane 0 alone issues while the other lanes wait at the warp's final sync.
+    // Its waits nearly always find the barrier complete, and a wait without
+    // the warp vote and reconvergence costs the issuing thread (which, not the
+    // tensor core, sets this kernel's pace) fewer cycles.
+    if (leader) {
+      auto lane_wait = [&](int i, uint32_t parity) -> bool { return mbar_wait(bar(i), parity, ctl, E + i); };
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
+      uint32_t g0 = 0;
+      int it = 0;
+      bool ok = true;
+      // operand descriptors of k-step 0, per tile and stage (k-steps add a constant)
+      const uint64_t dQA = desc_kmajor(sQA, 0), dQB = desc_kmajor(sQB, 0);
+      const uint64_t dK0 = desc_kmajor(sK, 0), dK1 = desc_kmajor(sK + Ly::TILE, 0);
+      const uint64_t dV0 = desc_mnmajor(sV, 0), dV1 = desc_mnmajor(sV + Ly::TILE, 0);
+      // S_X = Q_X K_g^T into TMEM columns colS (X = A: 0, B: 128)
+      auto issue_s = [&](uint64_t dq, uint32_t colS, int st) {
+        const uint64_t dk = st ? dK1 : dK0;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        mma_ss(tmem + colS, kmajor_step(dq, ks), kmajor_step(dk, ks), kIdS, ks > 0 ? 1u : 0u);
-    };
-    // O_X += P_X V_g, P_X in TMEM over S_X
-    auto issue_pv = [&](uint32_t colS, uint32_t colO, int st, bool first) {
-      const uint64_t dv = st ? dV1 : dV0;
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + colS, kmajor_step(dq, ks), kmajor_step(dk, ks), kIdS, ks > 0 ? 1u : 0u);
+      };
+      // O_X += P_X V_g, P_X in TMEM over S_X
+      auto issue_pv = [&](uint32_t colS, uint32_t colO, int st, bool first) {
+        const uint64_t dv = st ? dV1 : dV0;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_ts(tmem + colO, tmem + colS + ks * 8, mnmajor_step(dv, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
-    };
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-      const int n = g.n_tiles;
-      if (!warp_wait(F_QFULL, it & 1)) break;
-      if (!warp_wait(F_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
-      tc_fence_after();
-      if (leader) {
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tmem + colO, tmem + colS + ks * 8, mnmajor_step(dv, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
+      };
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+        const int n = g.n_tiles;
+        if (!lane_wait(F_QFULL, it & 1)) break;
+        if (!lane_wait(F_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
+        tc_fence_after();
         issue_s(dQA, 0, g0 & 1);
         tc_commit(bar(F_SFULL_A));
         issue_s(dQB, 128, g0 & 1);
         tc_commit(bar(F_SFULL_B));
         tc_commit(bar(F_KEMPTY0 + (g0 & 1)));
         if (n == 1) tc_commit(bar(F_QEMPTY));
-      }
-      __syncwarp();
-      for (int j = 0; j < n; ++j) {
-        const uint32_t gg = g0 + j;
-        const int st = gg & 1;
-        const uint32_t nn = gg >> 1;
-        // PV_A(g)
-        if (j == 0 && it > 0 && !warp_wait(F_OEMPTY_A, (it - 1) & 1)) { ok = false; break; }
-        if (!warp_wait(F_PFULL_A, gg & 1)) { ok = false; break; }
-        if (!warp_wait(F_VFULL0 + st, nn & 1)) { ok = false; break; }
-        tc_fence_after();
-        if (leader) {
+        for (int j = 0; j < n; ++j) {
+          const uint32_t gg = g0 + j;
+          const int st = gg & 1;
+          const uint32_t nn = gg >> 1;
+          // PV_A(g)
+          if (j == 0 && it > 0 && !lane_wait(F_OEMPTY_A, (it - 1) & 1)) { ok = false; break; }
+          if (!lane_wait(F_PFULL_A, gg & 1)) { ok = false; break; }
+          if (!lane_wait(F_VFULL0 + st, nn & 1)) { ok = false; break; }
+          tc_fence_after();
           issue_pv(0, 256, st, j == 0);
           tc_commit(bar(F_ODONE_A));
-        }
-        __syncwarp();
-        // S_A(g+1)
-        const bool more = j + 1 < n;
-        if (more) {
+          // S_A(g+1)
+          const bool more = j + 1 < n;
           const int st1 = (gg + 1) & 1;
-          if (!warp_wait(F_KFULL0 + st1, ((gg + 1) >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          if (leader) {
+          if (more) {
+            if (!lane_wait(F_KFULL0 + st1, ((gg + 1) >> 1) & 1)) { ok = false; break; }
+            tc_fence_after();
             issue_s(dQA, 0, st1);
             tc_commit(bar(F_SFULL_A));
           }
-          __syncwarp();
-        }
-        // PV_B(g)
-        if (j == 0 && it > 0 && !warp_wait(F_OEMPTY_B, (it - 1) & 1)) { ok = false; break; }
-        if (!warp_wait(F_PFULL_B, gg & 1)) { ok = false; break; }
-        tc_fence_after();
-        if (leader) {
+          // PV_B(g)
+          if (j == 0 && it > 0 && !lane_wait(F_OEMPTY_B, (it - 1) & 1)) { ok = false; break; }
+          if (!lane_wait(F_PFULL_B, gg & 1)) { ok = false; break; }
+          tc_fence_after();
           issue_pv(128, 256 + D, st, j == 0);
           tc_commit(bar(F_ODONE_B));
           tc_commit(bar(F_VEMPTY0 + st));
           // S_B(g+1)
           if (more) {
-            const int st1 = (gg + 1) & 1;
             issue_s(dQB, 128, st1);
             tc_commit(bar(F_SFULL_B));
             tc_commit(bar(F_KEMPTY0 + st1));
             if (j + 2 == n) tc_commit(bar(F_QEMPTY));
           }
         }
-        __syncwarp();
+        g0 += n;
       }
-      g0 += n;
-    }
-    if (leader) {
       tc_commit(bar(F_FINAL));
       mbar_drain(bar(F_FINAL), 0);
     }
