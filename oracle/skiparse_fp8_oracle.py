@@ -130,10 +130,12 @@ def quantize_channels(v: np.ndarray):
 
 
 def blocked_attention(sq, sk, q8, k8, v8, sv, scale, quantize_p=True):
-    """One scope problem: q8 (L, D) codes with row scales sq (L,), k8 (L, D) with
+    """One scope problem: q8 (Lq, D) codes with row scales sq (Lq,), k8 (L, D) with
     sk (L,), v8 (L, D) with channel scales sv (D,). Online softmax over blocks of
-    128 keys with the lazy rule; returns (out (L, D), lse (L,))."""
-    L, D = q8.shape
+    128 keys with the lazy rule; returns (out (Lq, D), lse (Lq,)). Query rows are
+    independent, so q8 may hold any subset of the scope's rows (Lq <= L)."""
+    Lq, D = q8.shape
+    L = k8.shape[0]
     log2e = 1.0 / math.log(2.0)
     raw = q8 @ k8.T                                                  # exact: sums of E4M3 products
     if quantize_p:
@@ -141,12 +143,12 @@ def blocked_attention(sq, sk, q8, k8, v8, sv, scale, quantize_p=True):
         # in float32, as the kernel forms the values its codes are decided on
         c = (np.float32(scale * log2e) * sq.astype(np.float32))[:, None] * sk.astype(np.float32)[None, :]
         c = c.astype(np.float32).astype(np.float64)
-        S = raw.astype(np.float32).astype(np.float64) * c            # (L, L), base-2 units
+        S = raw.astype(np.float32).astype(np.float64) * c            # (Lq, L), base-2 units
     else:
         S = (sq[:, None] * sk[None, :]) * raw * scale * log2e
-    m = np.zeros(L)
-    l = np.zeros(L)
-    acc = np.zeros((L, D))
+    m = np.zeros(Lq)
+    l = np.zeros(Lq)
+    acc = np.zeros((Lq, D))
     for j0 in range(0, L, BLOCK):
         Sb = S[:, j0:j0 + BLOCK]
         mx = Sb.max(axis=1)
@@ -211,3 +213,26 @@ def skiparse_fwd_fp8(q, k, v, T, H, W, sparse_k, mode, theta=10000.0, quantize=T
     out = O.reverse(o_r, sparse_k, mode)
     lse = O.reverse(lse_r, sparse_k, mode)
     return out, np.ascontiguousarray(np.transpose(lse, (0, 2, 1)))
+
+
+def skiparse_fwd_fp8_scope(q, k, v, T, H, W, sparse_k, mode, b, head, s, rows, theta=10000.0):
+    """The 8-bit forward for chosen query rows of one scope of one (batch, head),
+    for checks on large inputs. q, k, v are the full (B, N, heads, D) arrays
+    (bf16-valued); only the scope's k rows, the chosen q rows and v[b, :, head]
+    (whose per-channel scales span all N tokens) are read. `rows` index the
+    scope in scope order. Returns (tokens of those rows, out (n, D), lse (n,)),
+    the same numbers skiparse_fwd_fp8 gives for those rows."""
+    N, D = q.shape[1], q.shape[3]
+    scale = 1.0 / math.sqrt(D)
+    tok = O.scope_tokens(N, sparse_k, mode, s)
+    t, h, w = O.token_coords(N, T, H, W)
+    rows = np.asarray(rows)
+    qt = tok[rows]
+    qr = O._rope_rows(np.asarray(q[b, qt, head], dtype=np.float64), t[qt], h[qt], w[qt], theta)
+    kr = O._rope_rows(np.asarray(k[b, tok, head], dtype=np.float64), t[tok], h[tok], w[tok], theta)
+    q8, sq = quantize_rows(qr)
+    k8, sk = quantize_blocks(kr)
+    vh = np.asarray(v[b:b + 1, :, head:head + 1], dtype=np.float64)
+    v8, sv = quantize_channels(vh)
+    out, lse = blocked_attention(sq, sk, q8, k8, v8[0, tok, 0], sv[0, 0], scale)
+    return qt, out, lse

@@ -81,6 +81,58 @@ def test_fp8_forward_parity(env, case):
     assert st == 0, hex(detail)
 
 
+# the 8-bit workloads the bench times: (B, heads, (T, H, W), k, mode); D = 128
+FULL = [
+    ("group_16x45x80_k4", 1, 24, (16, 45, 80), 4, O.GROUP),
+    ("group_24x22x40_k4", 2, 24, (24, 22, 40), 4, O.GROUP),
+    ("single_8x32x32_k4", 1, 24, (8, 32, 32), 4, O.SINGLE),
+]
+
+
+@pytest.mark.parametrize("name,B,heads,grid,k,mode", FULL, ids=[f[0] for f in FULL])
+def test_fp8_full_size_sampled(env, name, B, heads, grid, k, mode):
+    """Full size, launched as the bench launches it (its workspace, a side
+    stream): the first and last 64 rows and 64 random rows of three scopes
+    against the 8-bit oracle's scope routine, with the parity cases' bars."""
+    import torch
+    skp, dev = env
+    T, H, W = grid
+    D, N = 128, T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D)
+    q, kk, v = (tl.to_device(ins[n], dev) for n in ("q", "k", "v"))
+    out = torch.empty((B, N, heads, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, heads, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(skp.skiparse_attn_fwd_fp8_workspace_bytes(B, heads, N, D, T, H, W, k, mode),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    skp.skiparse_attn_fwd_fp8(q, kk, v, out, lse, T, H, W, k, mode, stream=stream, workspace=ws)
+    stream.synchronize()
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
+    got, glse = tl.host(out), tl.host(lse)
+    assert np.all(np.isfinite(got)) and np.all(np.isfinite(glse))
+    L = N // k
+    rng = np.random.default_rng(31)
+    gsel, rsel, gl, rl = [], [], [], []
+    for b, h, s in [(0, 0, 0), (B - 1, heads - 1, k - 1), (B - 1, 7, k // 2)]:
+        rows = np.unique(np.concatenate([np.arange(64), np.arange(L - 64, L), rng.integers(0, L, 64)]))
+        sub = {n: synthetic.bf16_bits_to_f64(ins[n][b:b + 1, :, h:h + 1]) for n in ("q", "k", "v")}
+        tok, ro, rlse = F.skiparse_fwd_fp8_scope(sub["q"], sub["k"], sub["v"], T, H, W, k, mode, 0, 0, s, rows)
+        gsel.append(got[b, tok, h])
+        rsel.append(ro)
+        gl.append(glse[b, h, tok])
+        rl.append(rlse)
+    g_, r_ = np.concatenate(gsel), np.concatenate(rsel)
+    err = np.abs(g_ - r_)
+    assert err.mean() <= tl.TOL_MEAN, err.mean()
+    assert np.sqrt(np.sum(err ** 2) / np.sum(r_ ** 2)) <= tl.TOL_RMS_REL
+    assert np.count_nonzero(err > tl.TOL_MAX) <= max(1, err.size // 10000), np.count_nonzero(err > tl.TOL_MAX)
+    assert err.max() <= 0.1, err.max()
+    tl.compare("lse", np.concatenate(gl), np.concatenate(rl), tol_max=tl.TOL_LSE, tol_mean=tl.TOL_LSE,
+               tol_rel=1e-3)
+
+
 def test_fp8_rejects_d64_and_small_workspace(env):
     import torch
     skp, dev = env

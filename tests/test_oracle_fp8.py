@@ -138,3 +138,23 @@ def test_quantized_forward_error_is_of_the_expected_size():
     rel = np.sqrt(np.sum((out - rout) ** 2) / np.sum(rout ** 2))
     assert 1e-3 < rel < 8e-2
     assert np.max(np.abs(lse - rlse)) < 5e-2
+
+
+@pytest.mark.parametrize("mode", [O.SINGLE, O.GROUP], ids=["single", "group"])
+def test_scope_rows_match_the_whole_forward(mode):
+    """The row-sampled scope routine (used on full-size inputs) gives the whole
+    8-bit forward's numbers for the rows it is asked for: several key blocks
+    with a ragged last one, two batches and heads (v's channel scales span all
+    tokens of a (batch, head))."""
+    B, heads, D, T, H, W, k = 2, 2, 64, 3, 10, 12, 2
+    N = T * H * W
+    rs = np.random.RandomState(21)
+    q, kk, v = (rs.randn(B, N, heads, D) for _ in range(3))
+    out, lse = F.skiparse_fwd_fp8(q, kk, v, T, H, W, k, mode)
+    L = N // k
+    rows = np.array([0, 1, 127, 128, 129, L - 1])
+    for b, h, s in [(0, 0, 0), (1, 1, 1), (1, 0, 0)]:
+        tok, o, l = F.skiparse_fwd_fp8_scope(q, kk, v, T, H, W, k, mode, b, h, s, rows)
+        assert np.array_equal(tok, O.scope_tokens(N, k, mode, s)[rows])
+        assert np.allclose(o, out[b, tok, h], rtol=0, atol=1e-12)
+        assert np.allclose(l, lse[b, h, tok], rtol=0, atol=1e-12)
