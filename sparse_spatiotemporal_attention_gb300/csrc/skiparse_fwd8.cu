@@ -19,17 +19,21 @@
 // Kernels:
 //   skiparse_fwd8_vmax_kernel   max |v| per (b, head, channel) (atomicMax on the
 //                               bits of non-negative floats into a zeroed array);
-//   skiparse_fwd8_prep_kernel   persistent CTAs (one RoPE table each) over (scope,
-//                               128-position tile) items: RoPE and quantize q (per
-//                               row) and k (per tile), quantize v and transpose it
-//                               in shared memory, all in scope-tile order, so the
+//   skiparse_fwd8_prep_kernel   persistent CTAs, one per SM (one RoPE table each),
+//                               over (scope, 128-position tile) items: a TMA warp
+//                               stages the item's q and k tiles through the scope
+//                               gather in a two-slot ring; the compute warps apply
+//                               RoPE and quantize q (per row) and k (per tile),
+//                               quantize v (read one item ahead) and transpose it in
+//                               shared memory, all in scope-tile order, so the
 //                               attention kernel reads plain 128 x 128-byte boxes
 //                               (every 8-bit operand K-major);
-//   skiparse_fwd8_kernel        the forward kernel's structure (two Q tiles per
-//                               CTA, softmax warps 0-7, TMA warp 8, MMA warp 9)
-//                               with kind::f8f6f4 MMAs: 4 per 128 x 128 product
-//                               instead of 8, P stored as E4M3 over S (32 TMEM
-//                               columns per tile).
+//   skiparse_fwd8_kernel        two Q tiles per CTA as the bf16 forward (softmax
+//                               warps 0-7, TMA warp 8), kind::f8f6f4 MMAs (4 per
+//                               128 x 128 product instead of 8) issued by one warp
+//                               per Q tile (9, 10); P as E4M3 codes in shared
+//                               memory, so S of the next K tile is issued as soon
+//                               as the softmax warps hold S in registers.
 #include "skiparse_internal.h"
 
 namespace skp {
@@ -38,11 +42,21 @@ namespace {
 
 constexpr int kD8 = 128;
 constexpr int kF8Threads = 352;   // softmax 0-7, TMA 8, MMA issuers 9 (Q tile A) and 10 (Q tile B)
-constexpr int kPrepThreads = 256;
+constexpr int kPrepComputeWarps = 8;
+constexpr int kPrepThreads = (kPrepComputeWarps + 1) * 32;   // 8 compute warps, then the TMA warp
+constexpr int kPrepCompute = kPrepComputeWarps * 32;
+constexpr int kPrepHalf = 128 * 128;                          // 128 rows x 64 bf16 channels, 128-byte swizzle
+constexpr int kPrepStage = 4 * kPrepHalf;                     // q and k tiles, two channel halves each
 constexpr float kE4M3Max = 448.0f;
 
 // RoPE table bytes in the prep kernel's shared memory, rounded up to 16
 __host__ __device__ constexpr size_t prep_table_bytes(int entries) { return ((size_t)entries * 8 + 15) & ~(size_t)15; }
+// prep kernel shared memory: 1 KB header (barriers, per-warp maxima, abort
+// flag), the staging ring (1024-byte aligned for the swizzle), the V^T
+// transpose buffer (128 channels x 32 words), the RoPE table
+__host__ __device__ constexpr size_t prep_smem(int stages, int entries) {
+  return 1024 + (size_t)stages * kPrepStage + (size_t)128 * 32 * 4 + prep_table_bytes(entries);
+}
 #ifndef SKP_FWD8_FMA_PAIRS
 #define SKP_FWD8_FMA_PAIRS 0
 #endif
@@ -121,15 +135,16 @@ enum F8Bar {
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// max |v| per (b, head, channel): grid (token chunks of 256, B * heads)
+// max |v| per (b, head, channel): grid (B * heads, token chunks of 256), (b, head)
+// fastest so that blocks running together read whole token rows of v
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) skiparse_fwd8_vmax_kernel(const __grid_constant__ Fwd8Params p) {
   __shared__ float part[4][kD8];
   const Geom& g = p.g;
-  const int bh = blockIdx.y;
+  const int bh = blockIdx.x;
   const int b = bh / g.heads, head = bh - b * g.heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * 256;
+  const int t0 = blockIdx.y * 256;
   const int t1 = min(t0 + 256, g.N);
   float mx[4] = {0.f, 0.f, 0.f, 0.f};
   for (int i = t0 + warp; i < t1; i += 4) {
@@ -148,88 +163,201 @@ __global__ void __launch_bounds__(128) skiparse_fwd8_vmax_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------------------
-// prep: one CTA per (scope index sidx = (b * heads + head) * k + s, 128-position tile)
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPrepThreads) skiparse_fwd8_prep_kernel(const __grid_constant__ Fwd8Params p) {
-  extern __shared__ __align__(16) uint8_t psm[];
-  float2* tab = reinterpret_cast<float2*>(psm);                                     // RoPE table
-  uint32_t* vt = reinterpret_cast<uint32_t*>(psm + prep_table_bytes(p.rope.entries));  // 128 channels x 32 words
-  float* rowmax = reinterpret_cast<float*>(vt + kD8 * 32);                          // one per warp
-  const Geom& g = p.g;
+// prep: persistent CTAs (one per SM, one RoPE table each) over (scope index
+// sidx = (b * heads + head) * k + s, 128-position tile) items. The TMA warp
+// stages each item's q and k tiles (bf16, through the scope gather: smem row r
+// is scope position tile * 128 + r) in a ring of prep_stages slots, so the
+// next tiles load while the compute warps work on this one (two CTAs per SM
+// when their shared memory fits: one slot each); v rows are read directly, a
+// group of four rows ahead.
+__global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwd8_prep_kernel(const __grid_constant__ Fwd8Params p) {
+  extern __shared__ __align__(1024) uint8_t psm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((smem_u32(psm) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
+    return;
+  }
+  const Geom& g = p.g;
+  const int stages = p.prep_stages;
+  float* rowmax = reinterpret_cast<float*>(psm + 64);                               // one per compute warp
+  int* abort_flag = reinterpret_cast<int*>(psm + 192);
+  uint8_t* ring = psm + 1024;
+  uint32_t* vt = reinterpret_cast<uint32_t*>(ring + (size_t)stages * kPrepStage);  // 128 channels x 32 words
+  float2* tab = reinterpret_cast<float2*>(vt + kD8 * 32);                           // RoPE table
+  const uint32_t bar0 = smem_u32(psm);
+  // barriers: FULL of slot st at st, EMPTY of slot st at 2 + st
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  constexpr int E = ERR_KERNEL_FWD + 0xC0;
+  const Ctl ctl{abort_flag, p.err};
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int st = 0; st < stages; ++st) {
+      mbar_init(bar(st), 1);
+      mbar_init(bar(2 + st), kPrepComputeWarps);
+    }
+    mbar_fence_init();
+  }
   rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
   __syncthreads();
-  const PairSel sel0 = pair_select(p.rope, lane * 2);
-  const PairSel sel1 = pair_select(p.rope, lane * 2 + 1);
   const int n_items = g.B * g.heads * g.k * g.n_tiles;
-  // persistent: one (scope, 128-position tile) item at a time; warp w owns the
-  // tile's rows 4(w + 8i) .. 4(w + 8i) + 3, i = 0..3
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int tile = item % g.n_tiles;
-    const int sidx = item / g.n_tiles;
-    const int s = sidx % g.k;
+  // head fastest: the CTAs working at the same time read all heads of the same
+  // tokens, i.e. whole (token, heads x D) rows of q, k and v, not one head's
+  // 256-byte slice of every row
+  auto decode = [&](int item, int& tile, int& s, int& sidx, int& b, int& head) {
+    head = item % g.heads;
+    const int rest = item / g.heads;
+    tile = rest % g.n_tiles;
+    const int bs = rest / g.n_tiles;
+    s = bs % g.k;
+    b = bs / g.k;
+    sidx = (b * g.heads + head) * g.k + s;
+  };
+
+  if (warp == kPrepComputeWarps) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&p.tm_q);
+      tma_prefetch_map(&p.tm_k);
+      uint32_t issued[2] = {0, 0};
+      int it = 0;
+      for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+        const int st = it % stages;
+        const int n = it / stages;
+        if (n > 0 && !mbar_wait(bar(2 + st), (n - 1) & 1, ctl, E + 2 + st)) break;
+        int tile, s, sidx, b, head;
+        decode(item, tile, s, sidx, b, head);
+        const uint32_t dst = smem_u32(ring + (size_t)st * kPrepStage);
+        const int row = b * g.Nn + (tile * kTile) / g.G;
+        mbar_expect_tx(bar(st), kPrepStage);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tma_load_5d(dst + h * kPrepHalf, &p.tm_q, bar(st), h * 64, head, 0, s, row);
+          tma_load_5d(dst + (2 + h) * kPrepHalf, &p.tm_k, bar(st), h * 64, head, 0, s, row);
+        }
+        ++issued[st];
+      }
+      // copies still in flight (only after an abort) must land before exit
+      for (int st = 0; st < stages; ++st)
+        if (issued[st]) mbar_drain(bar(st), (issued[st] - 1) & 1);
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ------------------------------------------------------------ compute warps
+  // Warp w owns the tile's rows 4(w + 8 i) + rq, rq = 0..3, i = 0..3.
+  // q and k (staged): lane l takes row rq = l / 8 of each group and channels
+  // 16 cb .. 16 cb + 15, cb = l % 8 (pairs 8 cb .. 8 cb + 7, all in one RoPE
+  // chunk, contiguous in the table), so per-row work (token coordinates, table
+  // index, the row max over 8 lanes, the scale divisions) serves four rows per
+  // instruction. In a staged row those channels are the 16-byte chunks
+  // 2 (cb % 4) and 2 (cb % 4) + 1 of half cb / 4, each XOR (row % 8).
+  // v (read directly): lane l takes channels 4 l .. 4 l + 3 of all four rows,
+  // the layout the V^T transpose needs.
+  const int rq = lane >> 3, cb = lane & 7;
+  const uint32_t half_off = (uint32_t)(cb >> 2) * kPrepHalf;
+  const uint32_t chunk0 = (uint32_t)(2 * (cb & 3));
+  // this lane's 8 pairs in the table: base entry of the chunk and pair offset
+  int tab_base, tab_stride, tab_local, tab_axis;
+  {
+    const int pp = 8 * cb;                              // D = 128: pairs 0-15 t, 16-39 h, 40-63 w
+    const PairSel sel = pair_select(p.rope, pp);
+    tab_base = sel.base; tab_stride = sel.stride; tab_local = sel.local; tab_axis = sel.axis;
+  }
+  auto load_v = [&](int tile, int s, int b, int head, int i, uint2 (&vv)[4]) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int pos = tile * kTile + 4 * (warp + 8 * i) + rr;
+      vv[rr] = make_uint2(0u, 0u);
+      if (pos < g.L) {
+        const int tok = token_of(g, s, pos);
+        vv[rr] = __ldg(reinterpret_cast<const uint2*>(p.v + (((size_t)b * g.N + tok) * g.heads + head) * kD8 + lane * 4));
+      }
+    }
+  };
+  int it = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+    const int st = it % stages;
+    int tile, s, sidx, b, head;
+    decode(item, tile, s, sidx, b, head);
     const int bh = sidx / g.k;
-    const int b = bh / g.heads, head = bh - b * g.heads;
+    uint2 vcur[4];
+    load_v(tile, s, b, head, 0, vcur);               // in flight while the staged tiles land
     float inv_v[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float m = __uint_as_float(p.vmax[(size_t)bh * kD8 + lane * 4 + e]);
       inv_v[e] = m > 0.f ? kE4M3Max / m : 0.f;
     }
-    float kr[4][4][4];                 // rotated k of the warp's 16 rows, 4 channels per lane
+    if (!bar_and<1, kPrepCompute>(mbar_wait(bar(st), (it / stages) & 1, ctl, E + st))) break;
+    const uint8_t* q_tile = ring + (size_t)st * kPrepStage;
+    const uint8_t* k_tile = q_tile + 2 * kPrepHalf;
+    // k in two passes over the staged tile: the tile's max |k| first, the codes
+    // once it is known (rotating again instead of holding 64 values per thread)
     float kmax = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r0 = 4 * (warp + 8 * i);
-      // the group's loads first (all in flight together), then the arithmetic
-      uint2 qu4[4], ku4[4], vu4[4];
-      int tok4[4];
+      uint2 vnext[4] = {};
+      if (i < 3) load_v(tile, s, b, head, i + 1, vnext);
+      // ---- q and k of row r0 + rq, channels 16 cb .. 16 cb + 15
+      {
+        const int r = r0 + rq;
+        const int pos = tile * kTile + r;
+        const size_t slot = (size_t)sidx * p.Lp + pos;          // scope-order row
+        const bool valid = pos < g.L;                // not warp-uniform: four rows per warp
+        uint4 qc = make_uint4(0u, 0u, 0u, 0u);
+        float sq = 0.f;
+        float qr[16];
+        float qm = 0.f;
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int pos = tile * kTile + r0 + rr;
-        tok4[rr] = pos < g.L ? token_of(g, s, pos) : -1;
-        qu4[rr] = ku4[rr] = vu4[rr] = make_uint2(0u, 0u);
-        if (tok4[rr] >= 0) {
-          const size_t base = (((size_t)b * g.N + tok4[rr]) * g.heads + head) * kD8 + lane * 4;
-          qu4[rr] = __ldg(reinterpret_cast<const uint2*>(p.q + base));
-          ku4[rr] = __ldg(reinterpret_cast<const uint2*>(p.k + base));
-          vu4[rr] = __ldg(reinterpret_cast<const uint2*>(p.v + base));
+        for (int e = 0; e < 16; ++e) qr[e] = 0.f;
+        if (valid) {
+          const uint32_t rb = (uint32_t)r * 128u + half_off;
+          const uint32_t o0 = rb + ((chunk0 ^ (uint32_t)(r & 7)) << 4);
+          const uint32_t o1 = rb + (((chunk0 + 1u) ^ (uint32_t)(r & 7)) << 4);
+          uint32_t qw[8], kw[8];
+          *reinterpret_cast<uint4*>(qw) = *reinterpret_cast<const uint4*>(q_tile + o0);
+          *reinterpret_cast<uint4*>(qw + 4) = *reinterpret_cast<const uint4*>(q_tile + o1);
+          *reinterpret_cast<uint4*>(kw) = *reinterpret_cast<const uint4*>(k_tile + o0);
+          *reinterpret_cast<uint4*>(kw + 4) = *reinterpret_cast<const uint4*>(k_tile + o1);
+          int t, hh, w;
+          token_coords(p.rope, token_of(g, s, pos), t, hh, w);
+          const int apos = tab_axis == 0 ? t : (tab_axis == 1 ? hh : w);
+          const float4* tp = reinterpret_cast<const float4*>(tab + tab_base + apos * tab_stride + tab_local);
+#pragma unroll
+          for (int m2 = 0; m2 < 4; ++m2) {
+            const float4 cs = tp[m2];                              // pairs 2 m2, 2 m2 + 1
+            const float2 qa = rope_rotate(bf16lo(qw[2 * m2]), bf16hi(qw[2 * m2]), make_float2(cs.x, cs.y));
+            const float2 qb = rope_rotate(bf16lo(qw[2 * m2 + 1]), bf16hi(qw[2 * m2 + 1]), make_float2(cs.z, cs.w));
+            const float2 ka = rope_rotate(bf16lo(kw[2 * m2]), bf16hi(kw[2 * m2]), make_float2(cs.x, cs.y));
+            const float2 kb = rope_rotate(bf16lo(kw[2 * m2 + 1]), bf16hi(kw[2 * m2 + 1]), make_float2(cs.z, cs.w));
+            qr[4 * m2 + 0] = qa.x; qr[4 * m2 + 1] = qa.y; qr[4 * m2 + 2] = qb.x; qr[4 * m2 + 3] = qb.y;
+            qm = fmaxf(qm, fmaxf(fmaxf(fabsf(qa.x), fabsf(qa.y)), fmaxf(fabsf(qb.x), fabsf(qb.y))));
+            kmax = fmaxf(kmax, fmaxf(fmaxf(fabsf(ka.x), fabsf(ka.y)), fmaxf(fabsf(kb.x), fabsf(kb.y))));
+          }
         }
+        // q: per-row scale, the row's max over its 8 lanes (every lane takes part)
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+        if (valid) {
+          const float qi = qm > 0.f ? kE4M3Max / qm : 0.f;
+          qc.x = e4m3x4(qr[0] * qi, qr[1] * qi, qr[2] * qi, qr[3] * qi);
+          qc.y = e4m3x4(qr[4] * qi, qr[5] * qi, qr[6] * qi, qr[7] * qi);
+          qc.z = e4m3x4(qr[8] * qi, qr[9] * qi, qr[10] * qi, qr[11] * qi);
+          qc.w = e4m3x4(qr[12] * qi, qr[13] * qi, qr[14] * qi, qr[15] * qi);
+          sq = qm > 0.f ? qm / kE4M3Max : 1.f;
+        }
+        *reinterpret_cast<uint4*>(p.q8 + slot * kD8 + cb * 16) = qc;
+        if (cb == 0) p.sq[slot] = sq;
       }
+      // ---- v of rows r0 .. r0 + 3, channels 4 lane .. 4 lane + 3
       uint32_t vc[4];
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
-        const int pos = tile * kTile + r0 + rr;
-        const size_t slot = (size_t)sidx * p.Lp + pos;          // scope-order row
-        uint32_t qc = 0;
-        float sq = 0.f;
-        vc[rr] = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) kr[i][rr][e] = 0.f;
-        if (tok4[rr] >= 0) {
-          int t, hh, w;
-          token_coords(p.rope, tok4[rr], t, hh, w);
-          const uint2 qu = qu4[rr], ku = ku4[rr], vu = vu4[rr];
-          const float2 c0 = tab[pair_index(sel0, t, hh, w)];
-          const float2 c1 = tab[pair_index(sel1, t, hh, w)];
-          const float2 qa = rope_rotate(bf16lo(qu.x), bf16hi(qu.x), c0);
-          const float2 qb = rope_rotate(bf16lo(qu.y), bf16hi(qu.y), c1);
-          const float2 ka = rope_rotate(bf16lo(ku.x), bf16hi(ku.x), c0);
-          const float2 kb = rope_rotate(bf16lo(ku.y), bf16hi(ku.y), c1);
-          kr[i][rr][0] = ka.x; kr[i][rr][1] = ka.y; kr[i][rr][2] = kb.x; kr[i][rr][3] = kb.y;
-          // q: per-row scale
-          float qm = fmaxf(fmaxf(fabsf(qa.x), fabsf(qa.y)), fmaxf(fabsf(qb.x), fabsf(qb.y)));
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
-          const float qi = qm > 0.f ? kE4M3Max / qm : 0.f;
-          qc = e4m3x4(qa.x * qi, qa.y * qi, qb.x * qi, qb.y * qi);
-          sq = qm > 0.f ? qm / kE4M3Max : 1.f;
-          vc[rr] = e4m3x4(bf16lo(vu.x) * inv_v[0], bf16hi(vu.x) * inv_v[1], bf16lo(vu.y) * inv_v[2],
-                          bf16hi(vu.y) * inv_v[3]);
-          kmax = fmaxf(kmax, fmaxf(fmaxf(fabsf(ka.x), fabsf(ka.y)), fmaxf(fabsf(kb.x), fabsf(kb.y))));
-        }
-        *reinterpret_cast<uint32_t*>(p.q8 + slot * kD8 + lane * 4) = qc;
-        if (lane == 0) p.sq[slot] = sq;
+        const uint2 vu = vcur[rr];
+        vc[rr] = e4m3x4(bf16lo(vu.x) * inv_v[0], bf16hi(vu.x) * inv_v[1], bf16lo(vu.y) * inv_v[2],
+                        bf16hi(vu.y) * inv_v[3]);
       }
       // 4 rows x 4 channels of v codes -> channel 4 lane + e gets positions r0 .. r0+3 in one
       // word, stored at word (r0 / 4) ^ lane of the channel's 32 (conflict-free across lanes)
@@ -240,33 +368,57 @@ __global__ void __launch_bounds__(kPrepThreads) skiparse_fwd8_prep_kernel(const 
       vt[(4 * lane + 1) * 32 + wi] = __byte_perm(lo01, lo23, 0x7632);
       vt[(4 * lane + 2) * 32 + wi] = __byte_perm(hi01, hi23, 0x5410);
       vt[(4 * lane + 3) * 32 + wi] = __byte_perm(hi01, hi23, 0x7632);
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) vcur[rr] = vnext[rr];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
     if (lane == 0) rowmax[warp] = kmax;
-    __syncthreads();
+    asm volatile("bar.sync 2, %0;" :: "n"(kPrepCompute) : "memory");
     float tmax = 0.f;
 #pragma unroll
-    for (int w = 0; w < kPrepThreads / 32; ++w) tmax = fmaxf(tmax, rowmax[w]);
+    for (int w = 0; w < kPrepComputeWarps; ++w) tmax = fmaxf(tmax, rowmax[w]);
     const float ki = tmax > 0.f ? kE4M3Max / tmax : 0.f;
     if (threadIdx.x == 0) p.sk[(size_t)sidx * g.n_tiles + tile] = tmax > 0.f ? tmax / kE4M3Max : 1.f;
-    // k: one scale per tile
+    // k: one scale per tile; rows past the scope's end get zero codes
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+      const int r = 4 * (warp + 8 * i) + rq;
+      const int pos = tile * kTile + r;
+      const size_t slot = (size_t)sidx * p.Lp + pos;
+      uint4 kc = make_uint4(0u, 0u, 0u, 0u);
+      if (pos < g.L) {
+        const uint32_t rb = (uint32_t)r * 128u + half_off;
+        uint32_t kw[8];
+        *reinterpret_cast<uint4*>(kw) = *reinterpret_cast<const uint4*>(k_tile + rb + ((chunk0 ^ (uint32_t)(r & 7)) << 4));
+        *reinterpret_cast<uint4*>(kw + 4) =
+            *reinterpret_cast<const uint4*>(k_tile + rb + (((chunk0 + 1u) ^ (uint32_t)(r & 7)) << 4));
+        int t, hh, w;
+        token_coords(p.rope, token_of(g, s, pos), t, hh, w);
+        const int apos = tab_axis == 0 ? t : (tab_axis == 1 ? hh : w);
+        const float4* tp = reinterpret_cast<const float4*>(tab + tab_base + apos * tab_stride + tab_local);
+        uint32_t* kcw = reinterpret_cast<uint32_t*>(&kc);
 #pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const size_t slot = (size_t)sidx * p.Lp + tile * kTile + 4 * (warp + 8 * i) + rr;
-        *reinterpret_cast<uint32_t*>(p.k8 + slot * kD8 + lane * 4) =
-            e4m3x4(kr[i][rr][0] * ki, kr[i][rr][1] * ki, kr[i][rr][2] * ki, kr[i][rr][3] * ki);
+        for (int m2 = 0; m2 < 4; ++m2) {
+          const float4 cs = tp[m2];
+          const float2 ka = rope_rotate(bf16lo(kw[2 * m2]), bf16hi(kw[2 * m2]), make_float2(cs.x, cs.y));
+          const float2 kb = rope_rotate(bf16lo(kw[2 * m2 + 1]), bf16hi(kw[2 * m2 + 1]), make_float2(cs.z, cs.w));
+          kcw[m2] = e4m3x4(ka.x * ki, ka.y * ki, kb.x * ki, kb.y * ki);
+        }
       }
+      *reinterpret_cast<uint4*>(p.k8 + slot * kD8 + cb * 16) = kc;
     }
+    // this warp has read its rows of the staged q / k for the last time: the
+    // slot may be refilled
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(2 + st));
     // V^T rows: channel d of this tile's 128 positions, one word per thread per step
-    for (int idx = threadIdx.x; idx < kD8 * 32; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < kD8 * 32; idx += kPrepCompute) {
       const int d = idx >> 5, c = idx & 31;
       const uint32_t word = vt[d * 32 + (c ^ (d >> 2))];
       *reinterpret_cast<uint32_t*>(p.vt8 + ((size_t)sidx * kD8 + d) * p.Lp + tile * kTile + c * 4) = word;
     }
-    __syncthreads();                   // vt and rowmax are reused by the next item
+    asm volatile("bar.sync 3, %0;" :: "n"(kPrepCompute) : "memory");   // vt and rowmax are reused next
   }
 }
 
@@ -594,20 +746,26 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
 
 size_t fwd8_smem_bytes() { return F8Layout::BYTES; }
 
-size_t fwd8_prep_smem_bytes(int rope_entries) {
-  return prep_table_bytes(rope_entries) + (size_t)kD8 * 32 * 4 + (kPrepThreads / 32) * 4;
+size_t fwd8_prep_smem_bytes(int stages, int rope_entries) { return prep_smem(stages, rope_entries); }
+
+int fwd8_prep_stages(int rope_entries, size_t optin, size_t smem_sm) {
+  const size_t one = prep_smem(1, rope_entries);
+  if (one <= optin && 2 * (one + 1024) <= smem_sm) return 1;      // two CTAs per SM overlap their items
+  for (int st = 2; st >= 1; --st)
+    if (prep_smem(st, rope_entries) <= optin) return st;
+  return 0;
 }
 
 int fwd8_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 2); }
 
 cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream) {
-  const dim3 grid((p.g.N + 255) / 256, p.g.B * p.g.heads);
+  const dim3 grid(p.g.B * p.g.heads, (p.g.N + 255) / 256);
   skiparse_fwd8_vmax_kernel<<<grid, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd8_prep(const Fwd8Params& p, int sms, cudaStream_t stream) {
-  const size_t smem = fwd8_prep_smem_bytes(p.rope.entries);
+  const size_t smem = prep_smem(p.prep_stages, p.rope.entries);
   cudaError_t e = cudaFuncSetAttribute(skiparse_fwd8_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = one_wave(skiparse_fwd8_prep_kernel, p.g.B * p.g.heads * p.g.k * p.g.n_tiles, kPrepThreads, smem, sms);

@@ -53,6 +53,7 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   int smem_optin = 0;
+  int smem_sm = 0;     // shared memory per SM (all resident CTAs)
   int cc = 0;
   int* err_word = nullptr;
 };
@@ -74,7 +75,8 @@ int device_info(DeviceInfo& out) {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
       cudaGetLastError();
       return SKIPARSE_ERR_DEVICE;
     }
@@ -441,8 +443,8 @@ int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out
   if (any_alias({{out, tb}, {lse, lb}, {workspace, w.total}}, {{q, tb}, {k, tb}, {v, tb}})) return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
-  if ((size_t)dev.smem_optin < fwd8_smem_bytes() || (size_t)dev.smem_optin < fwd8_prep_smem_bytes(s.rope_entries))
-    return SKIPARSE_ERR_UNSUPPORTED;
+  const int prep_stages = fwd8_prep_stages(s.rope_entries, (size_t)dev.smem_optin, (size_t)dev.smem_sm);
+  if ((size_t)dev.smem_optin < fwd8_smem_bytes() || prep_stages == 0) return SKIPARSE_ERR_UNSUPPORTED;
 
   Fwd8Params p;
   std::memset(&p, 0, sizeof(p));
@@ -462,12 +464,14 @@ int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out
   p.lse = lse;
   p.err = dev.err_word;
   p.Lp = w.Lp;
+  p.prep_stages = prep_stages;
   p.n_units = fwd8_units(p.g);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const uint64_t Lp = (uint64_t)w.Lp, sc = (uint64_t)w.scopes;
   if (!encode_bytes_3d(&p.tm_q8, p.q8, 128, Lp, sc, 128, 128 * Lp) ||
       !encode_bytes_3d(&p.tm_k8, p.k8, 128, Lp, sc, 128, 128 * Lp) ||
-      !encode_bytes_3d(&p.tm_vt, p.vt8, Lp, 128, sc, Lp, 128 * Lp))
+      !encode_bytes_3d(&p.tm_vt, p.vt8, Lp, 128, sc, Lp, 128 * Lp) || !encode_scope_map(&p.tm_q, q, p.g) ||
+      !encode_scope_map(&p.tm_k, k, p.g))
     return SKIPARSE_ERR_LAUNCH;
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
   if (cudaMemsetAsync(p.vmax, 0, (size_t)B * heads * 128 * 4, stream) != cudaSuccess) return launch_status(cudaErrorUnknown);

@@ -64,6 +64,7 @@ struct BwdParams {
 struct Fwd8Params {
   CUtensorMap tm_q8, tm_k8;       // 8-bit q / k, scope-tile order: (128 bytes, Lp rows, scopes), 128 x 128 boxes
   CUtensorMap tm_vt;              // 8-bit V^T per scope: (Lp keys, 128 channels, scopes), 128 x 128 boxes
+  CUtensorMap tm_q, tm_k;         // bf16 inputs q / k through the scope gather (prep kernel's staged tiles)
   Geom g;
   RopeParams rope;
   const uint16_t* q;              // bf16 (B, N, heads, D) inputs
@@ -80,6 +81,7 @@ struct Fwd8Params {
   int* err;
   int n_units;                    // scopes * ceil(n_tiles / 2)
   int Lp;                         // L rounded up to a multiple of 128
+  int prep_stages;                // prep kernel's q / k staging ring: 1 or 2 tiles
   float scale_log2;               // log2(e) / sqrt(D)
 };
 
@@ -131,7 +133,12 @@ cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t 
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
 
 size_t fwd8_smem_bytes();
-size_t fwd8_prep_smem_bytes(int rope_entries);
+// prep kernel: shared memory for a staging ring of `stages` q / k tiles, and the
+// ring size to launch with: 1 when two such CTAs fit on an SM (`smem_sm` bytes,
+// 1 KB reserved per CTA), else the largest (2, 1) that fits one CTA (`optin`
+// bytes); 0 when none does
+size_t fwd8_prep_smem_bytes(int stages, int rope_entries);
+int fwd8_prep_stages(int rope_entries, size_t optin, size_t smem_sm);
 int fwd8_units(const Geom& g);
 cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream);
 cudaError_t launch_fwd8_prep(const Fwd8Params& p, int sms, cudaStream_t stream);
