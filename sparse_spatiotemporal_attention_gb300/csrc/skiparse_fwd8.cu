@@ -147,12 +147,22 @@ __global__ void __launch_bounds__(128) skiparse_fwd8_vmax_kernel(const __grid_co
   const int t0 = blockIdx.y * 256;
   const int t1 = min(t0 + 256, g.N);
   float mx[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int i = t0 + warp; i < t1; i += 4) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p.v + (((size_t)b * g.N + i) * g.heads + head) * kD8 + lane * 4);
-    mx[0] = fmaxf(mx[0], fabsf(bf16lo(u.x)));
-    mx[1] = fmaxf(mx[1], fabsf(bf16hi(u.x)));
-    mx[2] = fmaxf(mx[2], fabsf(bf16lo(u.y)));
-    mx[3] = fmaxf(mx[3], fabsf(bf16hi(u.y)));
+  // four independent rows per warp and iteration: four loads in flight per lane
+  for (int i0 = t0 + warp; i0 < t1; i0 += 16) {
+    uint2 u[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + 4 * j;
+      u[j] = i < t1 ? __ldg(reinterpret_cast<const uint2*>(p.v + (((size_t)b * g.N + i) * g.heads + head) * kD8 + lane * 4))
+                    : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mx[0] = fmaxf(mx[0], fabsf(bf16lo(u[j].x)));
+      mx[1] = fmaxf(mx[1], fabsf(bf16hi(u[j].x)));
+      mx[2] = fmaxf(mx[2], fabsf(bf16lo(u[j].y)));
+      mx[3] = fmaxf(mx[3], fabsf(bf16hi(u[j].y)));
+    }
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) part[warp][lane * 4 + e] = mx[e];
