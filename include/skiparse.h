@@ -98,10 +98,13 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
  * E4M3 operands for S = Q K^T and O = P V with fp32 accumulation across key
  * blocks. q is quantized after RoPE per (token, head) row, k per block of 128
  * keys of a scope, v per (batch, head, channel); P enters O = P V as E4M3 of
- * 2^8 P. Same arguments, layouts, outputs and errors as skiparse_attn_fwd,
- * with its own workspace (skiparse_attn_fwd_fp8_workspace_bytes(...) bytes,
- * 256-byte aligned, owned by the caller, contents undefined on return);
- * SKIPARSE_ERR_UNSUPPORTED for D != 128. The outputs approximate the bf16
+ * 2^6 P (lazy rescaling at 2^2 keeps it below 256). Same arguments, layouts,
+ * outputs and errors as skiparse_attn_fwd, with its own workspace
+ * (skiparse_attn_fwd_fp8_workspace_bytes(...) bytes, 256-byte aligned, owned
+ * by the caller, contents undefined on return); SKIPARSE_ERR_UNSUPPORTED for
+ * D != 128, and when the RoPE table of the grid (16 T + 24 (H + W) entries of
+ * 8 bytes) does not fit the preparation kernel's shared memory beside one
+ * 64 KB staging slot (about 18,600 entries on sm_103). The outputs approximate the bf16
  * forward to the accuracy of 8-bit operands (a few percent relative).
  */
 size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
