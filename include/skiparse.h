@@ -102,9 +102,8 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
  * outputs and errors as skiparse_attn_fwd, with its own workspace
  * (skiparse_attn_fwd_fp8_workspace_bytes(...) bytes, 256-byte aligned, owned
  * by the caller, contents undefined on return); SKIPARSE_ERR_UNSUPPORTED for
- * D != 128, and when the RoPE table of the grid (16 T + 24 (H + W) entries of
- * 8 bytes) does not fit the preparation kernel's shared memory beside one
- * 64 KB staging slot (about 18,600 entries on sm_103). The outputs approximate the bf16
+ * D != 128 and, as for every entry point, a RoPE table over 8192 pairs
+ * (16 T + 24 (H + W) for D = 128). The outputs approximate the bf16
  * forward to the accuracy of 8-bit operands (a few percent relative).
  */
 size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,

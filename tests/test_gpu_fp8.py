@@ -172,3 +172,23 @@ def test_fp8_forward_prerotated_inputs(env):
     tl.compare("lse", tl.host(lse), rlse, tol_max=tl.TOL_LSE, tol_mean=tl.TOL_LSE, tol_rel=1e-3)
     st, detail = skp.skiparse_device_error()
     assert st == 0, hex(detail)
+
+
+def test_rope_table_limit_rejected_on_the_host(env):
+    """16 T + 24 (H + W) = 8200 RoPE pairs exceed the 8192 every entry point
+    accepts: both forwards refuse the call before any launch (UNSUPPORTED) and
+    leave their outputs untouched."""
+    import torch
+    skp, dev = env
+    T, H, W, heads, D = 1, 1, 340, 1, 128
+    N = T * H * W
+    q = torch.zeros((1, N, heads, D), dtype=torch.bfloat16, device=dev)
+    out = torch.full_like(q, 3.0)
+    lse = torch.full((1, heads, N), 5.0, dtype=torch.float32, device=dev)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    for call in (skp.skiparse_attn_fwd_fp8, skp.skiparse_attn_fwd):
+        with pytest.raises(skp.SkiparseError) as e:
+            call(q, q, q, out, lse, T, H, W, 1, 0, workspace=ws)
+        assert e.value.status == -3
+    torch.cuda.synchronize()
+    assert bool((out == 3.0).all()) and bool((lse == 5.0).all())
