@@ -151,12 +151,17 @@ def test_peaky_softmax_rescale(env):
 def test_index_map_bit_exact(env, mode, N, k):
     import torch
     skp, dev = env
-    if mode == O.GROUP and (N % (k * k) or 128 % k):
-        pytest.skip("not a group-skip shape")
-    if N % k:
-        pytest.skip("not a single-skip shape")
-    scope = torch.empty(N, dtype=torch.int32, device=dev)
-    pos = torch.empty(N, dtype=torch.int32, device=dev)
+    scope = torch.full((N,), -7, dtype=torch.int32, device=dev)
+    pos = torch.full((N,), -7, dtype=torch.int32, device=dev)
+    bad_group = mode == O.GROUP and (N % (k * k) != 0 or 128 % k != 0)
+    if N % k or bad_group:
+        # no such rearrange (N not divisible by k, or by k^2 for group skip): refused, nothing written
+        with pytest.raises(skp.SkiparseError) as e:
+            skp.skiparse_debug_index_map(scope, pos, N, k, mode)
+        assert e.value.status == (-2 if (N % k or N % (k * k)) else -3)
+        torch.cuda.synchronize()
+        assert bool((scope == -7).all()) and bool((pos == -7).all())
+        return
     skp.skiparse_debug_index_map(scope, pos, N, k, mode)
     torch.cuda.synchronize()
     rs, rp = O.index_maps(N, k, mode)
