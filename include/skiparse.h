@@ -247,20 +247,6 @@ int skiparse_debug_rope(const void* x, float* x_rot, int B, int heads, int N, in
  */
 int skiparse_debug_wait_timeout(int code, cudaStream_t stream);
 
-/*
- * Test hook: the two base-2 exponentials the forward kernels' softmax uses for
- * P = 2^(S * scale * log2 e - m) (Open-Sora Plan docs, "Skiparse Attention":
- * attention within each scope is ordinary softmax attention). For i < n,
- * y[i] = 2^x[i] from the FMA-pipe routine (range reduction to [-1/2, 1/2],
- * degree-3 polynomial, exponent added as an integer; arguments below -125 are
- * clamped to -125) when mufu == 0, or from the hardware ex2.approx when
- * mufu == 1. x and y are device float32 arrays of n elements, owned by the
- * caller, 16-byte aligned and not overlapping; arguments must be < 128.
- * Returns SKIPARSE_ERR_INVALID_ARG for n < 0, a null pointer with n > 0 or
- * mufu not 0 / 1, SKIPARSE_ERR_ALIGNMENT and SKIPARSE_ERR_ALIAS as elsewhere.
- */
-int skiparse_debug_exp2(const float* x, float* y, int n, int mufu, cudaStream_t stream);
-
 /* Static, human-readable text for a status code. */
 const char* skiparse_status_string(int status);
 

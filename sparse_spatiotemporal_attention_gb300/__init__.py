@@ -28,7 +28,7 @@ EXPORTS = (
     "skiparse_debug_index_map", "skiparse_debug_rope", "skiparse_status_string",
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
     "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout", "skiparse_attn_bwd_saved",
-    "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8", "skiparse_debug_exp2",
+    "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8",
     "skiparse_qkv_rope",
 )
 
@@ -68,7 +68,6 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_kernel_name": (ctypes.c_char_p, [_c_int]),
         "skiparse_attn_bwd_noalloc": (_c_int, [_vp] * 9 + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_debug_wait_timeout": (_c_int, [_c_int, _vp]),
-        "skiparse_debug_exp2": (_c_int, [_vp, _vp, _c_int, _c_int, _vp]),
         "skiparse_qkv_rope": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _vp]),
         "skiparse_attn_fwd_fp8_workspace_bytes": (_c_size, [_c_int] * 9),
         "skiparse_attn_fwd_fp8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
@@ -243,16 +242,6 @@ def skiparse_qkv_rope(x, w, bias, q, k, v, T, H, W, rope_theta=10000.0, stream=N
     st = load_library().skiparse_qkv_rope(_ptr(x), _ptr(w), _ptr(bias), _ptr(q), _ptr(k), _ptr(v), B, N, C, heads,
                                           D, T, H, W, float(rope_theta), _stream(stream))
     _check(st, "skiparse_qkv_rope")
-
-
-def skiparse_debug_exp2(x, y, mufu=False, stream=None):
-    """y = 2^x (float32 device tensors of equal size) through the softmax's
-    FMA-pipe routine, or the MUFU ex2.approx with mufu=True."""
-    n = x.numel()
-    if y.numel() != n:
-        raise ValueError("x and y must have the same number of elements")
-    _check(load_library().skiparse_debug_exp2(_ptr(x), _ptr(y), n, int(bool(mufu)), _stream(stream)),
-           "skiparse_debug_exp2")
 
 
 def skiparse_device_error():

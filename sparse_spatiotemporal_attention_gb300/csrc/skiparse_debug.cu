@@ -64,33 +64,6 @@ __global__ void skiparse_debug_wait_timeout_kernel(int* err, int code) {
   __syncthreads();
 }
 
-// 2^x element by element, two per thread, through the forward kernels' two
-// routines (FMA-pipe polynomial or MUFU ex2.approx).
-__global__ void skiparse_debug_exp2_kernel(const float* x, float* y, int n, int mufu) {
-  for (long long i = 2 * ((long long)blockIdx.x * blockDim.x + threadIdx.x); i < n;
-       i += 2LL * gridDim.x * blockDim.x) {
-    const bool two = i + 1 < n;
-    const float x0 = x[i], x1 = two ? x[i + 1] : 0.f;
-    float y0, y1;
-    if (mufu) {
-      y0 = ex2(x0);
-      y1 = ex2(x1);
-    } else {
-      exp2_fma_x2(x0, x1, y0, y1);
-    }
-    y[i] = y0;
-    if (two) y[i + 1] = y1;
-  }
-}
-
-cudaError_t launch_debug_exp2(const float* x, float* y, int n, int mufu, cudaStream_t stream) {
-  if (n == 0) return cudaSuccess;
-  long long grid = ((long long)n + 511) / 512;
-  if (grid > 4096) grid = 4096;
-  skiparse_debug_exp2_kernel<<<(int)grid, 256, 0, stream>>>(x, y, n, mufu);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_debug_wait_timeout(int* err, int code, cudaStream_t stream) {
   skiparse_debug_wait_timeout_kernel<<<1, 64, 0, stream>>>(err, code);
   return cudaGetLastError();

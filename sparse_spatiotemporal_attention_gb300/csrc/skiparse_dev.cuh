@@ -166,13 +166,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Byte offset of the 4-byte word `w` (0..31) of row `r` inside a 128-row box
-// written by TMA with 128-byte swizzle: 16-byte chunk c of row r sits at chunk
-// c ^ (r mod 8).
-__device__ __forceinline__ uint32_t sw128_offset(int r, int w) {
-  return (uint32_t)(r * 128 + ((((w >> 2) ^ (r & 7))) << 4) + ((w & 3) << 2));
-}
-
 // ---------------------------------------------------------------------------
 // Shared memory / barriers / bounded waits
 // ---------------------------------------------------------------------------
@@ -308,14 +301,6 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" :: "l"((uint64_t)m) : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];"
-      :: "r"(dst), "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
 // Load into this CTA's shared memory, completing on a barrier that may be in
 // the other CTA of the pair (`bar` a shared::cluster address from mapa_shared).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1) {
@@ -323,17 +308,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];"
       :: "r"(dst), "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// The same load delivered to every CTA of the cluster in `mask`, at the same
-// shared-memory offset, completing on the barrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;"
-      :: "r"(dst), "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
       : "memory");
 }
 
@@ -454,13 +428,6 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
                :: "r"(bar), "h"(mask) : "memory");
 }
 
-// As tc_commit, arriving on the barrier at the same offset in every CTA of the
-// cluster in `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               :: "r"(bar), "h"(mask) : "memory");
-}
-
 // D[tmem] (+)= A[smem desc] * B[smem desc]
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -482,12 +449,6 @@ __device__ __forceinline__ void mma8_ss(uint32_t d, uint64_t a, uint64_t b, uint
                "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
                :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
-__device__ __forceinline__ void mma8_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
-               :: "r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-
 // Instruction descriptor, kind::f8f6f4: E4M3 A and B (format code 0), fp32 D,
 // both K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
@@ -601,24 +562,6 @@ __device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float (&v)[16])
 }
 
 
-// tcgen05.st, 32 lanes x 32 bit, 32 consecutive columns (no wait).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-      :: "r"(taddr),
-         "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-         "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-         "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
-         "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
-         "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
-         "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-}
-
 // Two tcgen05.ld 32x32b.x16 (16 consecutive columns at each of two addresses), one wait.
 __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)[16], float (&b)[16]) {
   uint32_t r[16], q[16];
@@ -640,7 +583,6 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)
   }
 }
 
-// tcgen05.st, 32 lanes x 32 bit, 8 consecutive columns (no wait).
 // tcgen05.ld, 32 lanes x 32 bit, 64 consecutive columns, one wait for all of them.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   uint32_t r[64];
@@ -665,6 +607,7 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// tcgen05.st, 32 lanes x 32 bit, 8 consecutive columns (no wait).
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
@@ -713,33 +656,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^x for two values on the FMA pipe. The softmax's exponentials run at the
-// MUFU's 16 per clock per SM, which matches the bf16 tensor rate of the S and
-// P V products and is half the E4M3 one, so a share of them is computed here.
-// Range reduction: adding 1.5 * 2^23 rounds x to the nearest integer j and
-// leaves j in the low mantissa bits of the sum; subtracting 1.5 * 2^23 back
-// gives j exactly, and f = x - j in [-1/2, 1/2] is exact too. 2^f is a
-// degree-3 polynomial with the least maximum relative error on that interval
-// (Remez exchange, fitted by exp2_poly_fit.py beside this file: 7.5e-5 with
-// float32 Horner steps), and 2^j enters as the integer j << 23 added to the
-// polynomial's bit pattern (its exponent field). x is clamped to -125 from
-// below so that field stays normal; valid for x < 128.
-__device__ __forceinline__ void exp2_fma_x2(float x0, float x1, float& y0, float& y1) {
-  constexpr float kRound = 12582912.0f;                  // 1.5 * 2^23
-  constexpr float kC0 = 0x1.fff692p-1f, kC1 = 0x1.62f31ap-1f, kC2 = 0x1.f0de1ap-3f, kC3 = 0x1.c3f76p-5f;
-  const unsigned long long xx = f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
-  const unsigned long long sh = fadd2(xx, f2_pack(kRound, kRound));
-  const unsigned long long f = fsub2(xx, fsub2(sh, f2_pack(kRound, kRound)));
-  unsigned long long p = ffma2(f, f2_pack(kC3, kC3), f2_pack(kC2, kC2));
-  p = ffma2(p, f, f2_pack(kC1, kC1));
-  p = ffma2(p, f, f2_pack(kC0, kC0));
-  float p0, p1, s0, s1;
-  f2_unpack(p, p0, p1);
-  f2_unpack(sh, s0, s1);
-  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(s0) << 23));
-  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(s1) << 23));
-}
-
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -765,13 +681,6 @@ __device__ __forceinline__ float row_max128(float (&x)[128], int valid) {
     for (int i = 0; i < 4; ++i) mm[i] = fmax3(mm[i], x[e + i], x[e + 4 + i]);
   }
   return fmax3(mm[0], mm[1], fmaxf(mm[2], mm[3]));
-}
-
-// Of every 16 consecutive element pairs of a softmax row chunk, NF take their
-// 2^x from exp2_fma_x2 and the rest from the MUFU, spread evenly.
-template <int NF>
-__host__ __device__ constexpr bool exp2_on_fma(int pair) {
-  return ((pair % 16 + 1) * NF) / 16 > ((pair % 16) * NF) / 16;
 }
 
 }  // namespace skp

@@ -54,11 +54,6 @@ enum FwdBar {
 
 constexpr int kFwdThreads = 320;
 constexpr int kRopeThreads = 256;
-#ifndef SKP_FWD_FMA_PAIRS
-#define SKP_FWD_FMA_PAIRS 0
-#endif
-// element pairs out of every 16 of a softmax row whose 2^x runs on the FMA pipe
-constexpr int kFmaPairs = SKP_FWD_FMA_PAIRS;
 
 // P = 2^(S * sl2 - m) for one softmax row held in registers (x, 128 keys), as
 // bf16 into TMEM at taddr (16 columns per 32 keys, over the row's S columns);
@@ -78,13 +73,7 @@ __device__ __forceinline__ float softmax_p_bf16(const float (&x)[kTile], uint32_
       const int k0 = c * 32 + 2 * e;
       float t0, t1;
       f2_unpack(ffma2(f2_pack(x[k0], x[k0 + 1]), sl2x2, negm2), t0, t1);
-      float a, bb;
-      if (exp2_on_fma<kFmaPairs>(e)) {
-        exp2_fma_x2(t0, t1, a, bb);
-      } else {
-        a = ex2(t0);
-        bb = ex2(t1);
-      }
+      float a = ex2(t0), bb = ex2(t1);
       if constexpr (RAGGED) {
         a = k0 < valid ? a : 0.f;
         bb = k0 + 1 < valid ? bb : 0.f;

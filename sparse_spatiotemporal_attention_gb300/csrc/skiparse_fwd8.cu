@@ -57,11 +57,6 @@ __host__ __device__ constexpr size_t prep_table_bytes(int entries) { return ((si
 __host__ __device__ constexpr size_t prep_smem(int stages, int entries) {
   return 1024 + (size_t)stages * kPrepStage + (size_t)128 * 32 * 4 + prep_table_bytes(entries);
 }
-#ifndef SKP_FWD8_FMA_PAIRS
-#define SKP_FWD8_FMA_PAIRS 0
-#endif
-// element pairs out of every 16 of a softmax row whose 2^x runs on the FMA pipe
-constexpr int kFmaPairs = SKP_FWD8_FMA_PAIRS;
 
 // 2^6 P = 2^(S * ck + off) for one softmax row held in registers (x, 128 keys;
 // off = 6 - m), as E4M3 codes: word w of pk holds keys 4w .. 4w+3, the first
@@ -81,19 +76,7 @@ __device__ __forceinline__ float softmax_p_e4m3(const float (&x)[kTile], uint32_
       float t0, t1, t2, t3;
       f2_unpack(ffma2(f2_pack(x[k0], x[k0 + 1]), ck2, off2), t0, t1);
       f2_unpack(ffma2(f2_pack(x[k0 + 2], x[k0 + 3]), ck2, off2), t2, t3);
-      float p0, p1, p2, p3;
-      if (exp2_on_fma<kFmaPairs>(2 * e)) {
-        exp2_fma_x2(t0, t1, p0, p1);
-      } else {
-        p0 = ex2(t0);
-        p1 = ex2(t1);
-      }
-      if (exp2_on_fma<kFmaPairs>(2 * e + 1)) {
-        exp2_fma_x2(t2, t3, p2, p3);
-      } else {
-        p2 = ex2(t2);
-        p3 = ex2(t3);
-      }
+      float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
       if constexpr (RAGGED) {
         p0 = k0 < valid ? p0 : 0.f;
         p1 = k0 + 1 < valid ? p1 : 0.f;

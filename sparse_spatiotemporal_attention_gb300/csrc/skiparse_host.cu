@@ -28,6 +28,26 @@ using namespace skp;
 
 __device__ int g_skiparse_error_word;
 
+namespace skp {
+
+void* current_context() {
+  typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+}  // namespace skp
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -51,6 +71,7 @@ EncodeTiledFn get_encode_fn() {
 
 struct DeviceInfo {
   bool ready = false;
+  void* ctx = nullptr;  // the context the cached error-word address belongs to
   int sms = 0;
   int smem_optin = 0;
   int smem_sm = 0;     // shared memory per SM (all resident CTAs)
@@ -68,8 +89,12 @@ int device_info(DeviceInfo& out) {
     cudaGetLastError();
     return SKIPARSE_ERR_DEVICE;
   }
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
+  // a new context on this device (a reset, or a caller's own context) holds
+  // its own copy of the library's device variables: look their address up again
+  if (d.ready && d.ctx != ctx) d.ready = false;
   if (!d.ready) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -89,6 +114,7 @@ int device_info(DeviceInfo& out) {
       }
     }
     d.err_word = static_cast<int*>(addr);
+    d.ctx = current_context();   // the runtime makes the primary context current if none was
     d.ready = true;
   }
   if (d.cc != 103) return SKIPARSE_ERR_DEVICE;
@@ -641,17 +667,6 @@ int skiparse_debug_wait_timeout(int code, cudaStream_t stream) {
   int st = device_info(dev);
   if (st != SKIPARSE_OK) return st;
   return launch_status(launch_debug_wait_timeout(dev.err_word, code, stream));
-}
-
-int skiparse_debug_exp2(const float* x, float* y, int n, int mufu, cudaStream_t stream) {
-  if (n < 0 || (mufu != 0 && mufu != 1) || (n > 0 && (!x || !y))) return SKIPARSE_ERR_INVALID_ARG;
-  if (n == 0) return SKIPARSE_OK;
-  if (!aligned16(x) || !aligned16(y)) return SKIPARSE_ERR_ALIGNMENT;
-  if (any_alias({{y, (size_t)n * 4}}, {{x, (size_t)n * 4}})) return SKIPARSE_ERR_ALIAS;
-  DeviceInfo dev;
-  const int st = device_info(dev);
-  if (st != SKIPARSE_OK) return st;
-  return launch_status(launch_debug_exp2(x, y, n, mufu, stream));
 }
 
 int skiparse_qkv_rope(const void* x, const void* w, const void* bias, void* q, void* k, void* v, int B, int N,

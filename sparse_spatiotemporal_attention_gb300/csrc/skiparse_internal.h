@@ -112,6 +112,11 @@ struct DebugParams {
   int* pos_of_token;
 };
 
+// The calling thread's current CUDA context (driver handle), or nullptr. Device
+// variables of this library have one copy per context, so addresses looked up
+// with cudaGetSymbolAddress are cached per (device, context).
+void* current_context();
+
 // Grid-stride row kernels: at most one wave of resident CTAs (SMs x CTAs per SM
 // at this block size and shared memory), so no partial second wave idles SMs.
 template <typename K>
@@ -159,6 +164,5 @@ cudaError_t launch_bwd_post(const BwdParams& p, int grid, int sms, cudaStream_t 
 cudaError_t launch_debug_index_map(const DebugParams& p, cudaStream_t stream);
 cudaError_t launch_debug_rope(const DebugParams& p, cudaStream_t stream);
 cudaError_t launch_debug_wait_timeout(int* err, int code, cudaStream_t stream);
-cudaError_t launch_debug_exp2(const float* x, float* y, int n, int mufu, cudaStream_t stream);
 
 }  // namespace skp

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/skiparse.h"
+#include "skiparse_internal.h"
 
 namespace {
 
@@ -24,18 +25,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+void* g_ctx[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device. In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached. The cache is keyed by the
+// device's current context too: after cudaDeviceReset, or under another
+// context the caller made current, the library's device image (and the array
+// in it) is a different one, so the address is looked up again.
 int scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return SKIPARSE_ERR_DEVICE;
   }
+  void* ctx = skp::current_context();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_addr[dev]) {
+  if (!g_addr[dev] || g_ctx[dev] != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -43,6 +49,7 @@ int scratch_address(void** out) {
       return SKIPARSE_ERR_DEVICE;
     }
     g_addr[dev] = p;
+    g_ctx[dev] = skp::current_context();   // the runtime makes the primary context current if none was
   }
   *out = g_addr[dev];
   return SKIPARSE_OK;

@@ -66,7 +66,8 @@ def test_forward_parity(env, case):
     assert st == 0, hex(detail)
 
 
-BWD_CASES = [c for c in CASES if c[3] * c[4] * c[5] <= 4096]
+# every case up to the 8x32x32 grid (one head, L = 2048: 16 query and 16 key tiles per scope)
+BWD_CASES = [c for c in CASES if c[3] * c[4] * c[5] <= 8192]
 
 
 @pytest.mark.parametrize("case", BWD_CASES, ids=_ids)
@@ -143,7 +144,7 @@ def test_peaky_softmax_rescale(env):
     for name, got, ref in (("out", fw["out"], rout), ("dv", bw["dv"], rdv), ("dk", bw["dk"], rdk),
                            ("dq", bw["dq"], rdq)):
         m = np.abs(ref).max()
-        tl.compare(name, tl.host(got), ref, tol_max=m / 16, tol_mean=m / 256, tol_rel=1e-2)
+        print(tl.compare(name, tl.host(got), ref, tol_max=m / 16, tol_mean=m / 256, tol_rel=1e-2), f"max|ref| {m:.3e}")
 
 
 @pytest.mark.parametrize("mode", [O.SINGLE, O.GROUP])

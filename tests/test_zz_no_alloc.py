@@ -4,9 +4,9 @@ It serves callers that cannot allocate device memory when they run the
 backward; its scratch is a fixed array inside the library. This checks, through
 the C ABI, that two calls in a row (different shapes, so the second call finds
 the first one's leftovers in the shared array) give the same gradients as the
-regular entry point with a caller-provided workspace, within the parity
-tolerances used everywhere else, and that sizes needing more scratch than the
-array holds are refused before anything runs.
+regular entry point with a caller-provided workspace and as the float64
+oracle, within the parity tolerances used everywhere else, and that sizes
+needing more scratch than the array holds are refused before anything runs.
 
 The file is named to be collected last, so a run that stops at the first
 failure has run every other test before this one.
@@ -44,8 +44,11 @@ def test_noalloc_backward_matches_workspace_backward_twice():
                                            B, heads, N, D, T, H, W, k, mode, 10000.0, stream)
         assert st == 0, skp.status_string(st)
         torch.cuda.synchronize()
-        for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        f = tl.f64_inputs(ins)
+        rdq, rdk, rdv, _, _ = O.skiparse_bwd(f["q"], f["k"], f["v"], f["do"], T, H, W, k, mode)
+        for name, got, want in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv)):
             tl.compare(f"call {call} {name}", tl.host(got), tl.host(ref[name]))
+            tl.compare(f"call {call} {name} vs oracle", tl.host(got), want)
         st, detail = skp.skiparse_device_error()
         assert st == 0, hex(detail)
 
