@@ -22,9 +22,11 @@ Printed JSON line (rank 0):
                8x32x32, the group-skip 24x22x40 (B=2) and the long-sequence
                group-skip 16x45x80 (57,600-token) configurations, the group ones
                also at k=1 (rank 0; skipped with --no-fwd-configs, the k=1
-               runs here and the step's k=1 run with --no-k1); each with the 8-bit
-               forward (skiparse_attn_fwd_fp8) beside it, against the FP8 peak
-               taken as the measured bf16 peak x the nominal FP8 / bf16 ratio.
+               runs here and the step's k=1 run with --no-k1), with GB/s of
+               algorithmic bytes; each with the two 8-bit forwards beside it:
+               skiparse_attn_fwd_mixed8 (INT8 S, E4M3 P V) and
+               skiparse_attn_fwd_fp8 (all E4M3, against the FP8 peak taken as
+               the measured bf16 peak x the nominal FP8 / bf16 ratio).
 
 --impl reference times the oracle alone (the reference arm of this method).
 Multi-GPU: one process per GPU (torchrun); every rank runs its own batch
@@ -64,7 +66,8 @@ FWD_CONFIGS = [
     dict(name="skiparse_fwd_group_16x45x80_k4", B=1, heads=24, D=128, T=16, H=45, W=80, k=4, mode=1, k1=True),
 ]
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / bf16 tensor-rate ratio (4.5 / 2.25 PFLOP/s)
-KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0, 4: 0.0, 5: 0.0, 6: 0.0, 7: 1.0}   # x forward FLOPs, per launch
+# x forward FLOPs, per launch, by kernel id
+KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0, 4: 0.0, 5: 0.0, 6: 0.0, 7: 1.0, 8: 0.0, 9: 0.0, 10: 1.0}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -295,30 +298,32 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10, with_k1=True):
                 "heads": heads, "D": D, "grid": f"{T}x{H}x{W}", "N": N, "sparse_k": c["k"], "ms_per_launch": ms,
                 "tflops": tf, "pct_of_peak": {"burst": tf / burst, "sustained": tf / sustained},
                 "gbs": fwd_bytes(c) / (ms * 1e-3) / 1e9, "pct_of_hbm": fwd_bytes(c) / (ms * 1e-3) / 1e9 / hbm}
-        # 8-bit forward on the same inputs (its own workspace; all of its kernels timed)
-        ws8 = torch.empty(skp.skiparse_attn_fwd_fp8_workspace_bytes(B, heads, N, D, T, H, W, c["k"], c["mode"]),
-                          dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            skp.skiparse_attn_fwd_fp8(d["q"], d["k"], d["v"], out, lse, T, H, W, c["k"], c["mode"], stream=stream,
-                                      workspace=ws8)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        skp.skiparse_trace_begin()
-        e0.record(stream)
-        for _ in range(launches):
-            skp.skiparse_attn_fwd_fp8(d["q"], d["k"], d["v"], out, lse, T, H, W, c["k"], c["mode"], stream=stream,
-                                      workspace=ws8)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        kms, kcnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
-        ms8 = e0.elapsed_time(e1) / launches
-        tf8 = fwd_flops(c) / (ms8 * 1e-3) / 1e12
-        line["fp8"] = {"ms_per_launch": ms8, "tflops": tf8, "dtype": "e4m3",
-                       "pct_of_fp8_peak": {"burst": tf8 / (FP8_OVER_BF16 * burst),
-                                           "sustained": tf8 / (FP8_OVER_BF16 * sustained)},
-                       "speedup_vs_bf16": ms / ms8,
-                       "kernels": {skp.KERNEL_NAMES[i]: kms[i] / kcnt[i] for i in range(len(kcnt)) if kcnt[i]}}
-        del ws8
+        # the two 8-bit forwards on the same inputs (own workspaces; all of their kernels timed)
+        for key, call in (("fp8", "skiparse_attn_fwd_fp8"), ("mixed8", "skiparse_attn_fwd_mixed8")):
+            fn = getattr(skp, call)
+            ws8 = torch.empty(getattr(skp, call + "_workspace_bytes")(B, heads, N, D, T, H, W, c["k"], c["mode"]),
+                              dtype=torch.uint8, device=dev)
+            for _ in range(3):
+                fn(d["q"], d["k"], d["v"], out, lse, T, H, W, c["k"], c["mode"], stream=stream, workspace=ws8)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            skp.skiparse_trace_begin()
+            e0.record(stream)
+            for _ in range(launches):
+                fn(d["q"], d["k"], d["v"], out, lse, T, H, W, c["k"], c["mode"], stream=stream, workspace=ws8)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            kms, kcnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
+            ms8 = e0.elapsed_time(e1) / launches
+            tf8 = fwd_flops(c) / (ms8 * 1e-3) / 1e12
+            line[key] = {"ms_per_launch": ms8, "tflops": tf8,
+                         "dtype": "e4m3" if key == "fp8" else "int8 (S) + e4m3 (P V)",
+                         "speedup_vs_bf16": ms / ms8,
+                         "kernels": {skp.KERNEL_NAMES[i]: kms[i] / kcnt[i] for i in range(len(kcnt)) if kcnt[i]}}
+            if key == "fp8":
+                line[key]["pct_of_fp8_peak"] = {"burst": tf8 / (FP8_OVER_BF16 * burst),
+                                                "sustained": tf8 / (FP8_OVER_BF16 * sustained)}
+            del ws8
         if c["k1"] and with_k1:
             ms1 = timed(1)
             line["k1"] = {"ms_per_launch": ms1, "tflops": fwd_flops(c, 1) / (ms1 * 1e-3) / 1e12,

@@ -93,18 +93,25 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
- * 8-bit forward pass (D = 128): the Wan 2.1 report, section 4.4.3
- * "Quantization", paragraph "8-Bit FlashAttention", applied to this forward:
- * E4M3 operands for S = Q K^T and O = P V with fp32 accumulation across key
- * blocks. q is quantized after RoPE per (token, head) row, k per block of 128
- * keys of a scope, v per (batch, head, channel); P enters O = P V as E4M3 of
- * 2^6 P (lazy rescaling at 2^2 keeps it below 256). Same arguments, layouts,
- * outputs and errors as skiparse_attn_fwd, with its own workspace
- * (skiparse_attn_fwd_fp8_workspace_bytes(...) bytes, 256-byte aligned, owned
+ * 8-bit forward passes (D = 128): the Wan 2.1 report, section 4.4.3
+ * "Quantization", paragraph "8-Bit FlashAttention", applied to this forward.
+ * Both quantize q after RoPE per (token, head) row, k after RoPE per block of
+ * 128 keys of a scope, and v per (batch, head, channel) to E4M3, and feed
+ * O = P V with E4M3(2^8 P), P taken relative to an integer base-2 row reference
+ * (P <= 1), accumulating across key blocks in fp32 tensor memory.
+ *   skiparse_attn_fwd_mixed8: the paragraph's "Mixed 8-Bit optimization":
+ *     INT8 q and k (scale max|x| / 127) for S = Q K^T. The integer dot
+ *     products are exact (the codes run through the bf16 tensor path, where
+ *     every INT8 value and every partial sum is exact in fp32).
+ *   skiparse_attn_fwd_fp8: E4M3 q and k for S as well (FlashAttention-3's
+ *     native FP8, the recipe the paragraph reports to lose quality), kept for
+ *     comparison: faster on this GPU, less accurate.
+ * Same arguments, layouts, outputs and errors as skiparse_attn_fwd, each with
+ * its own workspace (..._workspace_bytes(...) bytes, 256-byte aligned, owned
  * by the caller, contents undefined on return); SKIPARSE_ERR_UNSUPPORTED for
  * D != 128 and, as for every entry point, a RoPE table over 8192 pairs
- * (16 T + 24 (H + W) for D = 128). The outputs approximate the bf16
- * forward to the accuracy of 8-bit operands (a few percent relative).
+ * (16 T + 24 (H + W) for D = 128). The outputs approximate the bf16 forward
+ * to the accuracy of 8-bit operands (a few percent relative).
  */
 size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
                                              int sparse_k, int mode);
@@ -112,6 +119,12 @@ int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out
                           void* workspace, size_t workspace_bytes,
                           int B, int heads, int N, int D, int T, int H, int W,
                           int sparse_k, int mode, float rope_theta, cudaStream_t stream);
+size_t skiparse_attn_fwd_mixed8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
+                                                int sparse_k, int mode);
+int skiparse_attn_fwd_mixed8(const void* q, const void* k, const void* v, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes,
+                             int B, int heads, int N, int D, int T, int H, int W,
+                             int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
  * Bytes of device workspace skiparse_attn_bwd needs for these sizes: an fp32

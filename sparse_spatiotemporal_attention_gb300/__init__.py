@@ -18,7 +18,8 @@ SINGLE = 0
 GROUP = 1
 KERNEL_NAMES = ("skiparse_fwd_kernel", "skiparse_bwd_pre_kernel", "skiparse_bwd_main_kernel",
                 "skiparse_bwd_post_kernel", "skiparse_fwd_rope_kernel", "skiparse_fwd8_vmax_kernel",
-                "skiparse_fwd8_prep_kernel", "skiparse_fwd8_kernel", "skiparse_qkv_rope_kernel")
+                "skiparse_fwd8_prep_kernel", "skiparse_fwd8_kernel", "skiparse_qkv_rope_kernel",
+                "skiparse_fwdm8_prep_kernel", "skiparse_fwdm8_kernel")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libskiparse.so")
@@ -29,6 +30,7 @@ EXPORTS = (
     "skiparse_device_error", "skiparse_trace_begin", "skiparse_trace_end", "skiparse_kernel_name",
     "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout", "skiparse_attn_bwd_saved",
     "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8",
+    "skiparse_attn_fwd_mixed8_workspace_bytes", "skiparse_attn_fwd_mixed8",
     "skiparse_qkv_rope",
 )
 
@@ -71,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_qkv_rope": (_c_int, [_vp] * 6 + [_c_int] * 8 + [_c_float, _vp]),
         "skiparse_attn_fwd_fp8_workspace_bytes": (_c_size, [_c_int] * 9),
         "skiparse_attn_fwd_fp8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
+        "skiparse_attn_fwd_mixed8_workspace_bytes": (_c_size, [_c_int] * 9),
+        "skiparse_attn_fwd_mixed8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_bwd_saved": (_c_int, [_vp, _c_size] + [_vp] * 8 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
     }
     for name, (res, args) in sig.items():
@@ -142,21 +146,39 @@ def skiparse_attn_fwd_fp8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mod
     return int(load_library().skiparse_attn_fwd_fp8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode))
 
 
-def skiparse_attn_fwd_fp8(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=10000.0, stream=None,
-                          workspace=None, workspace_bytes=None):
-    """8-bit forward pass (D = 128) into caller-allocated out and lse; `workspace`
-    as for skiparse_attn_fwd, sized by skiparse_attn_fwd_fp8_workspace_bytes(...)."""
+def skiparse_attn_fwd_mixed8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode) -> int:
+    return int(load_library().skiparse_attn_fwd_mixed8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode))
+
+
+def _fwd8(name, q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, workspace, workspace_bytes):
+    lib = load_library()
     B, heads, N, D = _shape(q)
     if workspace is None:
         import torch
-        nbytes = skiparse_attn_fwd_fp8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode)
+        nbytes = getattr(lib, name + "_workspace_bytes")(B, heads, N, D, T, H, W, sparse_k, mode)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
-    st = load_library().skiparse_attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
-                                              int(workspace_bytes), B, heads, N, D, T, H, W, sparse_k, mode,
-                                              float(rope_theta), _stream(stream))
-    _check(st, "skiparse_attn_fwd_fp8")
+    st = getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                            B, heads, N, D, T, H, W, sparse_k, mode, float(rope_theta), _stream(stream))
+    _check(st, name)
+
+
+def skiparse_attn_fwd_fp8(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=10000.0, stream=None,
+                          workspace=None, workspace_bytes=None):
+    """8-bit forward pass with E4M3 q, k, v and P (D = 128) into caller-allocated
+    out and lse; `workspace` as for skiparse_attn_fwd, sized by
+    skiparse_attn_fwd_fp8_workspace_bytes(...)."""
+    _fwd8("skiparse_attn_fwd_fp8", q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, workspace,
+          workspace_bytes)
+
+
+def skiparse_attn_fwd_mixed8(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=10000.0, stream=None,
+                             workspace=None, workspace_bytes=None):
+    """8-bit forward pass with INT8 q, k for S and E4M3 P, v for P V (D = 128);
+    `workspace` sized by skiparse_attn_fwd_mixed8_workspace_bytes(...)."""
+    _fwd8("skiparse_attn_fwd_mixed8", q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, workspace,
+          workspace_bytes)
 
 
 def skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode) -> int:

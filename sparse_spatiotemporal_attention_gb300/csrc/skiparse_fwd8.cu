@@ -4,17 +4,28 @@
 // across key blocks), applied to the Skiparse forward pass of "Open-Sora Plan"
 // docs, "Skiparse Attention". D = 128.
 //
-// Quantization (readings, the page gives the recipe for Hopper):
-//   * E4M3 for both products (the page's INT8 for Q K^T is not a fast tensor
-//     path here); q after RoPE per (token, head) row, k after RoPE per block of
-//     128 consecutive keys of a scope (one scale per K tile), v per (batch,
-//     head, channel) over all tokens; scale = max|x| / 448, codes
-//     RNE(x * 448 / max|x|);
-//   * P = 2^(S * scale * log2 e - m) enters O = P V as RNE_E4M3(2^6 P); the row
-//     sum adds the unquantized P; O accumulates in fp32 TMEM across K tiles;
-//   * online softmax with lazy rescaling only when a K tile's row max exceeds
-//     the running max by more than 2^2 (2^8 in the fp32 kernel): P < 2^2 then,
-//     so 2^6 P < 256 never saturates E4M3 (448).
+// Two recipes share these kernels (template parameter SI8):
+//   * SI8 = true, the page's "Mixed 8-Bit optimization": INT8 q and k for
+//     S = Q K^T, E4M3 P and v for O = P V. sm_103a has no 8-bit integer MMA
+//     (ptxas: ".kind::i8 not supported on .target 'sm_103a'"), so the INT8
+//     codes are stored as bf16 values (every integer up to 256 is exact in
+//     bf16) and S runs as a kind::f16 MMA: every product is an integer below
+//     2^14 and every partial sum of a 128-channel row an integer below 2^21,
+//     all exact in the fp32 accumulator, so S is the exact INT8 dot product;
+//   * SI8 = false, FlashAttention-3's native FP8: E4M3 q, k, v and P
+//     (kind::f8f6f4 for both products), the recipe the page improves on.
+// Quantization (readings; the page gives the recipe for Hopper): q after RoPE
+// per (token, head) row, k after RoPE per block of 128 consecutive keys of a
+// scope (one scale per K tile), v per (batch, head, channel) over all tokens;
+// scale = max|x| / Q, codes RNE(x * Q / max|x|), Q = 127 (INT8) or 448 (E4M3).
+// P relative to an integer base-2 row reference M enters O = P V as
+// E4M3(2^8 P); O accumulates in fp32 TMEM across K tiles (the tensor memory
+// accumulator is fp32, which is what the page's "FP32 accumulation for
+// cross-block reduction" asks of the Hopper register path). The kernel keeps
+// an integer reference m <= M (raised to the ceiling of a K tile's row max only
+// when that exceeds m by more than 2) and quantizes 2^6 * 2^(t - m), which is
+// E4M3(2^8 P) times the exact power of two 2^(M - m - 2): the same codes in
+// E4M3's normal range, never above 256 < 448.
 //
 // Kernels:
 //   skiparse_fwd8_vmax_kernel   max |v| per (b, head, channel) (atomicMax on the
@@ -48,6 +59,16 @@ constexpr int kPrepCompute = kPrepComputeWarps * 32;
 constexpr int kPrepHalf = 128 * 128;                          // 128 rows x 64 bf16 channels, 128-byte swizzle
 constexpr int kPrepStage = 4 * kPrepHalf;                     // q and k tiles, two channel halves each
 constexpr float kE4M3Max = 448.0f;
+constexpr float kInt8Max = 127.0f;
+
+// bytes of one 128-channel row of q / k codes: E4M3 (1 byte each) or INT8
+// codes held as bf16 integers (2 bytes each, the operands of a kind::f16 MMA)
+__host__ __device__ constexpr int qk_row_bytes(bool si8) { return si8 ? 256 : 128; }
+
+// two INT8 codes RNE(a), RNE(b) (clamped to +-127) as a bf16 pair
+__device__ __forceinline__ uint32_t i8x2_bf16(float a, float b) {
+  return pack_bf16(fminf(fmaxf(rintf(a), -kInt8Max), kInt8Max), fminf(fmaxf(rintf(b), -kInt8Max), kInt8Max));
+}
 
 // RoPE table bytes in the prep kernel's shared memory, rounded up to 16
 __host__ __device__ constexpr size_t prep_table_bytes(int entries) { return ((size_t)entries * 8 + 15) & ~(size_t)15; }
@@ -94,13 +115,15 @@ __device__ __forceinline__ float softmax_p_e4m3(const float (&x)[kTile], uint32_
   return (s0 + s1) + (s2 + s3);
 }
 
+template <bool SI8>
 struct F8Layout {
   static constexpr int TILE = 128 * 128;          // 16 KB: 128 rows x 128 bytes, one 128-byte swizzled box
+  static constexpr int QK = 128 * qk_row_bytes(SI8);   // a Q or K tile: one E4M3 box, or two bf16 boxes
   static constexpr int HDR = 1024;
   static constexpr int QA_OFF = HDR;
-  static constexpr int QB_OFF = QA_OFF + TILE;
-  static constexpr int K_OFF = QB_OFF + TILE;
-  static constexpr int V_OFF = K_OFF + 2 * TILE;
+  static constexpr int QB_OFF = QA_OFF + QK;
+  static constexpr int K_OFF = QB_OFF + QK;
+  static constexpr int V_OFF = K_OFF + 2 * QK;
   static constexpr int PA_OFF = V_OFF + 2 * TILE;   // P of Q tile A as E4M3 codes (A operand of P V)
   static constexpr int PB_OFF = PA_OFF + TILE;
   static constexpr int BYTES = PB_OFF + TILE;
@@ -163,7 +186,10 @@ __global__ void __launch_bounds__(128) skiparse_fwd8_vmax_kernel(const __grid_co
 // next tiles load while the compute warps work on this one (two CTAs per SM
 // when their shared memory fits: one slot each); v rows are read directly, a
 // group of four rows ahead.
-__global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwd8_prep_kernel(const __grid_constant__ Fwd8Params p) {
+template <bool SI8>
+__device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
+  constexpr float QMAX = SI8 ? kInt8Max : kE4M3Max;
+  constexpr int QROW = qk_row_bytes(SI8);
   extern __shared__ __align__(1024) uint8_t psm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((smem_u32(psm) & 1023u) != 0) {
@@ -299,7 +325,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwd8_prep_kernel(con
         const int pos = tile * kTile + r;
         const size_t slot = (size_t)sidx * p.Lp + pos;          // scope-order row
         const bool valid = pos < g.L;                // not warp-uniform: four rows per warp
-        uint4 qc = make_uint4(0u, 0u, 0u, 0u);
+        uint4 qc = make_uint4(0u, 0u, 0u, 0u), qc2 = make_uint4(0u, 0u, 0u, 0u);
         float sq = 0.f;
         float qr[16];
         float qm = 0.f;
@@ -334,14 +360,31 @@ __global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwd8_prep_kernel(con
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
         if (valid) {
-          const float qi = qm > 0.f ? kE4M3Max / qm : 0.f;
-          qc.x = e4m3x4(qr[0] * qi, qr[1] * qi, qr[2] * qi, qr[3] * qi);
-          qc.y = e4m3x4(qr[4] * qi, qr[5] * qi, qr[6] * qi, qr[7] * qi);
-          qc.z = e4m3x4(qr[8] * qi, qr[9] * qi, qr[10] * qi, qr[11] * qi);
-          qc.w = e4m3x4(qr[12] * qi, qr[13] * qi, qr[14] * qi, qr[15] * qi);
-          sq = qm > 0.f ? qm / kE4M3Max : 1.f;
+          const float qi = qm > 0.f ? QMAX / qm : 0.f;
+          if constexpr (SI8) {
+            qc.x = i8x2_bf16(qr[0] * qi, qr[1] * qi);
+            qc.y = i8x2_bf16(qr[2] * qi, qr[3] * qi);
+            qc.z = i8x2_bf16(qr[4] * qi, qr[5] * qi);
+            qc.w = i8x2_bf16(qr[6] * qi, qr[7] * qi);
+            qc2.x = i8x2_bf16(qr[8] * qi, qr[9] * qi);
+            qc2.y = i8x2_bf16(qr[10] * qi, qr[11] * qi);
+            qc2.z = i8x2_bf16(qr[12] * qi, qr[13] * qi);
+            qc2.w = i8x2_bf16(qr[14] * qi, qr[15] * qi);
+          } else {
+            qc.x = e4m3x4(qr[0] * qi, qr[1] * qi, qr[2] * qi, qr[3] * qi);
+            qc.y = e4m3x4(qr[4] * qi, qr[5] * qi, qr[6] * qi, qr[7] * qi);
+            qc.z = e4m3x4(qr[8] * qi, qr[9] * qi, qr[10] * qi, qr[11] * qi);
+            qc.w = e4m3x4(qr[12] * qi, qr[13] * qi, qr[14] * qi, qr[15] * qi);
+          }
+          sq = qm > 0.f ? qm / QMAX : 1.f;
         }
-        *reinterpret_cast<uint4*>(p.q8 + slot * kD8 + cb * 16) = qc;
+        if constexpr (SI8) {
+          uint4* dst = reinterpret_cast<uint4*>(p.q8 + slot * QROW + cb * 32);
+          dst[0] = qc;
+          dst[1] = qc2;
+        } else {
+          *reinterpret_cast<uint4*>(p.q8 + slot * QROW + cb * 16) = qc;
+        }
         if (cb == 0) p.sq[slot] = sq;
       }
       // ---- v of rows r0 .. r0 + 3, channels 4 lane .. 4 lane + 3
@@ -371,15 +414,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwd8_prep_kernel(con
     float tmax = 0.f;
 #pragma unroll
     for (int w = 0; w < kPrepComputeWarps; ++w) tmax = fmaxf(tmax, rowmax[w]);
-    const float ki = tmax > 0.f ? kE4M3Max / tmax : 0.f;
-    if (threadIdx.x == 0) p.sk[(size_t)sidx * g.n_tiles + tile] = tmax > 0.f ? tmax / kE4M3Max : 1.f;
+    const float ki = tmax > 0.f ? QMAX / tmax : 0.f;
+    if (threadIdx.x == 0) p.sk[(size_t)sidx * g.n_tiles + tile] = tmax > 0.f ? tmax / QMAX : 1.f;
     // k: one scale per tile; rows past the scope's end get zero codes
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = 4 * (warp + 8 * i) + rq;
       const int pos = tile * kTile + r;
       const size_t slot = (size_t)sidx * p.Lp + pos;
-      uint4 kc = make_uint4(0u, 0u, 0u, 0u);
+      uint4 kc = make_uint4(0u, 0u, 0u, 0u), kc2 = make_uint4(0u, 0u, 0u, 0u);
       if (pos < g.L) {
         const uint32_t rb = (uint32_t)r * 128u + half_off;
         uint32_t kw[8];
@@ -391,15 +434,29 @@ __global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwd8_prep_kernel(con
         const int apos = tab_axis == 0 ? t : (tab_axis == 1 ? hh : w);
         const float4* tp = reinterpret_cast<const float4*>(tab + tab_base + apos * tab_stride + tab_local);
         uint32_t* kcw = reinterpret_cast<uint32_t*>(&kc);
+        uint32_t* kcw2 = reinterpret_cast<uint32_t*>(&kc2);
 #pragma unroll
         for (int m2 = 0; m2 < 4; ++m2) {
           const float4 cs = tp[m2];
           const float2 ka = rope_rotate(bf16lo(kw[2 * m2]), bf16hi(kw[2 * m2]), make_float2(cs.x, cs.y));
           const float2 kb = rope_rotate(bf16lo(kw[2 * m2 + 1]), bf16hi(kw[2 * m2 + 1]), make_float2(cs.z, cs.w));
-          kcw[m2] = e4m3x4(ka.x * ki, ka.y * ki, kb.x * ki, kb.y * ki);
+          if constexpr (SI8) {
+            // channels 4 m2 .. 4 m2 + 3 of this lane's 16: words 2 m2, 2 m2 + 1 of 8
+            uint32_t* w = m2 < 2 ? kcw : kcw2;
+            w[(2 * m2) & 3] = i8x2_bf16(ka.x * ki, ka.y * ki);
+            w[(2 * m2 + 1) & 3] = i8x2_bf16(kb.x * ki, kb.y * ki);
+          } else {
+            kcw[m2] = e4m3x4(ka.x * ki, ka.y * ki, kb.x * ki, kb.y * ki);
+          }
         }
       }
-      *reinterpret_cast<uint4*>(p.k8 + slot * kD8 + cb * 16) = kc;
+      if constexpr (SI8) {
+        uint4* dst = reinterpret_cast<uint4*>(p.k8 + slot * QROW + cb * 32);
+        dst[0] = kc;
+        dst[1] = kc2;
+      } else {
+        *reinterpret_cast<uint4*>(p.k8 + slot * QROW + cb * 16) = kc;
+      }
     }
     // this warp has read its rows of the staged q / k for the last time: the
     // slot may be refilled
@@ -415,11 +472,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwd8_prep_kernel(con
   }
 }
 
+__global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwd8_prep_kernel(const __grid_constant__ Fwd8Params p) {
+  fwd8_prep<false>(p);
+}
+__global__ void __launch_bounds__(kPrepThreads, 2) skiparse_fwdm8_prep_kernel(const __grid_constant__ Fwd8Params p) {
+  fwd8_prep<true>(p);
+}
+
 // ---------------------------------------------------------------------------
 // attention over 8-bit operands
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __grid_constant__ Fwd8Params p) {
-  using Ly = F8Layout;
+template <bool SI8>
+__device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
+  using Ly = F8Layout<SI8>;
   constexpr int D = kD8;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
@@ -477,9 +542,17 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
       const int pair = u % n_pairs, sidx = u / n_pairs;
       if (it > 0 && !warp_wait(E_QEMPTY, (it - 1) & 1)) break;
       if (leader) {
-        mbar_expect_tx(bar(E_QFULL), 2 * Ly::TILE);
-        tma_load_3d(sQA, &p.tm_q8, bar(E_QFULL), 0, 2 * pair * kTile, sidx);
-        tma_load_3d(sQB, &p.tm_q8, bar(E_QFULL), 0, (2 * pair + 1) * kTile, sidx);
+        mbar_expect_tx(bar(E_QFULL), 2 * Ly::QK);
+        if constexpr (SI8) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_3d(sQA + h * kHalfBytes, &p.tm_q8, bar(E_QFULL), h * 64, 2 * pair * kTile, sidx);
+            tma_load_3d(sQB + h * kHalfBytes, &p.tm_q8, bar(E_QFULL), h * 64, (2 * pair + 1) * kTile, sidx);
+          }
+        } else {
+          tma_load_3d(sQA, &p.tm_q8, bar(E_QFULL), 0, 2 * pair * kTile, sidx);
+          tma_load_3d(sQB, &p.tm_q8, bar(E_QFULL), 0, (2 * pair + 1) * kTile, sidx);
+        }
       }
       __syncwarp();
       ++q_issued;
@@ -489,8 +562,14 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
         const uint32_t n = gg >> 1;
         if (n > 0 && !warp_wait(E_KEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
         if (leader) {
-          mbar_expect_tx(bar(E_KFULL0 + st), Ly::TILE);
-          tma_load_3d(sK + st * Ly::TILE, &p.tm_k8, bar(E_KFULL0 + st), 0, j * kTile, sidx);
+          mbar_expect_tx(bar(E_KFULL0 + st), Ly::QK);
+          if constexpr (SI8) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(sK + st * Ly::QK + h * kHalfBytes, &p.tm_k8, bar(E_KFULL0 + st), h * 64, j * kTile, sidx);
+          } else {
+            tma_load_3d(sK + st * Ly::QK, &p.tm_k8, bar(E_KFULL0 + st), 0, j * kTile, sidx);
+          }
         }
         __syncwarp();
         ++k_issued[st];
@@ -519,8 +598,9 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
     // cycles per MMA issuing than the MMA runs).
     const int xb = warp - 9;
     constexpr uint32_t kId = idesc_e4m3(128, 128);
+    constexpr uint32_t kIdS = SI8 ? idesc_bf16(128, 128, false, false) : kId;
     const uint64_t dQ = desc_kmajor(xb ? sQB : sQA, 0);
-    const uint64_t dK0 = desc_kmajor(sK, 0), dK1 = desc_kmajor(sK + Ly::TILE, 0);
+    const uint64_t dK0 = desc_kmajor(sK, 0), dK1 = desc_kmajor(sK + Ly::QK, 0);
     const uint64_t dV0 = desc_kmajor(sV, 0), dV1 = desc_kmajor(sV + Ly::TILE, 0);
     const uint64_t dP = desc_kmajor(xb ? sPB : sPA, 0);
     const uint32_t colS = xb ? 128u : 0u;
@@ -530,11 +610,19 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
     const int barP = xb ? E_PFULL_B : E_PFULL_A;
     const int barO = xb ? E_ODONE_B : E_ODONE_A;
     const int barOE = xb ? E_OEMPTY_B : E_OEMPTY_A;
-    // S_X = Q_X K_g^T (4 k-steps of 32 bytes)
+    // S_X = Q_X K_g^T: 4 E4M3 k-steps of 32 channels, or 8 bf16 k-steps of 16
+    // channels over INT8-valued codes (exact integer sums in fp32)
     auto issue_s = [&](int st) {
       const uint64_t dk = st ? dK1 : dK0;
+      if constexpr (SI8) {
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) mma8_ss(tmem + colS, kmajor_step(dQ, ks), kmajor_step(dk, ks), kId, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tmem + colS, kmajor_step(dQ, ks), kmajor_step(dk, ks), kIdS, ks > 0 ? 1u : 0u);
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma8_ss(tmem + colS, kmajor_step(dQ, ks), kmajor_step(dk, ks), kIdS, ks > 0 ? 1u : 0u);
+      }
     };
     // O_X += P_X V_g: P_X as E4M3 codes in shared memory (K-major), V^T K-major
     auto issue_pv = [&](int st, bool first) {
@@ -639,13 +727,15 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
         const float mx = (valid == kTile ? row_max128<false>(x, valid) : row_max128<true>(x, valid)) * ck;
         float f = 1.f;
         bool rescale = false;
+        // integer reference m, raised to ceil(max) only when the tile's max
+        // exceeds it by more than 2: 2^(t - m) < 4, and rescales are powers of two
         if (j == 0) {
-          m = mx;
+          m = ceilf(mx);
         } else {
           const bool need = mx > m + 2.0f;
           rescale = __any_sync(0xffffffffu, need);
           if (rescale) {
-            const float m_new = need ? mx : m;
+            const float m_new = need ? ceilf(mx) : m;
             f = ex2(m - m_new);
             m = m_new;
             l *= f;
@@ -737,7 +827,16 @@ __global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __gr
   }
 }
 
-size_t fwd8_smem_bytes() { return F8Layout::BYTES; }
+__global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwd8_kernel(const __grid_constant__ Fwd8Params p) {
+  fwd8_attention<false>(p);
+}
+__global__ void __launch_bounds__(kF8Threads, 1) skiparse_fwdm8_kernel(const __grid_constant__ Fwd8Params p) {
+  fwd8_attention<true>(p);
+}
+
+size_t fwd8_smem_bytes(bool si8) { return si8 ? F8Layout<true>::BYTES : F8Layout<false>::BYTES; }
+
+size_t fwd8_qk_row_bytes(bool si8) { return (size_t)qk_row_bytes(si8); }
 
 size_t fwd8_prep_smem_bytes(int stages, int rope_entries) { return prep_smem(stages, rope_entries); }
 
@@ -757,20 +856,22 @@ cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd8_prep(const Fwd8Params& p, int sms, cudaStream_t stream) {
+cudaError_t launch_fwd8_prep(const Fwd8Params& p, bool si8, int sms, cudaStream_t stream) {
   const size_t smem = prep_smem(p.prep_stages, p.rope.entries);
-  cudaError_t e = cudaFuncSetAttribute(skiparse_fwd8_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kernel = si8 ? skiparse_fwdm8_prep_kernel : skiparse_fwd8_prep_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = one_wave(skiparse_fwd8_prep_kernel, p.g.B * p.g.heads * p.g.k * p.g.n_tiles, kPrepThreads, smem, sms);
-  skiparse_fwd8_prep_kernel<<<grid, kPrepThreads, smem, stream>>>(p);
+  const int grid = one_wave(kernel, p.g.B * p.g.heads * p.g.k * p.g.n_tiles, kPrepThreads, smem, sms);
+  kernel<<<grid, kPrepThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd8(const Fwd8Params& p, int grid, cudaStream_t stream) {
-  const size_t smem = fwd8_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(skiparse_fwd8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t launch_fwd8(const Fwd8Params& p, bool si8, int grid, cudaStream_t stream) {
+  const size_t smem = fwd8_smem_bytes(si8);
+  auto kernel = si8 ? skiparse_fwdm8_kernel : skiparse_fwd8_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  skiparse_fwd8_kernel<<<grid, kF8Threads, smem, stream>>>(p);
+  kernel<<<grid, kF8Threads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -298,22 +298,39 @@ bool encode_bytes_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
   return r == CUDA_SUCCESS;
 }
 
-// 8-bit forward workspace: E4M3 q, k (scopes, Lp, 128) and V^T (scopes, 128, Lp),
-// q scales per scope-order row, k scales per K tile, max |v| per (b, head, channel).
+// 3-D bf16 tensor map, 64-element x 128-row boxes with 128-byte swizzle: dims
+// (d0 innermost, d1, d2), byte strides s1, s2; reads past an edge fill zeros.
+bool encode_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 8-bit forward workspace: q, k codes (scopes, Lp, 128) (E4M3 bytes, or INT8
+// codes as bf16 for the mixed recipe) and E4M3 V^T (scopes, 128, Lp), q scales
+// per scope-order row, k scales per K tile, max |v| per (b, head, channel).
 struct Ws8Layout {
   size_t q8, k8, vt8, sq, sk, vmax, total;
   int Lp, scopes;
 };
 
-Ws8Layout ws8_layout(const Shape& s) {
+Ws8Layout ws8_layout(const Shape& s, bool si8) {
   Ws8Layout w;
   const int L = s.N / s.k;
   w.Lp = ((L + kTile - 1) / kTile) * kTile;
   w.scopes = s.B * s.heads * s.k;
   const size_t rows = (size_t)w.scopes * w.Lp;
+  const size_t qk_row = fwd8_qk_row_bytes(si8);
   size_t off = 0;
-  w.q8 = off;   off += align256(rows * 128);
-  w.k8 = off;   off += align256(rows * 128);
+  w.q8 = off;   off += align256(rows * qk_row);
+  w.k8 = off;   off += align256(rows * qk_row);
   w.vt8 = off;  off += align256(rows * 128);
   w.sq = off;   off += align256(rows * 4);
   w.sk = off;   off += align256((size_t)w.scopes * (w.Lp / kTile) * 4);
@@ -387,6 +404,8 @@ const char* skiparse_kernel_name(int id) {
     case 6: return "skiparse_fwd8_prep_kernel";
     case 7: return "skiparse_fwd8_kernel";
     case 8: return "skiparse_qkv_rope_kernel";
+    case 9: return "skiparse_fwdm8_prep_kernel";
+    case 10: return "skiparse_fwdm8_kernel";
     default: return "unknown";
   }
 }
@@ -449,20 +468,31 @@ size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int
                                              int mode) {
   Shape s;
   if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty || D != 128) return 0;
-  return ws8_layout(s).total;
+  return ws8_layout(s, false).total;
 }
 
-int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out, float* lse,
-                          void* workspace, size_t workspace_bytes,
-                          int B, int heads, int N, int D, int T, int H, int W,
-                          int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+size_t skiparse_attn_fwd_mixed8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k,
+                                                int mode) {
+  Shape s;
+  if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty || D != 128) return 0;
+  return ws8_layout(s, true).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The 8-bit forward: si8 = false all-E4M3 operands, si8 = true INT8 q / k for S.
+int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, float* lse, void* workspace,
+              size_t workspace_bytes, int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode,
+              float rope_theta, cudaStream_t stream) {
   Shape s;
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
   if (D != 128) return SKIPARSE_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
-  const Ws8Layout w = ws8_layout(s);
+  const Ws8Layout w = ws8_layout(s, si8);
   if (!workspace || workspace_bytes < w.total) return SKIPARSE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
   const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
@@ -470,7 +500,7 @@ int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
   const int prep_stages = fwd8_prep_stages(s.rope_entries, (size_t)dev.smem_optin, (size_t)dev.smem_sm);
-  if ((size_t)dev.smem_optin < fwd8_smem_bytes() || prep_stages == 0) return SKIPARSE_ERR_UNSUPPORTED;
+  if ((size_t)dev.smem_optin < fwd8_smem_bytes(si8) || prep_stages == 0) return SKIPARSE_ERR_UNSUPPORTED;
 
   Fwd8Params p;
   std::memset(&p, 0, sizeof(p));
@@ -494,18 +524,40 @@ int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out
   p.n_units = fwd8_units(p.g);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const uint64_t Lp = (uint64_t)w.Lp, sc = (uint64_t)w.scopes;
-  if (!encode_bytes_3d(&p.tm_q8, p.q8, 128, Lp, sc, 128, 128 * Lp) ||
-      !encode_bytes_3d(&p.tm_k8, p.k8, 128, Lp, sc, 128, 128 * Lp) ||
-      !encode_bytes_3d(&p.tm_vt, p.vt8, Lp, 128, sc, Lp, 128 * Lp) || !encode_scope_map(&p.tm_q, q, p.g) ||
+  const bool qk_ok = si8 ? encode_bf16_3d(&p.tm_q8, p.q8, 128, Lp, sc, 256, 256 * Lp) &&
+                               encode_bf16_3d(&p.tm_k8, p.k8, 128, Lp, sc, 256, 256 * Lp)
+                         : encode_bytes_3d(&p.tm_q8, p.q8, 128, Lp, sc, 128, 128 * Lp) &&
+                               encode_bytes_3d(&p.tm_k8, p.k8, 128, Lp, sc, 128, 128 * Lp);
+  if (!qk_ok || !encode_bytes_3d(&p.tm_vt, p.vt8, Lp, 128, sc, Lp, 128 * Lp) || !encode_scope_map(&p.tm_q, q, p.g) ||
       !encode_scope_map(&p.tm_k, k, p.g))
     return SKIPARSE_ERR_LAUNCH;
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
   if (cudaMemsetAsync(p.vmax, 0, (size_t)B * heads * 128 * 4, stream) != cudaSuccess) return launch_status(cudaErrorUnknown);
   st = launch_status(traced_launch(5, stream, [&] { return launch_fwd8_vmax(p, stream); }));
   if (st != SKIPARSE_OK) return st;
-  st = launch_status(traced_launch(6, stream, [&] { return launch_fwd8_prep(p, dev.sms, stream); }));
+  st = launch_status(traced_launch(si8 ? 9 : 6, stream, [&] { return launch_fwd8_prep(p, si8, dev.sms, stream); }));
   if (st != SKIPARSE_OK) return st;
-  return launch_status(traced_launch(7, stream, [&] { return launch_fwd8(p, grid, stream); }));
+  return launch_status(traced_launch(si8 ? 10 : 7, stream, [&] { return launch_fwd8(p, si8, grid, stream); }));
+}
+
+}  // namespace
+
+extern "C" {
+
+int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes,
+                          int B, int heads, int N, int D, int T, int H, int W,
+                          int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+  return fwd8_impl(false, q, k, v, out, lse, workspace, workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode,
+                   rope_theta, stream);
+}
+
+int skiparse_attn_fwd_mixed8(const void* q, const void* k, const void* v, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes,
+                             int B, int heads, int N, int D, int T, int H, int W,
+                             int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+  return fwd8_impl(true, q, k, v, out, lse, workspace, workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode,
+                   rope_theta, stream);
 }
 
 size_t skiparse_attn_bwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode) {

@@ -62,7 +62,9 @@ struct BwdParams {
 };
 
 struct Fwd8Params {
-  CUtensorMap tm_q8, tm_k8;       // 8-bit q / k, scope-tile order: (128 bytes, Lp rows, scopes), 128 x 128 boxes
+  CUtensorMap tm_q8, tm_k8;       // 8-bit q / k codes, scope-tile order (Lp rows per scope): E4M3 (128 bytes
+                                  // per row, 128 x 128 boxes) or INT8 held as bf16 (128 channels per row,
+                                  // 64-channel x 128-row boxes)
   CUtensorMap tm_vt;              // 8-bit V^T per scope: (Lp keys, 128 channels, scopes), 128 x 128 boxes
   CUtensorMap tm_q, tm_k;         // bf16 inputs q / k through the scope gather (prep kernel's staged tiles)
   Geom g;
@@ -70,7 +72,7 @@ struct Fwd8Params {
   const uint16_t* q;              // bf16 (B, N, heads, D) inputs
   const uint16_t* k;
   const uint16_t* v;
-  uint8_t* q8;                    // workspace: E4M3 codes (scopes, Lp, 128), scope order
+  uint8_t* q8;                    // workspace: codes (scopes, Lp, 128), scope order, 1 or 2 bytes each
   uint8_t* k8;
   uint8_t* vt8;                   // workspace: E4M3 V^T (scopes, 128, Lp)
   float* sq;                      // workspace: q scale per scope-order row (scopes, Lp)
@@ -137,7 +139,9 @@ int fwd_units(const Geom& g);
 cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
 
-size_t fwd8_smem_bytes();
+// si8: the mixed recipe (INT8 q / k codes held as bf16 for S, E4M3 P and v)
+size_t fwd8_smem_bytes(bool si8);
+size_t fwd8_qk_row_bytes(bool si8);
 // prep kernel: shared memory for a staging ring of `stages` q / k tiles, and the
 // ring size to launch with: 1 when two such CTAs fit on an SM (`smem_sm` bytes,
 // 1 KB reserved per CTA), else the largest (2, 1) that fits one CTA (`optin`
@@ -146,8 +150,8 @@ size_t fwd8_prep_smem_bytes(int stages, int rope_entries);
 int fwd8_prep_stages(int rope_entries, size_t optin, size_t smem_sm);
 int fwd8_units(const Geom& g);
 cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream);
-cudaError_t launch_fwd8_prep(const Fwd8Params& p, int sms, cudaStream_t stream);
-cudaError_t launch_fwd8(const Fwd8Params& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd8_prep(const Fwd8Params& p, bool si8, int sms, cudaStream_t stream);
+cudaError_t launch_fwd8(const Fwd8Params& p, bool si8, int grid, cudaStream_t stream);
 
 int proj_bn(int hd);
 size_t proj_stage_bytes(int bn);

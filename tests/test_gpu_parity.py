@@ -196,7 +196,8 @@ def test_trace_counts_launches(env):
     fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode, guard=False)
     tl.run_bwd(skp, dev, ins, fw, B, heads, N, D, T, H, W, k, mode, guard=False)
     ms, cnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
-    assert cnt == [1, 1, 1, 1, 1, 0, 0, 0, 0]         # the 8-bit forward and projection kernels did not run
+    assert cnt[:5] == [1, 1, 1, 1, 1]
+    assert all(c == 0 for c in cnt[5:])               # the 8-bit forwards and the projection did not run
     assert all(m > 0 for m in ms[:5]) and all(m == 0 for m in ms[5:])
 
 
