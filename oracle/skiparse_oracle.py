@@ -33,7 +33,14 @@ Readings taken where the page is silent:
     the 0-based integer coordinate on that axis;
   * LSE is the natural-log log-sum-exp of the scaled scores of each query row,
     stored in original token order as (B, heads, N);
-  * N must be divisible by k (single) or k*k (group); nothing is padded.
+  * N not divisible by k (single) or k*k (group), where the listings' rearrange
+    has no shape: the section's prose still defines the scopes for any N
+    (single: the tokens spaced k-1 apart, i.e. i mod k = s; group: the groups
+    of k adjacent tokens spaced k-1 groups apart, i.e. (i div k) mod k = s, the
+    last group holding the N mod k leftover tokens). Scope s then holds exactly
+    those tokens in ascending order, and scopes differ in length by at most one
+    token (single) or one group (group); nothing is padded. When N is
+    divisible this is the listings' rearrange exactly (a pinned property).
 
 Parity: every function here is pinned by tests in tests/test_oracle_*.py
 against library routines (einops.rearrange with the page's patterns, torch's
@@ -120,6 +127,19 @@ def rearrange(x, sparse_k, mode):
     return single_skip_rearrange(x, sparse_k) if mode == SINGLE else group_skip_rearrange(x, sparse_k)
 
 
+def divisible(N: int, sparse_k: int, mode: int) -> bool:
+    """True when the listings' rearrange applies: k | N (single), k*k | N (group)."""
+    return N % (sparse_k if mode == SINGLE else sparse_k * sparse_k) == 0
+
+
+def prose_scope_tokens(N: int, sparse_k: int, mode: int, s: int) -> np.ndarray:
+    """Scope s for any N from the section's prose: the tokens i with
+    i mod k = s (single skip) or (i div k) mod k = s (group skip), ascending."""
+    i = np.arange(N, dtype=np.int64)
+    a = i % sparse_k if mode == SINGLE else (i // sparse_k) % sparse_k
+    return i[a == s]
+
+
 def reverse(y, sparse_k, mode):
     return single_skip_reverse(y, sparse_k) if mode == SINGLE else group_skip_reverse(y, sparse_k)
 
@@ -127,7 +147,16 @@ def reverse(y, sparse_k, mode):
 def index_maps(N: int, sparse_k: int, mode: int):
     """scope_of_token[i], pos_of_token[i] as read off the rearrange itself:
     rearranging the token ids 0..N-1 (B = 1) gives, at [s, p], the token that
-    lands at position p of scope s (rearranged batch row s*B + b)."""
+    lands at position p of scope s (rearranged batch row s*B + b). For N the
+    rearrange cannot split, from the prose scopes (prose_scope_tokens)."""
+    if not divisible(N, sparse_k, mode):
+        scope = np.empty(N, dtype=np.int64)
+        pos = np.empty(N, dtype=np.int64)
+        for s in range(sparse_k):
+            tok = prose_scope_tokens(N, sparse_k, mode, s)
+            scope[tok] = s
+            pos[tok] = np.arange(len(tok))
+        return scope, pos
     ids = np.arange(N, dtype=np.int64)[None, :]
     r = rearrange(ids, sparse_k, mode)              # (k, N/k)
     scope = np.empty(N, dtype=np.int64)
@@ -140,7 +169,10 @@ def index_maps(N: int, sparse_k: int, mode: int):
 
 
 def scope_tokens(N: int, sparse_k: int, mode: int, s: int) -> np.ndarray:
-    """Token ids of scope s in in-scope order (row s of the rearranged ids)."""
+    """Token ids of scope s in in-scope order (row s of the rearranged ids; for N
+    the rearrange cannot split, the prose scope)."""
+    if not divisible(N, sparse_k, mode):
+        return prose_scope_tokens(N, sparse_k, mode, s)
     ids = np.arange(N, dtype=np.int64)[None, :]
     return rearrange(ids, sparse_k, mode)[s]
 
@@ -236,10 +268,45 @@ def softmax_attention_bwd(q, k, v, o, lse, do, scale):
 # The whole path: RoPE -> rearrange -> attention per scope -> reverse rearrange
 # ---------------------------------------------------------------------------
 
+def _by_scopes(q, k, v, do, T, H, W, sparse_k, mode, theta):
+    """The same steps for N the listings' rearrange cannot split: RoPE at the
+    original positions, then each prose scope gathered, attended and scattered
+    back. Returns (out, lse (B, N, heads), and dq, dk, dv when do is given)."""
+    B, N, nh, D = q.shape
+    scale = 1.0 / math.sqrt(D)
+    qr = apply_rope(q, T, H, W, theta)
+    kr = apply_rope(k, T, H, W, theta)
+    vv = np.asarray(v, dtype=np.float64)
+    out = np.empty_like(qr)
+    lse = np.empty((B, N, nh))
+    grads = None if do is None else [np.empty_like(qr) for _ in range(3)]
+    for s in range(sparse_k):
+        tok = prose_scope_tokens(N, sparse_k, mode, s)
+        if len(tok) == 0:
+            continue
+        for b in range(B):
+            for h in range(nh):
+                o, l = softmax_attention_fwd(qr[b, tok, h], kr[b, tok, h], vv[b, tok, h], scale)
+                out[b, tok, h], lse[b, tok, h] = o, l
+                if do is not None:
+                    g = softmax_attention_bwd(qr[b, tok, h], kr[b, tok, h], vv[b, tok, h], o, l,
+                                              np.asarray(do[b, tok, h], dtype=np.float64), scale)
+                    for a, gg in zip(grads, g):
+                        a[b, tok, h] = gg
+    if do is None:
+        return out, lse
+    dq = apply_rope(grads[0], T, H, W, theta, inverse=True)
+    dk = apply_rope(grads[1], T, H, W, theta, inverse=True)
+    return out, lse, dq, dk, grads[2]
+
+
 def skiparse_fwd(q, k, v, T, H, W, sparse_k, mode, theta=10000.0):
     """q, k, v: (B, N, heads, D) float64 (bf16-valued). Returns out (B, N, heads, D)
     and lse (B, heads, N), both float64."""
     B, N, nh, D = q.shape
+    if not divisible(N, sparse_k, mode):
+        out, lse = _by_scopes(q, k, v, None, T, H, W, sparse_k, mode, theta)
+        return out, np.ascontiguousarray(np.transpose(lse, (0, 2, 1)))
     scale = 1.0 / math.sqrt(D)
     qr = rearrange(apply_rope(q, T, H, W, theta), sparse_k, mode)
     kr = rearrange(apply_rope(k, T, H, W, theta), sparse_k, mode)
@@ -260,6 +327,9 @@ def skiparse_bwd(q, k, v, do, T, H, W, sparse_k, mode, theta=10000.0):
     """Gradients of <dO, out> w.r.t. the pre-RoPE q, k and v. Returns
     (dq, dk, dv, out, lse) in the layouts of skiparse_fwd."""
     B, N, nh, D = q.shape
+    if not divisible(N, sparse_k, mode):
+        out, lse, dq, dk, dv = _by_scopes(q, k, v, do, T, H, W, sparse_k, mode, theta)
+        return dq, dk, dv, out, np.ascontiguousarray(np.transpose(lse, (0, 2, 1)))
     scale = 1.0 / math.sqrt(D)
     qr = rearrange(apply_rope(q, T, H, W, theta), sparse_k, mode)
     kr = rearrange(apply_rope(k, T, H, W, theta), sparse_k, mode)

@@ -317,3 +317,75 @@ def test_planted_mistake_is_caught(monkeypatch, i):
     caught.append(not np.array_equal(O.rearrange(ids, 2, O.SINGLE),
                                      einops.rearrange(ids, "b (g k) d -> (k b) g d", k=2)))
     assert any(caught), name
+
+
+# ---- N the listings' rearrange cannot split: scopes from the prose (ragged lengths)
+
+RAGGED = [((1, 5, 7), 3, O.SINGLE), ((1, 5, 7), 4, O.SINGLE), ((2, 3, 5), 4, O.GROUP),
+          ((1, 6, 6), 5, O.GROUP), ((1, 3, 7), 2, O.GROUP), ((1, 2, 3), 4, O.GROUP)]
+
+
+@pytest.mark.parametrize("grid,k,mode", RAGGED)
+def test_ragged_equals_masked_dense(grid, k, mode):
+    """For N not divisible by k (single) or k*k (group) the forward and backward
+    equal dense attention under the prose mask, the oracle's independent path
+    (which never forms scopes), including scopes one token or one partial group
+    shorter than others, and empty scopes (N < k*k in the last case)."""
+    T, H, W = grid
+    c = small_case(mode, k=k, T=T, H=H, W=W, B=2, nh=2)
+    q, kk, v, do = c["q"], c["k"], c["v"], c["do"]
+    N, D = q.shape[1], q.shape[3]
+    assert not O.divisible(N, k, mode)
+    dq, dk, dv, out, lse = O.skiparse_bwd(q, kk, v, do, T, H, W, k, mode, THETA)
+    out2, lse2 = O.skiparse_fwd(q, kk, v, T, H, W, k, mode, THETA)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+    mask = O.skiparse_mask(N, k, mode)
+    R = _rot_mats(N, T, H, W, D)
+    for b in range(2):
+        for h in range(2):
+            qt = O.rope_closed_form(q, T, H, W, THETA)[b, :, h]
+            kt = O.rope_closed_form(kk, T, H, W, THETA)[b, :, h]
+            mo, ml = O.masked_dense_fwd(qt, kt, v[b, :, h], mask, 1 / math.sqrt(D))
+            gq, gk, gv = O.masked_dense_bwd(qt, kt, v[b, :, h], do[b, :, h], mask, 1 / math.sqrt(D))
+            gq = np.einsum("nji,nj->ni", R, gq)
+            gk = np.einsum("nji,nj->ni", R, gk)
+            assert np.max(np.abs(out[b, :, h] - mo)) < 1e-12
+            assert np.max(np.abs(lse[b, h] - ml)) < 1e-12
+            assert np.max(np.abs(dq[b, :, h] - gq)) < 1e-12
+            assert np.max(np.abs(dk[b, :, h] - gk)) < 1e-12
+            assert np.max(np.abs(dv[b, :, h] - gv)) < 1e-12
+
+
+@pytest.mark.parametrize("grid,k,mode", RAGGED[:3])
+def test_ragged_brute_force(grid, k, mode):
+    """Ragged scopes against the unstabilised pure-Python formula, with scope
+    membership written out from the prose (tokens spaced k-1 apart, or groups
+    of k spaced k-1 groups apart)."""
+    T, H, W = grid
+    c = small_case(mode, k=k, T=T, H=H, W=W, B=1, nh=1)
+    q, kk, v = c["q"], c["k"], c["v"]
+    N, D = q.shape[1], q.shape[3]
+    out, lse = O.skiparse_fwd(q, kk, v, T, H, W, k, mode, THETA)
+    qt = O.rope_closed_form(q, T, H, W, THETA)[0, :, 0].tolist()
+    kt = O.rope_closed_form(kk, T, H, W, THETA)[0, :, 0].tolist()
+    if mode == O.SINGLE:
+        same = lambda i, j: (i - j) % k == 0
+    else:
+        same = lambda i, j: (i // k - j // k) % k == 0
+    bo, bl = _brute_force(qt, kt, v[0, :, 0].tolist(), same, 1 / math.sqrt(D))
+    assert np.max(np.abs(out[0, :, 0] - bo)) < 1e-10
+    assert np.max(np.abs(lse[0, 0] - bl)) < 1e-10
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_ragged_scope_sampler_matches_full_path(mode):
+    T, H, W, k = 2, 5, 7, 3
+    c = small_case(mode, k=k, T=T, H=H, W=W, B=1, nh=2)
+    dq, dk, dv, out, lse = O.skiparse_bwd(c["q"], c["k"], c["v"], c["do"], T, H, W, k, mode, THETA)
+    for s in range(k):
+        r = O.skiparse_scope(c["q"], c["k"], c["v"], c["do"], T, H, W, k, mode, 0, 1, s, THETA)
+        tok = r["tokens"]
+        assert np.max(np.abs(r["out"] - out[0, tok, 1])) < 1e-12
+        assert np.max(np.abs(r["dq"] - dq[0, tok, 1])) < 1e-12
+        assert np.max(np.abs(r["dk"] - dk[0, tok, 1])) < 1e-12
+        assert np.max(np.abs(r["dv"] - dv[0, tok, 1])) < 1e-12

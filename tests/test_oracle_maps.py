@@ -114,3 +114,37 @@ def test_k1_is_identity():
     for mode, _ in MODES:
         x = np.random.default_rng(1).standard_normal((2, 12, 3))
         assert np.array_equal(O.rearrange(x, 1, mode), x)
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_prose_scopes_equal_the_rearrange_when_divisible(mode, name):
+    """Where the listings' rearrange applies, the prose definition of a scope
+    (the one used for every other N) gives exactly its rows."""
+    for _, N, k in _shapes(mode):
+        for s in range(k):
+            ids = O.rearrange(np.arange(N, dtype=np.int64)[None, :], k, mode)[s]
+            assert np.array_equal(O.prose_scope_tokens(N, k, mode, s), ids)
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_ragged_index_maps(mode, name):
+    """Any N: the maps are a bijection of the tokens onto (scope, position < L_s),
+    scope lengths differ by at most one token (single) or one group (group),
+    lower scopes are never shorter, and the in-scope position inverts by the
+    same closed forms as in the divisible case."""
+    for k in (2, 3, 4, 5, 8):
+        for N in range(1, 3 * k * k + 2):
+            scope, pos = O.index_maps(N, k, mode)
+            sizes = np.bincount(scope, minlength=k)
+            assert sizes.sum() == N
+            assert np.all(np.diff(sizes) <= 0)
+            assert sizes[0] - sizes[-1] <= (1 if mode == O.SINGLE else k)
+            flat = {(int(s_), int(p_)) for s_, p_ in zip(scope, pos)}
+            assert len(flat) == N and all(p_ < sizes[s_] for s_, p_ in flat)
+            if mode == O.SINGLE:
+                inv = pos * k + scope
+            else:
+                inv = (pos // k) * k * k + scope * k + pos % k
+            assert np.array_equal(inv, np.arange(N))
+            mask = O.skiparse_mask(N, k, mode)
+            assert np.array_equal(scope[:, None] == scope[None, :], mask)
