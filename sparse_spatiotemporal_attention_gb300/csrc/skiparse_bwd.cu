@@ -118,37 +118,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
       uint32_t g0 = 0;
       int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         int b, head, s, kt;
         decode_unit_bwd(g, u, b, head, s, kt);
+        const int nt = scope_tiles(g, s);
+        if (kt >= nt) continue;                       // a shorter scope has fewer key tiles
         if (it > 0 && !mbar_wait(bar(B_KVEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_BWD + B_KVEMPTY)) break;
         mbar_expect_tx(bar(B_KVFULL), 2 * Ly::TILE);
-        const int krow = b * g.Nn + (kt * kTile) / g.G;
 #pragma unroll
         for (int h = 0; h < Ly::HALVES; ++h) {
-          tma_load_5d(sK + h * kHalfBytes, &p.tm_k, bar(B_KVFULL), h * 64, head, 0, s, krow);
-          tma_load_5d(sV + h * kHalfBytes, &p.tm_v, bar(B_KVFULL), h * 64, head, 0, s, krow);
+          load_scope_tile(sK + h * kHalfBytes, &p.tm_k, bar(B_KVFULL), g, h * 64, head, s, b, kt * kTile);
+          load_scope_tile(sV + h * kHalfBytes, &p.tm_v, bar(B_KVFULL), g, h * 64, head, s, b, kt * kTile);
         }
         ++kv_issued;
         const size_t srow = (((size_t)b * g.heads + head) * g.k + s) * p.Lp;
-        for (int i = 0; i < g.n_tiles; ++i) {
+        for (int i = 0; i < nt; ++i) {
           const uint32_t gg = g0 + i;
           const int st = gg & 1;
           const uint32_t n = gg >> 1;
           if (n > 0 && !mbar_wait(bar(B_QEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_BWD + B_QEMPTY0 + st)) { ok = false; break; }
           mbar_expect_tx(bar(B_QFULL0 + st), 2 * Ly::TILE + 1024);
-          const int qrow = b * g.Nn + (i * kTile) / g.G;
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h) {
-            tma_load_5d(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(B_QFULL0 + st), h * 64, head, 0, s, qrow);
-            tma_load_5d(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(B_QFULL0 + st), h * 64, head, 0, s, qrow);
+            load_scope_tile(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(B_QFULL0 + st), g, h * 64, head, s, b,
+                            i * kTile);
+            load_scope_tile(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(B_QFULL0 + st), g, h * 64, head, s, b,
+                            i * kTile);
           }
           const uint32_t dst = smem_u32(stats + st * 256);
           bulk_load(dst, p.lse2s + srow + i * kTile, 512, bar(B_QFULL0 + st));
           bulk_load(dst + 512, p.delta_s + srow + i * kTile, 512, bar(B_QFULL0 + st));
           ++q_issued[st];
         }
-        g0 += g.n_tiles;
+        g0 += nt;
+        ++it;
       }
       if (kv_issued) mbar_drain(bar(B_KVFULL), (kv_issued - 1) & 1);
       for (int st = 0; st < 2; ++st)
@@ -164,11 +167,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
       uint32_t g0 = 0;
       int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        int b, head, s, kt;
+        decode_unit_bwd(g, u, b, head, s, kt);
+        const int nt = scope_tiles(g, s);
+        if (kt >= nt) continue;
         if (!mbar_wait(bar(B_KVFULL), it & 1, ctl, ERR_KERNEL_BWD + B_KVFULL)) break;
         if (it > 0 && !mbar_wait(bar(B_DKVFREE), (it - 1) & 1, ctl, ERR_KERNEL_BWD + B_DKVFREE)) break;
         tc_fence_after();
-        for (int i = 0; i < g.n_tiles; ++i) {
+        for (int i = 0; i < nt; ++i) {
           const uint32_t gg = g0 + i;
           const int st = gg & 1;
           const uint32_t n = gg >> 1;
@@ -203,7 +210,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
         if (!ok) break;
         tc_commit(bar(B_DKVDONE));
         tc_commit(bar(B_KVEMPTY));
-        g0 += g.n_tiles;
+        g0 += nt;
+        ++it;
       }
       tc_commit(bar(B_FINAL));
       mbar_drain(bar(B_FINAL), 0);
@@ -215,15 +223,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
       decode_unit_bwd(g, u, b, head, s, kt);
-      for (int i = 0; i < g.n_tiles; ++i) {
+      const int nt = scope_tiles(g, s);
+      if (kt >= nt) continue;
+      const int Ls = scope_len(g, s);
+      for (int i = 0; i < nt; ++i) {
         const uint32_t gg = g0 + i;
         if (!mbar_wait(bar(B_DQFULL), gg & 1, ctl, ERR_KERNEL_BWD + B_DQFULL)) { ok = false; break; }
         tc_fence_after();
         const int prow = i * kTile + qi;
-        const bool row_ok = prow < g.L;
+        const bool row_ok = prow < Ls;
         float* dst = p.dq_acc + ((((size_t)b * g.heads + head) * g.k + s) * p.Lp + prow) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -240,7 +251,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_DQFREE));
       }
-      g0 += g.n_tiles;
+      g0 += nt;
+      ++it;
     }
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps
@@ -251,11 +263,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
       decode_unit_bwd(g, u, b, head, s, kt);
-      const bool key_ok = kt * kTile + j < g.L;
-      for (int i = 0; i < g.n_tiles; ++i) {
+      const int nt = scope_tiles(g, s);
+      if (kt >= nt) continue;
+      const int Ls = scope_len(g, s);
+      const bool key_ok = kt * kTile + j < Ls;
+      for (int i = 0; i < nt; ++i) {
         const uint32_t gg = g0 + i;
         const int st = gg & 1;
         if (!mbar_wait(bar(B_SFULL), gg & 1, ctl, ERR_KERNEL_BWD + B_SFULL)) { ok = false; break; }
@@ -263,7 +278,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
         tc_fence_after();
         const float* lse2 = stats + st * 256;
         const float* delta = lse2 + 128;
-        const int qvalid = key_ok ? min(kTile, g.L - i * kTile) : 0;
+        const int qvalid = key_ok ? min(kTile, Ls - i * kTile) : 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float sv[32], dp[32];
@@ -337,7 +352,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_DKVFREE));
-      g0 += g.n_tiles;
+      g0 += nt;
+      ++it;
     }
   }
 
@@ -448,28 +464,28 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
       decode_unit_bwd(g, u, b, head, s, kt);
+      const int nt = scope_tiles(g, s);
+      if (kt >= nt) continue;                         // a shorter scope has fewer key tiles
       if (it > 0 && !warp_wait(T_KVEMPTY, (it - 1) & 1)) break;
       if (leader) {
         mbar_expect_tx(bar(T_KVFULL), 2 * Ly::TILE);
-        const int krow = b * g.Nn + (kt * kTile) / g.G;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          tma_load_5d(sK + h * kHalfBytes, &p.tm_k, bar(T_KVFULL), h * 64, head, 0, s, krow);
-          tma_load_5d(sV + h * kHalfBytes, &p.tm_v, bar(T_KVFULL), h * 64, head, 0, s, krow);
+          load_scope_tile(sK + h * kHalfBytes, &p.tm_k, bar(T_KVFULL), g, h * 64, head, s, b, kt * kTile);
+          load_scope_tile(sV + h * kHalfBytes, &p.tm_v, bar(T_KVFULL), g, h * 64, head, s, b, kt * kTile);
         }
       }
       __syncwarp();
       ++kv_issued;
       const size_t srow = (((size_t)b * g.heads + head) * g.k + s) * p.Lp;
-      for (int i = 0; i < g.n_tiles; ++i) {
+      for (int i = 0; i < nt; ++i) {
         const uint32_t gg = g0 + i;
         const int st = gg & 1;
         const uint32_t n = gg >> 1;
-        const int qi = stagger(i, kt, g.n_tiles);
-        const int qrow = b * g.Nn + (qi * kTile) / g.G;
+        const int qi = stagger(i, kt, nt);
         // a slot is refilled once the dQ~ staging of tile gg-2 placed in it has been read out
         if (n > 0 && !warp_wait(T_QFREE0 + st, (n - 1) & 1)) {
           ok = false;
@@ -479,7 +495,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
           mbar_expect_tx(bar(T_QFULL0 + st), Ly::TILE + 1024);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            tma_load_5d(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(T_QFULL0 + st), h * 64, head, 0, s, qrow);
+            load_scope_tile(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(T_QFULL0 + st), g, h * 64, head, s, b,
+                            qi * kTile);
           const uint32_t dst = smem_u32(stats + st * 256);
           bulk_load(dst, p.lse2s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
           bulk_load(dst + 512, p.delta_s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
@@ -493,12 +510,14 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
           mbar_expect_tx(bar(T_OFULL0 + st), Ly::TILE);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            tma_load_5d(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(T_OFULL0 + st), h * 64, head, 0, s, qrow);
+            load_scope_tile(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(T_OFULL0 + st), g, h * 64, head, s,
+                            b, qi * kTile);
         }
         __syncwarp();
         ++q_issued[st];
       }
-      g0 += g.n_tiles;
+      g0 += nt;
+      ++it;
     }
     if (leader) {
       if (kv_issued) mbar_drain(bar(T_KVFULL), (kv_issued - 1) & 1);
@@ -521,10 +540,14 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      int b, head, s, kt;
+      decode_unit_bwd(g, u, b, head, s, kt);
+      const int nt = scope_tiles(g, s);
+      if (kt >= nt) continue;
       if (!warp_wait(T_KVFULL, it & 1)) break;
       tc_fence_after();
-      for (int i = 0; ok && i < g.n_tiles; ++i) {
+      for (int i = 0; ok && i < nt; ++i) {
         const uint32_t gg = g0 + i;
         const int st = gg & 1;
         if (!warp_wait(T_QFULL0 + st, (gg >> 1) & 1)) { ok = false; break; }
@@ -596,7 +619,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         tc_commit(bar(T_KVEMPTY));
       }
       __syncwarp();
-      g0 += g.n_tiles;
+      g0 += nt;
+      ++it;
     }
     if (leader) {
       tc_commit(bar(T_FINAL));
@@ -618,8 +642,10 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
       decode_unit_bwd(g, u, b, head, s, kt);
+      const int nt = scope_tiles(g, s);
+      if (kt >= nt) continue;
       float* acc = p.dq_acc + (((size_t)b * g.heads + head) * g.k + s) * (size_t)p.Lp * D;
-      for (int i = 0; i < g.n_tiles; ++i) {
+      for (int i = 0; i < nt; ++i) {
         const uint32_t gg = g0 + i;
         const int st = gg & 1;
         if (!bar_and<3, 256>(mbar_wait(bar(T_DQFULL), gg & 1, ctl, E + T_DQFULL))) { ok = false; break; }
@@ -637,7 +663,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         asm volatile("bar.sync 4, 256;" ::: "memory");
         if (leader) {
           // the Q~ slot's half first: Q~ of tile gg+2 is needed before its dO
-          const int q0 = stagger(i, kt, g.n_tiles) * kTile;   // rows < Lp: padded rows get zeros
+          const int q0 = stagger(i, kt, nt) * kTile;   // rows < Lp: padded rows get zeros
           bulk_reduce_add_f32(acc + (size_t)q0 * D, smem_u32(smem + Ly::Q_OFF + st * Ly::TILE), 64 * D * 4);
           bulk_commit_group();
           bulk_reduce_add_f32(acc + (size_t)(q0 + 64) * D, smem_u32(smem + Ly::DO_OFF + st * Ly::TILE), 64 * D * 4);
@@ -649,7 +675,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         }
         __syncwarp();
       }
-      g0 += g.n_tiles;
+      g0 += nt;
     }
     if (leader) bulk_wait_all();
   } else {
@@ -662,18 +688,21 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
       decode_unit_bwd(g, u, b, head, s, kt);
-      const bool key_ok = kt * kTile + j < g.L;
-      for (int i = 0; i < g.n_tiles; ++i) {
+      const int nt = scope_tiles(g, s);
+      if (kt >= nt) continue;
+      const int Ls = scope_len(g, s);
+      const bool key_ok = kt * kTile + j < Ls;
+      for (int i = 0; i < nt; ++i) {
         const uint32_t gg = g0 + i;
         const int st = gg & 1;
         if (!bar_and<2, 256>(mbar_wait(bar(T_SRDY), gg & 1, ctl, E + T_SRDY))) { ok = false; break; }
         tc_fence_after();
         const float4* lse4 = reinterpret_cast<const float4*>(stats + st * 256);
         const float4* del4 = lse4 + 32;
-        const int qvalid = key_ok ? min(kTile, g.L - stagger(i, kt, g.n_tiles) * kTile) : 0;
+        const int qvalid = key_ok ? min(kTile, Ls - stagger(i, kt, nt) * kTile) : 0;
         // Full tiles (every key row of the warp and every query of the tile inside
         // the scope: all but the last query or key tile) take a select-free path;
         // rows and columns past the scope are zeroed otherwise. Warp-uniform, so
@@ -825,7 +854,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(T_DKVFREE));
-      g0 += g.n_tiles;
+      g0 += nt;
+      ++it;
     }
   }
 

@@ -124,6 +124,92 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
   }
 }
 
+// Preprocess for scopes of unequal length (N not divisible by k or k^2): the
+// same per-row work in scope order, one warp per row (s, b, pos, head) of the
+// scope-ordered copies (k, B, Lp, heads, D), head fastest. A row inside its
+// scope gathers its token's dO (and, with write_qkv, q and k, rotated, and v)
+// into the copies; a row past the scope's end writes zeros there, so the main
+// kernel's MMAs never meet uninitialised padding. delta and lse * log2(e) go to
+// the scope-order slot, whose dQ~ accumulator row is zeroed.
+template <int D>
+__global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pack_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ float2 tab[];
+  const Geom& g = p.g;
+  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < p.rope.entries; e += blockDim.x) p.rope_tab[e] = tab[e];
+  constexpr int PPL = D / 64;
+  const int lane = threadIdx.x & 31;
+  const long long wpb = blockDim.x >> 5;
+  PairSel sel[PPL];
+#pragma unroll
+  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
+  const bool rot = p.rotate_qk != 0;
+  const long long rows = (long long)g.k * g.B * g.Lp * g.heads;
+  const long long stride = (long long)gridDim.x * wpb;
+  for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += stride) {
+    const int sbp = fdiv((int)row, g.fheads);                 // (s * B + b) * Lp + pos
+    const int head = (int)row - sbp * g.heads;
+    const int sb = fdiv(sbp, g.fLp);
+    const int pos = sbp - sb * g.Lp;
+    const int s = fdiv(sb, g.fB);
+    const int b = sb - s * g.B;
+    const bool inside = pos < scope_len(g, s);
+    uint32_t qv[PPL], kv[PPL], vv[PPL], ov[PPL], dv[PPL];
+#pragma unroll
+    for (int e = 0; e < PPL; ++e) qv[e] = kv[e] = vv[e] = ov[e] = dv[e] = 0u;
+    float lse = 0.f, dsum = 0.f;
+    int tok = 0;
+    if (inside) {
+      tok = token_of(g, s, pos);
+      const size_t src = (((size_t)b * g.N + tok) * g.heads + head) * D + lane * 2 * PPL;
+      ld_slice<PPL>(p.out + src, ov);
+      ld_slice<PPL>(p.dout + src, dv);
+      if (p.write_qkv) {
+        ld_slice<PPL>(p.q + src, qv);
+        ld_slice<PPL>(p.k + src, kv);
+        ld_slice<PPL>(p.v + src, vv);
+      }
+      if (lane == 0) lse = p.lse[((size_t)b * g.heads + head) * g.N + tok];
+#pragma unroll
+      for (int e = 0; e < PPL; ++e) {
+        dsum = fmaf(bf16lo(ov[e]), bf16lo(dv[e]), dsum);
+        dsum = fmaf(bf16hi(ov[e]), bf16hi(dv[e]), dsum);
+      }
+      if (p.write_qkv && rot) {
+        int t, hh, w;
+        token_coords(p.rope, tok, t, hh, w);
+#pragma unroll
+        for (int e = 0; e < PPL; ++e) {
+          const float2 cs = tab[pair_index(sel[e], t, hh, w)];
+          const float2 a = rope_rotate(bf16lo(qv[e]), bf16hi(qv[e]), cs);
+          const float2 c = rope_rotate(bf16lo(kv[e]), bf16hi(kv[e]), cs);
+          qv[e] = pack_bf16(a.x, a.y);
+          kv[e] = pack_bf16(c.x, c.y);
+        }
+      }
+    }
+    const size_t dst = (size_t)row * D + lane * 2 * PPL;
+    st_slice<PPL>(p.dop + dst, dv);
+    if (p.write_qkv) {
+      st_slice<PPL>(p.qr + dst, qv);
+      st_slice<PPL>(p.kr + dst, kv);
+      st_slice<PPL>(p.vp + dst, vv);
+    }
+    const size_t idx = (((size_t)b * g.heads + head) * g.k + s) * p.Lp + pos;   // scope-order slot
+    float* acc = p.dq_acc + idx * D + lane * 2 * PPL;
+    if (PPL == 2) *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else *reinterpret_cast<float2*>(acc) = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+    if (lane == 0) {
+      p.delta_s[idx] = dsum;
+      p.lse2s[idx] = lse * 1.4426950408889634f;
+    }
+  }
+}
+
 // Post: dq = R^T (scale * dQ~) for each (b, token, head) row, read from the
 // row's scope-order accumulator slot; four rows per warp iteration.
 template <int D>
@@ -185,8 +271,21 @@ static cudaError_t launch_pre_variant(const BwdParams& p, int grid, int sms, siz
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_pack_variant(const BwdParams& p, int grid, int sms, size_t smem, cudaStream_t stream) {
+  const cudaError_t e =
+      cudaFuncSetAttribute(skiparse_bwd_pack_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  grid = one_wave(skiparse_bwd_pack_kernel<D>, grid, kRowThreads, smem, sms);
+  skiparse_bwd_pack_kernel<D><<<grid, kRowThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_pre(const BwdParams& p, int grid, int sms, cudaStream_t stream) {
   const size_t smem = (size_t)p.rope.entries * sizeof(float2);
+  if (p.g.packed)
+    return p.g.D == 128 ? launch_pack_variant<128>(p, grid, sms, smem, stream)
+                        : launch_pack_variant<64>(p, grid, sms, smem, stream);
   if (p.g.D == 128)
     return p.rotate_qk ? launch_pre_variant<128, true>(p, grid, sms, smem, stream)
                        : launch_pre_variant<128, false>(p, grid, sms, smem, stream);

@@ -12,7 +12,7 @@ __global__ void skiparse_debug_index_map_kernel(const __grid_constant__ DebugPar
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < g.N; i += gridDim.x * blockDim.x) {
     int s, pos;
     scope_pos_of(g, i, s, pos);
-    const bool ok = s >= 0 && s < g.k && pos >= 0 && pos < g.L && token_of(g, s, pos) == i;
+    const bool ok = s >= 0 && s < g.k && pos >= 0 && pos < scope_len(g, s) && token_of(g, s, pos) == i;
     p.scope_of_token[i] = ok ? s : -1;
     p.pos_of_token[i] = pos;
   }

@@ -58,9 +58,14 @@ struct Geom {
   int k;        // sparse_k: number of scopes
   int G;        // group size: 1 (single skip) or k (group skip); always a power of two
   int lgG;      // log2(G)
-  int L;        // scope length N / k
+  int L;        // length of the longest scope (scope 0): N / k when k (k^2) divides N
   int Nn;       // L / G: rows of the merged (n, b) tensor-map dimension per batch
-  int n_tiles;  // ceil(L / 128)
+  int n_tiles;  // ceil(L / 128): tiles of the longest scope
+  int packed;   // 1: q, k, v (dO) are read from scope-ordered copies (k, B, Lp, heads, D)
+  int Lp;       // n_tiles * 128: rows per (scope, batch) of the scope-ordered copies
+  int Qb, Rb;   // N = Qb * k * G + Rb: whole blocks of k groups, and the tokens left over
+  FastDiv fLp;  // division by Lp (scope-ordered row -> (scope, batch), position)
+  FastDiv fB;   // division by B
   FastDiv fk;   // division by k
   FastDiv fkG;  // division by k * G
   FastDiv fheads;  // division by heads (row index -> (b * N + token, head))
@@ -85,6 +90,15 @@ struct RopeParams {
   FastDiv fHW;        // division by H*W
   FastDiv fW;         // division by W
 };
+
+// Length of scope s: the tokens i with (i div G) mod k = s. Every block of k
+// groups gives each scope G tokens; the Rb tokens of the last, partial block
+// fill scope 0's group first, then scope 1's, ... (the last group may be partial).
+__host__ __device__ __forceinline__ int scope_len(const Geom& g, int s) {
+  const int extra = g.Rb - s * g.G;
+  return g.Qb * g.G + (extra < 0 ? 0 : (extra > g.G ? g.G : extra));
+}
+__host__ __device__ __forceinline__ int scope_tiles(const Geom& g, int s) { return (scope_len(g, s) + 127) >> 7; }
 
 __device__ __forceinline__ int token_of(const Geom& g, int s, int p) {
   return ((p >> g.lgG) * g.k << g.lgG) + (s << g.lgG) + (p & (g.G - 1));
@@ -337,6 +351,18 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
       :: "r"(dst), "l"((uint64_t)m), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
+}
+
+// One 128-position tile of a scope: positions p0 .. p0 + 127 of scope s, batch
+// b, channels c0 .. c0 + 63 of `head` (one 128-row box, 128-byte swizzle).
+// Unpacked: through the 5-D scope-gather map over the caller's (B, N, heads, D)
+// tensor (dims channel, head, in-group offset, scope, merged (batch, group)).
+// Packed: from the scope-ordered copy (k, B, Lp, heads, D) through a 3-D map
+// (channel, head, row), rows past a scope's end holding zeros.
+__device__ __forceinline__ void load_scope_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, const Geom& g,
+                                                int c0, int head, int s, int b, int p0) {
+  if (g.packed) tma_load_3d(dst, m, bar, c0, head, (s * g.B + b) * g.Lp + p0);
+  else tma_load_5d(dst, m, bar, c0, head, 0, s, b * g.Nn + p0 / g.G);
 }
 
 // Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).

@@ -163,6 +163,87 @@ __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_rope_kernel(const _
 }
 
 // ---------------------------------------------------------------------------
+// Pack pass (scopes of unequal length, N not divisible by k or k^2): q, k (rotated
+// unless rope_theta = 0) and v gathered into scope order (k, B, Lp, heads, D),
+// positions past each scope's end zero. One warp per scope-ordered row, two rows
+// per iteration, head fastest so a warp's consecutive rows read one token's
+// heads; lane l owns channel pairs l*PPL .. l*PPL+PPL-1.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_pack_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ float2 tab[];
+  const Geom& g = p.g;
+  if (p.rotate) rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  __syncthreads();
+  constexpr int PPL = D / 64;
+  const int lane = threadIdx.x & 31;
+  const long long wpb = blockDim.x >> 5;
+  PairSel sel[PPL];
+#pragma unroll
+  for (int e = 0; e < PPL; ++e) sel[e] = pair_select(p.rope, lane * PPL + e);
+  const long long rows = (long long)g.k * g.B * g.Lp * g.heads;
+  const long long stride = (long long)gridDim.x * wpb;
+  for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += 2 * stride) {
+    uint32_t qv[2][PPL], kv[2][PPL], vv[2][PPL];
+    int tok[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      tok[u] = -1;
+      const long long row = r0 + u * stride;
+      if (row >= rows) continue;
+      const int sbp = fdiv((int)row, g.fheads);              // (s * B + b) * Lp + pos
+      const int head = (int)row - sbp * g.heads;
+      const int sb = fdiv(sbp, g.fLp);
+      const int pos = sbp - sb * g.Lp;
+      const int s = fdiv(sb, g.fB);
+      const int b = sb - s * g.B;
+      if (pos >= scope_len(g, s)) continue;
+      tok[u] = token_of(g, s, pos);
+      const size_t src = (((size_t)b * g.N + tok[u]) * g.heads + head) * D + lane * 2 * PPL;
+#pragma unroll
+      for (int e = 0; e < PPL; ++e) {
+        qv[u][e] = *reinterpret_cast<const uint32_t*>(p.q + src + 2 * e);
+        kv[u][e] = *reinterpret_cast<const uint32_t*>(p.k + src + 2 * e);
+        vv[u][e] = *reinterpret_cast<const uint32_t*>(p.v + src + 2 * e);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long row = r0 + u * stride;
+      if (row >= rows) continue;
+      uint32_t qo[PPL], ko[PPL], vo[PPL];
+#pragma unroll
+      for (int e = 0; e < PPL; ++e) qo[e] = ko[e] = vo[e] = 0u;
+      if (tok[u] >= 0) {
+        int t = 0, hh = 0, w = 0;
+        if (p.rotate) token_coords(p.rope, tok[u], t, hh, w);
+#pragma unroll
+        for (int e = 0; e < PPL; ++e) {
+          vo[e] = vv[u][e];
+          if (p.rotate) {
+            const float2 cs = tab[pair_index(sel[e], t, hh, w)];
+            const float2 a = rope_rotate(bf16lo(qv[u][e]), bf16hi(qv[u][e]), cs);
+            const float2 c = rope_rotate(bf16lo(kv[u][e]), bf16hi(kv[u][e]), cs);
+            qo[e] = pack_bf16(a.x, a.y);
+            ko[e] = pack_bf16(c.x, c.y);
+          } else {
+            qo[e] = qv[u][e];
+            ko[e] = kv[u][e];
+          }
+        }
+      }
+      const size_t dst = (size_t)row * D + lane * 2 * PPL;
+#pragma unroll
+      for (int e = 0; e < PPL; ++e) {
+        *reinterpret_cast<uint32_t*>(p.qr + dst + 2 * e) = qo[e];
+        *reinterpret_cast<uint32_t*>(p.kr + dst + 2 * e) = ko[e];
+        *reinterpret_cast<uint32_t*>(p.vr + dst + 2 * e) = vo[e];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Attention over rotated q / k
 // ---------------------------------------------------------------------------
 template <int D>
@@ -217,32 +298,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
     uint32_t gk = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, pair;
       decode_unit(g, n_pairs, u, b, head, s, pair);
+      const int nt = scope_tiles(g, s);
+      if (2 * pair >= nt) continue;                  // a shorter scope has fewer Q-tile pairs
       if (it > 0 && !warp_wait(F_QEMPTY, (it - 1) & 1)) break;
       if (leader) {
         mbar_expect_tx(bar(F_QFULL), 2 * Ly::TILE);
-        const int qrow = b * g.Nn + (2 * pair * kTile) / g.G;
 #pragma unroll
         for (int h = 0; h < Ly::HALVES; ++h) {
-          tma_load_5d(sQA + h * kHalfBytes, &p.tm_q, bar(F_QFULL), h * 64, head, 0, s, qrow);
-          tma_load_5d(sQB + h * kHalfBytes, &p.tm_q, bar(F_QFULL), h * 64, head, 0, s, qrow + kTile / g.G);
+          load_scope_tile(sQA + h * kHalfBytes, &p.tm_q, bar(F_QFULL), g, h * 64, head, s, b, 2 * pair * kTile);
+          load_scope_tile(sQB + h * kHalfBytes, &p.tm_q, bar(F_QFULL), g, h * 64, head, s, b, (2 * pair + 1) * kTile);
         }
       }
       __syncwarp();
       ++q_issued;
-      for (int j = 0; j < g.n_tiles; ++j) {
+      for (int j = 0; j < nt; ++j) {
         const uint32_t gg = gk + j;
         const int st = gg & 1;
         const uint32_t n = gg >> 1;
-        const int krow = b * g.Nn + (j * kTile) / g.G;
         if (n > 0 && !warp_wait(F_KEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
         if (leader) {
           mbar_expect_tx(bar(F_KFULL0 + st), Ly::TILE);
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h)
-            tma_load_5d(sK + st * Ly::TILE + h * kHalfBytes, &p.tm_k, bar(F_KFULL0 + st), h * 64, head, 0, s, krow);
+            load_scope_tile(sK + st * Ly::TILE + h * kHalfBytes, &p.tm_k, bar(F_KFULL0 + st), g, h * 64, head, s, b,
+                            j * kTile);
         }
         __syncwarp();
         ++k_issued[st];
@@ -251,12 +333,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
           mbar_expect_tx(bar(F_VFULL0 + st), Ly::TILE);
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h)
-            tma_load_5d(sV + st * Ly::TILE + h * kHalfBytes, &p.tm_v, bar(F_VFULL0 + st), h * 64, head, 0, s, krow);
+            load_scope_tile(sV + st * Ly::TILE + h * kHalfBytes, &p.tm_v, bar(F_VFULL0 + st), g, h * 64, head, s, b,
+                            j * kTile);
         }
         __syncwarp();
         ++v_issued[st];
       }
-      gk += g.n_tiles;
+      gk += nt;
+      ++it;
     }
     // Copies still in flight (only after an abort) must land before exit.
     if (leader) {
@@ -298,8 +382,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tmem + colO, tmem + colS + ks * 8, mnmajor_step(dv, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
       };
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-        const int n = g.n_tiles;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        int b, head, s, pair;
+        decode_unit(g, n_pairs, u, b, head, s, pair);
+        const int n = scope_tiles(g, s);
+        if (2 * pair >= n) continue;
         if (!lane_wait(F_QFULL, it & 1)) break;
         if (!lane_wait(F_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
         tc_fence_after();
@@ -345,6 +432,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
           }
         }
         g0 += n;
+        ++it;
       }
       tc_commit(bar(F_FINAL));
       mbar_drain(bar(F_FINAL), 0);
@@ -365,16 +453,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, pair;
       decode_unit(g, n_pairs, u, b, head, s, pair);
+      const int nt = scope_tiles(g, s);
+      if (2 * pair >= nt) continue;
+      const int Ls = scope_len(g, s);
       const int tile = 2 * pair + wg;
       float m = 0.f, l = 0.f;
-      for (int j = 0; j < g.n_tiles; ++j) {
+      for (int j = 0; j < nt; ++j) {
         const uint32_t gg = g0 + j;
         if (!mbar_wait(bar(barS), gg & 1, ctl, ERR_KERNEL_FWD + barS)) { ok = false; break; }
         tc_fence_after();
-        const int valid = min(kTile, g.L - j * kTile);
+        const int valid = min(kTile, Ls - j * kTile);
         // the whole S row in registers with one TMEM round trip
         float x[kTile];
         tmem_ld128(tmem + lane_base + colS, x);
@@ -436,11 +527,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       if (!ok) break;
       // ---- epilogue: O / l to the token's original row, LSE in natural log.
       // S_X(glast) proved PV_X(glast-1) complete, so one parity wait suffices.
-      const uint32_t glast = g0 + g.n_tiles - 1;
+      const uint32_t glast = g0 + nt - 1;
       if (!mbar_wait(bar(barO), glast & 1, ctl, ERR_KERNEL_FWD + barO)) break;
       tc_fence_after();
       const int prow = tile * kTile + r;
-      const bool row_ok = prow < g.L;
+      const bool row_ok = prow < Ls;
       const int tok = row_ok ? token_of(g, s, prow) : 0;
       const float inv_l = 1.0f / l;
       uint16_t* orow = p.out + (((size_t)b * g.N + tok) * g.heads + head) * D;
@@ -465,7 +556,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(barOE));
-      g0 += g.n_tiles;
+      g0 += nt;
+      ++it;
     }
   }
 
@@ -496,6 +588,23 @@ cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t 
     if (e != cudaSuccess) return e;
     grid = one_wave(skiparse_fwd_rope_kernel<64>, grid, kRopeThreads, smem, sms);
     skiparse_fwd_rope_kernel<64><<<grid, kRopeThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_pack(const FwdParams& p, int grid, int sms, cudaStream_t stream) {
+  const size_t smem = p.rotate ? fwd_rope_smem_bytes(p.rope.entries) : 0;
+  cudaError_t e;
+  if (p.g.D == 128) {
+    e = cudaFuncSetAttribute(skiparse_fwd_pack_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    grid = one_wave(skiparse_fwd_pack_kernel<128>, grid, kRopeThreads, smem, sms);
+    skiparse_fwd_pack_kernel<128><<<grid, kRopeThreads, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(skiparse_fwd_pack_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    grid = one_wave(skiparse_fwd_pack_kernel<64>, grid, kRopeThreads, smem, sms);
+    skiparse_fwd_pack_kernel<64><<<grid, kRopeThreads, smem, stream>>>(p);
   }
   return cudaGetLastError();
 }

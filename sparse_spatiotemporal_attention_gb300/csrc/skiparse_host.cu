@@ -15,6 +15,7 @@
 // scope (position p = n*G + kk), landing as 128 rows of 128 B with 128-byte
 // swizzle. Rows past the end of a scope read the next batch's rows or zero
 // fill; the kernels mask them.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -170,18 +171,19 @@ int check_shape(int B, int heads, int N, int D, int T, int H, int W, int k, int 
     return SKIPARSE_OK;
   }
   if (D != 64 && D != 128) return SKIPARSE_ERR_UNSUPPORTED;
-  if (mode == SKIPARSE_SINGLE && N % k != 0) return SKIPARSE_ERR_SHAPE;
-  if (mode == SKIPARSE_GROUP) {
-    if ((long long)k * k > N || N % (k * k) != 0) return SKIPARSE_ERR_SHAPE;
-    if (128 % k != 0) return SKIPARSE_ERR_UNSUPPORTED;
-  }
+  // any N: scopes of unequal length when k (single) or k^2 (group) does not divide it
+  if (mode == SKIPARSE_GROUP && 128 % k != 0) return SKIPARSE_ERR_UNSUPPORTED;
   const long long entries = (long long)T * (D / 8) + (long long)H * (3 * D / 16) + (long long)W * (3 * D / 16);
   if (entries > kMaxRopeEntries) return SKIPARSE_ERR_UNSUPPORTED;
   s.rope_entries = (int)entries;
   s.elems = (long long)B * N * heads * D;
-  const long long L = N / k;
-  const long long units = (long long)B * heads * k * ((L + kTile - 1) / kTile);
-  if (s.elems > (1ll << 46) || units >= (1ll << 31) || (long long)B * N * heads >= (1ll << 31))
+  const long long G = mode == SKIPARSE_SINGLE ? 1 : k;
+  const long long L0 = (N / (k * G)) * G + std::min<long long>(N % (k * G), G);   // scope 0, the longest
+  const long long tiles = (L0 + kTile - 1) / kTile;
+  const long long units = (long long)B * heads * k * tiles;
+  const long long packed_rows = (long long)k * B * tiles * kTile * heads;         // scope-ordered copies
+  if (s.elems > (1ll << 46) || units >= (1ll << 31) || (long long)B * N * heads >= (1ll << 31) ||
+      packed_rows >= (1ll << 31))
     return SKIPARSE_ERR_UNSUPPORTED;
   return SKIPARSE_OK;
 }
@@ -223,9 +225,17 @@ Geom make_geom(const Shape& s) {
   g.fkG = make_fastdiv(s.k * g.G);
   g.fheads = make_fastdiv(s.heads > 0 ? s.heads : 1);
   g.fN = make_fastdiv(s.N > 0 ? s.N : 1);
-  g.L = s.N / s.k;
+  g.fB = make_fastdiv(s.B > 0 ? s.B : 1);
+  g.Qb = s.N / (s.k * g.G);
+  g.Rb = s.N % (s.k * g.G);
+  g.L = scope_len(g, 0);
   g.Nn = g.L / g.G;
   g.n_tiles = (g.L + kTile - 1) / kTile;
+  g.Lp = g.n_tiles * kTile;
+  g.fLp = make_fastdiv(g.Lp > 0 ? g.Lp : 1);
+  // scopes of unequal length are read from scope-ordered copies: the gather
+  // maps' per-dimension bounds cannot stop a read past the end of a shorter scope
+  g.packed = g.Rb != 0 ? 1 : 0;
   return g;
 }
 
@@ -266,6 +276,32 @@ bool encode_scope_map(CUtensorMap* m, const void* base, const Geom& g) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// 3-D bf16 map over a scope-ordered copy (k, B, Lp, heads, D): dims (channel,
+// head, row), a box of 64 channels x 1 head x 128 rows with 128-byte swizzle.
+bool encode_packed_map(CUtensorMap* m, const void* base, const Geom& g) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)g.heads, (cuuint64_t)g.k * g.B * g.Lp};
+  const cuuint64_t strides[2] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.heads * g.D * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// bytes of one scope-ordered bf16 copy (k, B, Lp, heads, D)
+size_t packed_bytes(const Geom& g) { return (size_t)g.k * g.B * g.Lp * g.heads * g.D * 2; }
+
+// Forward workspace: rotated q and k in row order, or (unequal scopes) q, k
+// and v in scope order.
+size_t fwd_ws_bytes(const Shape& s) {
+  const Geom g = make_geom(s);
+  if (g.packed) return 3 * align256(packed_bytes(g));
+  return 2 * align256((size_t)s.elems * 2);
+}
 
 // 2-D bf16 tensor map over a row-major (rows, cols) matrix: boxes of 64 columns
 // (128 bytes, 128-byte swizzle) x box_rows rows; reads past either edge fill zeros.
@@ -323,8 +359,7 @@ struct Ws8Layout {
 
 Ws8Layout ws8_layout(const Shape& s, bool si8) {
   Ws8Layout w;
-  const int L = s.N / s.k;
-  w.Lp = ((L + kTile - 1) / kTile) * kTile;
+  w.Lp = make_geom(s).Lp;
   w.scopes = s.B * s.heads * s.k;
   const size_t rows = (size_t)w.scopes * w.Lp;
   const size_t qk_row = fwd8_qk_row_bytes(si8);
@@ -340,22 +375,27 @@ Ws8Layout ws8_layout(const Shape& s, bool si8) {
 }
 
 struct WsLayout {
-  size_t dq_acc, qr, kr, lse2s, delta_s, tab, total;
+  size_t dq_acc, qr, kr, vp, dop, lse2s, delta_s, tab, total;
   int Lp;
 };
 
 // with_qk = false: the rotated q / k come from the forward pass's workspace and
 // their regions are left out (the full layout is a superset).
+// Scopes of unequal length (packed): q, k (rotated) and v in scope order unless
+// the forward's are reused (with_qk = false), and dout in scope order.
 WsLayout ws_layout(const Shape& s, bool with_qk = true) {
   WsLayout w;
   const size_t e = (size_t)s.elems;
-  const int L = s.N / s.k;
-  w.Lp = ((L + kTile - 1) / kTile) * kTile;
+  const Geom g = make_geom(s);
+  w.Lp = g.Lp;
   const size_t stats = (size_t)s.B * s.heads * s.k * w.Lp;
+  const size_t copy = g.packed ? align256(packed_bytes(g)) : align256(e * 2);
   size_t off = 0;
   w.dq_acc = off; off += align256(stats * (size_t)s.D * 4);   // scope order (B, heads, k, Lp, D)
-  w.qr = off;     off += with_qk ? align256(e * 2) : 0;
-  w.kr = off;     off += with_qk ? align256(e * 2) : 0;
+  w.qr = off;     off += with_qk ? copy : 0;
+  w.kr = off;     off += with_qk ? copy : 0;
+  w.vp = off;     off += (g.packed && with_qk) ? copy : 0;
+  w.dop = off;    off += g.packed ? copy : 0;
   w.lse2s = off;  off += align256(stats * 4);
   w.delta_s = off; off += align256(stats * 4);
   w.tab = off;    off += align256((size_t)s.rope_entries * sizeof(float2));
@@ -381,7 +421,7 @@ const char* skiparse_status_string(int status) {
   switch (status) {
     case SKIPARSE_OK: return "ok";
     case SKIPARSE_ERR_INVALID_ARG: return "invalid argument (NULL pointer, negative size, bad mode or rope_theta)";
-    case SKIPARSE_ERR_SHAPE: return "shape mismatch (N != T*H*W, or N not divisible by k (single) / k*k (group))";
+    case SKIPARSE_ERR_SHAPE: return "shape mismatch (N != T*H*W; the 8-bit forwards also need k (single) / k*k (group) to divide N)";
     case SKIPARSE_ERR_UNSUPPORTED: return "unsupported configuration (D must be 64 or 128; group k must divide 128; RoPE table too large)";
     case SKIPARSE_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case SKIPARSE_ERR_DEVICE: return "no CUDA device, or the current device is not sm_103 (GB300)";
@@ -413,7 +453,7 @@ const char* skiparse_kernel_name(int id) {
 size_t skiparse_attn_fwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode) {
   Shape s;
   if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty) return 0;
-  return 2 * align256((size_t)s.elems * 2);
+  return fwd_ws_bytes(s);
 }
 
 int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -425,11 +465,11 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   if (st != SKIPARSE_OK || s.empty) return st;
   if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
-  const size_t half = align256((size_t)s.elems * 2);
-  if (!workspace || workspace_bytes < 2 * half) return SKIPARSE_ERR_WORKSPACE;
+  const size_t need = fwd_ws_bytes(s);
+  if (!workspace || workspace_bytes < need) return SKIPARSE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
   const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
-  if (any_alias({{out, tb}, {lse, lb}, {workspace, 2 * half}}, {{q, tb}, {k, tb}, {v, tb}})) return SKIPARSE_ERR_ALIAS;
+  if (any_alias({{out, tb}, {lse, lb}, {workspace, need}}, {{q, tb}, {k, tb}, {v, tb}})) return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
   if ((size_t)dev.smem_optin < fwd_smem_bytes(D) || (size_t)dev.smem_optin < fwd_rope_smem_bytes(s.rope_entries))
@@ -442,12 +482,26 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);
-  p.qr = reinterpret_cast<uint16_t*>(ws);
-  p.kr = reinterpret_cast<uint16_t*>(ws + half);
+  p.v = static_cast<const uint16_t*>(v);
   const bool rotate = rope_theta != 0.0f;            // 0: q and k are already rotated
-  if (!encode_scope_map(&p.tm_q, rotate ? p.qr : q, p.g) || !encode_scope_map(&p.tm_k, rotate ? p.kr : k, p.g) ||
-      !encode_scope_map(&p.tm_v, v, p.g))
-    return SKIPARSE_ERR_LAUNCH;
+  p.rotate = rotate ? 1 : 0;
+  if (p.g.packed) {
+    // scopes of unequal length: q, k (rotated) and v in scope order
+    const size_t pb = align256(packed_bytes(p.g));
+    p.qr = reinterpret_cast<uint16_t*>(ws);
+    p.kr = reinterpret_cast<uint16_t*>(ws + pb);
+    p.vr = reinterpret_cast<uint16_t*>(ws + 2 * pb);
+    if (!encode_packed_map(&p.tm_q, p.qr, p.g) || !encode_packed_map(&p.tm_k, p.kr, p.g) ||
+        !encode_packed_map(&p.tm_v, p.vr, p.g))
+      return SKIPARSE_ERR_LAUNCH;
+  } else {
+    const size_t half = align256((size_t)s.elems * 2);
+    p.qr = reinterpret_cast<uint16_t*>(ws);
+    p.kr = reinterpret_cast<uint16_t*>(ws + half);
+    if (!encode_scope_map(&p.tm_q, rotate ? p.qr : q, p.g) || !encode_scope_map(&p.tm_k, rotate ? p.kr : k, p.g) ||
+        !encode_scope_map(&p.tm_v, v, p.g))
+      return SKIPARSE_ERR_LAUNCH;
+  }
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.err = dev.err_word;
@@ -457,7 +511,10 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
   long long rgrid = (rows + 15) / 16;                 // 8 warps per CTA, 2 rows per warp
   if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
-  if (rotate) {
+  if (p.g.packed) {
+    st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_pack(p, 8 * dev.sms, dev.sms, stream); }));
+    if (st != SKIPARSE_OK) return st;
+  } else if (rotate) {
     st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, dev.sms, stream); }));
     if (st != SKIPARSE_OK) return st;
   }
@@ -468,6 +525,7 @@ size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int
                                              int mode) {
   Shape s;
   if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty || D != 128) return 0;
+  if (make_geom(s).packed) return 0;
   return ws8_layout(s, false).total;
 }
 
@@ -475,6 +533,7 @@ size_t skiparse_attn_fwd_mixed8_workspace_bytes(int B, int heads, int N, int D, 
                                                 int mode) {
   Shape s;
   if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty || D != 128) return 0;
+  if (make_geom(s).packed) return 0;
   return ws8_layout(s, true).total;
 }
 
@@ -490,6 +549,8 @@ int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, 
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
   if (D != 128) return SKIPARSE_ERR_UNSUPPORTED;
+  // the 8-bit preparation gathers q and k through the scope maps: equal scopes only
+  if (make_geom(s).packed) return SKIPARSE_ERR_SHAPE;
   if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
   const Ws8Layout w = ws8_layout(s, si8);
@@ -570,53 +631,58 @@ size_t skiparse_attn_bwd_workspace_bytes(int B, int heads, int N, int D, int T, 
 
 namespace {
 
-// Backward: q / k given (rotated here, qr_in == kr_in == nullptr), or the
-// forward pass's rotated copies qr_in / kr_in (q == k == nullptr).
-int bwd_impl(const void* q, const void* k, const void* qr_in, const void* kr_in, size_t fwd_ws_bytes,
+// Backward: q / k given (rotated here; fwd_ws == nullptr), or the forward
+// pass's workspace (q == k == nullptr) holding its rotated q / k (row order), or
+// for scopes of unequal length its scope-ordered q, k and v.
+int bwd_impl(const void* q, const void* k, const void* fwd_ws, size_t fwd_ws_given,
              const void* v, const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
              void* workspace, size_t workspace_bytes, int B, int heads, int N, int D, int T, int H, int W,
              int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
   Shape s;
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
-  const bool saved = qr_in != nullptr;
+  const bool saved = fwd_ws != nullptr;
   const bool rotate = rope_theta != 0.0f;            // 0: q and k are already rotated
   if (saved && !rotate) return SKIPARSE_ERR_INVALID_ARG;   // the forward wrote no rotated copies
   if (!v || !out || !lse || !dout || !dq || !dk || !dv) return SKIPARSE_ERR_INVALID_ARG;
-  if (saved ? !kr_in : (!q || !k)) return SKIPARSE_ERR_INVALID_ARG;
-  const void* qa = saved ? qr_in : q;
-  const void* ka = saved ? kr_in : k;
+  if (!saved && (!q || !k)) return SKIPARSE_ERR_INVALID_ARG;
+  const Geom geom = make_geom(s);
+  const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
+  const size_t fwd_need = fwd_ws_bytes(s);
+  const uint8_t* fw = static_cast<const uint8_t*>(fwd_ws);
+  const size_t fcopy = geom.packed ? align256(packed_bytes(geom)) : align256(tb);
+  const void* qa = saved ? fw : q;
+  const void* ka = saved ? fw + fcopy : k;
   if (!aligned16(qa) || !aligned16(ka) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return SKIPARSE_ERR_ALIGNMENT;
-  const WsLayout w = ws_layout(s, !saved && rotate);
+  const WsLayout w = ws_layout(s, !saved && (rotate || geom.packed));
   if (!workspace || workspace_bytes < w.total) return SKIPARSE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
-  const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
-  if (saved && fwd_ws_bytes < 2 * align256(tb)) return SKIPARSE_ERR_WORKSPACE;
-  if (any_alias({{dq, tb}, {dk, tb}, {dv, tb}, {workspace, w.total}},
-                {{qa, tb}, {ka, tb}, {v, tb}, {out, tb}, {lse, lb}, {dout, tb}}))
-    return SKIPARSE_ERR_ALIAS;
+  if (saved && fwd_ws_given < fwd_need) return SKIPARSE_ERR_WORKSPACE;
+  std::vector<Range> ins = {{v, tb}, {out, tb}, {lse, lb}, {dout, tb}};
+  if (saved) ins.push_back({fwd_ws, fwd_need});
+  else {
+    ins.push_back({q, tb});
+    ins.push_back({k, tb});
+  }
+  if (any_alias({{dq, tb}, {dk, tb}, {dv, tb}, {workspace, w.total}}, ins)) return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
   if ((size_t)dev.smem_optin < bwd_main_smem_bytes(D)) return SKIPARSE_ERR_UNSUPPORTED;
 
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
-  p.g = make_geom(s);
+  p.g = geom;
   p.rope = make_rope(s, rope_theta);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
   p.out = static_cast<const uint16_t*>(out);
   p.dout = static_cast<const uint16_t*>(dout);
   p.lse = lse;
   p.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
-  p.rotate_qk = (!saved && rotate) ? 1 : 0;
-  p.qr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(qr_in))
-               : rotate ? reinterpret_cast<uint16_t*>(ws + w.qr) : const_cast<uint16_t*>(static_cast<const uint16_t*>(q));
-  p.kr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(kr_in))
-               : rotate ? reinterpret_cast<uint16_t*>(ws + w.kr) : const_cast<uint16_t*>(static_cast<const uint16_t*>(k));
   p.lse2s = reinterpret_cast<float*>(ws + w.lse2s);
   p.delta_s = reinterpret_cast<float*>(ws + w.delta_s);
   p.rope_tab = reinterpret_cast<float2*>(ws + w.tab);
@@ -628,15 +694,35 @@ int bwd_impl(const void* q, const void* k, const void* qr_in, const void* kr_in,
   p.n_units = B * heads * sparse_k * p.g.n_tiles;
   p.scale = (float)(1.0 / std::sqrt((double)D));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  if (!encode_scope_map(&p.tm_q, p.qr, p.g) || !encode_scope_map(&p.tm_k, p.kr, p.g) ||
-      !encode_scope_map(&p.tm_v, v, p.g) || !encode_scope_map(&p.tm_do, dout, p.g))
-    return SKIPARSE_ERR_LAUNCH;
+  bool maps_ok;
+  if (p.g.packed) {
+    // scopes of unequal length: every operand from a scope-ordered copy
+    p.write_qkv = saved ? 0 : 1;
+    p.rotate_qk = rotate ? 1 : 0;
+    uint8_t* fwm = const_cast<uint8_t*>(fw);
+    p.qr = reinterpret_cast<uint16_t*>(saved ? fwm : ws + w.qr);
+    p.kr = reinterpret_cast<uint16_t*>(saved ? fwm + fcopy : ws + w.kr);
+    p.vp = reinterpret_cast<uint16_t*>(saved ? fwm + 2 * fcopy : ws + w.vp);
+    p.dop = reinterpret_cast<uint16_t*>(ws + w.dop);
+    maps_ok = encode_packed_map(&p.tm_q, p.qr, p.g) && encode_packed_map(&p.tm_k, p.kr, p.g) &&
+              encode_packed_map(&p.tm_v, p.vp, p.g) && encode_packed_map(&p.tm_do, p.dop, p.g);
+  } else {
+    p.rotate_qk = (!saved && rotate) ? 1 : 0;
+    p.qr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(qa))
+                 : rotate ? reinterpret_cast<uint16_t*>(ws + w.qr) : const_cast<uint16_t*>(static_cast<const uint16_t*>(q));
+    p.kr = saved ? const_cast<uint16_t*>(static_cast<const uint16_t*>(ka))
+                 : rotate ? reinterpret_cast<uint16_t*>(ws + w.kr) : const_cast<uint16_t*>(static_cast<const uint16_t*>(k));
+    maps_ok = encode_scope_map(&p.tm_q, p.qr, p.g) && encode_scope_map(&p.tm_k, p.kr, p.g) &&
+              encode_scope_map(&p.tm_v, v, p.g) && encode_scope_map(&p.tm_do, dout, p.g);
+  }
+  if (!maps_ok) return SKIPARSE_ERR_LAUNCH;
 
   const long long rows = (long long)B * N * heads;
   long long rgrid = (rows + 15) / 16;                 // 8 warps per CTA, 2 rows per warp
   if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
+  const int pregrid = p.g.packed ? 8 * dev.sms : (int)rgrid;
   const int mgrid = p.n_units < dev.sms ? p.n_units : dev.sms;
-  st = launch_status(traced_launch(1, stream, [&] { return launch_bwd_pre(p, (int)rgrid, dev.sms, stream); }));
+  st = launch_status(traced_launch(1, stream, [&] { return launch_bwd_pre(p, pregrid, dev.sms, stream); }));
   if (st != SKIPARSE_OK) return st;
   st = launch_status(traced_launch(2, stream, [&] { return launch_bwd_main(p, mgrid, stream); }));
   if (st != SKIPARSE_OK) return st;
@@ -651,8 +737,8 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                       int B, int heads, int N, int D, int T, int H, int W,
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
-  return bwd_impl(q, k, nullptr, nullptr, 0, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, heads, N,
-                  D, T, H, W, sparse_k, mode, rope_theta, stream);
+  return bwd_impl(q, k, nullptr, 0, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, heads, N, D, T, H,
+                  W, sparse_k, mode, rope_theta, stream);
 }
 
 int skiparse_attn_bwd_saved(const void* fwd_workspace, size_t fwd_workspace_bytes, const void* v, const void* out,
@@ -664,10 +750,9 @@ int skiparse_attn_bwd_saved(const void* fwd_workspace, size_t fwd_workspace_byte
   if (st != SKIPARSE_OK || s.empty) return st;
   if (!fwd_workspace) return SKIPARSE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(fwd_workspace) & 255u) != 0) return SKIPARSE_ERR_ALIGNMENT;
-  // the forward workspace holds rotated q, then rotated k, each 256-byte aligned
-  const uint8_t* fw = static_cast<const uint8_t*>(fwd_workspace);
-  const size_t half = align256((size_t)s.elems * 2);
-  return bwd_impl(nullptr, nullptr, fw, fw + half, fwd_workspace_bytes, v, out, lse, dout, dq, dk, dv, workspace,
+  // the forward workspace holds rotated q, then rotated k (and, for scopes of
+  // unequal length, v), each 256-byte aligned
+  return bwd_impl(nullptr, nullptr, fwd_workspace, fwd_workspace_bytes, v, out, lse, dout, dq, dk, dv, workspace,
                   workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, stream);
 }
 
@@ -677,9 +762,6 @@ int skiparse_debug_index_map(int* scope_of_token, int* pos_of_token, int N, int 
   if (N < 0 || sparse_k < 1) return SKIPARSE_ERR_INVALID_ARG;
   if (N == 0) return SKIPARSE_OK;
   if (!scope_of_token || !pos_of_token) return SKIPARSE_ERR_INVALID_ARG;
-  if (N % sparse_k != 0) return SKIPARSE_ERR_SHAPE;
-  if (mode == SKIPARSE_GROUP && ((long long)sparse_k * sparse_k > N || N % (sparse_k * sparse_k) != 0))
-    return SKIPARSE_ERR_SHAPE;
   if (mode == SKIPARSE_GROUP && 128 % sparse_k != 0) return SKIPARSE_ERR_UNSUPPORTED;
   if (any_alias({{scope_of_token, (size_t)N * 4}, {pos_of_token, (size_t)N * 4}}, {})) return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;

@@ -24,8 +24,11 @@ struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;   // scope-gather maps over rotated q, rotated k (workspace) and v
   const uint16_t* q;              // pre-RoPE inputs (RoPE pass)
   const uint16_t* k;
-  uint16_t* qr;                   // workspace: rotated q, bf16 (B, N, heads, D)
-  uint16_t* kr;                   // workspace: rotated k
+  const uint16_t* v;              // v (pack pass)
+  uint16_t* qr;                   // workspace: rotated q, bf16 (B, N, heads, D); packed: (k, B, Lp, heads, D)
+  uint16_t* kr;                   // workspace: rotated k, likewise
+  uint16_t* vr;                   // packed only: v in scope order (k, B, Lp, heads, D)
+  int rotate;                     // 0: rope_theta = 0 (q, k arrive rotated; the pack pass only copies)
   Geom g;
   RopeParams rope;
   uint16_t* out;                  // bf16 (B, N, heads, D)
@@ -44,8 +47,13 @@ struct BwdParams {
   const uint16_t* out;
   const uint16_t* dout;
   const float* lse;
-  uint16_t* qr;            // rotated q, bf16 (B, N, heads, D): workspace, or the forward's
+  const uint16_t* v;
+  uint16_t* qr;            // rotated q, bf16 (B, N, heads, D): workspace, or the forward's;
+                           // packed: scope order (k, B, Lp, heads, D)
   uint16_t* kr;            // rotated k, likewise
+  uint16_t* vp;            // packed only: v in scope order (workspace, or the forward's)
+  uint16_t* dop;           // packed only: dout in scope order (workspace)
+  int write_qkv;           // packed only: 1 the pack pass writes qr, kr (rotated) and vp; 0 they are the forward's
   float* dq_acc;           // workspace: fp32 (B, heads, k, Lp, D), scope order
   float* lse2s;            // workspace: lse * log2(e), scope order (B, heads, k, Lp)
   float* delta_s;          // workspace: rowsum(dO * O), scope order (B, heads, k, Lp)
@@ -137,6 +145,7 @@ size_t fwd_smem_bytes(int D);
 size_t fwd_rope_smem_bytes(int rope_entries);
 int fwd_units(const Geom& g);
 cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t stream);
+cudaError_t launch_fwd_pack(const FwdParams& p, int grid, int sms, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
 
 // si8: the mixed recipe (INT8 q / k codes held as bf16 for S, E4M3 P and v)

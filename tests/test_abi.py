@@ -67,8 +67,14 @@ def test_fwd_validation(lib):
     assert fwd(lib, theta=float("inf")) == INVALID
     assert fwd(lib, N=255) == SHAPE                      # N != T*H*W
     assert fwd(lib, D=96) == UNSUP
-    assert fwd(lib, T=3, N=192, sk=5) == SHAPE           # 192 % 5
-    assert fwd(lib, N=256, sk=32, mode=1) == SHAPE       # 256 % 1024
+    # k (single) or k^2 (group) need not divide N: scopes of unequal length, valid
+    # (no GPU here), with the larger scope-ordered workspace
+    ragged_ws = lib.skiparse_attn_fwd_workspace_bytes(1, 2, 192, 64, 3, 8, 8, 5, 0)
+    assert fwd(lib, T=3, N=192, sk=5, ws_bytes=ragged_ws) == DEVICE
+    assert fwd(lib, T=3, N=192, sk=5, ws_bytes=ragged_ws - 1) == WORKSPACE
+    # group skip with k^2 > N: 8 scopes of one group each, 24 empty ones
+    assert fwd(lib, N=256, sk=32, mode=1, ws_bytes=lib.skiparse_attn_fwd_workspace_bytes(1, 2, 256, 64, 4, 8, 8, 32,
+                                                                                         1)) == DEVICE
     assert fwd(lib, T=9, H=6, W=6, N=324, sk=3, mode=1) == UNSUP   # group k must divide 128
     assert fwd(lib, T=2000, H=20, W=20, N=800000) == UNSUP         # RoPE table too large
     assert fwd(lib, q=None) == INVALID
@@ -134,8 +140,24 @@ def test_bwd_saved_validation(lib):
     assert bwd(ws_bytes=ws - 2 * 256 * 2 * 64 * 2) == DEVICE
 
 
+def test_ragged_workspace_sizes(lib):
+    """Scopes of unequal length read scope-ordered copies (k, B, Lp, heads, D) of
+    q, k, v (forward) and of q, k, v, dO (backward); the 8-bit forwards refuse them."""
+    B, heads, D, N, k = 1, 2, 64, 192, 5                 # single skip: L_0 = 39, Lp = 128
+    copy = k * B * 128 * heads * D * 2
+    assert lib.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, 3, 8, 8, k, 0) == 3 * copy
+    stats = B * heads * k * 128
+    want = stats * D * 4 + 4 * copy + 2 * stats * 4
+    got = lib.skiparse_attn_bwd_workspace_bytes(B, heads, N, D, 3, 8, 8, k, 0)
+    assert want <= got <= want + 8 * 256 + 16 * 8192
+    assert lib.skiparse_attn_fwd_fp8_workspace_bytes(1, 2, 192, 128, 3, 8, 8, 5, 0) == 0
+    assert lib.skiparse_attn_fwd_mixed8_workspace_bytes(1, 2, 192, 128, 3, 8, 8, 5, 0) == 0
+    assert lib.skiparse_attn_fwd_fp8(A, 2 * A, 3 * A, 4 * A, 5 * A, 10 * A, 1 << 30, 1, 2, 192, 128, 3, 8, 8, 5, 0,
+                                     10000.0, None) == SHAPE
+
+
 def test_debug_hook_validation(lib):
-    assert lib.skiparse_debug_index_map(A, 2 * A, 16, 3, 0, None) == SHAPE
+    assert lib.skiparse_debug_index_map(A, 2 * A, 16, 3, 0, None) == DEVICE     # any N: unequal scopes
     assert lib.skiparse_debug_index_map(A, 2 * A, 16, 2, 2, None) == INVALID
     assert lib.skiparse_debug_index_map(A, A, 16, 2, 0, None) == ALIAS
     assert lib.skiparse_debug_index_map(None, None, 0, 2, 0, None) == OK

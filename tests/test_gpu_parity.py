@@ -88,7 +88,41 @@ def test_backward_parity(env, case):
     assert st == 0, hex(detail)
 
 
-SAVED_CASES = [(1, 2, 128, 3, 10, 10, 2, O.GROUP), (2, 3, 64, 2, 8, 12, 2, O.SINGLE), (2, 2, 128, 3, 20, 24, 4, O.SINGLE)]
+# N that k (single) or k^2 (group) does not divide: scopes of unequal length,
+# read from scope-ordered copies. Each case names its scope lengths.
+RAGGED_CASES = [
+    (1, 2, 128, 4, 8, 9, 5, O.SINGLE),       # N = 288: scopes 58, 58, 58, 57, 57
+    (2, 2, 128, 5, 5, 41, 4, O.SINGLE),      # N = 1025: 257 (3 tiles), 256 x 3 (2 tiles), B = 2
+    (1, 2, 64, 3, 10, 11, 4, O.SINGLE),      # D = 64, N = 330: 83, 83, 82, 82
+    (1, 2, 128, 1, 27, 19, 4, O.GROUP),      # N = 513: 129 (2 tiles: a one-token group), 128 x 3
+    (2, 2, 128, 3, 7, 9, 4, O.GROUP),        # N = 189: 48, 48, 48, 45 (a partial group), B = 2
+    (1, 3, 64, 5, 5, 5, 2, O.GROUP),         # D = 64, N = 125: 63, 62 (the last group holds one token)
+    (1, 2, 128, 1, 8, 9, 8, O.GROUP),        # N = 72 < k^2 = 64 + 8: nine groups, scope 0 two (16), the rest one
+]
+
+
+@pytest.mark.parametrize("case", RAGGED_CASES, ids=_ids)
+def test_ragged_forward_backward_parity(env, case):
+    skp, dev = env
+    B, heads, D, T, H, W, k, mode = case
+    N = T * H * W
+    assert not O.divisible(N, k, mode)
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True)
+    fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode)
+    bw = tl.run_bwd(skp, dev, ins, fw, B, heads, N, D, T, H, W, k, mode)
+    f = tl.f64_inputs(ins)
+    rdq, rdk, rdv, rout, rlse = O.skiparse_bwd(f["q"], f["k"], f["v"], f["do"], T, H, W, k, mode)
+    tl.compare("out", tl.host(fw["out"]), rout)
+    tl.compare("lse", tl.host(fw["lse"]), rlse, tol_max=tl.TOL_LSE, tol_mean=tl.TOL_LSE, tol_rel=1e-3)
+    tl.compare("dv", tl.host(bw["dv"]), rdv)
+    tl.compare("dk", tl.host(bw["dk"]), rdk)
+    tl.compare("dq", tl.host(bw["dq"]), rdq)
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
+
+
+SAVED_CASES = [(1, 2, 128, 3, 10, 10, 2, O.GROUP), (2, 3, 64, 2, 8, 12, 2, O.SINGLE), (2, 2, 128, 3, 20, 24, 4, O.SINGLE),
+               (2, 2, 128, 3, 7, 9, 4, O.GROUP), (1, 2, 64, 3, 10, 11, 4, O.SINGLE)]
 
 
 @pytest.mark.parametrize("case", SAVED_CASES, ids=_ids)
@@ -148,18 +182,19 @@ def test_peaky_softmax_rescale(env):
 
 
 @pytest.mark.parametrize("mode", [O.SINGLE, O.GROUP])
-@pytest.mark.parametrize("N,k", [(256, 2), (4096, 4), (21120, 4), (57600, 4), (1024, 8), (300, 3), (512, 1)])
+@pytest.mark.parametrize("N,k", [(256, 2), (4096, 4), (21120, 4), (57600, 4), (1024, 8), (300, 3), (512, 1),
+                                 (1025, 4), (513, 4), (189, 4), (21525, 4), (77, 8), (7, 5)])
 def test_index_map_bit_exact(env, mode, N, k):
+    """Any N (scopes of unequal length where k or k^2 does not divide it)."""
     import torch
     skp, dev = env
     scope = torch.full((N,), -7, dtype=torch.int32, device=dev)
     pos = torch.full((N,), -7, dtype=torch.int32, device=dev)
-    bad_group = mode == O.GROUP and (N % (k * k) != 0 or 128 % k != 0)
-    if N % k or bad_group:
-        # no such rearrange (N not divisible by k, or by k^2 for group skip): refused, nothing written
+    if mode == O.GROUP and 128 % k != 0:
+        # a 128-row tile must hold whole groups: refused, nothing written
         with pytest.raises(skp.SkiparseError) as e:
             skp.skiparse_debug_index_map(scope, pos, N, k, mode)
-        assert e.value.status == (-2 if (N % k or N % (k * k)) else -3)
+        assert e.value.status == -3
         torch.cuda.synchronize()
         assert bool((scope == -7).all()) and bool((pos == -7).all())
         return
