@@ -29,8 +29,11 @@ Printed JSON line (rank 0):
                the measured bf16 peak x the nominal FP8 / bf16 ratio).
 
 --impl reference times the oracle alone (the reference arm of this method).
-Multi-GPU: one process per GPU (torchrun); every rank runs its own batch
-(weak scaling), the time is the max over ranks.
+Multi-GPU: one process per GPU (torchrun, or started here for --gpus N); the
+time is the max over ranks. --shard replicas (default): every rank runs its own
+batch (weak scaling). --shard scopes: the ranks split one batch's scopes
+round-robin (skiparse_attn_fwd_scopes / skiparse_attn_bwd_scopes), no data
+exchanged (strong scaling; useful up to sparse_k ranks).
 """
 from __future__ import annotations
 
@@ -397,7 +400,10 @@ def gpu_arm(args):
     w = WORKLOAD
     B, heads, D, T, H, W, k, mode = w["B"], w["heads"], w["D"], w["T"], w["H"], w["W"], w["k"], w["mode"]
     N = T * H * W
-    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True, seeds=rank_seeds(rank))
+    shard = args.shard == "scopes"
+    # scope shards: every rank holds the same batch and computes its scopes of it
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True, seeds=rank_seeds(0 if shard else rank))
+    first, sstep = skp.scope_shard(k, world, rank) if shard else (0, 1)
     pin = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for n, a in ins.items()}
     d = {n: t.to(dev) for n, t in pin.items()}
     out = torch.empty_like(d["q"])
@@ -412,6 +418,12 @@ def gpu_arm(args):
     # a training step: the backward reuses the rotated q / k the forward left in
     # its workspace (as autograd keeps a forward's saved tensors for its backward)
     def step(kk=k):
+        if shard:
+            skp.skiparse_attn_fwd_scopes(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, mode, first, sstep,
+                                         stream=stream, workspace=fws)
+            skp.skiparse_attn_bwd_scopes(d["q"], d["k"], d["v"], out, lse, d["do"], dq, dk, dv, ws, T, H, W, kk, mode,
+                                         first, sstep, stream=stream)
+            return
         skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, mode, stream=stream, workspace=fws)
         skp.skiparse_attn_bwd_saved(fws, d["v"], out, lse, d["do"], dq, dk, dv, ws, T, H, W, kk, mode,
                                     stream=stream)
@@ -449,7 +461,10 @@ def gpu_arm(args):
     ms = max_ranks(e0.elapsed_time(e1))
     ms_step = ms / args.steps
     flops_step = 3.5 * fwd_flops(w)
-    value = job_tflops(world, flops_step, ms_step)
+    # replicas: every rank a whole step of its own batch; scope shards: the ranks
+    # together one step of one batch
+    job_ranks = 1 if shard else world
+    value = job_tflops(job_ranks, flops_step, ms_step)
 
     # ---- e2e: every step's inputs copied in from pinned host memory and all of
     # its outputs copied out, inside the timed region. The copies run on two copy
@@ -467,6 +482,12 @@ def gpu_arm(args):
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def step_on(di, do_):
+        if shard:
+            skp.skiparse_attn_fwd_scopes(di["q"], di["k"], di["v"], do_["out"], do_["lse"], T, H, W, k, mode, first,
+                                         sstep, stream=stream, workspace=fws)
+            skp.skiparse_attn_bwd_scopes(di["q"], di["k"], di["v"], do_["out"], do_["lse"], di["do"], do_["dq"],
+                                         do_["dk"], do_["dv"], ws, T, H, W, k, mode, first, sstep, stream=stream)
+            return
         skp.skiparse_attn_fwd(di["q"], di["k"], di["v"], do_["out"], do_["lse"], T, H, W, k, mode, stream=stream,
                               workspace=fws)
         skp.skiparse_attn_bwd_saved(fws, di["v"], do_["out"], do_["lse"], di["do"], do_["dq"], do_["dk"], do_["dv"],
@@ -507,7 +528,7 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     barrier()
     ms_e2e = max_ranks(e_start.elapsed_time(e_end)) / e2e_steps
-    e2e = {"value": job_tflops(world, flops_step, ms_e2e), "unit": "TFLOP/s", "ms_per_step": ms_e2e,
+    e2e = {"value": job_tflops(job_ranks, flops_step, ms_e2e), "unit": "TFLOP/s", "ms_per_step": ms_e2e,
            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
            "copies": "pinned host <-> device on two copy streams, double-buffered, overlapping compute"}
     st, detail = skp.skiparse_device_error()
@@ -516,7 +537,7 @@ def gpu_arm(args):
 
     # ---- the same step at k=1 (dense attention) for the speedup
     k1 = None
-    if not args.no_k1:
+    if not args.no_k1 and not shard:
         k1_steps = max(2, min(args.steps // 10, 10))
         step(1)
         torch.cuda.synchronize()
@@ -547,7 +568,7 @@ def gpu_arm(args):
                                             "share": kms[i] / tot}
     dom = max(range(nk), key=lambda i: kms[i])
     dom_ms = kms[dom] / max(1, kcnt[dom])
-    dom_flops = KERNEL_FLOP_FACTOR[dom] * fwd_flops(w)
+    dom_flops = KERNEL_FLOP_FACTOR[dom] * fwd_flops(w) * len(range(first, k, sstep)) / k   # this rank's scopes
     # the timed region lasts a fraction of a second at full clocks: the burst
     # (dense) peak is the denominator; the sustained one is reported beside it
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -560,15 +581,18 @@ def gpu_arm(args):
                 "frac_of_sustained": achieved / peak_sus, "flops_per_launch": dom_flops}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "strong" if shard else "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) bf16 q, k, v, dO (splitmix64 + Box-Muller), no dataset",
         "config": {"workload": w["name"], "pass": "fwd+bwd", "B": B, "heads": heads, "D": D, "grid": f"{T}x{H}x{W}",
                    "N": N, "sparse_k": k, "mode": "group", "rope_theta": 10000.0,
                    "flops_per_step_per_gpu": flops_step,
                    "l2": "inputs larger than L2 (q, k, v, dO 260 MB each); no flush",
-                   "parallelism": f"replicas x{world}, each rank its own batch"},
+                   "parallelism": (f"scope shards x{world}: rank r computes scopes s = r mod {world} of one batch"
+                                   if shard else f"replicas x{world}, each rank its own batch")},
         "pct_of_peak": {"burst": value / world / peak, "sustained": value / world / peak_sus, "source": src},
+        "shard": args.shard,
         "fwd": {"ms_per_launch": fwd_ms, "tflops": fwd_flops(w) / (fwd_ms * 1e-3) / 1e12},
         "speedup_vs_k1": (k1 or {}).get("speedup"), "k1": k1,
         "fwd_configs": fwd_lines,
@@ -636,6 +660,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="train", choices=sorted(WORKLOADS))
+    ap.add_argument("--shard", default="replicas", choices=["replicas", "scopes"])
     ap.add_argument("--cpu-oracle-worker", type=float, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     global WORKLOAD

@@ -93,6 +93,30 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
+ * The forward and backward over a subset of the scopes: scopes scope_first,
+ * scope_first + scope_step, ... below sparse_k. Scopes never interact ("Open-
+ * Sora Plan" docs, "Skiparse Attention": attention runs inside each scope), so
+ * splitting them over GPUs needs no exchange of data: with G ranks, rank r
+ * passes (r, G) and the ranks' calls together compute the whole result. Only
+ * the rows of tokens in those scopes are written (out and lse; dq, dk and dv);
+ * every other row of the outputs is left as it was. Arguments, layouts,
+ * workspaces and errors are those of skiparse_attn_fwd / skiparse_attn_bwd
+ * (same workspace sizes); scope_first < 0 or scope_step < 1 give
+ * SKIPARSE_ERR_INVALID_ARG, and a subset with no scope (scope_first >=
+ * sparse_k) is a no-op returning SKIPARSE_OK. (0, 1) is the full call.
+ */
+int skiparse_attn_fwd_scopes(const void* q, const void* k, const void* v, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes,
+                             int B, int heads, int N, int D, int T, int H, int W,
+                             int sparse_k, int mode, float rope_theta, int scope_first, int scope_step,
+                             cudaStream_t stream);
+int skiparse_attn_bwd_scopes(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int B, int heads, int N, int D, int T, int H, int W,
+                             int sparse_k, int mode, float rope_theta, int scope_first, int scope_step,
+                             cudaStream_t stream);
+
+/*
  * 8-bit forward passes (D = 128): the Wan 2.1 report, section 4.4.3
  * "Quantization", paragraph "8-Bit FlashAttention", applied to this forward.
  * Both quantize q after RoPE per (token, head) row, k after RoPE per block of

@@ -31,6 +31,7 @@ EXPORTS = (
     "skiparse_attn_bwd_noalloc", "skiparse_debug_wait_timeout", "skiparse_attn_bwd_saved",
     "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8",
     "skiparse_attn_fwd_mixed8_workspace_bytes", "skiparse_attn_fwd_mixed8",
+    "skiparse_attn_fwd_scopes", "skiparse_attn_bwd_scopes",
     "skiparse_qkv_rope",
 )
 
@@ -74,6 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_attn_fwd_fp8_workspace_bytes": (_c_size, [_c_int] * 9),
         "skiparse_attn_fwd_fp8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_fwd_mixed8_workspace_bytes": (_c_size, [_c_int] * 9),
+        "skiparse_attn_fwd_scopes": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _c_int, _c_int, _vp]),
+        "skiparse_attn_bwd_scopes": (_c_int, [_vp] * 10 + [_c_size] + [_c_int] * 9 + [_c_float, _c_int, _c_int, _vp]),
         "skiparse_attn_fwd_mixed8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_bwd_saved": (_c_int, [_vp, _c_size] + [_vp] * 8 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
     }
@@ -197,6 +200,47 @@ def skiparse_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace, T, H, W, s
                                           B, heads, N, D, T, H, W, sparse_k, mode,
                                           float(rope_theta), _stream(stream))
     _check(st, "skiparse_attn_bwd")
+
+
+def skiparse_attn_fwd_scopes(q, k, v, out, lse, T, H, W, sparse_k, mode, scope_first, scope_step,
+                             rope_theta=10000.0, stream=None, workspace=None, workspace_bytes=None):
+    """Forward over the scopes scope_first, scope_first + scope_step, ... only;
+    the other rows of out and lse are left untouched."""
+    B, heads, N, D = _shape(q)
+    if workspace is None:
+        import torch
+        nbytes = skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = load_library().skiparse_attn_fwd_scopes(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace),
+                                                 int(workspace_bytes), B, heads, N, D, T, H, W, sparse_k, mode,
+                                                 float(rope_theta), int(scope_first), int(scope_step),
+                                                 _stream(stream))
+    _check(st, "skiparse_attn_fwd_scopes")
+
+
+def skiparse_attn_bwd_scopes(q, k, v, out, lse, dout, dq, dk, dv, workspace, T, H, W, sparse_k, mode, scope_first,
+                             scope_step, rope_theta=10000.0, stream=None, workspace_bytes=None):
+    """Backward over the scopes scope_first, scope_first + scope_step, ... only;
+    the other rows of dq, dk and dv are left untouched."""
+    B, heads, N, D = _shape(q)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = load_library().skiparse_attn_bwd_scopes(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes),
+                                                 B, heads, N, D, T, H, W, sparse_k, mode, float(rope_theta),
+                                                 int(scope_first), int(scope_step), _stream(stream))
+    _check(st, "skiparse_attn_bwd_scopes")
+
+
+def scope_shard(sparse_k, world, rank):
+    """(scope_first, scope_step) of one rank when `world` ranks split the scopes
+    round-robin: rank r computes the scopes s = r mod world. Ranks beyond
+    sparse_k get none (scope_first >= sparse_k: their calls are no-ops)."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("rank must lie in [0, world)")
+    return rank, world
 
 
 def skiparse_attn_bwd_saved(fwd_workspace, v, out, lse, dout, dq, dk, dv, workspace, T, H, W, sparse_k, mode,

@@ -64,8 +64,8 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 __device__ __forceinline__ void decode_unit_bwd(const Geom& g, int u, int& b, int& head, int& s, int& tile) {
   tile = u % g.n_tiles;
   int r = u / g.n_tiles;
-  s = r % g.k;
-  r /= g.k;
+  s = g.s0 + (r % g.ks) * g.sstep;               // the ks scopes of this call
+  r /= g.ks;
   head = r % g.heads;
   b = r / g.heads;
 }

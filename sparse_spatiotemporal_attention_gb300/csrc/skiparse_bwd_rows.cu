@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
       if (row >= rows) continue;
       int b, i, head;
       row_coords(g, (int)row, b, i, head);
+      int s, pp;
+      scope_pos_of(g, i, s, pp);
+      if (!in_subset(g, s)) continue;                // only the scopes this call computes
       float dsum = 0.f;
 #pragma unroll
       for (int e = 0; e < PPL; ++e) {
@@ -108,8 +111,6 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
         st_slice<PPL>(p.qr + base, qo);
         st_slice<PPL>(p.kr + base, ko);
       }
-      int s, pp;
-      scope_pos_of(g, i, s, pp);
       const size_t idx = (((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp;   // scope-order row
       float* acc = p.dq_acc + idx * D + lane * 2 * PPL;
       if (PPL == 2) *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pack_kernel(const __
     const int pos = sbp - sb * g.Lp;
     const int s = fdiv(sb, g.fB);
     const int b = sb - s * g.B;
+    if (!in_subset(g, s)) continue;                  // only the scopes this call computes
     const bool inside = pos < scope_len(g, s);
     uint32_t qv[PPL], kv[PPL], vv[PPL], ov[PPL], dv[PPL];
 #pragma unroll
@@ -227,15 +229,19 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __
   for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += R * stride) {
     float x[R][2 * PPL];
     int tt[R], th[R], tw[R];
+    bool skip[R];
 #pragma unroll
     for (int u = 0; u < R; ++u) {
       const long long row = r0 + u * stride;
-      if (row >= rows) continue;
+      skip[u] = row >= rows;
+      if (skip[u]) continue;
       int b, i, head;
       row_coords(g, (int)row, b, i, head);
-      token_coords(p.rope, i, tt[u], th[u], tw[u]);
       int s, pp;
       scope_pos_of(g, i, s, pp);
+      skip[u] = !in_subset(g, s);                    // dq rows of other scopes stay untouched
+      if (skip[u]) continue;
+      token_coords(p.rope, i, tt[u], th[u], tw[u]);
       const float* acc = p.dq_acc + ((((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp) * D + lane * 2 * PPL;
       if (PPL == 2) {
         const float4 a = *reinterpret_cast<const float4*>(acc);
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __
 #pragma unroll
     for (int u = 0; u < R; ++u) {
       const long long row = r0 + u * stride;
-      if (row >= rows) continue;
+      if (skip[u]) continue;
       uint32_t o[PPL];
 #pragma unroll
       for (int e = 0; e < PPL; ++e) {

@@ -66,6 +66,7 @@ struct Geom {
   int Qb, Rb;   // N = Qb * k * G + Rb: whole blocks of k groups, and the tokens left over
   FastDiv fLp;  // division by Lp (scope-ordered row -> (scope, batch), position)
   FastDiv fB;   // division by B
+  int s0, sstep, ks;   // the scopes computed: s0, s0 + sstep, ... below k, ks of them (all k by default)
   FastDiv fk;   // division by k
   FastDiv fkG;  // division by k * G
   FastDiv fheads;  // division by heads (row index -> (b * N + token, head))
@@ -99,6 +100,11 @@ __host__ __device__ __forceinline__ int scope_len(const Geom& g, int s) {
   return g.Qb * g.G + (extra < 0 ? 0 : (extra > g.G ? g.G : extra));
 }
 __host__ __device__ __forceinline__ int scope_tiles(const Geom& g, int s) { return (scope_len(g, s) + 127) >> 7; }
+
+// Whether scope s is among the scopes this call computes (s0 + j * sstep).
+__device__ __forceinline__ bool in_subset(const Geom& g, int s) {
+  return s >= g.s0 && (g.sstep == 1 || (s - g.s0) % g.sstep == 0);
+}
 
 __device__ __forceinline__ int token_of(const Geom& g, int s, int p) {
   return ((p >> g.lgG) * g.k << g.lgG) + (s << g.lgG) + (p & (g.G - 1));

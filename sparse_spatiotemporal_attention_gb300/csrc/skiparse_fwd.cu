@@ -92,8 +92,8 @@ __device__ __forceinline__ float softmax_p_bf16(const float (&x)[kTile], uint32_
 __device__ __forceinline__ void decode_unit(const Geom& g, int n_pairs, int u, int& b, int& head, int& s, int& pair) {
   pair = u % n_pairs;
   int r = u / n_pairs;
-  s = r % g.k;
-  r /= g.k;
+  s = g.s0 + (r % g.ks) * g.sstep;               // the ks scopes of this call
+  r /= g.ks;
   head = r % g.heads;
   b = r / g.heads;
 }
@@ -120,12 +120,20 @@ __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_rope_kernel(const _
   for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += 2 * stride) {
     uint32_t qv[2][PPL], kv[2][PPL];
     int tt[2], th[2], tw[2];
+    bool skip[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const long long row = r0 + u * stride;
-      if (row >= rows) continue;
+      skip[u] = row >= rows;
+      if (skip[u]) continue;
       int b, i, head;
       row_coords(g, (int)row, b, i, head);
+      if (g.ks < g.k) {                              // only the rows of the scopes this call computes
+        int s, pos;
+        scope_pos_of(g, i, s, pos);
+        skip[u] = !in_subset(g, s);
+        if (skip[u]) continue;
+      }
       token_coords(p.rope, i, tt[u], th[u], tw[u]);
       const size_t base = (size_t)row * D + lane * 2 * PPL;
       if (PPL == 2) {
@@ -140,7 +148,7 @@ __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_rope_kernel(const _
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const long long row = r0 + u * stride;
-      if (row >= rows) continue;
+      if (skip[u]) continue;
       uint32_t qo[PPL], ko[PPL];
 #pragma unroll
       for (int e = 0; e < PPL; ++e) {
@@ -186,18 +194,21 @@ __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_pack_kernel(const _
   for (long long r0 = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); r0 < rows; r0 += 2 * stride) {
     uint32_t qv[2][PPL], kv[2][PPL], vv[2][PPL];
     int tok[2];
+    bool skip[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       tok[u] = -1;
       const long long row = r0 + u * stride;
-      if (row >= rows) continue;
+      skip[u] = row >= rows;
+      if (skip[u]) continue;
       const int sbp = fdiv((int)row, g.fheads);              // (s * B + b) * Lp + pos
       const int head = (int)row - sbp * g.heads;
       const int sb = fdiv(sbp, g.fLp);
       const int pos = sbp - sb * g.Lp;
       const int s = fdiv(sb, g.fB);
       const int b = sb - s * g.B;
-      if (pos >= scope_len(g, s)) continue;
+      skip[u] = !in_subset(g, s);                    // the other scopes' rows are never read
+      if (skip[u] || pos >= scope_len(g, s)) continue;
       tok[u] = token_of(g, s, pos);
       const size_t src = (((size_t)b * g.N + tok[u]) * g.heads + head) * D + lane * 2 * PPL;
 #pragma unroll
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_pack_kernel(const _
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const long long row = r0 + u * stride;
-      if (row >= rows) continue;
+      if (skip[u]) continue;
       uint32_t qo[PPL], ko[PPL], vo[PPL];
 #pragma unroll
       for (int e = 0; e < PPL; ++e) qo[e] = ko[e] = vo[e] = 0u;
@@ -573,7 +584,7 @@ size_t fwd_smem_bytes(int D) { return D == 128 ? FwdLayout<128>::BYTES : FwdLayo
 
 size_t fwd_rope_smem_bytes(int rope_entries) { return (size_t)rope_entries * sizeof(float2); }
 
-int fwd_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 2); }
+int fwd_units(const Geom& g) { return g.B * g.heads * g.ks * ((g.n_tiles + 1) / 2); }
 
 cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t stream) {
   const size_t smem = fwd_rope_smem_bytes(p.rope.entries);

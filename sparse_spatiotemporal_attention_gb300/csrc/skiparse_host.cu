@@ -236,7 +236,19 @@ Geom make_geom(const Shape& s) {
   // scopes of unequal length are read from scope-ordered copies: the gather
   // maps' per-dimension bounds cannot stop a read past the end of a shorter scope
   g.packed = g.Rb != 0 ? 1 : 0;
+  g.s0 = 0;
+  g.sstep = 1;
+  g.ks = s.k;
   return g;
+}
+
+// Restricts a geometry to the scopes first, first + step, ... below k.
+int set_subset(Geom& g, int first, int step) {
+  if (first < 0 || step < 1) return SKIPARSE_ERR_INVALID_ARG;
+  g.s0 = first;
+  g.sstep = step;
+  g.ks = first < g.k ? (g.k - 1 - first) / step + 1 : 0;
+  return SKIPARSE_OK;
 }
 
 RopeParams make_rope(const Shape& s, float theta) {
@@ -456,13 +468,20 @@ size_t skiparse_attn_fwd_workspace_bytes(int B, int heads, int N, int D, int T, 
   return fwd_ws_bytes(s);
 }
 
-int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
-                      void* workspace, size_t workspace_bytes,
-                      int B, int heads, int N, int D, int T, int H, int W,
-                      int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Forward over the scopes first, first + step, ... (all of them for 0, 1).
+int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, void* workspace,
+             size_t workspace_bytes, int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode,
+             float rope_theta, int scope_first, int scope_step, cudaStream_t stream) {
   Shape s;
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
+  Geom geom = make_geom(s);
+  if ((st = set_subset(geom, scope_first, scope_step)) != SKIPARSE_OK) return st;
+  if (geom.ks == 0) return SKIPARSE_OK;
   if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
   const size_t need = fwd_ws_bytes(s);
@@ -477,7 +496,7 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
 
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
-  p.g = make_geom(s);
+  p.g = geom;
   p.rope = make_rope(s, rope_theta);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.q = static_cast<const uint16_t*>(q);
@@ -519,6 +538,27 @@ int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, fl
     if (st != SKIPARSE_OK) return st;
   }
   return launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));
+}
+
+}  // namespace
+
+extern "C" {
+
+int skiparse_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes,
+                      int B, int heads, int N, int D, int T, int H, int W,
+                      int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+  return fwd_impl(q, k, v, out, lse, workspace, workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode, rope_theta,
+                  0, 1, stream);
+}
+
+int skiparse_attn_fwd_scopes(const void* q, const void* k, const void* v, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes,
+                             int B, int heads, int N, int D, int T, int H, int W,
+                             int sparse_k, int mode, float rope_theta, int scope_first, int scope_step,
+                             cudaStream_t stream) {
+  return fwd_impl(q, k, v, out, lse, workspace, workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode, rope_theta,
+                  scope_first, scope_step, stream);
 }
 
 size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k,
@@ -637,16 +677,18 @@ namespace {
 int bwd_impl(const void* q, const void* k, const void* fwd_ws, size_t fwd_ws_given,
              const void* v, const void* out, const float* lse, const void* dout, void* dq, void* dk, void* dv,
              void* workspace, size_t workspace_bytes, int B, int heads, int N, int D, int T, int H, int W,
-             int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
+             int sparse_k, int mode, float rope_theta, int scope_first, int scope_step, cudaStream_t stream) {
   Shape s;
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
+  Geom geom = make_geom(s);
+  if ((st = set_subset(geom, scope_first, scope_step)) != SKIPARSE_OK) return st;
+  if (geom.ks == 0) return SKIPARSE_OK;
   const bool saved = fwd_ws != nullptr;
   const bool rotate = rope_theta != 0.0f;            // 0: q and k are already rotated
   if (saved && !rotate) return SKIPARSE_ERR_INVALID_ARG;   // the forward wrote no rotated copies
   if (!v || !out || !lse || !dout || !dq || !dk || !dv) return SKIPARSE_ERR_INVALID_ARG;
   if (!saved && (!q || !k)) return SKIPARSE_ERR_INVALID_ARG;
-  const Geom geom = make_geom(s);
   const size_t tb = (size_t)s.elems * 2, lb = (size_t)B * heads * N * 4;
   const size_t fwd_need = fwd_ws_bytes(s);
   const uint8_t* fw = static_cast<const uint8_t*>(fwd_ws);
@@ -691,7 +733,7 @@ int bwd_impl(const void* q, const void* k, const void* fwd_ws, size_t fwd_ws_giv
   p.dv = static_cast<uint16_t*>(dv);
   p.err = dev.err_word;
   p.Lp = w.Lp;
-  p.n_units = B * heads * sparse_k * p.g.n_tiles;
+  p.n_units = B * heads * p.g.ks * p.g.n_tiles;
   p.scale = (float)(1.0 / std::sqrt((double)D));
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   bool maps_ok;
@@ -738,7 +780,16 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       int B, int heads, int N, int D, int T, int H, int W,
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
   return bwd_impl(q, k, nullptr, 0, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, heads, N, D, T, H,
-                  W, sparse_k, mode, rope_theta, stream);
+                  W, sparse_k, mode, rope_theta, 0, 1, stream);
+}
+
+int skiparse_attn_bwd_scopes(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                             const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int B, int heads, int N, int D, int T, int H, int W,
+                             int sparse_k, int mode, float rope_theta, int scope_first, int scope_step,
+                             cudaStream_t stream) {
+  return bwd_impl(q, k, nullptr, 0, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, heads, N, D, T, H,
+                  W, sparse_k, mode, rope_theta, scope_first, scope_step, stream);
 }
 
 int skiparse_attn_bwd_saved(const void* fwd_workspace, size_t fwd_workspace_bytes, const void* v, const void* out,
@@ -753,7 +804,7 @@ int skiparse_attn_bwd_saved(const void* fwd_workspace, size_t fwd_workspace_byte
   // the forward workspace holds rotated q, then rotated k (and, for scopes of
   // unequal length, v), each 256-byte aligned
   return bwd_impl(nullptr, nullptr, fwd_workspace, fwd_workspace_bytes, v, out, lse, dout, dq, dk, dv, workspace,
-                  workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, stream);
+                  workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, 0, 1, stream);
 }
 
 int skiparse_debug_index_map(int* scope_of_token, int* pos_of_token, int N, int sparse_k, int mode,

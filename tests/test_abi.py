@@ -156,6 +156,41 @@ def test_ragged_workspace_sizes(lib):
                                      10000.0, None) == SHAPE
 
 
+def test_scope_subset_validation(lib):
+    """The scope-subset calls validate like the full ones, then their subset."""
+    def fwd_s(first, step, N=256, T=4):
+        return lib.skiparse_attn_fwd_scopes(A, 2 * A, 3 * A, 4 * A, 5 * A, 8 * A, FWD_WS, 1, 2, N, 64, T, 8, 8, 2, 0,
+                                            10000.0, first, step, None)
+    assert fwd_s(0, 1) == DEVICE
+    assert fwd_s(1, 2) == DEVICE
+    assert fwd_s(-1, 2) == INVALID
+    assert fwd_s(0, 0) == INVALID
+    assert fwd_s(2, 2) == OK                      # no scope >= k: nothing to do
+    assert fwd_s(0, 1, N=255) == SHAPE
+    ws = lib.skiparse_attn_bwd_workspace_bytes(1, 2, 256, 64, 4, 8, 8, 2, 0)
+
+    def bwd_s(first, step, ws_bytes=ws):
+        return lib.skiparse_attn_bwd_scopes(A, 2 * A, 3 * A, 4 * A, 5 * A, 6 * A, 7 * A, 8 * A, 9 * A, 10 * A,
+                                            ws_bytes, 1, 2, 256, 64, 4, 8, 8, 2, 0, 10000.0, first, step, None)
+    assert bwd_s(0, 2) == DEVICE
+    assert bwd_s(0, 0) == INVALID
+    assert bwd_s(5, 1) == OK
+    assert bwd_s(0, 2, ws_bytes=ws - 1) == WORKSPACE
+
+
+def test_scope_shard_partition():
+    """Round-robin shards of the scopes over ranks are disjoint and cover them."""
+    for k in (1, 2, 3, 4, 8):
+        for world in (1, 2, 3, 4, 8):
+            seen = []
+            for r in range(world):
+                first, step = skp.scope_shard(k, world, r)
+                seen += list(range(first, k, step))
+            assert sorted(seen) == list(range(k))
+    with pytest.raises(ValueError):
+        skp.scope_shard(4, 2, 2)
+
+
 def test_debug_hook_validation(lib):
     assert lib.skiparse_debug_index_map(A, 2 * A, 16, 3, 0, None) == DEVICE     # any N: unequal scopes
     assert lib.skiparse_debug_index_map(A, 2 * A, 16, 2, 2, None) == INVALID

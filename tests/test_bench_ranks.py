@@ -80,3 +80,56 @@ def test_reference_arm_only_on_rank0(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     bench.reference_arm(argparse.Namespace(steps=1, warmup=0))
     assert capsys.readouterr().out == ""
+
+
+def _shard_worker(rank, world, port, out_dir):
+    """One rank of a scope-sharded step, with the oracle standing in for the GPU
+    calls: the rank computes its round-robin scopes and writes only their rows;
+    the ranks' rows are then gathered (no exchange is needed by the method;
+    this only checks the partition and the assembled result)."""
+    sys.path.insert(0, ROOT)
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import sparse_spatiotemporal_attention_gb300 as skp
+    from oracle import skiparse_oracle as O
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        B, heads, D, T, H, W, k, mode = 1, 2, 16, 2, 5, 7, 3, O.GROUP       # N = 70: unequal scopes
+        N = T * H * W
+        rs = np.random.default_rng(5)
+        q, kk, v, do = (rs.standard_normal((B, N, heads, D)) for _ in range(4))
+        first, step = skp.scope_shard(k, world, rank)
+        out = np.zeros((B, N, heads, D))
+        owner = np.zeros(N)
+        for s in range(first, k, step):
+            for h in range(heads):
+                r = O.skiparse_scope(q, kk, v, do, T, H, W, k, mode, 0, h, s)
+                out[0, r["tokens"], h] = r["dq"]
+            owner[O.scope_tokens(N, k, mode, s)] += 1
+        t_out, t_own = torch.from_numpy(out), torch.from_numpy(owner)
+        dist.all_reduce(t_out)
+        dist.all_reduce(t_own)
+        dq, _, _, _, _ = O.skiparse_bwd(q, kk, v, do, T, H, W, k, mode)
+        res = {"covered_once": bool((t_own == 1).all()), "err": float(np.abs(t_out.numpy() - dq).max()),
+               "mine": list(range(first, k, step))}
+        with open(os.path.join(out_dir, f"shard{rank}.json"), "w") as f:
+            json.dump(res, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_scope_shards(tmp_path):
+    """Two ranks split the scopes of one batch round-robin: every token's rows
+    come from exactly one rank and the gathered gradients equal the whole
+    backward's."""
+    import torch.multiprocessing as mp
+    port = _free_port()
+    mp.start_processes(_shard_worker, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
+    res = [json.load(open(tmp_path / f"shard{r}.json")) for r in range(2)]
+    assert res[0]["mine"] == [0, 2] and res[1]["mine"] == [1]
+    for d in res:
+        assert d["covered_once"]
+        assert d["err"] < 1e-12
