@@ -70,7 +70,7 @@ FWD_CONFIGS = [
 ]
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / bf16 tensor-rate ratio (4.5 / 2.25 PFLOP/s)
 # x forward FLOPs, per launch, by kernel id
-KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0, 4: 0.0, 5: 0.0, 6: 0.0, 7: 1.0, 8: 0.0, 9: 0.0, 10: 1.0}
+KERNEL_FLOP_FACTOR = {0: 1.0, 1: 0.0, 2: 2.5, 3: 0.0, 4: 0.0, 5: 0.0, 6: 0.0, 7: 1.0, 8: 0.0, 9: 0.0, 10: 1.0, 11: 0.0}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -281,26 +281,32 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10, with_k1=True):
         fws = torch.empty(skp.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, 1, c["mode"]),
                           dtype=torch.uint8, device=dev)
 
-        def timed(kk):
+        def timed(kk, per_kernel=None):
             for _ in range(3):
                 skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, c["mode"], stream=stream,
                                       workspace=fws)
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            skp.skiparse_trace_begin()
             e0.record(stream)
             for _ in range(launches):
                 skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, c["mode"], stream=stream,
                                       workspace=fws)
             e1.record(stream)
             torch.cuda.synchronize()
+            kms, kcnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
+            if per_kernel is not None:
+                per_kernel.update({skp.KERNEL_NAMES[i]: kms[i] / kcnt[i] for i in range(len(kcnt)) if kcnt[i]})
             return e0.elapsed_time(e1) / launches
 
-        ms = timed(c["k"])
+        kern = {}
+        ms = timed(c["k"], kern)
         tf = fwd_flops(c) / (ms * 1e-3) / 1e12
         line = {"workload": c["name"], "pass": "fwd", "mode": "group" if c["mode"] else "single", "B": B,
                 "heads": heads, "D": D, "grid": f"{T}x{H}x{W}", "N": N, "sparse_k": c["k"], "ms_per_launch": ms,
                 "tflops": tf, "pct_of_peak": {"burst": tf / burst, "sustained": tf / sustained},
-                "gbs": fwd_bytes(c) / (ms * 1e-3) / 1e9, "pct_of_hbm": fwd_bytes(c) / (ms * 1e-3) / 1e9 / hbm}
+                "gbs": fwd_bytes(c) / (ms * 1e-3) / 1e9, "pct_of_hbm": fwd_bytes(c) / (ms * 1e-3) / 1e9 / hbm,
+                "kernels": kern}
         # the two 8-bit forwards on the same inputs (own workspaces; all of their kernels timed)
         for key, call in (("fp8", "skiparse_attn_fwd_fp8"), ("mixed8", "skiparse_attn_fwd_mixed8")):
             fn = getattr(skp, call)

@@ -50,7 +50,7 @@ typedef enum { SKIPARSE_SINGLE = 0, SKIPARSE_GROUP = 1 } skiparse_mode_t;
 typedef enum {
   SKIPARSE_OK = 0,
   SKIPARSE_ERR_INVALID_ARG = -1,    /* NULL pointer, negative size, bad mode or theta */
-  SKIPARSE_ERR_SHAPE = -2,          /* N != T*H*W, N % k (single) or N % k^2 (group) */
+  SKIPARSE_ERR_SHAPE = -2,          /* N != T*H*W; for the 8-bit forwards also N % k (single) or N % k^2 (group) */
   SKIPARSE_ERR_UNSUPPORTED = -3,    /* D not 64/128, group k not dividing 128, RoPE table too large,
                                        B * N * heads >= 2^31 */
   SKIPARSE_ERR_ALIGNMENT = -4,      /* a pointer not 16-byte aligned */
@@ -63,7 +63,12 @@ typedef enum {
 
 /*
  * Bytes of device workspace skiparse_attn_fwd needs for these sizes: rotated
- * bf16 copies of q and k (2 * B*N*heads*D*2 bytes, each rounded up to 256).
+ * bf16 copies of q and k (2 * B*N*heads*D*2 bytes, each rounded up to 256), or,
+ * when k (single) or k*k (group) does not divide N, scope-ordered copies of q,
+ * k and v (3 * k*B*Lp*heads*D*2 bytes, Lp the longest scope rounded up to a
+ * multiple of 128); then room for the partial results of the units the last
+ * round of the attention kernel splits over key ranges (160 slots of 256 rows
+ * x (D fp32 + 8 bytes): 21 MB for D = 128), and the RoPE cos/sin table (64 KB).
  * Returns 0 for empty or invalid sizes.
  */
 size_t skiparse_attn_fwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
@@ -73,16 +78,24 @@ size_t skiparse_attn_fwd_workspace_bytes(int B, int heads, int N, int D, int T, 
  * Forward pass. Page: "Open-Sora Plan" docs, "Skiparse Attention", both
  * implementation listings (RoPE, rearrange, scaled_dot_product_attention,
  * reverse rearrange): a RoPE kernel that rotates q and k once into the
- * workspace, then one persistent attention kernel over the scopes.
+ * workspace, then one persistent attention kernel over the scopes; when its
+ * last round of units would leave most SMs idle, those units are split over
+ * key ranges and a merge kernel combines their partial results (row max and
+ * sum in base 2). Any N = T*H*W: where k (single skip) or k*k (group skip)
+ * does not divide N, the section's prose defines the scopes (single: i mod k;
+ * group: (i div k) mod k, the last group holding N mod k tokens), which then
+ * differ in length by at most one token or one group; q, k and v are then
+ * gathered into scope order first.
  *   q, k, v   in : bf16 (B, N, heads, D), the PRE-RoPE projections.
  *   out       out: bf16 (B, N, heads, D), fully overwritten.
  *   lse       out: fp32 (B, heads, N), natural-log LSE of each query row.
  *   workspace scratch: device memory of at least
  *             skiparse_attn_fwd_workspace_bytes(...) bytes, 256-byte aligned,
  *             owned by the caller, contents ignored on entry; on return it
- *             holds the rotated q and k (row layout of q); with rope_theta = 0
- *             it is not written (the kernel gathers q and k directly and the
- *             RoPE pass is skipped). Must not overlap
+ *             holds the rotated q and k (row layout of q; scope order for
+ *             unequal scopes, with v); with rope_theta = 0 and equal scopes
+ *             they are not written (the kernel gathers q and k directly and
+ *             the RoPE pass is skipped). Must not overlap
  *             any tensor. SKIPARSE_ERR_WORKSPACE when NULL or too small.
  *   D in {64, 128}; sparse_k >= 1; mode is a skiparse_mode_t; rope_theta >= 0.
  *   Group mode needs sparse_k to divide 128.
@@ -134,7 +147,8 @@ int skiparse_attn_bwd_scopes(const void* q, const void* k, const void* v, const 
  * its own workspace (..._workspace_bytes(...) bytes, 256-byte aligned, owned
  * by the caller, contents undefined on return); SKIPARSE_ERR_UNSUPPORTED for
  * D != 128 and, as for every entry point, a RoPE table over 8192 pairs
- * (16 T + 24 (H + W) for D = 128). The outputs approximate the bf16 forward
+ * (16 T + 24 (H + W) for D = 128); SKIPARSE_ERR_SHAPE when k (single) or k*k
+ * (group) does not divide N (their workspace size is then 0). The outputs approximate the bf16 forward
  * to the accuracy of 8-bit operands (a few percent relative).
  */
 size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
@@ -187,7 +201,9 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
  *                           forward writes no rotated copies and this call
  *                           returns SKIPARSE_ERR_INVALID_ARG), unchanged since;
  *                           fwd_workspace_bytes at least
- *                           skiparse_attn_fwd_workspace_bytes(...); read only.
+ *                           skiparse_attn_fwd_workspace_bytes(...); read only
+ *                           (its rotated q and k, or scope-ordered q, k and v,
+ *                           and its cos/sin table).
  *   v, out, lse, dout  in : as for skiparse_attn_bwd.
  *   dq, dk, dv         out: as for skiparse_attn_bwd (gradients w.r.t. the
  *                           pre-RoPE q, k and v of the forward call).

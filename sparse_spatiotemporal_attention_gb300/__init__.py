@@ -19,7 +19,7 @@ GROUP = 1
 KERNEL_NAMES = ("skiparse_fwd_kernel", "skiparse_bwd_pre_kernel", "skiparse_bwd_main_kernel",
                 "skiparse_bwd_post_kernel", "skiparse_fwd_rope_kernel", "skiparse_fwd8_vmax_kernel",
                 "skiparse_fwd8_prep_kernel", "skiparse_fwd8_kernel", "skiparse_qkv_rope_kernel",
-                "skiparse_fwdm8_prep_kernel", "skiparse_fwdm8_kernel")
+                "skiparse_fwdm8_prep_kernel", "skiparse_fwdm8_kernel", "skiparse_fwd_merge_kernel")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libskiparse.so")

@@ -125,10 +125,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
         if (kt >= nt) continue;                       // a shorter scope has fewer key tiles
         if (it > 0 && !mbar_wait(bar(B_KVEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_BWD + B_KVEMPTY)) break;
         mbar_expect_tx(bar(B_KVFULL), 2 * Ly::TILE);
+        const TileCoord tck = scope_tile(g, s, b, kt * kTile);
 #pragma unroll
         for (int h = 0; h < Ly::HALVES; ++h) {
-          load_scope_tile(sK + h * kHalfBytes, &p.tm_k, bar(B_KVFULL), g, h * 64, head, s, b, kt * kTile);
-          load_scope_tile(sV + h * kHalfBytes, &p.tm_v, bar(B_KVFULL), g, h * 64, head, s, b, kt * kTile);
+          load_tile(sK + h * kHalfBytes, &p.tm_k, bar(B_KVFULL), tck, h * 64, head);
+          load_tile(sV + h * kHalfBytes, &p.tm_v, bar(B_KVFULL), tck, h * 64, head);
         }
         ++kv_issued;
         const size_t srow = (((size_t)b * g.heads + head) * g.k + s) * p.Lp;
@@ -138,12 +139,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const
           const uint32_t n = gg >> 1;
           if (n > 0 && !mbar_wait(bar(B_QEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_BWD + B_QEMPTY0 + st)) { ok = false; break; }
           mbar_expect_tx(bar(B_QFULL0 + st), 2 * Ly::TILE + 1024);
+          const TileCoord tci = scope_tile(g, s, b, i * kTile);
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h) {
-            load_scope_tile(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(B_QFULL0 + st), g, h * 64, head, s, b,
-                            i * kTile);
-            load_scope_tile(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(B_QFULL0 + st), g, h * 64, head, s, b,
-                            i * kTile);
+            load_tile(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(B_QFULL0 + st), tci, h * 64, head);
+            load_tile(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(B_QFULL0 + st), tci, h * 64, head);
           }
           const uint32_t dst = smem_u32(stats + st * 256);
           bulk_load(dst, p.lse2s + srow + i * kTile, 512, bar(B_QFULL0 + st));
@@ -472,10 +472,11 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
       if (it > 0 && !warp_wait(T_KVEMPTY, (it - 1) & 1)) break;
       if (leader) {
         mbar_expect_tx(bar(T_KVFULL), 2 * Ly::TILE);
+        const TileCoord tck = scope_tile(g, s, b, kt * kTile);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          load_scope_tile(sK + h * kHalfBytes, &p.tm_k, bar(T_KVFULL), g, h * 64, head, s, b, kt * kTile);
-          load_scope_tile(sV + h * kHalfBytes, &p.tm_v, bar(T_KVFULL), g, h * 64, head, s, b, kt * kTile);
+          load_tile(sK + h * kHalfBytes, &p.tm_k, bar(T_KVFULL), tck, h * 64, head);
+          load_tile(sV + h * kHalfBytes, &p.tm_v, bar(T_KVFULL), tck, h * 64, head);
         }
       }
       __syncwarp();
@@ -486,6 +487,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         const int st = gg & 1;
         const uint32_t n = gg >> 1;
         const int qi = stagger(i, kt, nt);
+        const TileCoord tcq = scope_tile(g, s, b, qi * kTile);   // before the slot waits
         // a slot is refilled once the dQ~ staging of tile gg-2 placed in it has been read out
         if (n > 0 && !warp_wait(T_QFREE0 + st, (n - 1) & 1)) {
           ok = false;
@@ -495,8 +497,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
           mbar_expect_tx(bar(T_QFULL0 + st), Ly::TILE + 1024);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            load_scope_tile(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(T_QFULL0 + st), g, h * 64, head, s, b,
-                            qi * kTile);
+            load_tile(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(T_QFULL0 + st), tcq, h * 64, head);
           const uint32_t dst = smem_u32(stats + st * 256);
           bulk_load(dst, p.lse2s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
           bulk_load(dst + 512, p.delta_s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
@@ -510,8 +511,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
           mbar_expect_tx(bar(T_OFULL0 + st), Ly::TILE);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            load_scope_tile(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(T_OFULL0 + st), g, h * 64, head, s,
-                            b, qi * kTile);
+            load_tile(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(T_OFULL0 + st), tcq, h * 64, head);
         }
         __syncwarp();
         ++q_issued[st];

@@ -40,17 +40,16 @@ __device__ __forceinline__ void st_slice(uint16_t* dst, const uint32_t (&v)[PPL]
 // also rotated bf16 copies of q and k (without it the forward pass's copies are
 // reused). One warp per row, R rows per iteration so each lane has the loads
 // of all R rows in flight before it uses any.
-template <int D, bool ROT>
-__global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
+template <int D, bool ROT, bool SUBSET>
+__global__ void __launch_bounds__(kRowThreads, ROT ? 5 : 8) skiparse_bwd_pre_kernel(const __grid_constant__ BwdParams p) {
   constexpr int R = 2;
   extern __shared__ float2 tab[];
   const Geom& g = p.g;
-  // the table rotates q and k here; without ROT only block 0 builds it, to hand
-  // it to the post kernel
-  if (ROT || blockIdx.x == 0) rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
-  __syncthreads();
-  if (blockIdx.x == 0)
-    for (int e = threadIdx.x; e < p.rope.entries; e += blockDim.x) p.rope_tab[e] = tab[e];
+  // the table (built once per call in the workspace) rotates q and k here
+  if (ROT) {
+    rope_load_table(tab, p.rope_tab, p.rope.entries, threadIdx.x, blockDim.x);
+    __syncthreads();
+  }
   constexpr int PPL = D / 64;               // channel pairs per lane
   const int lane = threadIdx.x & 31;
   const long long wpb = blockDim.x >> 5;
@@ -86,9 +85,11 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
       if (row >= rows) continue;
       int b, i, head;
       row_coords(g, (int)row, b, i, head);
-      int s, pp;
-      scope_pos_of(g, i, s, pp);
-      if (!in_subset(g, s)) continue;                // only the scopes this call computes
+      if (SUBSET) {                                  // only the scopes this call computes
+        int s, pp;
+        scope_pos_of(g, i, s, pp);
+        if (!in_subset(g, s)) continue;
+      }
       float dsum = 0.f;
 #pragma unroll
       for (int e = 0; e < PPL; ++e) {
@@ -111,6 +112,8 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pre_kernel(const __g
         st_slice<PPL>(p.qr + base, qo);
         st_slice<PPL>(p.kr + base, ko);
       }
+      int s, pp;
+      scope_pos_of(g, i, s, pp);
       const size_t idx = (((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp;   // scope-order row
       float* acc = p.dq_acc + idx * D + lane * 2 * PPL;
       if (PPL == 2) *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -136,10 +139,8 @@ template <int D>
 __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pack_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ float2 tab[];
   const Geom& g = p.g;
-  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  rope_load_table(tab, p.rope_tab, p.rope.entries, threadIdx.x, blockDim.x);
   __syncthreads();
-  if (blockIdx.x == 0)
-    for (int e = threadIdx.x; e < p.rope.entries; e += blockDim.x) p.rope_tab[e] = tab[e];
   constexpr int PPL = D / 64;
   const int lane = threadIdx.x & 31;
   const long long wpb = blockDim.x >> 5;
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_pack_kernel(const __
 
 // Post: dq = R^T (scale * dQ~) for each (b, token, head) row, read from the
 // row's scope-order accumulator slot; four rows per warp iteration.
-template <int D>
+template <int D, bool SUBSET>
 __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __grid_constant__ BwdParams p) {
   const Geom& g = p.g;
   constexpr int PPL = D / 64;
@@ -239,8 +240,10 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __
       row_coords(g, (int)row, b, i, head);
       int s, pp;
       scope_pos_of(g, i, s, pp);
-      skip[u] = !in_subset(g, s);                    // dq rows of other scopes stay untouched
-      if (skip[u]) continue;
+      if (SUBSET) {
+        skip[u] = !in_subset(g, s);                  // dq rows of other scopes stay untouched
+        if (skip[u]) continue;
+      }
       token_coords(p.rope, i, tt[u], th[u], tw[u]);
       const float* acc = p.dq_acc + ((((size_t)b * g.heads + head) * g.k + s) * p.Lp + pp) * D + lane * 2 * PPL;
       if (PPL == 2) {
@@ -269,11 +272,11 @@ __global__ void __launch_bounds__(kRowThreads) skiparse_bwd_post_kernel(const __
 
 template <int D, bool ROT>
 static cudaError_t launch_pre_variant(const BwdParams& p, int grid, int sms, size_t smem, cudaStream_t stream) {
-  const cudaError_t e =
-      cudaFuncSetAttribute(skiparse_bwd_pre_kernel<D, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kernel = p.g.ks < p.g.k ? skiparse_bwd_pre_kernel<D, ROT, true> : skiparse_bwd_pre_kernel<D, ROT, false>;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  grid = one_wave(skiparse_bwd_pre_kernel<D, ROT>, grid, kRowThreads, smem, sms);
-  skiparse_bwd_pre_kernel<D, ROT><<<grid, kRowThreads, smem, stream>>>(p);
+  grid = one_wave(kernel, grid, kRowThreads, smem, sms);
+  kernel<<<grid, kRowThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -288,7 +291,7 @@ static cudaError_t launch_pack_variant(const BwdParams& p, int grid, int sms, si
 }
 
 cudaError_t launch_bwd_pre(const BwdParams& p, int grid, int sms, cudaStream_t stream) {
-  const size_t smem = (size_t)p.rope.entries * sizeof(float2);
+  const size_t smem = (p.g.packed || p.rotate_qk) ? (size_t)p.rope.entries * sizeof(float2) : 0;
   if (p.g.packed)
     return p.g.D == 128 ? launch_pack_variant<128>(p, grid, sms, smem, stream)
                         : launch_pack_variant<64>(p, grid, sms, smem, stream);
@@ -300,13 +303,11 @@ cudaError_t launch_bwd_pre(const BwdParams& p, int grid, int sms, cudaStream_t s
 }
 
 cudaError_t launch_bwd_post(const BwdParams& p, int grid, int sms, cudaStream_t stream) {
-  if (p.g.D == 128) {
-    grid = one_wave(skiparse_bwd_post_kernel<128>, grid, kRowThreads, 0, sms);
-    skiparse_bwd_post_kernel<128><<<grid, kRowThreads, 0, stream>>>(p);
-  } else {
-    grid = one_wave(skiparse_bwd_post_kernel<64>, grid, kRowThreads, 0, sms);
-    skiparse_bwd_post_kernel<64><<<grid, kRowThreads, 0, stream>>>(p);
-  }
+  const bool sub = p.g.ks < p.g.k;
+  auto kernel = p.g.D == 128 ? (sub ? skiparse_bwd_post_kernel<128, true> : skiparse_bwd_post_kernel<128, false>)
+                             : (sub ? skiparse_bwd_post_kernel<64, true> : skiparse_bwd_post_kernel<64, false>);
+  grid = one_wave(kernel, grid, kRowThreads, 0, sms);
+  kernel<<<grid, kRowThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

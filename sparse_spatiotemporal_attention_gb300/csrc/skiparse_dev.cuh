@@ -136,20 +136,33 @@ __device__ __forceinline__ float2 rope_cos_sin(int pos, double om) {
   return make_float2(cs, sn);
 }
 
-__device__ __forceinline__ void rope_build_table(float2* tab, const RopeParams& r, int tid, int nthreads) {
+// Entry e of the table: (cos, sin) of position pos times omega_j for one axis.
+__host__ __device__ __forceinline__ void rope_entry_args(const RopeParams& r, int e, int& pos, double& om) {
   const int nt = r.T * r.dt2, nh = r.H * r.dh2;
+  int j;
+  if (e < nt) {
+    pos = e / r.dt2; j = e - pos * r.dt2; om = r.om_t[j];
+  } else if (e < nt + nh) {
+    const int e2 = e - nt; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j];
+  } else {
+    const int e2 = e - nt - nh; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j];
+  }
+}
+
+__device__ __forceinline__ void rope_build_table(float2* tab, const RopeParams& r, int tid, int nthreads) {
   for (int e = tid; e < r.entries; e += nthreads) {
-    int pos, j;
+    int pos;
     double om;
-    if (e < nt) {
-      pos = e / r.dt2; j = e - pos * r.dt2; om = r.om_t[j];
-    } else if (e < nt + nh) {
-      const int e2 = e - nt; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j];
-    } else {
-      const int e2 = e - nt - nh; pos = e2 / r.dh2; j = e2 - pos * r.dh2; om = r.om_hw[j];
-    }
+    rope_entry_args(r, e, pos, om);
     tab[e] = rope_cos_sin(pos, om);
   }
+}
+
+// Shared-memory copy of a table built once per call in global memory
+// (skiparse_rope_table_kernel), instead of each CTA rebuilding it: the angle
+// reduction runs on the FP64 pipe, which a wave of CTAs would otherwise share.
+__device__ __forceinline__ void rope_load_table(float2* tab, const float2* gtab, int entries, int tid, int nthreads) {
+  for (int e = tid; e < entries; e += nthreads) tab[e] = __ldg(gtab + e);
 }
 
 // Which table slice a channel pair pp (0 .. D/2-1) reads from.
@@ -360,15 +373,31 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, 
 }
 
 // One 128-position tile of a scope: positions p0 .. p0 + 127 of scope s, batch
-// b, channels c0 .. c0 + 63 of `head` (one 128-row box, 128-byte swizzle).
-// Unpacked: through the 5-D scope-gather map over the caller's (B, N, heads, D)
-// tensor (dims channel, head, in-group offset, scope, merged (batch, group)).
-// Packed: from the scope-ordered copy (k, B, Lp, heads, D) through a 3-D map
-// (channel, head, row), rows past a scope's end holding zeros.
-__device__ __forceinline__ void load_scope_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, const Geom& g,
-                                                int c0, int head, int s, int b, int p0) {
-  if (g.packed) tma_load_3d(dst, m, bar, c0, head, (s * g.B + b) * g.Lp + p0);
-  else tma_load_5d(dst, m, bar, c0, head, 0, s, b * g.Nn + p0 / g.G);
+// b (one 128-row box per 64 channels of a head, 128-byte swizzle). Unpacked:
+// through the 5-D scope-gather map over the caller's (B, N, heads, D) tensor
+// (dims channel, head, in-group offset, scope, merged (batch, group));
+// packed: from the scope-ordered copy (k, B, Lp, heads, D) through a 3-D map
+// (channel, head, row), rows past a scope's end holding zeros. The coordinate
+// is formed once per tile (its loads sit on the producers' critical path).
+struct TileCoord {
+  int s;      // scope coordinate of the 5-D map, or -1 for the packed 3-D map
+  int row;
+};
+__device__ __forceinline__ TileCoord scope_tile(const Geom& g, int s, int b, int p0) {
+  TileCoord c;
+  if (g.packed) {
+    c.s = -1;
+    c.row = (s * g.B + b) * g.Lp + p0;
+  } else {
+    c.s = s;
+    c.row = b * g.Nn + (p0 >> g.lgG);
+  }
+  return c;
+}
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* m, uint32_t bar, TileCoord c, int c0,
+                                          int head) {
+  if (c.s < 0) tma_load_3d(dst, m, bar, c0, head, c.row);
+  else tma_load_5d(dst, m, bar, c0, head, 0, c.s, c.row);
 }
 
 // Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).

@@ -98,16 +98,63 @@ __device__ __forceinline__ void decode_unit(const Geom& g, int n_pairs, int u, i
   b = r / g.heads;
 }
 
+// Work item `it`: a whole unit, or one key-tile range [j0, j1) of a unit of the
+// last round, split so that its pieces run on the SMs the round leaves idle
+// (slot >= 0 indexes the piece's partial results). False when the item has no
+// work: a Q-tile pair past a shorter scope's end, or an empty key range.
+struct Item {
+  int b, head, s, pair, nt, j0, j1, slot;
+};
+
+__device__ __forceinline__ bool decode_item(const FwdParams& p, int n_pairs, int it, Item& w) {
+  int u = it, piece = 0;
+  w.slot = -1;
+  if (it >= p.n_full) {
+    const int q = it - p.n_full;
+    const int r = q / p.pieces;
+    u = p.n_full + r;
+    piece = q - r * p.pieces;
+    w.slot = q;
+  }
+  decode_unit(p.g, n_pairs, u, w.b, w.head, w.s, w.pair);
+  w.nt = scope_tiles(p.g, w.s);
+  if (2 * w.pair >= w.nt) return false;             // a shorter scope has fewer Q-tile pairs
+  if (w.slot < 0) {
+    w.j0 = 0;
+    w.j1 = w.nt;
+  } else {
+    w.j0 = piece * w.nt / p.pieces;
+    w.j1 = (piece + 1) * w.nt / p.pieces;
+  }
+  return w.j1 > w.j0;
+}
+
 // ---------------------------------------------------------------------------
 // RoPE pass: q, k (pre-RoPE) -> rotated copies in the workspace. One warp per
 // (b, token, head) row, two rows per iteration so each lane has four 8-byte
 // loads in flight; lane l owns channel pairs l*PPL .. l*PPL+PPL-1.
 // ---------------------------------------------------------------------------
+// The cos/sin table: one thread per entry, written to global memory once per call.
+__global__ void __launch_bounds__(256) skiparse_rope_table_kernel(const RopeParams r, float2* tab) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < r.entries) {
+    int pos;
+    double om;
+    rope_entry_args(r, e, pos, om);
+    tab[e] = rope_cos_sin(pos, om);
+  }
+}
+
+cudaError_t launch_rope_table(const RopeParams& r, float2* tab, cudaStream_t stream) {
+  skiparse_rope_table_kernel<<<(r.entries + 255) / 256, 256, 0, stream>>>(r, tab);
+  return cudaGetLastError();
+}
+
 template <int D>
 __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_rope_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ float2 tab[];
   const Geom& g = p.g;
-  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  rope_load_table(tab, p.rope_gtab, p.rope.entries, threadIdx.x, blockDim.x);
   __syncthreads();
   constexpr int PPL = D / 64;
   const int lane = threadIdx.x & 31;
@@ -181,7 +228,7 @@ template <int D>
 __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_pack_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ float2 tab[];
   const Geom& g = p.g;
-  if (p.rotate) rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  if (p.rotate) rope_load_table(tab, p.rope_gtab, p.rope.entries, threadIdx.x, blockDim.x);
   __syncthreads();
   constexpr int PPL = D / 64;
   const int lane = threadIdx.x & 31;
@@ -309,33 +356,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
     uint32_t gk = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      int b, head, s, pair;
-      decode_unit(g, n_pairs, u, b, head, s, pair);
-      const int nt = scope_tiles(g, s);
-      if (2 * pair >= nt) continue;                  // a shorter scope has fewer Q-tile pairs
+    for (int wi = blockIdx.x; ok && wi < p.n_items; wi += gridDim.x) {
+      Item w;
+      if (!decode_item(p, n_pairs, wi, w)) continue;
+      const int b = w.b, head = w.head, s = w.s, pair = w.pair;
+      const int nt = w.j1 - w.j0;                    // K tiles of this item
       if (it > 0 && !warp_wait(F_QEMPTY, (it - 1) & 1)) break;
       if (leader) {
         mbar_expect_tx(bar(F_QFULL), 2 * Ly::TILE);
+        const TileCoord tcA = scope_tile(g, s, b, 2 * pair * kTile);
+        const TileCoord tcB = scope_tile(g, s, b, (2 * pair + 1) * kTile);
 #pragma unroll
         for (int h = 0; h < Ly::HALVES; ++h) {
-          load_scope_tile(sQA + h * kHalfBytes, &p.tm_q, bar(F_QFULL), g, h * 64, head, s, b, 2 * pair * kTile);
-          load_scope_tile(sQB + h * kHalfBytes, &p.tm_q, bar(F_QFULL), g, h * 64, head, s, b, (2 * pair + 1) * kTile);
+          load_tile(sQA + h * kHalfBytes, &p.tm_q, bar(F_QFULL), tcA, h * 64, head);
+          load_tile(sQB + h * kHalfBytes, &p.tm_q, bar(F_QFULL), tcB, h * 64, head);
         }
       }
       __syncwarp();
       ++q_issued;
-      for (int j = 0; j < nt; ++j) {
-        const uint32_t gg = gk + j;
+      for (int jj = 0; jj < nt; ++jj) {
+        const int j = w.j0 + jj;                     // the scope's K tile
+        const uint32_t gg = gk + jj;
         const int st = gg & 1;
         const uint32_t n = gg >> 1;
+        const TileCoord tcj = scope_tile(g, s, b, j * kTile);
         if (n > 0 && !warp_wait(F_KEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
         if (leader) {
           mbar_expect_tx(bar(F_KFULL0 + st), Ly::TILE);
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h)
-            load_scope_tile(sK + st * Ly::TILE + h * kHalfBytes, &p.tm_k, bar(F_KFULL0 + st), g, h * 64, head, s, b,
-                            j * kTile);
+            load_tile(sK + st * Ly::TILE + h * kHalfBytes, &p.tm_k, bar(F_KFULL0 + st), tcj, h * 64, head);
         }
         __syncwarp();
         ++k_issued[st];
@@ -344,8 +394,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
           mbar_expect_tx(bar(F_VFULL0 + st), Ly::TILE);
 #pragma unroll
           for (int h = 0; h < Ly::HALVES; ++h)
-            load_scope_tile(sV + st * Ly::TILE + h * kHalfBytes, &p.tm_v, bar(F_VFULL0 + st), g, h * 64, head, s, b,
-                            j * kTile);
+            load_tile(sV + st * Ly::TILE + h * kHalfBytes, &p.tm_v, bar(F_VFULL0 + st), tcj, h * 64, head);
         }
         __syncwarp();
         ++v_issued[st];
@@ -393,11 +442,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tmem + colO, tmem + colS + ks * 8, mnmajor_step(dv, ks), kIdPV, (!first || ks > 0) ? 1u : 0u);
       };
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        int b, head, s, pair;
-        decode_unit(g, n_pairs, u, b, head, s, pair);
-        const int n = scope_tiles(g, s);
-        if (2 * pair >= n) continue;
+      for (int wi = blockIdx.x; ok && wi < p.n_items; wi += gridDim.x) {
+        Item w;
+        if (!decode_item(p, n_pairs, wi, w)) continue;
+        const int n = w.j1 - w.j0;                   // K tiles of this item
         if (!lane_wait(F_QFULL, it & 1)) break;
         if (!lane_wait(F_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
         tc_fence_after();
@@ -464,16 +512,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      int b, head, s, pair;
-      decode_unit(g, n_pairs, u, b, head, s, pair);
-      const int nt = scope_tiles(g, s);
-      if (2 * pair >= nt) continue;
+    for (int wi = blockIdx.x; ok && wi < p.n_items; wi += gridDim.x) {
+      Item w;
+      if (!decode_item(p, n_pairs, wi, w)) continue;
+      const int b = w.b, head = w.head, s = w.s, pair = w.pair;
+      const int nt = w.j1 - w.j0;                    // K tiles of this item
       const int Ls = scope_len(g, s);
       const int tile = 2 * pair + wg;
       float m = 0.f, l = 0.f;
-      for (int j = 0; j < nt; ++j) {
-        const uint32_t gg = g0 + j;
+      for (int jj = 0; jj < nt; ++jj) {
+        const int j = w.j0 + jj;                     // the scope's K tile
+        const uint32_t gg = g0 + jj;
         if (!mbar_wait(bar(barS), gg & 1, ctl, ERR_KERNEL_FWD + barS)) { ok = false; break; }
         tc_fence_after();
         const int valid = min(kTile, Ls - j * kTile);
@@ -483,7 +532,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
         const float mx = (valid == kTile ? row_max128<false>(x, valid) : row_max128<true>(x, valid)) * sl2;
         float f = 1.f;
         bool rescale = false;
-        if (j == 0) {
+        if (jj == 0) {
           m = mx;
         } else {
           const bool need = mx > m + 8.0f;
@@ -542,6 +591,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       if (!mbar_wait(bar(barO), glast & 1, ctl, ERR_KERNEL_FWD + barO)) break;
       tc_fence_after();
       const int prow = tile * kTile + r;
+      if (w.slot >= 0) {
+        // a piece of a split unit: unnormalised O and (m, l) for the merge
+        float* po = p.part_o + ((size_t)w.slot * 256 + wg * kTile + r) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + colO + c * 32, o);
+          float4* dst = reinterpret_cast<float4*>(po + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) dst[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+        }
+        p.part_ml[(size_t)w.slot * 256 + wg * kTile + r] = make_float2(m, l);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(barOE));
+        g0 += nt;
+        ++it;
+        continue;
+      }
       const bool row_ok = prow < Ls;
       const int tok = row_ok ? token_of(g, s, prow) : 0;
       const float inv_l = 1.0f / l;
@@ -578,6 +646,70 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Merge of split units: one warp per row of a split unit's Q-tile pair. The
+// pieces' partial results (O unnormalised, row max m and sum l, base 2) combine
+// as O = sum_p 2^(m_p - M) O_p / L with M = max_p m_p and L = sum_p 2^(m_p - M) l_p,
+// LSE = (M + log2 L) ln 2; out and lse are written at the token's row.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) skiparse_fwd_merge_kernel(const __grid_constant__ FwdParams p) {
+  const Geom& g = p.g;
+  constexpr int CPL = D / 32;                        // channels per lane
+  const int lane = threadIdx.x & 31;
+  const int n_pairs = (g.n_tiles + 1) >> 1;
+  const int np = p.pieces;
+  const int units = (p.n_items - p.n_full) / np;
+  const int rows = units * 256;
+  for (int rr = blockIdx.x * 8 + (threadIdx.x >> 5); rr < rows; rr += gridDim.x * 8) {
+    const int r = rr >> 8, row = rr & 255;
+    int b, head, s, pair;
+    decode_unit(g, n_pairs, p.n_full + r, b, head, s, pair);
+    const int nt = scope_tiles(g, s);
+    if (2 * pair >= nt) continue;
+    const int prow = (2 * pair + (row >> 7)) * kTile + (row & 127);
+    if (prow >= scope_len(g, s)) continue;
+    const float2* ml = p.part_ml + (size_t)r * np * 256 + row;     // piece pc at ml[pc * 256]
+    // the row's largest m over the pieces, lanes striding the pieces (an empty
+    // key range wrote nothing and weighs 0)
+    float M = -INFINITY;
+    for (int pc = lane; pc < np; pc += 32)
+      if ((pc + 1) * nt / np > pc * nt / np) M = fmaxf(M, ml[(size_t)pc * 256].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // O and l: all pieces' loads issued ahead of their sums
+    float L = 0.f, acc[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
+    const float* po = p.part_o + ((size_t)r * np * 256 + row) * D + lane * CPL;
+#pragma unroll 8
+    for (int pc = 0; pc < np; ++pc) {
+      const float2 v = ml[(size_t)pc * 256];
+      const bool has = (pc + 1) * nt / np > pc * nt / np;
+      const float f = has ? ex2(v.x - M) : 0.f;
+      L = fmaf(f, has ? v.y : 0.f, L);
+      const float* q = po + (size_t)pc * 256 * D;
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) acc[e] = fmaf(f, has ? q[e] : 0.f, acc[e]);
+    }
+    const int tok = token_of(g, s, prow);
+    const float inv = 1.0f / L;
+    uint16_t* orow = p.out + (((size_t)b * g.N + tok) * g.heads + head) * D + lane * CPL;
+#pragma unroll
+    for (int e = 0; e < CPL; e += 2) *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    if (lane == 0) p.lse[((size_t)b * g.heads + head) * g.N + tok] = (M + log2f(L)) * 0.6931471805599453f;
+  }
+}
+
+cudaError_t launch_fwd_merge(const FwdParams& p, int sms, cudaStream_t stream) {
+  const int rows = (p.n_items - p.n_full) / p.pieces * 256;
+  int grid = (rows + 7) / 8;
+  if (grid > 4 * sms) grid = 4 * sms;
+  if (p.g.D == 128) skiparse_fwd_merge_kernel<128><<<grid, 256, 0, stream>>>(p);
+  else skiparse_fwd_merge_kernel<64><<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 size_t fwd_smem_bytes(int D) { return D == 128 ? FwdLayout<128>::BYTES : FwdLayout<64>::BYTES; }

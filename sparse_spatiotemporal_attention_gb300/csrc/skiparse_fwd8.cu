@@ -216,7 +216,7 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
     }
     mbar_fence_init();
   }
-  rope_build_table(tab, p.rope, threadIdx.x, blockDim.x);
+  rope_load_table(tab, p.rope_gtab, p.rope.entries, threadIdx.x, blockDim.x);
   __syncthreads();
   const int n_items = g.B * g.heads * g.k * g.n_tiles;
   // head fastest: the CTAs working at the same time read all heads of the same

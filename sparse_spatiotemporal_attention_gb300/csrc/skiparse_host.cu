@@ -307,12 +307,42 @@ bool encode_packed_map(CUtensorMap* m, const void* base, const Geom& g) {
 // bytes of one scope-ordered bf16 copy (k, B, Lp, heads, D)
 size_t packed_bytes(const Geom& g) { return (size_t)g.k * g.B * g.Lp * g.heads * g.D * 2; }
 
+// Partial results of the split units of a forward's last round: O (256 rows x
+// D fp32) and (m, l) per row for each slot.
+size_t fwd_part_o_bytes(const Shape& s) { return align256((size_t)kMaxFwdSlots * 256 * s.D * 4); }
+size_t fwd_part_ml_bytes() { return align256((size_t)kMaxFwdSlots * 256 * sizeof(float2)); }
+
 // Forward workspace: rotated q and k in row order, or (unequal scopes) q, k
-// and v in scope order.
-size_t fwd_ws_bytes(const Shape& s) {
+// and v in scope order; then the split units' partial results.
+size_t fwd_copies_bytes(const Shape& s) {
   const Geom g = make_geom(s);
   if (g.packed) return 3 * align256(packed_bytes(g));
   return 2 * align256((size_t)s.elems * 2);
+}
+size_t rope_tab_bytes() { return align256((size_t)kMaxRopeEntries * sizeof(float2)); }
+size_t fwd_ws_bytes(const Shape& s) {
+  return fwd_copies_bytes(s) + fwd_part_o_bytes(s) + fwd_part_ml_bytes() + rope_tab_bytes();
+}
+// offset of the cos/sin table in the forward workspace (its last region)
+size_t fwd_tab_offset(const Shape& s) { return fwd_ws_bytes(s) - rope_tab_bytes(); }
+
+// How a forward's units spread over the SMs: whole units in full rounds, and
+// the last round's units split into key ranges when that round leaves at least
+// half of the SMs idle (every piece then runs at once, one per SM).
+void plan_fwd_items(FwdParams& p, int sms) {
+  const int U = p.n_units;
+  const int rounds = (U + sms - 1) / sms;
+  const int R = U - (rounds - 1) * sms;             // units of the last round, 1 .. sms
+  int pieces = std::min(std::min(sms / R, kMaxFwdSlots / R), p.g.n_tiles);
+  if (pieces < 2) {
+    p.n_full = U;
+    p.pieces = 1;
+    p.n_items = U;
+    return;
+  }
+  p.n_full = U - R;
+  p.pieces = pieces;
+  p.n_items = p.n_full + R * pieces;
 }
 
 // 2-D bf16 tensor map over a row-major (rows, cols) matrix: boxes of 64 columns
@@ -365,7 +395,7 @@ bool encode_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
 // codes as bf16 for the mixed recipe) and E4M3 V^T (scopes, 128, Lp), q scales
 // per scope-order row, k scales per K tile, max |v| per (b, head, channel).
 struct Ws8Layout {
-  size_t q8, k8, vt8, sq, sk, vmax, total;
+  size_t q8, k8, vt8, sq, sk, vmax, tab, total;
   int Lp, scopes;
 };
 
@@ -382,6 +412,7 @@ Ws8Layout ws8_layout(const Shape& s, bool si8) {
   w.sq = off;   off += align256(rows * 4);
   w.sk = off;   off += align256((size_t)w.scopes * (w.Lp / kTile) * 4);
   w.vmax = off; off += align256((size_t)s.B * s.heads * 128 * 4);
+  w.tab = off;  off += align256((size_t)kMaxRopeEntries * sizeof(float2));
   w.total = off;
   return w;
 }
@@ -458,6 +489,7 @@ const char* skiparse_kernel_name(int id) {
     case 8: return "skiparse_qkv_rope_kernel";
     case 9: return "skiparse_fwdm8_prep_kernel";
     case 10: return "skiparse_fwdm8_kernel";
+    case 11: return "skiparse_fwd_merge_kernel";
     default: return "unknown";
   }
 }
@@ -526,10 +558,18 @@ int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
   p.err = dev.err_word;
   p.n_units = fwd_units(p.g);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  plan_fwd_items(p, dev.sms);
+  p.part_o = reinterpret_cast<float*>(ws + fwd_copies_bytes(s));
+  p.part_ml = reinterpret_cast<float2*>(ws + fwd_copies_bytes(s) + fwd_part_o_bytes(s));
+  p.rope_gtab = reinterpret_cast<float2*>(ws + fwd_tab_offset(s));
   const long long rows = (long long)B * N * heads;
   long long rgrid = (rows + 15) / 16;                 // 8 warps per CTA, 2 rows per warp
   if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
-  const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
+  const int grid = p.n_items < dev.sms ? p.n_items : dev.sms;
+  if (p.g.packed || rotate) {
+    st = launch_status(launch_rope_table(p.rope, p.rope_gtab, stream));
+    if (st != SKIPARSE_OK) return st;
+  }
   if (p.g.packed) {
     st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_pack(p, 8 * dev.sms, dev.sms, stream); }));
     if (st != SKIPARSE_OK) return st;
@@ -537,7 +577,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
     st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_rope(p, (int)rgrid, dev.sms, stream); }));
     if (st != SKIPARSE_OK) return st;
   }
-  return launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));
+  st = launch_status(traced_launch(0, stream, [&] { return launch_fwd(p, grid, stream); }));
+  if (st != SKIPARSE_OK || p.n_items == p.n_full) return st;
+  return launch_status(traced_launch(11, stream, [&] { return launch_fwd_merge(p, dev.sms, stream); }));
 }
 
 }  // namespace
@@ -617,6 +659,7 @@ int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, 
   p.sq = reinterpret_cast<float*>(ws + w.sq);
   p.sk = reinterpret_cast<float*>(ws + w.sk);
   p.vmax = reinterpret_cast<unsigned*>(ws + w.vmax);
+  p.rope_gtab = reinterpret_cast<float2*>(ws + w.tab);
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.err = dev.err_word;
@@ -635,6 +678,8 @@ int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, 
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
   if (cudaMemsetAsync(p.vmax, 0, (size_t)B * heads * 128 * 4, stream) != cudaSuccess) return launch_status(cudaErrorUnknown);
   st = launch_status(traced_launch(5, stream, [&] { return launch_fwd8_vmax(p, stream); }));
+  if (st != SKIPARSE_OK) return st;
+  st = launch_status(launch_rope_table(p.rope, p.rope_gtab, stream));
   if (st != SKIPARSE_OK) return st;
   st = launch_status(traced_launch(si8 ? 9 : 6, stream, [&] { return launch_fwd8_prep(p, si8, dev.sms, stream); }));
   if (st != SKIPARSE_OK) return st;
@@ -727,7 +772,10 @@ int bwd_impl(const void* q, const void* k, const void* fwd_ws, size_t fwd_ws_giv
   p.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
   p.lse2s = reinterpret_cast<float*>(ws + w.lse2s);
   p.delta_s = reinterpret_cast<float*>(ws + w.delta_s);
-  p.rope_tab = reinterpret_cast<float2*>(ws + w.tab);
+  // the cos/sin table: the forward call's when its workspace is reused (same
+  // sizes and rope_theta), else built here into this workspace
+  p.rope_tab = saved ? reinterpret_cast<float2*>(const_cast<uint8_t*>(fw) + fwd_tab_offset(s))
+                     : reinterpret_cast<float2*>(ws + w.tab);
   p.dq = static_cast<uint16_t*>(dq);
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
@@ -764,6 +812,10 @@ int bwd_impl(const void* q, const void* k, const void* fwd_ws, size_t fwd_ws_giv
   if (rgrid > 8ll * dev.sms) rgrid = 8ll * dev.sms;
   const int pregrid = p.g.packed ? 8 * dev.sms : (int)rgrid;
   const int mgrid = p.n_units < dev.sms ? p.n_units : dev.sms;
+  if (!saved) {
+    st = launch_status(launch_rope_table(p.rope, p.rope_tab, stream));
+    if (st != SKIPARSE_OK) return st;
+  }
   st = launch_status(traced_launch(1, stream, [&] { return launch_bwd_pre(p, pregrid, dev.sms, stream); }));
   if (st != SKIPARSE_OK) return st;
   st = launch_status(traced_launch(2, stream, [&] { return launch_bwd_main(p, mgrid, stream); }));

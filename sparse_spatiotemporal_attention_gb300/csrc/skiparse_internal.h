@@ -29,14 +29,25 @@ struct FwdParams {
   uint16_t* kr;                   // workspace: rotated k, likewise
   uint16_t* vr;                   // packed only: v in scope order (k, B, Lp, heads, D)
   int rotate;                     // 0: rope_theta = 0 (q, k arrive rotated; the pack pass only copies)
+  float2* rope_gtab;              // workspace: the cos/sin table (written by skiparse_rope_table_kernel)
   Geom g;
   RopeParams rope;
   uint16_t* out;                  // bf16 (B, N, heads, D)
   float* lse;                     // (B, heads, N)
   int* err;                       // device error word
   int n_units;                    // B * heads * k * ceil(n_tiles / 2): pairs of Q tiles
+  // Work items: units [0, n_full) whole, then the remaining units each split
+  // into `pieces` key-tile ranges whose partial O, m, l go to part_o / part_ml
+  // (slot = item - n_full) and are merged by skiparse_fwd_merge_kernel.
+  int n_full, pieces, n_items;
+  float* part_o;                  // workspace: (slots, 256 rows, D) fp32 unnormalised O of a Q-tile pair
+  float2* part_ml;                // workspace: (slots, 256 rows) (m, l) in base 2
   float scale_log2;               // log2(e) / sqrt(D)
 };
+
+// Most slots of split units a forward call uses (the pieces of its last round
+// of units run together, one per SM).
+constexpr int kMaxFwdSlots = 160;
 
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;   // maps over rotated q, rotated k, v, dout (128-row boxes)
@@ -80,6 +91,7 @@ struct Fwd8Params {
   const uint16_t* q;              // bf16 (B, N, heads, D) inputs
   const uint16_t* k;
   const uint16_t* v;
+  float2* rope_gtab;              // workspace: the cos/sin table (written by skiparse_rope_table_kernel)
   uint8_t* q8;                    // workspace: codes (scopes, Lp, 128), scope order, 1 or 2 bytes each
   uint8_t* k8;
   uint8_t* vt8;                   // workspace: E4M3 V^T (scopes, 128, Lp)
@@ -147,6 +159,9 @@ int fwd_units(const Geom& g);
 cudaError_t launch_fwd_rope(const FwdParams& p, int grid, int sms, cudaStream_t stream);
 cudaError_t launch_fwd_pack(const FwdParams& p, int grid, int sms, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_merge(const FwdParams& p, int sms, cudaStream_t stream);
+// the 3D RoPE cos/sin table of `r` into tab (r.entries float2), once per call
+cudaError_t launch_rope_table(const RopeParams& r, float2* tab, cudaStream_t stream);
 
 // si8: the mixed recipe (INT8 q / k codes held as bf16 for S, E4M3 P and v)
 size_t fwd8_smem_bytes(bool si8);
