@@ -161,11 +161,17 @@ def test_backward_saved_bitwise_and_parity(env, case):
 
 def test_peaky_softmax_rescale(env):
     """q scaled by 4 makes row maxima jump between key tiles, exercising the
-    online-softmax rescale of O. Not a contract workload: with |q| four times
-    larger, the bf16 rounding of the rotated q and k (the MMA operands) moves
-    each logit by up to ~2^-9 * |q~||k~| / sqrt(D), about 0.05 here, and the
-    bf16 P and output roundings add 2^-9 * max|v| each. The bound is therefore
-    stated relative to the data: relative RMS 1e-2, max-abs 2^-4 * max|ref|."""
+    online-softmax rescale of O. Not a contract workload; its bound is derived
+    from the operands' bf16 rounding instead. The rotated q~ and k~ are MMA
+    operands in bf16: each element carries a relative rounding error of
+    standard deviation 2^-8 / sqrt(12), so a logit q~.k~ / sqrt(D) moves by
+    about sigma = 2^-8 / sqrt(12) * sqrt(2 sum_d q~_d^2 k~_d^2) / sqrt(D), here
+    (|q~_d| ~ 4, |k~_d| ~ 1) about 0.0064. A softmax row split between keys
+    moves its output by at most (e^(2 d) - 1) |v_j - O| for logit shifts d;
+    with d = 5 sigma and |v_j - O| up to 2 max|v|, that is about 0.5 % of
+    max|v|, and the gradients, formed from the same P, carry the same relative
+    error. The bound, 2^-5 max|ref| per element (with relative RMS 1e-2),
+    leaves a factor of about six over that estimate."""
     skp, dev = env
     B, heads, D, T, H, W, k, mode = 1, 2, 128, 4, 16, 16, 2, O.SINGLE
     N = T * H * W
@@ -178,7 +184,7 @@ def test_peaky_softmax_rescale(env):
     for name, got, ref in (("out", fw["out"], rout), ("dv", bw["dv"], rdv), ("dk", bw["dk"], rdk),
                            ("dq", bw["dq"], rdq)):
         m = np.abs(ref).max()
-        print(tl.compare(name, tl.host(got), ref, tol_max=m / 16, tol_mean=m / 256, tol_rel=1e-2), f"max|ref| {m:.3e}")
+        tl.compare(name, tl.host(got), ref, tol_max=m / 32, tol_mean=m / 256, tol_rel=1e-2)
 
 
 @pytest.mark.parametrize("mode", [O.SINGLE, O.GROUP])
