@@ -35,8 +35,8 @@ Readings taken where the page is silent:
     stored in original token order as (B, heads, N);
   * N not divisible by k (single) or k*k (group), where the listings' rearrange
     has no shape: the section's prose still defines the scopes for any N
-    (single: the tokens spaced k-1 apart, i.e. i mod k = s; group: the groups
-    of k adjacent tokens spaced k-1 groups apart, i.e. (i div k) mod k = s, the
+    (single: every k-th token, i.e. i mod k = s; group: every k-th group of k
+    adjacent tokens, i.e. (i div k) mod k = s, the
     last group holding the N mod k leftover tokens). Scope s then holds exactly
     those tokens in ascending order, and scopes differ in length by at most one
     token (single) or one group (group); nothing is padded. When N is
@@ -423,8 +423,9 @@ def _rope_rows(x, t, h, w, theta, inverse=False):
 
 def skiparse_mask(N: int, sparse_k: int, mode: int) -> np.ndarray:
     """M[i, j] = True when tokens i and j share a scope, from the section's prose:
-    single skip attends to tokens spaced k-1 apart (i = j mod k); group skip
-    bundles groups of k adjacent tokens with groups spaced k-1 groups apart
+    single skip pairs tokens whose distance is a multiple of k (i = j mod k);
+    group skip pairs groups of k adjacent tokens whose group indices differ by a
+    multiple of k
     ((i div k) = (j div k) mod k)."""
     i = np.arange(N)
     if mode == SINGLE:

@@ -175,7 +175,7 @@ def test_brute_force_tiny(grid, k, mode):
     qt = O.rope_closed_form(c["q"], T, H, W, THETA)[0, :, 0].tolist()
     kt = O.rope_closed_form(c["k"], T, H, W, THETA)[0, :, 0].tolist()
     if mode == O.SINGLE:
-        same = lambda i, j: (i - j) % k == 0          # spaced k-1 apart
+        same = lambda i, j: (i - j) % k == 0          # every k-th token
     else:
         same = lambda i, j: (i // k - j // k) % k == 0
     bo, bl = _brute_force(qt, kt, c["v"][0, :, 0].tolist(), same, 1 / 4.0)
@@ -359,8 +359,8 @@ def test_ragged_equals_masked_dense(grid, k, mode):
 @pytest.mark.parametrize("grid,k,mode", RAGGED[:3])
 def test_ragged_brute_force(grid, k, mode):
     """Ragged scopes against the unstabilised pure-Python formula, with scope
-    membership written out from the prose (tokens spaced k-1 apart, or groups
-    of k spaced k-1 groups apart)."""
+    membership written out from the prose (every k-th token, or every k-th
+    group of k adjacent tokens)."""
     T, H, W = grid
     c = small_case(mode, k=k, T=T, H=H, W=W, B=1, nh=1)
     q, kk, v = c["q"], c["k"], c["v"]

@@ -103,7 +103,7 @@ def test_scope_mates_match_prose_mask(mode, name):
         assert np.array_equal(scope[:, None] == scope[None, :], mask)
         i = np.arange(N)
         if mode == O.SINGLE:
-            # "tokens spaced k-1 apart": j - i is a multiple of k
+            # every k-th token: j - i is a multiple of k
             assert np.array_equal(mask, ((i[:, None] - i[None, :]) % k) == 0)
         else:
             g = i // k
