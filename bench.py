@@ -61,6 +61,10 @@ WORKLOADS = {
                       mode=1, fwd=[dict(name="skiparse_fwd_group_24x22x40_k4_b1h8", B=1, heads=8, D=128, T=24, H=22,
                                         W=40, k=4, mode=1, k1=False)]),
 }
+# the short-scope forward (single skip 8x32x32) as a small case of its own for ncu
+WORKLOADS["ncu_single"] = dict(name="skiparse_step_single_8x32x32_k4", B=1, heads=24, D=128, T=8, H=32, W=32, k=4,
+                               mode=0, fwd=[dict(name="skiparse_fwd_single_8x32x32_k4", B=1, heads=24, D=128, T=8,
+                                                 H=32, W=32, k=4, mode=0, k1=False)])
 WORKLOAD = WORKLOADS["train"]
 # forward-only configurations reported beside the timed step (same kernels)
 FWD_CONFIGS = [
