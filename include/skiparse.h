@@ -166,8 +166,9 @@ int skiparse_attn_fwd_mixed8(const void* q, const void* k, const void* v, void* 
 
 /*
  * Bytes of device workspace skiparse_attn_bwd needs for these sizes: an fp32
- * dQ accumulator, rotated bf16 copies of q and k, per-scope fp32 LSE and
- * delta rows, and the RoPE cos/sin table. Returns 0 for empty or invalid sizes.
+ * dQ accumulator, rotated bf16 copies of q and k (for scopes of unequal length:
+ * scope-ordered copies of q, k, v and dout), per-scope fp32 LSE and delta rows,
+ * and the RoPE cos/sin table. Returns 0 for empty or invalid sizes.
  */
 size_t skiparse_attn_bwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
                                          int sparse_k, int mode);
@@ -191,8 +192,10 @@ int skiparse_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
- * Backward pass reusing the forward pass's rotated q and k: the same outputs,
- * bit for bit, as skiparse_attn_bwd on the q and k of that forward call, for
+ * Backward pass reusing the forward pass's rotated q and k: the same outputs
+ * as skiparse_attn_bwd on the q and k of that forward call (dk and dv bit for
+ * bit; dq up to the timing-set order of its fp32 accumulation, at most one bf16
+ * step per element), for
  * a training step that keeps the forward workspace until its backward (no
  * counterpart in the pages; it saves the preprocess's re-read of q and k and
  * its rewrite of their rotated copies).
@@ -230,9 +233,11 @@ int skiparse_attn_bwd_saved(const void* fwd_workspace, size_t fwd_workspace_byte
  *   - Returns SKIPARSE_ERR_WORKSPACE, launching nothing, when
  *     skiparse_attn_bwd_workspace_bytes(...) for these sizes is larger than
  *     SKIPARSE_NOALLOC_SCRATCH_BYTES (about 8M elements of B*N*heads*D).
+ *   - The first call on a device, and the first after the device's context
+ *     changed, looks up the array's address.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.
- *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *     That look-up runs with the device current; make the first call before
+ *     any stream capture.
  *   - Every call shares the one array, which keeps the previous call's
  *     contents; each call rewrites all it reads and zeroes its dQ accumulator.
  *     Calls that overlap on the GPU (e.g. on two streams) race on the array:

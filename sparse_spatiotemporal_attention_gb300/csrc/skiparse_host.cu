@@ -309,8 +309,14 @@ size_t packed_bytes(const Geom& g) { return (size_t)g.k * g.B * g.Lp * g.heads *
 
 // Partial results of the split units of a forward's last round: O (256 rows x
 // D fp32) and (m, l) per row for each slot.
-size_t fwd_part_o_bytes(const Shape& s) { return align256((size_t)kMaxFwdSlots * 256 * s.D * 4); }
-size_t fwd_part_ml_bytes() { return align256((size_t)kMaxFwdSlots * 256 * sizeof(float2)); }
+// at most kMaxFwdSlots, and never more than the call's (unit, K tile) pairs
+size_t fwd_part_slots(const Shape& s) {
+  const Geom g = make_geom(s);
+  const long long pairs = (long long)s.B * s.heads * s.k * ((g.n_tiles + 1) / 2) * g.n_tiles;
+  return (size_t)std::min<long long>(kMaxFwdSlots, pairs);
+}
+size_t fwd_part_o_bytes(const Shape& s) { return align256(fwd_part_slots(s) * 256 * s.D * 4); }
+size_t fwd_part_ml_bytes(const Shape& s) { return align256(fwd_part_slots(s) * 256 * sizeof(float2)); }
 
 // Forward workspace: rotated q and k in row order, or (unequal scopes) q, k
 // and v in scope order; then the split units' partial results.
@@ -321,7 +327,7 @@ size_t fwd_copies_bytes(const Shape& s) {
 }
 size_t rope_tab_bytes() { return align256((size_t)kMaxRopeEntries * sizeof(float2)); }
 size_t fwd_ws_bytes(const Shape& s) {
-  return fwd_copies_bytes(s) + fwd_part_o_bytes(s) + fwd_part_ml_bytes() + rope_tab_bytes();
+  return fwd_copies_bytes(s) + fwd_part_o_bytes(s) + fwd_part_ml_bytes(s) + rope_tab_bytes();
 }
 // offset of the cos/sin table in the forward workspace (its last region)
 size_t fwd_tab_offset(const Shape& s) { return fwd_ws_bytes(s) - rope_tab_bytes(); }
@@ -329,11 +335,11 @@ size_t fwd_tab_offset(const Shape& s) { return fwd_ws_bytes(s) - rope_tab_bytes(
 // How a forward's units spread over the SMs: whole units in full rounds, and
 // the last round's units split into key ranges when that round leaves at least
 // half of the SMs idle (every piece then runs at once, one per SM).
-void plan_fwd_items(FwdParams& p, int sms) {
+void plan_fwd_items(FwdParams& p, int sms, int slots) {
   const int U = p.n_units;
   const int rounds = (U + sms - 1) / sms;
   const int R = U - (rounds - 1) * sms;             // units of the last round, 1 .. sms
-  int pieces = std::min(std::min(sms / R, kMaxFwdSlots / R), p.g.n_tiles);
+  int pieces = std::min(std::min(sms / R, slots / R), p.g.n_tiles);
   if (pieces < 2) {
     p.n_full = U;
     p.pieces = 1;
@@ -558,7 +564,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse,
   p.err = dev.err_word;
   p.n_units = fwd_units(p.g);
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  plan_fwd_items(p, dev.sms);
+  plan_fwd_items(p, dev.sms, (int)fwd_part_slots(s));
   p.part_o = reinterpret_cast<float*>(ws + fwd_copies_bytes(s));
   p.part_ml = reinterpret_cast<float2*>(ws + fwd_copies_bytes(s) + fwd_part_o_bytes(s));
   p.rope_gtab = reinterpret_cast<float2*>(ws + fwd_tab_offset(s));

@@ -50,14 +50,18 @@ def test_status_strings(lib):
 A = 1 << 20  # fake, 16-byte-aligned device addresses: validation fails before any use
 
 
-def fwd_parts(D):
+def _a256(x):
+    return (x + 255) // 256 * 256
+
+
+def fwd_parts(D, slots):
     """Forward workspace past the q / k copies: the split units' partial results,
-    O (160 slots x 256 rows x D fp32) and (m, l) per row, and the cos/sin table
-    (8192 pairs of fp32)."""
-    return 160 * 256 * D * 4 + 160 * 256 * 8 + 8192 * 8
+    O (slots x 256 rows x D fp32) and (m, l) per row, with slots = min(160, the
+    call's (unit, K tile) pairs), and the cos/sin table (8192 pairs of fp32)."""
+    return _a256(slots * 256 * D * 4) + _a256(slots * 256 * 8) + 8192 * 8
 
 
-FWD_WS = 2 * 256 * 2 * 64 * 2 + fwd_parts(64)   # rotated q and k for B=1, heads=2, N=256, D=64, partials
+FWD_WS = 2 * 256 * 2 * 64 * 2 + fwd_parts(64, 4)   # B=1, heads=2, N=256, D=64, k=2: 4 units of 1 tile
 
 
 def fwd(lib, q=A, k=2 * A, v=3 * A, out=4 * A, lse=5 * A, ws=8 * A, ws_bytes=FWD_WS, B=1, heads=2, N=256, D=64,
@@ -104,7 +108,7 @@ def test_fwd_workspace_bytes(lib):
     assert lib.skiparse_attn_fwd_workspace_bytes(0, 2, 256, 64, 4, 8, 8, 2, 0) == 0
     assert lib.skiparse_attn_fwd_workspace_bytes(1, 2, 256, 96, 4, 8, 8, 2, 0) == 0
     # each rotated copy is rounded up to 256 bytes: 1 x 1 x 3 tokens x 64 channels
-    assert lib.skiparse_attn_fwd_workspace_bytes(1, 1, 3, 64, 1, 1, 3, 1, 0) == 2 * 512 + fwd_parts(64)
+    assert lib.skiparse_attn_fwd_workspace_bytes(1, 1, 3, 64, 1, 1, 3, 1, 0) == 2 * 512 + fwd_parts(64, 1)
 
 
 def test_bwd_validation_and_workspace(lib):
@@ -152,7 +156,7 @@ def test_ragged_workspace_sizes(lib):
     q, k, v (forward) and of q, k, v, dO (backward); the 8-bit forwards refuse them."""
     B, heads, D, N, k = 1, 2, 64, 192, 5                 # single skip: L_0 = 39, Lp = 128
     copy = k * B * 128 * heads * D * 2
-    assert lib.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, 3, 8, 8, k, 0) == 3 * copy + fwd_parts(D)
+    assert lib.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, 3, 8, 8, k, 0) == 3 * copy + fwd_parts(D, 10)
     stats = B * heads * k * 128
     want = stats * D * 4 + 4 * copy + 2 * stats * 4
     got = lib.skiparse_attn_bwd_workspace_bytes(B, heads, N, D, 3, 8, 8, k, 0)

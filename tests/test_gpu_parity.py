@@ -128,8 +128,11 @@ SAVED_CASES = [(1, 2, 128, 3, 10, 10, 2, O.GROUP), (2, 3, 64, 2, 8, 12, 2, O.SIN
 @pytest.mark.parametrize("case", SAVED_CASES, ids=_ids)
 def test_backward_saved_bitwise_and_parity(env, case):
     """The backward that reuses the forward's rotated q / k gives the regular
-    backward's outputs bit for bit (the same kernels read bitwise-equal rotated
-    copies), and so matches the oracle."""
+    backward's dk and dv bit for bit (the same kernels read bitwise-equal
+    rotated copies) and its dq up to the order of dq's fp32 accumulation: the
+    key tiles' bulk reduce-adds into the accumulator land in an order set by
+    timing, so the fp32 sums may differ in their last bits and a dq element by
+    one bf16 step after rounding. Both match the oracle."""
     import torch
     skp, dev = env
     B, heads, D, T, H, W, k, mode = case
@@ -148,8 +151,15 @@ def test_backward_saved_bitwise_and_parity(env, case):
     skp.skiparse_attn_bwd(q, kk, v, out, lse, do, *g1, ws, T, H, W, k, mode)
     skp.skiparse_attn_bwd_saved(fws, v, out, lse, do, *g2, ws, T, H, W, k, mode)
     torch.cuda.synchronize()
-    for name, a, b in zip(("dq", "dk", "dv"), g1, g2):
+    for name, a, b in zip(("dk", "dv"), g1[1:], g2[1:]):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
+    d1, d2 = tl.host(g1[0]), tl.host(g2[0])
+    diff = np.abs(d1 - d2)
+    worst = np.unravel_index(np.argmax(diff), diff.shape)
+    msg = f"dq: {np.count_nonzero(diff)} elements differ, worst {diff[worst]:.3e} at {d1[worst]:.3e} / {d2[worst]:.3e}"
+    print(msg)
+    # one bf16 step is at most 2^-7 of the value (at the bottom of a binade)
+    assert np.all(diff <= 2.0 ** -7 * np.maximum(np.abs(d1), np.abs(d2)) + 1e-7), msg
     f = tl.f64_inputs(ins)
     rdq, rdk, rdv, _, _ = O.skiparse_bwd(f["q"], f["k"], f["v"], f["do"], T, H, W, k, mode)
     tl.compare("dq", tl.host(g2[0]), rdq)
