@@ -70,13 +70,70 @@ __device__ __forceinline__ uint32_t i8x2_bf16(float a, float b) {
   return pack_bf16(fminf(fmaxf(rintf(a), -kInt8Max), kInt8Max), fminf(fmaxf(rintf(b), -kInt8Max), kInt8Max));
 }
 
-// RoPE table bytes in the prep kernel's shared memory, rounded up to 16
-__host__ __device__ constexpr size_t prep_table_bytes(int entries) { return ((size_t)entries * 8 + 15) & ~(size_t)15; }
+// The prep kernel's own shared-memory layout of the RoPE table (D = 128).
+// Lane class cb = 0..7 of a row rotates the channel pairs 8 cb .. 8 cb + 7,
+// which lie on one axis (cb 0-1: t, 2-4: h, 5-7: w) and take 64 bytes of the
+// global table per axis position. In that table every such run starts on a
+// 64-byte boundary, so the 8 lanes of a row read only two 16-byte bank groups
+// at a time (4-way conflicts). Here two classes share each 128-byte line:
+// region 0 holds classes 0 and 1 (line = lb[0] + t), region 1 classes 2 and 3
+// (lb[1] + h), region 2 classes 5 and 6 (lb[2] + w), region 3 classes 4 (h)
+// and 7 (w), line lb[3] + position; a region's lines number its longer axis,
+// so only region 3 leaves half-lines unused (|H - W| of them). Class cb of
+// region c starts at unit sigma = c (first class) or c + 4 (second), and its
+// 16-byte unit m' (pairs 2 m', 2 m' + 1 of its 8) sits at unit
+// (sigma + (m' ^ 2 (cb >> 2))) & 7 of the line: at step m a lane reads unit
+// (sigma + m) & 7, a different bank group for each of the 8 lanes. (The
+// m' ^ 2 (cb >> 2) matches the order in which lanes 4-7 read their staged
+// q / k chunks, second chunk first.)
+// 4-bit fields, index cb: region, sigma; index c: the region's two classes
+constexpr uint32_t kTabRegion = 0x32231100u, kTabSigma = 0x76235140u;
+constexpr uint32_t kTabFirst = 0x4520u, kTabSecond = 0x7631u;
+
+__host__ __device__ __forceinline__ int nibble(uint32_t x, int i) { return (int)((x >> (4 * i)) & 15u); }
+
+struct PrepTab { int lb[4]; int lines; };
+
+__host__ __device__ inline PrepTab prep_tab(int T, int H, int W) {
+  PrepTab t;
+  t.lb[0] = 0;
+  t.lb[1] = T;
+  t.lb[2] = T + H;
+  t.lb[3] = T + H + W;
+  t.lines = t.lb[3] + (H > W ? H : W);
+  return t;
+}
+
+// first line of region c (selects, not an indexed load from a local array)
+__host__ __device__ __forceinline__ int prep_lb(const PrepTab& t, int c) {
+  return c == 0 ? t.lb[0] : (c == 1 ? t.lb[1] : (c == 2 ? t.lb[2] : t.lb[3]));
+}
+
+__host__ __device__ inline size_t prep_table_bytes(int T, int H, int W) { return (size_t)prep_tab(T, H, W).lines * 128; }
+
 // prep kernel shared memory: 1 KB header (barriers, per-warp maxima, abort
 // flag), the staging ring (1024-byte aligned for the swizzle), the V^T
 // transpose buffer (128 channels x 32 words), the RoPE table
-__host__ __device__ constexpr size_t prep_smem(int stages, int entries) {
-  return 1024 + (size_t)stages * kPrepStage + (size_t)128 * 32 * 4 + prep_table_bytes(entries);
+__host__ __device__ inline size_t prep_smem(int stages, int T, int H, int W) {
+  return 1024 + (size_t)stages * kPrepStage + (size_t)128 * 32 * 4 + prep_table_bytes(T, H, W);
+}
+
+// copies the global table (built once per call) into the layout above
+__device__ __forceinline__ void prep_load_table(float4* tab, const float2* gtab, const RopeParams& r, const PrepTab& pt,
+                                                int tid, int nthreads) {
+  for (int u = tid; u < pt.lines * 8; u += nthreads) {
+    const int line = u >> 3, slot = u & 7;
+    const int c = line >= pt.lb[3] ? 3 : (line >= pt.lb[2] ? 2 : (line >= pt.lb[1] ? 1 : 0));
+    const int j = (slot - c) & 7;                       // 0-3: first class, 4-7: second
+    const int cb = nibble(j < 4 ? kTabFirst : kTabSecond, c);
+    const int mp = (j & 3) ^ (2 * (cb >> 2));
+    const int pos = line - prep_lb(pt, c);
+    const PairSel sel = pair_select(r, 8 * cb);
+    const int npos = sel.axis == 0 ? r.T : (sel.axis == 1 ? r.H : r.W);
+    float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (pos < npos) val = __ldg(reinterpret_cast<const float4*>(gtab + sel.base + pos * sel.stride + sel.local + 2 * mp));
+    tab[u] = val;
+  }
 }
 
 // 2^6 P = 2^(S * ck + off) for one softmax row held in registers (x, 128 keys;
@@ -202,7 +259,7 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
   int* abort_flag = reinterpret_cast<int*>(psm + 192);
   uint8_t* ring = psm + 1024;
   uint32_t* vt = reinterpret_cast<uint32_t*>(ring + (size_t)stages * kPrepStage);  // 128 channels x 32 words
-  float2* tab = reinterpret_cast<float2*>(vt + kD8 * 32);                           // RoPE table
+  float4* tab = reinterpret_cast<float4*>(vt + kD8 * 32);                           // RoPE table
   const uint32_t bar0 = smem_u32(psm);
   // barriers: FULL of slot st at st, EMPTY of slot st at 2 + st
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
@@ -216,7 +273,8 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
     }
     mbar_fence_init();
   }
-  rope_load_table(tab, p.rope_gtab, p.rope.entries, threadIdx.x, blockDim.x);
+  const PrepTab pt = prep_tab(p.rope.T, p.rope.H, p.rope.W);
+  prep_load_table(tab, p.rope_gtab, p.rope, pt, threadIdx.x, blockDim.x);
   __syncthreads();
   const int n_items = g.B * g.heads * g.k * g.n_tiles;
   // head fastest: the CTAs working at the same time read all heads of the same
@@ -270,19 +328,20 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
   // chunk, contiguous in the table), so per-row work (token coordinates, table
   // index, the row max over 8 lanes, the scale divisions) serves four rows per
   // instruction. In a staged row those channels are the 16-byte chunks
-  // 2 (cb % 4) and 2 (cb % 4) + 1 of half cb / 4, each XOR (row % 8).
+  // 2 (cb % 4) and 2 (cb % 4) + 1 of half cb / 4, each XOR (row % 8); lanes
+  // 4-7 (hsel = 1) read the second chunk first, so that the two halves' lanes
+  // fall on different bank groups. Their registers then hold pairs 4-7 before
+  // 0-3, which the table layout and the code stores undo.
   // v (read directly): lane l takes channels 4 l .. 4 l + 3 of all four rows,
   // the layout the V^T transpose needs.
   const int rq = lane >> 3, cb = lane & 7;
-  const uint32_t half_off = (uint32_t)(cb >> 2) * kPrepHalf;
-  const uint32_t chunk0 = (uint32_t)(2 * (cb & 3));
-  // this lane's 8 pairs in the table: base entry of the chunk and pair offset
-  int tab_base, tab_stride, tab_local, tab_axis;
-  {
-    const int pp = 8 * cb;                              // D = 128: pairs 0-15 t, 16-39 h, 40-63 w
-    const PairSel sel = pair_select(p.rope, pp);
-    tab_base = sel.base; tab_stride = sel.stride; tab_local = sel.local; tab_axis = sel.axis;
-  }
+  const int hsel = cb >> 2;
+  const uint32_t half_off = (uint32_t)hsel * kPrepHalf;
+  const uint32_t chunk_a = (uint32_t)(2 * (cb & 3) + hsel), chunk_b = (uint32_t)(2 * (cb & 3) + 1 - hsel);
+  // this lane's table lines: region of its class, axis that indexes it
+  const int tab_axis = pair_select(p.rope, 8 * cb).axis;   // D = 128: pairs 0-15 t, 16-39 h, 40-63 w
+  const float4* tab_lane = tab + (size_t)prep_lb(pt, nibble(kTabRegion, cb)) * 8;
+  const int tab_sigma = nibble(kTabSigma, cb);
   auto load_v = [&](int tile, int s, int b, int head, int i, uint2 (&vv)[4]) {
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
@@ -333,8 +392,8 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
         for (int e = 0; e < 16; ++e) qr[e] = 0.f;
         if (valid) {
           const uint32_t rb = (uint32_t)r * 128u + half_off;
-          const uint32_t o0 = rb + ((chunk0 ^ (uint32_t)(r & 7)) << 4);
-          const uint32_t o1 = rb + (((chunk0 + 1u) ^ (uint32_t)(r & 7)) << 4);
+          const uint32_t o0 = rb + ((chunk_a ^ (uint32_t)(r & 7)) << 4);
+          const uint32_t o1 = rb + ((chunk_b ^ (uint32_t)(r & 7)) << 4);
           uint32_t qw[8], kw[8];
           *reinterpret_cast<uint4*>(qw) = *reinterpret_cast<const uint4*>(q_tile + o0);
           *reinterpret_cast<uint4*>(qw + 4) = *reinterpret_cast<const uint4*>(q_tile + o1);
@@ -343,10 +402,10 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
           int t, hh, w;
           token_coords(p.rope, token_of(g, s, pos), t, hh, w);
           const int apos = tab_axis == 0 ? t : (tab_axis == 1 ? hh : w);
-          const float4* tp = reinterpret_cast<const float4*>(tab + tab_base + apos * tab_stride + tab_local);
+          const float4* tp = tab_lane + apos * 8;
 #pragma unroll
           for (int m2 = 0; m2 < 4; ++m2) {
-            const float4 cs = tp[m2];                              // pairs 2 m2, 2 m2 + 1
+            const float4 cs = tp[(tab_sigma + m2) & 7];            // the pairs of words 2 m2, 2 m2 + 1
             const float2 qa = rope_rotate(bf16lo(qw[2 * m2]), bf16hi(qw[2 * m2]), make_float2(cs.x, cs.y));
             const float2 qb = rope_rotate(bf16lo(qw[2 * m2 + 1]), bf16hi(qw[2 * m2 + 1]), make_float2(cs.z, cs.w));
             const float2 ka = rope_rotate(bf16lo(kw[2 * m2]), bf16hi(kw[2 * m2]), make_float2(cs.x, cs.y));
@@ -380,10 +439,11 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
         }
         if constexpr (SI8) {
           uint4* dst = reinterpret_cast<uint4*>(p.q8 + slot * QROW + cb * 32);
-          dst[0] = qc;
-          dst[1] = qc2;
+          dst[hsel] = qc;
+          dst[1 - hsel] = qc2;
         } else {
-          *reinterpret_cast<uint4*>(p.q8 + slot * QROW + cb * 16) = qc;
+          *reinterpret_cast<uint4*>(p.q8 + slot * QROW + cb * 16) =
+              hsel ? make_uint4(qc.z, qc.w, qc.x, qc.y) : qc;
         }
         if (cb == 0) p.sq[slot] = sq;
       }
@@ -426,22 +486,21 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
       if (pos < g.L) {
         const uint32_t rb = (uint32_t)r * 128u + half_off;
         uint32_t kw[8];
-        *reinterpret_cast<uint4*>(kw) = *reinterpret_cast<const uint4*>(k_tile + rb + ((chunk0 ^ (uint32_t)(r & 7)) << 4));
-        *reinterpret_cast<uint4*>(kw + 4) =
-            *reinterpret_cast<const uint4*>(k_tile + rb + (((chunk0 + 1u) ^ (uint32_t)(r & 7)) << 4));
+        *reinterpret_cast<uint4*>(kw) = *reinterpret_cast<const uint4*>(k_tile + rb + ((chunk_a ^ (uint32_t)(r & 7)) << 4));
+        *reinterpret_cast<uint4*>(kw + 4) = *reinterpret_cast<const uint4*>(k_tile + rb + ((chunk_b ^ (uint32_t)(r & 7)) << 4));
         int t, hh, w;
         token_coords(p.rope, token_of(g, s, pos), t, hh, w);
         const int apos = tab_axis == 0 ? t : (tab_axis == 1 ? hh : w);
-        const float4* tp = reinterpret_cast<const float4*>(tab + tab_base + apos * tab_stride + tab_local);
+        const float4* tp = tab_lane + apos * 8;
         uint32_t* kcw = reinterpret_cast<uint32_t*>(&kc);
         uint32_t* kcw2 = reinterpret_cast<uint32_t*>(&kc2);
 #pragma unroll
         for (int m2 = 0; m2 < 4; ++m2) {
-          const float4 cs = tp[m2];
+          const float4 cs = tp[(tab_sigma + m2) & 7];
           const float2 ka = rope_rotate(bf16lo(kw[2 * m2]), bf16hi(kw[2 * m2]), make_float2(cs.x, cs.y));
           const float2 kb = rope_rotate(bf16lo(kw[2 * m2 + 1]), bf16hi(kw[2 * m2 + 1]), make_float2(cs.z, cs.w));
           if constexpr (SI8) {
-            // channels 4 m2 .. 4 m2 + 3 of this lane's 16: words 2 m2, 2 m2 + 1 of 8
+            // register channels 4 m2 .. 4 m2 + 3 of this lane's 16: words 2 m2, 2 m2 + 1 of 8
             uint32_t* w = m2 < 2 ? kcw : kcw2;
             w[(2 * m2) & 3] = i8x2_bf16(ka.x * ki, ka.y * ki);
             w[(2 * m2 + 1) & 3] = i8x2_bf16(kb.x * ki, kb.y * ki);
@@ -452,10 +511,10 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
       }
       if constexpr (SI8) {
         uint4* dst = reinterpret_cast<uint4*>(p.k8 + slot * QROW + cb * 32);
-        dst[0] = kc;
-        dst[1] = kc2;
+        dst[hsel] = kc;
+        dst[1 - hsel] = kc2;
       } else {
-        *reinterpret_cast<uint4*>(p.k8 + slot * QROW + cb * 16) = kc;
+        *reinterpret_cast<uint4*>(p.k8 + slot * QROW + cb * 16) = hsel ? make_uint4(kc.z, kc.w, kc.x, kc.y) : kc;
       }
     }
     // this warp has read its rows of the staged q / k for the last time: the
@@ -838,13 +897,11 @@ size_t fwd8_smem_bytes(bool si8) { return si8 ? F8Layout<true>::BYTES : F8Layout
 
 size_t fwd8_qk_row_bytes(bool si8) { return (size_t)qk_row_bytes(si8); }
 
-size_t fwd8_prep_smem_bytes(int stages, int rope_entries) { return prep_smem(stages, rope_entries); }
-
-int fwd8_prep_stages(int rope_entries, size_t optin, size_t smem_sm) {
-  const size_t one = prep_smem(1, rope_entries);
+int fwd8_prep_stages(int T, int H, int W, size_t optin, size_t smem_sm) {
+  const size_t one = prep_smem(1, T, H, W);
   if (one <= optin && 2 * (one + 1024) <= smem_sm) return 1;      // two CTAs per SM overlap their items
   for (int st = 2; st >= 1; --st)
-    if (prep_smem(st, rope_entries) <= optin) return st;
+    if (prep_smem(st, T, H, W) <= optin) return st;
   return 0;
 }
 
@@ -857,7 +914,7 @@ cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_fwd8_prep(const Fwd8Params& p, bool si8, int sms, cudaStream_t stream) {
-  const size_t smem = prep_smem(p.prep_stages, p.rope.entries);
+  const size_t smem = prep_smem(p.prep_stages, p.rope.T, p.rope.H, p.rope.W);
   auto kernel = si8 ? skiparse_fwdm8_prep_kernel : skiparse_fwd8_prep_kernel;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

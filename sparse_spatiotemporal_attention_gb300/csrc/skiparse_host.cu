@@ -648,7 +648,7 @@ int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, 
   if (any_alias({{out, tb}, {lse, lb}, {workspace, w.total}}, {{q, tb}, {k, tb}, {v, tb}})) return SKIPARSE_ERR_ALIAS;
   DeviceInfo dev;
   if ((st = device_info(dev)) != SKIPARSE_OK) return st;
-  const int prep_stages = fwd8_prep_stages(s.rope_entries, (size_t)dev.smem_optin, (size_t)dev.smem_sm);
+  const int prep_stages = fwd8_prep_stages(s.T, s.H, s.W, (size_t)dev.smem_optin, (size_t)dev.smem_sm);
   if ((size_t)dev.smem_optin < fwd8_smem_bytes(si8) || prep_stages == 0) return SKIPARSE_ERR_UNSUPPORTED;
 
   Fwd8Params p;

@@ -170,8 +170,7 @@ size_t fwd8_qk_row_bytes(bool si8);
 // ring size to launch with: 1 when two such CTAs fit on an SM (`smem_sm` bytes,
 // 1 KB reserved per CTA), else the largest (2, 1) that fits one CTA (`optin`
 // bytes); 0 when none does
-size_t fwd8_prep_smem_bytes(int stages, int rope_entries);
-int fwd8_prep_stages(int rope_entries, size_t optin, size_t smem_sm);
+int fwd8_prep_stages(int T, int H, int W, size_t optin, size_t smem_sm);
 int fwd8_units(const Geom& g);
 cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream);
 cudaError_t launch_fwd8_prep(const Fwd8Params& p, bool si8, int sms, cudaStream_t stream);
