@@ -199,40 +199,61 @@ enum F8Bar {
 
 // ---------------------------------------------------------------------------
 // max |v| per (b, head, channel): grid (B * heads, token chunks of 256), (b, head)
-// fastest so that blocks running together read whole token rows of v
+// fastest so that blocks running together read whole token rows of v. A
+// half-warp reads one 256-byte (token, head) row per load, 16 bytes a lane, and
+// each lane keeps eight rows in flight: short sequences give each block little
+// work, so the loads in flight, not the bytes, set the pace.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) skiparse_fwd8_vmax_kernel(const __grid_constant__ Fwd8Params p) {
-  __shared__ float part[4][kD8];
+constexpr int kVmaxThreads = 256;
+
+__global__ void __launch_bounds__(kVmaxThreads) skiparse_fwd8_vmax_kernel(const __grid_constant__ Fwd8Params p) {
+  constexpr int kWarps = kVmaxThreads / 32;
+  __shared__ float part[kWarps][kD8];
   const Geom& g = p.g;
   const int bh = blockIdx.x;
   const int b = bh / g.heads, head = bh - b * g.heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hw = lane >> 4, c8 = lane & 15;          // row of the pair, group of 8 channels
   const int t0 = blockIdx.y * 256;
   const int t1 = min(t0 + 256, g.N);
-  float mx[4] = {0.f, 0.f, 0.f, 0.f};
-  // four independent rows per warp and iteration: four loads in flight per lane
-  for (int i0 = t0 + warp; i0 < t1; i0 += 16) {
-    uint2 u[4];
+  float mx[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = i0 + 4 * j;
-      u[j] = i < t1 ? __ldg(reinterpret_cast<const uint2*>(p.v + (((size_t)b * g.N + i) * g.heads + head) * kD8 + lane * 4))
-                    : make_uint2(0u, 0u);
+  for (int e = 0; e < 8; ++e) mx[e] = 0.f;
+  // rows t0 + 16 j + 2 warp + hw, j = 0..15, in two batches of eight loads
+#pragma unroll
+  for (int j0 = 0; j0 < 16; j0 += 8) {
+    uint4 u[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      // rows past the end read the chunk's last row again (a max ignores repeats),
+      // so the loads carry no branch and all eight issue back to back
+      const int i = min(t0 + 16 * (j0 + j) + 2 * warp + hw, t1 - 1);
+      u[j] = __ldg(reinterpret_cast<const uint4*>(p.v + (((size_t)b * g.N + i) * g.heads + head) * kD8 + c8 * 8));
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      mx[0] = fmaxf(mx[0], fabsf(bf16lo(u[j].x)));
-      mx[1] = fmaxf(mx[1], fabsf(bf16hi(u[j].x)));
-      mx[2] = fmaxf(mx[2], fabsf(bf16lo(u[j].y)));
-      mx[3] = fmaxf(mx[3], fabsf(bf16hi(u[j].y)));
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t w4[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mx[2 * e] = fmaxf(mx[2 * e], fabsf(bf16lo(w4[e])));
+        mx[2 * e + 1] = fmaxf(mx[2 * e + 1], fabsf(bf16hi(w4[e])));
+      }
     }
   }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) part[warp][lane * 4 + e] = mx[e];
+  for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+  if (hw == 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[warp][c8 * 8 + e] = mx[e];
+  }
   __syncthreads();
-  const int d = threadIdx.x;
-  const float m = fmaxf(fmaxf(part[0][d], part[1][d]), fmaxf(part[2][d], part[3][d]));
-  atomicMax(p.vmax + (size_t)bh * kD8 + d, __float_as_uint(m));   // non-negative floats order as their bits
+  if (threadIdx.x < kD8) {
+    const int d = threadIdx.x;
+    float m = part[0][d];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, part[w][d]);
+    atomicMax(p.vmax + (size_t)bh * kD8 + d, __float_as_uint(m));   // non-negative floats order as their bits
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -909,7 +930,7 @@ int fwd8_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 
 
 cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream) {
   const dim3 grid(p.g.B * p.g.heads, (p.g.N + 255) / 256);
-  skiparse_fwd8_vmax_kernel<<<grid, 128, 0, stream>>>(p);
+  skiparse_fwd8_vmax_kernel<<<grid, kVmaxThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
