@@ -285,23 +285,31 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10, with_k1=True):
         fws = torch.empty(skp.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, T, H, W, 1, c["mode"]),
                           dtype=torch.uint8, device=dev)
 
-        def timed(kk, per_kernel=None):
+        def run(fn, per_kernel=None):
+            """ms per call of fn over `launches` calls (no per-kernel events in
+            between: they would add their own gaps); then, if asked, the
+            per-kernel breakdown from a second, traced pass."""
             for _ in range(3):
-                skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, c["mode"], stream=stream,
-                                      workspace=fws)
+                fn()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            skp.skiparse_trace_begin()
             e0.record(stream)
             for _ in range(launches):
-                skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, c["mode"], stream=stream,
-                                      workspace=fws)
+                fn()
             e1.record(stream)
             torch.cuda.synchronize()
-            kms, kcnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
             if per_kernel is not None:
+                skp.skiparse_trace_begin()
+                for _ in range(launches):
+                    fn()
+                torch.cuda.synchronize()
+                kms, kcnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
                 per_kernel.update({skp.KERNEL_NAMES[i]: kms[i] / kcnt[i] for i in range(len(kcnt)) if kcnt[i]})
             return e0.elapsed_time(e1) / launches
+
+        def timed(kk, per_kernel=None):
+            return run(lambda: skp.skiparse_attn_fwd(d["q"], d["k"], d["v"], out, lse, T, H, W, kk, c["mode"],
+                                                     stream=stream, workspace=fws), per_kernel)
 
         kern = {}
         ms = timed(c["k"], kern)
@@ -316,23 +324,13 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10, with_k1=True):
             fn = getattr(skp, call)
             ws8 = torch.empty(getattr(skp, call + "_workspace_bytes")(B, heads, N, D, T, H, W, c["k"], c["mode"]),
                               dtype=torch.uint8, device=dev)
-            for _ in range(3):
-                fn(d["q"], d["k"], d["v"], out, lse, T, H, W, c["k"], c["mode"], stream=stream, workspace=ws8)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            skp.skiparse_trace_begin()
-            e0.record(stream)
-            for _ in range(launches):
-                fn(d["q"], d["k"], d["v"], out, lse, T, H, W, c["k"], c["mode"], stream=stream, workspace=ws8)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            kms, kcnt = skp.skiparse_trace_end(len(skp.KERNEL_NAMES))
-            ms8 = e0.elapsed_time(e1) / launches
+            kern8 = {}
+            ms8 = run(lambda: fn(d["q"], d["k"], d["v"], out, lse, T, H, W, c["k"], c["mode"], stream=stream,
+                                 workspace=ws8), kern8)
             tf8 = fwd_flops(c) / (ms8 * 1e-3) / 1e12
             line[key] = {"ms_per_launch": ms8, "tflops": tf8,
                          "dtype": "e4m3" if key == "fp8" else "int8 (S) + e4m3 (P V)",
-                         "speedup_vs_bf16": ms / ms8,
-                         "kernels": {skp.KERNEL_NAMES[i]: kms[i] / kcnt[i] for i in range(len(kcnt)) if kcnt[i]}}
+                         "speedup_vs_bf16": ms / ms8, "kernels": kern8}
             if key == "fp8":
                 line[key]["pct_of_fp8_peak"] = {"burst": tf8 / (FP8_OVER_BF16 * burst),
                                                 "sustained": tf8 / (FP8_OVER_BF16 * sustained)}

@@ -152,6 +152,7 @@ cudaError_t launch_rope_table(const RopeParams& r, float2* tab, cudaStream_t str
 
 template <int D>
 __global__ void __launch_bounds__(kRopeThreads) skiparse_fwd_rope_kernel(const __grid_constant__ FwdParams p) {
+  pdl_trigger();                                     // the attention kernel may take SMs as this pass drains
   extern __shared__ float2 tab[];
   const Geom& g = p.g;
   rope_load_table(tab, p.rope_gtab, p.rope.entries, threadIdx.x, blockDim.x);
@@ -340,6 +341,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();                                        // the RoPE / pack pass's copies are complete
   auto warp_wait = [&](int i, uint32_t parity) -> bool {
     return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ctl, E + i)) != 0;
   };
@@ -656,6 +659,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) skiparse_fwd_merge_kernel(const __grid_constant__ FwdParams p) {
+  pdl_wait();                                        // the attention kernel's partials are complete
   const Geom& g = p.g;
   constexpr int CPL = D / 32;                        // channels per lane
   const int lane = threadIdx.x & 31;
@@ -707,9 +711,8 @@ cudaError_t launch_fwd_merge(const FwdParams& p, int sms, cudaStream_t stream) {
   const int rows = (p.n_items - p.n_full) / p.pieces * 256;
   int grid = (rows + 7) / 8;
   if (grid > 4 * sms) grid = 4 * sms;
-  if (p.g.D == 128) skiparse_fwd_merge_kernel<128><<<grid, 256, 0, stream>>>(p);
-  else skiparse_fwd_merge_kernel<64><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (p.g.D == 128) return launch_after_previous(skiparse_fwd_merge_kernel<128>, grid, 256, 0, stream, p);
+  return launch_after_previous(skiparse_fwd_merge_kernel<64>, grid, 256, 0, stream, p);
 }
 
 size_t fwd_smem_bytes(int D) { return D == 128 ? FwdLayout<128>::BYTES : FwdLayout<64>::BYTES; }
@@ -758,13 +761,11 @@ cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
   if (p.g.D == 128) {
     e = cudaFuncSetAttribute(skiparse_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    skiparse_fwd_kernel<128><<<grid, kFwdThreads, smem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(skiparse_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_fwd_kernel<64><<<grid, kFwdThreads, smem, stream>>>(p);
+    return launch_after_previous(skiparse_fwd_kernel<128>, grid, kFwdThreads, smem, stream, p);
   }
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(skiparse_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_after_previous(skiparse_fwd_kernel<64>, grid, kFwdThreads, smem, stream, p);
 }
 
 }  // namespace skp

@@ -294,6 +294,8 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
     }
     mbar_fence_init();
   }
+  pdl_trigger();                                     // the attention kernel may take SMs as this pass drains
+  pdl_wait();                                        // the cos/sin table (and the v maxima before it) are complete
   const PrepTab pt = prep_tab(p.rope.T, p.rope.H, p.rope.W);
   prep_load_table(tab, p.rope_gtab, p.rope, pt, threadIdx.x, blockDim.x);
   __syncthreads();
@@ -602,6 +604,7 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();                                        // the prep kernel's codes and scales are complete
   auto warp_wait = [&](int i, uint32_t parity) -> bool {
     return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ctl, E + i)) != 0;
   };
@@ -940,8 +943,7 @@ cudaError_t launch_fwd8_prep(const Fwd8Params& p, bool si8, int sms, cudaStream_
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = one_wave(kernel, p.g.B * p.g.heads * p.g.k * p.g.n_tiles, kPrepThreads, smem, sms);
-  kernel<<<grid, kPrepThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_after_previous(kernel, grid, kPrepThreads, smem, stream, p);
 }
 
 cudaError_t launch_fwd8(const Fwd8Params& p, bool si8, int grid, cudaStream_t stream) {
@@ -949,8 +951,7 @@ cudaError_t launch_fwd8(const Fwd8Params& p, bool si8, int grid, cudaStream_t st
   auto kernel = si8 ? skiparse_fwdm8_kernel : skiparse_fwd8_kernel;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kF8Threads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_after_previous(kernel, grid, kF8Threads, smem, stream, p);
 }
 
 }  // namespace skp

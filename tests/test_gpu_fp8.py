@@ -74,6 +74,7 @@ CASES = [
     (1, 2, 2, 8, 16, 1, O.SINGLE),      # k = 1: dense, L = 256
     (1, 1, 2, 16, 32, 8, O.GROUP),      # k = 8, L = 128
     (1, 1, 8, 32, 32, 4, O.SINGLE),     # L = 2048, 16 tiles
+    (1, 2, 6, 24, 8, 2, O.GROUP),       # H > W and T > W: the prep kernel's RoPE-table regions of unequal length
 ]
 
 
