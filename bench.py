@@ -25,8 +25,9 @@ Printed JSON line (rank 0):
                runs here and the step's k=1 run with --no-k1), with GB/s of
                algorithmic bytes; each with the two 8-bit forwards beside it:
                skiparse_attn_fwd_mixed8 (INT8 S, E4M3 P V) and
-               skiparse_attn_fwd_fp8 (all E4M3, against the FP8 peak taken as
-               the measured bf16 peak x the nominal FP8 / bf16 ratio).
+               skiparse_attn_fwd_fp8 (all E4M3, against a dense E4M3 GEMM
+               rate measured here with cuBLASLt, or the measured bf16 peak x
+               the nominal FP8 / bf16 ratio where torch has no FP8 GEMM).
 
 --impl reference times the oracle alone (the reference arm of this method).
 Multi-GPU: one process per GPU (torchrun, or started here for --gpus N); the
@@ -265,6 +266,36 @@ def job_tflops(world, flops_per_rank_step, ms_per_step):
     return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
+def measure_fp8_peak(dev, n=8192, reps=10):
+    """Dense E4M3 GEMM rate of this GPU: cuBLASLt through torch._scaled_mm,
+    n^3 with bf16 output, best of `reps` single launches (a burst figure, like
+    the measured bf16 peak). None when this torch build has no FP8 GEMM."""
+    import torch
+    try:
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()     # column-major operand
+        one = torch.ones((), device=dev)
+
+        def gemm():
+            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            gemm()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gemm()
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:
+        return None
+
+
 def fwd_config_lines(skp, dev, stream, peaks, launches=10, with_k1=True):
     """Forward-only throughput (RoPE pass + attention) of FWD_CONFIGS, and the
     dense k = 1 forward on the same inputs where the configuration asks for it."""
@@ -274,6 +305,12 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10, with_k1=True):
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    fp8_measured = measure_fp8_peak(dev)
+    if fp8_measured is not None:
+        fp8_peak = {"burst": fp8_measured, "source": "measured: torch._scaled_mm E4M3 8192^3, bf16 out, best of 10"}
+    else:
+        fp8_peak = {"burst": FP8_OVER_BF16 * burst,
+                    "source": "measured bf16 burst x the nominal FP8 / bf16 ratio (no FP8 GEMM in this torch)"}
     lines = []
     for c in WORKLOAD.get("fwd", FWD_CONFIGS):
         B, heads, D, T, H, W = c["B"], c["heads"], c["D"], c["T"], c["H"], c["W"]
@@ -332,8 +369,8 @@ def fwd_config_lines(skp, dev, stream, peaks, launches=10, with_k1=True):
                          "dtype": "e4m3" if key == "fp8" else "int8 (S) + e4m3 (P V)",
                          "speedup_vs_bf16": ms / ms8, "kernels": kern8}
             if key == "fp8":
-                line[key]["pct_of_fp8_peak"] = {"burst": tf8 / (FP8_OVER_BF16 * burst),
-                                                "sustained": tf8 / (FP8_OVER_BF16 * sustained)}
+                line[key]["pct_of_fp8_peak"] = {"burst": tf8 / fp8_peak["burst"], "peak": fp8_peak["burst"],
+                                                "source": fp8_peak["source"]}
             del ws8
         if c["k1"] and with_k1:
             ms1 = timed(1)
