@@ -781,11 +781,12 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         if (!bar_and<2, 256>(mbar_wait(bar(T_DPRDY), gg & 1, ctl, E + T_DPRDY))) { ok = false; break; }
         tc_fence_after();
         auto ds_phase = [&](auto F) {
+          // dP^T of chunks 0 and 1 in one TMEM round trip
+          float dp01[2][16];
+          tmem_ld16x2(tmem + lane_base + 128 + ch * 16, tmem + lane_base + 128 + 32 + ch * 16, dp01[0], dp01[1]);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            float dp[16];
-            tmem_ld16(tmem + lane_base + 128 + c * 32 + ch * 16, dp);
-            store_ds(F, p01[c], dp, c, c * 32 + ch * 16);
+            store_ds(F, p01[c], dp01[c], c, c * 32 + ch * 16);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
