@@ -30,21 +30,24 @@
 // Kernels:
 //   skiparse_fwd8_vmax_kernel   max |v| per (b, head, channel) (atomicMax on the
 //                               bits of non-negative floats into a zeroed array);
-//   skiparse_fwd8_prep_kernel   persistent CTAs, one per SM (one RoPE table each),
-//                               over (scope, 128-position tile) items: a TMA warp
+//   skiparse_fwd8_prep_kernel   persistent CTAs (two per SM when their shared
+//                               memory fits, one RoPE table copy each) over
+//                               (scope, 128-position tile) items: a TMA warp
 //                               stages the item's q and k tiles through the scope
-//                               gather in a two-slot ring; the compute warps apply
-//                               RoPE and quantize q (per row) and k (per tile),
-//                               quantize v (read one item ahead) and transpose it in
+//                               gather (one slot per CTA, or a two-slot ring with
+//                               one CTA per SM); the compute warps apply RoPE and
+//                               quantize q (per row) and k (per tile), quantize v
+//                               (read one row group ahead) and transpose it in
 //                               shared memory, all in scope-tile order, so the
 //                               attention kernel reads plain 128 x 128-byte boxes
 //                               (every 8-bit operand K-major);
 //   skiparse_fwd8_kernel        two Q tiles per CTA as the bf16 forward (softmax
-//                               warps 0-7, TMA warp 8), kind::f8f6f4 MMAs (4 per
-//                               128 x 128 product instead of 8) issued by one warp
-//                               per Q tile (9, 10); P as E4M3 codes in shared
-//                               memory, so S of the next K tile is issued as soon
-//                               as the softmax warps hold S in registers.
+//   skiparse_fwdm8_kernel       warps 0-7, TMA warp 8), kind::f8f6f4 MMAs (4 per
+//                               128 x 128 product instead of 8; the mixed recipe's
+//                               S as 8 kind::f16 MMAs) issued by one warp per Q
+//                               tile (9, 10); P as E4M3 codes in shared memory, so
+//                               S of the next K tile is issued as soon as the
+//                               softmax warps hold S in registers.
 #include "skiparse_internal.h"
 
 namespace skp {
