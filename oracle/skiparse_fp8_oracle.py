@@ -194,6 +194,35 @@ def _quantize_qk(qr, kr_scope, recipe):
     return q8, sq, k8, sk
 
 
+def _by_scopes(q8, sq, kr, v8, sv, sparse_k, mode, scale, fmt, quantize):
+    """The same per-scope steps with each scope gathered by its token ids (the
+    section's prose scopes; for N the listings' rearrange cannot split): q codes
+    and v codes as quantized over the whole tensors, k quantized per block of
+    128 consecutive keys of the scope (the last block partial), the blocked
+    attention, results scattered back to the tokens' rows. Returns out
+    (B, N, heads, D), lse and l (B, heads, N)."""
+    B, N, nh, D = q8.shape
+    out = np.empty((B, N, nh, D))
+    lse = np.empty((B, nh, N))
+    lsum = np.empty((B, nh, N))
+    for s in range(sparse_k):
+        tok = O.scope_tokens(N, sparse_k, mode, s)
+        if len(tok) == 0:
+            continue
+        for b in range(B):
+            for h in range(nh):
+                if quantize:
+                    k8, sk = quantize_blocks(kr[b, tok, h], fmt)
+                else:
+                    k8, sk = kr[b, tok, h], np.ones(len(tok))
+                o, ls, l = blocked_attention(sq[b, tok, h], sk, q8[b, tok, h], k8, v8[b, tok, h], sv[b, h], scale,
+                                             quantize_p=quantize)
+                out[b, tok, h] = o
+                lse[b, h, tok] = ls
+                lsum[b, h, tok] = l
+    return out, lse, lsum
+
+
 def skiparse_fwd_fp8(q, k, v, T, H, W, sparse_k, mode, theta=10000.0, quantize=True, recipe="int8",
                      with_l=False):
     """q, k, v: (B, N, heads, D) float64 (bf16-valued). Returns out (B, N, heads, D)
@@ -213,6 +242,9 @@ def skiparse_fwd_fp8(q, k, v, T, H, W, sparse_k, mode, theta=10000.0, quantize=T
     else:
         q8, sq = qr, np.ones(qr.shape[:-1])
         v8, sv = vv, np.ones((B, nh, D))
+    if not O.divisible(N, sparse_k, mode):
+        out, lse, l = _by_scopes(q8, sq, kr, v8, sv, sparse_k, mode, scale, fmt, quantize)
+        return (out, lse, l) if with_l else (out, lse)
     q8r, v8r = (O.rearrange(a, sparse_k, mode) for a in (q8, v8))
     krr = O.rearrange(kr, sparse_k, mode)                              # k blocks are scope blocks
     sqr = O.rearrange(sq[..., None], sparse_k, mode)[..., 0]          # (kB, L, heads)

@@ -269,3 +269,62 @@ def test_scope_rows_match_the_whole_forward(mode, recipe):
         assert np.allclose(ls, lse[b, h, tok], rtol=0, atol=1e-12)
         assert np.allclose(ll, l[b, h, tok], rtol=0, atol=1e-12)
         assert np.all(ll > 0.5)
+
+
+@pytest.mark.parametrize("recipe", F.RECIPES)
+@pytest.mark.parametrize("mode", [O.SINGLE, O.GROUP], ids=["single", "group"])
+def test_unequal_scopes_exact_without_quantization(mode, recipe):
+    """N that k (single) or k^2 (group) does not divide: the prose scopes, of
+    unequal length. With every rounding replaced by the identity the 8-bit
+    method must equal exact Skiparse attention on those scopes (the main
+    oracle, itself pinned to dense attention under the prose masks)."""
+    B, heads, D, T, H, W, k = 2, 2, 64, 3, 10, 11, 4     # N = 330: scopes of 83, 83, 82, 82 (single)
+    N = T * H * W
+    assert not O.divisible(N, k, mode)
+    rs = np.random.RandomState(41)
+    q, kk, v = (rs.randn(B, N, heads, D) for _ in range(3))
+    out, lse = F.skiparse_fwd_fp8(q, kk, v, T, H, W, k, mode, quantize=False, recipe=recipe)
+    rout, rlse = O.skiparse_fwd(q, kk, v, T, H, W, k, mode)
+    assert np.max(np.abs(out - rout)) < 1e-12
+    assert np.max(np.abs(lse - rlse)) < 1e-10
+
+
+@pytest.mark.parametrize("recipe", F.RECIPES)
+@pytest.mark.parametrize("mode", [O.SINGLE, O.GROUP], ids=["single", "group"])
+def test_scope_gathered_path_equals_the_rearrange(mode, recipe):
+    """Where the listings' rearrange applies, gathering each scope by its token
+    ids (the path unequal scopes take) gives the rearrange path's numbers."""
+    B, heads, D, T, H, W, k = 2, 2, 64, 4, 8, 16, 2       # N = 512, L = 256: two key blocks
+    N = T * H * W
+    assert O.divisible(N, k, mode)
+    rs = np.random.RandomState(43)
+    q, kk, v = (rs.randn(B, N, heads, D) for _ in range(3))
+    out, lse, l = F.skiparse_fwd_fp8(q, kk, v, T, H, W, k, mode, recipe=recipe, with_l=True)
+    fmt = "int8" if recipe == "int8" else "e4m3"
+    qr = O.apply_rope(q, T, H, W, 10000.0)
+    kr = O.apply_rope(kk, T, H, W, 10000.0)
+    q8, sq = F.quantize_rows(qr, fmt)
+    v8, sv = F.quantize_channels(v)
+    gout, glse, gl = F._by_scopes(q8, sq, kr, v8, sv, k, mode, 1.0 / math.sqrt(D), fmt, True)
+    assert np.allclose(gout, out, rtol=0, atol=1e-12)
+    assert np.allclose(glse, lse, rtol=0, atol=1e-12)
+    assert np.allclose(gl, l, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("recipe", F.RECIPES)
+def test_scope_rows_match_the_whole_forward_unequal_scopes(recipe):
+    """The row-sampled scope routine on unequal scopes (group skip, N = 330,
+    k = 4: scopes of 84, 84, 82, 80 tokens) gives the whole forward's numbers."""
+    B, heads, D, T, H, W, k, mode = 1, 2, 64, 3, 10, 11, 4, O.GROUP
+    N = T * H * W
+    rs = np.random.RandomState(45)
+    q, kk, v = (rs.randn(B, N, heads, D) for _ in range(3))
+    out, lse, l = F.skiparse_fwd_fp8(q, kk, v, T, H, W, k, mode, recipe=recipe, with_l=True)
+    for s in range(k):
+        Ls = len(O.scope_tokens(N, k, mode, s))
+        rows = np.array([0, 1, Ls // 2, Ls - 1])
+        for h in range(heads):
+            tok, o, ls, ll = F.skiparse_fwd_fp8_scope(q, kk, v, T, H, W, k, mode, 0, h, s, rows, recipe=recipe)
+            assert np.allclose(o, out[0, tok, h], rtol=0, atol=1e-12)
+            assert np.allclose(ls, lse[0, h, tok], rtol=0, atol=1e-12)
+            assert np.allclose(ll, l[0, h, tok], rtol=0, atol=1e-12)
