@@ -50,7 +50,7 @@ typedef enum { SKIPARSE_SINGLE = 0, SKIPARSE_GROUP = 1 } skiparse_mode_t;
 typedef enum {
   SKIPARSE_OK = 0,
   SKIPARSE_ERR_INVALID_ARG = -1,    /* NULL pointer, negative size, bad mode or theta */
-  SKIPARSE_ERR_SHAPE = -2,          /* N != T*H*W; for the 8-bit forwards also N % k (single) or N % k^2 (group) */
+  SKIPARSE_ERR_SHAPE = -2,          /* N != T*H*W */
   SKIPARSE_ERR_UNSUPPORTED = -3,    /* D not 64/128, group k not dividing 128, RoPE table too large,
                                        B * N * heads >= 2^31 */
   SKIPARSE_ERR_ALIGNMENT = -4,      /* a pointer not 16-byte aligned */
@@ -147,9 +147,11 @@ int skiparse_attn_bwd_scopes(const void* q, const void* k, const void* v, const 
  * its own workspace (..._workspace_bytes(...) bytes, 256-byte aligned, owned
  * by the caller, contents undefined on return); SKIPARSE_ERR_UNSUPPORTED for
  * D != 128 and, as for every entry point, a RoPE table over 8192 pairs
- * (16 T + 24 (H + W) for D = 128); SKIPARSE_ERR_SHAPE when k (single) or k*k
- * (group) does not divide N (their workspace size is then 0). The outputs approximate the bf16 forward
- * to the accuracy of 8-bit operands (a few percent relative).
+ * (16 T + 24 (H + W) for D = 128). Any N, as skiparse_attn_fwd: when k
+ * (single) or k*k (group) does not divide N the scopes are the prose scopes of
+ * unequal length, and the workspace also holds scope-ordered bf16 copies of
+ * q, k and v. The outputs approximate the bf16 forward to the accuracy of
+ * 8-bit operands (a few percent relative).
  */
 size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W,
                                              int sparse_k, int mode);

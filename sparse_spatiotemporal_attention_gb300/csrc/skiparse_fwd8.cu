@@ -330,12 +330,13 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
         int tile, s, sidx, b, head;
         decode(item, tile, s, sidx, b, head);
         const uint32_t dst = smem_u32(ring + (size_t)st * kPrepStage);
-        const int row = b * g.Nn + (tile * kTile) / g.G;
+        // through the scope gather, or (unequal scopes) the scope-ordered copies
+        const TileCoord tc = scope_tile(g, s, b, tile * kTile);
         mbar_expect_tx(bar(st), kPrepStage);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          tma_load_5d(dst + h * kPrepHalf, &p.tm_q, bar(st), h * 64, head, 0, s, row);
-          tma_load_5d(dst + (2 + h) * kPrepHalf, &p.tm_k, bar(st), h * 64, head, 0, s, row);
+          load_tile(dst + h * kPrepHalf, &p.tm_q, bar(st), tc, h * 64, head);
+          load_tile(dst + (2 + h) * kPrepHalf, &p.tm_k, bar(st), tc, h * 64, head);
         }
         ++issued[st];
       }
@@ -368,12 +369,12 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
   const int tab_axis = pair_select(p.rope, 8 * cb).axis;   // D = 128: pairs 0-15 t, 16-39 h, 40-63 w
   const float4* tab_lane = tab + (size_t)prep_lb(pt, nibble(kTabRegion, cb)) * 8;
   const int tab_sigma = nibble(kTabSigma, cb);
-  auto load_v = [&](int tile, int s, int b, int head, int i, uint2 (&vv)[4]) {
+  auto load_v = [&](int tile, int s, int Ls, int b, int head, int i, uint2 (&vv)[4]) {
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
       const int pos = tile * kTile + 4 * (warp + 8 * i) + rr;
       vv[rr] = make_uint2(0u, 0u);
-      if (pos < g.L) {
+      if (pos < Ls) {
         const int tok = token_of(g, s, pos);
         vv[rr] = __ldg(reinterpret_cast<const uint2*>(p.v + (((size_t)b * g.N + tok) * g.heads + head) * kD8 + lane * 4));
       }
@@ -385,8 +386,9 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
     int tile, s, sidx, b, head;
     decode(item, tile, s, sidx, b, head);
     const int bh = sidx / g.k;
+    const int Ls = scope_len(g, s);                  // rows at or past it get zero codes
     uint2 vcur[4];
-    load_v(tile, s, b, head, 0, vcur);               // in flight while the staged tiles land
+    load_v(tile, s, Ls, b, head, 0, vcur);           // in flight while the staged tiles land
     float inv_v[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -403,13 +405,13 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
     for (int i = 0; i < 4; ++i) {
       const int r0 = 4 * (warp + 8 * i);
       uint2 vnext[4] = {};
-      if (i < 3) load_v(tile, s, b, head, i + 1, vnext);
+      if (i < 3) load_v(tile, s, Ls, b, head, i + 1, vnext);
       // ---- q and k of row r0 + rq, channels 16 cb .. 16 cb + 15
       {
         const int r = r0 + rq;
         const int pos = tile * kTile + r;
         const size_t slot = (size_t)sidx * p.Lp + pos;          // scope-order row
-        const bool valid = pos < g.L;                // not warp-uniform: four rows per warp
+        const bool valid = pos < Ls;                 // not warp-uniform: four rows per warp
         uint4 qc = make_uint4(0u, 0u, 0u, 0u), qc2 = make_uint4(0u, 0u, 0u, 0u);
         float sq = 0.f;
         float qr[16];
@@ -509,7 +511,7 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
       const int pos = tile * kTile + r;
       const size_t slot = (size_t)sidx * p.Lp + pos;
       uint4 kc = make_uint4(0u, 0u, 0u, 0u), kc2 = make_uint4(0u, 0u, 0u, 0u);
-      if (pos < g.L) {
+      if (pos < Ls) {
         const uint32_t rb = (uint32_t)r * 128u + half_off;
         uint32_t kw[8];
         *reinterpret_cast<uint4*>(kw) = *reinterpret_cast<const uint4*>(k_tile + rb + ((chunk_a ^ (uint32_t)(r & 7)) << 4));
@@ -594,6 +596,16 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
   const Geom& g = p.g;
   const int n_pairs = (g.n_tiles + 1) >> 1;
   constexpr int E = ERR_KERNEL_FWD + 0x80;
+  // unit u = (scope index sidx, Q-tile pair); false for a pair past a shorter
+  // scope's end (every role skips it alike)
+  auto unit_of = [&](int u, int& pair, int& sidx, int& nt, int& Ls) -> bool {
+    pair = u % n_pairs;
+    sidx = u / n_pairs;
+    const int s = sidx % g.k;
+    nt = scope_tiles(g, s);
+    Ls = scope_len(g, s);
+    return 2 * pair < nt;
+  };
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -624,8 +636,9 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
     uint32_t gk = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-      const int pair = u % n_pairs, sidx = u / n_pairs;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      int pair, sidx, nt, Ls;
+      if (!unit_of(u, pair, sidx, nt, Ls)) continue;
       if (it > 0 && !warp_wait(E_QEMPTY, (it - 1) & 1)) break;
       if (leader) {
         mbar_expect_tx(bar(E_QFULL), 2 * Ly::QK);
@@ -642,7 +655,7 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
       }
       __syncwarp();
       ++q_issued;
-      for (int j = 0; j < g.n_tiles; ++j) {
+      for (int j = 0; j < nt; ++j) {
         const uint32_t gg = gk + j;
         const int st = gg & 1;
         const uint32_t n = gg >> 1;
@@ -667,7 +680,8 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
         __syncwarp();
         ++v_issued[st];
       }
-      gk += g.n_tiles;
+      gk += nt;
+      ++it;
     }
     if (leader) {
       if (q_issued) mbar_drain(bar(E_QFULL), (q_issued - 1) & 1);
@@ -723,8 +737,9 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
     uint32_t g0 = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-      const int n = g.n_tiles;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      int pair, sidx, n, Ls;
+      if (!unit_of(u, pair, sidx, n, Ls)) continue;
       if (!warp_wait(E_QFULL, it & 1)) break;
       if (!warp_wait(E_KFULL0 + (g0 & 1), (g0 >> 1) & 1)) break;
       if (g0 > 0 && !warp_wait(barSF, (g0 - 1) & 1)) break;
@@ -765,6 +780,7 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
         __syncwarp();
       }
       g0 += n;
+      ++it;
     }
     if (leader) {
       tc_commit(bar(E_FINAL));
@@ -786,10 +802,10 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
     // this thread's row of P (128 codes, 128-byte swizzled rows as TMA writes them)
     uint8_t* prow_smem = smem + (wg ? Ly::PB_OFF : Ly::PA_OFF) + r * 128;
     uint32_t g0 = 0;
-    int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++it) {
-      const int pair = u % n_pairs, sidx = u / n_pairs;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      int pair, sidx, nt, Ls;
+      if (!unit_of(u, pair, sidx, nt, Ls)) continue;
       const int tile = 2 * pair + wg;
       const int prow = tile * kTile + r;
       // scaled score in log2 units = S * sq_row * sk_tile * scale * log2 e
@@ -797,12 +813,12 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
       const float crow = prow < p.Lp ? p.sq[(size_t)sidx * p.Lp + prow] * p.scale_log2 : 0.f;
       const float* skt = p.sk + (size_t)sidx * g.n_tiles;
       float m = 0.f, l = 0.f;          // l in units of 2^6 P
-      for (int j = 0; j < g.n_tiles; ++j) {
+      for (int j = 0; j < nt; ++j) {
         const uint32_t gg = g0 + j;
         const float ck = crow * __ldg(skt + j);
         if (!mbar_wait(bar(barS), gg & 1, ctl, E + barS)) { ok = false; break; }
         tc_fence_after();
-        const int valid = min(kTile, g.L - j * kTile);
+        const int valid = min(kTile, Ls - j * kTile);
         // the whole S row in registers with one TMEM round trip
         float x[kTile];
         tmem_ld128(tmem + lane_base + colS, x);
@@ -867,12 +883,12 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
       }
       if (!ok) break;
       // ---- epilogue: out = O * s_v / l (l and O both in units of 2^6 P); LSE natural log
-      const uint32_t glast = g0 + g.n_tiles - 1;
+      const uint32_t glast = g0 + nt - 1;
       if (!mbar_wait(bar(barO), glast & 1, ctl, E + barO)) break;
       tc_fence_after();
       const int s = sidx % g.k, bh = sidx / g.k;
       const int b = bh / g.heads, head = bh - b * g.heads;
-      const bool row_ok = prow < g.L;
+      const bool row_ok = prow < Ls;
       const int tok = row_ok ? token_of(g, s, prow) : 0;
       const float inv_l = 1.0f / (l * kE4M3Max);
       const unsigned* vm = p.vmax + (size_t)bh * D;
@@ -901,7 +917,7 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(barOE));
-      g0 += g.n_tiles;
+      g0 += nt;
     }
   }
 

@@ -399,9 +399,11 @@ bool encode_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, 
 
 // 8-bit forward workspace: q, k codes (scopes, Lp, 128) (E4M3 bytes, or INT8
 // codes as bf16 for the mixed recipe) and E4M3 V^T (scopes, 128, Lp), q scales
-// per scope-order row, k scales per K tile, max |v| per (b, head, channel).
+// per scope-order row, k scales per K tile, max |v| per (b, head, channel),
+// the cos/sin table; for scopes of unequal length, scope-ordered bf16 copies
+// of q, k and v (the prep kernel's tile loads read q and k from them).
 struct Ws8Layout {
-  size_t q8, k8, vt8, sq, sk, vmax, tab, total;
+  size_t q8, k8, vt8, sq, sk, vmax, tab, copies, total;
   int Lp, scopes;
 };
 
@@ -419,6 +421,8 @@ Ws8Layout ws8_layout(const Shape& s, bool si8) {
   w.sk = off;   off += align256((size_t)w.scopes * (w.Lp / kTile) * 4);
   w.vmax = off; off += align256((size_t)s.B * s.heads * 128 * 4);
   w.tab = off;  off += align256((size_t)kMaxRopeEntries * sizeof(float2));
+  const Geom g = make_geom(s);
+  w.copies = off; off += g.packed ? 3 * align256(packed_bytes(g)) : 0;
   w.total = off;
   return w;
 }
@@ -613,7 +617,6 @@ size_t skiparse_attn_fwd_fp8_workspace_bytes(int B, int heads, int N, int D, int
                                              int mode) {
   Shape s;
   if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty || D != 128) return 0;
-  if (make_geom(s).packed) return 0;
   return ws8_layout(s, false).total;
 }
 
@@ -621,7 +624,6 @@ size_t skiparse_attn_fwd_mixed8_workspace_bytes(int B, int heads, int N, int D, 
                                                 int mode) {
   Shape s;
   if (check_shape(B, heads, N, D, T, H, W, sparse_k, mode, 10000.0f, s) != SKIPARSE_OK || s.empty || D != 128) return 0;
-  if (make_geom(s).packed) return 0;
   return ws8_layout(s, true).total;
 }
 
@@ -637,8 +639,6 @@ int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, 
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
   if (D != 128) return SKIPARSE_ERR_UNSUPPORTED;
-  // the 8-bit preparation gathers q and k through the scope maps: equal scopes only
-  if (make_geom(s).packed) return SKIPARSE_ERR_SHAPE;
   if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
   const Ws8Layout w = ws8_layout(s, si8);
@@ -678,13 +678,35 @@ int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, 
                                encode_bf16_3d(&p.tm_k8, p.k8, 128, Lp, sc, 256, 256 * Lp)
                          : encode_bytes_3d(&p.tm_q8, p.q8, 128, Lp, sc, 128, 128 * Lp) &&
                                encode_bytes_3d(&p.tm_k8, p.k8, 128, Lp, sc, 128, 128 * Lp);
-  if (!qk_ok || !encode_bytes_3d(&p.tm_vt, p.vt8, Lp, 128, sc, Lp, 128 * Lp) || !encode_scope_map(&p.tm_q, q, p.g) ||
-      !encode_scope_map(&p.tm_k, k, p.g))
-    return SKIPARSE_ERR_LAUNCH;
+  // q and k tiles for the prep kernel: through the scope gather, or (unequal
+  // scopes, which no gather map can bound) from scope-ordered copies that the
+  // pack pass writes, unrotated (the prep kernel applies RoPE itself)
+  FwdParams pk;
+  std::memset(&pk, 0, sizeof(pk));
+  if (p.g.packed) {
+    const size_t pb = align256(packed_bytes(p.g));
+    pk.g = p.g;
+    pk.rope = p.rope;
+    pk.q = p.q;
+    pk.k = p.k;
+    pk.v = p.v;
+    pk.qr = reinterpret_cast<uint16_t*>(ws + w.copies);
+    pk.kr = reinterpret_cast<uint16_t*>(ws + w.copies + pb);
+    pk.vr = reinterpret_cast<uint16_t*>(ws + w.copies + 2 * pb);
+    pk.rotate = 0;
+    pk.err = dev.err_word;
+  }
+  const bool maps_ok = p.g.packed ? encode_packed_map(&p.tm_q, pk.qr, p.g) && encode_packed_map(&p.tm_k, pk.kr, p.g)
+                                  : encode_scope_map(&p.tm_q, q, p.g) && encode_scope_map(&p.tm_k, k, p.g);
+  if (!qk_ok || !encode_bytes_3d(&p.tm_vt, p.vt8, Lp, 128, sc, Lp, 128 * Lp) || !maps_ok) return SKIPARSE_ERR_LAUNCH;
   const int grid = p.n_units < dev.sms ? p.n_units : dev.sms;
   if (cudaMemsetAsync(p.vmax, 0, (size_t)B * heads * 128 * 4, stream) != cudaSuccess) return launch_status(cudaErrorUnknown);
   st = launch_status(traced_launch(5, stream, [&] { return launch_fwd8_vmax(p, stream); }));
   if (st != SKIPARSE_OK) return st;
+  if (p.g.packed) {
+    st = launch_status(traced_launch(4, stream, [&] { return launch_fwd_pack(pk, 8 * dev.sms, dev.sms, stream); }));
+    if (st != SKIPARSE_OK) return st;
+  }
   st = launch_status(launch_rope_table(p.rope, p.rope_gtab, stream));
   if (st != SKIPARSE_OK) return st;
   st = launch_status(traced_launch(si8 ? 9 : 6, stream, [&] { return launch_fwd8_prep(p, si8, dev.sms, stream); }));

@@ -153,7 +153,7 @@ def test_bwd_saved_validation(lib):
 
 def test_ragged_workspace_sizes(lib):
     """Scopes of unequal length read scope-ordered copies (k, B, Lp, heads, D) of
-    q, k, v (forward) and of q, k, v, dO (backward); the 8-bit forwards refuse them."""
+    q, k, v (forward, both 8-bit forwards too) and of q, k, v, dO (backward)."""
     B, heads, D, N, k = 1, 2, 64, 192, 5                 # single skip: L_0 = 39, Lp = 128
     copy = k * B * 128 * heads * D * 2
     assert lib.skiparse_attn_fwd_workspace_bytes(B, heads, N, D, 3, 8, 8, k, 0) == 3 * copy + fwd_parts(D, 10)
@@ -161,10 +161,13 @@ def test_ragged_workspace_sizes(lib):
     want = stats * D * 4 + 4 * copy + 2 * stats * 4
     got = lib.skiparse_attn_bwd_workspace_bytes(B, heads, N, D, 3, 8, 8, k, 0)
     assert want <= got <= want + 8 * 256 + 16 * 8192
-    assert lib.skiparse_attn_fwd_fp8_workspace_bytes(1, 2, 192, 128, 3, 8, 8, 5, 0) == 0
-    assert lib.skiparse_attn_fwd_mixed8_workspace_bytes(1, 2, 192, 128, 3, 8, 8, 5, 0) == 0
+    copy128 = k * 1 * 128 * 2 * 128 * 2                  # B = 1, heads = 2, D = 128
+    for fn in ("skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_mixed8_workspace_bytes"):
+        ws8 = getattr(lib, fn)(1, 2, 192, 128, 3, 8, 8, k, 0)
+        equal = getattr(lib, fn)(1, 2, 192, 128, 3, 8, 8, 4, 0)   # k = 4 divides 192
+        assert ws8 >= 3 * copy128 and equal > 0
     assert lib.skiparse_attn_fwd_fp8(A, 2 * A, 3 * A, 4 * A, 5 * A, 10 * A, 1 << 30, 1, 2, 192, 128, 3, 8, 8, 5, 0,
-                                     10000.0, None) == SHAPE
+                                     10000.0, None) == DEVICE
 
 
 def test_scope_subset_validation(lib):
