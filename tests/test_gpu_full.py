@@ -104,3 +104,33 @@ def test_full_training_step_sampled(env):
         assert np.all(np.isfinite(got[n])), n
     st, detail = skp.skiparse_device_error()
     assert st == 0, hex(detail)
+
+
+def test_full_training_step_sampled_unequal_scopes(env):
+    """The training step at a size next to the bench's with N that k^2 does not
+    divide (23x22x41: N = 20,746, scopes of 5,188, 5,188, 5,186 and 5,184
+    tokens): forward and backward through the scope-ordered copies, whole
+    scopes of two (batch, head) pairs against the oracle."""
+    skp, dev = env
+    B, heads, D, (T, H, W), k, mode = 2, 24, 128, (23, 22, 41), 4, O.GROUP
+    N = T * H * W
+    assert not O.divisible(N, k, mode)
+    ins = inputs(B, N, heads, D, True)
+    fw = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode, guard=False)
+    bw = tl.run_bwd(skp, dev, ins, fw, B, heads, N, D, T, H, W, k, mode, guard=False)
+    got = {n: bw[n].float().cpu().numpy() for n in ("dq", "dk", "dv")}
+    got["out"] = fw["out"].float().cpu().numpy()
+    got_lse = fw["lse"].cpu().numpy()
+    for b, h, s in [(0, 5, 0), (1, 17, 3)]:
+        sub = {n: _slice(ins[n], b, h) for n in ("q", "k", "v", "do")}
+        r = O.skiparse_scope(sub["q"], sub["k"], sub["v"], sub["do"], T, H, W, k, mode, 0, 0, s)
+        tok = r["tokens"]
+        assert len(tok) == len(O.prose_scope_tokens(N, k, mode, s))
+        for n in ("out", "dq", "dk", "dv"):
+            tl.compare(f"unequal {n} b{b} h{h} s{s}", got[n][b, tok, h], r[n])
+        tl.compare(f"unequal lse b{b} h{h} s{s}", got_lse[b, h, tok], r["lse"], tol_max=tl.TOL_LSE,
+                   tol_mean=tl.TOL_LSE, tol_rel=1e-3)
+    for n in ("dq", "dk", "dv"):
+        assert np.all(np.isfinite(got[n])), n
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
