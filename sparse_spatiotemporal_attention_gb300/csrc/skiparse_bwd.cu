@@ -15,29 +15,23 @@
 //                dV  += P^T dO           dK~ += dS^T Q~          dQ~_part = dS K~
 //              P^T = exp(S^T * scale - lse), dS^T = P^T * (dP^T - delta).
 //              dQ~_part is added into the fp32 accumulator (scope order) by
-//              bulk reduce-adds (D = 128) or vector atomics (D = 64).
+//              bulk reduce-adds.
 //              Epilogue: dv, and dk = scale * R^T dK~, stored at original rows.
 //  post        dq = R^T (scale * dQ~_acc) -> bf16.
-// Two main kernels share that plan. D = 128 (the 18-warp tile kernel):
+// One main kernel for D = 128 and D = 64 (18 warps):
 //   warps 0-7   P^T / dS^T in four 32-query chunks (one key row, 16 queries of
 //               a chunk per thread) and the dK / dV epilogue;
 //   warps 8-15  dQ~^T out of TMEM (one channel, 64 queries per thread), staged
 //               in the tile's dead Q~ / dO slots and bulk-added to the accumulator;
 //   warp 16     TMA producer (K~, V per unit; Q~, dO, lse, delta per Q tile);
-//   warp 17     MMA issuer; every MMA has M = N = 128.
-// D = 64 (the 10-warp kernel): warps 0-3 P^T / dS^T and the epilogue, warps
-// 4-7 one query row each for the dQ~ adds (vector atomics), warp 8 TMA, warp 9 MMA.
+//   warp 17     MMA issuer; every MMA has M = 128 and N = 128 or D.
 // TMEM columns: S^T (P^T as bf16) 0..127, dP^T / dQ~ partial 128..255,
-// dV 256..383, dK~ 384..511.
+// dV from 256, dK~ from 384 (D columns each).
 #include <type_traits>
 
 #include "skiparse_internal.h"
 
 namespace skp {
-
-// ===========================================================================
-// main kernel for D = 64: 128-query tiles, dQ~ added by four of its warps
-// ===========================================================================
 
 template <int D>
 struct BwdLayout {
@@ -53,14 +47,6 @@ struct BwdLayout {
   static constexpr int BYTES = DS_OFF + DS_BYTES;
 };
 
-enum BwdBar {
-  B_KVFULL, B_KVEMPTY, B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1, B_SFULL, B_DSREADY, B_DSFREE,
-  B_DQFULL, B_DQFREE, B_DKVDONE, B_DKVFREE, B_FINAL, B_NBARS
-};
-
-constexpr int kBwdThreads = 320;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
-
 __device__ __forceinline__ void decode_unit_bwd(const Geom& g, int u, int& b, int& head, int& s, int& tile) {
   tile = u % g.n_tiles;
   int r = u / g.n_tiles;
@@ -68,301 +54,6 @@ __device__ __forceinline__ void decode_unit_bwd(const Geom& g, int u, int& b, in
   r /= g.ks;
   head = r % g.heads;
   b = r / g.heads;
-}
-
-template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1) skiparse_bwd_main_kernel(const __grid_constant__ BwdParams p) {
-  using Ly = BwdLayout<D>;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  if ((smem_u32(smem) & 1023u) != 0) {
-    if (tid == 0) atomicCAS(p.err, 0, ERR_SMEM_ALIGN);
-    return;
-  }
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
-  int* abort_flag = reinterpret_cast<int*>(smem + 520);
-  float* stats = reinterpret_cast<float*>(smem + Ly::STATS_OFF);
-  const uint32_t sK = smem_u32(smem + Ly::K_OFF);
-  const uint32_t sV = smem_u32(smem + Ly::V_OFF);
-  const uint32_t sQ = smem_u32(smem + Ly::Q_OFF);
-  const uint32_t sDO = smem_u32(smem + Ly::DO_OFF);
-  const uint32_t sDS = smem_u32(smem + Ly::DS_OFF);
-  const uint32_t bar0 = smem_u32(bars);
-  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
-  const Ctl ctl{abort_flag, p.err};
-  const Geom& g = p.g;
-
-  if (tid == 0) {
-    *abort_flag = 0;
-    const uint32_t counts[B_NBARS] = {1, 1, 1, 1, 1, 1, 1, 4, 1, 1, 4, 1, 4, 1};
-    for (int i = 0; i < B_NBARS; ++i) mbar_init(bar(i), counts[i]);
-    mbar_fence_init();
-  }
-  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_map(&p.tm_q);
-      tma_prefetch_map(&p.tm_k);
-      tma_prefetch_map(&p.tm_v);
-      tma_prefetch_map(&p.tm_do);
-      uint32_t kv_issued = 0, q_issued[2] = {0, 0};
-      uint32_t g0 = 0;
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        int b, head, s, kt;
-        decode_unit_bwd(g, u, b, head, s, kt);
-        const int nt = scope_tiles(g, s);
-        if (kt >= nt) continue;                       // a shorter scope has fewer key tiles
-        if (it > 0 && !mbar_wait(bar(B_KVEMPTY), (it - 1) & 1, ctl, ERR_KERNEL_BWD + B_KVEMPTY)) break;
-        mbar_expect_tx(bar(B_KVFULL), 2 * Ly::TILE);
-        const TileCoord tck = scope_tile(g, s, b, kt * kTile);
-#pragma unroll
-        for (int h = 0; h < Ly::HALVES; ++h) {
-          load_tile(sK + h * kHalfBytes, &p.tm_k, bar(B_KVFULL), tck, h * 64, head);
-          load_tile(sV + h * kHalfBytes, &p.tm_v, bar(B_KVFULL), tck, h * 64, head);
-        }
-        ++kv_issued;
-        const size_t srow = (((size_t)b * g.heads + head) * g.k + s) * p.Lp;
-        for (int i = 0; i < nt; ++i) {
-          const uint32_t gg = g0 + i;
-          const int st = gg & 1;
-          const uint32_t n = gg >> 1;
-          if (n > 0 && !mbar_wait(bar(B_QEMPTY0 + st), (n - 1) & 1, ctl, ERR_KERNEL_BWD + B_QEMPTY0 + st)) { ok = false; break; }
-          mbar_expect_tx(bar(B_QFULL0 + st), 2 * Ly::TILE + 1024);
-          const TileCoord tci = scope_tile(g, s, b, i * kTile);
-#pragma unroll
-          for (int h = 0; h < Ly::HALVES; ++h) {
-            load_tile(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(B_QFULL0 + st), tci, h * 64, head);
-            load_tile(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(B_QFULL0 + st), tci, h * 64, head);
-          }
-          const uint32_t dst = smem_u32(stats + st * 256);
-          bulk_load(dst, p.lse2s + srow + i * kTile, 512, bar(B_QFULL0 + st));
-          bulk_load(dst + 512, p.delta_s + srow + i * kTile, 512, bar(B_QFULL0 + st));
-          ++q_issued[st];
-        }
-        g0 += nt;
-        ++it;
-      }
-      if (kv_issued) mbar_drain(bar(B_KVFULL), (kv_issued - 1) & 1);
-      for (int st = 0; st < 2; ++st)
-        if (q_issued[st]) mbar_drain(bar(B_QFULL0 + st), (q_issued[st] - 1) & 1);
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
-      constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO (MN-major)
-      constexpr uint32_t kIdDK = idesc_bf16(128, D, false, true);     // dS^T (K-major) x Q~ (MN-major)
-      constexpr uint32_t kIdDQ = idesc_bf16(128, D, true, true);      // dS (MN-major) x K~ (MN-major)
-      uint32_t g0 = 0;
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        int b, head, s, kt;
-        decode_unit_bwd(g, u, b, head, s, kt);
-        const int nt = scope_tiles(g, s);
-        if (kt >= nt) continue;
-        if (!mbar_wait(bar(B_KVFULL), it & 1, ctl, ERR_KERNEL_BWD + B_KVFULL)) break;
-        if (it > 0 && !mbar_wait(bar(B_DKVFREE), (it - 1) & 1, ctl, ERR_KERNEL_BWD + B_DKVFREE)) break;
-        tc_fence_after();
-        for (int i = 0; i < nt; ++i) {
-          const uint32_t gg = g0 + i;
-          const int st = gg & 1;
-          const uint32_t n = gg >> 1;
-          if (!mbar_wait(bar(B_QFULL0 + st), n & 1, ctl, ERR_KERNEL_BWD + B_QFULL0 + st)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t qt = sQ + st * Ly::TILE;
-          const uint32_t dot = sDO + st * Ly::TILE;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tmem + kColS, desc_kmajor(sK, ks), desc_kmajor(qt, ks), kIdS, ks > 0 ? 1u : 0u);
-          if (gg > 0 && !mbar_wait(bar(B_DQFREE), (gg - 1) & 1, ctl, ERR_KERNEL_BWD + B_DQFREE)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tmem + kColDP, desc_kmajor(sV, ks), desc_kmajor(dot, ks), kIdS, ks > 0 ? 1u : 0u);
-          tc_commit(bar(B_SFULL));
-          if (!mbar_wait(bar(B_DSREADY), gg & 1, ctl, ERR_KERNEL_BWD + B_DSREADY)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ts(tmem + kColDV, tmem + kColS + ks * 8, desc_mnmajor(dot, ks), kIdDV, (i > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ss(tmem + kColDK, desc_kmajor(sDS, ks), desc_mnmajor(qt, ks), kIdDK, (i > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ss(tmem + kColDP, desc_mnmajor(sDS, ks), desc_mnmajor(sK, ks), kIdDQ, ks > 0 ? 1u : 0u);
-          tc_commit(bar(B_DQFULL));
-          tc_commit(bar(B_QEMPTY0 + st));
-          tc_commit(bar(B_DSFREE));
-        }
-        if (!ok) break;
-        tc_commit(bar(B_DKVDONE));
-        tc_commit(bar(B_KVEMPTY));
-        g0 += nt;
-        ++it;
-      }
-      tc_commit(bar(B_FINAL));
-      mbar_drain(bar(B_FINAL), 0);
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ dQ warps
-    const int qi = tid - 128;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    uint32_t g0 = 0;
-    int it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      int b, head, s, kt;
-      decode_unit_bwd(g, u, b, head, s, kt);
-      const int nt = scope_tiles(g, s);
-      if (kt >= nt) continue;
-      const int Ls = scope_len(g, s);
-      for (int i = 0; i < nt; ++i) {
-        const uint32_t gg = g0 + i;
-        if (!mbar_wait(bar(B_DQFULL), gg & 1, ctl, ERR_KERNEL_BWD + B_DQFULL)) { ok = false; break; }
-        tc_fence_after();
-        const int prow = i * kTile + qi;
-        const bool row_ok = prow < Ls;
-        float* dst = p.dq_acc + ((((size_t)b * g.heads + head) * g.k + s) * p.Lp + prow) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float x[32];
-          tmem_ld32(tmem + lane_base + kColDP + c * 32, x);
-          if (row_ok) {
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + q4 * 4),
-                        make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]));
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_DQFREE));
-      }
-      g0 += nt;
-      ++it;
-    }
-  } else {
-    // ------------------------------------------------------------ P^T / dS^T warps
-    const int j = tid;                                       // key row of the K/V tile = TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const float sl2 = p.scale_log2;
-    uint8_t* ds_row = smem + Ly::DS_OFF + j * 128;
-    uint32_t g0 = 0;
-    int it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      int b, head, s, kt;
-      decode_unit_bwd(g, u, b, head, s, kt);
-      const int nt = scope_tiles(g, s);
-      if (kt >= nt) continue;
-      const int Ls = scope_len(g, s);
-      const bool key_ok = kt * kTile + j < Ls;
-      for (int i = 0; i < nt; ++i) {
-        const uint32_t gg = g0 + i;
-        const int st = gg & 1;
-        if (!mbar_wait(bar(B_SFULL), gg & 1, ctl, ERR_KERNEL_BWD + B_SFULL)) { ok = false; break; }
-        if (gg > 0 && !mbar_wait(bar(B_DSFREE), (gg - 1) & 1, ctl, ERR_KERNEL_BWD + B_DSFREE)) { ok = false; break; }
-        tc_fence_after();
-        const float* lse2 = stats + st * 256;
-        const float* delta = lse2 + 128;
-        const int qvalid = key_ok ? min(kTile, Ls - i * kTile) : 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float sv[32], dp[32];
-          tmem_ld32(tmem + lane_base + kColS + c * 32, sv);
-          tmem_ld32(tmem + lane_base + kColDP + c * 32, dp);
-          uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int q0 = c * 32 + 2 * e;
-            const float p0 = q0 < qvalid ? ex2(fmaf(sv[2 * e], sl2, -lse2[q0])) : 0.f;
-            const float p1 = q0 + 1 < qvalid ? ex2(fmaf(sv[2 * e + 1], sl2, -lse2[q0 + 1])) : 0.f;
-            const float d0 = q0 < qvalid ? p0 * (dp[2 * e] - delta[q0]) : 0.f;
-            const float d1 = q0 + 1 < qvalid ? p1 * (dp[2 * e + 1] - delta[q0 + 1]) : 0.f;
-            pk[e] = pack_bf16(p0, p1);
-            dk[e] = pack_bf16(d0, d1);
-          }
-          tmem_st16(tmem + lane_base + kColS + c * 16, pk);
-          // dS^T row j, query columns 32c .. 32c+31: box c/2, 16-byte chunks (c%2)*4 ..
-          uint8_t* rowp = ds_row + (c >> 1) * kHalfBytes;
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int chunk = ((c & 1) * 4 + q4) ^ (j & 7);
-            *reinterpret_cast<uint4*>(rowp + chunk * 16) = make_uint4(dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2], dk[4 * q4 + 3]);
-          }
-        }
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_DSREADY));
-      }
-      if (!ok) break;
-      // ---- epilogue: dv and dk = scale * R^T dK~ at the key's original row
-      if (!mbar_wait(bar(B_DKVDONE), it & 1, ctl, ERR_KERNEL_BWD + B_DKVDONE)) break;
-      tc_fence_after();
-      const int prow = kt * kTile + j;
-      const int tok = key_ok ? token_of(g, s, prow) : 0;
-      int t = 0, hh = 0, w = 0;
-      if (key_ok) token_coords(p.rope, tok, t, hh, w);
-      const size_t rbase = (((size_t)b * g.N + tok) * g.heads + head) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float x[32];
-        tmem_ld32(tmem + lane_base + kColDV + c * 32, x);
-        if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(pack_bf16(x[8 * q4], x[8 * q4 + 1]), pack_bf16(x[8 * q4 + 2], x[8 * q4 + 3]),
-                                 pack_bf16(x[8 * q4 + 4], x[8 * q4 + 5]), pack_bf16(x[8 * q4 + 6], x[8 * q4 + 7]));
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float x[32];
-        tmem_ld32(tmem + lane_base + kColDK + c * 32, x);
-        if (key_ok) {
-          uint32_t o[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const PairSel sl = pair_select(p.rope, c * 16 + e);
-            const float2 cs = __ldg(&p.rope_tab[pair_index(sl, t, hh, w)]);
-            const float2 r = rope_rotate_t(x[2 * e] * p.scale, x[2 * e + 1] * p.scale, cs);
-            o[e] = pack_bf16(r.x, r.y);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DKVFREE));
-      g0 += nt;
-      ++it;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
 }
 
 // ===========================================================================
@@ -408,9 +99,9 @@ __device__ __forceinline__ int stagger(int i, int kt, int n) {
   return r >= n ? r - n : r;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel(const __grid_constant__ BwdParams p) {
-  using Ly = BwdLayout<128>;
-  constexpr int D = 128;
+  using Ly = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -474,7 +165,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         mbar_expect_tx(bar(T_KVFULL), 2 * Ly::TILE);
         const TileCoord tck = scope_tile(g, s, b, kt * kTile);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < Ly::HALVES; ++h) {
           load_tile(sK + h * kHalfBytes, &p.tm_k, bar(T_KVFULL), tck, h * 64, head);
           load_tile(sV + h * kHalfBytes, &p.tm_v, bar(T_KVFULL), tck, h * 64, head);
         }
@@ -496,7 +187,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         if (leader) {
           mbar_expect_tx(bar(T_QFULL0 + st), Ly::TILE + 1024);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < Ly::HALVES; ++h)
             load_tile(sQ + st * Ly::TILE + h * kHalfBytes, &p.tm_q, bar(T_QFULL0 + st), tcq, h * 64, head);
           const uint32_t dst = smem_u32(stats + st * 256);
           bulk_load(dst, p.lse2s + srow + qi * kTile, 512, bar(T_QFULL0 + st));
@@ -510,7 +201,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         if (leader) {
           mbar_expect_tx(bar(T_OFULL0 + st), Ly::TILE);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < Ly::HALVES; ++h)
             load_tile(sDO + st * Ly::TILE + h * kHalfBytes, &p.tm_do, bar(T_OFULL0 + st), tcq, h * 64, head);
         }
         __syncwarp();
@@ -533,7 +224,10 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);   // S^T, dP^T
     constexpr uint32_t kIdDV = idesc_bf16(128, D, false, true);     // P^T (TMEM) x dO (MN-major)
     constexpr uint32_t kIdDK = idesc_bf16(128, D, false, true);     // dS^T (K-major) x Q~ (MN-major)
-    constexpr uint32_t kIdDQ = idesc_bf16(D, 128, true, true);      // K~^T (MN-major) x dS^T (MN-major)
+    // dQ~^T = K~^T dS^T: M = 128 channel rows, N = 128 queries. With D = 64 the
+    // A operand's second 64-row block is the V tile (the next 16 KB): rows 64-127
+    // of the product are not used (an M = 64 product would take as many MMAs)
+    constexpr uint32_t kIdDQ = idesc_bf16(128, 128, true, true);      // K~^T (MN-major) x dS^T (MN-major)
     // k-step-0 descriptors of every operand tile; k-steps add a constant
     const uint64_t dKk = desc_kmajor(sK, 0), dKmn = desc_mnmajor(sK, 0), dVk = desc_kmajor(sV, 0);
     const uint64_t dDSk = desc_kmajor(sDS, 0), dDSmn = desc_mnmajor(sDS, 0);
@@ -657,8 +351,10 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(T_DQFREE));
         float* slot = reinterpret_cast<float*>(smem + (qh ? Ly::DO_OFF : Ly::Q_OFF) + st * Ly::TILE);
+        if (D == 128 || j < D) {                       // D = 64: TMEM lanes 64-127 hold unused rows
 #pragma unroll
-        for (int q = 0; q < 64; ++q) slot[q * D + j] = x[q];
+          for (int q = 0; q < 64; ++q) slot[q * D + j] = x[q];
+        }
         fence_proxy_async_smem();
         asm volatile("bar.sync 4, 256;" ::: "memory");
         if (leader) {
@@ -868,25 +564,22 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
   }
 }
 
-bool bwd_uses_tile_kernel(int D) { return D == 128; }
-
 size_t bwd_main_smem_bytes(int D) {
   return D == 128 ? (size_t)BwdLayout<128>::BYTES : (size_t)BwdLayout<64>::BYTES;
 }
 
-cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = bwd_main_smem_bytes(p.g.D);
-  cudaError_t e;
-  if (bwd_uses_tile_kernel(p.g.D)) {
-    e = cudaFuncSetAttribute(skiparse_bwd_main_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_bwd_main_tile_kernel<<<grid, kTileThreads, smem, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(skiparse_bwd_main_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    skiparse_bwd_main_kernel<64><<<grid, kBwdThreads, smem, stream>>>(p);
-  }
+template <int D>
+static cudaError_t launch_tile(const BwdParams& p, int grid, cudaStream_t stream) {
+  const cudaError_t e = cudaFuncSetAttribute(skiparse_bwd_main_tile_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)bwd_main_smem_bytes(D));
+  if (e != cudaSuccess) return e;
+  skiparse_bwd_main_tile_kernel<D><<<grid, kTileThreads, bwd_main_smem_bytes(D), stream>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream) {
+  return p.g.D == 128 ? launch_tile<128>(p, grid, stream) : launch_tile<64>(p, grid, stream);
 }
 
 }  // namespace skp

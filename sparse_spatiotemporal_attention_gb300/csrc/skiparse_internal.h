@@ -183,7 +183,6 @@ size_t proj_header_bytes(int rope_entries);
 cudaError_t launch_proj(const ProjParams& p, int bn, int grid, cudaStream_t stream);
 
 size_t bwd_main_smem_bytes(int D);
-bool bwd_uses_tile_kernel(int D);
 cudaError_t launch_bwd_pre(const BwdParams& p, int grid, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdParams& p, int grid, int sms, cudaStream_t stream);
