@@ -167,6 +167,25 @@ int skiparse_attn_fwd_mixed8(const void* q, const void* k, const void* v, void* 
                              int sparse_k, int mode, float rope_theta, cudaStream_t stream);
 
 /*
+ * The two 8-bit forwards over a subset of the scopes (scope_first,
+ * scope_first + scope_step, ... below sparse_k), as skiparse_attn_fwd_scopes is
+ * to skiparse_attn_fwd: only the subset's rows of out and lse are written, the
+ * workspace is the full call's, and the v scales still span all N tokens (so
+ * each scope's results equal the full call's bit for bit). Invalid subsets give
+ * SKIPARSE_ERR_INVALID_ARG; an empty one is a no-op returning SKIPARSE_OK.
+ */
+int skiparse_attn_fwd_fp8_scopes(const void* q, const void* k, const void* v, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes,
+                                 int B, int heads, int N, int D, int T, int H, int W,
+                                 int sparse_k, int mode, float rope_theta, int scope_first, int scope_step,
+                                 cudaStream_t stream);
+int skiparse_attn_fwd_mixed8_scopes(const void* q, const void* k, const void* v, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes,
+                                    int B, int heads, int N, int D, int T, int H, int W,
+                                    int sparse_k, int mode, float rope_theta, int scope_first, int scope_step,
+                                    cudaStream_t stream);
+
+/*
  * Bytes of device workspace skiparse_attn_bwd needs for these sizes: an fp32
  * dQ accumulator, rotated bf16 copies of q and k (for scopes of unequal length:
  * scope-ordered copies of q, k, v and dout), per-scope fp32 LSE and delta rows,

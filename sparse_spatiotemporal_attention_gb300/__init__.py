@@ -32,6 +32,7 @@ EXPORTS = (
     "skiparse_attn_fwd_fp8_workspace_bytes", "skiparse_attn_fwd_fp8",
     "skiparse_attn_fwd_mixed8_workspace_bytes", "skiparse_attn_fwd_mixed8",
     "skiparse_attn_fwd_scopes", "skiparse_attn_bwd_scopes",
+    "skiparse_attn_fwd_fp8_scopes", "skiparse_attn_fwd_mixed8_scopes",
     "skiparse_qkv_rope",
 )
 
@@ -76,6 +77,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "skiparse_attn_fwd_fp8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_fwd_mixed8_workspace_bytes": (_c_size, [_c_int] * 9),
         "skiparse_attn_fwd_scopes": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _c_int, _c_int, _vp]),
+        "skiparse_attn_fwd_fp8_scopes": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _c_int, _c_int, _vp]),
+        "skiparse_attn_fwd_mixed8_scopes": (_c_int,
+                                            [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _c_int, _c_int, _vp]),
         "skiparse_attn_bwd_scopes": (_c_int, [_vp] * 10 + [_c_size] + [_c_int] * 9 + [_c_float, _c_int, _c_int, _vp]),
         "skiparse_attn_fwd_mixed8": (_c_int, [_vp] * 6 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
         "skiparse_attn_bwd_saved": (_c_int, [_vp, _c_size] + [_vp] * 8 + [_c_size] + [_c_int] * 9 + [_c_float, _vp]),
@@ -153,7 +157,8 @@ def skiparse_attn_fwd_mixed8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, 
     return int(load_library().skiparse_attn_fwd_mixed8_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode))
 
 
-def _fwd8(name, q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, workspace, workspace_bytes):
+def _fwd8(name, q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, workspace, workspace_bytes,
+          subset=None):
     lib = load_library()
     B, heads, N, D = _shape(q)
     if workspace is None:
@@ -162,9 +167,14 @@ def _fwd8(name, q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, 
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
-    st = getattr(lib, name)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
-                            B, heads, N, D, T, H, W, sparse_k, mode, float(rope_theta), _stream(stream))
-    _check(st, name)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+            B, heads, N, D, T, H, W, sparse_k, mode, float(rope_theta)]
+    call = name
+    if subset is not None:
+        call = name + "_scopes"
+        args += [int(subset[0]), int(subset[1])]
+    st = getattr(lib, call)(*args, _stream(stream))
+    _check(st, call)
 
 
 def skiparse_attn_fwd_fp8(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta=10000.0, stream=None,
@@ -182,6 +192,22 @@ def skiparse_attn_fwd_mixed8(q, k, v, out, lse, T, H, W, sparse_k, mode, rope_th
     `workspace` sized by skiparse_attn_fwd_mixed8_workspace_bytes(...)."""
     _fwd8("skiparse_attn_fwd_mixed8", q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, workspace,
           workspace_bytes)
+
+
+def skiparse_attn_fwd_fp8_scopes(q, k, v, out, lse, T, H, W, sparse_k, mode, scope_first, scope_step,
+                                 rope_theta=10000.0, stream=None, workspace=None, workspace_bytes=None):
+    """skiparse_attn_fwd_fp8 over the scopes scope_first, scope_first +
+    scope_step, ... only; the other rows of out and lse are left untouched."""
+    _fwd8("skiparse_attn_fwd_fp8", q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, workspace,
+          workspace_bytes, subset=(scope_first, scope_step))
+
+
+def skiparse_attn_fwd_mixed8_scopes(q, k, v, out, lse, T, H, W, sparse_k, mode, scope_first, scope_step,
+                                    rope_theta=10000.0, stream=None, workspace=None, workspace_bytes=None):
+    """skiparse_attn_fwd_mixed8 over the scopes scope_first, scope_first +
+    scope_step, ... only; the other rows of out and lse are left untouched."""
+    _fwd8("skiparse_attn_fwd_mixed8", q, k, v, out, lse, T, H, W, sparse_k, mode, rope_theta, stream, workspace,
+          workspace_bytes, subset=(scope_first, scope_step))
 
 
 def skiparse_attn_bwd_workspace_bytes(B, heads, N, D, T, H, W, sparse_k, mode) -> int:

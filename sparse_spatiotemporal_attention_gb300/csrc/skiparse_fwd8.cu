@@ -302,17 +302,17 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
   const PrepTab pt = prep_tab(p.rope.T, p.rope.H, p.rope.W);
   prep_load_table(tab, p.rope_gtab, p.rope, pt, threadIdx.x, blockDim.x);
   __syncthreads();
-  const int n_items = g.B * g.heads * g.k * g.n_tiles;
+  const int n_items = g.B * g.heads * g.ks * g.n_tiles;
   // head fastest: the CTAs working at the same time read all heads of the same
   // tokens, i.e. whole (token, heads x D) rows of q, k and v, not one head's
-  // 256-byte slice of every row
+  // 256-byte slice of every row. Only the call's ks scopes s0, s0 + sstep, ...
   auto decode = [&](int item, int& tile, int& s, int& sidx, int& b, int& head) {
     head = item % g.heads;
     const int rest = item / g.heads;
     tile = rest % g.n_tiles;
     const int bs = rest / g.n_tiles;
-    s = bs % g.k;
-    b = bs / g.k;
+    s = g.s0 + (bs % g.ks) * g.sstep;
+    b = bs / g.ks;
     sidx = (b * g.heads + head) * g.k + s;
   };
 
@@ -600,8 +600,9 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
   // scope's end (every role skips it alike)
   auto unit_of = [&](int u, int& pair, int& sidx, int& nt, int& Ls) -> bool {
     pair = u % n_pairs;
-    sidx = u / n_pairs;
-    const int s = sidx % g.k;
+    const int r = u / n_pairs;                       // (b, head) * ks + the call's scope number
+    const int s = g.s0 + (r % g.ks) * g.sstep;
+    sidx = (r / g.ks) * g.k + s;
     nt = scope_tiles(g, s);
     Ls = scope_len(g, s);
     return 2 * pair < nt;
@@ -948,7 +949,7 @@ int fwd8_prep_stages(int T, int H, int W, size_t optin, size_t smem_sm) {
   return 0;
 }
 
-int fwd8_units(const Geom& g) { return g.B * g.heads * g.k * ((g.n_tiles + 1) / 2); }
+int fwd8_units(const Geom& g) { return g.B * g.heads * g.ks * ((g.n_tiles + 1) / 2); }
 
 cudaError_t launch_fwd8_vmax(const Fwd8Params& p, cudaStream_t stream) {
   const dim3 grid(p.g.B * p.g.heads, (p.g.N + 255) / 256);
@@ -961,7 +962,7 @@ cudaError_t launch_fwd8_prep(const Fwd8Params& p, bool si8, int sms, cudaStream_
   auto kernel = si8 ? skiparse_fwdm8_prep_kernel : skiparse_fwd8_prep_kernel;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = one_wave(kernel, p.g.B * p.g.heads * p.g.k * p.g.n_tiles, kPrepThreads, smem, sms);
+  const int grid = one_wave(kernel, p.g.B * p.g.heads * p.g.ks * p.g.n_tiles, kPrepThreads, smem, sms);
   return launch_after_previous(kernel, grid, kPrepThreads, smem, stream, p);
 }
 

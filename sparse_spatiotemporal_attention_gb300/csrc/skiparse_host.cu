@@ -631,14 +631,18 @@ size_t skiparse_attn_fwd_mixed8_workspace_bytes(int B, int heads, int N, int D, 
 
 namespace {
 
-// The 8-bit forward: si8 = false all-E4M3 operands, si8 = true INT8 q / k for S.
+// The 8-bit forward: si8 = false all-E4M3 operands, si8 = true INT8 q / k for S;
+// the scopes scope_first, scope_first + scope_step, ... (0, 1: all).
 int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, float* lse, void* workspace,
               size_t workspace_bytes, int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode,
-              float rope_theta, cudaStream_t stream) {
+              float rope_theta, int scope_first, int scope_step, cudaStream_t stream) {
   Shape s;
   int st = check_shape(B, heads, N, D, T, H, W, sparse_k, mode, rope_theta, s);
   if (st != SKIPARSE_OK || s.empty) return st;
   if (D != 128) return SKIPARSE_ERR_UNSUPPORTED;
+  Geom geom = make_geom(s);
+  if ((st = set_subset(geom, scope_first, scope_step)) != SKIPARSE_OK) return st;
+  if (geom.ks == 0) return SKIPARSE_OK;
   if (!q || !k || !v || !out || !lse) return SKIPARSE_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return SKIPARSE_ERR_ALIGNMENT;
   const Ws8Layout w = ws8_layout(s, si8);
@@ -653,7 +657,7 @@ int fwd8_impl(bool si8, const void* q, const void* k, const void* v, void* out, 
 
   Fwd8Params p;
   std::memset(&p, 0, sizeof(p));
-  p.g = make_geom(s);
+  p.g = geom;
   p.rope = make_rope(s, rope_theta);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.q = static_cast<const uint16_t*>(q);
@@ -723,7 +727,7 @@ int skiparse_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out
                           int B, int heads, int N, int D, int T, int H, int W,
                           int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
   return fwd8_impl(false, q, k, v, out, lse, workspace, workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode,
-                   rope_theta, stream);
+                   rope_theta, 0, 1, stream);
 }
 
 int skiparse_attn_fwd_mixed8(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -731,7 +735,25 @@ int skiparse_attn_fwd_mixed8(const void* q, const void* k, const void* v, void* 
                              int B, int heads, int N, int D, int T, int H, int W,
                              int sparse_k, int mode, float rope_theta, cudaStream_t stream) {
   return fwd8_impl(true, q, k, v, out, lse, workspace, workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode,
-                   rope_theta, stream);
+                   rope_theta, 0, 1, stream);
+}
+
+int skiparse_attn_fwd_fp8_scopes(const void* q, const void* k, const void* v, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes,
+                                 int B, int heads, int N, int D, int T, int H, int W,
+                                 int sparse_k, int mode, float rope_theta, int scope_first, int scope_step,
+                                 cudaStream_t stream) {
+  return fwd8_impl(false, q, k, v, out, lse, workspace, workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode,
+                   rope_theta, scope_first, scope_step, stream);
+}
+
+int skiparse_attn_fwd_mixed8_scopes(const void* q, const void* k, const void* v, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes,
+                                    int B, int heads, int N, int D, int T, int H, int W,
+                                    int sparse_k, int mode, float rope_theta, int scope_first, int scope_step,
+                                    cudaStream_t stream) {
+  return fwd8_impl(true, q, k, v, out, lse, workspace, workspace_bytes, B, heads, N, D, T, H, W, sparse_k, mode,
+                   rope_theta, scope_first, scope_step, stream);
 }
 
 size_t skiparse_attn_bwd_workspace_bytes(int B, int heads, int N, int D, int T, int H, int W, int sparse_k, int mode) {

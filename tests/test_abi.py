@@ -190,6 +190,20 @@ def test_scope_subset_validation(lib):
     assert bwd_s(0, 0) == INVALID
     assert bwd_s(5, 1) == OK
     assert bwd_s(0, 2, ws_bytes=ws - 1) == WORKSPACE
+    for name in ("skiparse_attn_fwd_fp8", "skiparse_attn_fwd_mixed8"):
+        ws8 = getattr(lib, name + "_workspace_bytes")(1, 2, 256, 128, 4, 8, 8, 2, 0)
+        fn = getattr(lib, name + "_scopes")
+
+        def fwd8_s(first, step, D=128, ws_bytes=ws8):
+            return fn(A, 2 * A, 3 * A, 4 * A, 5 * A, 10 * A, ws_bytes, 1, 2, 256, D, 4, 8, 8, 2, 0, 10000.0,
+                      first, step, None)
+        assert fwd8_s(0, 1) == DEVICE
+        assert fwd8_s(1, 2) == DEVICE
+        assert fwd8_s(-1, 1) == INVALID
+        assert fwd8_s(0, 0) == INVALID
+        assert fwd8_s(2, 1) == OK                 # no scope >= k
+        assert fwd8_s(0, 1, D=64) == UNSUP
+        assert fwd8_s(0, 2, ws_bytes=ws8 - 1) == WORKSPACE
 
 
 def test_scope_shard_partition():

@@ -83,3 +83,46 @@ def test_scope_shards_cover_the_call(env, case):
     tl.compare("dv", tl.host(grads[2]), rdv)
     st, detail = skp.skiparse_device_error()
     assert st == 0, hex(detail)
+
+
+# (B, heads, T, H, W, k, mode, G); D = 128
+CASES8 = [
+    (1, 2, 3, 20, 24, 4, O.SINGLE, 2),          # equal scopes, two ranks
+    (1, 2, 3, 7, 9, 4, O.GROUP, 3),             # unequal scopes with a partial group, three ranks
+]
+
+
+@pytest.mark.parametrize("recipe", ["int8", "e4m3"])
+@pytest.mark.parametrize("case", CASES8, ids=lambda c: f"{c[2]}x{c[3]}x{c[4]}_k{c[5]}_G{c[7]}")
+def test_8bit_scope_shards_equal_the_full_call(env, case, recipe):
+    """The 8-bit forwards' scope subsets: each shard writes exactly its scopes'
+    rows, and the union equals the full call bit for bit (every scope's codes,
+    scales and products are the full call's; v's scales span all tokens either
+    way)."""
+    import torch
+    skp, dev = env
+    B, heads, T, H, W, k, mode, G = case
+    D, N = 128, T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D)
+    q, kk, v = (tl.to_device(ins[n], dev) for n in ("q", "k", "v"))
+    full = skp.skiparse_attn_fwd_mixed8 if recipe == "int8" else skp.skiparse_attn_fwd_fp8
+    part = skp.skiparse_attn_fwd_mixed8_scopes if recipe == "int8" else skp.skiparse_attn_fwd_fp8_scopes
+    ref_out = torch.empty((B, N, heads, D), dtype=torch.bfloat16, device=dev)
+    ref_lse = torch.empty((B, heads, N), dtype=torch.float32, device=dev)
+    full(q, kk, v, ref_out, ref_lse, T, H, W, k, mode)
+    out = torch.empty_like(ref_out)
+    out.view(torch.int16).fill_(tl.SENTINEL)
+    lse = torch.full((B, heads, N), float("nan"), dtype=torch.float32, device=dev)
+    scope_of, _ = O.index_maps(N, k, mode)
+    done = np.zeros(N, dtype=bool)
+    for rank in range(G):
+        first, step = skp.scope_shard(k, G, rank)
+        part(q, kk, v, out, lse, T, H, W, k, mode, first, step)
+        torch.cuda.synchronize()
+        done |= (scope_of % step) == first
+        written = (out.view(torch.int16) != tl.SENTINEL).any(dim=3).any(dim=2).any(dim=0).cpu().numpy()
+        assert np.array_equal(written, done), f"rank {rank}: wrote other scopes' rows"
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
