@@ -45,14 +45,19 @@ def guards_intact(buf, pad=4096):
 
 
 def compare(name, got, ref, tol_max=TOL_MAX, tol_mean=TOL_MEAN, tol_rel=TOL_RMS_REL):
+    """Max-abs and mean-abs bars, and the relative RMS bar wherever the
+    reference has a size to be relative to (a gradient that is zero by
+    construction, as dq and dk of one-token scopes, is held to the absolute
+    bars alone; real outputs here have RMS of order 1e-2 and up)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
     err = np.abs(got - ref)
     rel = np.sqrt(np.sum(err ** 2) / max(np.sum(ref ** 2), 1e-300))
+    sized = np.sqrt(np.mean(ref ** 2)) > 1e-5
     msg = f"{name}: max {err.max():.3e} mean {err.mean():.3e} relrms {rel:.3e}"
-    assert err.max() <= tol_max and err.mean() <= tol_mean and rel <= tol_rel, msg
+    assert err.max() <= tol_max and err.mean() <= tol_mean and (rel <= tol_rel or not sized), msg
     return msg
 
 

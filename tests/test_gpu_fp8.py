@@ -77,6 +77,7 @@ CASES = [
     (1, 2, 6, 24, 8, 2, O.GROUP),       # H > W and T > W: the prep kernel's RoPE-table regions of unequal length
     (2, 2, 3, 19, 23, 4, O.SINGLE),     # N = 1311: unequal scopes (328, 328, 328, 327), three tiles each
     (1, 2, 5, 13, 21, 4, O.GROUP),      # N = 1365: unequal scopes of whole and partial groups
+    (1, 2, 1, 2, 5, 4, O.GROUP),        # N = 10: scopes 4, 4, 2 and an empty one
 ]
 
 
