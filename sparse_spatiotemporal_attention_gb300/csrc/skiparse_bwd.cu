@@ -57,10 +57,11 @@ __device__ __forceinline__ void decode_unit_bwd(const Geom& g, int u, int& b, in
 }
 
 // ===========================================================================
-// main kernel for D = 128: full 128-query tiles, dQ drained by its own warps
+// main kernel (D = 128 and 64): full 128-query tiles, dQ drained by its own warps
 // ===========================================================================
 //
-// Every MMA has M = N = 128 (40 tcgen05.mma per key-tile x query-tile pair).
+// Every MMA has M = 128 and N = 128 (N = D for dV and dK~): 40 tcgen05.mma per
+// key-tile x query-tile pair at D = 128, 32 at D = 64.
 // Per query tile i:
 //   MMA1:  S^T = K~ Q~_i^T -> TMEM 0..127, dP^T = V dO_i^T -> TMEM 128..255
 //   warps 0-7 form P^T / dS^T in four chunks of 32 queries. P^T of chunks
