@@ -400,6 +400,18 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* m, ui
   else tma_load_5d(dst, m, bar, c0, head, 0, c.s, c.row);
 }
 
+// L2 prefetch of the tile load_tile with the same arguments fetches (no
+// shared-memory destination, nothing to wait for): issued a few tiles ahead of
+// a work unit's first loads, it turns their HBM latency into an L2 hit.
+__device__ __forceinline__ void prefetch_tile(const CUtensorMap* m, TileCoord c, int c0, int head) {
+  if (c.s < 0)
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 :: "l"((uint64_t)m), "r"(c0), "r"(head), "r"(c.row) : "memory");
+  else
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];"
+                 :: "l"((uint64_t)m), "r"(c0), "r"(head), "r"(0), "r"(c.s), "r"(c.row) : "memory");
+}
+
 // Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(

@@ -53,6 +53,7 @@ enum FwdBar {
 };
 
 constexpr int kFwdThreads = 320;
+constexpr int kPrefetchLead = 4;   // K tiles before an item's end at which the next item's Q pair is prefetched
 constexpr int kRopeThreads = 256;
 
 // P = 2^(S * sl2 - m) for one softmax row held in registers (x, 128 keys), as
@@ -377,12 +378,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       }
       __syncwarp();
       ++q_issued;
+      // the next item's Q pair (read once, from HBM) is prefetched into L2 a few
+      // K tiles before this item ends, so its load after QEMPTY hits L2
+      Item wn;
+      bool next = false;
+      for (int wi2 = wi + gridDim.x; wi2 < p.n_items; wi2 += gridDim.x)
+        if (decode_item(p, n_pairs, wi2, wn)) {
+          next = true;
+          break;
+        }
+      const int pf_at = nt > kPrefetchLead ? nt - kPrefetchLead : 0;
       for (int jj = 0; jj < nt; ++jj) {
         const int j = w.j0 + jj;                     // the scope's K tile
         const uint32_t gg = gk + jj;
         const int st = gg & 1;
         const uint32_t n = gg >> 1;
         const TileCoord tcj = scope_tile(g, s, b, j * kTile);
+        if (leader && next && jj == pf_at) {
+          const TileCoord nA = scope_tile(g, wn.s, wn.b, 2 * wn.pair * kTile);
+          const TileCoord nB = scope_tile(g, wn.s, wn.b, (2 * wn.pair + 1) * kTile);
+#pragma unroll
+          for (int h = 0; h < Ly::HALVES; ++h) {
+            prefetch_tile(&p.tm_q, nA, h * 64, wn.head);
+            prefetch_tile(&p.tm_q, nB, h * 64, wn.head);
+          }
+        }
         if (n > 0 && !warp_wait(F_KEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
         if (leader) {
           mbar_expect_tx(bar(F_KFULL0 + st), Ly::TILE);
