@@ -656,10 +656,29 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
       }
       __syncwarp();
       ++q_issued;
+      // the next unit's Q codes, prefetched into L2 a few K tiles before this
+      // unit ends so that its Q load hits L2
+      int npair = 0, nsidx = 0, nnt = 0, nLs = 0;
+      bool next = false;
+      for (int u2 = u + gridDim.x; u2 < p.n_units; u2 += gridDim.x)
+        if (unit_of(u2, npair, nsidx, nnt, nLs)) {
+          next = true;
+          break;
+        }
+      const int pf_at = nt > 4 ? nt - 4 : 0;
       for (int j = 0; j < nt; ++j) {
         const uint32_t gg = gk + j;
         const int st = gg & 1;
         const uint32_t n = gg >> 1;
+        if (leader && next && j == pf_at) {
+#pragma unroll
+          for (int h = 0; h < (SI8 ? 2 : 1); ++h)
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+              asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                           :: "l"((uint64_t)&p.tm_q8), "r"(h * 64), "r"((2 * npair + x) * kTile), "r"(nsidx)
+                           : "memory");
+        }
         if (n > 0 && !warp_wait(E_KEMPTY0 + st, (n - 1) & 1)) { ok = false; break; }
         if (leader) {
           mbar_expect_tx(bar(E_KFULL0 + st), Ly::QK);
