@@ -516,37 +516,50 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
       int t = 0, hh = 0, w = 0;
       if (key_ok) token_coords(p.rope, tok, t, hh, w);
       const size_t rbase = (((size_t)b * g.N + tok) * g.heads + head) * D;
-      if (ch == 0) {
+      // Each of the two warps on a key row writes half of dv and half of dk: the
+      // dk chunks' cos / sin reads (scattered over the tokens of the warp's 32
+      // key rows, the w axis worst) are shared out, chunks 0 + 3 and 1 + 2.
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float y[32];
-          tmem_ld32(tmem + lane_base + 256 + c * 32, y);
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = ch * (D / 64) + cc;              // dv chunks 0, 1 / 2, 3 (D = 64: 0 / 1)
+        float y[32];
+        tmem_ld32(tmem + lane_base + 256 + c * 32, y);
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              dst[q4] = make_uint4(pack_bf16(y[8 * q4], y[8 * q4 + 1]), pack_bf16(y[8 * q4 + 2], y[8 * q4 + 3]),
-                                   pack_bf16(y[8 * q4 + 4], y[8 * q4 + 5]), pack_bf16(y[8 * q4 + 6], y[8 * q4 + 7]));
-          }
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_uint4(pack_bf16(y[8 * q4], y[8 * q4 + 1]), pack_bf16(y[8 * q4 + 2], y[8 * q4 + 3]),
+                                 pack_bf16(y[8 * q4 + 4], y[8 * q4 + 5]), pack_bf16(y[8 * q4 + 6], y[8 * q4 + 7]));
         }
-      } else {
+      }
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float y[32];
-          tmem_ld32(tmem + lane_base + 384 + c * 32, y);
-          if (key_ok) {
-            uint32_t o[16];
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = D == 128 ? (ch == 0 ? 3 * cc : 1 + cc) : ch + 2 * cc;   // dk chunks 0, 3 / 1, 2
+        if (c >= D / 32) break;
+        float y[32];
+        tmem_ld32(tmem + lane_base + 384 + c * 32, y);
+        if (key_ok) {
+          // pairs 16c .. 16c + 15, two per 16-byte table read (an axis never
+          // splits a pair of pairs: its bounds D/8 and 5D/16 are even)
+          float4 cs[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const PairSel sel = pair_select(p.rope, c * 16 + e);
-              const float2 cs = __ldg(&p.rope_tab[pair_index(sel, t, hh, w)]);
-              const float2 r = rope_rotate_t(y[2 * e] * p.scale, y[2 * e + 1] * p.scale, cs);
-              o[e] = pack_bf16(r.x, r.y);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+          for (int e2 = 0; e2 < 8; ++e2) {
+            const PairSel sel = pair_select(p.rope, c * 16 + 2 * e2);
+            cs[e2] = __ldg(reinterpret_cast<const float4*>(&p.rope_tab[pair_index(sel, t, hh, w)]));
           }
+          uint32_t o[16];
+#pragma unroll
+          for (int e2 = 0; e2 < 8; ++e2) {
+            const float2 r0 = rope_rotate_t(y[4 * e2] * p.scale, y[4 * e2 + 1] * p.scale,
+                                            make_float2(cs[e2].x, cs[e2].y));
+            const float2 r1 = rope_rotate_t(y[4 * e2 + 2] * p.scale, y[4 * e2 + 3] * p.scale,
+                                            make_float2(cs[e2].z, cs[e2].w));
+            o[2 * e2] = pack_bf16(r0.x, r0.y);
+            o[2 * e2 + 1] = pack_bf16(r1.x, r1.y);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
         }
       }
       tc_fence_before();
