@@ -20,9 +20,12 @@
 //  post        dq = R^T (scale * dQ~_acc) -> bf16.
 // One main kernel for D = 128 and D = 64 (18 warps):
 //   warps 0-7   P^T / dS^T in four 32-query chunks (one key row, 16 queries of
-//               a chunk per thread) and the dK / dV epilogue;
+//               a chunk per thread);
 //   warps 8-15  dQ~^T out of TMEM (one channel, 64 queries per thread), staged
 //               in the tile's dead Q~ / dO slots and bulk-added to the accumulator;
+//               after a unit's last tile, its dK / dV epilogue (one key row,
+//               half of the channels per thread), while warps 0-7 start the
+//               next unit;
 //   warp 16     TMA producer (K~, V per unit; Q~, dO, lse, delta per Q tile);
 //   warp 17     MMA issuer; every MMA has M = 128 and N = 128 or D.
 // TMEM columns: S^T (P^T as bf16) 0..127, dP^T / dQ~ partial 128..255,
@@ -85,7 +88,7 @@ enum BwdTileBar {
   T_OFULL0, T_OFULL1,       // dO tile of stage 0 / 1 landed
   T_QFREE0, T_QFREE1,       // Q~ slot of stage 0 / 1 free again (its dQ~ staging has been read)
   T_OFREE0, T_OFREE1,       // dO slot likewise
-  T_SRDY, T_DPRDY, T_PRDY, T_DSC0, T_DSC1, T_DSC2, T_DSC3, T_DQFULL, T_DQFREE, T_DKVDONE, T_DKVFREE, T_FINAL,
+  T_SRDY, T_DPRDY, T_PRDY, T_DSC0, T_DSC1, T_DSC2, T_DSC3, T_DQFULL, T_DQFREE, T_DKVDONE, T_DVFREE, T_DKFREE, T_FINAL,
   T_NBARS
 };
 
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
 
   if (tid == 0) {
     *abort_flag = 0;
-    const uint32_t counts[T_NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 8, 8, 1, 8, 1, 8, 1};
+    const uint32_t counts[T_NBARS] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 8, 8, 8, 8, 8, 1, 8, 1, 8, 8, 1};
     for (int i = 0; i < T_NBARS; ++i) mbar_init(bar(i), counts[i]);
     mbar_fence_init();
   }
@@ -271,8 +274,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         __syncwarp();
         // P^T of queries 0..63 is published while dP^T is still being computed
         if (!warp_wait(T_PRDY, gg & 1)) { ok = false; break; }
-        // the previous unit's dV / dK must have been written out before the first accumulate
-        if (i == 0 && it > 0 && !warp_wait(T_DKVFREE, (it - 1) & 1)) { ok = false; break; }
+        // the previous unit's dV must have been read out of TMEM before the first accumulate
+        if (i == 0 && it > 0 && !warp_wait(T_DVFREE, (it - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         if (leader) {
 #pragma unroll
@@ -282,6 +285,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         __syncwarp();
         for (int c = 0; c < 4; ++c) {
           if (!warp_wait(T_DSC0 + c, gg & 1)) { ok = false; break; }
+          // likewise the previous unit's dK~ before the first dK~ accumulate
+          if (c == 0 && i == 0 && it > 0 && !warp_wait(T_DKFREE, (it - 1) & 1)) { ok = false; break; }
           tc_fence_after();
           if (leader) {
             if (c >= 2) {
@@ -333,6 +338,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const bool leader = tid == 256;
     uint32_t g0 = 0;
+    int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
@@ -372,7 +378,74 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         }
         __syncwarp();
       }
+      if (!ok) break;
+      const int jr = (warp & 3) * 32 + lane;             // key row (TMEM lane)
+      const bool key_ok = kt * kTile + jr < scope_len(g, s);
+      // ---- epilogue of the unit (these warps wait for the next unit's first dQ~
+      // anyway; the softmax warps go straight on): dv, and dk = scale * R^T dK~
+      // (key row jr; the two warps on a row share the chunks out)
+      if (!bar_and<3, 256>(mbar_wait(bar(T_DKVDONE), it & 1, ctl, E + T_DKVDONE))) break;
+      tc_fence_after();
+      const int prow = kt * kTile + jr;
+      const int tok = key_ok ? token_of(g, s, prow) : 0;
+      int t = 0, hh = 0, w = 0;
+      if (key_ok) token_coords(p.rope, tok, t, hh, w);
+      const size_t rbase = (((size_t)b * g.N + tok) * g.heads + head) * D;
+      // Each of the two warps on a key row writes half of dv and half of dk: the
+      // dk chunks' cos / sin reads (scattered over the tokens of the warp's 32
+      // key rows, the w axis worst) are shared out, chunks 0 + 3 and 1 + 2.
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = qh * (D / 64) + cc;              // dv chunks 0, 1 / 2, 3 (D = 64: 0 / 1)
+        float y[32];
+        tmem_ld32(tmem + lane_base + 256 + c * 32, y);
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_uint4(pack_bf16(y[8 * q4], y[8 * q4 + 1]), pack_bf16(y[8 * q4 + 2], y[8 * q4 + 3]),
+                                 pack_bf16(y[8 * q4 + 4], y[8 * q4 + 5]), pack_bf16(y[8 * q4 + 6], y[8 * q4 + 7]));
+        }
+      }
+      // dV is out of TMEM: the next unit's first P^T dO may start while dk is formed
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(T_DVFREE));
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = D == 128 ? (qh == 0 ? 3 * cc : 1 + cc) : qh + 2 * cc;   // dk chunks 0, 3 / 1, 2
+        if (c >= D / 32) break;
+        float y[32];
+        tmem_ld32(tmem + lane_base + 384 + c * 32, y);
+        if (key_ok) {
+          // pairs 16c .. 16c + 15, two per 16-byte table read (an axis never
+          // splits a pair of pairs: its bounds D/8 and 5D/16 are even)
+          float4 cs[8];
+#pragma unroll
+          for (int e2 = 0; e2 < 8; ++e2) {
+            const PairSel sel = pair_select(p.rope, c * 16 + 2 * e2);
+            cs[e2] = __ldg(reinterpret_cast<const float4*>(&p.rope_tab[pair_index(sel, t, hh, w)]));
+          }
+          uint32_t o[16];
+#pragma unroll
+          for (int e2 = 0; e2 < 8; ++e2) {
+            const float2 r0 = rope_rotate_t(y[4 * e2] * p.scale, y[4 * e2 + 1] * p.scale,
+                                            make_float2(cs[e2].x, cs[e2].y));
+            const float2 r1 = rope_rotate_t(y[4 * e2 + 2] * p.scale, y[4 * e2 + 3] * p.scale,
+                                            make_float2(cs[e2].z, cs[e2].w));
+            o[2 * e2] = pack_bf16(r0.x, r0.y);
+            o[2 * e2 + 1] = pack_bf16(r1.x, r1.y);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(T_DKFREE));
       g0 += nt;
+      ++it;
     }
     if (leader) bulk_wait_all();
   } else {
@@ -383,7 +456,6 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
     const float sl2 = p.scale_log2;
     uint8_t* ds_row = smem + Ly::DS_OFF + j * 128;
     uint32_t g0 = 0;
-    int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int b, head, s, kt;
@@ -508,65 +580,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         else ds_phase(std::false_type{});
       }
       if (!ok) break;
-      // ---- epilogue: warps 0-3 write dv, warps 4-7 write dk = scale * R^T dK~ (key row j)
-      if (!bar_and<2, 256>(mbar_wait(bar(T_DKVDONE), it & 1, ctl, E + T_DKVDONE))) break;
-      tc_fence_after();
-      const int prow = kt * kTile + j;
-      const int tok = key_ok ? token_of(g, s, prow) : 0;
-      int t = 0, hh = 0, w = 0;
-      if (key_ok) token_coords(p.rope, tok, t, hh, w);
-      const size_t rbase = (((size_t)b * g.N + tok) * g.heads + head) * D;
-      // Each of the two warps on a key row writes half of dv and half of dk: the
-      // dk chunks' cos / sin reads (scattered over the tokens of the warp's 32
-      // key rows, the w axis worst) are shared out, chunks 0 + 3 and 1 + 2.
-#pragma unroll 1
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = ch * (D / 64) + cc;              // dv chunks 0, 1 / 2, 3 (D = 64: 0 / 1)
-        float y[32];
-        tmem_ld32(tmem + lane_base + 256 + c * 32, y);
-        if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(pack_bf16(y[8 * q4], y[8 * q4 + 1]), pack_bf16(y[8 * q4 + 2], y[8 * q4 + 3]),
-                                 pack_bf16(y[8 * q4 + 4], y[8 * q4 + 5]), pack_bf16(y[8 * q4 + 6], y[8 * q4 + 7]));
-        }
-      }
-#pragma unroll 1
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = D == 128 ? (ch == 0 ? 3 * cc : 1 + cc) : ch + 2 * cc;   // dk chunks 0, 3 / 1, 2
-        if (c >= D / 32) break;
-        float y[32];
-        tmem_ld32(tmem + lane_base + 384 + c * 32, y);
-        if (key_ok) {
-          // pairs 16c .. 16c + 15, two per 16-byte table read (an axis never
-          // splits a pair of pairs: its bounds D/8 and 5D/16 are even)
-          float4 cs[8];
-#pragma unroll
-          for (int e2 = 0; e2 < 8; ++e2) {
-            const PairSel sel = pair_select(p.rope, c * 16 + 2 * e2);
-            cs[e2] = __ldg(reinterpret_cast<const float4*>(&p.rope_tab[pair_index(sel, t, hh, w)]));
-          }
-          uint32_t o[16];
-#pragma unroll
-          for (int e2 = 0; e2 < 8; ++e2) {
-            const float2 r0 = rope_rotate_t(y[4 * e2] * p.scale, y[4 * e2 + 1] * p.scale,
-                                            make_float2(cs[e2].x, cs[e2].y));
-            const float2 r1 = rope_rotate_t(y[4 * e2 + 2] * p.scale, y[4 * e2 + 3] * p.scale,
-                                            make_float2(cs[e2].z, cs[e2].w));
-            o[2 * e2] = pack_bf16(r0.x, r0.y);
-            o[2 * e2 + 1] = pack_bf16(r1.x, r1.y);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(T_DKVFREE));
       g0 += nt;
-      ++it;
     }
   }
 

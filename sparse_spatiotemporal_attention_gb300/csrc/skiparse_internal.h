@@ -11,8 +11,7 @@
 namespace skp {
 
 // Codes written to the device error word when a bounded wait runs out:
-// kernel base + barrier index; the backward main kernels add 0x00 (128-query
-// tiles, D = 64), 0x40 (64-query halves) or 0x80 (128-query tiles, D = 128).
+// kernel base + barrier index; the backward main kernel adds 0x80.
 enum : int {
   ERR_KERNEL_FWD = 0x1000,
   ERR_KERNEL_BWD = 0x2000,
