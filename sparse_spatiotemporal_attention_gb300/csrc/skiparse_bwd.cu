@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
       for (int i = 0; i < nt; ++i) {
         const uint32_t gg = g0 + i;
         const int st = gg & 1;
-        if (!bar_and<2, 256>(mbar_wait(bar(T_SRDY), gg & 1, ctl, E + T_SRDY))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(T_SRDY), gg & 1, ctl, E + T_SRDY))) { ok = false; break; }
         tc_fence_after();
         const float4* lse4 = reinterpret_cast<const float4*>(stats + st * 256);
         const float4* del4 = lse4 + 32;
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(T_PRDY));
         // DPRDY also says the previous tile's MMAs (readers of the dS^T buffer) are done
-        if (!bar_and<2, 256>(mbar_wait(bar(T_DPRDY), gg & 1, ctl, E + T_DPRDY))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(T_DPRDY), gg & 1, ctl, E + T_DPRDY))) { ok = false; break; }
         tc_fence_after();
         auto ds_phase = [&](auto F) {
           // dP^T of chunks 0 and 1 in one TMEM round trip
