@@ -29,6 +29,8 @@
 // keeps every parity wait on the O-done barriers one phase ahead at most.
 // The softmax reads S twice from TMEM (max pass, then exp pass); online softmax
 // with lazy O rescaling (threshold 2^8), P written back over S as bf16.
+#include <type_traits>
+
 #include "skiparse_internal.h"
 
 namespace skp {
@@ -708,15 +710,18 @@ __global__ void __launch_bounds__(256) skiparse_fwd_merge_kernel(const __grid_co
 #pragma unroll
     for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
     const float* po = p.part_o + ((size_t)r * np * 256 + row) * D + lane * CPL;
-#pragma unroll 8
+    // a lane's CPL channels of a piece in one vector load (16 or 8 bytes)
+    using VecT = typename std::conditional<CPL == 4, float4, float2>::type;
+#pragma unroll 16
     for (int pc = 0; pc < np; ++pc) {
       const float2 v = ml[(size_t)pc * 256];
       const bool has = (pc + 1) * nt / np > pc * nt / np;
       const float f = has ? ex2(v.x - M) : 0.f;
       L = fmaf(f, has ? v.y : 0.f, L);
-      const float* q = po + (size_t)pc * 256 * D;
+      const VecT q = *reinterpret_cast<const VecT*>(po + (size_t)pc * 256 * D);
+      const float* qe = reinterpret_cast<const float*>(&q);
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) acc[e] = fmaf(f, has ? q[e] : 0.f, acc[e]);
+      for (int e = 0; e < CPL; ++e) acc[e] = fmaf(f, has ? qe[e] : 0.f, acc[e]);
     }
     const int tok = token_of(g, s, prow);
     const float inv = 1.0f / L;
