@@ -638,28 +638,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       const bool row_ok = prow < Ls;
       const int tok = row_ok ? token_of(g, s, prow) : 0;
       const float inv_l = 1.0f / l;
-      uint16_t* orow = p.out + (((size_t)b * g.N + tok) * g.heads + head) * D;
+      // the whole O row out of TMEM in one round trip, normalised and packed;
+      // the O columns are released before the global stores, so the next
+      // unit's first P V does not wait for them
+      uint32_t pk[D / 2];
+      {
+        float o[D];
+        if constexpr (D == 128) tmem_ld128(tmem + lane_base + colO, o);
+        else tmem_ld64(tmem + lane_base + colO, o);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(tmem + lane_base + colO + c * 32, o);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16(o[8 * q4 + 0] * inv_l, o[8 * q4 + 1] * inv_l);
-            w.y = pack_bf16(o[8 * q4 + 2] * inv_l, o[8 * q4 + 3] * inv_l);
-            w.z = pack_bf16(o[8 * q4 + 4] * inv_l, o[8 * q4 + 5] * inv_l);
-            w.w = pack_bf16(o[8 * q4 + 6] * inv_l, o[8 * q4 + 7] * inv_l);
-            dst[q4] = w;
-          }
-        }
+        for (int e = 0; e < D / 2; ++e) pk[e] = pack_bf16(o[2 * e] * inv_l, o[2 * e + 1] * inv_l);
       }
-      if (row_ok) p.lse[((size_t)b * g.heads + head) * g.N + tok] = (m + log2f(l)) * 0.6931471805599453f;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(barOE));
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b * g.N + tok) * g.heads + head) * D);
+#pragma unroll
+        for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        p.lse[((size_t)b * g.heads + head) * g.N + tok] = (m + log2f(l)) * 0.6931471805599453f;
+      }
       g0 += nt;
       ++it;
     }
