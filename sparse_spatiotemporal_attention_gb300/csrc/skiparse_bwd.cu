@@ -400,11 +400,11 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
         float y[32];
         tmem_ld32(tmem + lane_base + 256 + c * 32, y);
         if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dv + rbase + c * 32);
+          uint32_t o[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(pack_bf16(y[8 * q4], y[8 * q4 + 1]), pack_bf16(y[8 * q4 + 2], y[8 * q4 + 3]),
-                                 pack_bf16(y[8 * q4 + 4], y[8 * q4 + 5]), pack_bf16(y[8 * q4 + 6], y[8 * q4 + 7]));
+          for (int e = 0; e < 16; ++e) o[e] = pack_bf16(y[2 * e], y[2 * e + 1]);
+          // rows are D * 2 bytes apart: 32-byte stores whenever the base allows
+          st_global_64b(p.dv + rbase + c * 32, o, (reinterpret_cast<uintptr_t>(p.dv) & 31u) == 0);
         }
       }
       // dV is out of TMEM: the next unit's first P^T dO may start while dk is formed
@@ -436,9 +436,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) skiparse_bwd_main_tile_kernel
             o[2 * e2] = pack_bf16(r0.x, r0.y);
             o[2 * e2 + 1] = pack_bf16(r1.x, r1.y);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.dk + rbase + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+          st_global_64b(p.dk + rbase + c * 32, o, (reinterpret_cast<uintptr_t>(p.dk) & 31u) == 0);
         }
       }
       tc_fence_before();

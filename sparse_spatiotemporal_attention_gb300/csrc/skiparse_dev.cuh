@@ -199,6 +199,26 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// One 32-byte global store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_32b(void* p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                              uint32_t w4, uint32_t w5, uint32_t w6, uint32_t w7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(w0), "r"(w1), "r"(w2), "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7) : "memory");
+}
+
+// 64 bytes to global memory: two 32-byte stores when `wide` (dst 32-byte
+// aligned), else four 16-byte ones.
+__device__ __forceinline__ void st_global_64b(void* dst, const uint32_t (&w)[16], bool wide) {
+  if (wide) {
+    st_global_32b(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+    st_global_32b(static_cast<uint8_t*>(dst) + 32, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+  } else {
+    uint4* d = static_cast<uint4*>(dst);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) d[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Shared memory / barriers / bounded waits
 // ---------------------------------------------------------------------------

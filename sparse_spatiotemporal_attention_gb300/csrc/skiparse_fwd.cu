@@ -653,9 +653,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) skiparse_fwd_kernel(const __gr
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(barOE));
       if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (((size_t)b * g.N + tok) * g.heads + head) * D);
+        uint16_t* orow = p.out + (((size_t)b * g.N + tok) * g.heads + head) * D;
+        // 32-byte stores when out's base allows them (rows are D * 2 bytes apart)
+        if ((reinterpret_cast<uintptr_t>(p.out) & 31u) == 0) {
 #pragma unroll
-        for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          for (int q8 = 0; q8 < D / 16; ++q8)
+            st_global_32b(orow + 16 * q8, pk[8 * q8], pk[8 * q8 + 1], pk[8 * q8 + 2], pk[8 * q8 + 3], pk[8 * q8 + 4],
+                          pk[8 * q8 + 5], pk[8 * q8 + 6], pk[8 * q8 + 7]);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
         p.lse[((size_t)b * g.heads + head) * g.N + tok] = (m + log2f(l)) * 0.6931471805599453f;
       }
       g0 += nt;

@@ -918,19 +918,13 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
         float o[32];
         tmem_ld32(tmem + lane_base + colO + c * 32, o);
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          uint32_t w[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = o[8 * q4 + e] * (__uint_as_float(__ldg(vm + c * 32 + 8 * q4 + e)) * inv_l);
-            uint4 w;
-            w.x = pack_bf16(y[0], y[1]);
-            w.y = pack_bf16(y[2], y[3]);
-            w.z = pack_bf16(y[4], y[5]);
-            w.w = pack_bf16(y[6], y[7]);
-            dst[q4] = w;
-          }
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16(o[2 * e] * (__uint_as_float(__ldg(vm + c * 32 + 2 * e)) * inv_l),
+                             o[2 * e + 1] * (__uint_as_float(__ldg(vm + c * 32 + 2 * e + 1)) * inv_l));
+          // rows are D * 2 bytes apart: 32-byte stores whenever out's base allows
+          st_global_64b(orow + c * 32, w, (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0);
         }
       }
       if (row_ok) p.lse[((size_t)b * g.heads + head) * g.N + tok] = (m + log2f(l) - 6.0f) * 0.6931471805599453f;

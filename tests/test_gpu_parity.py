@@ -175,6 +175,38 @@ def test_backward_saved_bitwise_and_parity(env, case):
     assert st == 0, hex(detail)
 
 
+@pytest.mark.parametrize("case", [(1, 2, 128, 3, 10, 10, 2, O.GROUP), (1, 2, 64, 3, 10, 11, 4, O.SINGLE)],
+                         ids=_ids)
+def test_outputs_off_a_32_byte_boundary(env, case):
+    """out, dq, dk and dv placed 16 bytes past a 32-byte boundary (the least
+    alignment the library accepts) take the kernels' 16-byte store path; the
+    results equal those of 32-byte-aligned outputs (32-byte stores): out, lse,
+    dk and dv bit for bit, dq up to the order of its fp32 accumulation."""
+    import torch
+    skp, dev = env
+    B, heads, D, T, H, W, k, mode = case
+    N = T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D, with_grad=True)
+    fa = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode)
+    fb = tl.run_fwd(skp, dev, ins, B, heads, N, D, T, H, W, k, mode, pad=4104)
+    assert fa["out"].data_ptr() % 32 == 0 and fb["out"].data_ptr() % 32 == 16
+    assert torch.equal(fa["out"].view(torch.int16), fb["out"].view(torch.int16))
+    assert torch.equal(fa["lse"], fb["lse"])
+    ba = tl.run_bwd(skp, dev, ins, fa, B, heads, N, D, T, H, W, k, mode)
+    bb = tl.run_bwd(skp, dev, ins, fb, B, heads, N, D, T, H, W, k, mode, pad=4104)
+    assert bb["dq"].data_ptr() % 32 == 16
+    for name in ("dk", "dv"):
+        assert torch.equal(ba[name].view(torch.int16), bb[name].view(torch.int16)), name
+    d1, d2 = tl.host(ba["dq"]), tl.host(bb["dq"])
+    assert np.all(np.abs(d1 - d2) <= 2.0 ** -7 * np.maximum(np.abs(d1), np.abs(d2)) + 1e-7)
+    f = tl.f64_inputs(ins)
+    rdq, rdk, rdv, rout, _ = O.skiparse_bwd(f["q"], f["k"], f["v"], f["do"], T, H, W, k, mode)
+    tl.compare("out", tl.host(fb["out"]), rout)
+    tl.compare("dq", d2, rdq)
+    tl.compare("dk", tl.host(bb["dk"]), rdk)
+    tl.compare("dv", tl.host(bb["dv"]), rdv)
+
+
 def test_peaky_softmax_rescale(env):
     """q scaled by 4 makes row maxima jump between key tiles, exercising the
     online-softmax rescale of O. Not a contract workload; its bound is derived
