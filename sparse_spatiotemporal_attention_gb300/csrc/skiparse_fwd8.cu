@@ -918,11 +918,20 @@ __device__ __forceinline__ void fwd8_attention(const Fwd8Params& p) {
         float o[32];
         tmem_ld32(tmem + lane_base + colO + c * 32, o);
         if (row_ok) {
+          // the chunk's 32 per-channel v scales (the same for every row: broadcast loads), 16 bytes at a time
+          float sv[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(vm + c * 32) + q4);
+            sv[4 * q4] = __uint_as_float(u.x);
+            sv[4 * q4 + 1] = __uint_as_float(u.y);
+            sv[4 * q4 + 2] = __uint_as_float(u.z);
+            sv[4 * q4 + 3] = __uint_as_float(u.w);
+          }
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16(o[2 * e] * (__uint_as_float(__ldg(vm + c * 32 + 2 * e)) * inv_l),
-                             o[2 * e + 1] * (__uint_as_float(__ldg(vm + c * 32 + 2 * e + 1)) * inv_l));
+            w[e] = pack_bf16(o[2 * e] * (sv[2 * e] * inv_l), o[2 * e + 1] * (sv[2 * e + 1] * inv_l));
           // rows are D * 2 bytes apart: 32-byte stores whenever out's base allows
           st_global_64b(orow + c * 32, w, (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0);
         }
