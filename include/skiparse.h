@@ -32,6 +32,11 @@
  *     must not overlap any input or each other.
  *   - B, heads or N equal to 0 is a valid empty call: nothing is launched and
  *     the pointers may be NULL.
+ *   - Tensors must start 16-byte aligned (SKIPARSE_ERR_ALIGNMENT otherwise).
+ *     Outputs whose rows one thread writes alone (out of the forwards, dk and
+ *     dv of the backward) are written with 32-byte stores when their base is
+ *     32-byte aligned, and with 16-byte stores otherwise: same results, the
+ *     former faster.
  *   - Kernel-side waits are bounded; a wait that runs out records a code in a
  *     device error word that skiparse_device_error() returns.
  */
