@@ -27,8 +27,11 @@
 // the tensor core alternates between the two Q tiles. Because S_X(g) is issued
 // after PV_X(g-1), the S-full barrier of tile g proves PV_X(g-1) complete, which
 // keeps every parity wait on the O-done barriers one phase ahead at most.
-// The softmax reads S twice from TMEM (max pass, then exp pass); online softmax
-// with lazy O rescaling (threshold 2^8), P written back over S as bf16.
+// The softmax reads each 128-score row from TMEM in one load (row max, then
+// exponentials from registers); online softmax with lazy O rescaling
+// (threshold 2^8), P written back over S as bf16. The epilogue reads O in one
+// load, releases its columns, then writes each out row (32-byte stores when
+// out's base allows).
 #include <type_traits>
 
 #include "skiparse_internal.h"
