@@ -118,6 +118,49 @@ def test_8bit_forward_parity(env, case, recipe):
     assert st == 0, hex(detail)
 
 
+def _random_cases(n=8, seed=20261203):
+    """Seeded random small grids for the 8-bit forwards (D = 128): either mode,
+    k from 1 to 8 (single) or a power of two up to 8 (group), batch 1 or 2."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        mode = O.SINGLE if rng.integers(2) == 0 else O.GROUP
+        k = int(rng.integers(1, 9)) if mode == O.SINGLE else int(rng.choice([1, 2, 4, 8]))
+        T, H, W = int(rng.integers(1, 5)), int(rng.integers(1, 13)), int(rng.integers(1, 25))
+        out.append((int(rng.integers(1, 3)), int(rng.integers(1, 4)), T, H, W, k, mode))
+    return out
+
+
+@pytest.mark.parametrize("recipe", F.RECIPES)
+@pytest.mark.parametrize("case", _random_cases(), ids=_ids)
+def test_8bit_forward_random_shapes(env, case, recipe):
+    """The bars of test_8bit_forward_parity on seeded random small shapes
+    (unequal, one-token and empty scopes included)."""
+    import torch
+    skp, dev = env
+    B, heads, T, H, W, k, mode = case
+    D, N = 128, T * H * W
+    ins = synthetic.attention_inputs(B, N, heads, D)
+    q, kk, v = (tl.to_device(ins[n], dev) for n in ("q", "k", "v"))
+    obuf, out = tl.guarded_empty((B, N, heads, D), torch.bfloat16, dev)
+    lbuf, lse = tl.guarded_empty((B, heads, N), torch.float32, dev)
+    getattr(skp, RECIPE_CALL[recipe])(q, kk, v, out, lse, T, H, W, k, mode)
+    torch.cuda.synchronize()
+    assert tl.guards_intact(obuf) and tl.guards_intact(lbuf), "8-bit forward wrote outside its outputs"
+    f = tl.f64_inputs(ins)
+    rout, rlse, rl = F.skiparse_fwd_fp8(f["q"], f["k"], f["v"], T, H, W, k, mode, recipe=recipe, with_l=True)
+    got = tl.host(out)
+    bidx, _, hidx = np.meshgrid(np.arange(B), np.arange(N), np.arange(heads), indexing="ij")
+    bound = flip_bound(vmax_rows(f["v"], bidx.ravel(), hidx.ravel()),
+                       np.transpose(rl, (0, 2, 1)).ravel()).reshape(B, N, heads, D)
+    check_out(got, rout, bound, recipe)
+    lens = [len(O.prose_scope_tokens(N, k, mode, s)) for s in range(k)]
+    lse_rel = 2.0 ** -8 if min(n for n in lens if n) == 1 else 1e-3
+    tl.compare("lse", tl.host(lse), rlse, tol_max=tl.TOL_LSE, tol_mean=tl.TOL_LSE, tol_rel=lse_rel)
+    st, detail = skp.skiparse_device_error()
+    assert st == 0, hex(detail)
+
+
 def test_mixed_recipe_is_more_accurate(env):
     """The page's reason for INT8 S: on the same inputs the mixed kernel's
     output is closer to exact attention than the all-E4M3 kernel's."""
