@@ -466,9 +466,9 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
           sq = qm > 0.f ? qm / QMAX : 1.f;
         }
         if constexpr (SI8) {
-          uint4* dst = reinterpret_cast<uint4*>(p.q8 + slot * QROW + cb * 32);
-          dst[hsel] = qc;
-          dst[1 - hsel] = qc2;
+          // the lane's 32 bytes of the row in one store (the workspace rows are 32-byte aligned)
+          const uint4 lo = hsel ? qc2 : qc, hi = hsel ? qc : qc2;
+          st_global_32b(p.q8 + slot * QROW + cb * 32, lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w);
         } else {
           *reinterpret_cast<uint4*>(p.q8 + slot * QROW + cb * 16) =
               hsel ? make_uint4(qc.z, qc.w, qc.x, qc.y) : qc;
@@ -538,9 +538,8 @@ __device__ __forceinline__ void fwd8_prep(const Fwd8Params& p) {
         }
       }
       if constexpr (SI8) {
-        uint4* dst = reinterpret_cast<uint4*>(p.k8 + slot * QROW + cb * 32);
-        dst[hsel] = kc;
-        dst[1 - hsel] = kc2;
+        const uint4 lo = hsel ? kc2 : kc, hi = hsel ? kc : kc2;
+        st_global_32b(p.k8 + slot * QROW + cb * 32, lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w);
       } else {
         *reinterpret_cast<uint4*>(p.k8 + slot * QROW + cb * 16) = hsel ? make_uint4(kc.z, kc.w, kc.x, kc.y) : kc;
       }
